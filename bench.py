@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""KDA forward-path benchmark on GB300.  Prints ONE JSON line (rank 0).
+
+A step is one chunked prefill (``kda_chunk_fwd``) of the dense serving
+workload B=2, T=4096, Hqk=Hv=16, D=128 (bf16 activations, fp32 initial state
+read, fp32 final state written), inputs resident in HBM; L2 is flushed (a
+256 MB write) before every timed step and the flush is outside the events.
+The same line carries the decode / verify / varlen / long-context results
+under ``extras``, the dominant kernel's roofline, the end-to-end number
+through the public API with pinned host buffers, and the CPU oracle timed on
+this host as a reported baseline.
+
+Multi-GPU (torchrun): one replica per rank, no collective in the data path
+("weak" scaling); a barrier brackets the timed region and the slowest rank's
+time is used.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample per step
+on this host's cores (rank 0 only) and prints the same keys.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D = 128
+CHUNK = 64
+WORKLOAD = dict(name="dense", B=2, T=4096, hqk=16, hv=16)
+METRIC = "chunk_kda prefill tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc():
+    w = WORKLOAD
+    return (f"dense prefill B={w['B']} T={w['T']} Hqk={w['hqk']} Hv={w['hv']} D=128, bf16 "
+            f"q/k/v/g/beta, fp32 initial state N(0,0.02), final state returned, "
+            f"lower_bound=-5, A_log=log U[1,16], dt_bias N(0,0.1)")
+
+
+def flop_per_token_head():
+    return 6 * D * D + 10 * CHUNK * D
+
+
+def prefill_bytes_per_token_head(hqk, hv):
+    return 2 * 256 / (hv // hqk) + 512 + 2 + 256
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.file.name)
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id.lower()[-12:])]
+            rows = mine or rows
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        busy = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+def make_flush(torch):
+    buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        buf.zero_()
+    return flush
+
+
+def time_device(torch, fn, steps, flush, barrier):
+    """Sum of per-step CUDA-event durations of ``fn`` on the current stream
+    (flush outside the events), bracketed by barrier + synchronize."""
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3  # seconds
+
+
+def preroll(torch, fn, seconds=1.0):
+    """Keep the GPU busy so the clock sampler sees the load."""
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, barrier, reduce_max):
+    import torch
+
+    import linear_attention_serving_fwd_gb300 as kda
+    from linear_attention_serving_fwd_gb300 import _native, workloads as W
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dev = torch.device("cuda")
+    pk = peaks()
+    w = WORKLOAD
+    x = W.dense_prefill(w["B"], w["T"], w["hqk"], w["hv"], seed=rank, device=dev)
+    n = w["B"]
+    T = x.t_total
+    out = torch.empty((T, w["hv"], D), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((n, w["hv"], D, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.chunk_workspace_bytes(n, T, w["hv"], 0), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, A_log=x.A_log, dt_bias=x.dt_bias,
+                          scale=x.scale, lower_bound=x.lower_bound, n_seqs=n,
+                          initial_state=x.initial_state, final_state=fin, out=out,
+                          workspace=ws)
+
+    flush = make_flush(torch)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        bus = None
+    clocks = ClockSampler(str(bus) if bus else None)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clocks.start()
+    preroll(torch, step, 1.0)
+    secs = time_device(torch, step, args.steps, flush, barrier)
+    clk = clocks.stop()
+    secs = reduce_max(secs)
+    ms_per_step = secs / args.steps * 1e3
+    tokens = n * w["T"] * world
+    value = tokens * args.steps / secs
+    th = n * w["T"] * w["hv"]
+    tflops = th * flop_per_token_head() * args.steps * world / secs / 1e12
+
+    # dominant kernel, timed live with the library's event tracing
+    _native.trace_enable(True)
+    time_device(torch, step, args.steps, flush, barrier)
+    tr = _native.trace_read()
+    _native.trace_enable(False)
+    launches = sum(c for _, c in tr.values())
+    dom = max(tr, key=lambda k: tr[k][0])
+    dom_ms = tr[dom][0] / tr[dom][1]
+    per_kernel_flop = {"kda_prologue": 8 * CHUNK * D, "kda_walk": 6 * D * D + 2 * CHUNK * D,
+                       "kda_walk_pass1": 2 * (6 * D * D), "kda_group_compose": 0}
+    f_unit = per_kernel_flop.get(dom, flop_per_token_head())
+    achieved = th * f_unit / (dom_ms / 1e3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 3),
+                "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4),
+                "traffic": None, "peak_source": f"{pk['src']} bf16 dense (burst)",
+                "per_launch_ms": round(dom_ms, 4),
+                "kernels_ms_per_step": {k: round(v[0] / v[1], 4) for k, v in tr.items()}}
+
+    # end to end through the public API with pinned host buffers
+    host = {name: getattr(x, name).cpu().pin_memory()
+            for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")}
+    dbuf = {name: torch.empty_like(getattr(x, name)) for name in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def e2e_step():
+        for name, t in host.items():
+            dbuf[name].copy_(t, non_blocking=True)
+        kda.kda_chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"],
+                          A_log=dbuf["A_log"], dt_bias=dbuf["dt_bias"], scale=x.scale,
+                          lower_bound=x.lower_bound, n_seqs=n,
+                          initial_state=dbuf["initial_state"], final_state=fin, out=out,
+                          workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_secs = reduce_max(time_device(torch, e2e_step, max(5, args.steps // 5), flush, barrier))
+    e2e_value = tokens * max(5, args.steps // 5) / e2e_secs
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, random gate parameters, no weights)",
+        "config": {"workload": workload_desc(), "global_batch": n * world, "seq_len": w["T"],
+                   "parallelism": f"replicas x{world}", "l2": "flushed before each step (256 MB write)",
+                   "groups": "auto"},
+        "tflops": round(tflops, 3), "pct_bf16_peak": round(100 * tflops / pk["bf16"], 2),
+        "hbm_gbs_algorithmic": round(th * prefill_bytes_per_token_head(w["hqk"], w["hv"])
+                                     * args.steps * world / secs / 1e9, 1),
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x)
+    if not args.no_extras:
+        line["extras"] = extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world)
+    return line
+
+
+def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
+    from linear_attention_serving_fwd_gb300 import _native
+    res = {}
+    steps = max(5, min(args.steps, 20))
+    sb = 4 * D * D
+    # decode / verify on the 256-request batch, H=32, 512-slot pool
+    for window in (1, 4):
+        y = W.workload("decode", window=window, seed=rank, device="cuda")
+        pool = y.state_pool
+        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
+        counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+        corr = torch.empty((y.n_seqs, y.hv, window, D), dtype=torch.float32, device="cuda")
+        kg = torch.empty((y.n_seqs, y.hv, window, 2 * D), dtype=torch.bfloat16, device="cuda")
+        for verify in (False, True):
+            if verify and window == 1:
+                continue
+
+            def fn():
+                if verify:
+                    kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens,
+                                   y.state_indices, window, A_log=y.A_log, dt_bias=y.dt_bias,
+                                   out=out, corr=corr, kg=kg, work_counter=counter)
+                else:
+                    kda.kda_decode(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens,
+                                   y.state_indices, window, A_log=y.A_log, dt_bias=y.dt_bias,
+                                   out=out)
+            for _ in range(3):
+                fn()
+            secs = reduce_max(time_device(torch, fn, steps, flush, barrier))
+            items = y.n_seqs * y.hv
+            t = secs / steps
+            state_bytes = items * sb * (1 if verify else 2)
+            act_bytes = y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)  # q,k per v-head (GVA 1), v,g,o
+            rec_bytes = (y.t_total * y.hv * (4 * D + 4 * D)) if verify else 0
+            gbs = (state_bytes + act_bytes + rec_bytes) / t / 1e9
+            key = f"{'verify' if verify else 'decode'}_q{window}"
+            res[key] = {"tokens_per_s": round(y.t_total * world / t, 1),
+                        "ms_per_step": round(t * 1e3, 4),
+                        "state_gbs": round(state_bytes / t / 1e9, 1),
+                        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                                     "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                                     "traffic": None,
+                                     "peak_source": f"{pk['src']} HBM copy bandwidth"},
+                        "workload": f"256 requests x window {window}, Hqk=Hv=32, 512-slot fp32 pool"}
+        del y, pool
+    # varlen paged and long-context prefill
+    for name in ("varlen", "long"):
+        z = W.workload(name, seed=rank, device="cuda")
+        out = torch.empty((z.t_total, z.hv, D), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(kda.chunk_workspace_bytes(z.n_seqs, z.t_total, z.hv, 0),
+                         dtype=torch.uint8, device="cuda")
+        fin = None
+        if z.state_pool is None:
+            fin = torch.empty((z.n_seqs, z.hv, D, D), dtype=torch.float32, device="cuda")
+
+        def fn():
+            if z.state_pool is not None:
+                kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
+                                  cu_seqlens=z.cu_seqlens, state_cache=z.state_pool,
+                                  state_indices=z.state_indices,
+                                  has_initial_state=z.has_initial_state, out=out, workspace=ws)
+            else:
+                kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
+                                  n_seqs=z.n_seqs, final_state=fin, out=out, workspace=ws)
+        fn()
+        torch.cuda.synchronize()
+        s2 = 3 if name == "long" else steps
+        secs = reduce_max(time_device(torch, fn, s2, flush, barrier))
+        t = secs / s2
+        th = z.t_total * z.hv
+        tfl = th * flop_per_token_head() / t / 1e12
+        res[name] = {"tokens_per_s": round(z.t_total * world / t, 1), "ms_per_step": round(t * 1e3, 3),
+                     "tflops": round(tfl, 3), "pct_bf16_peak": round(100 * tfl / pk["bf16"], 2),
+                     "workload": ("8 seqs (U[64,8192] rescaled to 32768), Hqk=8 Hv=32, paged fp32 cache"
+                                  if name == "varlen" else "B=1 T=131072 Hqk=Hv=32, zero initial state")}
+        del z, out, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(x, n_heads=16, n_tokens=4096):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    sequence 0, ``n_heads`` heads, its first ``n_tokens`` tokens."""
+    import oracle
+    sl = slice(0, n_tokens)
+    h = slice(0, n_heads)
+    q, k = x.q[sl, h].cpu(), x.k[sl, h].cpu()
+    v, g, b = x.v[sl, h].cpu(), x.g[sl, h].cpu(), x.beta[sl, h].cpu()
+    A_log, dt = x.A_log[h].cpu(), x.dt_bias[h].cpu()
+    h0 = x.initial_state[0:1, h].cpu() if x.initial_state is not None else None
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.recurrence(q, k, v, g, b, [0, n_tokens], A_log=A_log, dt_bias=dt,
+                      lower_bound=x.lower_bound, h0=h0, n_threads=threads)
+    dt_s = time.perf_counter() - t0
+    th_per_s = n_heads * n_tokens / dt_s
+    return {"value": round(th_per_s / x.hv, 2), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt_s, 3),
+            "sample": f"sequence 0, heads 0..{n_heads - 1}, tokens 0..{n_tokens - 1} of the dense "
+                      f"workload (fp64 token recurrence, OpenMP); token-heads/s divided by Hv={x.hv}"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import torch  # noqa: F401
+
+    import oracle
+    from linear_attention_serving_fwd_gb300 import workloads as W
+    w = WORKLOAD
+    # bounded sample per step: 2 heads x 1024 tokens of sequence 0
+    nh, nt = 2, 1024
+    x = W.dense_prefill(1, nt, nh, nh, seed=0)
+    threads = os.cpu_count() or 1
+    args_ = (x.q, x.k, x.v, x.g, x.beta, [0, nt])
+    kw = dict(A_log=x.A_log, dt_bias=x.dt_bias, lower_bound=x.lower_bound,
+              h0=x.initial_state, n_threads=threads)
+    for _ in range(max(1, args.warmup)):
+        oracle.recurrence(*args_, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrence(*args_, **kw)
+    secs = time.perf_counter() - t0
+    value = nh * nt * args.steps / secs / w["hv"]
+    sample = (f"per step: {nh} heads x {nt} tokens of one dense sequence (fp64 token "
+              f"recurrence, OpenMP, {threads} threads); token-heads/s divided by Hv={w['hv']}")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(), "global_batch": w["B"], "seq_len": w["T"],
+                   "parallelism": "cpu oracle, rank 0"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+    barrier = lambda: None
+    reduce_max = lambda s: s
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+
+        def barrier():
+            dist.barrier()
+
+        def reduce_max(s):
+            t = torch.tensor([s], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+    line = run_ours(args, rank, world, barrier, reduce_max)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * kda.h - C ABI of the GB300 (sm_103a) Kimi Delta Attention forward path.
+ *
+ * The operation (all three entry points): the gated delta rule with
+ * per-channel decay, head dimension K = V = 128, value heads Hv a multiple of
+ * query/key heads Hqk (value head h reads query/key head h / (Hv/Hqk)):
+ *
+ *   gate_t = lower_bound * sigmoid(exp(A_log[h]) * (g_t + dt_bias[h]))   [K]
+ *   beta_t = sigmoid(b_t)
+ *   k^_t = k_t / sqrt(|k_t|^2 + 1e-6),  q~_t = scale * q_t / sqrt(|q_t|^2 + 1e-6)
+ *   S_t  = (I - beta_t k^_t k^_t^T) diag(exp(gate_t)) S_{t-1} + beta_t k^_t v_t^T
+ *   o_t  = S_t^T q~_t
+ *
+ * as the MATE kda module defines it (chunk_kda docstring: gate parameters
+ * A_log [Hv] and dt_bias [Hv, 128], lower_bound default -5, in-kernel q/k L2
+ * norm, scale default 128^-0.5, beta given as logits) and as the vLLM
+ * kimi_k3 CuTeDSL verify page's windowed solve (KdaTcVerify.kernel, steps
+ * 2-4) unrolls it.  Without A_log/dt_bias the gate input g is the log decay
+ * and lower_bound is unused.
+ *
+ * Layouts.  Activations are token-major: q, k [T_tot, Hqk, 128];
+ * v, g [T_tot, Hv, 128]; beta [T_tot, Hv], with explicit token and head
+ * strides in elements and the last dimension contiguous (g and beta may be
+ * column slices of a fused projection, as the vLLM kimi_k3 AMD kda_chunk page
+ * notes for fused_kda_prologue).  Outputs o are [T_tot, Hv, 128] contiguous.
+ * Recurrent states are fp32 and V-first: [.., Hv, V=128, K=128] with K
+ * contiguous (the decode page's default state_v_first layout, the verify
+ * page's [slots, H, V, K] state and fused_kda_chunk's final state).  A paged
+ * cache is [slots, Hv, 128, 128] with a caller-chosen slot stride (in floats,
+ * a multiple of 4, >= Hv*128*128).
+ *
+ * Ownership.  Every pointer is caller-owned device memory unless stated; the
+ * library allocates no device memory and never synchronises inside an entry
+ * point.  Work is enqueued on ``stream`` (a cudaStream_t; NULL = legacy
+ * default stream).  The library keeps one device-resident error word per
+ * device, set by kernels that meet a bad index or an expired wait; read it
+ * with kda_device_status().
+ *
+ * Errors.  Every entry point returns a kda_status.  Host-side validation
+ * failures return before any launch and leave all outputs untouched; the
+ * message is available from kda_last_error() (thread-local).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARGUMENT = 1, /* shape / pointer / size rule broken */
+  KDA_ERR_UNSUPPORTED_DTYPE = 2, /* only bf16 activations are built */
+  KDA_ERR_CUDA = 3,              /* a CUDA runtime call or launch failed */
+  KDA_ERR_DEVICE_TIMEOUT = 4,    /* a bounded device wait expired */
+  KDA_ERR_DEVICE_INDEX = 5       /* a kernel met a bad slot / length */
+} kda_status;
+
+enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP16 = 1 };
+
+/* The activations of one call (token-major; strides in elements). */
+typedef struct kda_activations {
+  const void* q;    int64_t q_stride_tok, q_stride_head;       /* [T, Hqk, 128] */
+  const void* k;    int64_t k_stride_tok, k_stride_head;       /* [T, Hqk, 128] */
+  const void* v;    int64_t v_stride_tok, v_stride_head;       /* [T, Hv, 128]  */
+  const void* g;    int64_t g_stride_tok, g_stride_head;       /* [T, Hv, 128]  */
+  const void* beta; int64_t beta_stride_tok, beta_stride_head; /* [T, Hv] logits */
+  const float* A_log;   /* [Hv] fp32, or NULL (then dt_bias must be NULL)      */
+  const float* dt_bias; /* [Hv, 128] fp32 contiguous, or NULL                   */
+  int32_t dtype;        /* KDA_DTYPE_BF16 (KDA_DTYPE_FP16 is rejected)          */
+  int32_t t_total;      /* total tokens T                                        */
+  int32_t hqk, hv;      /* heads; hv % hqk == 0                                  */
+  int32_t use_qk_l2norm;/* must be 1: the in-kernel L2 norm of q and k          */
+  float scale;          /* q scale applied after the norm (128^-0.5 usual)       */
+  float lower_bound;    /* gate lower bound in [-11, 0] (-5 usual); unused
+                           without A_log                                        */
+} kda_activations;
+
+/*
+ * kda_chunk_workspace_bytes - device scratch needed by kda_chunk_fwd.
+ *   n_seqs  number of sequences; t_total total tokens; hv value heads;
+ *   groups  chunk groups per sequence for the parallel scan (the same value
+ *           later passed to kda_chunk_fwd; <= 0 lets the library choose).
+ * The size covers the worst case chunk count t_total/64 + n_seqs and the
+ * chunk-group scan buffers.  Returns 0 on invalid sizes.
+ */
+size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, int32_t groups);
+
+/*
+ * kda_chunk_fwd - chunked prefill (chunk = 64): the MATE chunk_kda contract
+ * restricted to fp32 states, and the vLLM kimi_k3 AMD fused_kda_prologue +
+ * fused_kda_chunk pair (including the paged-cache form and the chunk-group
+ * parallel scan of _chunk_groups / _kda_group_workspace).
+ *
+ *   x              activations (see kda_activations)
+ *   out            [T, Hv, 128] bf16 contiguous, written
+ *   cu_seqlens     device int32 [n_seqs + 1] token offsets (0, .., T), or
+ *                  NULL for n_seqs dense sequences of T / n_seqs tokens
+ *   n_seqs         number of sequences (>= 1)
+ *   initial_state  [n_seqs, Hv, 128, 128] fp32 or NULL (zero start)
+ *   final_state    [n_seqs, Hv, 128, 128] fp32 or NULL (not returned)
+ *   state_cache    [slots, Hv, 128, 128] fp32 paged cache, or NULL.  When
+ *                  given, sequence n starts from row state_indices[n] (zero
+ *                  when has_initial_state[n] == 0) and its final state is
+ *                  written back to that row; initial_state and final_state
+ *                  must then be NULL.  A negative row skips the state I/O of
+ *                  that sequence (zero start, final state dropped).
+ *   slot_stride    floats between cache rows (multiple of 4, >= Hv*16384)
+ *   n_slots        rows in the cache; a row >= n_slots sets
+ *                  KDA_ERR_DEVICE_INDEX in the device error word and is skipped
+ *   state_indices  device int32 [n_seqs]
+ *   has_initial_state device uint8 [n_seqs] or NULL (= all true)
+ *   groups         chunk groups per sequence (vLLM _chunk_groups): 1 walks
+ *                  each chain serially; G > 1 runs the exact group scan
+ *                  (pass one per group, serial composition of the transfer
+ *                  operators, pass two); <= 0 lets the library choose
+ *   workspace      device scratch of >= kda_chunk_workspace_bytes(.., groups)
+ *                  bytes, 16-byte aligned; contents need not be initialised
+ *   stream         cudaStream_t
+ * cu_seqlens must start at 0, be non-decreasing and end at T; a violation
+ * found on the device sets KDA_ERR_DEVICE_INDEX.  The gate's 16-token
+ * sub-chunk factorisation needs any 8 consecutive per-token log decays to
+ * sum above -88 (always true for lower_bound >= -11, which is enforced).
+ */
+int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens,
+                  int32_t n_seqs, const float* initial_state, float* final_state,
+                  float* state_cache, int64_t slot_stride, int64_t n_slots,
+                  const int32_t* state_indices, const uint8_t* has_initial_state,
+                  int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kda_decode - in-place decode of a short window (1 <= window <= 8 tokens per
+ * request) on a paged fp32 state cache: the MATE gated_delta_rule_decode
+ * contract for fp32 V-first states with in-kernel gate, lower bound, beta
+ * sigmoid and q/k L2 norm, continuous batching by slot.
+ *
+ *   x            activations; x->t_total = query_start[n_req]
+ *   out          [T, Hv, 128] bf16, written (zero for padding requests)
+ *   state_pool   [n_slots, Hv, 128, 128] fp32, read and updated in place:
+ *                request b's row state_indices[b] ends holding the state
+ *                after all of its tokens
+ *   slot_stride  floats between rows (multiple of 4, >= Hv*16384)
+ *   query_start  device int32 [n_req + 1]; request b owns tokens
+ *                query_start[b] .. query_start[b+1]-1, at most ``window``
+ *   slots        device int32 [n_req]; a negative slot is a padding entry
+ *                (zero output, no state traffic); a slot >= n_slots or a
+ *                request longer than ``window`` sets KDA_ERR_DEVICE_INDEX
+ *                and is treated as padding
+ * Requests must use distinct slots (two requests on one row race).
+ */
+int kda_decode(const kda_activations* x, void* out, float* state_pool,
+               int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
+               const int32_t* slots, int32_t n_req, int32_t window, void* stream);
+
+/*
+ * kda_verify - windowed speculative verify (1 <= window <= 8): the vLLM
+ * kimi_k3 CuTeDSL KdaTcVerify contract with fp32 states.  Same inputs and
+ * outputs ``out`` as kda_decode, but the state pool is only read, and per
+ * request b, value head h and window position t < qlen it records
+ *   corr [n_req, Hv, window, 128] fp32 : the correction U_t (the delta-rule
+ *        term beta_t (v_t - S_{t-1}^T k^_t) of token t)
+ *   kg   [n_req, Hv, window, 256] bf16 : raw k_t (its query/key head) then
+ *        raw g_t, as loaded
+ * from which the accepted prefix's state can be rebuilt.  Entries t >= qlen
+ * and padding requests are not written.
+ *   work_counter  device int32[1], zero on entry; the launch's persistent
+ *                 scheduler takes tickets from it and leaves it zero.
+ */
+int kda_verify(const kda_activations* x, void* out, const float* state_pool,
+               int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
+               const int32_t* slots, int32_t n_req, int32_t window, float* corr,
+               void* kg, int32_t* work_counter, void* stream);
+
+/* Thread-local text of the last error returned on this thread ("" if none). */
+const char* kda_last_error(void);
+
+/*
+ * kda_device_status - synchronise ``stream``, read this device's error word
+ * and return KDA_OK, KDA_ERR_DEVICE_INDEX or KDA_ERR_DEVICE_TIMEOUT (the
+ * most severe seen since the last clear).  clear != 0 resets the word.
+ */
+int kda_device_status(void* stream, int32_t clear);
+
+/*
+ * Kernel tracing (off by default).  kda_trace_enable(1) clears the totals and
+ * starts recording a CUDA event pair around every kernel the library
+ * launches, on the launching stream; kda_trace_enable(0) stops.
+ * kda_trace_read(i, ..) synchronises on the recorded events, fills entry i
+ * (kernel name, total milliseconds, launch count; any out pointer may be
+ * NULL) and returns the number of entries.  Host-thread safe; not meant
+ * for use inside CUDA graph capture.
+ */
+int kda_trace_enable(int32_t on);
+int kda_trace_read(int32_t index, char* name, int32_t name_cap, double* total_ms,
+                   int32_t* launches);
+
+/* Library version, e.g. "kda-gb300 0.1 sm_103a". */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,217 @@
+"""GB300 (sm_103a) Kimi Delta Attention forward path.
+
+Python binding of the C ABI in ``include/kda.h``: these functions only
+marshal torch tensors into pointers, strides and the current CUDA stream;
+every step of the computation runs in the library's CUDA kernels.
+
+* :func:`kda_chunk_fwd` - chunked prefill (dense, varlen, paged state cache,
+  optional chunk-group scan).
+* :func:`kda_decode` - in-place window decode on a paged fp32 state cache.
+* :func:`kda_verify` - speculative verify (state read only, correction
+  records).
+* :func:`kda_device_status` - read (and clear) the device error word.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _native
+from ._native import KdaError
+
+D = 128
+__all__ = ["kda_chunk_fwd", "kda_decode", "kda_verify", "kda_device_status",
+           "chunk_workspace_bytes", "KdaError", "library_path"]
+
+
+def library_path() -> str:
+    return _native.lib_path()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _as_tokens(x: torch.Tensor, name: str, heads_dim: bool = True) -> torch.Tensor:
+    """[T, H, 128] (or [T, H] for beta) view; [B, T, ...] dense input is
+    flattened when its batch and time strides allow a single token stride."""
+    want = 3 if heads_dim else 2
+    if x.dim() == want + 1:
+        x = x.reshape(-1, *x.shape[2:])
+    if x.dim() != want:
+        raise ValueError(f"{name} must be [T, H, 128] / [B, T, H, 128] (got {tuple(x.shape)}).")
+    if heads_dim and (x.shape[-1] != D or x.stride(-1) != 1):
+        raise ValueError(f"{name} needs a contiguous last dimension of 128.")
+    return x
+
+
+def _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound):
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor.")
+    if q.dtype == torch.float16:
+        dtype = _native.KDA_DTYPE_FP16
+    elif q.dtype == torch.bfloat16:
+        dtype = _native.KDA_DTYPE_BF16
+    else:
+        raise TypeError("chunk_kda supports torch.float16 and torch.bfloat16 inputs.")
+    for name, t in (("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if t.dtype != q.dtype:
+            raise TypeError("k, v, g and beta must have the same dtype as q.")
+    if k.shape != q.shape:
+        raise ValueError("k must have the same shape as q.")
+    if g.shape != v.shape:
+        raise ValueError("g must have the same shape as v.")
+    if q.shape[0] != v.shape[0]:
+        raise ValueError("q, v and g must have matching token counts.")
+    if tuple(beta.shape) != tuple(v.shape[:2]):
+        raise ValueError("beta must have shape [T, Hv].")
+    if (A_log is None) != (dt_bias is None):
+        raise ValueError("A_log and dt_bias must be provided together.")
+    if A_log is not None:
+        if A_log.dtype != torch.float32 or dt_bias.dtype != torch.float32:
+            raise TypeError("A_log and dt_bias must be float32.")
+        A_log = A_log.contiguous()
+        dt_bias = dt_bias.contiguous()
+    a = _native.KdaActivations()
+    a.q, a.q_stride_tok, a.q_stride_head = q.data_ptr(), q.stride(0), q.stride(1)
+    a.k, a.k_stride_tok, a.k_stride_head = k.data_ptr(), k.stride(0), k.stride(1)
+    a.v, a.v_stride_tok, a.v_stride_head = v.data_ptr(), v.stride(0), v.stride(1)
+    a.g, a.g_stride_tok, a.g_stride_head = g.data_ptr(), g.stride(0), g.stride(1)
+    a.beta, a.beta_stride_tok, a.beta_stride_head = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    a.A_log = None if A_log is None else A_log.data_ptr()
+    a.dt_bias = None if dt_bias is None else dt_bias.data_ptr()
+    a.dtype = dtype
+    a.t_total, a.hqk, a.hv = q.shape[0], q.shape[1], v.shape[1]
+    a.use_qk_l2norm = 1
+    a.scale = D ** -0.5 if scale is None else float(scale)
+    a.lower_bound = float(lower_bound)
+    return a, (A_log, dt_bias)  # keep contiguous copies alive
+
+
+def chunk_workspace_bytes(n_seqs: int, t_total: int, hv: int, groups: int = 0) -> int:
+    return int(_native.lib().kda_chunk_workspace_bytes(n_seqs, t_total, hv, groups))
+
+
+def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, lower_bound=-5.0,
+                  cu_seqlens=None, n_seqs=None, initial_state=None, output_final_state=False,
+                  final_state=None, out=None, state_cache=None, state_indices=None,
+                  has_initial_state=None, groups: int = 0, workspace=None, stream=None):
+    """Chunked KDA prefill.  Returns (out, final_state or None).
+
+    q, k: [T, Hqk, 128] or [B, T, Hqk, 128]; v, g: [T, Hv, 128]; beta:
+    [T, Hv] logits; bf16.  Dense [B, T] input without ``cu_seqlens`` runs B
+    sequences of T tokens.  ``state_cache`` [slots, Hv, 128, 128] fp32 with
+    ``state_indices`` [N] int32 (and optional ``has_initial_state`` [N])
+    replaces initial_state / final_state and is updated in place.
+    """
+    dense_b = q.shape[0] if q.dim() == 4 else None
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
+    v, g = _as_tokens(v, "v"), _as_tokens(g, "g")
+    beta = _as_tokens(beta, "beta", heads_dim=False)
+    a, keep = _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound)
+    T, hv = q.shape[0], v.shape[1]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must have dtype torch.int32.")
+        cu_seqlens = cu_seqlens.contiguous()
+        n = cu_seqlens.numel() - 1
+    else:
+        n = n_seqs if n_seqs is not None else (dense_b if dense_b is not None else 1)
+    if out is None:
+        out = torch.empty((T, hv, D), dtype=q.dtype, device=q.device)
+    elif out.shape != (T, hv, D) or not out.is_contiguous():
+        out = out.view(T, hv, D)
+    slot_stride, n_slots = 0, 0
+    if state_cache is not None:
+        if state_indices is None:
+            raise ValueError("state_cache needs state_indices.")
+        state_indices = state_indices.to(torch.int32).contiguous()
+        if has_initial_state is not None:
+            has_initial_state = has_initial_state.to(torch.uint8).contiguous()
+        slot_stride, n_slots = state_cache.stride(0), state_cache.shape[0]
+        if tuple(state_cache.shape[1:]) != (hv, D, D) or state_cache[0].stride() != (D * D, D, 1):
+            raise ValueError("state_cache must be [slots, Hv, 128, 128] with contiguous rows.")
+    if output_final_state and final_state is None:
+        final_state = torch.empty((n, hv, D, D), dtype=torch.float32, device=q.device)
+    if initial_state is not None:
+        if initial_state.dtype != torch.float32:
+            raise TypeError("initial_state must be float32.")
+        initial_state = initial_state.contiguous()
+    ws_bytes = chunk_workspace_bytes(n, T, hv, groups)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    rc = _native.lib().kda_chunk_fwd(
+        ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
+        _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
+        int(groups), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    _native.check(rc)
+    del keep
+    return out, final_state
+
+
+def _window_call(verify, q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log,
+                 dt_bias, scale, lower_bound, out, corr, kg, work_counter, stream):
+    a, keep = _activations(_as_tokens(q, "q"), _as_tokens(k, "k"), _as_tokens(v, "v"),
+                           _as_tokens(g, "g"), _as_tokens(beta, "beta", heads_dim=False),
+                           A_log, dt_bias, scale, lower_bound)
+    T, hv = a.t_total, a.hv
+    n_req = slots.numel()
+    if query_start.dtype != torch.int32 or slots.dtype != torch.int32:
+        raise TypeError("query_start and slots must have dtype torch.int32.")
+    if state_pool.dtype != torch.float32:
+        raise TypeError("state_pool must be float32.")
+    if tuple(state_pool.shape[1:]) != (hv, D, D) or state_pool[0].stride() != (D * D, D, 1):
+        raise ValueError("state_pool must be [slots, Hv, 128, 128] with contiguous rows.")
+    if out is None:
+        out = torch.empty((T, hv, D), dtype=q.dtype, device=q.device)
+    lib = _native.lib()
+    if verify:
+        if corr is None:
+            corr = torch.empty((n_req, hv, window, D), dtype=torch.float32, device=q.device)
+        if kg is None:
+            kg = torch.empty((n_req, hv, window, 2 * D), dtype=q.dtype, device=q.device)
+        if work_counter is None:
+            work_counter = torch.zeros(1, dtype=torch.int32, device=q.device)
+        rc = lib.kda_verify(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
+                            state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
+                            _ptr(corr), _ptr(kg), _ptr(work_counter), _stream_handle(stream))
+    else:
+        rc = lib.kda_decode(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
+                            state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
+                            _stream_handle(stream))
+    _native.check(rc)
+    del keep
+    return out, corr, kg
+
+
+def kda_decode(q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log=None,
+               dt_bias=None, scale=None, lower_bound=-5.0, out=None, stream=None):
+    """In-place decode: request b runs tokens query_start[b]..query_start[b+1]-1
+    (at most ``window``) on pool row slots[b] (negative = padding).  Returns out."""
+    return _window_call(False, q, k, v, g, beta, state_pool, query_start, slots, window,
+                        A_log=A_log, dt_bias=dt_bias, scale=scale, lower_bound=lower_bound,
+                        out=out, corr=None, kg=None, work_counter=None, stream=stream)[0]
+
+
+def kda_verify(q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log=None,
+               dt_bias=None, scale=None, lower_bound=-5.0, out=None, corr=None, kg=None,
+               work_counter=None, stream=None):
+    """Speculative verify (state read only).  Returns (out, corr, kg)."""
+    return _window_call(True, q, k, v, g, beta, state_pool, query_start, slots, window,
+                        A_log=A_log, dt_bias=dt_bias, scale=scale, lower_bound=lower_bound,
+                        out=out, corr=corr, kg=kg, work_counter=work_counter, stream=stream)
+
+
+def kda_device_status(stream=None, clear: bool = True) -> int:
+    """Synchronise and read the device error word (0 = clean)."""
+    return int(_native.lib().kda_device_status(_stream_handle(stream), int(clear)))

@@ -1,0 +1,352 @@
+// Host side of the C ABI declared in include/kda.h: argument validation
+// (the shape, dtype and pairing rules of the MATE chunk_kda /
+// gated_delta_rule_decode validation and of the vLLM fused_kda_chunk cache
+// rules), the per-device error word, and the kernel launches.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kda_params.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// One error word per device that loads the library.  Host code passes its
+// device address (cudaGetSymbolAddress) to every kernel.
+__device__ unsigned int g_error_word = 0u;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+unsigned* error_word_ptr() {
+  static unsigned* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rules shared by all entry points.
+int check_activations(const kda_activations* x, bool need_rows_aligned) {
+  if (!x) return fail(KDA_ERR_INVALID_ARGUMENT, "activations must not be NULL.");
+  if (x->dtype == KDA_DTYPE_FP16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "only bfloat16 q/k/v/g/beta are built (got float16).");
+  if (x->dtype != KDA_DTYPE_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "q/k/v/g/beta dtype must be bfloat16.");
+  if (x->hqk <= 0 || x->hv <= 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "head counts must be positive (hqk=%d, hv=%d).", x->hqk, x->hv);
+  if (x->hv % x->hqk != 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "GVA requires v/g heads to be divisible by q/k heads (hv=%d, hqk=%d).", x->hv, x->hqk);
+  if (x->t_total < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "t_total must be >= 0.");
+  if ((x->A_log == nullptr) != (x->dt_bias == nullptr))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "A_log and dt_bias must be provided together.");
+  if (x->use_qk_l2norm != 1)
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "use_qk_l2norm must be 1: only the in-kernel q/k L2 norm is built.");
+  if (x->A_log && !(x->lower_bound <= 0.f && x->lower_bound >= -11.f))
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "lower_bound must lie in [-11, 0] (got %g).", (double)x->lower_bound);
+  if (x->t_total > 0) {
+    if (!x->q || !x->k || !x->v || !x->g || !x->beta)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "q, k, v, g and beta must not be NULL.");
+    const void* rows[4] = {x->q, x->k, x->v, x->g};
+    const int64_t st[8] = {x->q_stride_tok, x->q_stride_head, x->k_stride_tok, x->k_stride_head,
+                           x->v_stride_tok, x->v_stride_head, x->g_stride_tok, x->g_stride_head};
+    for (int i = 0; i < 8; ++i)
+      if (st[i] < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "strides must be non-negative.");
+    if (x->beta_stride_tok < 0 || x->beta_stride_head < 0)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "strides must be non-negative.");
+    if (need_rows_aligned) {
+      for (int i = 0; i < 4; ++i)
+        if (!aligned16(rows[i]))
+          return fail(KDA_ERR_INVALID_ARGUMENT, "q, k, v and g must be 16-byte aligned.");
+      for (int i = 0; i < 8; ++i)
+        if (st[i] % 8 != 0)
+          return fail(KDA_ERR_INVALID_ARGUMENT,
+                      "q/k/v/g token and head strides must be multiples of 8 elements.");
+    }
+    if (x->A_log && !aligned16(x->dt_bias))
+      return fail(KDA_ERR_INVALID_ARGUMENT, "dt_bias must be 16-byte aligned.");
+  }
+  return KDA_OK;
+}
+
+void fill_common(const kda_activations* x, const __nv_bfloat16*& q, const __nv_bfloat16*& k,
+                 const __nv_bfloat16*& v, const __nv_bfloat16*& g, const __nv_bfloat16*& b) {
+  q = static_cast<const __nv_bfloat16*>(x->q);
+  k = static_cast<const __nv_bfloat16*>(x->k);
+  v = static_cast<const __nv_bfloat16*>(x->v);
+  g = static_cast<const __nv_bfloat16*>(x->g);
+  b = static_cast<const __nv_bfloat16*>(x->beta);
+}
+
+int check_pool(const float* pool, int64_t slot_stride, int64_t n_slots, int hv, const char* name) {
+  if (!pool) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must not be NULL.", name);
+  if (!aligned16(pool)) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned.", name);
+  if (n_slots <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "state pool must contain at least one slot.");
+  if (slot_stride % 4 != 0 || slot_stride < (int64_t)hv * kda::D * kda::D)
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "slot_stride must be a multiple of 4 floats and >= Hv*128*128 (got %lld).",
+                (long long)slot_stride);
+  return KDA_OK;
+}
+
+int choose_groups(int32_t n_seqs, int32_t t_total, int32_t hv, int32_t requested) {
+  if (requested > 0) return requested < 64 ? requested : 64;
+  (void)n_seqs; (void)t_total; (void)hv;
+  return 1;
+}
+
+// --- kernel tracing --------------------------------------------------------
+struct TraceRec {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+struct TraceTotal {
+  std::string name;
+  double ms;
+  int launches;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace_pending;
+std::vector<TraceTotal> g_trace_totals;
+std::vector<cudaEvent_t> g_trace_free;
+
+cudaEvent_t trace_event() {
+  if (!g_trace_free.empty()) {
+    cudaEvent_t e = g_trace_free.back();
+    g_trace_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void trace_drain() {  // caller holds the lock
+  for (auto& r : g_trace_pending) {
+    float ms = 0.f;
+    cudaEventSynchronize(r.stop);
+    cudaEventElapsedTime(&ms, r.start, r.stop);
+    bool found = false;
+    for (auto& t : g_trace_totals)
+      if (t.name == r.name) { t.ms += ms; t.launches += 1; found = true; break; }
+    if (!found) g_trace_totals.push_back({r.name, (double)ms, 1});
+    g_trace_free.push_back(r.start);
+    g_trace_free.push_back(r.stop);
+  }
+  g_trace_pending.clear();
+}
+
+}  // namespace
+
+namespace kda {
+void trace_begin(const char* name, cudaStream_t stream) {
+  if (!g_trace_on) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  TraceRec r{name, trace_event(), trace_event()};
+  cudaEventRecord(r.start, stream);
+  g_trace_pending.push_back(r);
+}
+void trace_end(cudaStream_t stream) {
+  if (!g_trace_on) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_pending.empty()) cudaEventRecord(g_trace_pending.back().stop, stream);
+}
+}  // namespace kda
+
+extern "C" {
+
+int kda_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  trace_drain();
+  g_trace_totals.clear();
+  g_trace_on = on != 0;
+  return KDA_OK;
+}
+
+int kda_trace_read(int32_t index, char* name, int32_t name_cap, double* total_ms,
+                   int32_t* launches) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  trace_drain();
+  const int n = (int)g_trace_totals.size();
+  if (index >= 0 && index < n) {
+    const TraceTotal& t = g_trace_totals[index];
+    if (name && name_cap > 0) {
+      strncpy(name, t.name.c_str(), (size_t)name_cap - 1);
+      name[name_cap - 1] = 0;
+    }
+    if (total_ms) *total_ms = t.ms;
+    if (launches) *launches = t.launches;
+  }
+  return n;
+}
+
+const char* kda_version(void) { return "kda-gb300 0.1 sm_103a"; }
+
+const char* kda_last_error(void) { return g_last_error.c_str(); }
+
+size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, int32_t groups) {
+  if (n_seqs <= 0 || t_total < 0 || hv <= 0) return 0;
+  const int G = choose_groups(n_seqs, t_total, hv, groups);
+  return 4 * kda::chunk_workspace_floats(n_seqs, t_total, hv, G, nullptr);
+}
+
+int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
+                  const float* initial_state, float* final_state, float* state_cache,
+                  int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
+                  const uint8_t* has_initial_state, int32_t groups, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  int rc = check_activations(x, true);
+  if (rc) return rc;
+  if (n_seqs <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs must be >= 1.");
+  if (!cu_seqlens && x->t_total % n_seqs != 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "dense mode (no cu_seqlens) needs t_total divisible by n_seqs.");
+  if (x->t_total > 0 && !out) return fail(KDA_ERR_INVALID_ARGUMENT, "out must not be NULL.");
+  if (state_cache) {
+    if (initial_state || final_state)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "state_cache replaces initial_state/final_state.");
+    if (!state_indices) return fail(KDA_ERR_INVALID_ARGUMENT, "state_cache needs state_indices.");
+    rc = check_pool(state_cache, slot_stride, n_slots, x->hv, "state_cache");
+    if (rc) return rc;
+  }
+  if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "states must be 16-byte aligned.");
+  const int G = choose_groups(n_seqs, x->t_total, x->hv, groups);
+  const size_t need = 4 * kda::chunk_workspace_floats(n_seqs, x->t_total, x->hv, G, nullptr);
+  if (!workspace || workspace_bytes < need)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "workspace needs %zu bytes (got %zu).", need,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(KDA_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned.");
+  unsigned* err = error_word_ptr();
+  if (!err) return fail(KDA_ERR_CUDA, "cannot resolve the device error word.");
+
+  kda::ChunkParams p;
+  memset(&p, 0, sizeof(p));
+  fill_common(x, p.q, p.k, p.v, p.g, p.beta);
+  p.q_st = x->q_stride_tok; p.q_sh = x->q_stride_head;
+  p.k_st = x->k_stride_tok; p.k_sh = x->k_stride_head;
+  p.v_st = x->v_stride_tok; p.v_sh = x->v_stride_head;
+  p.g_st = x->g_stride_tok; p.g_sh = x->g_stride_head;
+  p.b_st = x->beta_stride_tok; p.b_sh = x->beta_stride_head;
+  p.A_log = x->A_log; p.dt_bias = x->dt_bias; p.has_gate = x->A_log != nullptr;
+  p.scale = x->scale; p.lower_bound = x->lower_bound;
+  p.t_total = x->t_total; p.hqk = x->hqk; p.hv = x->hv; p.n_seqs = n_seqs;
+  p.dense_len = cu_seqlens ? 0 : x->t_total / n_seqs;
+  p.cu_seqlens = cu_seqlens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.h0 = initial_state; p.hT = final_state; p.cache = state_cache;
+  p.slot_stride = slot_stride; p.n_slots = n_slots;
+  p.state_indices = state_indices; p.has_init = has_initial_state;
+  p.groups = G;
+  p.err = err;
+  if (kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream)) != 0)
+    return cuda_fail(cudaGetLastError(), "kda_chunk_fwd launch");
+  return ok();
+}
+
+static int window_common(const kda_activations* x, void* out, const float* pool, int64_t slot_stride,
+                         int64_t n_slots, const int32_t* query_start, const int32_t* slots,
+                         int32_t n_req, int32_t window, bool verify, float* corr, void* kg,
+                         int32_t* counter, void* stream) {
+  int rc = check_activations(x, true);
+  if (rc) return rc;
+  if (window < 1 || window > kda::MAX_WINDOW)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "window must satisfy 1 <= window <= 8 (got %d).", window);
+  if (n_req < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_req must be >= 0.");
+  if (n_req == 0) return ok();
+  if (!query_start || !slots)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "query_start and slots must not be NULL.");
+  if (x->t_total > 0 && !out) return fail(KDA_ERR_INVALID_ARGUMENT, "out must not be NULL.");
+  rc = check_pool(pool, slot_stride, n_slots, x->hv, "state_pool");
+  if (rc) return rc;
+  if (verify && (!corr || !kg || !counter))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "verify needs corr, kg and work_counter.");
+  if ((int64_t)n_req * x->hv > 0x7fffffff)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "n_req * Hv exceeds 2^31.");
+  unsigned* err = error_word_ptr();
+  if (!err) return fail(KDA_ERR_CUDA, "cannot resolve the device error word.");
+  kda::WindowParams p;
+  memset(&p, 0, sizeof(p));
+  fill_common(x, p.q, p.k, p.v, p.g, p.beta);
+  p.q_st = x->q_stride_tok; p.q_sh = x->q_stride_head;
+  p.k_st = x->k_stride_tok; p.k_sh = x->k_stride_head;
+  p.v_st = x->v_stride_tok; p.v_sh = x->v_stride_head;
+  p.g_st = x->g_stride_tok; p.g_sh = x->g_stride_head;
+  p.b_st = x->beta_stride_tok; p.b_sh = x->beta_stride_head;
+  p.A_log = x->A_log; p.dt_bias = x->dt_bias; p.has_gate = x->A_log != nullptr;
+  p.scale = x->scale; p.lower_bound = x->lower_bound;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.pool = const_cast<float*>(pool);
+  p.slot_stride = slot_stride; p.n_slots = n_slots;
+  p.query_start = query_start; p.slots = slots;
+  p.n_req = n_req; p.window = window; p.hqk = x->hqk; p.hv = x->hv;
+  p.corr = corr; p.kg = static_cast<__nv_bfloat16*>(kg); p.counter = counter;
+  p.err = err;
+  if (kda::launch_window(p, verify, static_cast<cudaStream_t>(stream)) != 0)
+    return cuda_fail(cudaGetLastError(), verify ? "kda_verify launch" : "kda_decode launch");
+  return ok();
+}
+
+int kda_decode(const kda_activations* x, void* out, float* state_pool, int64_t slot_stride,
+               int64_t n_slots, const int32_t* query_start, const int32_t* slots, int32_t n_req,
+               int32_t window, void* stream) {
+  return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req,
+                       window, false, nullptr, nullptr, nullptr, stream);
+}
+
+int kda_verify(const kda_activations* x, void* out, const float* state_pool, int64_t slot_stride,
+               int64_t n_slots, const int32_t* query_start, const int32_t* slots, int32_t n_req,
+               int32_t window, float* corr, void* kg, int32_t* work_counter, void* stream) {
+  return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req,
+                       window, true, corr, kg, work_counter, stream);
+}
+
+int kda_device_status(void* stream, int32_t clear) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_device_status sync");
+  unsigned word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "kda_device_status read");
+  if (clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_device_status clear");
+  }
+  if (word & kda::ERR_TIMEOUT) return fail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device wait expired.");
+  if (word & kda::ERR_INDEX)
+    return fail(KDA_ERR_DEVICE_INDEX, "a kernel met an out-of-range slot or sequence length.");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Kernel parameter blocks shared by the API layer and the kernels.
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+struct WindowParams {
+  const __nv_bfloat16 *q, *k, *v, *g, *beta;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh, g_st, g_sh, b_st, b_sh;
+  const float* A_log;
+  const float* dt_bias;
+  float scale, lower_bound;
+  int has_gate;
+  __nv_bfloat16* out;  // [T, Hv, 128]
+  float* pool;         // [n_slots, Hv, 128, 128] (read only for verify)
+  int64_t slot_stride;
+  int64_t n_slots;
+  const int32_t* query_start;
+  const int32_t* slots;
+  int n_req, window, hqk, hv;
+  float* corr;          // verify: [n_req, Hv, window, 128]
+  __nv_bfloat16* kg;    // verify: [n_req, Hv, window, 256]
+  int32_t* counter;     // verify: ticket counter
+  unsigned* err;        // device error word
+};
+
+struct ChunkParams {
+  const __nv_bfloat16 *q, *k, *v, *g, *beta;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh, g_st, g_sh, b_st, b_sh;
+  const float* A_log;
+  const float* dt_bias;
+  float scale, lower_bound;
+  int has_gate;
+  int t_total, hqk, hv, n_seqs;
+  int dense_len;               // > 0: dense sequences of this length (no cu_seqlens)
+  const int32_t* cu_seqlens;   // [N+1] or null
+  __nv_bfloat16* out;
+  const float* h0;             // [N, Hv, 128, 128] or null
+  float* hT;                   // [N, Hv, 128, 128] or null
+  float* cache;                // paged cache or null
+  int64_t slot_stride, n_slots;
+  const int32_t* state_indices;
+  const uint8_t* has_init;
+  int max_chunks;
+  int groups;
+  // workspace carve
+  int32_t* chunk_off;   // [N+1]
+  int32_t* chunk_seq;   // [max_chunks]
+  int32_t* chunk_j;     // [max_chunks]
+  int32_t* n_chunks;    // [1]
+  float* ch;            // [max_chunks, Hv, CH_FLOATS]
+  float* gM;            // [N, Hv, G, 128, 128]  M_g^T
+  float* gB;            // [N, Hv, G, 128, 128]  B_g^T
+  float* gS;            // [N, Hv, G, 128, 128]  incoming state of each group (V-first)
+  unsigned* err;        // device error word
+};
+
+// Kernel tracing (kda_trace_* in the API layer): when enabled, CUDA events
+// are recorded on the launching stream around each kernel; off by default,
+// then these are one predictable branch each.
+void trace_begin(const char* name, cudaStream_t stream);
+void trace_end(cudaStream_t stream);
+
+// Launchers (kernels' translation units); return 0 or -1 (see cudaGetLastError).
+int launch_window(const WindowParams& p, bool verify, cudaStream_t stream);
+size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out);
+int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream);
+
+}  // namespace kda

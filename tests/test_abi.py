@@ -1,0 +1,152 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/kda.h declares, and its host-side validation rejects each broken
+argument rule (the MATE chunk_kda / gated_delta_rule_decode checks and the
+fused_kda_chunk state-cache rules) with the documented status code, before
+touching the device.  Pointers here are fake, aligned addresses that are
+never dereferenced: validation fails first."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_serving_fwd_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INVALID, DTYPE, CUDA = 1, 2, 3
+FAKE = 0x10000  # aligned, never dereferenced
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    lib = _native.lib()
+    declared = _header_functions()
+    assert set(declared) == set(_native.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.kda_version().decode().startswith("kda-gb300")
+
+
+def _acts(**over):
+    a = _native.KdaActivations()
+    for name in ("q", "k", "v", "g", "beta"):
+        setattr(a, name, FAKE)
+    a.q_stride_tok = a.k_stride_tok = 2 * 128
+    a.q_stride_head = a.k_stride_head = 128
+    a.v_stride_tok = a.g_stride_tok = 4 * 128
+    a.v_stride_head = a.g_stride_head = 128
+    a.beta_stride_tok, a.beta_stride_head = 4, 1
+    a.A_log, a.dt_bias = FAKE, FAKE
+    a.dtype, a.t_total, a.hqk, a.hv = 0, 64, 2, 4
+    a.use_qk_l2norm, a.scale, a.lower_bound = 1, 128 ** -0.5, -5.0
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def _chunk(a, **kw):
+    lib = _native.lib()
+    args = dict(out=FAKE, cu=None, n=1, h0=None, hT=None, cache=None, stride=0, slots=0,
+                idx=None, hi=None, groups=1, ws=FAKE, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return lib.kda_chunk_fwd(ctypes.byref(a), args["out"], args["cu"], args["n"], args["h0"],
+                             args["hT"], args["cache"], args["stride"], args["slots"],
+                             args["idx"], args["hi"], args["groups"], args["ws"],
+                             args["ws_bytes"], args["stream"])
+
+
+def _msg():
+    return _native.lib().kda_last_error().decode()
+
+
+@pytest.mark.parametrize("over,code,text", [
+    (dict(dtype=1), DTYPE, "bfloat16"),
+    (dict(dtype=7), DTYPE, "bfloat16"),
+    (dict(hv=3), INVALID, "GVA requires"),
+    (dict(hqk=0), INVALID, "positive"),
+    (dict(A_log=None), INVALID, "provided together"),
+    (dict(use_qk_l2norm=0), INVALID, "L2 norm"),
+    (dict(lower_bound=-12.0), INVALID, "lower_bound"),
+    (dict(q=FAKE + 2), INVALID, "16-byte aligned"),
+    (dict(v_stride_tok=4 * 128 + 1), INVALID, "multiples of 8"),
+    (dict(k=None), INVALID, "must not be NULL"),
+    (dict(t_total=-1), INVALID, "t_total"),
+])
+def test_chunk_validation(over, code, text):
+    assert _chunk(_acts(**over)) == code
+    assert text in _msg()
+
+
+def test_chunk_rules_on_states_and_workspace():
+    a = _acts()
+    assert _chunk(a, cache=FAKE, h0=FAKE, idx=FAKE, stride=4 * 16384, slots=3) == INVALID
+    assert "replaces initial_state" in _msg()
+    assert _chunk(a, cache=FAKE, stride=4 * 16384, slots=3) == INVALID
+    assert "needs state_indices" in _msg()
+    assert _chunk(a, cache=FAKE, idx=FAKE, stride=4 * 16384 + 2, slots=3) == INVALID
+    assert "slot_stride" in _msg()
+    assert _chunk(a, cache=FAKE, idx=FAKE, stride=4 * 16384, slots=0) == INVALID
+    assert "at least one slot" in _msg()
+    assert _chunk(a, ws_bytes=16) == INVALID
+    assert "workspace needs" in _msg()
+    assert _chunk(a, n=0) == INVALID
+    assert _chunk(_acts(t_total=65), n=2) == INVALID
+    assert "divisible" in _msg()
+
+
+def test_workspace_query():
+    lib = _native.lib()
+    assert lib.kda_chunk_workspace_bytes(0, 64, 4, 1) == 0
+    one = lib.kda_chunk_workspace_bytes(2, 8192, 16, 1)
+    four = lib.kda_chunk_workspace_bytes(2, 8192, 16, 4)
+    assert one > 0 and four > one
+    # three 64 KB planes per (sequence, head, group) for the group scan
+    assert four - one == 3 * 2 * 16 * 4 * 128 * 128 * 4
+
+
+def _window(a, verify=False, **kw):
+    lib = _native.lib()
+    args = dict(out=FAKE, pool=FAKE, stride=4 * 16384, slots=8, qs=FAKE, sl=FAKE, n=2, win=1,
+                corr=FAKE, kg=FAKE, ctr=FAKE, stream=None)
+    args.update(kw)
+    if verify:
+        return lib.kda_verify(ctypes.byref(a), args["out"], args["pool"], args["stride"],
+                              args["slots"], args["qs"], args["sl"], args["n"], args["win"],
+                              args["corr"], args["kg"], args["ctr"], args["stream"])
+    return lib.kda_decode(ctypes.byref(a), args["out"], args["pool"], args["stride"],
+                          args["slots"], args["qs"], args["sl"], args["n"], args["win"],
+                          args["stream"])
+
+
+@pytest.mark.parametrize("verify", [False, True])
+def test_window_validation(verify):
+    a = _acts()
+    assert _window(a, verify, win=0) == INVALID and "window" in _msg()
+    assert _window(a, verify, win=9) == INVALID and "window" in _msg()
+    assert _window(a, verify, pool=None) == INVALID and "state_pool" in _msg()
+    assert _window(a, verify, slots=0) == INVALID and "at least one slot" in _msg()
+    assert _window(a, verify, qs=None) == INVALID
+    assert _window(a, verify, n=-1) == INVALID
+    assert _window(a, verify, n=0) == 0  # nothing to do
+    assert _window(_acts(hv=3), verify) == INVALID
+    if verify:
+        assert _window(a, True, ctr=None) == INVALID and "work_counter" in _msg()
+
+
+def test_valid_call_without_gpu_reports_cuda_error():
+    """Arguments that pass validation reach the CUDA runtime, which on a host
+    without a GPU fails cleanly with KDA_ERR_CUDA."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    assert _window(_acts(), False) == CUDA

@@ -1,0 +1,137 @@
+"""GPU parity of kda_chunk_fwd (chunked prefill) against the fp64 oracle,
+through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_serving_fwd_gb300 import workloads as W
+from tests.helpers import check_out, check_state, np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(x, groups=1, dense=False):
+    import linear_attention_serving_fwd_gb300 as kda
+    xd = x.to("cuda")
+    kw = dict(A_log=xd.A_log, dt_bias=xd.dt_bias, scale=x.scale, lower_bound=x.lower_bound,
+              groups=groups)
+    pool = None
+    if xd.state_pool is not None:
+        pool = xd.state_pool.clone()
+        out, fin = kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, cu_seqlens=xd.cu_seqlens,
+                                     state_cache=pool, state_indices=xd.state_indices,
+                                     has_initial_state=xd.has_initial_state, **kw)
+    elif dense:
+        out, fin = kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, n_seqs=x.n_seqs,
+                                     initial_state=xd.initial_state, output_final_state=True, **kw)
+    else:
+        out, fin = kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, cu_seqlens=xd.cu_seqlens,
+                                     initial_state=xd.initial_state, output_final_state=True, **kw)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status(clear=True) == 0
+    return out, fin, pool
+
+
+def _check(x, out, fin, pool, ref, tag):
+    r_o = check_out(out, ref["out"], f"{tag} out")
+    if pool is not None:
+        idx = x.state_indices.tolist()
+        live = [s for s in idx if s >= 0]
+        check_state(pool[live], ref["pool"][live], f"{tag} cache rows")
+        untouched = [s for s in range(pool.shape[0]) if s not in live]
+        assert torch.equal(pool[untouched].cpu(), x.state_pool[untouched]), "untouched rows changed"
+    else:
+        check_state(fin, ref["state"], f"{tag} final state")
+    return r_o
+
+
+def test_tiny_prefill():
+    """B=1, T=256, H=1, no initial state, final state returned."""
+    x = W.workload("tiny")
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x, dense=True)
+    _check(x, out, fin, pool, ref, "tiny")
+
+
+@pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 130, 200])
+def test_ragged_lengths(T):
+    x = W.dense_prefill(1, T, 1, 2, seed=T)
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x)
+    _check(x, out, fin, pool, ref, f"T={T}")
+
+
+@pytest.mark.parametrize("lb,g_shift,scale", [(-0.05, 0.0, 128 ** -0.5), (-5.0, -6.0, 1.0),
+                                              (-1.0, 0.0, 1.0)])
+def test_weak_decay_exercises_the_walk(lb, g_shift, scale):
+    """Weak decay keeps the state alive across chunks, so the inter-chunk walk
+    and the initial state matter for every output."""
+    x = W.dense_prefill(2, 320, 2, 4, seed=3, lower_bound=lb, g_shift=g_shift, scale=scale,
+                        state_std=0.3)
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x)
+    _check(x, out, fin, pool, ref, f"lb={lb}")
+
+
+def test_varlen_paged_gva_small():
+    x = W.varlen_paged([70, 1, 129, 64, 5, 300], 2, 4, slots=9, seed=4, lower_bound=-0.4,
+                       has_initial=[1, 0, 1, 1, 1, 0])
+    x.state_indices[4] = -1  # a sequence that skips its state I/O
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x)
+    _check(x, out, fin, pool, ref, "varlen")
+
+
+@pytest.mark.parametrize("groups", [2, 3, 8])
+def test_group_scan_equals_serial(groups):
+    """The chunk-group scan (pass one, composition, pass two) against the
+    oracle, with chains long enough that several groups are non-empty."""
+    x = W.dense_prefill(1, 64 * 21 + 9, 1, 2, seed=groups, lower_bound=-0.05, state_std=0.2)
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x, groups=groups)
+    _check(x, out, fin, pool, ref, f"G={groups}")
+
+
+def test_group_scan_paged_varlen():
+    x = W.varlen_paged([700, 64, 1300], 1, 2, slots=5, seed=9, lower_bound=-0.1,
+                       has_initial=[1, 1, 0])
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x, groups=4)
+    _check(x, out, fin, pool, ref, "G=4 varlen")
+
+
+def test_dense_prefill_full():
+    """B=2, T=4096, H=16, initial state N(0, 0.02), final state returned."""
+    x = W.workload("dense")
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x, dense=True)
+    _check(x, out, fin, pool, ref, "dense")
+
+
+def test_varlen_paged_full():
+    """8 sequences summing to 32768 tokens, Hqk=8, Hv=32, 64-slot fp32 cache."""
+    x = W.workload("varlen")
+    ref = oracle.prefill(x)
+    out, fin, pool = _run(x)
+    _check(x, out, fin, pool, ref, "varlen full")
+
+
+@pytest.mark.parametrize("groups", [1, 8])
+def test_long_prefill_sampled(groups):
+    """B=1, T=131072, H=32: the oracle runs two of the 32 heads over the whole
+    sequence; outputs of those heads and their final states are compared."""
+    x = W.workload("long", device="cuda")
+    import linear_attention_serving_fwd_gb300 as kda
+    out, fin = kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, A_log=x.A_log, dt_bias=x.dt_bias,
+                                 n_seqs=1, output_final_state=True, groups=groups)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status(clear=True) == 0
+    for h in (0, 29):
+        ref = oracle.recurrence(x.q[:, h:h + 1], x.k[:, h:h + 1], x.v[:, h:h + 1],
+                                x.g[:, h:h + 1], x.beta[:, h:h + 1], [0, x.t_total],
+                                A_log=x.A_log[h:h + 1], dt_bias=x.dt_bias[h:h + 1])
+        check_out(out[:, h:h + 1], ref["out"], f"long head {h}")
+        check_state(fin[:, h:h + 1], ref["state"], f"long head {h} state")
