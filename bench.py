@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--extras", default="decode,verify,varlen,long",
+                    help="comma list of extra workloads: decode, verify, varlen, long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -288,7 +290,10 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
     steps = max(5, min(args.steps, 20))
     sb = 4 * D * D
     # decode / verify on the 256-request batch, H=32, 512-slot pool
+    want = set(args.extras.split(","))
     for window in (1, 4):
+        if not ({"decode", "verify"} & want):
+            break
         y = W.workload("decode", window=window, seed=rank, device="cuda")
         pool = y.state_pool
         out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
@@ -297,6 +302,8 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
         kg = torch.empty((y.n_seqs, y.hv, window, 2 * D), dtype=torch.bfloat16, device="cuda")
         for verify in (False, True):
             if verify and window == 1:
+                continue
+            if ("verify" if verify else "decode") not in want:
                 continue
 
             def fn():
@@ -329,6 +336,8 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
         del y, pool
     # varlen paged and long-context prefill
     for name in ("varlen", "long"):
+        if name not in want:
+            continue
         z = W.workload(name, seed=rank, device="cuda")
         out = torch.empty((z.t_total, z.hv, D), dtype=torch.bfloat16, device="cuda")
         ws = torch.empty(kda.chunk_workspace_bytes(z.n_seqs, z.t_total, z.hv, 0),

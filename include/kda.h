@@ -132,6 +132,32 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
                   int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that cannot allocate
+ * device memory.  The paper has no counterpart; this is a deployment aid.
+ *
+ * Who needs it: a runtime that reserves all device memory up front, or that
+ * records work into CUDA graphs and forbids cudaMalloc afterwards; a plugin
+ * whose host owns the allocator; code that must not synchronise (cudaMalloc
+ * may).  Such callers cannot provide the prefill's workspace.
+ *
+ * Same arguments and results as kda_chunk_fwd, without workspace and
+ * workspace_bytes.  The scratch is one fixed 64 MiB array inside the library,
+ * held by every GPU that loads the library until the process exits.  A call
+ * whose kda_chunk_workspace_bytes(n_seqs, T, Hv, groups) exceeds 64 MiB is
+ * rejected with KDA_ERR_INVALID_ARGUMENT before any launch.  The first call
+ * on a device resolves the array's device address (cudaGetSymbolAddress), so
+ * make that first call before any stream capture.  All calls share the one
+ * array and it keeps the last call's contents; nothing in it needs to start
+ * at zero.  Calls that overlap on the GPU (other streams, other threads) race
+ * on it: serialise them.  Allocates nothing (no cudaMalloc / cudaFree).
+ */
+int kda_chunk_fwd_noalloc(const kda_activations* x, void* out, const int32_t* cu_seqlens,
+                          int32_t n_seqs, const float* initial_state, float* final_state,
+                          float* state_cache, int64_t slot_stride, int64_t n_slots,
+                          const int32_t* state_indices, const uint8_t* has_initial_state,
+                          int32_t groups, void* stream);
+
+/*
  * kda_decode - in-place decode of a short window (1 <= window <= 8 tokens per
  * request) on a paged fp32 state cache: the MATE gated_delta_rule_decode
  * contract for fp32 V-first states with in-kernel gate, lower bound, beta

@@ -22,8 +22,8 @@ from . import _native
 from ._native import KdaError
 
 D = 128
-__all__ = ["kda_chunk_fwd", "kda_decode", "kda_verify", "kda_device_status",
-           "chunk_workspace_bytes", "KdaError", "library_path"]
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode", "kda_verify",
+           "kda_device_status", "chunk_workspace_bytes", "KdaError", "library_path"]
 
 
 def library_path() -> str:
@@ -154,6 +154,37 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
         _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
         int(groups), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream_handle(stream))
+    _native.check(rc)
+    del keep
+    return out, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, out, A_log=None, dt_bias=None, scale=None,
+                          lower_bound=-5.0, cu_seqlens=None, n_seqs=None, initial_state=None,
+                          final_state=None, state_cache=None, state_indices=None,
+                          has_initial_state=None, groups: int = 0, stream=None):
+    """Chunked prefill through ``kda_chunk_fwd_noalloc``: for callers that
+    cannot allocate device memory.  The library's fixed 64 MiB scratch array
+    replaces the workspace; the caller passes every input and output
+    (``out`` and, if wanted, ``final_state``), so with contiguous A_log /
+    dt_bias this wrapper allocates nothing on the device either.  Calls that
+    overlap on the GPU race on the shared scratch.  Returns (out, final_state)."""
+    dense_b = q.shape[0] if q.dim() == 4 else None
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
+    v, g = _as_tokens(v, "v"), _as_tokens(g, "g")
+    beta = _as_tokens(beta, "beta", heads_dim=False)
+    a, keep = _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound)
+    if cu_seqlens is not None:
+        n = cu_seqlens.numel() - 1
+    else:
+        n = n_seqs if n_seqs is not None else (dense_b if dense_b is not None else 1)
+    slot_stride, n_slots = 0, 0
+    if state_cache is not None:
+        slot_stride, n_slots = state_cache.stride(0), state_cache.shape[0]
+    rc = _native.lib().kda_chunk_fwd_noalloc(
+        ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
+        _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
+        int(groups), _stream_handle(stream))
     _native.check(rc)
     del keep
     return out, final_state

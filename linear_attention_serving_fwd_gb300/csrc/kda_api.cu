@@ -170,6 +170,11 @@ void trace_drain() {  // caller holds the lock
 }  // namespace
 
 namespace kda {
+void set_last_error(int code, const char* msg) {
+  (void)code;
+  g_last_error = msg;
+}
+
 void trace_begin(const char* name, cudaStream_t stream) {
   if (!g_trace_on) return;
   std::lock_guard<std::mutex> lk(g_trace_mu);

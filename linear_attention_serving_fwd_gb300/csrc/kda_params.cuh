@@ -62,6 +62,9 @@ struct ChunkParams {
 void trace_begin(const char* name, cudaStream_t stream);
 void trace_end(cudaStream_t stream);
 
+// Set the thread-local text that kda_last_error() returns.
+void set_last_error(int code, const char* msg);
+
 // Launchers (kernels' translation units); return 0 or -1 (see cudaGetLastError).
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream);
 size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out);
