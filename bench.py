@@ -225,7 +225,10 @@ def run_ours(args, rank, world, barrier, reduce_max):
     launches = sum(c for _, c in tr.values())
     dom = max(tr, key=lambda k: tr[k][0])
     dom_ms = tr[dom][0] / tr[dom][1]
-    per_kernel_flop = {"kda_prologue": 8 * CHUNK * D, "kda_walk": 6 * D * D + 2 * CHUNK * D,
+    # algorithmic flop per (token, v-head) by kernel: the prologue forms A_kk,
+    # A_qk and w = T Kg (6 C K); the walk forms w S, qg' S, kg^T U (6 K V) and
+    # [u ; A_qk u] = [T ; A_qk T] v (4 C K)
+    per_kernel_flop = {"kda_prologue": 6 * CHUNK * D, "kda_walk": 6 * D * D + 4 * CHUNK * D,
                        "kda_walk_pass1": 2 * (6 * D * D), "kda_group_compose": 0}
     f_unit = per_kernel_flop.get(dom, flop_per_token_head())
     achieved = th * f_unit / (dom_ms / 1e3) / 1e12

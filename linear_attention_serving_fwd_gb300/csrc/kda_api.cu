@@ -119,10 +119,31 @@ int check_pool(const float* pool, int64_t slot_stride, int64_t n_slots, int hv, 
   return KDA_OK;
 }
 
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();  // no device here: size for a full GB300
+    return 152;
+  }
+  return sms;
+}
+
+// Chunk groups per sequence for the parallel scan (the vLLM kda_chunk page's
+// _chunk_groups rule, fitted to this walk): the walk runs one CTA per SM and
+// is latency bound, so splitting a chain only pays while pass one's grid
+// (8 column blocks per sequence, head and group) still fits on the SMs, and
+// while groups stay at least 8 chunks long.  G = 2 is depth-neutral, so the
+// split starts at G = 4.
 int choose_groups(int32_t n_seqs, int32_t t_total, int32_t hv, int32_t requested) {
   if (requested > 0) return requested < 64 ? requested : 64;
-  (void)n_seqs; (void)t_total; (void)hv;
-  return 1;
+  const int sms = device_sm_count();
+  const long pass1 = 8L * n_seqs * hv;
+  const long chunks = ((long)t_total + kda::CHUNK - 1) / kda::CHUNK;
+  const long avg = chunks / (n_seqs > 0 ? n_seqs : 1);
+  int g = 1;
+  while (g < 64 && pass1 * 2 * g <= sms && avg / (2 * g) >= 8) g *= 2;
+  return g >= 4 ? g : 1;
 }
 
 // --- kernel tracing --------------------------------------------------------

@@ -1,35 +1,49 @@
-// Chunked KDA prefill (chunk = 64), as the vLLM kimi_k3 AMD kda_chunk page
-// splits it: a prologue that is parallel over chunks (gate, beta, L2 norms,
-// gate cumsum, both intra-chunk passes, the WY/UT solve) and a walk that is
-// serial over chunks per (sequence, head) and fused with the output, plus
-// the chunk-group parallel scan of _chunk_groups for long chains.
+// Chunked KDA prefill (chunk = 64) on tcgen05 tensor cores.
 //
-// Per chunk of rows r = 0..63 (Lam = in-chunk cumsum of the gate):
-//   A_kk[r,i] = beta_r sum_c k^_rc k^_ic e^{Lam_rc - Lam_ic}   (i < r)
-//   A_qk[r,i] = sum_c q~_rc k^_ic e^{Lam_rc - Lam_ic}           (i <= r)
-//   (I + A_kk) w = diag(beta) (e^{Lam} * k^),  (I + A_kk) u = diag(beta) v
-//   qg = e^{Lam} * q~,  kg = e^{Lam_C - Lam} * k^,  d = e^{Lam_C}
-// and the walk, with S the K x V state:
-//   U = u - w S,  o = qg S + A_qk U,  S <- diag(d) S + kg^T U.
-// The exponent differences are factored per 16-row sub-chunk I around
-// ref_I = Lam at the middle row 16 I + 7 of I: below the block the row factor
-// e^{Lam_r - ref_I} is <= 1 and the column factor e^{ref_I - Lam_i} is at most
-// e^{8 |gate|max}; so factors stay inside fp32 (and bf16) range as long as
-// any 8 consecutive gates sum to more than -88 (a lower_bound >= -11).
+// Split as the vLLM kimi_k3 AMD kda_chunk page splits it: a prologue that is
+// parallel over (chunk, head) - gate, beta, L2 norms, gate cumsum, both
+// intra-chunk passes and the WY/UT solve - and a walk that is serial over the
+// chunks of a (sequence, head) and fused with the output, plus the chunk-group
+// parallel scan of _chunk_groups for long chains.
+//
+// Per chunk of rows r = 0..63 (Lam = in-chunk cumsum of the gate, C = 63):
+//   A_kk[r,i] = beta_r sum_c k^_rc k^_ic e^{Lam_rc - Lam_ic}  (i < r)
+//   A_qk[r,i] = sum_c q~_rc k^_ic e^{Lam_rc - Lam_ic}          (i <= r)
+//   T  = (I + A_kk)^{-1} diag(beta)
+//   Kg = e^{Lam} * k^,  qg = e^{Lam} * q~,  kg = e^{Lam_C - Lam} * k^,  d = e^{Lam_C}
+// The prologue emits, per (chunk, head), the walk's tensor-core operands in
+// their shared-memory layout (fp16, K-major, no swizzle):
+//   WQ = [w ; qg']  with w = T Kg and qg' = qg - A_qk w        (128 x 128)
+//   KGT = kg^T                                                 (128 x 64)
+//   TT = [T ; A_qk T]                                          (128 x 64)
+//   d                                                          (fp32, 128)
+// and the walk, per 32 value columns of the K x V state S, computes
+//   [u ; o_intra] = TT v,   X = WQ S,   U = u - X_w,   o = X_qg' + o_intra,
+//   S <- diag(d) S + KGT U
+// which equals U = u - w S, o = qg S + A_qk U, S' = diag(d) S + kg^T U.
+//
+// Precision: A_kk / A_qk use kind::tf32 (their operands carry exponent
+// factors up to e^{8 |gate|}, outside fp16 range); every other product uses
+// fp16 operands (11-bit significands, the tf32 class of rounding) with fp32
+// accumulation, and the state stays fp32.  Operand magnitudes: T, w, kg, Kg,
+// qg are bounded by 1 (scale); U and S scale with v and the initial state.
+//
+// The exponent differences of A_kk / A_qk are factored per 16-row sub-chunk I
+// around ref_I = Lam at its middle row 16 I + 7:
+//   e^{Lam_r - Lam_i} = (e^{Lam_r - ref_R} e^{ref_R - ref_I}) (e^{ref_I - Lam_i})
+// for r in block R >= I, i in block I; every factor stays within e^{+-88} as
+// long as any 8 consecutive gates sum above -88 (lower_bound >= -11).
 #include "kda_params.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
-// Floats of per-(chunk, head) prologue output in the workspace.
-constexpr int CH_W = 0;
-constexpr int CH_U = CH_W + CHUNK * D;
-constexpr int CH_QG = CH_U + CHUNK * D;
-constexpr int CH_KG = CH_QG + CHUNK * D;
-constexpr int CH_AQK = CH_KG + CHUNK * D;
-constexpr int CH_D = CH_AQK + CHUNK * CHUNK;
-constexpr int CH_FLOATS = CH_D + D;
-
-
+// Per-(chunk, head) workspace record, bytes.
+constexpr uint32_t CH_WQ = 0;                       // fp16 128 x 128
+constexpr uint32_t CH_KGT = CH_WQ + 128 * 128 * 2;  // fp16 128 x 64
+constexpr uint32_t CH_TT = CH_KGT + 128 * 64 * 2;   // fp16 128 x 64
+constexpr uint32_t CH_D = CH_TT + 128 * 64 * 2;     // fp32 128
+constexpr uint32_t CH_BYTES = CH_D + 128 * 4;       // 66048
 
 __device__ __forceinline__ int seq_bos(const ChunkParams& p, int n) {
   return p.cu_seqlens ? p.cu_seqlens[n] : n * p.dense_len;
@@ -38,12 +52,35 @@ __device__ __forceinline__ int seq_eos(const ChunkParams& p, int n) {
   return p.cu_seqlens ? p.cu_seqlens[n + 1] : (n + 1) * p.dense_len;
 }
 
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Bounded mbarrier wait that also gives up once another thread of the CTA has
+// raised the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t phase, volatile int* abort,
+                                              unsigned* err) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < WAIT_CAP; ++i) {
+    if (mbar_try_wait(bar, phase)) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort) return false;
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > WAIT_NS) break;
+    }
+  }
+  set_error(err, ERR_TIMEOUT);
+  *abort = 1;
+  return false;
+}
+
 // --------------------------------------------------------------------------
 // Chunk index builder: chunk_off[n] = first global chunk of sequence n,
-// chunk_seq/chunk_j name each chunk.  One block.
+// chunk_seq / chunk_j name each chunk.  One block.
 // --------------------------------------------------------------------------
 __global__ void kda_chunk_index_kernel(ChunkParams p) {
-  __shared__ int s_total;
   if (threadIdx.x == 0) {
     int off = 0;
     bool bad = p.cu_seqlens && p.cu_seqlens[0] != 0;
@@ -58,7 +95,6 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
     if (p.cu_seqlens && p.cu_seqlens[p.n_seqs] != p.t_total) bad = true;
     p.chunk_off[p.n_seqs] = off;
     *p.n_chunks = off;
-    s_total = off;
     if (bad) set_error(p.err, ERR_INDEX);
   }
   __syncthreads();
@@ -72,175 +108,443 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 }
 
 // --------------------------------------------------------------------------
-// Prologue + intra-chunk solve, one CTA (256 threads) per (chunk, head).
+// Prologue: one CTA (256 threads) per (chunk, head).
 // --------------------------------------------------------------------------
 constexpr int PRO_THREADS = 256;
-constexpr int LDA = D + 4;  // padded row stride (floats) for the [64][128] tiles
+constexpr int LDH = 136;  // padded row stride (halves) of the [64][128] fp16 tiles
+constexpr int LDE = 132;  // padded row stride (floats) of the [64][128] fp32 tile
+constexpr int LDT = 65;   // row stride of the 64 x 64 fp32 matrices
 
-struct ProSmem {
-  float kh[CHUNK][LDA];
-  float qh[CHUNK][LDA];
-  float lam[CHUNK][LDA];
-  float Y[16][LDA];
-  float Akk[CHUNK][CHUNK + 1];
-  float Aqk[CHUNK][CHUNK + 1];
-  float beta[CHUNK];
-  float ref[D];
+struct __align__(1024) ProSmem {
+  // 64 KB region: tf32 X operand (128 x 128) during the A_kk / A_qk products,
+  // afterwards A2 = [A_qk; 0] (fp16 128 x 64), B2 = T^T (fp16 64 x 64) and
+  // A3 = [[T, 0], [-A_qk T, I]] (fp16 128 x 128).
+  unsigned char X[65536];
+  unsigned char B3[32768];  // fp16 [c][K]: K 0..63 = Kg rows, 64..127 = qg rows
+  unsigned char Y[8192];    // tf32 16 x 128 column operand of one sub-chunk
+  __half kh[64 * LDH];      // k^; with qh reused for the fp32 inverse L^{-1}
+  __half qh[64 * LDH];      // q~
+  float E[64 * LDE];        // e^{Lam_r - ref_R}
+  float A[64 * LDT];        // A_kk (masked, beta-scaled), then T
+  float ref[4][128];        // Lam at row 16R + 7
+  float eref[4][128];       // e^{ref_R}
+  float ekc[4][128];        // e^{Lam_C - ref_R}
+  float F[4][4][128];       // e^{ref_R - ref_I}, R > I
+  float ssq[4][64];         // partial |q|^2 per channel group
+  float ssk[4][64];         // partial |k|^2 per channel group
+  float half_tot[128];      // Lam at row 31
+  float lamc[128];          // Lam at row 63
+  float beta[64];
+  uint64_t bar;
+  uint32_t tmem;
+  int abort;
 };
+static_assert(sizeof(float) * 64 * LDT <= sizeof(__half) * 2 * 64 * LDH, "inverse fits");
 
 __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   ProSmem& s = *reinterpret_cast<ProSmem*>(smem_raw);
-  const int c = blockIdx.x, h = blockIdx.y;
-  if (c >= *p.n_chunks) return;
+  const int c_glob = blockIdx.x, h = blockIdx.y;
+  if (c_glob >= *p.n_chunks) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = p.chunk_seq[c], j = p.chunk_j[c];
+  const int n = p.chunk_seq[c_glob], j = p.chunk_j[c_glob];
   const int bos = seq_bos(p, n) + j * CHUNK;
   const int len = min(CHUNK, seq_eos(p, n) - bos);
   const int hq = h / (p.hv / p.hqk);
-  const float a = p.has_gate ? __expf(p.A_log[h]) : 0.f;
+  const float a_h = p.has_gate ? __expf(p.A_log[h]) : 0.f;
+  unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
 
-  // 1. loads and the gate
-  for (int e = tid; e < CHUNK * D; e += PRO_THREADS) {
-    const int r = e >> 7, ch = e & (D - 1);
-    float qv = 0.f, kv = 0.f, gate = 0.f;
-    if (r < len) {
-      const int64_t tok = bos + r;
-      qv = bf2f(p.q[tok * p.q_st + hq * p.q_sh + ch]);
-      kv = bf2f(p.k[tok * p.k_st + hq * p.k_sh + ch]);
-      const float gv = bf2f(p.g[tok * p.g_st + h * p.g_sh + ch]);
-      gate = p.has_gate ? p.lower_bound * sigmoidf_(a * (gv + p.dt_bias[h * D + ch])) : gv;
-    }
-    s.qh[r][ch] = qv;
-    s.kh[r][ch] = kv;
-    s.lam[r][ch] = gate;
+  if (warp == 0) {
+    tc::tmem_alloc(&s.tmem, 256);
+    tc::tmem_relinquish();
   }
-  if (tid < CHUNK) {
-    s.beta[tid] = tid < len ? sigmoidf_(bf2f(p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh])) : 0.f;
+  if (tid == 0) {
+    mbar_init(&s.bar, 1);
+    fence_mbar_init();
+    s.abort = 0;
   }
-  __syncthreads();
-  // 2. L2 norms (warp per row) and 3. gate cumsum (thread per channel)
-  for (int r = warp; r < CHUNK; r += PRO_THREADS / 32) {
-    float sq = 0.f, sk = 0.f;
-    for (int ch = lane; ch < D; ch += 32) {
-      sq += s.qh[r][ch] * s.qh[r][ch];
-      sk += s.kh[r][ch] * s.kh[r][ch];
-    }
-    sq = warp_sum(sq);
-    sk = warp_sum(sk);
-    const float rq = rsqrtf(sq + 1e-6f) * p.scale, rk = rsqrtf(sk + 1e-6f);
-    for (int ch = lane; ch < D; ch += 32) {
-      s.qh[r][ch] *= rq;
-      s.kh[r][ch] *= rk;
-    }
-  }
-  if (tid < D) {
+
+  // ---- phase 1: elementwise, thread = (channel c, row half rh) ------------
+  const int c = tid & 127, rh = tid >> 7;
+  float lam[32], kv[32], qv[32];
+  {
+    const float dt = p.has_gate ? p.dt_bias[h * D + c] : 0.f;
     float acc = 0.f;
-    for (int r = 0; r < CHUNK; ++r) {
-      acc += s.lam[r][tid];
-      s.lam[r][tid] = acc;
-    }
-  }
-  __syncthreads();
-
-  // 4. A_kk and A_qk, one 16-column block I at a time
-  for (int I = 0; I < 4; ++I) {
-    if (tid < D) s.ref[tid] = s.lam[16 * I + 7][tid];
-    __syncthreads();
-    for (int e = tid; e < 16 * D; e += PRO_THREADS) {
-      const int i = e >> 7, ch = e & (D - 1);
-      s.Y[i][ch] = s.kh[16 * I + i][ch] * __expf(s.ref[ch] - s.lam[16 * I + i][ch]);
-    }
-    __syncthreads();
-    const int r = tid >> 2, part = tid & 3;
-    float ak[16], aq[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ak[i] = aq[i] = 0.f;
-    if (r >= 16 * I) {
-      for (int cc = 0; cc < 32; ++cc) {
-        const int ch = part + 4 * cc;
-        const float f = __expf(s.lam[r][ch] - s.ref[ch]);
-        const float xk = s.kh[r][ch] * f, xq = s.qh[r][ch] * f;
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * rh + i;
+      float g = 0.f, q = 0.f, k = 0.f;
+      if (r < len) {
+        const int64_t tok = bos + r;
+        q = bf2f(p.q[tok * p.q_st + hq * p.q_sh + c]);
+        k = bf2f(p.k[tok * p.k_st + hq * p.k_sh + c]);
+        g = bf2f(p.g[tok * p.g_st + h * p.g_sh + c]);
+        g = p.has_gate ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
+      }
+      acc += g;
+      lam[i] = acc;
+      kv[i] = k;
+      qv[i] = q;
+    }
+    if (rh == 0) s.half_tot[c] = acc;
+    // row norms: reduce-scatter the 32 per-row partials over the warp's 32
+    // channels, then the four channel groups meet in shared memory
+    float pk[32], pq[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          ak[i] = fmaf(xk, s.Y[i][ch], ak[i]);
-          aq[i] = fmaf(xq, s.Y[i][ch], aq[i]);
-        }
+    for (int i = 0; i < 32; ++i) { pk[i] = kv[i] * kv[i]; pq[i] = qv[i] * qv[i]; }
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) {
+      const bool up = (lane & sh) != 0;
+#pragma unroll
+      for (int m = 0; m < sh; ++m) {
+        const float sk = up ? pk[m] : pk[m + sh], kk = up ? pk[m + sh] : pk[m];
+        const float sq = up ? pq[m] : pq[m + sh], qq = up ? pq[m + sh] : pq[m];
+        pk[m] = kk + __shfl_xor_sync(0xffffffffu, sk, sh);
+        pq[m] = qq + __shfl_xor_sync(0xffffffffu, sq, sh);
       }
     }
+    s.ssk[warp & 3][32 * rh + lane] = pk[0];
+    s.ssq[warp & 3][32 * rh + lane] = pq[0];
+    if (tid < 64)
+      s.beta[tid] = tid < len ? sigmoidf_(bf2f(p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh])) : 0.f;
+  }
+  __syncthreads();
+  if (rh == 1) {
+    const float off = s.half_tot[c];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) lam[i] += off;
+    s.lamc[c] = lam[31];
+  }
+  // sub-chunk references: rows 7, 23 (rh 0) and 39, 55 (rh 1)
+  s.ref[2 * rh][c] = lam[7];
+  s.ref[2 * rh + 1][c] = lam[23];
+  __syncthreads();
+  {
+    const float lamC = s.lamc[c];
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      const int R = 2 * rh + bb;
+      const float rf = s.ref[R][c];
+      s.eref[R][c] = __expf(rf);
+      s.ekc[R][c] = __expf(lamC - rf);
+      for (int I = 0; I < R; ++I) s.F[R][I][c] = __expf(rf - s.ref[I][c]);
+    }
+    if (rh == 0) reinterpret_cast<float*>(wsb + CH_D)[c] = __expf(lamC);
+  }
+  __syncthreads();
+  {
+    uint32_t kgw[16], kgx[16], qgx[16];  // packed fp16 pairs along rows
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float kgv[2], Kgv[2], qgv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int ii = i + u;
+        const int r = 32 * rh + ii;
+        const int R = r >> 4;
+        const float sk = s.ssk[0][r] + s.ssk[1][r] + s.ssk[2][r] + s.ssk[3][r];
+        const float sq = s.ssq[0][r] + s.ssq[1][r] + s.ssq[2][r] + s.ssq[3][r];
+        const float kh = kv[ii] * rsqrtf(sk + 1e-6f);
+        const float qh = qv[ii] * rsqrtf(sq + 1e-6f) * p.scale;
+        const float e = __expf(lam[ii] - s.ref[R][c]);
+        s.E[r * LDE + c] = e;
+        s.kh[r * LDH + c] = __float2half_rn(kh);
+        s.qh[r * LDH + c] = __float2half_rn(qh);
+        Kgv[u] = kh * e * s.eref[R][c];
+        qgv[u] = qh * e * s.eref[R][c];
+        kgv[u] = e > 0.f ? kh * s.ekc[R][c] / e : 0.f;
+      }
+      kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
+      kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
+      qgx[i >> 1] = pack_half2(qgv[0], qgv[1]);
+    }
+    // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KGT [k = c][K = r]
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      const int r0 = 32 * rh + 8 * g8;
+      *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, r0, 128)) =
+          make_uint4(kgx[4 * g8], kgx[4 * g8 + 1], kgx[4 * g8 + 2], kgx[4 * g8 + 3]);
+      *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, 64 + r0, 128)) =
+          make_uint4(qgx[4 * g8], qgx[4 * g8 + 1], qgx[4 * g8 + 2], qgx[4 * g8 + 3]);
+      *reinterpret_cast<uint4*>(wsb + CH_KGT + tc::kmajor_offset(c, r0, 128)) =
+          make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s.tmem;
+
+  // ---- phase 2: A_kk / A_qk on kind::tf32, one 16-column block at a time ---
+  // row-owner mapping: row ro = 32 (warp & 1) + lane, channels cg .. cg + 31
+  const int ro = 32 * (warp & 1) + lane;
+  const int cg = 32 * (warp >> 1);
+  const int Ro = ro >> 4;
+  uint32_t bar_phase = 0;
+  for (int I = 0; I < 4; ++I) {
+    if (ro >= 16 * I) {
+#pragma unroll
+      for (int c4 = 0; c4 < 32; c4 += 4) {
+        const int cc = cg + c4;
+        float4 xk, xq;
+        float* pk = &xk.x;
+        float* pq = &xq.x;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float f = (Ro > I ? s.F[Ro][I][cc + u] : 1.f) * s.E[ro * LDE + cc + u];
+          pk[u] = tc::to_tf32(__half2float(s.kh[ro * LDH + cc + u]) * f);
+          pq[u] = tc::to_tf32(__half2float(s.qh[ro * LDH + cc + u]) * f);
+        }
+        *reinterpret_cast<float4*>(s.X + tc::kmajor_offset32(ro, cc, 128)) = xk;
+        *reinterpret_cast<float4*>(s.X + tc::kmajor_offset32(64 + ro, cc, 128)) = xq;
+      }
+    }
+    if (Ro == I) {
+#pragma unroll
+      for (int c4 = 0; c4 < 32; c4 += 4) {
+        const int cc = cg + c4;
+        float4 y;
+        float* py = &y.x;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float e = s.E[ro * LDE + cc + u];
+          py[u] = e > 0.f ? tc::to_tf32(__half2float(s.kh[ro * LDH + cc + u]) / e) : 0.f;
+        }
+        *reinterpret_cast<float4*>(s.Y + tc::kmajor_offset32(ro - 16 * I, cc, 16)) = y;
+      }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_kloop_tf32(tmem + 16 * I, smem_u32(s.X), smem_u32(s.Y), 128, 16, 128, false);
+      tc::mma_commit(&s.bar);
+    }
+    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+    bar_phase ^= 1u;
+    tc::fence_after_sync();
+  }
+
+  // ---- phase 3: read A_kk / A_qk; blocked inverse of L = I + A_kk ---------
+  unsigned char* A2 = s.X;           // [128][64]  fp16 = [A_qk ; 0]
+  unsigned char* B2 = s.X + 16384;   // [64][64]   fp16 = T^T
+  unsigned char* A3 = s.X + 32768;   // [128][128] fp16 = [[T, 0], [-A_qk T, I]]
+  float* Li = reinterpret_cast<float*>(s.kh);  // L^{-1}, [64][LDT]
+  if (warp < 4) {
+    float a[32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 32 * half), a);
+      if (warp < 2) {
+        const int r = 32 * warp + lane;
+        const float b = s.beta[r];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int col = 32 * half + i;
+          s.A[r * LDT + col] = col < r ? b * a[i] : 0.f;
+        }
+      } else {
+        const int r = 32 * (warp - 2) + lane;
+        uint32_t hv[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int col = 32 * half + i;
+          hv[i >> 1] = pack_half2(col <= r ? a[i] : 0.f, col + 1 <= r ? a[i + 1] : 0.f);
+        }
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, 32 * half + 8 * g8, 128)) =
+              make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+      }
+    }
+  } else {
+    const int t = tid - 128;
+    for (int e = t; e < 64 * 8; e += 128) {
+      const int r = 64 + (e >> 3), kk = 8 * (e & 7);
+      *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, kk, 128)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+  // diagonal 16 x 16 blocks of L^{-1} (unit lower triangular): thread = column
+  if (tid < 64) {
+    const int R = tid >> 4, jc = tid & 15, base = 16 * R;
+    float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], 1);
-      ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], 2);
-      aq[i] += __shfl_xor_sync(0xffffffffu, aq[i], 1);
-      aq[i] += __shfl_xor_sync(0xffffffffu, aq[i], 2);
-    }
-    if (part == 0) {
+      float acc = (i == jc) ? 1.f : 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int col = 16 * I + i;
-        s.Akk[r][col] = (col < r) ? s.beta[r] * ak[i] : 0.f;
-        s.Aqk[r][col] = (col <= r) ? aq[i] : 0.f;
-      }
+      for (int m = 0; m < i; ++m) acc -= s.A[(base + i) * LDT + base + m] * x[m];
+      x[i] = (i < jc) ? 0.f : acc;
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Li[(base + i) * LDT + base + jc] = x[i];
+  }
+  for (int e = tid; e < 64 * 64; e += PRO_THREADS) {
+    const int r = e >> 6, cc = e & 63;
+    if ((cc >> 4) > (r >> 4)) Li[r * LDT + cc] = 0.f;
+  }
+  __syncthreads();
+  // off-diagonal blocks, block row by block row:
+  //   L^{-1}_{RI} = - L^{-1}_{RR} sum_{J=I}^{R-1} A_{RJ} L^{-1}_{JI}
+  // (R * 256 elements per block row; each thread takes up to three)
+  for (int R = 1; R < 4; ++R) {
+    const int i = (tid >> 4) & 15, jj = tid & 15;
+    float pv[3] = {0.f, 0.f, 0.f};
+    for (int I = 0; I < R; ++I)
+      for (int J = I; J < R; ++J)
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          pv[I] += s.A[(16 * R + i) * LDT + 16 * J + m] * Li[(16 * J + m) * LDT + 16 * I + jj];
+    __syncthreads();
+    for (int I = 0; I < R; ++I) Li[(16 * R + i) * LDT + 16 * I + jj] = pv[I];  // partial sums in place
+    __syncthreads();
+    float lv[3] = {0.f, 0.f, 0.f};
+    for (int I = 0; I < R; ++I)
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        lv[I] -= Li[(16 * R + i) * LDT + 16 * R + m] * Li[(16 * R + m) * LDT + 16 * I + jj];
+    __syncthreads();
+    for (int I = 0; I < R; ++I) Li[(16 * R + i) * LDT + 16 * I + jj] = lv[I];
     __syncthreads();
   }
-
-  // 5. forward substitution: thread ch < 128 solves column ch of w, thread
-  //    128 + ch column ch of u; rows depend only on earlier rows of the same
-  //    column.
-  float* ws = p.ch + ((int64_t)c * p.hv + h) * CH_FLOATS;
-  {
-    const int ch = tid & (D - 1);
-    const bool is_u = tid >= D;
-    float col[CHUNK];
+  // T = L^{-1} diag(beta): T into A (fp32), A3 rows 0..63, TT rows 0..63
+  if (tid < 64) {
+    const int r = tid;
+    uint32_t tv[32];
 #pragma unroll
-    for (int r = 0; r < CHUNK; ++r) {
-      float rhs;
-      if (is_u) {
-        rhs = r < len ? bf2f(p.v[(int64_t)(bos + r) * p.v_st + h * p.v_sh + ch]) : 0.f;
-      } else {
-        rhs = __expf(s.lam[r][ch]) * s.kh[r][ch];
-      }
-      float acc = s.beta[r] * rhs;
-#pragma unroll
-      for (int i = 0; i < r; ++i) acc = fmaf(-s.Akk[r][i], col[i], acc);
-      col[r] = acc;
+    for (int i = 0; i < 64; i += 2) {
+      const float t0 = Li[r * LDT + i] * s.beta[i];
+      const float t1 = Li[r * LDT + i + 1] * s.beta[i + 1];
+      s.A[r * LDT + i] = t0;
+      s.A[r * LDT + i + 1] = t1;
+      tv[i >> 1] = pack_half2(t0, t1);
     }
-    float* dst = ws + (is_u ? CH_U : CH_W);
 #pragma unroll
-    for (int r = 0; r < CHUNK; ++r) dst[r * D + ch] = col[r];
+    for (int g8 = 0; g8 < 8; ++g8) {
+      const uint4 v4 = make_uint4(tv[4 * g8], tv[4 * g8 + 1], tv[4 * g8 + 2], tv[4 * g8 + 3]);
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g8, 128)) = v4;
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g8, 128)) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(r, 8 * g8, 128)) = v4;
+    }
+  } else if (tid >= 128 && tid < 192) {
+    const int r = tid - 128;  // A3 rows 64..127, K 64..127: the identity
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k0 = 8 * g8 + 2 * u;
+        w4[u] = pack_half2(k0 == r ? 1.f : 0.f, k0 + 1 == r ? 1.f : 0.f);
+      }
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g8, 128)) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
   }
-  // 6. qg, kg, d, A_qk
-  for (int e = tid; e < CHUNK * D; e += PRO_THREADS) {
-    const int r = e >> 7, ch = e & (D - 1);
-    const float lc = s.lam[CHUNK - 1][ch];
-    ws[CH_QG + e] = __expf(s.lam[r][ch]) * s.qh[r][ch];
-    ws[CH_KG + e] = __expf(lc - s.lam[r][ch]) * s.kh[r][ch];
+  __syncthreads();
+  if (tid < 64) {
+    const int jcol = tid;  // B2 [j][i] = T[i][j]
+    uint32_t tv[32];
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) tv[i >> 1] = pack_half2(s.A[i * LDT + jcol], s.A[(i + 1) * LDT + jcol]);
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8)
+      *reinterpret_cast<uint4*>(B2 + tc::kmajor_offset(jcol, 8 * g8, 64)) =
+          make_uint4(tv[4 * g8], tv[4 * g8 + 1], tv[4 * g8 + 2], tv[4 * g8 + 3]);
   }
-  for (int e = tid; e < CHUNK * CHUNK; e += PRO_THREADS) ws[CH_AQK + e] = s.Aqk[e >> 6][e & 63];
-  if (tid < D) ws[CH_D + tid] = __expf(s.lam[CHUNK - 1][tid]);
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+
+  // ---- phase 4: A_qk T (fp16 MMA) -> A3 rows 64.. (negated), TT rows 64.. ----
+  if (tid == 0) {
+    tc::fence_after_sync();
+    tc::mma_kloop(tmem + 64, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
+    tc::mma_commit(&s.bar);
+  }
+  wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+  bar_phase ^= 1u;
+  tc::fence_after_sync();
+  if (warp < 2) {
+    const int r = 32 * warp + lane;
+    float a[32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 64 + 32 * half), a);
+      uint32_t pos[16], neg[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        pos[i >> 1] = pack_half2(a[i], a[i + 1]);
+        neg[i >> 1] = pack_half2(-a[i], -a[i + 1]);
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const int k0 = 32 * half + 8 * g8;
+        *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, k0, 128)) =
+            make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
+        *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(64 + r, k0, 128)) =
+            make_uint4(pos[4 * g8], pos[4 * g8 + 1], pos[4 * g8 + 2], pos[4 * g8 + 3]);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+
+  // ---- phase 5: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA) -> WQ -------------------
+  if (tid == 0) {
+    tc::fence_after_sync();
+    tc::mma_kloop(tmem + 128, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
+    tc::mma_commit(&s.bar);
+  }
+  wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+  bar_phase ^= 1u;
+  tc::fence_after_sync();
+  if (warp < 4) {
+    const int row = 32 * warp + lane;
+    float a[32];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 128 + 32 * q4), a);
+      uint32_t hv[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) hv[i >> 1] = pack_half2(a[i], a[i + 1]);
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8)
+        *reinterpret_cast<uint4*>(wsb + CH_WQ + tc::kmajor_offset(row, 32 * q4 + 8 * g8, 128)) =
+            make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 // --------------------------------------------------------------------------
-// Inter-chunk walk.  One CTA per (column block of 32, head, sequence x group).
-// mode 0: outputs (+ final state when groups == 1), state from the initial
-//         state (group 0) or the composed incoming state;
-// mode 1: pass one of the group scan: zero start with u for the 4 value
-//         blocks -> B_g, identity start with u = 0 for blocks 4..7 -> M_g.
+// Inter-chunk walk on tcgen05.  One CTA (6 warps) per (column block of 32,
+// head, sequence x group): warps 0-3 own TMEM lanes (state row k = tid and
+// chunk row r), warp 4 streams the chunk records in, warp 5 issues MMAs.
+// mode 0: outputs (+ final state when groups == 1); mode 1: pass one of the
+// group scan (blocks 0..3 walk value columns from zero -> B_g, blocks 4..7
+// walk identity columns with u = 0 -> M_g).
 // --------------------------------------------------------------------------
-constexpr int WALK_THREADS = 256;
-constexpr int NB = 32;  // state columns per CTA
+constexpr int WALK_THREADS = 192;
+constexpr int NB = 32;
+// B operands of the walk (32 rows): K groups 528 bytes apart instead of 512,
+// so that a warp's column-wise stores (32 consecutive K of one row) spread
+// over 16 banks instead of 4
+constexpr uint32_t B_LBO = NB * 16 + 16;
 
-struct WalkSmem {
-  float w[CHUNK][D];
-  float qg[CHUNK][D];
-  float kg[CHUNK][D];
-  float aqk[CHUNK][CHUNK];
-  float u[CHUNK][NB];
-  float U[CHUNK][NB];
-  float S[D][NB];
-  float d[D];
+struct __align__(1024) WalkSmem {
+  unsigned char ch[2][CH_BYTES];          // chunk records (double buffered)
+  unsigned char v16[2][B_LBO * 64 / 8];   // v^T block, fp16 [v][r]
+  unsigned char s16[B_LBO * 128 / 8];     // S^T block, fp16 [v][k]
+  unsigned char u16[B_LBO * 64 / 8];      // U^T block, fp16 [v][r]
+  uint64_t full[2], vfull[2], empty[2];
+  uint64_t s_ready, u_ready, bar_x, bar_z;
+  int issued[2];
+  uint32_t tmem;
+  int abort;
 };
 
 __device__ __forceinline__ const float* initial_state(const ChunkParams& p, int n, int h) {
@@ -270,115 +574,214 @@ __device__ __forceinline__ void group_range(const ChunkParams& p, int n, int gid
   c1 = base + min(nc, (gidx + 1) * per);
 }
 
+// fp16 S^T block [v][k] from the fp32 state row k held by this thread
+__device__ __forceinline__ void write_s16(unsigned char* s16, int k, const float (&S)[32]) {
+#pragma unroll
+  for (int v = 0; v < 32; ++v)
+    *reinterpret_cast<__half*>(s16 + tc::kmajor_offset_lbo(v, k, B_LBO)) = __float2half_rn(S[v]);
+}
+
 __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p, int mode) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   WalkSmem& s = *reinterpret_cast<WalkSmem*>(smem_raw);
   const int cb = blockIdx.x, h = blockIdx.y;
   const int n = blockIdx.z / p.groups, gidx = blockIdx.z % p.groups;
-  const int tid = threadIdx.x;
-  const bool ident = mode == 1 && cb >= D / NB;   // M_g columns
-  const int col0 = (cb % (D / NB)) * NB;          // first value (or identity) column
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool ident = mode == 1 && cb >= D / NB;
+  const int col0 = (cb % (D / NB)) * NB;
   int c0, c1;
   group_range(p, n, gidx, c0, c1);
+  const int nch = c1 - c0;
   const int64_t plane = (((int64_t)n * p.hv + h) * p.groups + gidx) * D * D;
+  const unsigned char* wsb = reinterpret_cast<const unsigned char*>(p.ch);
 
-  // incoming state columns col0..col0+31, stored S[k][v]
-  {
-    const float* src = nullptr;
-    if (mode == 0) src = (p.groups > 1) ? p.gS + plane : initial_state(p, n, h);
-    for (int e = tid; e < D * NB; e += WALK_THREADS) {
-      const int v = e >> 7, k = e & (D - 1);
-      float x = 0.f;
-      if (mode == 1) x = (ident && k == col0 + v) ? 1.f : 0.f;
-      else if (src) x = src[(int64_t)(col0 + v) * D + k];
-      s.S[k][v] = x;
-    }
+  if (warp == 0) {
+    tc::tmem_alloc(&s.tmem, 128);
+    tc::tmem_relinquish();
   }
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.full[b], 1);
+      mbar_init(&s.vfull[b], 1);
+      mbar_init(&s.empty[b], 1);
+      s.issued[b] = 0;
+    }
+    mbar_init(&s.s_ready, 128);
+    mbar_init(&s.u_ready, 128);
+    mbar_init(&s.bar_x, 1);
+    mbar_init(&s.bar_z, 1);
+    fence_mbar_init();
+    s.abort = 0;
+  }
+  tc::fence_before_sync();
   __syncthreads();
-  const int lv = tid & 31;        // state column within the block
-  const int rg = tid >> 5;        // row group (8 warps)
-  for (int c = c0; c < c1; ++c) {
-    const float* ws = p.ch + ((int64_t)c * p.hv + h) * CH_FLOATS;
-    const int n_ = p.chunk_seq[c];
-    const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
-    const int len = min(CHUNK, seq_eos(p, n_) - bos);
-    for (int e = tid; e < CHUNK * D / 4; e += WALK_THREADS) {
-      reinterpret_cast<float4*>(&s.w[0][0])[e] = reinterpret_cast<const float4*>(ws + CH_W)[e];
-      reinterpret_cast<float4*>(&s.kg[0][0])[e] = reinterpret_cast<const float4*>(ws + CH_KG)[e];
-      if (mode == 0)
-        reinterpret_cast<float4*>(&s.qg[0][0])[e] = reinterpret_cast<const float4*>(ws + CH_QG)[e];
-    }
-    if (mode == 0)
-      for (int e = tid; e < CHUNK * CHUNK / 4; e += WALK_THREADS)
-        reinterpret_cast<float4*>(&s.aqk[0][0])[e] = reinterpret_cast<const float4*>(ws + CH_AQK)[e];
-    for (int e = tid; e < CHUNK * NB; e += WALK_THREADS) {
-      const int r = e >> 5, v = e & 31;
-      s.u[r][v] = ident ? 0.f : ws[CH_U + r * D + col0 + v];
-    }
-    if (tid < D) s.d[tid] = ws[CH_D + tid];
-    __syncthreads();
-    // U = u - w S and the inter-chunk part of o (8 rows per thread)
-    float accU[8], accO[8];
+  tc::fence_after_sync();
+  const uint32_t tmem = s.tmem;
+  const uint32_t T_UO = 0, T_X = 64, T_Z = 96;  // D_uo[b] at columns 32 b
+
+  if (warp < 4) {
+    // ---------------- math warps ----------------
+    const int k = tid;  // state row and TMEM lane
+    float S[32];
+    {
+      const float* src = nullptr;
+      if (mode == 0) src = (p.groups > 1) ? p.gS + plane : initial_state(p, n, h);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) accU[i] = accO[i] = 0.f;
-    for (int k = 0; k < D; k += 4) {
-      const float s0 = s.S[k][lv], s1 = s.S[k + 1][lv], s2 = s.S[k + 2][lv], s3 = s.S[k + 3][lv];
+      for (int v = 0; v < 32; ++v) {
+        float x = 0.f;
+        if (mode == 1) x = (ident && k == col0 + v) ? 1.f : 0.f;
+        else if (src) x = src[(int64_t)(col0 + v) * D + k];
+        S[v] = x;
+      }
+    }
+    if (nch > 0) {
+      write_s16(s.s16, k, S);
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&s.s_ready);
+    }
+    for (int it = 0; it < nch; ++it) {
+      const int b = it & 1;
+      const int c = c0 + it;
+      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) break;
+      if (!wait_or_abort(&s.bar_x, it & 1, &s.abort, p.err)) break;
+      tc::fence_after_sync();
+      const float dk = reinterpret_cast<const float*>(s.ch[b] + CH_D)[k];
+      float x[32], uo[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_X), x);
+      if (!ident) {
+        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_UO + 32 * b), uo);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = rg * 8 + i;
-        const float4 w4 = *reinterpret_cast<const float4*>(&s.w[r][k]);
-        accU[i] += w4.x * s0 + w4.y * s1 + w4.z * s2 + w4.w * s3;
-        if (mode == 0) {
-          const float4 q4 = *reinterpret_cast<const float4*>(&s.qg[r][k]);
-          accO[i] += q4.x * s0 + q4.y * s1 + q4.z * s2 + q4.w * s3;
+        for (int v = 0; v < 32; ++v) uo[v] = 0.f;
+      }
+      if (warp < 2) {
+        const int r = k;  // U = u - X_w, stored U^T fp16 [v][r]
+#pragma unroll
+        for (int v = 0; v < 32; ++v)
+          *reinterpret_cast<__half*>(s.u16 + tc::kmajor_offset_lbo(v, r, B_LBO)) =
+              __float2half_rn(uo[v] - x[v]);
+        fence_proxy_async_smem();
+      }
+      // TMEM read (and U written): the next MMAs may go
+      tc::fence_before_sync();
+      mbar_arrive(&s.u_ready);
+      if (warp >= 2 && mode == 0) {
+        const int r = k - 64;  // o = X_qg' + o_intra
+        const int n_ = p.chunk_seq[c];
+        const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
+        const int len = min(CHUNK, seq_eos(p, n_) - bos);
+        if (r < len) {
+          __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D + col0;
+#pragma unroll
+          for (int v8 = 0; v8 < 32; v8 += 8) {
+            uint4 w;
+            __nv_bfloat162 t0 = __floats2bfloat162_rn(x[v8] + uo[v8], x[v8 + 1] + uo[v8 + 1]);
+            __nv_bfloat162 t1 = __floats2bfloat162_rn(x[v8 + 2] + uo[v8 + 2], x[v8 + 3] + uo[v8 + 3]);
+            __nv_bfloat162 t2 = __floats2bfloat162_rn(x[v8 + 4] + uo[v8 + 4], x[v8 + 5] + uo[v8 + 5]);
+            __nv_bfloat162 t3 = __floats2bfloat162_rn(x[v8 + 6] + uo[v8 + 6], x[v8 + 7] + uo[v8 + 7]);
+            w.x = *reinterpret_cast<uint32_t*>(&t0);
+            w.y = *reinterpret_cast<uint32_t*>(&t1);
+            w.z = *reinterpret_cast<uint32_t*>(&t2);
+            w.w = *reinterpret_cast<uint32_t*>(&t3);
+            *reinterpret_cast<uint4*>(dst + v8) = w;
+          }
         }
       }
-    }
+      if (!wait_or_abort(&s.bar_z, it & 1, &s.abort, p.err)) break;
+      tc::fence_after_sync();
+      float z[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_Z), z);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s.U[rg * 8 + i][lv] = s.u[rg * 8 + i][lv] - accU[i];
-    __syncthreads();
-    if (mode == 0) {
-      for (int i2 = 0; i2 < CHUNK; ++i2) {
-        const float ui = s.U[i2][lv];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) accO[i] = fmaf(s.aqk[rg * 8 + i][i2], ui, accO[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = rg * 8 + i;
-        if (r < len)
-          p.out[((int64_t)(bos + r) * p.hv + h) * D + col0 + lv] = __float2bfloat16_rn(accO[i]);
+      for (int v = 0; v < 32; ++v) S[v] = fmaf(dk, S[v], z[v]);
+      if (it + 1 < nch) {
+        write_s16(s.s16, k, S);
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        mbar_arrive(&s.s_ready);
       }
     }
-    // S <- diag(d) S + kg^T U (16 state rows per thread)
-    float accS[16];
+    float* dst = nullptr;  // end state of this column block, V-first rows col0..
+    if (mode == 1) dst = (ident ? p.gM : p.gB) + plane;
+    else if (p.groups == 1) dst = final_state(p, n, h);
+    if (dst && !s.abort)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) accS[i] = s.d[rg * 16 + i] * s.S[rg * 16 + i][lv];
-    for (int r = 0; r < CHUNK; ++r) {
-      const float ur = s.U[r][lv];
-#pragma unroll
-      for (int i = 0; i < 16; i += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(&s.kg[r][rg * 16 + i]);
-        accS[i] = fmaf(k4.x, ur, accS[i]);
-        accS[i + 1] = fmaf(k4.y, ur, accS[i + 1]);
-        accS[i + 2] = fmaf(k4.z, ur, accS[i + 2]);
-        accS[i + 3] = fmaf(k4.w, ur, accS[i + 3]);
+      for (int v = 0; v < 32; ++v) dst[(int64_t)(col0 + v) * D + k] = S[v];
+  } else if (warp == 4) {
+    // ---------------- loader warp ----------------
+    for (int it = 0; it < nch; ++it) {
+      const int b = it & 1;
+      const int c = c0 + it;
+      if (it >= 2 && !wait_or_abort(&s.empty[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+      if (lane == 0) {
+        const unsigned char* src = wsb + ((size_t)c * p.hv + h) * CH_BYTES;
+        mbar_arrive_expect_tx(&s.full[b], CH_BYTES);
+        bulk_g2s(s.ch[b], src, 32768, &s.full[b]);
+        bulk_g2s(s.ch[b] + 32768, src + 32768, CH_BYTES - 32768, &s.full[b]);
+        s.issued[b] += 1;
       }
-    }
-    __syncthreads();  // everyone done reading S, U, chunk tiles
+      if (!ident) {
+        const int n_ = p.chunk_seq[c];
+        const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
+        const int len = min(CHUNK, seq_eos(p, n_) - bos);
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = lane + 32 * rr;
+          float vals[32];
+          if (r < len) {
+            const __nv_bfloat16* src = p.v + (int64_t)(bos + r) * p.v_st + h * p.v_sh + col0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s.S[rg * 16 + i][lv] = accS[i];
-    __syncthreads();
+            for (int q4 = 0; q4 < 32; q4 += 4) load_bf16x4(src + q4, &vals[q4]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) vals[v] = 0.f;
+          }
+#pragma unroll
+          for (int v = 0; v < 32; ++v)
+            *reinterpret_cast<__half*>(s.v16[b] + tc::kmajor_offset_lbo(v, r, B_LBO)) =
+                __float2half_rn(vals[v]);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.vfull[b]);
+    }
+  } else if (warp == 5 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    auto issue_uo = [&](int it) -> bool {
+      const int b = it & 1;
+      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return false;
+      if (!wait_or_abort(&s.vfull[b], (it >> 1) & 1, &s.abort, p.err)) return false;
+      tc::fence_after_sync();
+      if (!ident)
+        tc::mma_kloop(tmem + T_UO + 32 * b, smem_u32(s.ch[b] + CH_TT), smem_u32(s.v16[b]), 128, 32,
+                      64, 0, false, B_LBO);
+      return true;
+    };
+    bool ok = nch > 0 ? issue_uo(0) : true;
+    for (int it = 0; it < nch && ok; ++it) {
+      const int b = it & 1;
+      if (!wait_or_abort(&s.s_ready, it & 1, &s.abort, p.err)) break;
+      tc::fence_after_sync();
+      tc::mma_kloop(tmem + T_X, smem_u32(s.ch[b] + CH_WQ), smem_u32(s.s16), 128, 32, 128, 0, false,
+                    B_LBO);
+      tc::mma_commit(&s.bar_x);
+      if (it + 1 < nch && !issue_uo(it + 1)) break;
+      if (!wait_or_abort(&s.u_ready, it & 1, &s.abort, p.err)) break;
+      tc::fence_after_sync();
+      tc::mma_kloop(tmem + T_Z, smem_u32(s.ch[b] + CH_KGT), smem_u32(s.u16), 128, 32, 64, 0, false,
+                    B_LBO);
+      tc::mma_commit(&s.bar_z);
+      tc::mma_commit(&s.empty[b]);
+    }
   }
-  // end state of this column block, V-first rows col0..col0+31
-  float* dst = nullptr;
-  if (mode == 1) dst = (ident ? p.gM : p.gB) + plane;
-  else if (p.groups == 1) dst = final_state(p, n, h);
-  if (dst)
-    for (int e = tid; e < D * NB; e += WALK_THREADS) {
-      const int v = e >> 7, k = e & (D - 1);
-      dst[(int64_t)(col0 + v) * D + k] = s.S[k][v];
-    }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0 && s.abort) {
+    // leave no bulk copy in flight: wait (bounded) for the last load of each buffer
+    for (int b = 0; b < 2; ++b)
+      if (s.issued[b] > 0) mbar_wait_bounded(&s.full[b], (s.issued[b] - 1) & 1, p.err);
+  }
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 // --------------------------------------------------------------------------
@@ -386,23 +789,23 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
 // recording each group's incoming state; the last one is the final state.
 // One CTA (256 threads) per (value block of 32 rows, head, sequence).
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(WALK_THREADS, 1) kda_compose_kernel(ChunkParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+constexpr int COMPOSE_THREADS = 256;
+
+__global__ void __launch_bounds__(COMPOSE_THREADS, 1) kda_compose_kernel(ChunkParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   float* St = reinterpret_cast<float*>(smem_raw);  // [32][128] rows v0..v0+31 of S^T
   float* Mt = St + NB * D;                         // [128][128]
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int tid = threadIdx.x;
   const int v0 = vb * NB;
   const float* src = initial_state(p, n, h);
-  for (int e = tid; e < NB * D; e += WALK_THREADS)
-    St[e] = src ? src[(int64_t)v0 * D + e] : 0.f;
+  for (int e = tid; e < NB * D; e += COMPOSE_THREADS) St[e] = src ? src[(int64_t)v0 * D + e] : 0.f;
   __syncthreads();
   for (int gi = 0; gi < p.groups; ++gi) {
     const int64_t plane = (((int64_t)n * p.hv + h) * p.groups + gi) * D * D;
-    for (int e = tid; e < NB * D; e += WALK_THREADS) p.gS[plane + (int64_t)v0 * D + e] = St[e];
-    for (int e = tid; e < D * D; e += WALK_THREADS) Mt[e] = p.gM[plane + e];
+    for (int e = tid; e < NB * D; e += COMPOSE_THREADS) p.gS[plane + (int64_t)v0 * D + e] = St[e];
+    for (int e = tid; e < D * D; e += COMPOSE_THREADS) Mt[e] = p.gM[plane + e];
     __syncthreads();
-    // thread: row v = tid >> 3, 16 columns k = (tid & 7) + 8 j
     const int v = tid >> 3, kq = tid & 7;
     float acc[16];
 #pragma unroll
@@ -419,20 +822,24 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_compose_kernel(ChunkParam
   }
   float* dst = final_state(p, n, h);
   if (dst)
-    for (int e = tid; e < NB * D; e += WALK_THREADS) dst[(int64_t)v0 * D + e] = St[e];
+    for (int e = tid; e < NB * D; e += COMPOSE_THREADS) dst[(int64_t)v0 * D + e] = St[e];
 }
 
 // --------------------------------------------------------------------------
 // Host side
 // --------------------------------------------------------------------------
+static size_t int_words(int n_seqs, int max_chunks) {
+  size_t ints = 4 + (size_t)(n_seqs + 1) + 2 * (size_t)max_chunks;
+  return (ints + 63) & ~(size_t)63;  // keep the record area 256-byte aligned
+}
+
 size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out) {
   const int max_chunks = t_total / CHUNK + n_seqs;
   if (max_chunks_out) *max_chunks_out = max_chunks;
-  size_t ints = 4 + (size_t)(n_seqs + 1) + 2 * (size_t)max_chunks;
-  ints = (ints + 3) & ~(size_t)3;  // keep the float area 16-byte aligned
-  size_t floats = (size_t)max_chunks * hv * CH_FLOATS;
-  if (groups > 1) floats += 3 * (size_t)n_seqs * hv * groups * D * D;
-  return ints + floats;  // in 4-byte words
+  size_t words = int_words(n_seqs, max_chunks);
+  words += (size_t)max_chunks * hv * (CH_BYTES / 4);
+  if (groups > 1) words += 3 * (size_t)n_seqs * hv * groups * D * D;
+  return words;  // 4-byte words
 }
 
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
@@ -454,11 +861,9 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   p.chunk_off = iw + 4;
   p.chunk_seq = p.chunk_off + (p.n_seqs + 1);
   p.chunk_j = p.chunk_seq + max_chunks;
-  size_t ints = 4 + (size_t)(p.n_seqs + 1) + 2 * (size_t)max_chunks;
-  ints = (ints + 3) & ~(size_t)3;
-  float* fw = reinterpret_cast<float*>(iw + ints);
+  float* fw = reinterpret_cast<float*>(iw + int_words(p.n_seqs, max_chunks));
   p.ch = fw;
-  fw += (size_t)max_chunks * p.hv * CH_FLOATS;
+  fw += (size_t)max_chunks * p.hv * (CH_BYTES / 4);
   if (p.groups > 1) {
     const size_t plane = (size_t)p.n_seqs * p.hv * p.groups * D * D;
     p.gM = fw;
@@ -477,7 +882,7 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
                       sizeof(WalkSmem), stream>>>(p, 1);
     trace_end(stream);
     trace_begin("kda_group_compose", stream);
-    kda_compose_kernel<<<dim3(D / NB, p.hv, p.n_seqs), WALK_THREADS,
+    kda_compose_kernel<<<dim3(D / NB, p.hv, p.n_seqs), COMPOSE_THREADS,
                          (NB * D + D * D) * sizeof(float), stream>>>(p);
     trace_end(stream);
   }

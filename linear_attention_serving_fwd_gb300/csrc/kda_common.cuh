@@ -17,9 +17,17 @@ constexpr int MAX_WINDOW = 8;
 constexpr unsigned ERR_INDEX = 1u;    // bad slot / length seen by a kernel
 constexpr unsigned ERR_TIMEOUT = 2u;  // a bounded wait expired
 
-// Bounded waits: iteration cap for every mbarrier / flag spin.  At ~20 ns
-// per try_wait round this is far beyond any legitimate wait (~0.3 s).
-constexpr uint32_t WAIT_CAP = 1u << 24;
+// Bounded waits: every mbarrier / flag spin gives up after WAIT_NS of wall
+// time (read from %globaltimer every 64 rounds) or WAIT_CAP rounds, far
+// beyond any legitimate wait.
+constexpr uint32_t WAIT_CAP = 1u << 26;
+constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Kernels report through a pointer to the library's per-device error word
 // (passed in their parameters; see the API layer).
@@ -74,6 +82,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   uint32_t ok;
   asm volatile(
@@ -92,8 +104,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
 // expiry sets ERR_TIMEOUT and returns false; the caller must stop using the
 // guarded buffer.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, unsigned* err) {
-  for (uint32_t i = 0; i < WAIT_CAP; ++i)
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < WAIT_CAP; ++i) {
     if (mbar_try_wait(bar, phase)) return true;
+    if ((i & 63u) == 63u) {
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > WAIT_NS) break;
+    }
+  }
   set_error(err, ERR_TIMEOUT);
   return false;
 }

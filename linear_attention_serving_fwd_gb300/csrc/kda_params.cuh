@@ -49,7 +49,7 @@ struct ChunkParams {
   int32_t* chunk_seq;   // [max_chunks]
   int32_t* chunk_j;     // [max_chunks]
   int32_t* n_chunks;    // [1]
-  float* ch;            // [max_chunks, Hv, CH_FLOATS]
+  float* ch;            // per-(chunk, head) records, CH_BYTES each
   float* gM;            // [N, Hv, G, 128, 128]  M_g^T
   float* gB;            // [N, Hv, G, 128, 128]  B_g^T
   float* gS;            // [N, Hv, G, 128, 128]  incoming state of each group (V-first)
