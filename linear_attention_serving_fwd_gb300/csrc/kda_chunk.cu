@@ -38,12 +38,18 @@
 
 namespace kda {
 
-// Per-(chunk, head) workspace record, bytes.
+// Per-(chunk, head) workspace record, bytes.  The walk's B operands of
+// 32 rows (value columns) keep their K groups VB_LBO = 528 bytes apart (not
+// 512) so that column-wise shared-memory stores avoid bank conflicts.
+constexpr uint32_t VB_LBO = 32 * 16 + 16;
+constexpr uint32_t VB_BYTES = VB_LBO * 64 / 8;      // fp16 v^T block [32 v][64 r]: 4224
 constexpr uint32_t CH_WQ = 0;                       // fp16 128 x 128
 constexpr uint32_t CH_KGT = CH_WQ + 128 * 128 * 2;  // fp16 128 x 64
 constexpr uint32_t CH_TT = CH_KGT + 128 * 64 * 2;   // fp16 128 x 64
 constexpr uint32_t CH_D = CH_TT + 128 * 64 * 2;     // fp32 128
-constexpr uint32_t CH_BYTES = CH_D + 128 * 4;       // 66048
+constexpr uint32_t CH_MAIN = CH_D + 128 * 4;        // 66048: what every value block reads
+constexpr uint32_t CH_V16 = CH_MAIN;                // 4 x fp16 v^T blocks, one per 32 columns
+constexpr uint32_t CH_BYTES = CH_V16 + 4 * VB_BYTES;  // 82944
 
 __device__ __forceinline__ int seq_bos(const ChunkParams& p, int n) {
   return p.cu_seqlens ? p.cu_seqlens[n] : n * p.dense_len;
@@ -64,12 +70,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t phase, vol
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < WAIT_CAP; ++i) {
     if (mbar_try_wait(bar, phase)) return true;
-    if ((i & 63u) == 63u) {
-      if (*abort) return false;
-      const uint64_t t = globaltimer_ns();
-      if (t0 == 0) t0 = t;
-      else if (t - t0 > WAIT_NS) break;
-    }
+    if (*abort) return false;
+    const uint64_t t = globaltimer_ns();
+    if (t0 == 0) t0 = t;
+    else if (t - t0 > WAIT_NS) break;
   }
   set_error(err, ERR_TIMEOUT);
   *abort = 1;
@@ -111,7 +115,7 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 // Prologue: one CTA (256 threads) per (chunk, head).
 // --------------------------------------------------------------------------
 constexpr int PRO_THREADS = 256;
-constexpr int LDH = 136;  // padded row stride (halves) of the [64][128] fp16 tiles
+constexpr int LDH = 132;  // padded row stride (halves) of the [64][128] fp16 tiles
 constexpr int LDE = 132;  // padded row stride (floats) of the [64][128] fp32 tile
 constexpr int LDT = 65;   // row stride of the 64 x 64 fp32 matrices
 
@@ -134,6 +138,7 @@ struct __align__(1024) ProSmem {
   float ssk[4][64];         // partial |k|^2 per channel group
   float half_tot[128];      // Lam at row 31
   float lamc[128];          // Lam at row 63
+  float rk[64], rq[64];     // 1/|k_r| and scale/|q_r|
   float beta[64];
   uint64_t bar;
   uint32_t tmem;
@@ -164,28 +169,52 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     s.abort = 0;
   }
 
+  // ---- phase 0: the chunk's q, k, g, v rows (bf16, 64 x 128 each) land in
+  // the X region with one batch of 16-byte asynchronous copies; rows past the
+  // sequence end are zero-filled
+  {
+    __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.X);
+    for (int e = tid; e < 4 * 64 * 16; e += PRO_THREADS) {
+      const int chunk16 = e & 15, r = (e >> 4) & 63, which = e >> 10;
+      const int64_t tok = bos + (r < len ? r : 0);
+      const __nv_bfloat16* src;
+      if (which == 0) src = p.q + tok * p.q_st + hq * p.q_sh;
+      else if (which == 1) src = p.k + tok * p.k_st + hq * p.k_sh;
+      else if (which == 2) src = p.g + tok * p.g_st + h * p.g_sh;
+      else src = p.v + tok * p.v_st + h * p.v_sh;
+      cp_async16(tiles + (which * 64 + r) * D + 8 * chunk16, src + 8 * chunk16, r < len ? 16u : 0u);
+    }
+    cp_async_wait_all();
+  }
+  __syncthreads();
+
   // ---- phase 1: elementwise, thread = (channel c, row half rh) ------------
   const int c = tid & 127, rh = tid >> 7;
   float lam[32], kv[32], qv[32];
   {
+    const __nv_bfloat16* tiles = reinterpret_cast<const __nv_bfloat16*>(s.X);
     const float dt = p.has_gate ? p.dt_bias[h * D + c] : 0.f;
     float acc = 0.f;
+    uint32_t vw[16];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int r = 32 * rh + i;
-      float g = 0.f, q = 0.f, k = 0.f;
-      if (r < len) {
-        const int64_t tok = bos + r;
-        q = bf2f(p.q[tok * p.q_st + hq * p.q_sh + c]);
-        k = bf2f(p.k[tok * p.k_st + hq * p.k_sh + c]);
-        g = bf2f(p.g[tok * p.g_st + h * p.g_sh + c]);
-        g = p.has_gate ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
-      }
+      const float q = bf2f(tiles[(0 * 64 + r) * D + c]);
+      const float k = bf2f(tiles[(1 * 64 + r) * D + c]);
+      float g = bf2f(tiles[(2 * 64 + r) * D + c]);
+      g = (p.has_gate && r < len) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
       acc += g;
       lam[i] = acc;
       kv[i] = k;
       qv[i] = q;
+      if (i & 1) vw[i >> 1] = pack_half2(bf2f(tiles[(3 * 64 + r - 1) * D + c]), bf2f(tiles[(3 * 64 + r) * D + c]));
     }
+    // v^T block of this column (value block c / 32), K groups of 8 rows
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8)
+      *reinterpret_cast<uint4*>(wsb + CH_V16 + (c >> 5) * VB_BYTES +
+                                tc::kmajor_offset_lbo(c & 31, 32 * rh + 8 * g8, VB_LBO)) =
+          make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
     if (rh == 0) s.half_tot[c] = acc;
     // row norms: reduce-scatter the 32 per-row partials over the warp's 32
     // channels, then the four channel groups meet in shared memory
@@ -218,6 +247,12 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
   // sub-chunk references: rows 7, 23 (rh 0) and 39, 55 (rh 1)
   s.ref[2 * rh][c] = lam[7];
   s.ref[2 * rh + 1][c] = lam[23];
+  if (tid < 64) {
+    const float sk = s.ssk[0][tid] + s.ssk[1][tid] + s.ssk[2][tid] + s.ssk[3][tid];
+    const float sq = s.ssq[0][tid] + s.ssq[1][tid] + s.ssq[2][tid] + s.ssq[3][tid];
+    s.rk[tid] = rsqrtf(sk + 1e-6f);
+    s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
+  }
   __syncthreads();
   {
     const float lamC = s.lamc[c];
@@ -242,17 +277,15 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
         const int ii = i + u;
         const int r = 32 * rh + ii;
         const int R = r >> 4;
-        const float sk = s.ssk[0][r] + s.ssk[1][r] + s.ssk[2][r] + s.ssk[3][r];
-        const float sq = s.ssq[0][r] + s.ssq[1][r] + s.ssq[2][r] + s.ssq[3][r];
-        const float kh = kv[ii] * rsqrtf(sk + 1e-6f);
-        const float qh = qv[ii] * rsqrtf(sq + 1e-6f) * p.scale;
+        const float kh = kv[ii] * s.rk[r];
+        const float qh = qv[ii] * s.rq[r];
         const float e = __expf(lam[ii] - s.ref[R][c]);
         s.E[r * LDE + c] = e;
         s.kh[r * LDH + c] = __float2half_rn(kh);
         s.qh[r * LDH + c] = __float2half_rn(qh);
         Kgv[u] = kh * e * s.eref[R][c];
         qgv[u] = qh * e * s.eref[R][c];
-        kgv[u] = e > 0.f ? kh * s.ekc[R][c] / e : 0.f;
+        kgv[u] = e > 0.f ? __fdividef(kh * s.ekc[R][c], e) : 0.f;
       }
       kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
       kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
@@ -281,20 +314,28 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
   const int cg = 32 * (warp >> 1);
   const int Ro = ro >> 4;
   uint32_t bar_phase = 0;
+  // Vector loads: lanes are consecutive rows, so the padded strides (132
+  // floats / 132 halves) put a quarter-warp's 16-byte (or a half-warp's
+  // 8-byte) accesses on distinct banks.
   for (int I = 0; I < 4; ++I) {
     if (ro >= 16 * I) {
 #pragma unroll
       for (int c4 = 0; c4 < 32; c4 += 4) {
         const int cc = cg + c4;
-        float4 xk, xq;
-        float* pk = &xk.x;
-        float* pq = &xq.x;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float f = (Ro > I ? s.F[Ro][I][cc + u] : 1.f) * s.E[ro * LDE + cc + u];
-          pk[u] = tc::to_tf32(__half2float(s.kh[ro * LDH + cc + u]) * f);
-          pq[u] = tc::to_tf32(__half2float(s.qh[ro * LDH + cc + u]) * f);
-        }
+        const float4 e4 = *reinterpret_cast<const float4*>(&s.E[ro * LDE + cc]);
+        const float4 f4 = Ro > I ? *reinterpret_cast<const float4*>(&s.F[Ro][I][cc])
+                                 : make_float4(1.f, 1.f, 1.f, 1.f);
+        const uint2 k2 = *reinterpret_cast<const uint2*>(&s.kh[ro * LDH + cc]);
+        const uint2 q2 = *reinterpret_cast<const uint2*>(&s.qh[ro * LDH + cc]);
+        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&k2.x));
+        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&k2.y));
+        const float2 q01 = __half22float2(*reinterpret_cast<const __half2*>(&q2.x));
+        const float2 q23 = __half22float2(*reinterpret_cast<const __half2*>(&q2.y));
+        const float f0 = e4.x * f4.x, f1 = e4.y * f4.y, f2 = e4.z * f4.z, f3 = e4.w * f4.w;
+        const float4 xk = make_float4(tc::to_tf32(k01.x * f0), tc::to_tf32(k01.y * f1),
+                                      tc::to_tf32(k23.x * f2), tc::to_tf32(k23.y * f3));
+        const float4 xq = make_float4(tc::to_tf32(q01.x * f0), tc::to_tf32(q01.y * f1),
+                                      tc::to_tf32(q23.x * f2), tc::to_tf32(q23.y * f3));
         *reinterpret_cast<float4*>(s.X + tc::kmajor_offset32(ro, cc, 128)) = xk;
         *reinterpret_cast<float4*>(s.X + tc::kmajor_offset32(64 + ro, cc, 128)) = xq;
       }
@@ -303,13 +344,14 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
 #pragma unroll
       for (int c4 = 0; c4 < 32; c4 += 4) {
         const int cc = cg + c4;
-        float4 y;
-        float* py = &y.x;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float e = s.E[ro * LDE + cc + u];
-          py[u] = e > 0.f ? tc::to_tf32(__half2float(s.kh[ro * LDH + cc + u]) / e) : 0.f;
-        }
+        const float4 e4 = *reinterpret_cast<const float4*>(&s.E[ro * LDE + cc]);
+        const uint2 k2 = *reinterpret_cast<const uint2*>(&s.kh[ro * LDH + cc]);
+        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&k2.x));
+        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&k2.y));
+        const float4 y = make_float4(e4.x > 0.f ? tc::to_tf32(__fdividef(k01.x, e4.x)) : 0.f,
+                                     e4.y > 0.f ? tc::to_tf32(__fdividef(k01.y, e4.y)) : 0.f,
+                                     e4.z > 0.f ? tc::to_tf32(__fdividef(k23.x, e4.z)) : 0.f,
+                                     e4.w > 0.f ? tc::to_tf32(__fdividef(k23.y, e4.w)) : 0.f);
         *reinterpret_cast<float4*>(s.Y + tc::kmajor_offset32(ro - 16 * I, cc, 16)) = y;
       }
     }
@@ -530,17 +572,15 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
 // --------------------------------------------------------------------------
 constexpr int WALK_THREADS = 192;
 constexpr int NB = 32;
-// B operands of the walk (32 rows): K groups 528 bytes apart instead of 512,
-// so that a warp's column-wise stores (32 consecutive K of one row) spread
-// over 16 banks instead of 4
-constexpr uint32_t B_LBO = NB * 16 + 16;
+constexpr uint32_t B_LBO = VB_LBO;  // fp16 B operands of 32 rows, padded K groups
 
 struct __align__(1024) WalkSmem {
-  unsigned char ch[2][CH_BYTES];          // chunk records (double buffered)
-  unsigned char v16[2][B_LBO * 64 / 8];   // v^T block, fp16 [v][r]
+  unsigned char ch[2][CH_MAIN];           // chunk records (double buffered)
+  unsigned char v16[2][VB_BYTES];         // this block's v^T, fp16 [v][r]
   unsigned char s16[B_LBO * 128 / 8];     // S^T block, fp16 [v][k]
   unsigned char u16[B_LBO * 64 / 8];      // U^T block, fp16 [v][r]
-  uint64_t full[2], vfull[2], empty[2];
+  int2 meta[2];                           // (first token, rows) of the buffered chunk
+  uint64_t full[2], empty[2];
   uint64_t s_ready, u_ready, bar_x, bar_z;
   int issued[2];
   uint32_t tmem;
@@ -602,7 +642,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.full[b], 1);
-      mbar_init(&s.vfull[b], 1);
       mbar_init(&s.empty[b], 1);
       s.issued[b] = 0;
     }
@@ -642,11 +681,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     }
     for (int it = 0; it < nch; ++it) {
       const int b = it & 1;
-      const int c = c0 + it;
       if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) break;
       if (!wait_or_abort(&s.bar_x, it & 1, &s.abort, p.err)) break;
       tc::fence_after_sync();
+      // read everything of buffer b now: after u_ready the loader may refill it
       const float dk = reinterpret_cast<const float*>(s.ch[b] + CH_D)[k];
+      const int2 meta = s.meta[b];
       float x[32], uo[32];
       tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_X), x);
       if (!ident) {
@@ -668,9 +708,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       mbar_arrive(&s.u_ready);
       if (warp >= 2 && mode == 0) {
         const int r = k - 64;  // o = X_qg' + o_intra
-        const int n_ = p.chunk_seq[c];
-        const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
-        const int len = min(CHUNK, seq_eos(p, n_) - bos);
+        const int bos = meta.x, len = meta.y;
         if (r < len) {
           __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D + col0;
 #pragma unroll
@@ -709,48 +747,27 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       for (int v = 0; v < 32; ++v) dst[(int64_t)(col0 + v) * D + k] = S[v];
   } else if (warp == 4) {
     // ---------------- loader warp ----------------
-    for (int it = 0; it < nch; ++it) {
-      const int b = it & 1;
-      const int c = c0 + it;
-      if (it >= 2 && !wait_or_abort(&s.empty[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
-      if (lane == 0) {
-        const unsigned char* src = wsb + ((size_t)c * p.hv + h) * CH_BYTES;
-        mbar_arrive_expect_tx(&s.full[b], CH_BYTES);
-        bulk_g2s(s.ch[b], src, 32768, &s.full[b]);
-        bulk_g2s(s.ch[b] + 32768, src + 32768, CH_BYTES - 32768, &s.full[b]);
-        s.issued[b] += 1;
-      }
-      if (!ident) {
+    if (lane == 0) {
+      for (int it = 0; it < nch; ++it) {
+        const int b = it & 1;
+        const int c = c0 + it;
+        if (it >= 2 && !wait_or_abort(&s.empty[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
         const int n_ = p.chunk_seq[c];
         const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
-        const int len = min(CHUNK, seq_eos(p, n_) - bos);
-        for (int rr = 0; rr < 2; ++rr) {
-          const int r = lane + 32 * rr;
-          float vals[32];
-          if (r < len) {
-            const __nv_bfloat16* src = p.v + (int64_t)(bos + r) * p.v_st + h * p.v_sh + col0;
-#pragma unroll
-            for (int q4 = 0; q4 < 32; q4 += 4) load_bf16x4(src + q4, &vals[q4]);
-          } else {
-#pragma unroll
-            for (int v = 0; v < 32; ++v) vals[v] = 0.f;
-          }
-#pragma unroll
-          for (int v = 0; v < 32; ++v)
-            *reinterpret_cast<__half*>(s.v16[b] + tc::kmajor_offset_lbo(v, r, B_LBO)) =
-                __float2half_rn(vals[v]);
-        }
-        fence_proxy_async_smem();
+        s.meta[b] = make_int2(bos, min(CHUNK, seq_eos(p, n_) - bos));
+        const unsigned char* src = wsb + ((size_t)c * p.hv + h) * CH_BYTES;
+        mbar_arrive_expect_tx(&s.full[b], CH_MAIN + (ident ? 0u : VB_BYTES));
+        bulk_g2s(s.ch[b], src, 32768, &s.full[b]);
+        bulk_g2s(s.ch[b] + 32768, src + 32768, CH_MAIN - 32768, &s.full[b]);
+        if (!ident) bulk_g2s(s.v16[b], src + CH_V16 + (cb % (D / NB)) * VB_BYTES, VB_BYTES, &s.full[b]);
+        s.issued[b] += 1;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.vfull[b]);
     }
   } else if (warp == 5 && lane == 0) {
     // ---------------- MMA issuer ----------------
     auto issue_uo = [&](int it) -> bool {
       const int b = it & 1;
       if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return false;
-      if (!wait_or_abort(&s.vfull[b], (it >> 1) & 1, &s.abort, p.err)) return false;
       tc::fence_after_sync();
       if (!ident)
         tc::mma_kloop(tmem + T_UO + 32 * b, smem_u32(s.ch[b] + CH_TT), smem_u32(s.v16[b]), 128, 32,

@@ -53,7 +53,8 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float v[4])
   *reinterpret_cast<uint2*>(p) = raw;
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// logistic function with the fast (2-ulp) divide; exp(-x) = inf gives 0
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -86,16 +87,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Test (and briefly wait for) the completion of ``phase``: the thread may be
+// suspended until the phase completes or about 0.1 ms pass, so waiting
+// threads park instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   uint32_t ok;
   asm volatile(
       "{\n"
       ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n"
       "}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(phase)
+      : "r"(smem_u32(bar)), "r"(phase), "r"(100000u)
       : "memory");
   return ok != 0;
 }
@@ -107,11 +111,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase,
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < WAIT_CAP; ++i) {
     if (mbar_try_wait(bar, phase)) return true;
-    if ((i & 63u) == 63u) {
-      const uint64_t t = globaltimer_ns();
-      if (t0 == 0) t0 = t;
-      else if (t - t0 > WAIT_NS) break;
-    }
+    const uint64_t t = globaltimer_ns();
+    if (t0 == 0) t0 = t;
+    else if (t - t0 > WAIT_NS) break;
   }
   set_error(err, ERR_TIMEOUT);
   return false;
@@ -144,6 +146,16 @@ __device__ __forceinline__ void bulk_wait_read() {
 template <int N>
 __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (Ampere-style cp.async);
+// src_bytes = 0 fills the destination with zeros without reading.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy

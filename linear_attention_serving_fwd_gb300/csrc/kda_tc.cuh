@@ -57,6 +57,28 @@ __host__ __device__ __forceinline__ uint32_t kmajor_offset32(uint32_t row, uint3
   return (k >> 2) * (R * 16u) + (row >> 3) * 128u + (row & 7u) * 16u + (k & 3u) * 4u;
 }
 
+// 128-byte-swizzled K-major fp32 operand of R rows (R % 8 == 0): K blocks of
+// 32 elements (128 bytes per row) are R * 128 bytes apart; inside a block,
+// rows are 128 bytes apart and the 16-byte chunk c of row r sits at chunk
+// c ^ (r % 8).  The block base must be 1024-byte aligned.  A warp storing 32
+// consecutive k of one row covers one 128-byte line: bank-conflict free.
+__host__ __device__ __forceinline__ uint32_t sw128_offset32(uint32_t row, uint32_t k, uint32_t R) {
+  const uint32_t kin = k & 31u;
+  return (k >> 5) * (R * 128u) + (row >> 3) * 1024u + (row & 7u) * 128u +
+         ((((kin >> 2) ^ (row & 7u)) & 7u) << 4) + (kin & 3u) * 4u;
+}
+
+// descriptor of a 128-byte-swizzled K-major operand (8-row groups 1024 bytes apart)
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;                  // leading offset: unused for swizzled K-major
+  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;                  // SWIZZLE_128B
+  return d;
+}
+
 // round an fp32 value to tf32 (nearest, ties away), kept in fp32 storage
 __device__ __forceinline__ float to_tf32(float x) {
   uint32_t r;
@@ -151,6 +173,21 @@ __device__ __forceinline__ void mma_kloop_tf32(uint32_t d_tmem, uint32_t a_saddr
   for (uint32_t s = 0; s < K / 8u; ++s) {
     const uint64_t ad = smem_desc(a_saddr + s * 2u * a_lbo, a_lbo, 128u);
     const uint64_t bd = smem_desc(b_saddr + s * 2u * b_lbo, b_lbo, 128u);
+    mma_tf32(d_tmem, ad, bd, idesc, (s > 0 || accumulate_first) ? 1u : 0u);
+  }
+}
+
+// kind::tf32 over K elements with both operands 128-byte-swizzled K-major:
+// four K = 8 steps per 128-byte block (start address + 32 bytes each), then
+// the next block (+ rows * 128 bytes).
+__device__ __forceinline__ void mma_kloop_tf32_sw128(uint32_t d_tmem, uint32_t a_saddr,
+                                                     uint32_t b_saddr, uint32_t M, uint32_t N,
+                                                     uint32_t K, bool accumulate_first) {
+  const uint32_t idesc = idesc_tf32(M, N);
+  for (uint32_t s = 0; s < K / 8u; ++s) {
+    const uint32_t kb = s >> 2, kk = s & 3u;
+    const uint64_t ad = smem_desc_sw128(a_saddr + kb * M * 128u + kk * 32u);
+    const uint64_t bd = smem_desc_sw128(b_saddr + kb * N * 128u + kk * 32u);
     mma_tf32(d_tmem, ad, bd, idesc, (s > 0 || accumulate_first) ? 1u : 0u);
   }
 }

@@ -19,7 +19,10 @@ from linear_attention_serving_fwd_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 D, C = 128, 64
-REC = 128 * 128 * 2 + 128 * 64 * 2 * 2 + 128 * 4
+MAIN = 128 * 128 * 2 + 128 * 64 * 2 * 2 + 128 * 4
+VB_LBO = 528
+VB = VB_LBO * 8
+REC = MAIN + 4 * VB
 
 
 def _kmajor_decode(raw: np.ndarray, R: int, K: int) -> np.ndarray:
@@ -28,6 +31,14 @@ def _kmajor_decode(raw: np.ndarray, R: int, K: int) -> np.ndarray:
     rows = np.arange(R)[:, None]
     ks = np.arange(K)[None, :]
     idx = ((ks // 8) * (R * 16) + (rows // 8) * 128 + (rows % 8) * 16 + (ks % 8) * 2) // 2
+    return h[idx]
+
+
+def _kmajor_decode_lbo(raw: np.ndarray, R: int, K: int, lbo: int) -> np.ndarray:
+    h = raw.view(np.float16).astype(np.float64)
+    rows = np.arange(R)[:, None]
+    ks = np.arange(K)[None, :]
+    idx = ((ks // 8) * lbo + (rows // 8) * 128 + (rows % 8) * 16 + (ks % 8) * 2) // 2
     return h[idx]
 
 
@@ -83,3 +94,10 @@ def test_prologue_records_match_chunk_form(T, lb):
             assert _rel(got_d, ops["d"]) < 1e-4, f"d {tag}"
             assert _rel(got_wq[:64], want_wq[:64]) < 5e-3, f"w {tag}: {_rel(got_wq[:64], want_wq[:64])}"
             assert _rel(got_wq[64:], want_wq[64:]) < 1e-2, f"qg' {tag}: {_rel(got_wq[64:], want_wq[64:])}"
+            # v^T blocks, fp16 [32 value columns][64 rows]: bf16 v converted to
+            # fp16, exact except below fp16's normal range (absolute 3e-8)
+            vv = pad(f(x.v[s:e, h]), (C, D))
+            for jb in range(4):
+                got_v = _kmajor_decode_lbo(rec[MAIN + jb * VB:MAIN + (jb + 1) * VB], 32, 64, VB_LBO)
+                np.testing.assert_allclose(got_v, vv[:, 32 * jb:32 * (jb + 1)].T, rtol=0, atol=3e-8,
+                                           err_msg=f"v block {jb} {tag}")
