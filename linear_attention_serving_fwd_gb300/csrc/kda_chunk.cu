@@ -563,14 +563,15 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
 }
 
 // --------------------------------------------------------------------------
-// Inter-chunk walk on tcgen05.  One CTA (6 warps) per (column block of 32,
+// Inter-chunk walk on tcgen05.  One CTA (5 warps) per (column block of 32,
 // head, sequence x group): warps 0-3 own TMEM lanes (state row k = tid and
-// chunk row r), warp 4 streams the chunk records in, warp 5 issues MMAs.
+// chunk row r) and their thread 0 issues the MMAs after a named barrier of
+// the four warps; warp 4 streams the chunk records in.
 // mode 0: outputs (+ final state when groups == 1); mode 1: pass one of the
 // group scan (blocks 0..3 walk value columns from zero -> B_g, blocks 4..7
 // walk identity columns with u = 0 -> M_g).
 // --------------------------------------------------------------------------
-constexpr int WALK_THREADS = 192;
+constexpr int WALK_THREADS = 160;
 constexpr int NB = 32;
 constexpr uint32_t B_LBO = VB_LBO;  // fp16 B operands of 32 rows, padded K groups
 
@@ -581,7 +582,7 @@ struct __align__(1024) WalkSmem {
   unsigned char u16[B_LBO * 64 / 8];      // U^T block, fp16 [v][r]
   int2 meta[2];                           // (first token, rows) of the buffered chunk
   uint64_t full[2], empty[2];
-  uint64_t s_ready, u_ready, bar_x, bar_z;
+  uint64_t bar_x, bar_z;
   int issued[2];
   uint32_t tmem;
   int abort;
@@ -645,8 +646,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       mbar_init(&s.empty[b], 1);
       s.issued[b] = 0;
     }
-    mbar_init(&s.s_ready, 128);
-    mbar_init(&s.u_ready, 128);
     mbar_init(&s.bar_x, 1);
     mbar_init(&s.bar_z, 1);
     fence_mbar_init();
@@ -659,8 +658,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   const uint32_t T_UO = 0, T_X = 64, T_Z = 96;  // D_uo[b] at columns 32 b
 
   if (warp < 4) {
-    // ---------------- math warps ----------------
+    // ---------------- TMEM warps: math, and thread 0 issues the MMAs --------
     const int k = tid;  // state row and TMEM lane
+    const bool issuer = tid == 0;
     float S[32];
     {
       const float* src = nullptr;
@@ -673,18 +673,40 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         S[v] = x;
       }
     }
+    // [u ; o_intra] = TT v for chunk it (one chunk ahead of its use)
+    auto issue_uo = [&](int it) {
+      const int b = it & 1;
+      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return;
+      tc::fence_after_sync();
+      if (!ident)
+        tc::mma_kloop(tmem + T_UO + 32 * b, smem_u32(s.ch[b] + CH_TT), smem_u32(s.v16[b]), 128, 32,
+                      64, 0, false, B_LBO);
+    };
+    // X = WQ S for chunk it, after S16 holds the state entering it
+    auto issue_x = [&](int it) {
+      const int b = it & 1;
+      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return;
+      tc::fence_after_sync();
+      tc::mma_kloop(tmem + T_X, smem_u32(s.ch[b] + CH_WQ), smem_u32(s.s16), 128, 32, 128, 0, false,
+                    B_LBO);
+      tc::mma_commit(&s.bar_x);
+    };
     if (nch > 0) {
       write_s16(s.s16, k, S);
       fence_proxy_async_smem();
       tc::fence_before_sync();
-      mbar_arrive(&s.s_ready);
+      named_bar_sync(1, 128);
+      if (issuer) {
+        issue_uo(0);
+        issue_x(0);
+      }
     }
     for (int it = 0; it < nch; ++it) {
       const int b = it & 1;
       if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) break;
       if (!wait_or_abort(&s.bar_x, it & 1, &s.abort, p.err)) break;
       tc::fence_after_sync();
-      // read everything of buffer b now: after u_ready the loader may refill it
+      // read everything of buffer b now: after Z is issued the loader may refill it
       const float dk = reinterpret_cast<const float*>(s.ch[b] + CH_D)[k];
       const int2 meta = s.meta[b];
       float x[32], uo[32];
@@ -703,9 +725,16 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
               __float2half_rn(uo[v] - x[v]);
         fence_proxy_async_smem();
       }
-      // TMEM read (and U written): the next MMAs may go
       tc::fence_before_sync();
-      mbar_arrive(&s.u_ready);
+      named_bar_sync(1, 128);  // U written, TMEM read: Z may go
+      if (issuer) {
+        tc::fence_after_sync();
+        tc::mma_kloop(tmem + T_Z, smem_u32(s.ch[b] + CH_KGT), smem_u32(s.u16), 128, 32, 64, 0, false,
+                      B_LBO);
+        tc::mma_commit(&s.bar_z);
+        tc::mma_commit(&s.empty[b]);
+        if (it + 1 < nch) issue_uo(it + 1);
+      }
       if (warp >= 2 && mode == 0) {
         const int r = k - 64;  // o = X_qg' + o_intra
         const int bos = meta.x, len = meta.y;
@@ -736,7 +765,8 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         write_s16(s.s16, k, S);
         fence_proxy_async_smem();
         tc::fence_before_sync();
-        mbar_arrive(&s.s_ready);
+        named_bar_sync(1, 128);  // S16 holds the next chunk's state: X may go
+        if (issuer && !s.abort) issue_x(it + 1);
       }
     }
     float* dst = nullptr;  // end state of this column block, V-first rows col0..
@@ -762,33 +792,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         if (!ident) bulk_g2s(s.v16[b], src + CH_V16 + (cb % (D / NB)) * VB_BYTES, VB_BYTES, &s.full[b]);
         s.issued[b] += 1;
       }
-    }
-  } else if (warp == 5 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    auto issue_uo = [&](int it) -> bool {
-      const int b = it & 1;
-      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return false;
-      tc::fence_after_sync();
-      if (!ident)
-        tc::mma_kloop(tmem + T_UO + 32 * b, smem_u32(s.ch[b] + CH_TT), smem_u32(s.v16[b]), 128, 32,
-                      64, 0, false, B_LBO);
-      return true;
-    };
-    bool ok = nch > 0 ? issue_uo(0) : true;
-    for (int it = 0; it < nch && ok; ++it) {
-      const int b = it & 1;
-      if (!wait_or_abort(&s.s_ready, it & 1, &s.abort, p.err)) break;
-      tc::fence_after_sync();
-      tc::mma_kloop(tmem + T_X, smem_u32(s.ch[b] + CH_WQ), smem_u32(s.s16), 128, 32, 128, 0, false,
-                    B_LBO);
-      tc::mma_commit(&s.bar_x);
-      if (it + 1 < nch && !issue_uo(it + 1)) break;
-      if (!wait_or_abort(&s.u_ready, it & 1, &s.abort, p.err)) break;
-      tc::fence_after_sync();
-      tc::mma_kloop(tmem + T_Z, smem_u32(s.ch[b] + CH_KGT), smem_u32(s.u16), 128, 32, 64, 0, false,
-                    B_LBO);
-      tc::mma_commit(&s.bar_z);
-      tc::mma_commit(&s.empty[b]);
     }
   }
   tc::fence_before_sync();

@@ -56,6 +56,11 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float v[4])
 // logistic function with the fast (2-ulp) divide; exp(-x) = inf gives 0
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
+// barrier among ``count`` threads (whole warps) on hardware barrier ``id``
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
