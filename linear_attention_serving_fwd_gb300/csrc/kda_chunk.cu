@@ -28,11 +28,13 @@
 // accumulation, and the state stays fp32.  Operand magnitudes: T, w, kg, Kg,
 // qg are bounded by 1 (scale); U and S scale with v and the initial state.
 //
-// The exponent differences of A_kk / A_qk are factored per 16-row sub-chunk I
-// around ref_I = Lam at its middle row 16 I + 7:
-//   e^{Lam_r - Lam_i} = (e^{Lam_r - ref_R} e^{ref_R - ref_I}) (e^{ref_I - Lam_i})
-// for r in block R >= I, i in block I; every factor stays within e^{+-88} as
-// long as any 8 consecutive gates sum above -88 (lower_bound >= -11).
+// The exponent differences of A_kk / A_qk are factored around m_R = Lam at
+// the middle row 16 R + 7 of the row's own 16-row sub-chunk R:
+//   e^{Lam_r - Lam_i} = (e^{Lam_r - m_R}) (e^{m_R - Lam_i})      (i <= 16 R + 15)
+// The first factor stays within e^{+-88} as long as any 8 consecutive gates
+// sum above -88 (lower_bound >= -11); the second is at most e^{88} and below 1
+// for every i before the middle row.  Kg, qg, kg are exponentiated directly
+// (e^{Lam_i}, e^{Lam_C - Lam_i} <= 1), so no factor of theirs can overflow.
 #include "kda_params.cuh"
 #include "kda_tc.cuh"
 
@@ -112,31 +114,50 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 }
 
 // --------------------------------------------------------------------------
-// Prologue: one CTA (256 threads) per (chunk, head).
+// Prologue: one CTA (512 threads, 16 warps) per (chunk, head).
+//
+// Phase 1 is channel-owner: thread (c, R) holds channel c of the 16 rows of
+// sub-chunk R and writes every operand that needs the gate cumsum straight
+// into its MMA layout (tf32 128-byte-swizzled K-major, which a warp's 32
+// consecutive channels of one row fill without bank conflicts):
+//   X   = [k^ e^{Lam - m} ; q~ e^{Lam - m}]          128 rows (m = m_R of the row)
+//   Y_R = k^_i e^{m_R - Lam_i},  i = 0 .. 16R + 15   16 (R + 1) rows
+// One batch of four kind::tf32 MMAs D_R = X Y_R^T then holds, in the rows of
+// sub-chunk R, A_kk (rows 0..63) and A_qk (rows 64..127) against every
+// column of sub-chunks 0..R.
+//
+// The inverse of L = I + A_kk (unit lower triangular) is built by recursive
+// doubling: the four diagonal 16 x 16 blocks by forward substitution, then
+//   L^{-1}_{ba} = - L^{-1}_{bb} A_{ba} L^{-1}_{aa}
+// for the two 16-row pairs and then for the two 32-row halves.
 // --------------------------------------------------------------------------
-constexpr int PRO_THREADS = 256;
-constexpr int LDH = 132;  // padded row stride (halves) of the [64][128] fp16 tiles
-constexpr int LDE = 132;  // padded row stride (floats) of the [64][128] fp32 tile
-constexpr int LDT = 65;   // row stride of the 64 x 64 fp32 matrices
+constexpr int PRO_THREADS = 512;
+constexpr int LDT = 65;  // row stride (floats) of the 64 x 64 fp32 matrices
+constexpr int LDW = 33;  // row stride of the 32 x 32 fp32 temporary
+
+// byte offset of Y_R inside the Y region and its first TMEM column
+__host__ __device__ constexpr uint32_t y_off(int R) { return 8192u * (uint32_t)(R * (R + 1) / 2); }
+__host__ __device__ constexpr uint32_t d_col(int R) { return 8u * (uint32_t)(R * (R + 1)); }
+
+// After the A_kk / A_qk MMAs the X / Y region holds (byte offsets):
+constexpr uint32_t P_A3 = 0;        // fp16 [128][128] = [[T, 0], [-A_qk T, I]]
+constexpr uint32_t P_A2 = 32768;    // fp16 [128][64]  = [A_qk ; 0]
+constexpr uint32_t P_B2 = 49152;    // fp16 [64][64]   = T^T
+constexpr uint32_t P_A = 57344;     // fp32 [64][LDT]  = beta-scaled strictly lower A_kk
+constexpr uint32_t P_LI = 74240;    // fp32 [64][LDT]  = L^{-1}
+constexpr uint32_t P_W = 90880;     // fp32 [32][LDW]  temporary product
+static_assert(P_A + 64 * LDT * 4 <= P_LI && P_LI + 64 * LDT * 4 <= P_W, "prologue carve");
 
 struct __align__(1024) ProSmem {
-  // 64 KB region: tf32 X operand (128 x 128) during the A_kk / A_qk products,
-  // afterwards A2 = [A_qk; 0] (fp16 128 x 64), B2 = T^T (fp16 64 x 64) and
-  // A3 = [[T, 0], [-A_qk T, I]] (fp16 128 x 128).
+  // q, k, g, v tiles (bf16 [4][64][128]) on entry, then X (tf32, 128 x 128);
+  // with Y the carve P_* above once the MMAs have read them
   unsigned char X[65536];
+  unsigned char Y[81920];   // Y_0 .. Y_3 at y_off(R)
   unsigned char B3[32768];  // fp16 [c][K]: K 0..63 = Kg rows, 64..127 = qg rows
-  unsigned char Y[8192];    // tf32 16 x 128 column operand of one sub-chunk
-  __half kh[64 * LDH];      // k^; with qh reused for the fp32 inverse L^{-1}
-  __half qh[64 * LDH];      // q~
-  float E[64 * LDE];        // e^{Lam_r - ref_R}
-  float A[64 * LDT];        // A_kk (masked, beta-scaled), then T
-  float ref[4][128];        // Lam at row 16R + 7
-  float eref[4][128];       // e^{ref_R}
-  float ekc[4][128];        // e^{Lam_C - ref_R}
-  float F[4][4][128];       // e^{ref_R - ref_I}, R > I
-  float ssq[4][64];         // partial |q|^2 per channel group
-  float ssk[4][64];         // partial |k|^2 per channel group
-  float half_tot[128];      // Lam at row 31
+  float ref[4][128];        // m_R = Lam at row 16R + 7
+  float qtot[4][128];       // gate sum of each sub-chunk
+  float ssk[4][64];         // |k_r|^2 partial per group of 32 channels
+  float ssq[4][64];
   float lamc[128];          // Lam at row 63
   float rk[64], rq[64];     // 1/|k_r| and scale/|q_r|
   float beta[64];
@@ -144,7 +165,7 @@ struct __align__(1024) ProSmem {
   uint32_t tmem;
   int abort;
 };
-static_assert(sizeof(float) * 64 * LDT <= sizeof(__half) * 2 * 64 * LDH, "inverse fits");
+static_assert(P_W + 32 * LDW * 4 <= sizeof(ProSmem::X) + sizeof(ProSmem::Y), "carve fits");
 
 __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -170,11 +191,13 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
   }
 
   // ---- phase 0: the chunk's q, k, g, v rows (bf16, 64 x 128 each) land in
-  // the X region with one batch of 16-byte asynchronous copies; rows past the
-  // sequence end are zero-filled
+  // X with one batch of 16-byte asynchronous copies; rows past the sequence
+  // end are zero-filled
   {
     __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.X);
-    for (int e = tid; e < 4 * 64 * 16; e += PRO_THREADS) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = tid + u * PRO_THREADS;
       const int chunk16 = e & 15, r = (e >> 4) & 63, which = e >> 10;
       const int64_t tok = bos + (r < len ? r : 0);
       const __nv_bfloat16* src;
@@ -184,45 +207,45 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
       else src = p.v + tok * p.v_st + h * p.v_sh;
       cp_async16(tiles + (which * 64 + r) * D + 8 * chunk16, src + 8 * chunk16, r < len ? 16u : 0u);
     }
+    if (tid < 64)
+      s.beta[tid] = tid < len ? sigmoidf_(bf2f(p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh])) : 0.f;
     cp_async_wait_all();
   }
   __syncthreads();
 
-  // ---- phase 1: elementwise, thread = (channel c, row half rh) ------------
-  const int c = tid & 127, rh = tid >> 7;
-  float lam[32], kv[32], qv[32];
+  // ---- phase 1: channel-owner, thread = (channel c, sub-chunk Rq) ----------
+  const int c = tid & 127, Rq = tid >> 7;
+  float lam[16], kv[16], qv[16];
   {
     const __nv_bfloat16* tiles = reinterpret_cast<const __nv_bfloat16*>(s.X);
     const float dt = p.has_gate ? p.dt_bias[h * D + c] : 0.f;
     float acc = 0.f;
-    uint32_t vw[16];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
+    uint32_t vw[8];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = 32 * rh + i;
-      const float q = bf2f(tiles[(0 * 64 + r) * D + c]);
-      const float k = bf2f(tiles[(1 * 64 + r) * D + c]);
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * Rq + i;
+      qv[i] = bf2f(tiles[(0 * 64 + r) * D + c]);
+      kv[i] = bf2f(tiles[(1 * 64 + r) * D + c]);
       float g = bf2f(tiles[(2 * 64 + r) * D + c]);
       g = (p.has_gate && r < len) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
       acc += g;
       lam[i] = acc;
-      kv[i] = k;
-      qv[i] = q;
       if (i & 1) vw[i >> 1] = pack_half2(bf2f(tiles[(3 * 64 + r - 1) * D + c]), bf2f(tiles[(3 * 64 + r) * D + c]));
     }
     // v^T block of this column (value block c / 32), K groups of 8 rows
 #pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8)
+    for (int g8 = 0; g8 < 2; ++g8)
       *reinterpret_cast<uint4*>(wsb + CH_V16 + (c >> 5) * VB_BYTES +
-                                tc::kmajor_offset_lbo(c & 31, 32 * rh + 8 * g8, VB_LBO)) =
+                                tc::kmajor_offset_lbo(c & 31, 16 * Rq + 8 * g8, VB_LBO)) =
           make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
-    if (rh == 0) s.half_tot[c] = acc;
-    // row norms: reduce-scatter the 32 per-row partials over the warp's 32
-    // channels, then the four channel groups meet in shared memory
-    float pk[32], pq[32];
+    s.qtot[Rq][c] = acc;
+    // row norms: reduce-scatter the 16 per-row partials over the warp's 32
+    // channels (row = lane % 16), then the four channel groups meet in smem
+    float pk[16], pq[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) { pk[i] = kv[i] * kv[i]; pq[i] = qv[i] * qv[i]; }
+    for (int i = 0; i < 16; ++i) { pk[i] = kv[i] * kv[i]; pq[i] = qv[i] * qv[i]; }
 #pragma unroll
-    for (int sh = 16; sh >= 1; sh >>= 1) {
+    for (int sh = 8; sh >= 1; sh >>= 1) {
       const bool up = (lane & sh) != 0;
 #pragma unroll
       for (int m = 0; m < sh; ++m) {
@@ -232,330 +255,297 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
         pq[m] = qq + __shfl_xor_sync(0xffffffffu, sq, sh);
       }
     }
-    s.ssk[warp & 3][32 * rh + lane] = pk[0];
-    s.ssq[warp & 3][32 * rh + lane] = pq[0];
-    if (tid < 64)
-      s.beta[tid] = tid < len ? sigmoidf_(bf2f(p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh])) : 0.f;
+    pk[0] += __shfl_xor_sync(0xffffffffu, pk[0], 16);
+    pq[0] += __shfl_xor_sync(0xffffffffu, pq[0], 16);
+    if (lane < 16) {
+      s.ssk[c >> 5][16 * Rq + lane] = pk[0];
+      s.ssq[c >> 5][16 * Rq + lane] = pq[0];
+    }
   }
   __syncthreads();
-  if (rh == 1) {
-    const float off = s.half_tot[c];
+  float mR;
+  {
+    float off = 0.f;
+    for (int R2 = 0; R2 < Rq; ++R2) off += s.qtot[R2][c];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) lam[i] += off;
-    s.lamc[c] = lam[31];
-  }
-  // sub-chunk references: rows 7, 23 (rh 0) and 39, 55 (rh 1)
-  s.ref[2 * rh][c] = lam[7];
-  s.ref[2 * rh + 1][c] = lam[23];
-  if (tid < 64) {
-    const float sk = s.ssk[0][tid] + s.ssk[1][tid] + s.ssk[2][tid] + s.ssk[3][tid];
-    const float sq = s.ssq[0][tid] + s.ssq[1][tid] + s.ssq[2][tid] + s.ssq[3][tid];
-    s.rk[tid] = rsqrtf(sk + 1e-6f);
-    s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
+    for (int i = 0; i < 16; ++i) lam[i] += off;
+    mR = lam[7];
+    s.ref[Rq][c] = mR;
+    if (Rq == 3) {
+      s.lamc[c] = lam[15];
+      reinterpret_cast<float*>(wsb + CH_D)[c] = __expf(lam[15]);
+    }
+    if (tid < 64) {
+      const float sk = s.ssk[0][tid] + s.ssk[1][tid] + s.ssk[2][tid] + s.ssk[3][tid];
+      const float sq = s.ssq[0][tid] + s.ssq[1][tid] + s.ssq[2][tid] + s.ssq[3][tid];
+      s.rk[tid] = rsqrtf(sk + 1e-6f);
+      s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
+    }
   }
   __syncthreads();
   {
     const float lamC = s.lamc[c];
+    float F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
 #pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-      const int R = 2 * rh + bb;
-      const float rf = s.ref[R][c];
-      s.eref[R][c] = __expf(rf);
-      s.ekc[R][c] = __expf(lamC - rf);
-      for (int I = 0; I < R; ++I) s.F[R][I][c] = __expf(rf - s.ref[I][c]);
-    }
-    if (rh == 0) reinterpret_cast<float*>(wsb + CH_D)[c] = __expf(lamC);
-  }
-  __syncthreads();
-  {
-    uint32_t kgw[16], kgx[16], qgx[16];  // packed fp16 pairs along rows
+    for (int R2 = 0; R2 < 4; ++R2) F[R2] = R2 > Rq ? __expf(s.ref[R2][c] - mR) : 1.f;
+    uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
+    for (int i = 0; i < 16; i += 2) {
       float kgv[2], Kgv[2], qgv[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int ii = i + u;
-        const int r = 32 * rh + ii;
-        const int R = r >> 4;
-        const float kh = kv[ii] * s.rk[r];
-        const float qh = qv[ii] * s.rq[r];
-        const float e = __expf(lam[ii] - s.ref[R][c]);
-        s.E[r * LDE + c] = e;
-        s.kh[r * LDH + c] = __float2half_rn(kh);
-        s.qh[r * LDH + c] = __float2half_rn(qh);
-        Kgv[u] = kh * e * s.eref[R][c];
-        qgv[u] = qh * e * s.eref[R][c];
-        kgv[u] = e > 0.f ? __fdividef(kh * s.ekc[R][c], e) : 0.f;
+        const int ii = i + u, r = 16 * Rq + ii;
+        const float kh = kv[ii] * s.rk[r], qh = qv[ii] * s.rq[r];
+        const float E = __expf(lam[ii] - mR);  // within e^{+-88}
+        const float iE = E > 0.f ? __fdividef(1.f, E) : 0.f;
+        const float eL = __expf(lam[ii]);
+        kgv[u] = kh * __expf(lamC - lam[ii]);
+        Kgv[u] = kh * eL;
+        qgv[u] = qh * eL;
+        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(kh * E);
+        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(qh * E);
+        const float y = kh * iE;
+#pragma unroll
+        for (int R2 = 0; R2 < 4; ++R2)
+          if (R2 >= Rq)
+            *reinterpret_cast<float*>(s.Y + y_off(R2) + tc::sw128_offset32(r, c, 16 * (R2 + 1))) =
+                tc::to_tf32(y * F[R2]);
       }
       kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
-      kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
+      Kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
       qgx[i >> 1] = pack_half2(qgv[0], qgv[1]);
     }
     // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KGT [k = c][K = r]
 #pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      const int r0 = 32 * rh + 8 * g8;
+    for (int g8 = 0; g8 < 2; ++g8) {
+      const int r0 = 16 * Rq + 8 * g8;
       *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, r0, 128)) =
-          make_uint4(kgx[4 * g8], kgx[4 * g8 + 1], kgx[4 * g8 + 2], kgx[4 * g8 + 3]);
+          make_uint4(Kgx[4 * g8], Kgx[4 * g8 + 1], Kgx[4 * g8 + 2], Kgx[4 * g8 + 3]);
       *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, 64 + r0, 128)) =
           make_uint4(qgx[4 * g8], qgx[4 * g8 + 1], qgx[4 * g8 + 2], qgx[4 * g8 + 3]);
       *reinterpret_cast<uint4*>(wsb + CH_KGT + tc::kmajor_offset(c, r0, 128)) =
           make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
     }
   }
+  fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
 
-  // ---- phase 2: A_kk / A_qk on kind::tf32, one 16-column block at a time ---
-  // row-owner mapping: row ro = 32 (warp & 1) + lane, channels cg .. cg + 31
-  const int ro = 32 * (warp & 1) + lane;
-  const int cg = 32 * (warp >> 1);
-  const int Ro = ro >> 4;
-  uint32_t bar_phase = 0;
-  // Vector loads: lanes are consecutive rows, so the padded strides (132
-  // floats / 132 halves) put a quarter-warp's 16-byte (or a half-warp's
-  // 8-byte) accesses on distinct banks.
-  for (int I = 0; I < 4; ++I) {
-    if (ro >= 16 * I) {
+  // ---- phase 2: A_kk / A_qk, four kind::tf32 MMAs, one commit ---------------
+  if (tid == 0) {
 #pragma unroll
-      for (int c4 = 0; c4 < 32; c4 += 4) {
-        const int cc = cg + c4;
-        const float4 e4 = *reinterpret_cast<const float4*>(&s.E[ro * LDE + cc]);
-        const float4 f4 = Ro > I ? *reinterpret_cast<const float4*>(&s.F[Ro][I][cc])
-                                 : make_float4(1.f, 1.f, 1.f, 1.f);
-        const uint2 k2 = *reinterpret_cast<const uint2*>(&s.kh[ro * LDH + cc]);
-        const uint2 q2 = *reinterpret_cast<const uint2*>(&s.qh[ro * LDH + cc]);
-        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&k2.x));
-        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&k2.y));
-        const float2 q01 = __half22float2(*reinterpret_cast<const __half2*>(&q2.x));
-        const float2 q23 = __half22float2(*reinterpret_cast<const __half2*>(&q2.y));
-        const float f0 = e4.x * f4.x, f1 = e4.y * f4.y, f2 = e4.z * f4.z, f3 = e4.w * f4.w;
-        const float4 xk = make_float4(tc::to_tf32(k01.x * f0), tc::to_tf32(k01.y * f1),
-                                      tc::to_tf32(k23.x * f2), tc::to_tf32(k23.y * f3));
-        const float4 xq = make_float4(tc::to_tf32(q01.x * f0), tc::to_tf32(q01.y * f1),
-                                      tc::to_tf32(q23.x * f2), tc::to_tf32(q23.y * f3));
-        *reinterpret_cast<float4*>(s.X + tc::kmajor_offset32(ro, cc, 128)) = xk;
-        *reinterpret_cast<float4*>(s.X + tc::kmajor_offset32(64 + ro, cc, 128)) = xq;
-      }
-    }
-    if (Ro == I) {
-#pragma unroll
-      for (int c4 = 0; c4 < 32; c4 += 4) {
-        const int cc = cg + c4;
-        const float4 e4 = *reinterpret_cast<const float4*>(&s.E[ro * LDE + cc]);
-        const uint2 k2 = *reinterpret_cast<const uint2*>(&s.kh[ro * LDH + cc]);
-        const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&k2.x));
-        const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&k2.y));
-        const float4 y = make_float4(e4.x > 0.f ? tc::to_tf32(__fdividef(k01.x, e4.x)) : 0.f,
-                                     e4.y > 0.f ? tc::to_tf32(__fdividef(k01.y, e4.y)) : 0.f,
-                                     e4.z > 0.f ? tc::to_tf32(__fdividef(k23.x, e4.z)) : 0.f,
-                                     e4.w > 0.f ? tc::to_tf32(__fdividef(k23.y, e4.w)) : 0.f);
-        *reinterpret_cast<float4*>(s.Y + tc::kmajor_offset32(ro - 16 * I, cc, 16)) = y;
-      }
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      tc::mma_kloop_tf32(tmem + 16 * I, smem_u32(s.X), smem_u32(s.Y), 128, 16, 128, false);
-      tc::mma_commit(&s.bar);
-    }
-    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-    bar_phase ^= 1u;
-    tc::fence_after_sync();
+    for (int R = 0; R < 4; ++R)
+      tc::mma_kloop_tf32_sw128(tmem + d_col(R), smem_u32(s.X), smem_u32(s.Y + y_off(R)), 128,
+                               16 * (R + 1), 128, false);
+    tc::mma_commit(&s.bar);
   }
+  uint32_t bar_phase = 0;
+  wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+  bar_phase ^= 1u;
+  tc::fence_after_sync();
 
-  // ---- phase 3: read A_kk / A_qk; blocked inverse of L = I + A_kk ---------
-  unsigned char* A2 = s.X;           // [128][64]  fp16 = [A_qk ; 0]
-  unsigned char* B2 = s.X + 16384;   // [64][64]   fp16 = T^T
-  unsigned char* A3 = s.X + 32768;   // [128][128] fp16 = [[T, 0], [-A_qk T, I]]
-  float* Li = reinterpret_cast<float*>(s.kh);  // L^{-1}, [64][LDT]
-  if (warp < 4) {
-    float a[32];
+  float* Af = reinterpret_cast<float*>(s.X + P_A);
+  float* Li = reinterpret_cast<float*>(s.X + P_LI);
+  float* Wt = reinterpret_cast<float*>(s.X + P_W);
+  unsigned char* A2 = s.X + P_A2;
+  unsigned char* A3 = s.X + P_A3;
+  unsigned char* B2 = s.X + P_B2;
+  {
+    // warp = (TMEM sub-partition sp, 16-column group cg); rows 0..63 of the
+    // accumulators are A_kk, rows 64..127 A_qk
+    const int sp = warp & 3, cg = warp >> 2;
+    const int r = 32 * (sp & 1) + lane, Rr = r >> 4, Rlo = 2 * (sp & 1);
+    float a0[16], a1[16];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 32 * half), a);
-      if (warp < 2) {
-        const int r = 32 * warp + lane;
-        const float b = s.beta[r];
+    for (int t = 0; t < 16; ++t) { a0[t] = 0.f; a1[t] = 0.f; }
+    if (cg <= Rlo) tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, d_col(Rlo) + 16 * cg), a0);
+    if (cg <= Rlo + 1) tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, d_col(Rlo + 1) + 16 * cg), a1);
+    const bool hi = Rr != Rlo, live = cg <= Rr;
+    if (sp < 2) {
+      const float b = s.beta[r];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = 32 * half + i;
-          s.A[r * LDT + col] = col < r ? b * a[i] : 0.f;
-        }
-      } else {
-        const int r = 32 * (warp - 2) + lane;
-        uint32_t hv[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int col = 32 * half + i;
-          hv[i >> 1] = pack_half2(col <= r ? a[i] : 0.f, col + 1 <= r ? a[i + 1] : 0.f);
-        }
-#pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, 32 * half + 8 * g8, 128)) =
-              make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+      for (int t = 0; t < 16; ++t) {
+        const int col = 16 * cg + t;
+        Af[r * LDT + col] = (live && col < r) ? b * (hi ? a1[t] : a0[t]) : 0.f;
       }
+    } else {
+      uint32_t hv[8];
+#pragma unroll
+      for (int t = 0; t < 16; t += 2) {
+        const int col = 16 * cg + t;
+        const float x0 = (live && col <= r) ? (hi ? a1[t] : a0[t]) : 0.f;
+        const float x1 = (live && col + 1 <= r) ? (hi ? a1[t + 1] : a0[t + 1]) : 0.f;
+        hv[t >> 1] = pack_half2(x0, x1);
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < 2; ++g8)
+        *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, 16 * cg + 8 * g8, 128)) =
+            make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
     }
-  } else {
-    const int t = tid - 128;
-    for (int e = t; e < 64 * 8; e += 128) {
-      const int r = 64 + (e >> 3), kk = 8 * (e & 7);
-      *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, kk, 128)) = make_uint4(0, 0, 0, 0);
+    // A2 rows 64..127 are zero; L^{-1} above its diagonal blocks is zero
+    *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(64 + (tid & 63), 8 * (tid >> 6), 128)) =
+        make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = tid + u * PRO_THREADS, rr = e >> 6, cc = e & 63;
+      if ((cc >> 4) > (rr >> 4)) Li[rr * LDT + cc] = 0.f;
     }
   }
   __syncthreads();
-  // diagonal 16 x 16 blocks of L^{-1} (unit lower triangular): thread = column
+
+  // ---- phase 3: L^{-1} by recursive doubling ---------------------------------
   if (tid < 64) {
-    const int R = tid >> 4, jc = tid & 15, base = 16 * R;
+    // diagonal 16 x 16 blocks, thread = (block R, column jc), forward substitution
+    const int b0 = 16 * (tid >> 4), jc = tid & 15;
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float acc = (i == jc) ? 1.f : 0.f;
+      float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc -= s.A[(base + i) * LDT + base + m] * x[m];
-      x[i] = (i < jc) ? 0.f : acc;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) Li[(base + i) * LDT + base + jc] = x[i];
-  }
-  for (int e = tid; e < 64 * 64; e += PRO_THREADS) {
-    const int r = e >> 6, cc = e & 63;
-    if ((cc >> 4) > (r >> 4)) Li[r * LDT + cc] = 0.f;
-  }
-  __syncthreads();
-  // off-diagonal blocks, block row by block row:
-  //   L^{-1}_{RI} = - L^{-1}_{RR} sum_{J=I}^{R-1} A_{RJ} L^{-1}_{JI}
-  // (R * 256 elements per block row; each thread takes up to three)
-  for (int R = 1; R < 4; ++R) {
-    const int i = (tid >> 4) & 15, jj = tid & 15;
-    float pv[3] = {0.f, 0.f, 0.f};
-    for (int I = 0; I < R; ++I)
-      for (int J = I; J < R; ++J)
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          pv[I] += s.A[(16 * R + i) * LDT + 16 * J + m] * Li[(16 * J + m) * LDT + 16 * I + jj];
-    __syncthreads();
-    for (int I = 0; I < R; ++I) Li[(16 * R + i) * LDT + 16 * I + jj] = pv[I];  // partial sums in place
-    __syncthreads();
-    float lv[3] = {0.f, 0.f, 0.f};
-    for (int I = 0; I < R; ++I)
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        lv[I] -= Li[(16 * R + i) * LDT + 16 * R + m] * Li[(16 * R + m) * LDT + 16 * I + jj];
-    __syncthreads();
-    for (int I = 0; I < R; ++I) Li[(16 * R + i) * LDT + 16 * I + jj] = lv[I];
-    __syncthreads();
-  }
-  // T = L^{-1} diag(beta): T into A (fp32), A3 rows 0..63, TT rows 0..63
-  if (tid < 64) {
-    const int r = tid;
-    uint32_t tv[32];
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      const float t0 = Li[r * LDT + i] * s.beta[i];
-      const float t1 = Li[r * LDT + i + 1] * s.beta[i + 1];
-      s.A[r * LDT + i] = t0;
-      s.A[r * LDT + i + 1] = t1;
-      tv[i >> 1] = pack_half2(t0, t1);
-    }
-#pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8) {
-      const uint4 v4 = make_uint4(tv[4 * g8], tv[4 * g8 + 1], tv[4 * g8 + 2], tv[4 * g8 + 3]);
-      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g8, 128)) = v4;
-      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g8, 128)) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(r, 8 * g8, 128)) = v4;
-    }
-  } else if (tid >= 128 && tid < 192) {
-    const int r = tid - 128;  // A3 rows 64..127, K 64..127: the identity
-#pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8) {
-      uint32_t w4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k0 = 8 * g8 + 2 * u;
-        w4[u] = pack_half2(k0 == r ? 1.f : 0.f, k0 + 1 == r ? 1.f : 0.f);
+      for (int m = 0; m + 1 < i; m += 2) {
+        s0 -= Af[(b0 + i) * LDT + b0 + m] * x[m];
+        s1 -= Af[(b0 + i) * LDT + b0 + m + 1] * x[m + 1];
       }
-      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g8, 128)) =
-          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      if (i & 1) s0 -= Af[(b0 + i) * LDT + b0 + i - 1] * x[i - 1];
+      x[i] = (i < jc) ? 0.f : s0 + s1;
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Li[(b0 + i) * LDT + b0 + jc] = x[i];
   }
   __syncthreads();
-  if (tid < 64) {
-    const int jcol = tid;  // B2 [j][i] = T[i][j]
-    uint32_t tv[32];
+  {
+    // 16-row pairs (a, b) = (2P, 2P + 1): W = A_ba L^{-1}_aa
+    const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
+    const int a0 = 32 * P, b0 = 32 * P + 16;
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; i += 2) tv[i >> 1] = pack_half2(s.A[i * LDT + jcol], s.A[(i + 1) * LDT + jcol]);
+    for (int m = 0; m < 16; m += 2) {
+      s0 += Af[(b0 + i) * LDT + a0 + m] * Li[(a0 + m) * LDT + a0 + jc];
+      s1 += Af[(b0 + i) * LDT + a0 + m + 1] * Li[(a0 + m + 1) * LDT + a0 + jc];
+    }
+    Wt[(16 * P + i) * LDW + jc] = s0 + s1;
+  }
+  __syncthreads();
+  {
+    // L^{-1}_ba = - L^{-1}_bb W
+    const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
+    const int a0 = 32 * P, b0 = 32 * P + 16;
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8)
-      *reinterpret_cast<uint4*>(B2 + tc::kmajor_offset(jcol, 8 * g8, 64)) =
-          make_uint4(tv[4 * g8], tv[4 * g8 + 1], tv[4 * g8 + 2], tv[4 * g8 + 3]);
+    for (int m = 0; m < 16; m += 2) {
+      s0 += Li[(b0 + i) * LDT + b0 + m] * Wt[(16 * P + m) * LDW + jc];
+      s1 += Li[(b0 + i) * LDT + b0 + m + 1] * Wt[(16 * P + m + 1) * LDW + jc];
+    }
+    Li[(b0 + i) * LDT + a0 + jc] = -(s0 + s1);
+  }
+  __syncthreads();
+  {
+    // 32-row halves: W = A_{[32,64) [0,32)} L^{-1}_{[0,32) [0,32)}
+    const int i = tid >> 4, jc = tid & 15;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+      const float a = Af[(32 + i) * LDT + m];
+      s0 += a * Li[m * LDT + jc];
+      s1 += a * Li[m * LDT + 16 + jc];
+    }
+    Wt[i * LDW + jc] = s0;
+    Wt[i * LDW + 16 + jc] = s1;
+  }
+  __syncthreads();
+  {
+    const int i = tid >> 4, jc = tid & 15;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+      const float l = Li[(32 + i) * LDT + 32 + m];
+      s0 += l * Wt[m * LDW + jc];
+      s1 += l * Wt[m * LDW + 16 + jc];
+    }
+    Li[(32 + i) * LDT + jc] = -s0;
+    Li[(32 + i) * LDT + 16 + jc] = -s1;
+  }
+  __syncthreads();
+
+  // ---- phase 4: T = L^{-1} diag(beta) into A3 / TT / B2, A3's zero and
+  // identity blocks; thread = (row r, K group g of 8)
+  {
+    const int r = tid & 63, g = tid >> 6;
+    const float br = s.beta[r];
+    uint32_t tv[4], bv[4], iv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i0 = 8 * g + 2 * u;
+      tv[u] = pack_half2(Li[r * LDT + i0] * s.beta[i0], Li[r * LDT + i0 + 1] * s.beta[i0 + 1]);
+      bv[u] = pack_half2(Li[i0 * LDT + r] * br, Li[(i0 + 1) * LDT + r] * br);
+      iv[u] = pack_half2(i0 == r ? 1.f : 0.f, i0 + 1 == r ? 1.f : 0.f);
+    }
+    const uint4 t4 = make_uint4(tv[0], tv[1], tv[2], tv[3]);
+    *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g, 128)) = t4;
+    *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(r, 8 * g, 128)) = t4;
+    *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g, 128)) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g, 128)) =
+        make_uint4(iv[0], iv[1], iv[2], iv[3]);
+    *reinterpret_cast<uint4*>(B2 + tc::kmajor_offset(r, 8 * g, 64)) = make_uint4(bv[0], bv[1], bv[2], bv[3]);
   }
   fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
 
-  // ---- phase 4: A_qk T (fp16 MMA) -> A3 rows 64.. (negated), TT rows 64.. ----
+  // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated), TT rows 64.. ----
   if (tid == 0) {
     tc::fence_after_sync();
-    tc::mma_kloop(tmem + 64, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
+    tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
     tc::mma_commit(&s.bar);
   }
   wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
   bar_phase ^= 1u;
   tc::fence_after_sync();
-  if (warp < 2) {
-    const int r = 32 * warp + lane;
-    float a[32];
+  if ((warp & 3) < 2) {
+    const int r = 32 * (warp & 3) + lane, cg = warp >> 2;
+    float a[16];
+    tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 16 * cg), a);
+    uint32_t pos[8], neg[8];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 64 + 32 * half), a);
-      uint32_t pos[16], neg[16];
+    for (int t = 0; t < 16; t += 2) {
+      pos[t >> 1] = pack_half2(a[t], a[t + 1]);
+      neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
+    }
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        pos[i >> 1] = pack_half2(a[i], a[i + 1]);
-        neg[i >> 1] = pack_half2(-a[i], -a[i + 1]);
-      }
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const int k0 = 32 * half + 8 * g8;
-        *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, k0, 128)) =
-            make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
-        *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(64 + r, k0, 128)) =
-            make_uint4(pos[4 * g8], pos[4 * g8 + 1], pos[4 * g8 + 2], pos[4 * g8 + 3]);
-      }
+    for (int g8 = 0; g8 < 2; ++g8) {
+      const int k0 = 16 * cg + 8 * g8;
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, k0, 128)) =
+          make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
+      *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(64 + r, k0, 128)) =
+          make_uint4(pos[4 * g8], pos[4 * g8 + 1], pos[4 * g8 + 2], pos[4 * g8 + 3]);
     }
   }
   fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
 
-  // ---- phase 5: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA) -> WQ -------------------
+  // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA) -> WQ -------------------
   if (tid == 0) {
     tc::fence_after_sync();
-    tc::mma_kloop(tmem + 128, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
+    tc::mma_kloop(tmem, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
     tc::mma_commit(&s.bar);
   }
   wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
   bar_phase ^= 1u;
   tc::fence_after_sync();
-  if (warp < 4) {
-    const int row = 32 * warp + lane;
+  {
+    const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
     float a[32];
+    tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 32 * cq), a);
+    uint32_t hv[16];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 128 + 32 * q4), a);
-      uint32_t hv[16];
+    for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) hv[i >> 1] = pack_half2(a[i], a[i + 1]);
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(wsb + CH_WQ + tc::kmajor_offset(row, 32 * q4 + 8 * g8, 128)) =
-            make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
-    }
+    for (int g8 = 0; g8 < 4; ++g8)
+      *reinterpret_cast<uint4*>(wsb + CH_WQ + tc::kmajor_offset(row, 32 * cq + 8 * g8, 128)) =
+          make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
   }
   tc::fence_before_sync();
   __syncthreads();
