@@ -75,7 +75,7 @@ typedef struct kda_activations {
   int32_t hqk, hv;      /* heads; hv % hqk == 0                                  */
   int32_t use_qk_l2norm;/* must be 1: the in-kernel L2 norm of q and k          */
   float scale;          /* q scale applied after the norm (128^-0.5 usual)       */
-  float lower_bound;    /* gate lower bound in [-11, 0] (-5 usual); unused
+  float lower_bound;    /* gate lower bound in [-10.5, 0] (-5 usual); unused
                            without A_log                                        */
 } kda_activations;
 
@@ -123,7 +123,8 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
  * cu_seqlens must start at 0, be non-decreasing and end at T; a violation
  * found on the device sets KDA_ERR_DEVICE_INDEX.  The gate's 16-token
  * sub-chunk factorisation needs any 8 consecutive per-token log decays to
- * sum above -88 (always true for lower_bound >= -11, which is enforced).
+ * sum above -87, inside fp32's exponent range (always true for
+ * lower_bound >= -10.5, which is enforced).
  */
 int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens,
                   int32_t n_seqs, const float* initial_state, float* final_state,

@@ -71,9 +71,9 @@ int check_activations(const kda_activations* x, bool need_rows_aligned) {
   if (x->use_qk_l2norm != 1)
     return fail(KDA_ERR_INVALID_ARGUMENT,
                 "use_qk_l2norm must be 1: only the in-kernel q/k L2 norm is built.");
-  if (x->A_log && !(x->lower_bound <= 0.f && x->lower_bound >= -11.f))
+  if (x->A_log && !(x->lower_bound <= 0.f && x->lower_bound >= -10.5f))
     return fail(KDA_ERR_INVALID_ARGUMENT,
-                "lower_bound must lie in [-11, 0] (got %g).", (double)x->lower_bound);
+                "lower_bound must lie in [-10.5, 0] (got %g).", (double)x->lower_bound);
   if (x->t_total > 0) {
     if (!x->q || !x->k || !x->v || !x->g || !x->beta)
       return fail(KDA_ERR_INVALID_ARGUMENT, "q, k, v, g and beta must not be NULL.");

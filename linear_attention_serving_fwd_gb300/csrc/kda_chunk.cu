@@ -31,10 +31,10 @@
 // The exponent differences of A_kk / A_qk are factored around m_R = Lam at
 // the middle row 16 R + 7 of the row's own 16-row sub-chunk R:
 //   e^{Lam_r - Lam_i} = (e^{Lam_r - m_R}) (e^{m_R - Lam_i})      (i <= 16 R + 15)
-// The first factor stays within e^{+-88} as long as any 8 consecutive gates
-// sum above -88 (lower_bound >= -11); the second is at most e^{88} and below 1
-// for every i before the middle row.  Kg, qg, kg are exponentiated directly
-// (e^{Lam_i}, e^{Lam_C - Lam_i} <= 1), so no factor of theirs can overflow.
+// The first factor stays within e^{+-84} as long as any 8 consecutive gates
+// sum above -84 (lower_bound >= -10.5); the second is at most e^{84} and
+// below 1 for every i before the middle row.  Kg, qg and kg are products of
+// factors chained so that every partial product is at most |k^| or |q~|.
 #include "kda_params.cuh"
 #include "kda_tc.cuh"
 
@@ -122,9 +122,10 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 // consecutive channels of one row fill without bank conflicts):
 //   X   = [k^ e^{Lam - m} ; q~ e^{Lam - m}]          128 rows (m = m_R of the row)
 //   Y_R = k^_i e^{m_R - Lam_i},  i = 0 .. 16R + 15   16 (R + 1) rows
-// One batch of four kind::tf32 MMAs D_R = X Y_R^T then holds, in the rows of
-// sub-chunk R, A_kk (rows 0..63) and A_qk (rows 64..127) against every
-// column of sub-chunks 0..R.
+// The four Y_R are stacked into one 160-row operand (Y_R from row 8R(R+1)),
+// so one kind::tf32 product D = X Y^T (N = 160) holds, in the rows of
+// sub-chunk R and columns 8R(R+1).., A_kk (rows 0..63) and A_qk (rows
+// 64..127) against every column of sub-chunks 0..R.
 //
 // The inverse of L = I + A_kk (unit lower triangular) is built by recursive
 // doubling: the four diagonal 16 x 16 blocks by forward substitution, then
@@ -132,11 +133,11 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 // for the two 16-row pairs and then for the two 32-row halves.
 // --------------------------------------------------------------------------
 constexpr int PRO_THREADS = 512;
-constexpr int LDT = 65;  // row stride (floats) of the 64 x 64 fp32 matrices
+constexpr int LDT = 68;  // row stride (floats) of the 64 x 64 fp32 matrices (16-byte rows)
 constexpr int LDW = 33;  // row stride of the 32 x 32 fp32 temporary
+constexpr int YROWS = 160;  // rows of the stacked Y operand
 
-// byte offset of Y_R inside the Y region and its first TMEM column
-__host__ __device__ constexpr uint32_t y_off(int R) { return 8192u * (uint32_t)(R * (R + 1) / 2); }
+// first row of Y_R in the stacked operand = its first TMEM accumulator column
 __host__ __device__ constexpr uint32_t d_col(int R) { return 8u * (uint32_t)(R * (R + 1)); }
 
 // After the A_kk / A_qk MMAs the X / Y region holds (byte offsets):
@@ -144,15 +145,15 @@ constexpr uint32_t P_A3 = 0;        // fp16 [128][128] = [[T, 0], [-A_qk T, I]]
 constexpr uint32_t P_A2 = 32768;    // fp16 [128][64]  = [A_qk ; 0]
 constexpr uint32_t P_B2 = 49152;    // fp16 [64][64]   = T^T
 constexpr uint32_t P_A = 57344;     // fp32 [64][LDT]  = beta-scaled strictly lower A_kk
-constexpr uint32_t P_LI = 74240;    // fp32 [64][LDT]  = L^{-1}
-constexpr uint32_t P_W = 90880;     // fp32 [32][LDW]  temporary product
+constexpr uint32_t P_LI = 74752;    // fp32 [64][LDT]  = L^{-1}
+constexpr uint32_t P_W = 92160;     // fp32 [32][LDW]  temporary product
 static_assert(P_A + 64 * LDT * 4 <= P_LI && P_LI + 64 * LDT * 4 <= P_W, "prologue carve");
 
 struct __align__(1024) ProSmem {
   // q, k, g, v tiles (bf16 [4][64][128]) on entry, then X (tf32, 128 x 128);
   // with Y the carve P_* above once the MMAs have read them
   unsigned char X[65536];
-  unsigned char Y[81920];   // Y_0 .. Y_3 at y_off(R)
+  unsigned char Y[81920];   // Y_0 .. Y_3 stacked, tf32 [YROWS][128]
   unsigned char B3[32768];  // fp16 [c][K]: K 0..63 = Kg rows, 64..127 = qg rows
   float ref[4][128];        // m_R = Lam at row 16R + 7
   float qtot[4][128];       // gate sum of each sub-chunk
@@ -263,10 +264,11 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     }
   }
   __syncthreads();
-  float mR;
+  float mR, sR;  // Lam at rows 16 Rq + 7 and 16 Rq - 1 (0 before the chunk)
   {
     float off = 0.f;
     for (int R2 = 0; R2 < Rq; ++R2) off += s.qtot[R2][c];
+    sR = off;
 #pragma unroll
     for (int i = 0; i < 16; ++i) lam[i] += off;
     mR = lam[7];
@@ -288,6 +290,11 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     float F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
 #pragma unroll
     for (int R2 = 0; R2 < 4; ++R2) F[R2] = R2 > Rq ? __expf(s.ref[R2][c] - mR) : 1.f;
+    // Kg = ((k^ E) e^{m - sR}) e^{sR} = k^ e^{Lam}; kg = ((k^ / E) e^{eR - m}) e^{Lam_C - eR}
+    // with eR = Lam at row 16 Rq + 15: each partial product is at most |k^|,
+    // so none overflows and one underflows only where the result is below e^{-87}
+    const float Pm = __expf(mR - sR), Qs = __expf(sR);
+    const float He = __expf(lam[15] - mR), Jc = __expf(lamC - lam[15]);
     uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
@@ -296,19 +303,18 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
       for (int u = 0; u < 2; ++u) {
         const int ii = i + u, r = 16 * Rq + ii;
         const float kh = kv[ii] * s.rk[r], qh = qv[ii] * s.rq[r];
-        const float E = __expf(lam[ii] - mR);  // within e^{+-88}
+        const float E = __expf(lam[ii] - mR);  // within e^{+-84}
         const float iE = E > 0.f ? __fdividef(1.f, E) : 0.f;
-        const float eL = __expf(lam[ii]);
-        kgv[u] = kh * __expf(lamC - lam[ii]);
-        Kgv[u] = kh * eL;
-        qgv[u] = qh * eL;
-        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(kh * E);
-        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(qh * E);
-        const float y = kh * iE;
+        const float xk = kh * E, xq = qh * E, y = kh * iE;
+        kgv[u] = (y * He) * Jc;
+        Kgv[u] = (xk * Pm) * Qs;
+        qgv[u] = (xq * Pm) * Qs;
+        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk);
+        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq);
 #pragma unroll
         for (int R2 = 0; R2 < 4; ++R2)
           if (R2 >= Rq)
-            *reinterpret_cast<float*>(s.Y + y_off(R2) + tc::sw128_offset32(r, c, 16 * (R2 + 1))) =
+            *reinterpret_cast<float*>(s.Y + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
                 tc::to_tf32(y * F[R2]);
       }
       kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
@@ -333,12 +339,9 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
 
-  // ---- phase 2: A_kk / A_qk, four kind::tf32 MMAs, one commit ---------------
+  // ---- phase 2: A_kk / A_qk, one kind::tf32 product (N = 160) --------------
   if (tid == 0) {
-#pragma unroll
-    for (int R = 0; R < 4; ++R)
-      tc::mma_kloop_tf32_sw128(tmem + d_col(R), smem_u32(s.X), smem_u32(s.Y + y_off(R)), 128,
-                               16 * (R + 1), 128, false);
+    tc::mma_kloop_tf32_sw128(tmem, smem_u32(s.X), smem_u32(s.Y), 128, YROWS, 128, false);
     tc::mma_commit(&s.bar);
   }
   uint32_t bar_phase = 0;
@@ -365,11 +368,15 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     const bool hi = Rr != Rlo, live = cg <= Rr;
     if (sp < 2) {
       const float b = s.beta[r];
+      float av[16];
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
         const int col = 16 * cg + t;
-        Af[r * LDT + col] = (live && col < r) ? b * (hi ? a1[t] : a0[t]) : 0.f;
+        av[t] = (live && col < r) ? b * (hi ? a1[t] : a0[t]) : 0.f;
       }
+#pragma unroll
+      for (int t = 0; t < 16; t += 4)
+        *reinterpret_cast<float4*>(&Af[r * LDT + 16 * cg + t]) = make_float4(av[t], av[t + 1], av[t + 2], av[t + 3]);
     } else {
       uint32_t hv[8];
 #pragma unroll
@@ -441,31 +448,43 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     Li[(b0 + i) * LDT + a0 + jc] = -(s0 + s1);
   }
   __syncthreads();
+  // 32-row halves: warp = rows (2 warp, 2 warp + 1), lane = column; the
+  // column of the right factor sits in registers, the rows of the left one
+  // are read as 16-byte broadcasts
   {
-    // 32-row halves: W = A_{[32,64) [0,32)} L^{-1}_{[0,32) [0,32)}
-    const int i = tid >> 4, jc = tid & 15;
+    // W = A_{[32,64) [0,32)} L^{-1}_{[0,32) [0,32)}
+    float col[32];
+#pragma unroll
+    for (int m = 0; m < 32; ++m) col[m] = Li[m * LDT + lane];
+    const int i0 = 2 * warp;
     float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float a = Af[(32 + i) * LDT + m];
-      s0 += a * Li[m * LDT + jc];
-      s1 += a * Li[m * LDT + 16 + jc];
+#pragma unroll
+    for (int m = 0; m < 32; m += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(&Af[(32 + i0) * LDT + m]);
+      const float4 z = *reinterpret_cast<const float4*>(&Af[(33 + i0) * LDT + m]);
+      s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
+      s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
     }
-    Wt[i * LDW + jc] = s0;
-    Wt[i * LDW + 16 + jc] = s1;
+    Wt[i0 * LDW + lane] = s0;
+    Wt[(i0 + 1) * LDW + lane] = s1;
   }
   __syncthreads();
   {
-    const int i = tid >> 4, jc = tid & 15;
+    // L^{-1}_{[32,64) [0,32)} = - L^{-1}_{[32,64) [32,64)} W
+    float col[32];
+#pragma unroll
+    for (int m = 0; m < 32; ++m) col[m] = Wt[m * LDW + lane];
+    const int i0 = 2 * warp;
     float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float l = Li[(32 + i) * LDT + 32 + m];
-      s0 += l * Wt[m * LDW + jc];
-      s1 += l * Wt[m * LDW + 16 + jc];
+#pragma unroll
+    for (int m = 0; m < 32; m += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(&Li[(32 + i0) * LDT + 32 + m]);
+      const float4 z = *reinterpret_cast<const float4*>(&Li[(33 + i0) * LDT + 32 + m]);
+      s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
+      s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
     }
-    Li[(32 + i) * LDT + jc] = -s0;
-    Li[(32 + i) * LDT + 16 + jc] = -s1;
+    Li[(32 + i0) * LDT + lane] = -s0;
+    Li[(33 + i0) * LDT + lane] = -s1;
   }
   __syncthreads();
 
@@ -475,10 +494,13 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     const int r = tid & 63, g = tid >> 6;
     const float br = s.beta[r];
     uint32_t tv[4], bv[4], iv[4];
+    const float4 l0 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g]);
+    const float4 l1 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g + 4]);
+    const float lr[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i0 = 8 * g + 2 * u;
-      tv[u] = pack_half2(Li[r * LDT + i0] * s.beta[i0], Li[r * LDT + i0 + 1] * s.beta[i0 + 1]);
+      tv[u] = pack_half2(lr[2 * u] * s.beta[i0], lr[2 * u + 1] * s.beta[i0 + 1]);
       bv[u] = pack_half2(Li[i0 * LDT + r] * br, Li[(i0 + 1) * LDT + r] * br);
       iv[u] = pack_half2(i0 == r ? 1.f : 0.f, i0 + 1 == r ? 1.f : 0.f);
     }
