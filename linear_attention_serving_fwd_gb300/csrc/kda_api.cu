@@ -295,6 +295,7 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
   p.slot_stride = slot_stride; p.n_slots = n_slots;
   p.state_indices = state_indices; p.has_init = has_initial_state;
   p.groups = G;
+  p.sm_count = device_sm_count();
   p.err = err;
   if (kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream)) != 0)
     return cuda_fail(cudaGetLastError(), "kda_chunk_fwd launch");

@@ -114,7 +114,10 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 }
 
 // --------------------------------------------------------------------------
-// Prologue: one CTA (512 threads, 16 warps) per (chunk, head).
+// Prologue: persistent, one CTA (512 threads, 16 warps) per SM looping over
+// (chunk, head) items; while an item runs its inverse and last two products,
+// the next item's q, k, g, v rows stream into the part of the operand region
+// those steps leave free.
 //
 // Phase 1 is channel-owner: thread (c, R) holds channel c of the 16 rows of
 // sub-chunk R and writes every operand that needs the gate cumsum straight
@@ -141,19 +144,21 @@ constexpr int YROWS = 160;  // rows of the stacked Y operand
 __host__ __device__ constexpr uint32_t d_col(int R) { return 8u * (uint32_t)(R * (R + 1)); }
 
 // After the A_kk / A_qk MMAs the X / Y region holds (byte offsets):
-constexpr uint32_t P_A3 = 0;        // fp16 [128][128] = [[T, 0], [-A_qk T, I]]
-constexpr uint32_t P_A2 = 32768;    // fp16 [128][64]  = [A_qk ; 0]
-constexpr uint32_t P_B2 = 49152;    // fp16 [64][64]   = T^T
-constexpr uint32_t P_A = 57344;     // fp32 [64][LDT]  = beta-scaled strictly lower A_kk
-constexpr uint32_t P_LI = 74752;    // fp32 [64][LDT]  = L^{-1}
-constexpr uint32_t P_W = 92160;     // fp32 [32][LDW]  temporary product
-static_assert(P_A + 64 * LDT * 4 <= P_LI && P_LI + 64 * LDT * 4 <= P_W, "prologue carve");
+constexpr uint32_t P_LI = 0;         // fp32 [64][LDT]  = L^{-1}
+constexpr uint32_t P_A = 17408;      // fp32 [64][LDT]  = beta-scaled strictly lower A_kk
+constexpr uint32_t P_W = 34816;      // fp32 [32][LDW]  temporary product
+constexpr uint32_t P_A3 = 17408;     // fp16 [128][128] = [[T, 0], [-A_qk T, I]], over A and W
+constexpr uint32_t P_A2 = 50176;     // fp16 [128][64]  = [A_qk ; 0]
+constexpr uint32_t P_B2 = 66560;     // fp16 [64][64]   = T^T
+constexpr uint32_t P_TILES = 75776;  // bf16 [4][64][128]: q, k, g, v of the next item
+static_assert(P_LI + 64 * LDT * 4 <= P_A && P_A + 64 * LDT * 4 <= P_W, "prologue carve");
+static_assert(P_W + 32 * LDW * 4 <= P_A3 + 32768 && P_A3 + 32768 <= P_A2, "A3 covers A and W");
+static_assert(P_A2 + 16384 <= P_B2 && P_B2 + 8192 <= P_TILES, "prologue carve");
 
 struct __align__(1024) ProSmem {
-  // q, k, g, v tiles (bf16 [4][64][128]) on entry, then X (tf32, 128 x 128);
-  // with Y the carve P_* above once the MMAs have read them
-  unsigned char X[65536];
-  unsigned char Y[81920];   // Y_0 .. Y_3 stacked, tf32 [YROWS][128]
+  // X (tf32, 128 x 128) at XY, Y_0 .. Y_3 stacked (tf32 [YROWS][128]) at
+  // XY + 65536; the carve P_* above once the MMAs have read them
+  unsigned char XY[65536 + 81920];
   unsigned char B3[32768];  // fp16 [c][K]: K 0..63 = Kg rows, 64..127 = qg rows
   float ref[4][128];        // m_R = Lam at row 16R + 7
   float qtot[4][128];       // gate sum of each sub-chunk
@@ -162,24 +167,62 @@ struct __align__(1024) ProSmem {
   float lamc[128];          // Lam at row 63
   float rk[64], rq[64];     // 1/|k_r| and scale/|q_r|
   float beta[64];
+  int4 meta[2];             // (chunk, head, first token, rows) of this and the next item
   uint64_t bar;
   uint32_t tmem;
   int abort;
 };
-static_assert(P_W + 32 * LDW * 4 <= sizeof(ProSmem::X) + sizeof(ProSmem::Y), "carve fits");
+static_assert(P_TILES + 4 * 64 * D * 2 <= sizeof(ProSmem::XY), "carve fits");
+
+// item t = chunk * Hv + head
+__device__ __forceinline__ int4 item_meta(const ChunkParams& p, int t) {
+  const int c = t / p.hv, h = t - c * p.hv;
+  const int n = p.chunk_seq[c];
+  const int bos = seq_bos(p, n) + p.chunk_j[c] * CHUNK;
+  return make_int4(c, h, bos, min(CHUNK, seq_eos(p, n) - bos));
+}
+
+// One item's q, k, g, v rows (bf16, 64 x 128 each) into ``tiles`` with 16-byte
+// asynchronous copies; rows past the sequence end are zero-filled.
+__device__ __forceinline__ void load_tiles(const ChunkParams& p, int4 m, __nv_bfloat16* tiles, int tid) {
+  const int h = m.y, bos = m.z, len = m.w, hq = h / (p.hv / p.hqk);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int e = tid + u * PRO_THREADS;
+    const int chunk16 = e & 15, r = (e >> 4) & 63, which = e >> 10;
+    const int64_t tok = bos + (r < len ? r : 0);
+    const __nv_bfloat16* src;
+    if (which == 0) src = p.q + tok * p.q_st + hq * p.q_sh;
+    else if (which == 1) src = p.k + tok * p.k_st + hq * p.k_sh;
+    else if (which == 2) src = p.g + tok * p.g_st + h * p.g_sh;
+    else src = p.v + tok * p.v_st + h * p.v_sh;
+    cp_async16(tiles + (which * 64 + r) * D + 8 * chunk16, src + 8 * chunk16, r < len ? 16u : 0u);
+  }
+}
+
+// The item's raw per-row beta (threads 0..63), dt_bias of channel tid % 128
+// and A_log: loaded early, consumed at the item's start.
+struct ItemScalars {
+  __nv_bfloat16 beta;
+  float dt, alog;
+};
+__device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m, int tid) {
+  ItemScalars r;
+  const int h = m.y, bos = m.z, len = m.w;
+  r.beta = (tid < 64 && tid < len) ? p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh]
+                                   : __float2bfloat16(0.f);
+  r.dt = p.has_gate ? p.dt_bias[h * D + (tid & 127)] : 0.f;
+  r.alog = p.has_gate ? p.A_log[h] : 0.f;
+  return r;
+}
 
 __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   ProSmem& s = *reinterpret_cast<ProSmem*>(smem_raw);
-  const int c_glob = blockIdx.x, h = blockIdx.y;
-  if (c_glob >= *p.n_chunks) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = p.chunk_seq[c_glob], j = p.chunk_j[c_glob];
-  const int bos = seq_bos(p, n) + j * CHUNK;
-  const int len = min(CHUNK, seq_eos(p, n) - bos);
-  const int hq = h / (p.hv / p.hqk);
-  const float a_h = p.has_gate ? __expf(p.A_log[h]) : 0.f;
-  unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
+  const int n_items = *p.n_chunks * p.hv;
+  if ((int)blockIdx.x >= n_items) return;
+  __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.XY + P_TILES);
 
   if (warp == 0) {
     tc::tmem_alloc(&s.tmem, 256);
@@ -189,388 +232,393 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     mbar_init(&s.bar, 1);
     fence_mbar_init();
     s.abort = 0;
+    s.meta[0] = item_meta(p, blockIdx.x);
   }
-
-  // ---- phase 0: the chunk's q, k, g, v rows (bf16, 64 x 128 each) land in
-  // X with one batch of 16-byte asynchronous copies; rows past the sequence
-  // end are zero-filled
-  {
-    __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.X);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = tid + u * PRO_THREADS;
-      const int chunk16 = e & 15, r = (e >> 4) & 63, which = e >> 10;
-      const int64_t tok = bos + (r < len ? r : 0);
-      const __nv_bfloat16* src;
-      if (which == 0) src = p.q + tok * p.q_st + hq * p.q_sh;
-      else if (which == 1) src = p.k + tok * p.k_st + hq * p.k_sh;
-      else if (which == 2) src = p.g + tok * p.g_st + h * p.g_sh;
-      else src = p.v + tok * p.v_st + h * p.v_sh;
-      cp_async16(tiles + (which * 64 + r) * D + 8 * chunk16, src + 8 * chunk16, r < len ? 16u : 0u);
-    }
-    if (tid < 64)
-      s.beta[tid] = tid < len ? sigmoidf_(bf2f(p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh])) : 0.f;
-    cp_async_wait_all();
-  }
-  __syncthreads();
-
-  // ---- phase 1: channel-owner, thread = (channel c, sub-chunk Rq) ----------
-  const int c = tid & 127, Rq = tid >> 7;
-  float lam[16], kv[16], qv[16];
-  {
-    const __nv_bfloat16* tiles = reinterpret_cast<const __nv_bfloat16*>(s.X);
-    const float dt = p.has_gate ? p.dt_bias[h * D + c] : 0.f;
-    float acc = 0.f;
-    uint32_t vw[8];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int r = 16 * Rq + i;
-      qv[i] = bf2f(tiles[(0 * 64 + r) * D + c]);
-      kv[i] = bf2f(tiles[(1 * 64 + r) * D + c]);
-      float g = bf2f(tiles[(2 * 64 + r) * D + c]);
-      g = (p.has_gate && r < len) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
-      acc += g;
-      lam[i] = acc;
-      if (i & 1) vw[i >> 1] = pack_half2(bf2f(tiles[(3 * 64 + r - 1) * D + c]), bf2f(tiles[(3 * 64 + r) * D + c]));
-    }
-    // v^T block of this column (value block c / 32), K groups of 8 rows
-#pragma unroll
-    for (int g8 = 0; g8 < 2; ++g8)
-      *reinterpret_cast<uint4*>(wsb + CH_V16 + (c >> 5) * VB_BYTES +
-                                tc::kmajor_offset_lbo(c & 31, 16 * Rq + 8 * g8, VB_LBO)) =
-          make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
-    s.qtot[Rq][c] = acc;
-    // row norms: reduce-scatter the 16 per-row partials over the warp's 32
-    // channels (row = lane % 16), then the four channel groups meet in smem
-    float pk[16], pq[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) { pk[i] = kv[i] * kv[i]; pq[i] = qv[i] * qv[i]; }
-#pragma unroll
-    for (int sh = 8; sh >= 1; sh >>= 1) {
-      const bool up = (lane & sh) != 0;
-#pragma unroll
-      for (int m = 0; m < sh; ++m) {
-        const float sk = up ? pk[m] : pk[m + sh], kk = up ? pk[m + sh] : pk[m];
-        const float sq = up ? pq[m] : pq[m + sh], qq = up ? pq[m + sh] : pq[m];
-        pk[m] = kk + __shfl_xor_sync(0xffffffffu, sk, sh);
-        pq[m] = qq + __shfl_xor_sync(0xffffffffu, sq, sh);
-      }
-    }
-    pk[0] += __shfl_xor_sync(0xffffffffu, pk[0], 16);
-    pq[0] += __shfl_xor_sync(0xffffffffu, pq[0], 16);
-    if (lane < 16) {
-      s.ssk[c >> 5][16 * Rq + lane] = pk[0];
-      s.ssq[c >> 5][16 * Rq + lane] = pq[0];
-    }
-  }
-  __syncthreads();
-  float mR, sR;  // Lam at rows 16 Rq + 7 and 16 Rq - 1 (0 before the chunk)
-  {
-    float off = 0.f;
-    for (int R2 = 0; R2 < Rq; ++R2) off += s.qtot[R2][c];
-    sR = off;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) lam[i] += off;
-    mR = lam[7];
-    s.ref[Rq][c] = mR;
-    if (Rq == 3) {
-      s.lamc[c] = lam[15];
-      reinterpret_cast<float*>(wsb + CH_D)[c] = __expf(lam[15]);
-    }
-    if (tid < 64) {
-      const float sk = s.ssk[0][tid] + s.ssk[1][tid] + s.ssk[2][tid] + s.ssk[3][tid];
-      const float sq = s.ssq[0][tid] + s.ssq[1][tid] + s.ssq[2][tid] + s.ssq[3][tid];
-      s.rk[tid] = rsqrtf(sk + 1e-6f);
-      s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
-    }
-  }
-  __syncthreads();
-  {
-    const float lamC = s.lamc[c];
-    float F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
-#pragma unroll
-    for (int R2 = 0; R2 < 4; ++R2) F[R2] = R2 > Rq ? __expf(s.ref[R2][c] - mR) : 1.f;
-    // Kg = ((k^ E) e^{m - sR}) e^{sR} = k^ e^{Lam}; kg = ((k^ / E) e^{eR - m}) e^{Lam_C - eR}
-    // with eR = Lam at row 16 Rq + 15: each partial product is at most |k^|,
-    // so none overflows and one underflows only where the result is below e^{-87}
-    const float Pm = __expf(mR - sR), Qs = __expf(sR);
-    const float He = __expf(lam[15] - mR), Jc = __expf(lamC - lam[15]);
-    uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      float kgv[2], Kgv[2], qgv[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int ii = i + u, r = 16 * Rq + ii;
-        const float kh = kv[ii] * s.rk[r], qh = qv[ii] * s.rq[r];
-        const float E = __expf(lam[ii] - mR);  // within e^{+-84}
-        const float iE = E > 0.f ? __fdividef(1.f, E) : 0.f;
-        const float xk = kh * E, xq = qh * E, y = kh * iE;
-        kgv[u] = (y * He) * Jc;
-        Kgv[u] = (xk * Pm) * Qs;
-        qgv[u] = (xq * Pm) * Qs;
-        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk);
-        *reinterpret_cast<float*>(s.X + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq);
-#pragma unroll
-        for (int R2 = 0; R2 < 4; ++R2)
-          if (R2 >= Rq)
-            *reinterpret_cast<float*>(s.Y + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
-                tc::to_tf32(y * F[R2]);
-      }
-      kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
-      Kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
-      qgx[i >> 1] = pack_half2(qgv[0], qgv[1]);
-    }
-    // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KGT [k = c][K = r]
-#pragma unroll
-    for (int g8 = 0; g8 < 2; ++g8) {
-      const int r0 = 16 * Rq + 8 * g8;
-      *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, r0, 128)) =
-          make_uint4(Kgx[4 * g8], Kgx[4 * g8 + 1], Kgx[4 * g8 + 2], Kgx[4 * g8 + 3]);
-      *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, 64 + r0, 128)) =
-          make_uint4(qgx[4 * g8], qgx[4 * g8 + 1], qgx[4 * g8 + 2], qgx[4 * g8 + 3]);
-      *reinterpret_cast<uint4*>(wsb + CH_KGT + tc::kmajor_offset(c, r0, 128)) =
-          make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
-    }
-  }
-  fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
-
-  // ---- phase 2: A_kk / A_qk, one kind::tf32 product (N = 160) --------------
-  if (tid == 0) {
-    tc::mma_kloop_tf32_sw128(tmem, smem_u32(s.X), smem_u32(s.Y), 128, YROWS, 128, false);
-    tc::mma_commit(&s.bar);
-  }
+  load_tiles(p, s.meta[0], tiles, tid);
+  ItemScalars sc = load_scalars(p, s.meta[0], tid);
   uint32_t bar_phase = 0;
-  wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-  bar_phase ^= 1u;
-  tc::fence_after_sync();
+  int cur = 0;
+  for (int t = blockIdx.x; t < n_items; t += gridDim.x, cur ^= 1) {
+    const int4 meta = s.meta[cur];
+    const int c_glob = meta.x, h = meta.y, len = meta.w;
+    const float a_h = p.has_gate ? __expf(sc.alog) : 0.f;
+    const float dt = sc.dt;
+    if (tid < 64) s.beta[tid] = tid < len ? sigmoidf_(bf2f(sc.beta)) : 0.f;
+    unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
+    // ---- phase 0: this item's tiles (issued during the previous item) -------
+    cp_async_wait_all();
+    __syncthreads();
 
-  float* Af = reinterpret_cast<float*>(s.X + P_A);
-  float* Li = reinterpret_cast<float*>(s.X + P_LI);
-  float* Wt = reinterpret_cast<float*>(s.X + P_W);
-  unsigned char* A2 = s.X + P_A2;
-  unsigned char* A3 = s.X + P_A3;
-  unsigned char* B2 = s.X + P_B2;
-  {
-    // warp = (TMEM sub-partition sp, 16-column group cg); rows 0..63 of the
-    // accumulators are A_kk, rows 64..127 A_qk
-    const int sp = warp & 3, cg = warp >> 2;
-    const int r = 32 * (sp & 1) + lane, Rr = r >> 4, Rlo = 2 * (sp & 1);
-    float a0[16], a1[16];
+    // ---- phase 1: channel-owner, thread = (channel c, sub-chunk Rq) ----------
+    const int c = tid & 127, Rq = tid >> 7;
+    float lam[16], kv[16], qv[16];
+    {
+      float acc = 0.f;
+      uint32_t vw[8];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
 #pragma unroll
-    for (int t = 0; t < 16; ++t) { a0[t] = 0.f; a1[t] = 0.f; }
-    if (cg <= Rlo) tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, d_col(Rlo) + 16 * cg), a0);
-    if (cg <= Rlo + 1) tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, d_col(Rlo + 1) + 16 * cg), a1);
-    const bool hi = Rr != Rlo, live = cg <= Rr;
-    if (sp < 2) {
-      const float b = s.beta[r];
-      float av[16];
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int col = 16 * cg + t;
-        av[t] = (live && col < r) ? b * (hi ? a1[t] : a0[t]) : 0.f;
+      for (int i = 0; i < 16; ++i) {
+        const int r = 16 * Rq + i;
+        qv[i] = bf2f(tiles[(0 * 64 + r) * D + c]);
+        kv[i] = bf2f(tiles[(1 * 64 + r) * D + c]);
+        float g = bf2f(tiles[(2 * 64 + r) * D + c]);
+        g = (p.has_gate && r < len) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
+        acc += g;
+        lam[i] = acc;
+        if (i & 1)
+          vw[i >> 1] = pack_half2(bf2f(tiles[(3 * 64 + r - 1) * D + c]), bf2f(tiles[(3 * 64 + r) * D + c]));
       }
-#pragma unroll
-      for (int t = 0; t < 16; t += 4)
-        *reinterpret_cast<float4*>(&Af[r * LDT + 16 * cg + t]) = make_float4(av[t], av[t + 1], av[t + 2], av[t + 3]);
-    } else {
-      uint32_t hv[8];
-#pragma unroll
-      for (int t = 0; t < 16; t += 2) {
-        const int col = 16 * cg + t;
-        const float x0 = (live && col <= r) ? (hi ? a1[t] : a0[t]) : 0.f;
-        const float x1 = (live && col + 1 <= r) ? (hi ? a1[t + 1] : a0[t + 1]) : 0.f;
-        hv[t >> 1] = pack_half2(x0, x1);
-      }
+      // v^T block of this column (value block c / 32), K groups of 8 rows
 #pragma unroll
       for (int g8 = 0; g8 < 2; ++g8)
-        *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, 16 * cg + 8 * g8, 128)) =
+        *reinterpret_cast<uint4*>(wsb + CH_V16 + (c >> 5) * VB_BYTES +
+                                  tc::kmajor_offset_lbo(c & 31, 16 * Rq + 8 * g8, VB_LBO)) =
+            make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
+      s.qtot[Rq][c] = acc;
+      // row norms: reduce-scatter the 16 per-row partials over the warp's 32
+      // channels (row = lane % 16), then the four channel groups meet in smem
+      float pk[16], pq[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { pk[i] = kv[i] * kv[i]; pq[i] = qv[i] * qv[i]; }
+#pragma unroll
+      for (int sh = 8; sh >= 1; sh >>= 1) {
+        const bool up = (lane & sh) != 0;
+#pragma unroll
+        for (int m = 0; m < sh; ++m) {
+          const float sk = up ? pk[m] : pk[m + sh], kk = up ? pk[m + sh] : pk[m];
+          const float sq = up ? pq[m] : pq[m + sh], qq = up ? pq[m + sh] : pq[m];
+          pk[m] = kk + __shfl_xor_sync(0xffffffffu, sk, sh);
+          pq[m] = qq + __shfl_xor_sync(0xffffffffu, sq, sh);
+        }
+      }
+      pk[0] += __shfl_xor_sync(0xffffffffu, pk[0], 16);
+      pq[0] += __shfl_xor_sync(0xffffffffu, pq[0], 16);
+      if (lane < 16) {
+        s.ssk[c >> 5][16 * Rq + lane] = pk[0];
+        s.ssq[c >> 5][16 * Rq + lane] = pq[0];
+      }
+    }
+    __syncthreads();
+    float mR, sR;  // Lam at rows 16 Rq + 7 and 16 Rq - 1 (0 before the chunk)
+    {
+      float off = 0.f;
+      for (int R2 = 0; R2 < Rq; ++R2) off += s.qtot[R2][c];
+      sR = off;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lam[i] += off;
+      mR = lam[7];
+      s.ref[Rq][c] = mR;
+      if (Rq == 3) {
+        s.lamc[c] = lam[15];
+        reinterpret_cast<float*>(wsb + CH_D)[c] = __expf(lam[15]);
+      }
+      if (tid < 64) {
+        const float sk = s.ssk[0][tid] + s.ssk[1][tid] + s.ssk[2][tid] + s.ssk[3][tid];
+        const float sq = s.ssq[0][tid] + s.ssq[1][tid] + s.ssq[2][tid] + s.ssq[3][tid];
+        s.rk[tid] = rsqrtf(sk + 1e-6f);
+        s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
+      }
+    }
+    __syncthreads();
+    {
+      const float lamC = s.lamc[c];
+      float F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
+#pragma unroll
+      for (int R2 = 0; R2 < 4; ++R2) F[R2] = R2 > Rq ? __expf(s.ref[R2][c] - mR) : 1.f;
+      // Kg = ((k^ E) e^{m - sR}) e^{sR} = k^ e^{Lam}; kg = ((k^ / E) e^{eR - m}) e^{Lam_C - eR}
+      // with eR = Lam at row 16 Rq + 15: each partial product is at most |k^|,
+      // so none overflows and one underflows only where the result is below e^{-87}
+      const float Pm = __expf(mR - sR), Qs = __expf(sR);
+      const float He = __expf(lam[15] - mR), Jc = __expf(lamC - lam[15]);
+      uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        float kgv[2], Kgv[2], qgv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int ii = i + u, r = 16 * Rq + ii;
+          const float kh = kv[ii] * s.rk[r], qh = qv[ii] * s.rq[r];
+          const float E = __expf(lam[ii] - mR);  // within e^{+-84}
+          const float iE = E > 0.f ? __fdividef(1.f, E) : 0.f;
+          const float xk = kh * E, xq = qh * E, y = kh * iE;
+          kgv[u] = (y * He) * Jc;
+          Kgv[u] = (xk * Pm) * Qs;
+          qgv[u] = (xq * Pm) * Qs;
+          *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk);
+          *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq);
+#pragma unroll
+          for (int R2 = 0; R2 < 4; ++R2)
+            if (R2 >= Rq)
+              *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
+                  tc::to_tf32(y * F[R2]);
+        }
+        kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
+        Kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
+        qgx[i >> 1] = pack_half2(qgv[0], qgv[1]);
+      }
+      // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KGT [k = c][K = r]
+#pragma unroll
+      for (int g8 = 0; g8 < 2; ++g8) {
+        const int r0 = 16 * Rq + 8 * g8;
+        *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, r0, 128)) =
+            make_uint4(Kgx[4 * g8], Kgx[4 * g8 + 1], Kgx[4 * g8 + 2], Kgx[4 * g8 + 3]);
+        *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, 64 + r0, 128)) =
+            make_uint4(qgx[4 * g8], qgx[4 * g8 + 1], qgx[4 * g8 + 2], qgx[4 * g8 + 3]);
+        *reinterpret_cast<uint4*>(wsb + CH_KGT + tc::kmajor_offset(c, r0, 128)) =
+            make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // ---- phase 2: A_kk / A_qk, one kind::tf32 product (N = 160) --------------
+    if (tid == 0) {
+      tc::mma_kloop_tf32_sw128(tmem, smem_u32(s.XY), smem_u32(s.XY + 65536), 128, YROWS, 128, false);
+      tc::mma_commit(&s.bar);
+    }
+    const bool has_next = t + (int)gridDim.x < n_items;
+    if (tid == 32 && has_next) s.meta[cur ^ 1] = item_meta(p, t + gridDim.x);
+    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+    bar_phase ^= 1u;
+    tc::fence_after_sync();
+
+    float* Af = reinterpret_cast<float*>(s.XY + P_A);
+    float* Li = reinterpret_cast<float*>(s.XY + P_LI);
+    float* Wt = reinterpret_cast<float*>(s.XY + P_W);
+    unsigned char* A2 = s.XY + P_A2;
+    unsigned char* A3 = s.XY + P_A3;
+    unsigned char* B2 = s.XY + P_B2;
+    {
+      // warp = (TMEM sub-partition sp, 16-column group cg); rows 0..63 of the
+      // accumulators are A_kk, rows 64..127 A_qk
+      const int sp = warp & 3, cg = warp >> 2;
+      const int r = 32 * (sp & 1) + lane, Rr = r >> 4, Rlo = 2 * (sp & 1);
+      float a0[16], a1[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) { a0[t] = 0.f; a1[t] = 0.f; }
+      if (cg <= Rlo) tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, d_col(Rlo) + 16 * cg), a0);
+      if (cg <= Rlo + 1) tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, d_col(Rlo + 1) + 16 * cg), a1);
+      const bool hi = Rr != Rlo, live = cg <= Rr;
+      if (sp < 2) {
+        const float b = s.beta[r];
+        float av[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const int col = 16 * cg + t;
+          av[t] = (live && col < r) ? b * (hi ? a1[t] : a0[t]) : 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; t += 4)
+          *reinterpret_cast<float4*>(&Af[r * LDT + 16 * cg + t]) =
+              make_float4(av[t], av[t + 1], av[t + 2], av[t + 3]);
+      } else {
+        uint32_t hv[8];
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+          const int col = 16 * cg + t;
+          const float x0 = (live && col <= r) ? (hi ? a1[t] : a0[t]) : 0.f;
+          const float x1 = (live && col + 1 <= r) ? (hi ? a1[t + 1] : a0[t + 1]) : 0.f;
+          hv[t >> 1] = pack_half2(x0, x1);
+        }
+#pragma unroll
+        for (int g8 = 0; g8 < 2; ++g8)
+          *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(r, 16 * cg + 8 * g8, 128)) =
+              make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+      }
+      // A2 rows 64..127 are zero; L^{-1} above its diagonal blocks is zero
+      *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(64 + (tid & 63), 8 * (tid >> 6), 128)) =
+          make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + u * PRO_THREADS, rr = e >> 6, cc = e & 63;
+        if ((cc >> 4) > (rr >> 4)) Li[rr * LDT + cc] = 0.f;
+      }
+    }
+    __syncthreads();
+
+    // the next item's rows stream in behind the carve
+    if (has_next) {
+      const int4 mn = s.meta[cur ^ 1];
+      load_tiles(p, mn, tiles, tid);
+      sc = load_scalars(p, mn, tid);
+    }
+
+    // ---- phase 3: L^{-1} by recursive doubling ---------------------------------
+    if (tid < 64) {
+      // diagonal 16 x 16 blocks, thread = (block R, column jc), forward substitution
+      const int b0 = 16 * (tid >> 4), jc = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+        for (int m = 0; m + 1 < i; m += 2) {
+          s0 -= Af[(b0 + i) * LDT + b0 + m] * x[m];
+          s1 -= Af[(b0 + i) * LDT + b0 + m + 1] * x[m + 1];
+        }
+        if (i & 1) s0 -= Af[(b0 + i) * LDT + b0 + i - 1] * x[i - 1];
+        x[i] = (i < jc) ? 0.f : s0 + s1;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) Li[(b0 + i) * LDT + b0 + jc] = x[i];
+    }
+    __syncthreads();
+    {
+      // 16-row pairs (a, b) = (2P, 2P + 1): W = A_ba L^{-1}_aa
+      const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
+      const int a0 = 32 * P, b0 = 32 * P + 16;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; m += 2) {
+        s0 += Af[(b0 + i) * LDT + a0 + m] * Li[(a0 + m) * LDT + a0 + jc];
+        s1 += Af[(b0 + i) * LDT + a0 + m + 1] * Li[(a0 + m + 1) * LDT + a0 + jc];
+      }
+      Wt[(16 * P + i) * LDW + jc] = s0 + s1;
+    }
+    __syncthreads();
+    {
+      // L^{-1}_ba = - L^{-1}_bb W
+      const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
+      const int a0 = 32 * P, b0 = 32 * P + 16;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; m += 2) {
+        s0 += Li[(b0 + i) * LDT + b0 + m] * Wt[(16 * P + m) * LDW + jc];
+        s1 += Li[(b0 + i) * LDT + b0 + m + 1] * Wt[(16 * P + m + 1) * LDW + jc];
+      }
+      Li[(b0 + i) * LDT + a0 + jc] = -(s0 + s1);
+    }
+    __syncthreads();
+    // 32-row halves: warp = rows (2 warp, 2 warp + 1), lane = column; the
+    // column of the right factor sits in registers, the rows of the left one
+    // are read as 16-byte broadcasts
+    {
+      // W = A_{[32,64) [0,32)} L^{-1}_{[0,32) [0,32)}
+      float col[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) col[m] = Li[m * LDT + lane];
+      const int i0 = 2 * warp;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; m += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(&Af[(32 + i0) * LDT + m]);
+        const float4 z = *reinterpret_cast<const float4*>(&Af[(33 + i0) * LDT + m]);
+        s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
+        s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
+      }
+      Wt[i0 * LDW + lane] = s0;
+      Wt[(i0 + 1) * LDW + lane] = s1;
+    }
+    __syncthreads();
+    {
+      // L^{-1}_{[32,64) [0,32)} = - L^{-1}_{[32,64) [32,64)} W
+      float col[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) col[m] = Wt[m * LDW + lane];
+      const int i0 = 2 * warp;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; m += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(&Li[(32 + i0) * LDT + 32 + m]);
+        const float4 z = *reinterpret_cast<const float4*>(&Li[(33 + i0) * LDT + 32 + m]);
+        s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
+        s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
+      }
+      Li[(32 + i0) * LDT + lane] = -s0;
+      Li[(33 + i0) * LDT + lane] = -s1;
+    }
+    __syncthreads();
+
+    // ---- phase 4: T = L^{-1} diag(beta) into A3 / TT / B2, A3's zero and
+    // identity blocks; thread = (row r, K group g of 8)
+    {
+      const int r = tid & 63, g = tid >> 6;
+      const float br = s.beta[r];
+      uint32_t tv[4], bv[4], iv[4];
+      const float4 l0 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g]);
+      const float4 l1 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g + 4]);
+      const float lr[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i0 = 8 * g + 2 * u;
+        tv[u] = pack_half2(lr[2 * u] * s.beta[i0], lr[2 * u + 1] * s.beta[i0 + 1]);
+        bv[u] = pack_half2(Li[i0 * LDT + r] * br, Li[(i0 + 1) * LDT + r] * br);
+        iv[u] = pack_half2(i0 == r ? 1.f : 0.f, i0 + 1 == r ? 1.f : 0.f);
+      }
+      const uint4 t4 = make_uint4(tv[0], tv[1], tv[2], tv[3]);
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g, 128)) = t4;
+      *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(r, 8 * g, 128)) = t4;
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g, 128)) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g, 128)) =
+          make_uint4(iv[0], iv[1], iv[2], iv[3]);
+      *reinterpret_cast<uint4*>(B2 + tc::kmajor_offset(r, 8 * g, 64)) =
+          make_uint4(bv[0], bv[1], bv[2], bv[3]);
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated), TT rows 64.. ----
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
+      tc::mma_commit(&s.bar);
+    }
+    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+    bar_phase ^= 1u;
+    tc::fence_after_sync();
+    if ((warp & 3) < 2) {
+      const int r = 32 * (warp & 3) + lane, cg = warp >> 2;
+      float a[16];
+      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 16 * cg), a);
+      uint32_t pos[8], neg[8];
+#pragma unroll
+      for (int t = 0; t < 16; t += 2) {
+        pos[t >> 1] = pack_half2(a[t], a[t + 1]);
+        neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < 2; ++g8) {
+        const int k0 = 16 * cg + 8 * g8;
+        *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, k0, 128)) =
+            make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
+        *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(64 + r, k0, 128)) =
+            make_uint4(pos[4 * g8], pos[4 * g8 + 1], pos[4 * g8 + 2], pos[4 * g8 + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA) -> WQ -------------------
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_kloop(tmem, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
+      tc::mma_commit(&s.bar);
+    }
+    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+    bar_phase ^= 1u;
+    tc::fence_after_sync();
+    {
+      const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
+      float a[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 32 * cq), a);
+      uint32_t hv[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8)
+        *reinterpret_cast<uint4*>(wsb + CH_WQ + tc::kmajor_offset(row, 32 * cq + 8 * g8, 128)) =
             make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
     }
-    // A2 rows 64..127 are zero; L^{-1} above its diagonal blocks is zero
-    *reinterpret_cast<uint4*>(A2 + tc::kmajor_offset(64 + (tid & 63), 8 * (tid >> 6), 128)) =
-        make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = tid + u * PRO_THREADS, rr = e >> 6, cc = e & 63;
-      if ((cc >> 4) > (rr >> 4)) Li[rr * LDT + cc] = 0.f;
-    }
-  }
-  __syncthreads();
-
-  // ---- phase 3: L^{-1} by recursive doubling ---------------------------------
-  if (tid < 64) {
-    // diagonal 16 x 16 blocks, thread = (block R, column jc), forward substitution
-    const int b0 = 16 * (tid >> 4), jc = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s0 = (i == jc) ? 1.f : 0.f, s1 = 0.f;
-#pragma unroll
-      for (int m = 0; m + 1 < i; m += 2) {
-        s0 -= Af[(b0 + i) * LDT + b0 + m] * x[m];
-        s1 -= Af[(b0 + i) * LDT + b0 + m + 1] * x[m + 1];
-      }
-      if (i & 1) s0 -= Af[(b0 + i) * LDT + b0 + i - 1] * x[i - 1];
-      x[i] = (i < jc) ? 0.f : s0 + s1;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) Li[(b0 + i) * LDT + b0 + jc] = x[i];
-  }
-  __syncthreads();
-  {
-    // 16-row pairs (a, b) = (2P, 2P + 1): W = A_ba L^{-1}_aa
-    const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
-    const int a0 = 32 * P, b0 = 32 * P + 16;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; m += 2) {
-      s0 += Af[(b0 + i) * LDT + a0 + m] * Li[(a0 + m) * LDT + a0 + jc];
-      s1 += Af[(b0 + i) * LDT + a0 + m + 1] * Li[(a0 + m + 1) * LDT + a0 + jc];
-    }
-    Wt[(16 * P + i) * LDW + jc] = s0 + s1;
-  }
-  __syncthreads();
-  {
-    // L^{-1}_ba = - L^{-1}_bb W
-    const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
-    const int a0 = 32 * P, b0 = 32 * P + 16;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; m += 2) {
-      s0 += Li[(b0 + i) * LDT + b0 + m] * Wt[(16 * P + m) * LDW + jc];
-      s1 += Li[(b0 + i) * LDT + b0 + m + 1] * Wt[(16 * P + m + 1) * LDW + jc];
-    }
-    Li[(b0 + i) * LDT + a0 + jc] = -(s0 + s1);
-  }
-  __syncthreads();
-  // 32-row halves: warp = rows (2 warp, 2 warp + 1), lane = column; the
-  // column of the right factor sits in registers, the rows of the left one
-  // are read as 16-byte broadcasts
-  {
-    // W = A_{[32,64) [0,32)} L^{-1}_{[0,32) [0,32)}
-    float col[32];
-#pragma unroll
-    for (int m = 0; m < 32; ++m) col[m] = Li[m * LDT + lane];
-    const int i0 = 2 * warp;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 32; m += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(&Af[(32 + i0) * LDT + m]);
-      const float4 z = *reinterpret_cast<const float4*>(&Af[(33 + i0) * LDT + m]);
-      s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
-      s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
-    }
-    Wt[i0 * LDW + lane] = s0;
-    Wt[(i0 + 1) * LDW + lane] = s1;
-  }
-  __syncthreads();
-  {
-    // L^{-1}_{[32,64) [0,32)} = - L^{-1}_{[32,64) [32,64)} W
-    float col[32];
-#pragma unroll
-    for (int m = 0; m < 32; ++m) col[m] = Wt[m * LDW + lane];
-    const int i0 = 2 * warp;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 32; m += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(&Li[(32 + i0) * LDT + 32 + m]);
-      const float4 z = *reinterpret_cast<const float4*>(&Li[(33 + i0) * LDT + 32 + m]);
-      s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
-      s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
-    }
-    Li[(32 + i0) * LDT + lane] = -s0;
-    Li[(33 + i0) * LDT + lane] = -s1;
-  }
-  __syncthreads();
-
-  // ---- phase 4: T = L^{-1} diag(beta) into A3 / TT / B2, A3's zero and
-  // identity blocks; thread = (row r, K group g of 8)
-  {
-    const int r = tid & 63, g = tid >> 6;
-    const float br = s.beta[r];
-    uint32_t tv[4], bv[4], iv[4];
-    const float4 l0 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g]);
-    const float4 l1 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g + 4]);
-    const float lr[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i0 = 8 * g + 2 * u;
-      tv[u] = pack_half2(lr[2 * u] * s.beta[i0], lr[2 * u + 1] * s.beta[i0 + 1]);
-      bv[u] = pack_half2(Li[i0 * LDT + r] * br, Li[(i0 + 1) * LDT + r] * br);
-      iv[u] = pack_half2(i0 == r ? 1.f : 0.f, i0 + 1 == r ? 1.f : 0.f);
-    }
-    const uint4 t4 = make_uint4(tv[0], tv[1], tv[2], tv[3]);
-    *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g, 128)) = t4;
-    *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(r, 8 * g, 128)) = t4;
-    *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g, 128)) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g, 128)) =
-        make_uint4(iv[0], iv[1], iv[2], iv[3]);
-    *reinterpret_cast<uint4*>(B2 + tc::kmajor_offset(r, 8 * g, 64)) = make_uint4(bv[0], bv[1], bv[2], bv[3]);
-  }
-  fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-
-  // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated), TT rows 64.. ----
-  if (tid == 0) {
-    tc::fence_after_sync();
-    tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
-    tc::mma_commit(&s.bar);
-  }
-  wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-  bar_phase ^= 1u;
-  tc::fence_after_sync();
-  if ((warp & 3) < 2) {
-    const int r = 32 * (warp & 3) + lane, cg = warp >> 2;
-    float a[16];
-    tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 16 * cg), a);
-    uint32_t pos[8], neg[8];
-#pragma unroll
-    for (int t = 0; t < 16; t += 2) {
-      pos[t >> 1] = pack_half2(a[t], a[t + 1]);
-      neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
-    }
-#pragma unroll
-    for (int g8 = 0; g8 < 2; ++g8) {
-      const int k0 = 16 * cg + 8 * g8;
-      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, k0, 128)) =
-          make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
-      *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(64 + r, k0, 128)) =
-          make_uint4(pos[4 * g8], pos[4 * g8 + 1], pos[4 * g8 + 2], pos[4 * g8 + 3]);
-    }
-  }
-  fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-
-  // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA) -> WQ -------------------
-  if (tid == 0) {
-    tc::fence_after_sync();
-    tc::mma_kloop(tmem, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
-    tc::mma_commit(&s.bar);
-  }
-  wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-  bar_phase ^= 1u;
-  tc::fence_after_sync();
-  {
-    const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
-    float a[32];
-    tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 32 * cq), a);
-    uint32_t hv[16];
-#pragma unroll
-    for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8)
-      *reinterpret_cast<uint4*>(wsb + CH_WQ + tc::kmajor_offset(row, 32 * cq + 8 * g8, 128)) =
-          make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
+    tc::fence_before_sync();
+    __syncthreads();
+  }  // items
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
@@ -906,7 +954,9 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
   trace_end(stream);
   trace_begin("kda_prologue", stream);
-  kda_prologue_kernel<<<dim3(max_chunks, p.hv), PRO_THREADS, sizeof(ProSmem), stream>>>(p);
+  const int items = max_chunks * p.hv;
+  const int sms = p.sm_count > 0 ? p.sm_count : 152;
+  kda_prologue_kernel<<<items < sms ? items : sms, PRO_THREADS, sizeof(ProSmem), stream>>>(p);
   trace_end(stream);
   if (p.groups > 1) {
     trace_begin("kda_walk_pass1", stream);

@@ -44,6 +44,7 @@ struct ChunkParams {
   const uint8_t* has_init;
   int max_chunks;
   int groups;
+  int sm_count;         // SMs of the device: the persistent prologue's grid
   // workspace carve
   int32_t* chunk_off;   // [N+1]
   int32_t* chunk_seq;   // [max_chunks]
