@@ -297,8 +297,9 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
   p.groups = G;
   p.sm_count = device_sm_count();
   p.err = err;
-  if (kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream)) != 0)
-    return cuda_fail(cudaGetLastError(), "kda_chunk_fwd launch");
+  const int lrc = kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream));
+  if (lrc == -2) return KDA_ERR_INVALID_ARGUMENT;  // message set by the launcher
+  if (lrc != 0) return cuda_fail(cudaGetLastError(), "kda_chunk_fwd launch");
   return ok();
 }
 

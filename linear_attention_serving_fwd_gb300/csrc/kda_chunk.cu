@@ -35,6 +35,9 @@
 // sum above -84 (lower_bound >= -10.5); the second is at most e^{84} and
 // below 1 for every i before the middle row.  Kg, qg and kg are products of
 // factors chained so that every partial product is at most |k^| or |q~|.
+#include <cuda.h>  // CUtensorMap (types only; the encoder comes via the runtime)
+#include <cudaTypedefs.h>
+
 #include "kda_params.cuh"
 #include "kda_tc.cuh"
 
@@ -169,6 +172,7 @@ struct __align__(1024) ProSmem {
   float beta[64];
   int4 meta[2];             // (chunk, head, first token, rows) of this and the next item
   uint64_t bar;
+  uint64_t tbar;            // tile loads
   uint32_t tmem;
   int abort;
 };
@@ -182,22 +186,33 @@ __device__ __forceinline__ int4 item_meta(const ChunkParams& p, int t) {
   return make_int4(c, h, bos, min(CHUNK, seq_eos(p, n) - bos));
 }
 
-// One item's q, k, g, v rows (bf16, 64 x 128 each) into ``tiles`` with 16-byte
-// asynchronous copies; rows past the sequence end are zero-filled.
-__device__ __forceinline__ void load_tiles(const ChunkParams& p, int4 m, __nv_bfloat16* tiles, int tid) {
-  const int h = m.y, bos = m.z, len = m.w, hq = h / (p.hv / p.hqk);
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int e = tid + u * PRO_THREADS;
-    const int chunk16 = e & 15, r = (e >> 4) & 63, which = e >> 10;
-    const int64_t tok = bos + (r < len ? r : 0);
-    const __nv_bfloat16* src;
-    if (which == 0) src = p.q + tok * p.q_st + hq * p.q_sh;
-    else if (which == 1) src = p.k + tok * p.k_st + hq * p.k_sh;
-    else if (which == 2) src = p.g + tok * p.g_st + h * p.g_sh;
-    else src = p.v + tok * p.v_st + h * p.v_sh;
-    cp_async16(tiles + (which * 64 + r) * D + 8 * chunk16, src + 8 * chunk16, r < len ? 16u : 0u);
-  }
+// Tensor maps of q, k (dims 128 x Hqk x T) and g, v (128 x Hv x T), bf16,
+// box 128 x 1 x 64: one tiled TMA load brings a (chunk, head) tile.
+struct TileMaps {
+  CUtensorMap q, k, g, v;
+};
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// One item's q, k, g, v rows (bf16, 64 x 128 each) into ``tiles`` with four
+// tiled TMA loads completing on ``bar`` (one thread).  Tokens past T arrive
+// as zeros; rows past the sequence end hold the next sequence's tokens and
+// readers mask them.
+__device__ __forceinline__ void load_tiles(const ChunkParams& p, const TileMaps& maps, int4 m,
+                                           __nv_bfloat16* tiles, uint64_t* bar) {
+  const int h = m.y, bos = m.z, hq = h / (p.hv / p.hqk);
+  mbar_arrive_expect_tx(bar, 4u * 64u * D * 2u);
+  tma_load_3d(tiles + 0 * 64 * D, &maps.q, 0, hq, bos, bar);
+  tma_load_3d(tiles + 1 * 64 * D, &maps.k, 0, hq, bos, bar);
+  tma_load_3d(tiles + 2 * 64 * D, &maps.g, 0, h, bos, bar);
+  tma_load_3d(tiles + 3 * 64 * D, &maps.v, 0, h, bos, bar);
 }
 
 // The item's raw per-row beta (threads 0..63), dt_bias of channel tid % 128
@@ -216,7 +231,8 @@ __device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m
   return r;
 }
 
-__global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(PRO_THREADS, 1)
+    kda_prologue_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   ProSmem& s = *reinterpret_cast<ProSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -230,17 +246,18 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
   }
   if (tid == 0) {
     mbar_init(&s.bar, 1);
+    mbar_init(&s.tbar, 1);
     fence_mbar_init();
     s.abort = 0;
     s.meta[0] = item_meta(p, blockIdx.x);
+    load_tiles(p, maps, s.meta[0], tiles, &s.tbar);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
-  load_tiles(p, s.meta[0], tiles, tid);
   ItemScalars sc = load_scalars(p, s.meta[0], tid);
-  uint32_t bar_phase = 0;
+  uint32_t bar_phase = 0, tile_phase = 0, tiles_issued = 1;
   int cur = 0;
   for (int t = blockIdx.x; t < n_items; t += gridDim.x, cur ^= 1) {
     const int4 meta = s.meta[cur];
@@ -250,7 +267,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     if (tid < 64) s.beta[tid] = tid < len ? sigmoidf_(bf2f(sc.beta)) : 0.f;
     unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
     // ---- phase 0: this item's tiles (issued during the previous item) -------
-    cp_async_wait_all();
+    wait_or_abort(&s.tbar, tile_phase, &s.abort, p.err);
+    tile_phase ^= 1u;
     __syncthreads();
 
     // ---- phase 1: channel-owner, thread = (channel c, sub-chunk Rq) ----------
@@ -262,14 +280,16 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = 16 * Rq + i;
-        qv[i] = bf2f(tiles[(0 * 64 + r) * D + c]);
-        kv[i] = bf2f(tiles[(1 * 64 + r) * D + c]);
-        float g = bf2f(tiles[(2 * 64 + r) * D + c]);
-        g = (p.has_gate && r < len) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
+        const bool in = r < len;  // later rows belong to the next sequence
+        qv[i] = in ? bf2f(tiles[(0 * 64 + r) * D + c]) : 0.f;
+        kv[i] = in ? bf2f(tiles[(1 * 64 + r) * D + c]) : 0.f;
+        float g = in ? bf2f(tiles[(2 * 64 + r) * D + c]) : 0.f;
+        g = (p.has_gate && in) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
         acc += g;
         lam[i] = acc;
         if (i & 1)
-          vw[i >> 1] = pack_half2(bf2f(tiles[(3 * 64 + r - 1) * D + c]), bf2f(tiles[(3 * 64 + r) * D + c]));
+          vw[i >> 1] = pack_half2(r - 1 < len ? bf2f(tiles[(3 * 64 + r - 1) * D + c]) : 0.f,
+                                  in ? bf2f(tiles[(3 * 64 + r) * D + c]) : 0.f);
       }
       // v^T block of this column (value block c / 32), K groups of 8 rows
 #pragma unroll
@@ -444,7 +464,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     // the next item's rows stream in behind the carve
     if (has_next) {
       const int4 mn = s.meta[cur ^ 1];
-      load_tiles(p, mn, tiles, tid);
+      if (tid == 96) load_tiles(p, maps, mn, tiles, &s.tbar);  // a warp idle in the diagonal solve
+      tiles_issued += 1;
       sc = load_scalars(p, mn, tid);
     }
 
@@ -619,6 +640,10 @@ __global__ void __launch_bounds__(PRO_THREADS, 1) kda_prologue_kernel(ChunkParam
     tc::fence_before_sync();
     __syncthreads();
   }  // items
+  // after an abort, leave no tile load in flight: wait (bounded) for the last
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0 && s.abort) mbar_wait_bounded(&s.tbar, (tiles_issued - 1) & 1, p.err);
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
@@ -922,6 +947,34 @@ size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* 
   return words;  // 4-byte words
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda)
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// rows of ``heads`` x 128 bf16 per token: dims (128, heads, T), box (128, 1, 64)
+static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, int64_t st_head,
+                        int64_t st_tok) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)st_head * 2, (cuuint64_t)st_tok * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)CHUNK};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   static bool attrs = false;
   if (!attrs) {
@@ -953,10 +1006,20 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   trace_begin("kda_chunk_index", stream);
   kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
   trace_end(stream);
+  TileMaps maps;
+  if (!encode_rows(&maps.q, p.q, p.hqk, p.t_total, p.q_sh, p.q_st) ||
+      !encode_rows(&maps.k, p.k, p.hqk, p.t_total, p.k_sh, p.k_st) ||
+      !encode_rows(&maps.g, p.g, p.hv, p.t_total, p.g_sh, p.g_st) ||
+      !encode_rows(&maps.v, p.v, p.hv, p.t_total, p.v_sh, p.v_st)) {
+    set_last_error(KDA_ERR_INVALID_ARGUMENT,
+                   "kda_chunk_fwd: q/k/v/g layout cannot be described by a TMA tensor map "
+                   "(strides must be positive multiples of 8 elements below 2^39 bytes).");
+    return -2;
+  }
   trace_begin("kda_prologue", stream);
   const int items = max_chunks * p.hv;
   const int sms = p.sm_count > 0 ? p.sm_count : 152;
-  kda_prologue_kernel<<<items < sms ? items : sms, PRO_THREADS, sizeof(ProSmem), stream>>>(p);
+  kda_prologue_kernel<<<items < sms ? items : sms, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
   trace_end(stream);
   if (p.groups > 1) {
     trace_begin("kda_walk_pass1", stream);
