@@ -11,16 +11,17 @@
 //   A_qk[r,i] = sum_c q~_rc k^_ic e^{Lam_rc - Lam_ic}          (i <= r)
 //   T  = (I + A_kk)^{-1} diag(beta)
 //   Kg = e^{Lam} * k^,  qg = e^{Lam} * q~,  kg = e^{Lam_C - Lam} * k^,  d = e^{Lam_C}
+// With w = T Kg and U = T v - w S the chunk step is
+//   o = qg S + A_qk U,   S' = diag(d) S + kg^T U,
+// which the walk evaluates in transition form, S kept in fp32:
+//   S' = d * S + P S + R v,      P = -kg^T w  (K x K),  R = kg^T T  (K x C)
+//   o  = qg' S + o_intra,        qg' = qg - A_qk w,  o_intra = A_qk T v
+// so that only the product P S (K = 128) lies on the chunk-to-chunk chain.
 // The prologue emits, per (chunk, head), the walk's tensor-core operands in
 // their shared-memory layout (fp16, K-major, no swizzle):
-//   WQ = [w ; qg']  with w = T Kg and qg' = qg - A_qk w        (128 x 128)
-//   KGT = kg^T                                                 (128 x 64)
-//   TT = [T ; A_qk T]                                          (128 x 64)
-//   d                                                          (fp32, 128)
-// and the walk, per 32 value columns of the K x V state S, computes
-//   [u ; o_intra] = TT v,   X = WQ S,   U = u - X_w,   o = X_qg' + o_intra,
-//   S <- diag(d) S + KGT U
-// which equals U = u - w S, o = qg S + A_qk U, S' = diag(d) S + kg^T U.
+//   P (128 x 128), R (128 x 64), d (fp32, 128), qg' (64 x 128),
+//   o_intra (bf16, four blocks of [64 r][32 v]) and v^T in four blocks of
+//   32 value columns.
 //
 // Precision: A_kk / A_qk use kind::tf32 (their operands carry exponent
 // factors up to e^{8 |gate|}, outside fp16 range); every other product uses
@@ -48,13 +49,16 @@ namespace kda {
 // 512) so that column-wise shared-memory stores avoid bank conflicts.
 constexpr uint32_t VB_LBO = 32 * 16 + 16;
 constexpr uint32_t VB_BYTES = VB_LBO * 64 / 8;      // fp16 v^T block [32 v][64 r]: 4224
-constexpr uint32_t CH_WQ = 0;                       // fp16 128 x 128
-constexpr uint32_t CH_KGT = CH_WQ + 128 * 128 * 2;  // fp16 128 x 64
-constexpr uint32_t CH_TT = CH_KGT + 128 * 64 * 2;   // fp16 128 x 64
-constexpr uint32_t CH_D = CH_TT + 128 * 64 * 2;     // fp32 128
-constexpr uint32_t CH_MAIN = CH_D + 128 * 4;        // 66048: what every value block reads
-constexpr uint32_t CH_V16 = CH_MAIN;                // 4 x fp16 v^T blocks, one per 32 columns
-constexpr uint32_t CH_BYTES = CH_V16 + 4 * VB_BYTES;  // 82944
+constexpr uint32_t CH_P = 0;                        // fp16 128 x 128, rows k, K = k'
+constexpr uint32_t CH_R = CH_P + 128 * 128 * 2;     // fp16 128 x 64,  rows k, K = r
+constexpr uint32_t CH_D = CH_R + 128 * 64 * 2;      // fp32 128
+constexpr uint32_t CH_QG = CH_D + 128 * 4;          // fp16 64 x 128,  rows r, K = k'
+constexpr uint32_t OI_BLOCK = 64 * 32 * 2;          // bf16 o_intra block [64 r][32 v]
+constexpr uint32_t CH_OI = CH_QG + 64 * 128 * 2;    // 4 o_intra blocks, one per 32 columns
+constexpr uint32_t CH_V16 = CH_OI + 4 * OI_BLOCK;   // 4 x fp16 v^T blocks, one per 32 columns
+constexpr uint32_t CH_BYTES = CH_V16 + 4 * VB_BYTES;  // 99328
+constexpr uint32_t CH_A_BYTES = CH_QG - CH_P;       // P, R, d: the chain's part (49664)
+constexpr uint32_t QG_BYTES = CH_OI - CH_QG;        // qg' (16384)
 
 __device__ __forceinline__ int seq_bos(const ChunkParams& p, int n) {
   return p.cu_seqlens ? p.cu_seqlens[n] : n * p.dense_len;
@@ -72,6 +76,7 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 // raised the abort flag.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t phase, volatile int* abort,
                                               unsigned* err) {
+  if (mbar_test_wait(bar, phase)) return true;  // already complete: no parking round trip
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < WAIT_CAP; ++i) {
     if (mbar_try_wait(bar, phase)) return true;
@@ -154,6 +159,8 @@ constexpr uint32_t P_A3 = 17408;     // fp16 [128][128] = [[T, 0], [-A_qk T, I]]
 constexpr uint32_t P_A2 = 50176;     // fp16 [128][64]  = [A_qk ; 0]
 constexpr uint32_t P_B2 = 66560;     // fp16 [64][64]   = T^T
 constexpr uint32_t P_TILES = 75776;  // bf16 [4][64][128]: q, k, g, v of the next item
+constexpr uint32_t P_WT = 0;         // fp16 w^T, MN-major [k'][r] (over L^{-1} once dead)
+constexpr uint32_t WT_LBO = 128, WT_SBO = 1024;  // its 8-row r groups / 8-column k' groups
 static_assert(P_LI + 64 * LDT * 4 <= P_A && P_A + 64 * LDT * 4 <= P_W, "prologue carve");
 static_assert(P_W + 32 * LDW * 4 <= P_A3 + 32768 && P_A3 + 32768 <= P_A2, "A3 covers A and W");
 static_assert(P_A2 + 16384 <= P_B2 && P_B2 + 8192 <= P_TILES, "prologue carve");
@@ -163,6 +170,8 @@ struct __align__(1024) ProSmem {
   // XY + 65536; the carve P_* above once the MMAs have read them
   unsigned char XY[65536 + 81920];
   unsigned char B3[32768];  // fp16 [c][K]: K 0..63 = Kg rows, 64..127 = qg rows
+  unsigned char KG[16384];  // fp16 kg^T, K-major [k][r]
+  unsigned char VT[16384];  // fp16 v^T, K-major [v][r] (K groups 2048 bytes apart)
   float ref[4][128];        // m_R = Lam at row 16R + 7
   float qtot[4][128];       // gate sum of each sub-chunk
   float ssk[4][64];         // |k_r|^2 partial per group of 32 channels
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.XY + P_TILES);
 
   if (warp == 0) {
-    tc::tmem_alloc(&s.tmem, 256);
+    tc::tmem_alloc(&s.tmem, 512);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -291,12 +300,14 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
           vw[i >> 1] = pack_half2(r - 1 < len ? bf2f(tiles[(3 * 64 + r - 1) * D + c]) : 0.f,
                                   in ? bf2f(tiles[(3 * 64 + r) * D + c]) : 0.f);
       }
-      // v^T block of this column (value block c / 32), K groups of 8 rows
+      // v^T of this column: the record's block c / 32, and VT for o_intra
 #pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8)
+      for (int g8 = 0; g8 < 2; ++g8) {
+        const uint4 v4 = make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
         *reinterpret_cast<uint4*>(wsb + CH_V16 + (c >> 5) * VB_BYTES +
-                                  tc::kmajor_offset_lbo(c & 31, 16 * Rq + 8 * g8, VB_LBO)) =
-            make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
+                                  tc::kmajor_offset_lbo(c & 31, 16 * Rq + 8 * g8, VB_LBO)) = v4;
+        *reinterpret_cast<uint4*>(s.VT + tc::kmajor_offset(c, 16 * Rq + 8 * g8, 128)) = v4;
+      }
       s.qtot[Rq][c] = acc;
       // row norms: reduce-scatter the 16 per-row partials over the warp's 32
       // channels (row = lane % 16), then the four channel groups meet in smem
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         Kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
         qgx[i >> 1] = pack_half2(qgv[0], qgv[1]);
       }
-      // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KGT [k = c][K = r]
+      // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KG [k = c][K = r]
 #pragma unroll
       for (int g8 = 0; g8 < 2; ++g8) {
         const int r0 = 16 * Rq + 8 * g8;
@@ -387,7 +398,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
             make_uint4(Kgx[4 * g8], Kgx[4 * g8 + 1], Kgx[4 * g8 + 2], Kgx[4 * g8 + 3]);
         *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, 64 + r0, 128)) =
             make_uint4(qgx[4 * g8], qgx[4 * g8 + 1], qgx[4 * g8 + 2], qgx[4 * g8 + 3]);
-        *reinterpret_cast<uint4*>(wsb + CH_KGT + tc::kmajor_offset(c, r0, 128)) =
+        *reinterpret_cast<uint4*>(s.KG + tc::kmajor_offset(c, r0, 128)) =
             make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
       }
     }
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     }
     __syncthreads();
 
-    // ---- phase 4: T = L^{-1} diag(beta) into A3 / TT / B2, A3's zero and
+    // ---- phase 4: T = L^{-1} diag(beta) into A3 and B2, A3's zero and
     // identity blocks; thread = (row r, K group g of 8)
     {
       const int r = tid & 63, g = tid >> 6;
@@ -573,7 +584,6 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
       const uint4 t4 = make_uint4(tv[0], tv[1], tv[2], tv[3]);
       *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g, 128)) = t4;
-      *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(r, 8 * g, 128)) = t4;
       *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g, 128)) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g, 128)) =
           make_uint4(iv[0], iv[1], iv[2], iv[3]);
@@ -584,7 +594,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated), TT rows 64.. ----
+    // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated) ----------------
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
@@ -597,26 +607,20 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       const int r = 32 * (warp & 3) + lane, cg = warp >> 2;
       float a[16];
       tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 16 * cg), a);
-      uint32_t pos[8], neg[8];
+      uint32_t neg[8];
 #pragma unroll
-      for (int t = 0; t < 16; t += 2) {
-        pos[t >> 1] = pack_half2(a[t], a[t + 1]);
-        neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
-      }
+      for (int t = 0; t < 16; t += 2) neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
 #pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8) {
-        const int k0 = 16 * cg + 8 * g8;
-        *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, k0, 128)) =
+      for (int g8 = 0; g8 < 2; ++g8)
+        *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 16 * cg + 8 * g8, 128)) =
             make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
-        *reinterpret_cast<uint4*>(wsb + CH_TT + tc::kmajor_offset(64 + r, k0, 128)) =
-            make_uint4(pos[4 * g8], pos[4 * g8 + 1], pos[4 * g8 + 2], pos[4 * g8 + 3]);
-      }
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA) -> WQ -------------------
+    // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA): w^T to shared memory
+    // (MN-major B operand of P), qg' to the record
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop(tmem, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
@@ -625,6 +629,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
     tc::fence_after_sync();
+    unsigned char* WT = s.XY + P_WT;
     {
       const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
       float a[32];
@@ -633,9 +638,67 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
 #pragma unroll
       for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
 #pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const uint4 h4 = make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+        const int k0 = 32 * cq + 8 * g8;
+        if (row < 64)  // w^T [n = k'][K = r]: 8 consecutive k' of row r
+          *reinterpret_cast<uint4*>(WT + tc::mnmajor_offset(k0, row, WT_LBO, WT_SBO)) = h4;
+        else
+          *reinterpret_cast<uint4*>(wsb + CH_QG + tc::kmajor_offset(row - 64, k0, 64)) = h4;
+      }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- phase 7: P = -kg^T w, R = kg^T T (A = kg^T) and -o_intra =
+    // (-A_qk T) v (A = A3's rows 64.., M = 64: row r at lane r % 16 + 32 (r / 16))
+    if (tid == 0) {
+      tc::fence_after_sync();
+      tc::mma_kloop_bmn(tmem, smem_u32(s.KG), smem_u32(WT), 128, 128, 64, WT_LBO, WT_SBO, false);
+      tc::mma_kloop(tmem + 128, smem_u32(s.KG), smem_u32(B2), 128, 64, 64, 0, false);
+      tc::mma_run<4>(tmem + 256, tc::smem_desc(smem_u32(A3) + 1024, 2048, 128),
+                     tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096, tc::idesc_f16(64, 128, 0), false);
+      tc::mma_commit(&s.bar);
+    }
+    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+    bar_phase ^= 1u;
+    tc::fence_after_sync();
+    {
+      const int k = 32 * (warp & 3) + lane, cq = warp >> 2;
+      float a[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 32 * cq), a);
+      uint32_t hv[16];
+#pragma unroll
+      for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(-a[t], -a[t + 1]);
+#pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(wsb + CH_WQ + tc::kmajor_offset(row, 32 * cq + 8 * g8, 128)) =
+        *reinterpret_cast<uint4*>(wsb + CH_P + tc::kmajor_offset(k, 32 * cq + 8 * g8, 128)) =
             make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+      float b[16];
+      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 128 + 16 * cq), b);
+      uint32_t rv[8];
+#pragma unroll
+      for (int t = 0; t < 16; t += 2) rv[t >> 1] = pack_half2(b[t], b[t + 1]);
+#pragma unroll
+      for (int g8 = 0; g8 < 2; ++g8)
+        *reinterpret_cast<uint4*>(wsb + CH_R + tc::kmajor_offset(k, 16 * cq + 8 * g8, 128)) =
+            make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
+      // o_intra, value block cq: lanes 0..15 of the warp hold rows 16 (warp & 3) + lane
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 256 + 32 * cq), a);
+      if (lane < 16) {
+        const int r = 16 * (warp & 3) + lane;
+        uint32_t ov[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(-a[t], -a[t + 1]);
+          ov[t >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(wsb + CH_OI + cq * OI_BLOCK + r * 64 + 16 * g8) =
+              make_uint4(ov[4 * g8], ov[4 * g8 + 1], ov[4 * g8 + 2], ov[4 * g8 + 3]);
+      }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -644,34 +707,41 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (tid == 0 && s.abort) mbar_wait_bounded(&s.tbar, (tiles_issued - 1) & 1, p.err);
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // --------------------------------------------------------------------------
-// Inter-chunk walk on tcgen05.  One CTA (5 warps) per (column block of 32,
-// head, sequence x group): warps 0-3 own TMEM lanes (state row k = tid and
-// chunk row r) and their thread 0 issues the MMAs after a named barrier of
-// the four warps; warp 4 streams the chunk records in.
-// mode 0: outputs (+ final state when groups == 1); mode 1: pass one of the
-// group scan (blocks 0..3 walk value columns from zero -> B_g, blocks 4..7
-// walk identity columns with u = 0 -> M_g).
+// Inter-chunk walk on tcgen05, transition form.  One CTA per (block of 32
+// value columns, head, sequence x group); thread k of warps 0-3 holds state
+// row k in fp32 and TMEM lane k.  Per chunk c:
+//   Y_c = P_c S_c,  RV_c = R_c v_c  (TMEM),   S_{c+1} = d_c * S_c + Y_c + RV_c
+//   o_c = qg'_c S_c + o_intra_c   (M = 64: row r at lane r % 16 + 32 (r / 16))
+// Warps 0-3 keep the chain; P S, the one product on it, is issued as two
+// K halves into two accumulators by threads 0 and 32, which halves its issue
+// time; warp 9 issues qg' S once S16 holds S_c, and R v one chunk ahead;
+// warps 4-7 add o_intra and write the output rows; warp 8 streams the
+// records in (chain part triple buffered, output part double buffered).
+// mode 1 is the group scan's pass one: B_g from a zero state (blocks 0..3)
+// and M_g from the identity (blocks 4..7, no R v), no output.
 // --------------------------------------------------------------------------
-constexpr int WALK_THREADS = 160;
+constexpr int WALK_THREADS = 320;
 constexpr int NB = 32;
-constexpr uint32_t B_LBO = VB_LBO;  // fp16 B operands of 32 rows, padded K groups
+constexpr uint32_t S16_LBO = 128, S16_SBO = 2048;  // S^T block, MN-major [v][k]
+constexpr uint32_t S16_BYTES = 8192;
+constexpr uint32_t B_BYTES = QG_BYTES + OI_BLOCK;  // qg' and this block's o_intra
 
 struct __align__(1024) WalkSmem {
-  unsigned char ch[2][CH_MAIN];           // chunk records (double buffered)
-  unsigned char v16[2][VB_BYTES];         // this block's v^T, fp16 [v][r]
-  unsigned char s16[B_LBO * 128 / 8];     // S^T block, fp16 [v][k]
-  unsigned char u16[B_LBO * 64 / 8];      // U^T block, fp16 [v][r]
-  int2 meta[2];                           // (first token, rows) of the buffered chunk
-  uint64_t full[2], empty[2];
-  uint64_t bar_x, bar_z;
-  int issued[2];
+  unsigned char a[3][CH_A_BYTES];   // P, R, d of a chunk
+  unsigned char va[3][VB_BYTES];    // this block's v^T, fp16 [v][r]
+  unsigned char b[2][B_BYTES];      // qg' and o_intra of a chunk
+  unsigned char s16[3][S16_BYTES];  // fp16 S of the chunk being entered
+  uint64_t fullA[3], emptyA[3], fullB[2];
+  uint64_t bar_y[2][2], bar_rv[2], bar_o[2], o_done[2], s_ready[3], s_free[3];
+  int issuedA[3], issuedB[2];
   uint32_t tmem;
   int abort;
 };
+static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
 __device__ __forceinline__ const float* initial_state(const ChunkParams& p, int n, int h) {
   if (p.cache) {
@@ -700,13 +770,6 @@ __device__ __forceinline__ void group_range(const ChunkParams& p, int n, int gid
   c1 = base + min(nc, (gidx + 1) * per);
 }
 
-// fp16 S^T block [v][k] from the fp32 state row k held by this thread
-__device__ __forceinline__ void write_s16(unsigned char* s16, int k, const float (&S)[32]) {
-#pragma unroll
-  for (int v = 0; v < 32; ++v)
-    *reinterpret_cast<__half*>(s16 + tc::kmajor_offset_lbo(v, k, B_LBO)) = __float2half_rn(S[v]);
-}
-
 __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p, int mode) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   WalkSmem& s = *reinterpret_cast<WalkSmem*>(smem_raw);
@@ -714,7 +777,8 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   const int n = blockIdx.z / p.groups, gidx = blockIdx.z % p.groups;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool ident = mode == 1 && cb >= D / NB;
-  const int col0 = (cb % (D / NB)) * NB;
+  const bool outp = mode == 0;
+  const int vblk = cb % (D / NB), col0 = vblk * NB;
   int c0, c1;
   group_range(p, n, gidx, c0, c1);
   const int nch = c1 - c0;
@@ -722,17 +786,26 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   const unsigned char* wsb = reinterpret_cast<const unsigned char*>(p.ch);
 
   if (warp == 0) {
-    tc::tmem_alloc(&s.tmem, 128);
+    tc::tmem_alloc(&s.tmem, 256);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s.full[b], 1);
-      mbar_init(&s.empty[b], 1);
-      s.issued[b] = 0;
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s.fullA[i], 1);
+      mbar_init(&s.emptyA[i], ident ? 2 : 3);  // the chain's two P S halves and warp 9's R v
+      mbar_init(&s.s_ready[i], 1);
+      mbar_init(&s.s_free[i], 1);
+      s.issuedA[i] = 0;
     }
-    mbar_init(&s.bar_x, 1);
-    mbar_init(&s.bar_z, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.fullB[i], 1);
+      mbar_init(&s.bar_y[0][i], 1);
+      mbar_init(&s.bar_y[1][i], 1);
+      mbar_init(&s.bar_rv[i], 1);
+      mbar_init(&s.bar_o[i], 1);
+      mbar_init(&s.o_done[i], 4);  // the four output warps
+      s.issuedB[i] = 0;
+    }
     fence_mbar_init();
     s.abort = 0;
   }
@@ -740,12 +813,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
-  const uint32_t T_UO = 0, T_X = 64, T_Z = 96;  // D_uo[b] at columns 32 b
+  const uint32_t T_Y = 0, T_RV = 128, T_O = 192;  // Y half j, buffer b at T_Y + 64 j + 32 b
 
   if (warp < 4) {
-    // ---------------- TMEM warps: math, and thread 0 issues the MMAs --------
-    const int k = tid;  // state row and TMEM lane
-    const bool issuer = tid == 0;
+    // ---------------- chain: state row k; threads 0 and 32 issue P S ---------
+    const int k = tid;
+    const int half = tid == 0 ? 0 : (tid == 32 ? 1 : -1);  // P S issuers
     float S[32];
     {
       const float* src = nullptr;
@@ -758,101 +831,78 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         S[v] = x;
       }
     }
-    // [u ; o_intra] = TT v for chunk it (one chunk ahead of its use)
-    auto issue_uo = [&](int it) {
-      const int b = it & 1;
-      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return;
-      tc::fence_after_sync();
-      if (!ident)
-        tc::mma_kloop(tmem + T_UO + 32 * b, smem_u32(s.ch[b] + CH_TT), smem_u32(s.v16[b]), 128, 32,
-                      64, 0, false, B_LBO);
+    // fp16 S^T block: thread k writes its 32 columns as four 8-column chunks
+    auto write_s16 = [&](int sb) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(s.s16[sb] + tc::mnmajor_offset(8 * j, k, S16_LBO, S16_SBO)) =
+            make_uint4(pack_half2(S[8 * j], S[8 * j + 1]), pack_half2(S[8 * j + 2], S[8 * j + 3]),
+                       pack_half2(S[8 * j + 4], S[8 * j + 5]), pack_half2(S[8 * j + 6], S[8 * j + 7]));
     };
-    // X = WQ S for chunk it, after S16 holds the state entering it
-    auto issue_x = [&](int it) {
-      const int b = it & 1;
-      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) return;
-      tc::fence_after_sync();
-      tc::mma_kloop(tmem + T_X, smem_u32(s.ch[b] + CH_WQ), smem_u32(s.s16), 128, 32, 128, 0, false,
-                    B_LBO);
-      tc::mma_commit(&s.bar_x);
+    auto issue_ps = [&](int it) {  // Y_half[it & 1] = P_it[:, half] S16[it % 3][half, :]
+      if (half == 0) mbar_arrive(&s.s_ready[it % 3]);  // S16 holds S_it: warp 9 may go
+      // K = 64 half * 64 ..: 8 K groups of P (2048 bytes each), 8 of S16 (128 bytes)
+      tc::mma_kloop_bmn(tmem + T_Y + 64 * half + 32 * (it & 1),
+                        smem_u32(s.a[it % 3] + CH_P) + half * 8 * 2048,
+                        smem_u32(s.s16[it % 3]) + half * 8 * S16_LBO, 128, 32, 64, S16_LBO, S16_SBO, false);
+      tc::mma_commit(&s.bar_y[half][it & 1]);
     };
+    // A failed wait sets ``fail``; the chain stops only at a barrier, all
+    // 128 threads together.
+    float dcur = 0.f;
+    bool fail = false;
     if (nch > 0) {
-      write_s16(s.s16, k, S);
+      fail = !wait_or_abort(&s.fullA[0], 0, &s.abort, p.err);
+      if (!fail) dcur = reinterpret_cast<const float*>(s.a[0] + CH_D)[k];
+      write_s16(0);
       fence_proxy_async_smem();
       tc::fence_before_sync();
-      named_bar_sync(1, 128);
-      if (issuer) {
-        issue_uo(0);
-        issue_x(0);
+      fail = named_bar_or(1, 128, fail);
+      if (half >= 0 && !fail) {
+        tc::fence_after_sync();
+        issue_ps(0);
       }
     }
-    for (int it = 0; it < nch; ++it) {
-      const int b = it & 1;
-      if (!wait_or_abort(&s.full[b], (it >> 1) & 1, &s.abort, p.err)) break;
-      if (!wait_or_abort(&s.bar_x, it & 1, &s.abort, p.err)) break;
-      tc::fence_after_sync();
-      // read everything of buffer b now: after Z is issued the loader may refill it
-      const float dk = reinterpret_cast<const float*>(s.ch[b] + CH_D)[k];
-      const int2 meta = s.meta[b];
-      float x[32], uo[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_X), x);
-      if (!ident) {
-        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_UO + 32 * b), uo);
-      } else {
-#pragma unroll
-        for (int v = 0; v < 32; ++v) uo[v] = 0.f;
+    for (int it = 0; !fail && it < nch; ++it) {
+      const int yb = it & 1, ab = (it + 1) % 3;
+      const bool more = it + 1 < nch;
+      float dnext = 0.f;
+      // while P S runs: the next record's d, and the S16 buffer it will take
+      // (last read by the output product of chunk it - 2)
+      if (more) {
+        fail = !wait_or_abort(&s.fullA[ab], ((it + 1) / 3) & 1, &s.abort, p.err);
+        if (!fail) dnext = reinterpret_cast<const float*>(s.a[ab] + CH_D)[k];
+        if (!fail && outp && it >= 2)
+          fail = !wait_or_abort(&s.s_free[ab], ((it - 2) / 3) & 1, &s.abort, p.err);
       }
-      if (warp < 2) {
-        const int r = k;  // U = u - X_w, stored U^T fp16 [v][r]
+      if (!fail) fail = !wait_or_abort(&s.bar_y[0][yb], (it >> 1) & 1, &s.abort, p.err);
+      if (!fail) fail = !wait_or_abort(&s.bar_y[1][yb], (it >> 1) & 1, &s.abort, p.err);
+      if (!fail && !ident) fail = !wait_or_abort(&s.bar_rv[yb], (it >> 1) & 1, &s.abort, p.err);
+      if (!fail) {
+        tc::fence_after_sync();
+        uint32_t y0[32], y1[32], y2[32];
+        tc::tmem_ld32_async(tc::tmem_addr(tmem, 32 * warp, T_Y + 32 * yb), y0);
+        tc::tmem_ld32_async(tc::tmem_addr(tmem, 32 * warp, T_Y + 64 + 32 * yb), y1);
+        if (!ident) tc::tmem_ld32_async(tc::tmem_addr(tmem, 32 * warp, T_RV + 32 * yb), y2);
+        tc::tmem_wait_ld();
 #pragma unroll
         for (int v = 0; v < 32; ++v)
-          *reinterpret_cast<__half*>(s.u16 + tc::kmajor_offset_lbo(v, r, B_LBO)) =
-              __float2half_rn(uo[v] - x[v]);
-        fence_proxy_async_smem();
-      }
-      tc::fence_before_sync();
-      named_bar_sync(1, 128);  // U written, TMEM read: Z may go
-      if (issuer) {
-        tc::fence_after_sync();
-        tc::mma_kloop(tmem + T_Z, smem_u32(s.ch[b] + CH_KGT), smem_u32(s.u16), 128, 32, 64, 0, false,
-                      B_LBO);
-        tc::mma_commit(&s.bar_z);
-        tc::mma_commit(&s.empty[b]);
-        if (it + 1 < nch) issue_uo(it + 1);
-      }
-      if (warp >= 2 && mode == 0) {
-        const int r = k - 64;  // o = X_qg' + o_intra
-        const int bos = meta.x, len = meta.y;
-        if (r < len) {
-          __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D + col0;
-#pragma unroll
-          for (int v8 = 0; v8 < 32; v8 += 8) {
-            uint4 w;
-            __nv_bfloat162 t0 = __floats2bfloat162_rn(x[v8] + uo[v8], x[v8 + 1] + uo[v8 + 1]);
-            __nv_bfloat162 t1 = __floats2bfloat162_rn(x[v8 + 2] + uo[v8 + 2], x[v8 + 3] + uo[v8 + 3]);
-            __nv_bfloat162 t2 = __floats2bfloat162_rn(x[v8 + 4] + uo[v8 + 4], x[v8 + 5] + uo[v8 + 5]);
-            __nv_bfloat162 t3 = __floats2bfloat162_rn(x[v8 + 6] + uo[v8 + 6], x[v8 + 7] + uo[v8 + 7]);
-            w.x = *reinterpret_cast<uint32_t*>(&t0);
-            w.y = *reinterpret_cast<uint32_t*>(&t1);
-            w.z = *reinterpret_cast<uint32_t*>(&t2);
-            w.w = *reinterpret_cast<uint32_t*>(&t3);
-            *reinterpret_cast<uint4*>(dst + v8) = w;
-          }
+          S[v] = fmaf(dcur, S[v], __uint_as_float(y0[v]) + __uint_as_float(y1[v]) +
+                                      (ident ? 0.f : __uint_as_float(y2[v])));
+        if (more) {
+          write_s16(ab);
+          fence_proxy_async_smem();
         }
       }
-      if (!wait_or_abort(&s.bar_z, it & 1, &s.abort, p.err)) break;
-      tc::fence_after_sync();
-      float z[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, T_Z), z);
-#pragma unroll
-      for (int v = 0; v < 32; ++v) S[v] = fmaf(dk, S[v], z[v]);
-      if (it + 1 < nch) {
-        write_s16(s.s16, k, S);
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        named_bar_sync(1, 128);  // S16 holds the next chunk's state: X may go
-        if (issuer && !s.abort) issue_x(it + 1);
+      tc::fence_before_sync();
+      fail = named_bar_or(1, 128, fail);  // Y, RV read; S16 holds S_{it+1}
+      if (fail) break;
+      if (half >= 0) {
+        tc::fence_after_sync();
+        tc::mma_commit(&s.emptyA[it % 3]);  // chunk it's P and d
+        if (more) issue_ps(it + 1);
       }
+      dcur = dnext;
     }
     float* dst = nullptr;  // end state of this column block, V-first rows col0..
     if (mode == 1) dst = (ident ? p.gM : p.gB) + plane;
@@ -860,22 +910,93 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     if (dst && !s.abort)
 #pragma unroll
       for (int v = 0; v < 32; ++v) dst[(int64_t)(col0 + v) * D + k] = S[v];
-  } else if (warp == 4) {
-    // ---------------- loader warp ----------------
+  } else if (warp < 8) {
+    // ---------------- output rows: O[b] lanes 16 q .. 16 q + 15 --------------
+    const int q = warp - 4, r = 16 * q + (lane & 15);
+    for (int it = 0; outp && it < nch; ++it) {
+      const int ob = it & 1;
+      if (!wait_or_abort(&s.bar_o[ob], (it >> 1) & 1, &s.abort, p.err)) break;
+      tc::fence_after_sync();
+      float o[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * q, T_O + 32 * ob), o);
+      uint4 oi[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) oi[j] = *reinterpret_cast<const uint4*>(s.b[ob] + QG_BYTES + r * 64 + 16 * j);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.o_done[ob]);  // O[ob] and b[ob] read
+      const int c = c0 + it, n_ = p.chunk_seq[c];
+      const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
+      const int len = min(CHUNK, seq_eos(p, n_) - bos);
+      if (lane < 16 && r < len) {
+        __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D + col0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162* ib = reinterpret_cast<const __nv_bfloat162*>(&oi[j]);
+          uint4 w;
+          uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(ib[u]);
+            __nv_bfloat162 t = __floats2bfloat162_rn(o[8 * j + 2 * u] + f.x, o[8 * j + 2 * u + 1] + f.y);
+            wp[u] = *reinterpret_cast<uint32_t*>(&t);
+          }
+          *reinterpret_cast<uint4*>(dst + 8 * j) = w;
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // ---------------- loaders: lane 0 the chain's part, lane 16 the output's -
     if (lane == 0) {
       for (int it = 0; it < nch; ++it) {
-        const int b = it & 1;
-        const int c = c0 + it;
-        if (it >= 2 && !wait_or_abort(&s.empty[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
-        const int n_ = p.chunk_seq[c];
-        const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
-        s.meta[b] = make_int2(bos, min(CHUNK, seq_eos(p, n_) - bos));
-        const unsigned char* src = wsb + ((size_t)c * p.hv + h) * CH_BYTES;
-        mbar_arrive_expect_tx(&s.full[b], CH_MAIN + (ident ? 0u : VB_BYTES));
-        bulk_g2s(s.ch[b], src, 32768, &s.full[b]);
-        bulk_g2s(s.ch[b] + 32768, src + 32768, CH_MAIN - 32768, &s.full[b]);
-        if (!ident) bulk_g2s(s.v16[b], src + CH_V16 + (cb % (D / NB)) * VB_BYTES, VB_BYTES, &s.full[b]);
-        s.issued[b] += 1;
+        const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
+        const int ab = it % 3;
+        if (it >= 3 && !wait_or_abort(&s.emptyA[ab], ((it / 3) - 1) & 1, &s.abort, p.err)) break;
+        mbar_arrive_expect_tx(&s.fullA[ab], CH_A_BYTES + (ident ? 0u : VB_BYTES));
+        bulk_g2s(s.a[ab], src + CH_P, 32768, &s.fullA[ab]);
+        bulk_g2s(s.a[ab] + 32768, src + CH_P + 32768, CH_A_BYTES - 32768, &s.fullA[ab]);
+        if (!ident) bulk_g2s(s.va[ab], src + CH_V16 + vblk * VB_BYTES, VB_BYTES, &s.fullA[ab]);
+        s.issuedA[ab] += 1;
+      }
+    } else if (lane == 16 && outp) {
+      for (int it = 0; it < nch; ++it) {
+        const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
+        const int bb = it & 1;
+        if (it >= 2 && !wait_or_abort(&s.o_done[bb], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+        mbar_arrive_expect_tx(&s.fullB[bb], B_BYTES);
+        bulk_g2s(s.b[bb], src + CH_QG, QG_BYTES, &s.fullB[bb]);
+        bulk_g2s(s.b[bb] + QG_BYTES, src + CH_OI + vblk * OI_BLOCK, OI_BLOCK, &s.fullB[bb]);
+        s.issuedB[bb] += 1;
+      }
+    }
+  } else if (!ident) {
+    // ---------------- R v one chunk ahead, and qg' S ----------------
+    if (lane == 0) {
+      auto issue_rv = [&](int it) {  // RV[it & 1] = R_it v_it
+        const int ab = it % 3;
+        if (!wait_or_abort(&s.fullA[ab], (it / 3) & 1, &s.abort, p.err)) return false;
+        tc::fence_after_sync();
+        tc::mma_kloop(tmem + T_RV + 32 * (it & 1), smem_u32(s.a[ab] + CH_R), smem_u32(s.va[ab]), 128, 32,
+                      64, 0, false, VB_LBO);
+        tc::mma_commit(&s.bar_rv[it & 1]);
+        return true;
+      };
+      bool go = nch > 0 && issue_rv(0);
+      for (int it = 0; go && it < nch; ++it) {
+        const int ob = it & 1, sb = it % 3;
+        // S16[sb] holds S_it, and the chain has read RV of chunk it - 1
+        if (!wait_or_abort(&s.s_ready[sb], (it / 3) & 1, &s.abort, p.err)) break;
+        if (outp) {
+          if (!wait_or_abort(&s.fullB[ob], (it >> 1) & 1, &s.abort, p.err)) break;
+          if (it >= 2 && !wait_or_abort(&s.o_done[ob], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+          tc::fence_after_sync();
+          tc::mma_kloop_bmn(tmem + T_O + 32 * ob, smem_u32(s.b[ob]), smem_u32(s.s16[sb]), 64, 32, 128,
+                            S16_LBO, S16_SBO, false);
+          tc::mma_commit(&s.bar_o[ob]);
+          tc::mma_commit(&s.s_free[sb]);
+        }
+        if (it + 1 < nch && !issue_rv(it + 1)) break;
+        tc::mma_commit(&s.emptyA[sb]);  // chunk it's R and v
       }
     }
   }
@@ -883,10 +1004,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   __syncthreads();
   if (tid == 0 && s.abort) {
     // leave no bulk copy in flight: wait (bounded) for the last load of each buffer
-    for (int b = 0; b < 2; ++b)
-      if (s.issued[b] > 0) mbar_wait_bounded(&s.full[b], (s.issued[b] - 1) & 1, p.err);
+    for (int i = 0; i < 3; ++i)
+      if (s.issuedA[i] > 0) mbar_wait_bounded(&s.fullA[i], (s.issuedA[i] - 1) & 1, p.err);
+    for (int i = 0; i < 2; ++i)
+      if (s.issuedB[i] > 0) mbar_wait_bounded(&s.fullB[i], (s.issuedB[i] - 1) & 1, p.err);
   }
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 // --------------------------------------------------------------------------

@@ -61,6 +61,23 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Barrier among ``count`` threads on hardware barrier ``id`` that also
+// returns whether any of them passed ``pred`` true: a uniform decision.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.or.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
@@ -109,10 +126,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
+// Non-blocking test of ``phase``: the fast path before a parking wait.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for ``phase`` of ``bar`` to complete, at most WAIT_CAP rounds.  On
 // expiry sets ERR_TIMEOUT and returns false; the caller must stop using the
 // guarded buffer.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, unsigned* err) {
+  if (mbar_test_wait(bar, phase)) return true;
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < WAIT_CAP; ++i) {
     if (mbar_try_wait(bar, phase)) return true;

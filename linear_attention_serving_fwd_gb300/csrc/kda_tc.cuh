@@ -1,7 +1,8 @@
 // tcgen05 (5th-generation tensor core) building blocks for sm_103a, written
 // as inline PTX: TMEM allocation, shared-memory matrix descriptors for the
-// canonical K-major no-swizzle layout, the kind::f16 MMA with fp32
-// accumulation in TMEM, commit to an mbarrier, and TMEM loads.
+// canonical K-major and MN-major no-swizzle layouts and the 128-byte
+// swizzled K-major one, kind::f16 / kind::tf32 MMAs with fp32 accumulation
+// in TMEM, commit to an mbarrier, and TMEM loads.
 //
 // Operand layout used throughout (K-major, no swizzle).  A matrix of R rows
 // (M or N) by K 16-bit elements is stored as core matrices of 8 rows x 16
@@ -149,6 +150,19 @@ __host__ __device__ __forceinline__ uint32_t kmajor_offset_lbo(uint32_t row, uin
   return (k >> 3) * lbo + (row >> 3) * 128u + (row & 7u) * 16u + (k & 7u) * 2u;
 }
 
+// A run of STEPS kind::f16 instructions whose descriptors advance by fixed
+// byte steps (a_step, b_step; multiples of 16): the descriptors are built
+// once and only their start-address fields move, which keeps the issuing
+// thread's work per instruction to two adds.
+template <int STEPS>
+__device__ __forceinline__ void mma_run(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t a_step,
+                                        uint32_t b_step, uint32_t idesc, bool accumulate_first) {
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s)
+    mma_f16(d_tmem, ad + (uint64_t)((s * a_step) >> 4), bd + (uint64_t)((s * b_step) >> 4), idesc,
+            (s > 0 || accumulate_first) ? 1u : 0u);
+}
+
 // One K-major x K-major product over K elements (K % 16 == 0): A has M rows
 // at a_saddr, B has N rows at b_saddr, both in the layout above (B's K groups
 // b_lbo bytes apart; 0 = packed, N * 16).
@@ -162,6 +176,28 @@ __device__ __forceinline__ void mma_kloop(uint32_t d_tmem, uint32_t a_saddr, uin
     const uint64_t bd = smem_desc(b_saddr + s * 2u * b_lbo, b_lbo, 128u);
     mma_f16(d_tmem, ad, bd, idesc, (s > 0 || accumulate_first) ? 1u : 0u);
   }
+}
+
+// K-major A times MN-major B over K elements (K % 16 == 0).  B's layout:
+//     byte(n, k) = (n / 8) * b_sbo + (k / 8) * b_lbo + (k % 8) * 16 + (n % 8) * 2
+// (8 consecutive n contiguous), selected by bit 16 of the instruction
+// descriptor; each instruction advances B by two 8-row K groups.
+__device__ __forceinline__ void mma_kloop_bmn(uint32_t d_tmem, uint32_t a_saddr, uint32_t b_saddr,
+                                              uint32_t M, uint32_t N, uint32_t K, uint32_t b_lbo,
+                                              uint32_t b_sbo, bool accumulate_first) {
+  const uint32_t idesc = idesc_f16(M, N, 0) | (1u << 16);
+  const uint32_t a_lbo = M * 16u;
+  for (uint32_t s = 0; s < K / 16u; ++s) {
+    const uint64_t ad = smem_desc(a_saddr + s * 2u * a_lbo, a_lbo, 128u);
+    const uint64_t bd = smem_desc(b_saddr + s * 2u * b_lbo, b_lbo, b_sbo);
+    mma_f16(d_tmem, ad, bd, idesc, (s > 0 || accumulate_first) ? 1u : 0u);
+  }
+}
+
+// byte offset of element (n, k) of an MN-major 16-bit operand (layout above)
+__host__ __device__ __forceinline__ uint32_t mnmajor_offset(uint32_t n, uint32_t k, uint32_t lbo,
+                                                           uint32_t sbo) {
+  return (n >> 3) * sbo + (k >> 3) * lbo + (k & 7u) * 16u + (n & 7u) * 2u;
 }
 
 // Same for fp32 operands on kind::tf32 (K in elements, K % 8 == 0).
@@ -211,6 +247,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tmem_ld32 without the wait: issue several, then tmem_wait_ld() once before
+// using any of them.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {

@@ -1,11 +1,13 @@
 """The prefill's per-(chunk, head) records against the oracle's chunk form.
 
-kda_chunk_fwd's prologue writes, for every (chunk, head), the tensor-core
-operands of the walk into the caller's workspace (fp16, K-major core-matrix
-layout):  WQ = [w ; qg - A_qk w] (128 x 128), KGT = kg^T (128 x 64),
-TT = [T ; A_qk T] (128 x 64) and d (fp32 128).  This test decodes them and
-compares each with the same quantity built by oracle/chunked.py, which pins
-the prologue's intermediates, not only the end result.
+kda_chunk_fwd's prologue writes, for every (chunk, head), the walk's
+tensor-core operands into the caller's workspace (fp16, K-major core-matrix
+layout): P = -kg^T w (128 x 128), R = kg^T T (128 x 64), d (fp32 128),
+qg' = qg - A_qk w (64 x 128), o_intra = A_qk T v (bf16, four row-major
+blocks of [64 rows][32 value columns]) and v^T in four blocks of 32 value
+columns.  This test decodes them and compares each with the same
+quantity built by oracle/chunked.py, which pins the prologue's
+intermediates, not only the end result.
 """
 from __future__ import annotations
 
@@ -19,10 +21,10 @@ from linear_attention_serving_fwd_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 D, C = 128, 64
-MAIN = 128 * 128 * 2 + 128 * 64 * 2 * 2 + 128 * 4
+OFF_P, OFF_R, OFF_D, OFF_QG, OFF_OI, OFF_V = 0, 32768, 49152, 49664, 66048, 82432
 VB_LBO = 528
 VB = VB_LBO * 8
-REC = MAIN + 4 * VB
+REC = OFF_V + 4 * VB
 
 
 def _kmajor_decode(raw: np.ndarray, R: int, K: int) -> np.ndarray:
@@ -44,6 +46,13 @@ def _kmajor_decode_lbo(raw: np.ndarray, R: int, K: int, lbo: int) -> np.ndarray:
 
 def _rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _err(a, b):
+    """Relative Frobenius error with an absolute floor of 1e-6 per element:
+    fp16 records flush entries below its subnormal range (6e-8) to zero, and
+    under strong decay a whole operand can sit there."""
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-6 * np.sqrt(b.size)))
 
 
 @pytest.mark.parametrize("T,lb", [(130, -0.3), (64, -5.0)])
@@ -78,26 +87,29 @@ def test_prologue_records_match_chunk_form(T, lb):
             Aqk = pad(ops["Aqk"], (C, C))
             qg = pad(ops["qg"], (C, D))
             kg = pad(ops["kg"], (C, D))
-            want_wq = np.vstack([w, qg - Aqk @ w])
-            want_kgt = kg.T
-            want_tt = np.vstack([Tm, Aqk @ Tm])
+            want_P = -kg.T @ w
+            want_R = kg.T @ Tm
+            want_qg = qg - Aqk @ w
+            vv = pad(f(x.v[s:e, h]), (C, D))
+            want_oi = Aqk @ Tm @ vv
             off = base + (c * 2 + h) * REC
             rec = raw[off:off + REC]
-            got_wq = _kmajor_decode(rec[0:32768], 128, 128)
-            got_kgt = _kmajor_decode(rec[32768:49152], 128, 64)
-            got_tt = _kmajor_decode(rec[49152:65536], 128, 64)
-            got_d = rec[65536:66048].view(np.float32).astype(np.float64)
+            got_P = _kmajor_decode(rec[OFF_P:OFF_R], 128, 128)
+            got_R = _kmajor_decode(rec[OFF_R:OFF_D], 128, 64)
+            got_d = rec[OFF_D:OFF_QG].view(np.float32).astype(np.float64)
+            got_qg = _kmajor_decode(rec[OFF_QG:OFF_OI], 64, 128)
+            oi_raw = rec[OFF_OI:OFF_V].view(np.uint16).astype(np.uint32) << 16
+            got_oi = np.concatenate([oi_raw.view(np.float32).astype(np.float64)[j * 2048:(j + 1) * 2048]
+                                     .reshape(64, 32) for j in range(4)], axis=1)
             tag = f"T={T} head {h} chunk {c} (len {L})"
-            assert _rel(got_tt[:64], want_tt[:64]) < 2e-3, f"T block {tag}: {_rel(got_tt[:64], want_tt[:64])}"
-            assert _rel(got_tt[64:], want_tt[64:]) < 1e-2, f"A_qk T {tag}: {_rel(got_tt[64:], want_tt[64:])}"
-            assert _rel(got_kgt, want_kgt) < 2e-3, f"kg {tag}"
             assert _rel(got_d, ops["d"]) < 1e-4, f"d {tag}"
-            assert _rel(got_wq[:64], want_wq[:64]) < 5e-3, f"w {tag}: {_rel(got_wq[:64], want_wq[:64])}"
-            assert _rel(got_wq[64:], want_wq[64:]) < 1e-2, f"qg' {tag}: {_rel(got_wq[64:], want_wq[64:])}"
+            assert _err(got_R, want_R) < 5e-3, f"R {tag}: {_err(got_R, want_R)}"
+            assert _err(got_P, want_P) < 1e-2, f"P {tag}: {_err(got_P, want_P)}"
+            assert _err(got_qg, want_qg) < 1e-2, f"qg' {tag}: {_err(got_qg, want_qg)}"
+            assert _err(got_oi, want_oi) < 1e-2, f"o_intra {tag}: {_err(got_oi, want_oi)}"
             # v^T blocks, fp16 [32 value columns][64 rows]: bf16 v converted to
             # fp16, exact except below fp16's normal range (absolute 3e-8)
-            vv = pad(f(x.v[s:e, h]), (C, D))
             for jb in range(4):
-                got_v = _kmajor_decode_lbo(rec[MAIN + jb * VB:MAIN + (jb + 1) * VB], 32, 64, VB_LBO)
+                got_v = _kmajor_decode_lbo(rec[OFF_V + jb * VB:OFF_V + (jb + 1) * VB], 32, 64, VB_LBO)
                 np.testing.assert_allclose(got_v, vv[:, 32 * jb:32 * (jb + 1)].T, rtol=0, atol=3e-8,
                                            err_msg=f"v block {jb} {tag}")
