@@ -713,18 +713,22 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
 // --------------------------------------------------------------------------
 // Inter-chunk walk on tcgen05, transition form.  One CTA per (block of 32
 // value columns, head, sequence x group); thread k of warps 0-3 holds state
-// row k in fp32 and TMEM lane k.  Per chunk c:
+// row k in fp32 and TMEM lane k (warps 4-7 the same rows' other 16 of the
+// block's 32 columns).  Per chunk c:
 //   Y_c = P_c S_c,  RV_c = R_c v_c  (TMEM),   S_{c+1} = d_c * S_c + Y_c + RV_c
 //   o_c = qg'_c S_c + o_intra_c   (M = 64: row r at lane r % 16 + 32 (r / 16))
-// Warps 0-3 keep the chain; P S, the one product on it, is issued as two
+// Warps 0-7 keep the chain; P S, the one product on it, is issued as two
 // K halves into two accumulators by threads 0 and 32, which halves its issue
-// time; warp 9 issues qg' S once S16 holds S_c, and R v one chunk ahead;
-// warps 4-7 add o_intra and write the output rows; warp 8 streams the
-// records in (chain part triple buffered, output part double buffered).
+// time, and both halves and R v complete on one barrier; warp 13 issues
+// qg' S and the next chunk's R v once that barrier has fired, so that they
+// run while the chain threads work, not beside P S; warps 8-11 add o_intra
+// and write the output rows; warp 12 streams the records in (chain part
+// triple buffered, output part double buffered).
 // mode 1 is the group scan's pass one: B_g from a zero state (blocks 0..3)
 // and M_g from the identity (blocks 4..7, no R v), no output.
 // --------------------------------------------------------------------------
-constexpr int WALK_THREADS = 320;
+constexpr int WALK_THREADS = 448;
+constexpr int CHAIN_THREADS = 256;
 constexpr int NB = 32;
 constexpr uint32_t S16_LBO = 128, S16_SBO = 2048;  // S^T block, MN-major [v][k]
 constexpr uint32_t S16_BYTES = 8192;
@@ -736,7 +740,7 @@ struct __align__(1024) WalkSmem {
   unsigned char b[2][B_BYTES];      // qg' and o_intra of a chunk
   unsigned char s16[3][S16_BYTES];  // fp16 S of the chunk being entered
   uint64_t fullA[3], emptyA[3], fullB[2];
-  uint64_t bar_y[2][2], bar_rv[2], bar_o[2], o_done[2], s_ready[3], s_free[3];
+  uint64_t bar_y[2], bar_o[2], o_done[2], s_free[3];
   int issuedA[3], issuedB[2];
   uint32_t tmem;
   int abort;
@@ -793,15 +797,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     for (int i = 0; i < 3; ++i) {
       mbar_init(&s.fullA[i], 1);
       mbar_init(&s.emptyA[i], ident ? 2 : 3);  // the chain's two P S halves and warp 9's R v
-      mbar_init(&s.s_ready[i], 1);
       mbar_init(&s.s_free[i], 1);
       s.issuedA[i] = 0;
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.fullB[i], 1);
-      mbar_init(&s.bar_y[0][i], 1);
-      mbar_init(&s.bar_y[1][i], 1);
-      mbar_init(&s.bar_rv[i], 1);
+      mbar_init(&s.bar_y[i], ident ? 2 : 3);  // the two P S halves and R v
       mbar_init(&s.bar_o[i], 1);
       mbar_init(&s.o_done[i], 4);  // the four output warps
       s.issuedB[i] = 0;
@@ -815,37 +816,38 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   const uint32_t tmem = s.tmem;
   const uint32_t T_Y = 0, T_RV = 128, T_O = 192;  // Y half j, buffer b at T_Y + 64 j + 32 b
 
-  if (warp < 4) {
-    // ---------------- chain: state row k; threads 0 and 32 issue P S ---------
-    const int k = tid;
-    const int half = tid == 0 ? 0 : (tid == 32 ? 1 : -1);  // P S issuers
-    float S[32];
+  if (warp < 8) {
+    // ---------------- chain: state row k, columns 16 ch ..; threads 0 and 32
+    // issue the two halves of P S
+    const int k = tid & 127, ch = tid >> 7;
+    const int half = tid == 0 ? 0 : (tid == 32 ? 1 : -1);
+    float S[16];
     {
       const float* src = nullptr;
       if (mode == 0) src = (p.groups > 1) ? p.gS + plane : initial_state(p, n, h);
 #pragma unroll
-      for (int v = 0; v < 32; ++v) {
+      for (int v = 0; v < 16; ++v) {
+        const int col = col0 + 16 * ch + v;
         float x = 0.f;
-        if (mode == 1) x = (ident && k == col0 + v) ? 1.f : 0.f;
-        else if (src) x = src[(int64_t)(col0 + v) * D + k];
+        if (mode == 1) x = (ident && k == col) ? 1.f : 0.f;
+        else if (src) x = src[(int64_t)col * D + k];
         S[v] = x;
       }
     }
-    // fp16 S^T block: thread k writes its 32 columns as four 8-column chunks
+    // fp16 S^T block: thread (k, ch) writes its 16 columns as two 8-column chunks
     auto write_s16 = [&](int sb) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(s.s16[sb] + tc::mnmajor_offset(8 * j, k, S16_LBO, S16_SBO)) =
+      for (int j = 0; j < 2; ++j)
+        *reinterpret_cast<uint4*>(s.s16[sb] + tc::mnmajor_offset(16 * ch + 8 * j, k, S16_LBO, S16_SBO)) =
             make_uint4(pack_half2(S[8 * j], S[8 * j + 1]), pack_half2(S[8 * j + 2], S[8 * j + 3]),
                        pack_half2(S[8 * j + 4], S[8 * j + 5]), pack_half2(S[8 * j + 6], S[8 * j + 7]));
     };
     auto issue_ps = [&](int it) {  // Y_half[it & 1] = P_it[:, half] S16[it % 3][half, :]
-      if (half == 0) mbar_arrive(&s.s_ready[it % 3]);  // S16 holds S_it: warp 9 may go
       // K = 64 half * 64 ..: 8 K groups of P (2048 bytes each), 8 of S16 (128 bytes)
       tc::mma_kloop_bmn(tmem + T_Y + 64 * half + 32 * (it & 1),
                         smem_u32(s.a[it % 3] + CH_P) + half * 8 * 2048,
                         smem_u32(s.s16[it % 3]) + half * 8 * S16_LBO, 128, 32, 64, S16_LBO, S16_SBO, false);
-      tc::mma_commit(&s.bar_y[half][it & 1]);
+      tc::mma_commit(&s.bar_y[it & 1]);
     };
     // A failed wait sets ``fail``; the chain stops only at a barrier, all
     // 128 threads together.
@@ -857,7 +859,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       write_s16(0);
       fence_proxy_async_smem();
       tc::fence_before_sync();
-      fail = named_bar_or(1, 128, fail);
+      fail = named_bar_or(1, CHAIN_THREADS, fail);
       if (half >= 0 && !fail) {
         tc::fence_after_sync();
         issue_ps(0);
@@ -875,18 +877,17 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         if (!fail && outp && it >= 2)
           fail = !wait_or_abort(&s.s_free[ab], ((it - 2) / 3) & 1, &s.abort, p.err);
       }
-      if (!fail) fail = !wait_or_abort(&s.bar_y[0][yb], (it >> 1) & 1, &s.abort, p.err);
-      if (!fail) fail = !wait_or_abort(&s.bar_y[1][yb], (it >> 1) & 1, &s.abort, p.err);
-      if (!fail && !ident) fail = !wait_or_abort(&s.bar_rv[yb], (it >> 1) & 1, &s.abort, p.err);
+      if (!fail) fail = !wait_or_abort(&s.bar_y[yb], (it >> 1) & 1, &s.abort, p.err);
       if (!fail) {
         tc::fence_after_sync();
-        uint32_t y0[32], y1[32], y2[32];
-        tc::tmem_ld32_async(tc::tmem_addr(tmem, 32 * warp, T_Y + 32 * yb), y0);
-        tc::tmem_ld32_async(tc::tmem_addr(tmem, 32 * warp, T_Y + 64 + 32 * yb), y1);
-        if (!ident) tc::tmem_ld32_async(tc::tmem_addr(tmem, 32 * warp, T_RV + 32 * yb), y2);
+        uint32_t y0[16], y1[16], y2[16];
+        const uint32_t lanes = tc::tmem_addr(tmem, 32 * (warp & 3), 16 * ch + 32 * yb);
+        tc::tmem_ld16_async(lanes + T_Y, y0);
+        tc::tmem_ld16_async(lanes + T_Y + 64, y1);
+        if (!ident) tc::tmem_ld16_async(lanes + T_RV, y2);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < 32; ++v)
+        for (int v = 0; v < 16; ++v)
           S[v] = fmaf(dcur, S[v], __uint_as_float(y0[v]) + __uint_as_float(y1[v]) +
                                       (ident ? 0.f : __uint_as_float(y2[v])));
         if (more) {
@@ -895,7 +896,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         }
       }
       tc::fence_before_sync();
-      fail = named_bar_or(1, 128, fail);  // Y, RV read; S16 holds S_{it+1}
+      fail = named_bar_or(1, CHAIN_THREADS, fail);  // Y, RV read; S16 holds S_{it+1}
       if (fail) break;
       if (half >= 0) {
         tc::fence_after_sync();
@@ -909,10 +910,10 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     else if (p.groups == 1) dst = final_state(p, n, h);
     if (dst && !s.abort)
 #pragma unroll
-      for (int v = 0; v < 32; ++v) dst[(int64_t)(col0 + v) * D + k] = S[v];
-  } else if (warp < 8) {
+      for (int v = 0; v < 16; ++v) dst[(int64_t)(col0 + 16 * ch + v) * D + k] = S[v];
+  } else if (warp < 12) {
     // ---------------- output rows: O[b] lanes 16 q .. 16 q + 15 --------------
-    const int q = warp - 4, r = 16 * q + (lane & 15);
+    const int q = warp - 8, r = 16 * q + (lane & 15);
     for (int it = 0; outp && it < nch; ++it) {
       const int ob = it & 1;
       if (!wait_or_abort(&s.bar_o[ob], (it >> 1) & 1, &s.abort, p.err)) break;
@@ -945,11 +946,18 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         }
       }
     }
-  } else if (warp == 8) {
-    // ---------------- loaders: lane 0 the chain's part, lane 16 the output's -
+  } else if (warp == 12) {
+    // ---------------- loaders: lane 0 the chain's part, lane 16 the output's;
+    // each also warms L2 with the record it will load LOOKAHEAD chunks later
+    constexpr int LOOKAHEAD = 4;
     if (lane == 0) {
       for (int it = 0; it < nch; ++it) {
         const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
+        if (it == 0)
+          for (int j = 1; j < LOOKAHEAD && j < nch; ++j)
+            bulk_prefetch_l2(wsb + ((size_t)(c0 + j) * p.hv + h) * CH_BYTES, CH_A_BYTES);
+        if (it + LOOKAHEAD < nch)
+          bulk_prefetch_l2(wsb + ((size_t)(c0 + it + LOOKAHEAD) * p.hv + h) * CH_BYTES, CH_A_BYTES);
         const int ab = it % 3;
         if (it >= 3 && !wait_or_abort(&s.emptyA[ab], ((it / 3) - 1) & 1, &s.abort, p.err)) break;
         mbar_arrive_expect_tx(&s.fullA[ab], CH_A_BYTES + (ident ? 0u : VB_BYTES));
@@ -961,6 +969,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     } else if (lane == 16 && outp) {
       for (int it = 0; it < nch; ++it) {
         const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
+        if (it + LOOKAHEAD < nch)
+          bulk_prefetch_l2(wsb + ((size_t)(c0 + it + LOOKAHEAD) * p.hv + h) * CH_BYTES + CH_QG,
+                           QG_BYTES + 4 * OI_BLOCK + 4 * VB_BYTES);
         const int bb = it & 1;
         if (it >= 2 && !wait_or_abort(&s.o_done[bb], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
         mbar_arrive_expect_tx(&s.fullB[bb], B_BYTES);
@@ -978,14 +989,15 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         tc::fence_after_sync();
         tc::mma_kloop(tmem + T_RV + 32 * (it & 1), smem_u32(s.a[ab] + CH_R), smem_u32(s.va[ab]), 128, 32,
                       64, 0, false, VB_LBO);
-        tc::mma_commit(&s.bar_rv[it & 1]);
+        tc::mma_commit(&s.bar_y[it & 1]);
         return true;
       };
       bool go = nch > 0 && issue_rv(0);
       for (int it = 0; go && it < nch; ++it) {
         const int ob = it & 1, sb = it % 3;
-        // S16[sb] holds S_it, and the chain has read RV of chunk it - 1
-        if (!wait_or_abort(&s.s_ready[sb], (it / 3) & 1, &s.abort, p.err)) break;
+        // chunk it's P S and R v are done: S16[sb] holds S_it and the chain
+        // has read RV of chunk it - 1
+        if (!wait_or_abort(&s.bar_y[ob], (it >> 1) & 1, &s.abort, p.err)) break;
         if (outp) {
           if (!wait_or_abort(&s.fullB[ob], (it >> 1) & 1, &s.abort, p.err)) break;
           if (it >= 2 && !wait_or_abort(&s.o_done[ob], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;

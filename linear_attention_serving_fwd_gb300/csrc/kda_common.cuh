@@ -126,6 +126,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
+// Bring ``bytes`` (a multiple of 16, 16-byte aligned) at ``src`` into L2
+// without waiting.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Non-blocking test of ``phase``: the fast path before a parking wait.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t phase) {
   uint32_t ok;
