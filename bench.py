@@ -65,6 +65,40 @@ def prefill_bytes_per_token_head(hqk, hv):
     return 2 * 256 / (hv // hqk) + 512 + 2 + 256
 
 
+# Sources each kernel is built from: a profiled DRAM traffic figure is only
+# reported while these files are unchanged since the capture.
+KERNEL_SOURCES = {
+    "kda_prologue": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh"],
+    "kda_walk": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh"],
+    "kda_window": ["kda_window.cu", "kda_common.cuh", "kda_params.cuh"],
+}
+
+
+def sources_sha256(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "linear_attention_serving_fwd_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch (read + write) from the committed ncu summary in
+    profiles/, or None when the kernel's sources changed since the capture."""
+    import re
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        text = open(path).read()
+        block = re.search(r"```json\n(.*?)\n```", text, re.S).group(1)
+        rec = json.loads(block).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("sources_sha256") != sources_sha256(kernel):
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -217,7 +251,8 @@ def run_ours(args, rank, world, barrier, reduce_max):
     th = n * w["T"] * w["hv"]
     tflops = th * flop_per_token_head() * args.steps * world / secs / 1e12
 
-    # dominant kernel, timed live with the library's event tracing
+    # dominant kernel, timed live with the library's event tracing (CUDA
+    # events recorded by the library on its launch stream)
     _native.trace_enable(True)
     time_device(torch, step, args.steps, flush, barrier)
     tr = _native.trace_read()
@@ -225,17 +260,41 @@ def run_ours(args, rank, world, barrier, reduce_max):
     launches = sum(c for _, c in tr.values())
     dom = max(tr, key=lambda k: tr[k][0])
     dom_ms = tr[dom][0] / tr[dom][1]
-    # algorithmic flop per (token, v-head) by kernel: the prologue forms A_kk,
-    # A_qk and w = T Kg (6 C K); the walk forms w S, qg' S, kg^T U (6 K V) and
-    # [u ; A_qk u] = [T ; A_qk T] v (4 C K)
-    per_kernel_flop = {"kda_prologue": 6 * CHUNK * D, "kda_walk": 6 * D * D + 4 * CHUNK * D,
-                       "kda_walk_pass1": 2 * (6 * D * D), "kda_group_compose": 0}
-    f_unit = per_kernel_flop.get(dom, flop_per_token_head())
-    achieved = th * f_unit / (dom_ms / 1e3) / 1e12
-    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 3),
-                "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4),
-                "traffic": None, "peak_source": f"{pk['src']} bf16 dense (burst)",
-                "per_launch_ms": round(dom_ms, 4),
+    # Algorithmic work per (token, v-head) by kernel.  The prologue streams the
+    # step's inputs once (q, k per q/k head, v, g, beta): an HBM roofline.  The
+    # walk carries the method's three 64 x 128 x 128 contractions (6 K V flop)
+    # and writes o: a tensor roofline over a serial chain.
+    r = w["hv"] // w["hqk"]
+    in_bytes = 2 * 256 / r + 512 + 2
+    kern = {
+        "kda_prologue": {"bound": "hbm", "unit": "GB/s", "peak": pk["hbm"],
+                         "work": th * in_bytes, "scale": 1e9,
+                         "peak_source": f"{pk['src']} HBM copy bandwidth",
+                         "per_unit": f"{in_bytes:.0f} B of q/k/v/g/beta per (token, v-head)"},
+        "kda_walk": {"bound": "tensor", "unit": "TFLOP/s", "peak": pk["bf16"],
+                     "work": th * 6 * D * D, "scale": 1e12,
+                     "peak_source": f"{pk['src']} bf16 dense (burst)",
+                     "per_unit": "6 K V flop per (token, v-head)"},
+    }
+    details = {}
+    for name, kd in kern.items():
+        if name not in tr:
+            continue
+        ms = tr[name][0] / tr[name][1]
+        ach = kd["work"] / (ms / 1e3) / kd["scale"]
+        details[name] = {"bound": kd["bound"], "achieved": round(ach, 3), "peak": kd["peak"],
+                         "unit": kd["unit"], "frac": round(ach / kd["peak"], 4),
+                         "per_launch_ms": round(ms, 4), "per_unit": kd["per_unit"]}
+    d = details.get(dom)
+    if d is None:  # a kernel without a model: report its time only
+        d = {"bound": "tensor", "achieved": None, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": None,
+             "per_launch_ms": round(dom_ms, 4)}
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"],
+                "traffic": profiled_traffic(dom) if dom in KERNEL_SOURCES else None,
+                "peak_source": kern.get(dom, {}).get("peak_source"),
+                "per_launch_ms": d["per_launch_ms"], "per_unit": d.get("per_unit"),
+                "kernels": details,
                 "kernels_ms_per_step": {k: round(v[0] / v[1], 4) for k, v in tr.items()}}
 
     # end to end through the public API with pinned host buffers
@@ -333,7 +392,8 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                         "state_gbs": round(state_bytes / t / 1e9, 1),
                         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
                                      "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                                     "traffic": None,
+                                     "traffic": profiled_traffic("kda_window") if window == 1 and not verify
+                                     else None,
                                      "peak_source": f"{pk['src']} HBM copy bandwidth"},
                         "workload": f"256 requests x window {window}, Hqk=Hv=32, 512-slot fp32 pool"}
         del y, pool
