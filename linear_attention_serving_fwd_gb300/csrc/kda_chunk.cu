@@ -364,31 +364,44 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       // so none overflows and one underflows only where the result is below e^{-87}
       const float Pm = __expf(mR - sR), Qs = __expf(sR);
       const float He = __expf(lam[15] - mR), Jc = __expf(lamC - lam[15]);
+      // normalised keys and queries (the row norms are the warp's: 16-byte
+      // broadcasts)
+#pragma unroll
+      for (int i4 = 0; i4 < 16; i4 += 4) {
+        const float4 r4 = *reinterpret_cast<const float4*>(&s.rk[16 * Rq + i4]);
+        const float4 q4 = *reinterpret_cast<const float4*>(&s.rq[16 * Rq + i4]);
+        kv[i4] *= r4.x; kv[i4 + 1] *= r4.y; kv[i4 + 2] *= r4.z; kv[i4 + 3] *= r4.w;
+        qv[i4] *= q4.x; qv[i4 + 1] *= q4.y; qv[i4 + 2] *= q4.z; qv[i4 + 3] *= q4.w;
+      }
       uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
+      // rows in pairs: packed fp32x2 products
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        float kgv[2], Kgv[2], qgv[2];
+        const int r = 16 * Rq + i;
+        // e^{Lam - m} and e^{m - Lam}, both within e^{+-84}
+        const float2 E = make_float2(__expf(lam[i] - mR), __expf(lam[i + 1] - mR));
+        const float2 iE = make_float2(__expf(mR - lam[i]), __expf(mR - lam[i + 1]));
+        const float2 kh = make_float2(kv[i], kv[i + 1]), qh = make_float2(qv[i], qv[i + 1]);
+        const float2 xk = fmul2(kh, E), xq = fmul2(qh, E), y = fmul2(kh, iE);
+        const float2 kg2 = fmul2(fmul2(y, make_float2(He, He)), make_float2(Jc, Jc));
+        const float2 Kg2 = fmul2(fmul2(xk, make_float2(Pm, Pm)), make_float2(Qs, Qs));
+        const float2 qg2 = fmul2(fmul2(xq, make_float2(Pm, Pm)), make_float2(Qs, Qs));
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk.x);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r + 1, c, 128)) = tc::to_tf32(xk.y);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq.x);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(65 + r, c, 128)) = tc::to_tf32(xq.y);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int ii = i + u, r = 16 * Rq + ii;
-          const float kh = kv[ii] * s.rk[r], qh = qv[ii] * s.rq[r];
-          const float E = __expf(lam[ii] - mR);  // within e^{+-84}
-          const float iE = E > 0.f ? __fdividef(1.f, E) : 0.f;
-          const float xk = kh * E, xq = qh * E, y = kh * iE;
-          kgv[u] = (y * He) * Jc;
-          Kgv[u] = (xk * Pm) * Qs;
-          qgv[u] = (xq * Pm) * Qs;
-          *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk);
-          *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq);
-#pragma unroll
-          for (int R2 = 0; R2 < 4; ++R2)
-            if (R2 >= Rq)
-              *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
-                  tc::to_tf32(y * F[R2]);
-        }
-        kgw[i >> 1] = pack_half2(kgv[0], kgv[1]);
-        Kgx[i >> 1] = pack_half2(Kgv[0], Kgv[1]);
-        qgx[i >> 1] = pack_half2(qgv[0], qgv[1]);
+        for (int R2 = 0; R2 < 4; ++R2)
+          if (R2 >= Rq) {
+            const float2 yf = fmul2(y, make_float2(F[R2], F[R2]));
+            *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
+                tc::to_tf32(yf.x);
+            *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r + 1, c, YROWS)) =
+                tc::to_tf32(yf.y);
+          }
+        kgw[i >> 1] = pack_half2(kg2.x, kg2.y);
+        Kgx[i >> 1] = pack_half2(Kg2.x, Kg2.y);
+        qgx[i >> 1] = pack_half2(qg2.x, qg2.y);
       }
       // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KG [k = c][K = r]
 #pragma unroll

@@ -53,6 +53,23 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float v[4])
   *reinterpret_cast<uint2*>(p) = raw;
 }
 
+// packed fp32x2 helpers
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ar = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long br = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long cr = *reinterpret_cast<unsigned long long*>(&c);
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ar), "l"(br), "l"(cr));
+  return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  unsigned long long ar = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long br = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ar), "l"(br));
+  return *reinterpret_cast<float2*>(&r);
+}
+
 // logistic function with the fast (2-ulp) divide; exp(-x) = inf gives 0
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 

@@ -93,23 +93,6 @@ __device__ __forceinline__ void issue_inputs(const WindowParams& p, const ItemIn
   }
 }
 
-// packed fp32x2 helpers
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long ar = *reinterpret_cast<unsigned long long*>(&a);
-  unsigned long long br = *reinterpret_cast<unsigned long long*>(&b);
-  unsigned long long cr = *reinterpret_cast<unsigned long long*>(&c);
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ar), "l"(br), "l"(cr));
-  return *reinterpret_cast<float2*>(&r);
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  unsigned long long ar = *reinterpret_cast<unsigned long long*>(&a);
-  unsigned long long br = *reinterpret_cast<unsigned long long*>(&b);
-  unsigned long long r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ar), "l"(br));
-  return *reinterpret_cast<float2*>(&r);
-}
-
 // Token t's per-channel vectors, computed by one warp (lane = 4 channels).
 __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s, int h,
                                               const __nv_bfloat16* rowp, int64_t tok, int t,
