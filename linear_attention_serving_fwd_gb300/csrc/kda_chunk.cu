@@ -286,19 +286,30 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     {
       float acc = 0.f;
       uint32_t vw[8];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
+      const float2 ah2 = make_float2(a_h, a_h), adt2 = make_float2(a_h * dt, a_h * dt);
+      // rows in pairs; rows at or past ``len`` belong to the next sequence
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 16; i += 2) {
         const int r = 16 * Rq + i;
-        const bool in = r < len;  // later rows belong to the next sequence
-        qv[i] = in ? bf2f(tiles[(0 * 64 + r) * D + c]) : 0.f;
-        kv[i] = in ? bf2f(tiles[(1 * 64 + r) * D + c]) : 0.f;
-        float g = in ? bf2f(tiles[(2 * 64 + r) * D + c]) : 0.f;
-        g = (p.has_gate && in) ? p.lower_bound * sigmoidf_(a_h * (g + dt)) : g;
-        acc += g;
+        const bool in0 = r < len, in1 = r + 1 < len;
+        qv[i] = in0 ? bf2f(tiles[(0 * 64 + r) * D + c]) : 0.f;
+        qv[i + 1] = in1 ? bf2f(tiles[(0 * 64 + r + 1) * D + c]) : 0.f;
+        kv[i] = in0 ? bf2f(tiles[(1 * 64 + r) * D + c]) : 0.f;
+        kv[i + 1] = in1 ? bf2f(tiles[(1 * 64 + r + 1) * D + c]) : 0.f;
+        float2 g = make_float2(in0 ? bf2f(tiles[(2 * 64 + r) * D + c]) : 0.f,
+                               in1 ? bf2f(tiles[(2 * 64 + r + 1) * D + c]) : 0.f);
+        if (p.has_gate) {  // lower_bound * sigmoid(a (g + dt_bias)), in pairs
+          const float2 t = ffma2(ah2, g, adt2);
+          const float2 den = fadd2(make_float2(__expf(-t.x), __expf(-t.y)), make_float2(1.f, 1.f));
+          g = make_float2(in0 ? __fdividef(p.lower_bound, den.x) : 0.f,
+                          in1 ? __fdividef(p.lower_bound, den.y) : 0.f);
+        }
+        acc += g.x;
         lam[i] = acc;
-        if (i & 1)
-          vw[i >> 1] = pack_half2(r - 1 < len ? bf2f(tiles[(3 * 64 + r - 1) * D + c]) : 0.f,
-                                  in ? bf2f(tiles[(3 * 64 + r) * D + c]) : 0.f);
+        acc += g.y;
+        lam[i + 1] = acc;
+        vw[i >> 1] = pack_half2(in0 ? bf2f(tiles[(3 * 64 + r) * D + c]) : 0.f,
+                                in1 ? bf2f(tiles[(3 * 64 + r + 1) * D + c]) : 0.f);
       }
       // v^T of this column: the record's block c / 32, and VT for o_intra
 #pragma unroll
@@ -313,7 +324,12 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       // channels (row = lane % 16), then the four channel groups meet in smem
       float pk[16], pq[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) { pk[i] = kv[i] * kv[i]; pq[i] = qv[i] * qv[i]; }
+      for (int i = 0; i < 16; i += 2) {
+        const float2 k2 = make_float2(kv[i], kv[i + 1]), q2 = make_float2(qv[i], qv[i + 1]);
+        const float2 kk = fmul2(k2, k2), qq = fmul2(q2, q2);
+        pk[i] = kk.x; pk[i + 1] = kk.y;
+        pq[i] = qq.x; pq[i + 1] = qq.y;
+      }
 #pragma unroll
       for (int sh = 8; sh >= 1; sh >>= 1) {
         const bool up = (lane & sh) != 0;

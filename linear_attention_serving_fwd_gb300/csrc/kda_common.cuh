@@ -62,6 +62,13 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ar), "l"(br), "l"(cr));
   return *reinterpret_cast<float2*>(&r);
 }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  unsigned long long ar = *reinterpret_cast<unsigned long long*>(&a);
+  unsigned long long br = *reinterpret_cast<unsigned long long*>(&b);
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ar), "l"(br));
+  return *reinterpret_cast<float2*>(&r);
+}
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   unsigned long long ar = *reinterpret_cast<unsigned long long*>(&a);
   unsigned long long br = *reinterpret_cast<unsigned long long*>(&b);
