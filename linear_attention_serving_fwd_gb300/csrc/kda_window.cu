@@ -6,7 +6,11 @@
 //  * persistent grid, one CTA per SM, 512 threads = 16 warps;
 //  * two 64 KB state buffers filled by 1-D bulk async copies (TMA engine)
 //    completing on mbarriers, plus two small buffers for the window's
-//    q/k/v/g rows; the state of the item two ahead streams in while one runs;
+//    q/k/v/g rows (issued by the lanes of one warp); the state of the item
+//    two ahead streams in while one runs, and the next item's per-token
+//    scalars (beta, A_log, dt_bias) are loaded into registers a step ahead;
+//  * decode writes the new state back through a third 64 KB buffer and two
+//    bulk stores, so no thread waits on its write;
 //  * per item, warp t < qlen first turns token t's raw rows into the vectors
 //    every warp needs (L2-normalised k^ and q~, exp(gate), their products)
 //    in shared memory, once;
@@ -35,6 +39,7 @@ constexpr int ROW_BYTES = D * 2;                      // one bf16 row of 128
 
 struct __align__(128) WinSmem {
   float state[2][D * D];
+  float sout[D * D];  // decode: the new state, written back by bulk stores
   __nv_bfloat16 in[2][MAX_WINDOW * 4 * D];
   float tp[MAX_WINDOW][D];    // e^gate * k^
   float tr[MAX_WINDOW][D];    // e^gate * q~
@@ -45,6 +50,8 @@ struct __align__(128) WinSmem {
   uint64_t sbar[2], ibar[2];
   int next;
 };
+
+static_assert(sizeof(WinSmem) <= 227 * 1024, "window kernel shared memory");
 
 struct ItemInfo {
   int request, head, qs, qlen;
@@ -79,24 +86,50 @@ __device__ __forceinline__ void issue_state(const WindowParams& p, const ItemInf
   bulk_g2s(sbuf + D * D / 2, src + D * D / 2, STATE_BYTES / 2, sbar);
 }
 
+// The window's q/k/v/g rows, one bulk copy per lane of the calling warp.
 __device__ __forceinline__ void issue_inputs(const WindowParams& p, const ItemInfo& it,
-                                             __nv_bfloat16* ibuf, uint64_t* ibar) {
+                                             __nv_bfloat16* ibuf, uint64_t* ibar, int lane) {
   const int hq = it.head / (p.hv / p.hqk);
-  mbar_arrive_expect_tx(ibar, it.qlen * 4 * ROW_BYTES);
-  for (int t = 0; t < it.qlen; ++t) {
+  if (lane == 0) mbar_arrive_expect_tx(ibar, it.qlen * 4 * ROW_BYTES);
+  __syncwarp();
+  if (lane < 4 * it.qlen) {
+    const int t = lane >> 2, which = lane & 3;
     const int64_t tok = it.qs + t;
-    __nv_bfloat16* dst = ibuf + t * 4 * D;
-    bulk_g2s(dst + 0 * D, p.q + tok * p.q_st + hq * p.q_sh, ROW_BYTES, ibar);
-    bulk_g2s(dst + 1 * D, p.k + tok * p.k_st + hq * p.k_sh, ROW_BYTES, ibar);
-    bulk_g2s(dst + 2 * D, p.v + tok * p.v_st + it.head * p.v_sh, ROW_BYTES, ibar);
-    bulk_g2s(dst + 3 * D, p.g + tok * p.g_st + it.head * p.g_sh, ROW_BYTES, ibar);
+    const __nv_bfloat16* src;
+    if (which == 0) src = p.q + tok * p.q_st + hq * p.q_sh;
+    else if (which == 1) src = p.k + tok * p.k_st + hq * p.k_sh;
+    else if (which == 2) src = p.v + tok * p.v_st + it.head * p.v_sh;
+    else src = p.g + tok * p.g_st + it.head * p.g_sh;
+    bulk_g2s(ibuf + (t * 4 + which) * D, src, ROW_BYTES, ibar);
   }
 }
 
+// Token ``t = warp``'s scalars, loaded a step before their use: beta (lane 0),
+// dt_bias for the lane's 4 channels and A_log of the head.
+struct TokenScalars {
+  float4 dt;
+  float alog;
+  __nv_bfloat16 beta;
+};
+__device__ __forceinline__ TokenScalars load_token_scalars(const WindowParams& p, const ItemInfo& it, int t,
+                                                           int lane) {
+  TokenScalars r;
+  r.dt = make_float4(0.f, 0.f, 0.f, 0.f);
+  r.alog = 0.f;
+  r.beta = __float2bfloat16(0.f);
+  if (it.work && t < it.qlen) {
+    if (p.has_gate) {
+      r.dt = *reinterpret_cast<const float4*>(p.dt_bias + it.head * D + 4 * lane);
+      r.alog = p.A_log[it.head];
+    }
+    r.beta = p.beta[(it.qs + t) * p.b_st + it.head * p.b_sh];
+  }
+  return r;
+}
+
 // Token t's per-channel vectors, computed by one warp (lane = 4 channels).
-__device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s, int h,
-                                              const __nv_bfloat16* rowp, int64_t tok, int t,
-                                              int lane) {
+__device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s, const TokenScalars& ts,
+                                              const __nv_bfloat16* rowp, int t, int lane) {
   float qv[4], kv[4], gv[4];
   load_bf16x4(rowp + 0 * D + 4 * lane, qv);
   load_bf16x4(rowp + 1 * D + 4 * lane, kv);
@@ -104,10 +137,8 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
   const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
   const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
   const float rq = rsqrtf(sq + 1e-6f) * p.scale, rk = rsqrtf(sk + 1e-6f);
-  const float a = p.has_gate ? __expf(p.A_log[h]) : 0.f;
-  float4 dtb = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (p.has_gate) dtb = *reinterpret_cast<const float4*>(p.dt_bias + h * D + 4 * lane);
-  const float dt[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
+  const float a = p.has_gate ? __expf(ts.alog) : 0.f;
+  const float dt[4] = {ts.dt.x, ts.dt.y, ts.dt.z, ts.dt.w};
   float kh[4], dec[4], pk[4], pq[4], kq = 0.f;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -126,7 +157,7 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
   *reinterpret_cast<float4*>(&s.tkh[t][4 * lane]) = make_float4(kh[0], kh[1], kh[2], kh[3]);
   if (lane == 0) {
     s.tkq[t] = kq;
-    s.tbeta[t] = sigmoidf_(bf2f(p.beta[tok * p.b_st + h * p.b_sh]));
+    s.tbeta[t] = sigmoidf_(bf2f(ts.beta));
   }
 }
 
@@ -236,23 +267,26 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
   int nxt = s.next;
   __syncthreads();
 
-  if (tid == 0) {
+  if (warp == 0) {
     const int its[2] = {cur, nxt};
     for (int b = 0; b < 2; ++b) {
       if (its[b] < items) {
         const ItemInfo ii = item_info(p, its[b]);
         if (ii.work) {
-          issue_state(p, ii, s.state[b], &s.sbar[b]);
-          issue_inputs(p, ii, s.in[b], &s.ibar[b]);
+          if (lane == 0) issue_state(p, ii, s.state[b], &s.sbar[b]);
+          issue_inputs(p, ii, s.in[b], &s.ibar[b], lane);
         }
       }
     }
   }
+  ItemInfo it = cur < items ? item_info(p, cur) : ItemInfo{};
+  ItemInfo itn = nxt < items ? item_info(p, nxt) : ItemInfo{};
+  TokenScalars ts = load_token_scalars(p, it, warp, lane);
   uint32_t sphase[2] = {0u, 0u}, iphase[2] = {0u, 0u};
   int b = 0;
+  bool stored = false;  // a bulk state store is in flight from sout
   while (cur < items) {
     if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
-    const ItemInfo it = item_info(p, cur);
     bool ok = true;
     float2 S[8][2];
     if (it.work) {
@@ -261,8 +295,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       sphase[b] ^= 1u;
       iphase[b] ^= 1u;
       if (ok) {
-        if (warp < it.qlen)
-          token_vectors(p, s, it.head, s.in[b] + warp * 4 * D, it.qs + warp, warp, lane);
+        if (warp < it.qlen) token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 x4 = *reinterpret_cast<const float4*>(s.state[b] + (8 * warp + i) * D + 4 * lane);
@@ -274,24 +307,32 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
     // state buffer b read, token vectors written, the next ticket published
     if (__syncthreads_or(!ok)) {
       // a copy never landed (error word set): wait, bounded, for the copies
-      // still in flight into the other buffer before leaving
+      // still in flight into the other buffer, and for the last state store,
+      // before leaving
       if (tid == 0 && nxt < items && item_info(p, nxt).work) {
         mbar_wait_bounded(&s.sbar[b ^ 1], sphase[b ^ 1], p.err);
         mbar_wait_bounded(&s.ibar[b ^ 1], iphase[b ^ 1], p.err);
       }
+      if (!VERIFY && tid == 0) bulk_wait<0>();
       return;
     }
     const int nn = s.next;
     const ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
     if (tid == 0 && nn < items && it2.work) issue_state(p, it2, s.state[b], &s.sbar[b]);
+    // the next item's scalars, used a step from now
+    const TokenScalars ts_next = load_token_scalars(p, itn, warp, lane);
     if (it.work) {
       run_tokens<VERIFY>(p, s, it, S, s.in[b], warp, lane);
       if (!VERIFY) {
-        float* dst = p.pool + it.slot * p.slot_stride + (int64_t)it.head * D * D;
+        // the previous item's bulk store has read sout by now (a whole item
+        // ago); confirm it before anyone overwrites sout
+        if (tid == 0 && stored) bulk_wait_read<0>();
+        __syncthreads();
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(dst + (8 * warp + i) * D + 4 * lane) =
+          *reinterpret_cast<float4*>(s.sout + (8 * warp + i) * D + 4 * lane) =
               make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
+        fence_proxy_async_smem();
       }
     } else if (it.zero) {
       for (int e = tid; e < it.qlen * D; e += WIN_THREADS) {
@@ -300,12 +341,23 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       }
     }
     if (tid == 0 && it.bad) set_error(p.err, ERR_INDEX);
-    __syncthreads();  // input buffer b and the token vectors consumed
-    if (tid == 0 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b]);
+    __syncthreads();  // input buffer b and the token vectors consumed, sout written
+    if (!VERIFY && tid == 0 && it.work) {
+      float* dst = p.pool + it.slot * p.slot_stride + (int64_t)it.head * D * D;
+      bulk_s2g(dst, s.sout, STATE_BYTES / 2);
+      bulk_s2g(dst + D * D / 2, s.sout + D * D / 2, STATE_BYTES / 2);
+      bulk_commit();
+      stored = true;
+    }
+    if (warp == 1 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane);
+    ts = ts_next;
     cur = nxt;
     nxt = nn;
+    it = itn;
+    itn = it2;
     b ^= 1;
   }
+  if (!VERIFY && tid == 0) bulk_wait<0>();  // the last state store has landed
 }
 
 // Host-side launcher (called from the API layer after validation).
