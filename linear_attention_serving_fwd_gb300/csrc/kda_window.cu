@@ -14,13 +14,14 @@
 //  * per item, warp t < qlen first turns token t's raw rows into the vectors
 //    every warp needs (L2-normalised k^ and q~, exp(gate), their products)
 //    in shared memory, once;
-//  * warp w owns state rows v = 8w..8w+7 (rows of S^T), lane L owns key
-//    channels 4L..4L+3, so a warp reads 512-byte rows (bank-conflict free)
-//    and the state lives in 32 registers per thread;
-//  * per token, the 16 row dot products of a warp (with exp(gate) * k^ and
-//    with exp(gate) * q~) are reduced by one recursive-halving
-//    reduce-scatter, after which lane pairs hold one row's correction U or
-//    output; products use packed fp32x2 FMAs.
+//  * warp w owns state rows v = 8w..8w+7 (rows of S^T); each half warp
+//    holds four of them and lane L key channels 8 (L % 16)..+7, so the state
+//    lives in 32 registers per thread and a row's dot products reduce over
+//    16 lanes;
+//  * per token, the 8 dot products of a half warp (its rows with
+//    exp(gate) * k^ and with exp(gate) * q~) are reduced by one
+//    recursive-halving reduce-scatter, after which lane pairs hold one row's
+//    correction U or output; products use packed fp32x2 FMAs.
 // Token order inside the window follows the recurrence exactly:
 //   S <- diag(e^gate) S;  U = beta (v - S^T k^);  S <- S + k^ U^T;  o = S^T q~
 // computed as U = beta (v - S_old^T (e^gate * k^)),
@@ -161,49 +162,59 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
   }
 }
 
+// Thread (warp w, lane L) holds state rows v = 8w + 4 (L / 16) + i, i < 4,
+// at key channels 4 (L % 16) + 64 j .. + 3, j < 2, as float2 pairs S[i][jj]
+// (jj = 2 j, 2 j + 1): each row's dot products reduce over the 16 lanes of
+// a half warp, and a half warp's 16-byte accesses to a row are contiguous.
+__device__ __forceinline__ int win_row(int warp, int lane, int i) { return 8 * warp + 4 * (lane >> 4) + i; }
+__device__ __forceinline__ int win_chan(int lane, int j) { return 4 * (lane & 15) + 64 * j; }
+
 template <bool VERIFY>
 __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, const ItemInfo& it,
-                                           float2 (&S)[8][2], const __nv_bfloat16* ibuf, int warp,
+                                           float2 (&S)[4][4], const __nv_bfloat16* ibuf, int warp,
                                            int lane) {
   const int h = it.head;
-  const int ri = (lane >> 1) & 7;  // this lane pair's row within the warp
-  const int vrow = 8 * warp + ri;
+  const int m = (lane & 15) >> 1;            // the value this lane pair ends with
+  const int my_row = win_row(warp, lane, m & 3);
   for (int t = 0; t < it.qlen; ++t) {
     const int64_t tok = it.qs + t;
-    const float4 p4 = *reinterpret_cast<const float4*>(&s.tp[t][4 * lane]);
-    const float4 r4 = *reinterpret_cast<const float4*>(&s.tr[t][4 * lane]);
-    const float4 d4 = *reinterpret_cast<const float4*>(&s.tdec[t][4 * lane]);
-    const float4 k4 = *reinterpret_cast<const float4*>(&s.tkh[t][4 * lane]);
+    float2 pv[4], rv[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float4 p4 = *reinterpret_cast<const float4*>(&s.tp[t][win_chan(lane, j)]);
+      const float4 r4 = *reinterpret_cast<const float4*>(&s.tr[t][win_chan(lane, j)]);
+      pv[2 * j] = make_float2(p4.x, p4.y);
+      pv[2 * j + 1] = make_float2(p4.z, p4.w);
+      rv[2 * j] = make_float2(r4.x, r4.y);
+      rv[2 * j + 1] = make_float2(r4.z, r4.w);
+    }
     const float beta = s.tbeta[t], kq = s.tkq[t];
-    const float vval = bf2f(ibuf[t * 4 * D + 2 * D + vrow]);
-    const float2 p01 = make_float2(p4.x, p4.y), p23 = make_float2(p4.z, p4.w);
-    const float2 r01 = make_float2(r4.x, r4.y), r23 = make_float2(r4.z, r4.w);
-    float x[16];
+    // x[i]: row i . (e^gate k^), x[4 + i]: row i . (e^gate q~), over this lane's 8 channels
+    float x[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 a = ffma2(S[i][1], p23, fmul2(S[i][0], p01));
-      const float2 b = ffma2(S[i][1], r23, fmul2(S[i][0], r01));
+    for (int i = 0; i < 4; ++i) {
+      float2 a = fmul2(S[i][0], pv[0]), bq = fmul2(S[i][0], rv[0]);
+#pragma unroll
+      for (int jj = 1; jj < 4; ++jj) {
+        a = ffma2(S[i][jj], pv[jj], a);
+        bq = ffma2(S[i][jj], rv[jj], bq);
+      }
       x[i] = a.x + a.y;
-      x[8 + i] = b.x + b.y;
+      x[4 + i] = bq.x + bq.y;
     }
-    // reduce-scatter of 16 sums over 32 lanes: lane L ends with index L >> 1
+    // reduce-scatter of 8 sums over the half warp's 16 lanes: lane pair
+    // (2 m, 2 m + 1) of the half ends with value m
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const bool up = (lane & 16) != 0;
-      const float send = up ? x[m] : x[m + 8], keep = up ? x[m + 8] : x[m];
-      x[m] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int q = 0; q < 4; ++q) {
       const bool up = (lane & 8) != 0;
-      const float send = up ? x[m] : x[m + 4], keep = up ? x[m + 4] : x[m];
-      x[m] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      const float send = up ? x[q] : x[q + 4], keep = up ? x[q + 4] : x[q];
+      x[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
     }
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
+    for (int q = 0; q < 2; ++q) {
       const bool up = (lane & 4) != 0;
-      const float send = up ? x[m] : x[m + 2], keep = up ? x[m + 2] : x[m];
-      x[m] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      const float send = up ? x[q] : x[q + 2], keep = up ? x[q + 2] : x[q];
+      x[q] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
     }
     {
       const bool up = (lane & 2) != 0;
@@ -211,13 +222,15 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
       x[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
     }
     const float mine = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
-    const float U = beta * (vval - mine);  // meaningful on lanes 0..15
-    const float Urow = __shfl_sync(0xffffffffu, U, lane & 15);
-    if (lane >= 16) {
-      if ((lane & 1) == 0)
-        p.out[(tok * p.hv + h) * D + vrow] = __float2bfloat16_rn(mine + Urow * kq);
+    // lanes with m < 4: U of row m; lanes with m >= 4: the output of row m - 4
+    const float vval = bf2f(ibuf[t * 4 * D + 2 * D + my_row]);
+    const float U = beta * (vval - mine);
+    const int half = lane & 16;
+    const float Urow = __shfl_sync(0xffffffffu, U, half | (2 * (m & 3)));
+    if (m >= 4) {
+      if ((lane & 1) == 0) p.out[(tok * p.hv + h) * D + my_row] = __float2bfloat16_rn(mine + Urow * kq);
     } else if (VERIFY && (lane & 1) == 0) {
-      p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + vrow] = U;
+      p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + my_row] = U;
     }
     if (VERIFY && warp == 0) {
       __nv_bfloat16* dst = p.kg + (((int64_t)it.request * p.hv + h) * p.window + t) * 2 * D;
@@ -225,14 +238,22 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
       *reinterpret_cast<uint2*>(dst + 4 * lane) = *reinterpret_cast<const uint2*>(rowp + 1 * D + 4 * lane);
       *reinterpret_cast<uint2*>(dst + D + 4 * lane) = *reinterpret_cast<const uint2*>(rowp + 3 * D + 4 * lane);
     }
-    const float2 d01 = make_float2(d4.x, d4.y), d23 = make_float2(d4.z, d4.w);
-    const float2 k01 = make_float2(k4.x, k4.y), k23 = make_float2(k4.z, k4.w);
+    float2 dv[4], kv[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float Ui = __shfl_sync(0xffffffffu, U, 2 * i);
+    for (int j = 0; j < 2; ++j) {
+      const float4 d4 = *reinterpret_cast<const float4*>(&s.tdec[t][win_chan(lane, j)]);
+      const float4 k4 = *reinterpret_cast<const float4*>(&s.tkh[t][win_chan(lane, j)]);
+      dv[2 * j] = make_float2(d4.x, d4.y);
+      dv[2 * j + 1] = make_float2(d4.z, d4.w);
+      kv[2 * j] = make_float2(k4.x, k4.y);
+      kv[2 * j + 1] = make_float2(k4.z, k4.w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float Ui = __shfl_sync(0xffffffffu, U, half | (2 * i));
       const float2 uu = make_float2(Ui, Ui);
-      S[i][0] = ffma2(S[i][0], d01, fmul2(k01, uu));
-      S[i][1] = ffma2(S[i][1], d23, fmul2(k23, uu));
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) S[i][jj] = ffma2(S[i][jj], dv[jj], fmul2(kv[jj], uu));
     }
   }
 }
@@ -288,7 +309,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
   while (cur < items) {
     if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
     bool ok = true;
-    float2 S[8][2];
+    float2 S[4][4];
     if (it.work) {
       ok = mbar_wait_bounded(&s.sbar[b], sphase[b], p.err);
       ok = mbar_wait_bounded(&s.ibar[b], iphase[b], p.err) && ok;
@@ -297,11 +318,14 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       if (ok) {
         if (warp < it.qlen) token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 x4 = *reinterpret_cast<const float4*>(s.state[b] + (8 * warp + i) * D + 4 * lane);
-          S[i][0] = make_float2(x4.x, x4.y);
-          S[i][1] = make_float2(x4.z, x4.w);
-        }
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float4 x4 = *reinterpret_cast<const float4*>(s.state[b] + win_row(warp, lane, i) * D +
+                                                               win_chan(lane, j));
+            S[i][2 * j] = make_float2(x4.x, x4.y);
+            S[i][2 * j + 1] = make_float2(x4.z, x4.w);
+          }
       }
     }
     // state buffer b read, token vectors written, the next ticket published
@@ -329,9 +353,11 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
         if (tid == 0 && stored) bulk_wait_read<0>();
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          *reinterpret_cast<float4*>(s.sout + (8 * warp + i) * D + 4 * lane) =
-              make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<float4*>(s.sout + win_row(warp, lane, i) * D + win_chan(lane, j)) =
+                make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y);
         fence_proxy_async_smem();
       }
     } else if (it.zero) {
