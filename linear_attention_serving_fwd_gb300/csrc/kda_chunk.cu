@@ -34,8 +34,8 @@
 //   e^{Lam_r - Lam_i} = (e^{Lam_r - m_R}) (e^{m_R - Lam_i})      (i <= 16 R + 15)
 // The first factor stays within e^{+-84} as long as any 8 consecutive gates
 // sum above -84 (lower_bound >= -10.5); the second is at most e^{84} and
-// below 1 for every i before the middle row.  Kg, qg and kg are products of
-// factors chained so that every partial product is at most |k^| or |q~|.
+// below 1 for every i before the middle row.  Kg, qg and kg take their
+// exponentials directly (e^{Lam_i}, e^{Lam_C - Lam_i}, both at most 1).
 #include <cuda.h>  // CUtensorMap (types only; the encoder comes via the runtime)
 #include <cudaTypedefs.h>
 
@@ -349,11 +349,10 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
     }
     __syncthreads();
-    float mR, sR;  // Lam at rows 16 Rq + 7 and 16 Rq - 1 (0 before the chunk)
+    float mR;  // Lam at row 16 Rq + 7
     {
       float off = 0.f;
       for (int R2 = 0; R2 < Rq; ++R2) off += s.qtot[R2][c];
-      sR = off;
 #pragma unroll
       for (int i = 0; i < 16; ++i) lam[i] += off;
       mR = lam[7];
@@ -375,11 +374,6 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       float F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
 #pragma unroll
       for (int R2 = 0; R2 < 4; ++R2) F[R2] = R2 > Rq ? __expf(s.ref[R2][c] - mR) : 1.f;
-      // Kg = ((k^ E) e^{m - sR}) e^{sR} = k^ e^{Lam}; kg = ((k^ / E) e^{eR - m}) e^{Lam_C - eR}
-      // with eR = Lam at row 16 Rq + 15: each partial product is at most |k^|,
-      // so none overflows and one underflows only where the result is below e^{-87}
-      const float Pm = __expf(mR - sR), Qs = __expf(sR);
-      const float He = __expf(lam[15] - mR), Jc = __expf(lamC - lam[15]);
       // normalised keys and queries (the row norms are the warp's: 16-byte
       // broadcasts)
 #pragma unroll
@@ -389,8 +383,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         kv[i4] *= r4.x; kv[i4 + 1] *= r4.y; kv[i4 + 2] *= r4.z; kv[i4 + 3] *= r4.w;
         qv[i4] *= q4.x; qv[i4 + 1] *= q4.y; qv[i4 + 2] *= q4.z; qv[i4 + 3] *= q4.w;
       }
-      uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
-      // rows in pairs: packed fp32x2 products
+      // X and Y first (rows in pairs, packed fp32x2 products): the A_kk /
+      // A_qk product starts on them while the B3 / KG operands are built
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
         const int r = 16 * Rq + i;
@@ -399,9 +393,6 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         const float2 iE = make_float2(__expf(mR - lam[i]), __expf(mR - lam[i + 1]));
         const float2 kh = make_float2(kv[i], kv[i + 1]), qh = make_float2(qv[i], qv[i + 1]);
         const float2 xk = fmul2(kh, E), xq = fmul2(qh, E), y = fmul2(kh, iE);
-        const float2 kg2 = fmul2(fmul2(y, make_float2(He, He)), make_float2(Jc, Jc));
-        const float2 Kg2 = fmul2(fmul2(xk, make_float2(Pm, Pm)), make_float2(Qs, Qs));
-        const float2 qg2 = fmul2(fmul2(xq, make_float2(Pm, Pm)), make_float2(Qs, Qs));
         *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk.x);
         *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r + 1, c, 128)) = tc::to_tf32(xk.y);
         *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq.x);
@@ -415,6 +406,26 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
             *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r + 1, c, YROWS)) =
                 tc::to_tf32(yf.y);
           }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+
+      // ---- phase 2: A_kk / A_qk, one kind::tf32 product (N = 160) ------------
+      if (tid == 0) {
+        tc::mma_kloop_tf32_sw128(tmem, smem_u32(s.XY), smem_u32(s.XY + 65536), 128, YROWS, 128, false);
+        tc::mma_commit(&s.bar);
+      }
+      // meanwhile: Kg = k^ e^{Lam}, qg = q~ e^{Lam}, kg = k^ e^{Lam_C - Lam}
+      // (each factor at most 1: an underflow only drops a term below e^{-87})
+      uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        const float2 eL = make_float2(__expf(lam[i]), __expf(lam[i + 1]));
+        const float2 eC = make_float2(__expf(lamC - lam[i]), __expf(lamC - lam[i + 1]));
+        const float2 kh = make_float2(kv[i], kv[i + 1]), qh = make_float2(qv[i], qv[i + 1]);
+        const float2 Kg2 = fmul2(kh, eL), qg2 = fmul2(qh, eL), kg2 = fmul2(kh, eC);
         kgw[i >> 1] = pack_half2(kg2.x, kg2.y);
         Kgx[i >> 1] = pack_half2(Kg2.x, Kg2.y);
         qgx[i >> 1] = pack_half2(qg2.x, qg2.y);
@@ -430,16 +441,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         *reinterpret_cast<uint4*>(s.KG + tc::kmajor_offset(c, r0, 128)) =
             make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
       }
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    // ---- phase 2: A_kk / A_qk, one kind::tf32 product (N = 160) --------------
-    if (tid == 0) {
-      tc::mma_kloop_tf32_sw128(tmem, smem_u32(s.XY), smem_u32(s.XY + 65536), 128, YROWS, 128, false);
-      tc::mma_commit(&s.bar);
+      fence_proxy_async_smem();
     }
     const bool has_next = t + (int)gridDim.x < n_items;
     if (tid == 32 && has_next) s.meta[cur ^ 1] = item_meta(p, t + gridDim.x);
