@@ -44,8 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,verify,varlen,long",
-                    help="comma list of extra workloads: decode, verify, varlen, long")
+    ap.add_argument("--extras", default="decode,verify,commit,varlen,long",
+                    help="comma list of extra workloads: decode, verify, commit, varlen, long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -354,7 +354,7 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
     # decode / verify on the 256-request batch, H=32, 512-slot pool
     want = set(args.extras.split(","))
     for window in (1, 4):
-        if not ({"decode", "verify"} & want):
+        if not ({"decode", "verify", "commit"} & want):
             break
         y = W.workload("decode", window=window, seed=rank, device="cuda")
         pool = y.state_pool
@@ -396,6 +396,31 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                                      else None,
                                      "peak_source": f"{pk['src']} HBM copy bandwidth"},
                         "workload": f"256 requests x window {window}, Hqk=Hv=32, 512-slot fp32 pool"}
+        if "commit" in want and window == 4:
+            # rebuild every request's state after all 4 verified tokens from
+            # verify's records, in place: 64 KB in + 64 KB out per item
+            kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, window,
+                           A_log=y.A_log, dt_bias=y.dt_bias, out=out, corr=corr, kg=kg,
+                           work_counter=counter)
+            acc = torch.full((y.n_seqs,), window, dtype=torch.int32, device="cuda")
+
+            def fc():
+                kda.kda_commit(pool, y.state_indices, acc, corr, kg, window, A_log=y.A_log,
+                               dt_bias=y.dt_bias, lower_bound=y.lower_bound)
+            for _ in range(3):
+                fc()
+            secs = reduce_max(time_device(torch, fc, steps, flush, barrier))
+            items = y.n_seqs * y.hv
+            t = secs / steps
+            nbytes = items * (2 * sb + window * (4 * D + 4 * D))
+            gbs = nbytes / t / 1e9
+            res["commit_q4"] = {"requests_per_s": round(y.n_seqs * world / t, 1),
+                                "ms_per_step": round(t * 1e3, 4),
+                                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                                             "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                                             "traffic": None,
+                                             "peak_source": f"{pk['src']} HBM copy bandwidth"},
+                                "workload": "256 requests x 4 accepted tokens, Hv=32, 512-slot fp32 pool"}
         del y, pool
     # varlen paged and long-context prefill
     for name in ("varlen", "long"):

@@ -201,6 +201,37 @@ int kda_verify(const kda_activations* x, void* out, const float* state_pool,
                const int32_t* slots, int32_t n_req, int32_t window, float* corr,
                void* kg, int32_t* work_counter, void* stream);
 
+/*
+ * kda_commit - speculative-decode commit: rebuild each request's state after
+ * its accepted prefix from the records kda_verify wrote, in place.  The
+ * vLLM kimi_k3 verify page (KdaTcVerify) writes the corr and kg records so
+ * that the accepted prefix's state can be rebuilt; with tokens t = 1..a of
+ * request b accepted, the recurrence unrolls to
+ *   S_a = diag(e^{L_a}) S_0 + sum_{t <= a} diag(e^{L_a - L_t}) k^_t U_t^T
+ * (L_t the per-channel cumsum of gate_t, k^_t = k_t / sqrt(|k_t|^2 + 1e-6)).
+ *   state_pool, slot_stride, n_slots : the pool kda_verify read (fp32
+ *                  V-first rows, as in kda_decode); row slots[b] holds S_0
+ *                  on entry and S_a on return
+ *   slots          device int32[n_req]; negative = padding (skipped); a slot
+ *                  >= n_slots sets KDA_ERR_DEVICE_INDEX and is skipped
+ *   num_accepted   device int32[n_req], a in [0, window]; a = 0 leaves the
+ *                  row untouched; a outside the range sets
+ *                  KDA_ERR_DEVICE_INDEX and is skipped.  a must not exceed
+ *                  the request's verified token count (records past it are
+ *                  not defined).
+ *   hv, window     value heads and the window kda_verify ran with
+ *   corr, kg       kda_verify's records [n_req, hv, window, 128] fp32 and
+ *                  [n_req, hv, window, 256] bf16, 16-byte aligned
+ *   A_log, dt_bias, lower_bound : the gate parameters kda_verify used (both
+ *                  NULL: raw g is the log decay)
+ *   stream         cudaStream_t
+ * Returns KDA_OK or an error status; nothing is allocated.
+ */
+int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const int32_t* slots,
+               const int32_t* num_accepted, int32_t n_req, int32_t hv, int32_t window,
+               const float* corr, const void* kg, const float* A_log, const float* dt_bias,
+               float lower_bound, void* stream);
+
 /* Thread-local text of the last error returned on this thread ("" if none). */
 const char* kda_last_error(void);
 

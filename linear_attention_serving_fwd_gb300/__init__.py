@@ -22,7 +22,7 @@ from . import _native
 from ._native import KdaError
 
 D = 128
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode", "kda_verify",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode", "kda_verify", "kda_commit",
            "kda_device_status", "chunk_workspace_bytes", "KdaError", "library_path"]
 
 
@@ -241,6 +241,39 @@ def kda_verify(q, k, v, g, beta, state_pool, query_start, slots, window, *, A_lo
     return _window_call(True, q, k, v, g, beta, state_pool, query_start, slots, window,
                         A_log=A_log, dt_bias=dt_bias, scale=scale, lower_bound=lower_bound,
                         out=out, corr=corr, kg=kg, work_counter=work_counter, stream=stream)
+
+
+def kda_commit(state_pool, slots, num_accepted, corr, kg, window, *, A_log=None, dt_bias=None,
+               lower_bound=-5.0, stream=None):
+    """Speculative-decode commit: rebuild pool rows slots[b] in place as the
+    state after request b's first num_accepted[b] verified tokens, from the
+    corr / kg records of :func:`kda_verify` (same pool, window and gate
+    parameters).  Returns the pool."""
+    if slots.dtype != torch.int32 or num_accepted.dtype != torch.int32:
+        raise TypeError("slots and num_accepted must have dtype torch.int32.")
+    if state_pool.dtype != torch.float32:
+        raise TypeError("state_pool must be float32.")
+    hv = state_pool.shape[1]
+    if tuple(state_pool.shape[1:]) != (hv, D, D) or state_pool[0].stride() != (D * D, D, 1):
+        raise ValueError("state_pool must be [slots, Hv, 128, 128] with contiguous rows.")
+    n_req = slots.numel()
+    if num_accepted.numel() != n_req:
+        raise ValueError("num_accepted must have one entry per request.")
+    if tuple(corr.shape) != (n_req, hv, window, D) or corr.dtype != torch.float32 or not corr.is_contiguous():
+        raise ValueError("corr must be a contiguous float32 [n_req, Hv, window, 128] tensor.")
+    if tuple(kg.shape) != (n_req, hv, window, 2 * D) or kg.dtype != torch.bfloat16 or not kg.is_contiguous():
+        raise ValueError("kg must be a contiguous bfloat16 [n_req, Hv, window, 256] tensor.")
+    keep = []
+    if A_log is not None:
+        A_log = A_log.detach().float().contiguous()
+        dt_bias = dt_bias.detach().float().contiguous()
+        keep = [A_log, dt_bias]
+    rc = _native.lib().kda_commit(_ptr(state_pool), state_pool.stride(0), state_pool.shape[0], _ptr(slots),
+                                  _ptr(num_accepted), n_req, hv, window, _ptr(corr), _ptr(kg),
+                                  _ptr(A_log), _ptr(dt_bias), float(lower_bound), _stream_handle(stream))
+    _native.check(rc)
+    del keep
+    return state_pool
 
 
 def kda_device_status(stream=None, clear: bool = True) -> int:

@@ -360,6 +360,44 @@ int kda_verify(const kda_activations* x, void* out, const float* state_pool, int
                        window, true, corr, kg, work_counter, stream);
 }
 
+int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const int32_t* slots,
+               const int32_t* num_accepted, int32_t n_req, int32_t hv, int32_t window,
+               const float* corr, const void* kg, const float* A_log, const float* dt_bias,
+               float lower_bound, void* stream) {
+  if (window < 1 || window > kda::MAX_WINDOW)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "window must satisfy 1 <= window <= 8 (got %d).", window);
+  if (n_req < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_req must be >= 0.");
+  if (hv <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "hv must be positive (got %d).", hv);
+  if (n_req == 0) return ok();
+  if (!slots || !num_accepted)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "slots and num_accepted must not be NULL.");
+  if (!corr || !kg) return fail(KDA_ERR_INVALID_ARGUMENT, "corr and kg must not be NULL.");
+  if (!aligned16(corr) || !aligned16(kg))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "corr and kg must be 16-byte aligned.");
+  if ((A_log == nullptr) != (dt_bias == nullptr))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "A_log and dt_bias must be provided together.");
+  if (A_log && !aligned16(dt_bias)) return fail(KDA_ERR_INVALID_ARGUMENT, "dt_bias must be 16-byte aligned.");
+  if (A_log && !(lower_bound <= 0.f && lower_bound >= -10.5f))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "lower_bound must lie in [-10.5, 0] (got %g).", (double)lower_bound);
+  int rc = check_pool(state_pool, slot_stride, n_slots, hv, "state_pool");
+  if (rc) return rc;
+  if ((int64_t)n_req * hv > 0x7fffffff)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "n_req * Hv exceeds 2^31.");
+  unsigned* err = error_word_ptr();
+  if (!err) return fail(KDA_ERR_CUDA, "cannot resolve the device error word.");
+  kda::CommitParams p;
+  memset(&p, 0, sizeof(p));
+  p.pool = state_pool; p.slot_stride = slot_stride; p.n_slots = n_slots;
+  p.slots = slots; p.accepted = num_accepted;
+  p.corr = corr; p.kg = static_cast<const __nv_bfloat16*>(kg);
+  p.A_log = A_log; p.dt_bias = dt_bias; p.lower_bound = lower_bound; p.has_gate = A_log != nullptr;
+  p.n_req = n_req; p.hv = hv; p.window = window;
+  p.err = err;
+  if (kda::launch_commit(p, static_cast<cudaStream_t>(stream)) != 0)
+    return cuda_fail(cudaGetLastError(), "kda_commit launch");
+  return ok();
+}
+
 int kda_device_status(void* stream, int32_t clear) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kda_device_status sync");

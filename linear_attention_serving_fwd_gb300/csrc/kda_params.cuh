@@ -25,6 +25,21 @@ struct WindowParams {
   unsigned* err;        // device error word
 };
 
+struct CommitParams {
+  float* pool;                 // [n_slots, Hv, 128, 128] fp32, rewritten in place
+  int64_t slot_stride, n_slots;
+  const int32_t* slots;        // [n_req]
+  const int32_t* accepted;     // [n_req] accepted prefix length a
+  const float* corr;           // [n_req, Hv, window, 128] U_t from kda_verify
+  const __nv_bfloat16* kg;     // [n_req, Hv, window, 256] raw k_t, raw g_t from kda_verify
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound;
+  int has_gate;
+  int n_req, hv, window;
+  unsigned* err;
+};
+
 struct ChunkParams {
   const __nv_bfloat16 *q, *k, *v, *g, *beta;
   int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh, g_st, g_sh, b_st, b_sh;
@@ -68,6 +83,7 @@ void set_last_error(int code, const char* msg);
 
 // Launchers (kernels' translation units); return 0 or -1 (see cudaGetLastError).
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream);
+int launch_commit(const CommitParams& p, cudaStream_t stream);
 size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out);
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream);
 

@@ -48,6 +48,31 @@ def activations(q, k, g, beta, A_log_h, dt_bias_h, scale, lower_bound, l2norm=Tr
     return scale * qh, kh, gate, _sig(np.asarray(beta, np.float64))
 
 
+def commit_from_records(S0, kg_raw, corr, A_log_h, dt_bias_h, lower_bound):
+    """The state after an accepted prefix, rebuilt from speculative verify's
+    records (the vLLM kimi_k3 verify page writes corr = U_t and kg = raw k_t,
+    raw g_t so that it can be rebuilt).  Unrolling S_t = diag(e^{gate_t})
+    S_{t-1} + k^_t U_t^T over the accepted tokens t = 1..a gives
+
+        S_a = diag(e^{L_a}) S_0 + sum_{t <= a} diag(e^{L_a - L_t}) k^_t U_t^T
+
+    with L_t the per-channel cumsum of the gates.  S0 is V-first [V, K];
+    kg_raw [a, 2K] (raw k, raw g); corr [a, V].  Returns the V-first S_a."""
+    kg_raw = np.asarray(kg_raw, np.float64)
+    corr = np.asarray(corr, np.float64)
+    a = corr.shape[0]
+    S = np.asarray(S0, np.float64).T.copy()  # K x V
+    if a == 0:
+        return S.T
+    k, g = kg_raw[:, :D], kg_raw[:, D:]
+    _, kh, gate, _ = activations(k, k, g, np.zeros(a), A_log_h, dt_bias_h, 1.0, lower_bound)
+    L = np.cumsum(gate, axis=0)                        # [a, K]
+    S *= np.exp(L[-1])[:, None]
+    for t in range(a):
+        S += np.outer(np.exp(L[-1] - L[t]) * kh[t], corr[t])
+    return S.T
+
+
 def chunk_operands(qh, kh, gate, b):
     """Intra-chunk quantities for one chunk (rows beyond the chunk absent)."""
     C = kh.shape[0]

@@ -150,3 +150,29 @@ def test_valid_call_without_gpu_reports_cuda_error():
     except ImportError:
         pass
     assert _window(_acts(), False) == CUDA
+
+
+def _commit(**kw):
+    lib = _native.lib()
+    args = dict(pool=FAKE, stride=4 * 16384, slots=8, sl=FAKE, acc=FAKE, n=2, hv=4, win=4, corr=FAKE,
+                kg=FAKE, A_log=FAKE, dt=FAKE, lb=-5.0, stream=None)
+    args.update(kw)
+    return lib.kda_commit(args["pool"], args["stride"] * args["hv"], args["slots"], args["sl"], args["acc"], args["n"], args["hv"], args["win"],
+                          args["corr"], args["kg"], args["A_log"], args["dt"], ctypes.c_float(args["lb"]),
+                          args["stream"])
+
+
+def test_commit_validation():
+    assert _commit(win=0) == INVALID and "window" in _msg()
+    assert _commit(win=9) == INVALID and "window" in _msg()
+    assert _commit(n=-1) == INVALID
+    assert _commit(n=0) == 0  # nothing to do
+    assert _commit(hv=0) == INVALID and "hv" in _msg()
+    assert _commit(sl=None) == INVALID and "must not be NULL" in _msg()
+    assert _commit(acc=None) == INVALID and "must not be NULL" in _msg()
+    assert _commit(corr=None) == INVALID and "corr and kg" in _msg()
+    assert _commit(kg=FAKE + 8) == INVALID and "16-byte aligned" in _msg()
+    assert _commit(A_log=None) == INVALID and "provided together" in _msg()
+    assert _commit(lb=-11.0) == INVALID and "lower_bound" in _msg()
+    assert _commit(pool=None) == INVALID and "state_pool" in _msg()
+    assert _commit(slots=0) == INVALID and "at least one slot" in _msg()

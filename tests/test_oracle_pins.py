@@ -279,3 +279,34 @@ def test_no_gate_params_uses_g_directly():
     res = oracle.recurrence(q, k, v, g, b, [0, 3], h0=h0)
     np.testing.assert_allclose(res["state"][0, 0], np.exp(g.double().sum(0)[0].numpy())[None, :]
                                * np.ones((D, 1)), rtol=1e-13)
+
+
+@pytest.mark.parametrize("gated", [True, False])
+def test_commit_from_records_equals_prefix_recurrence(gated):
+    """Rebuilding the state after an accepted prefix from verify's records
+    (corr = U_t, raw k_t, raw g_t) equals the recurrence run on the first a
+    tokens alone, for every a = 0..qlen (GVA: v-head h reads the raw k of
+    its q/k head)."""
+    x = W.decode_batch(3, 5, 1, 2, slots=6, seed=13, qlens=[5, 3, 4], lower_bound=-0.8,
+                       g_shift=0.0 if gated else -3.0)
+    if not gated:
+        x.A_log, x.dt_bias = None, None
+    res = oracle.window(x)
+    pool = x.state_pool.double().numpy()
+    cu = x.cu_seqlens.tolist()
+    idx = x.state_indices.tolist()
+    f = lambda t: t.float().numpy().astype(np.float64)
+    for b in range(3):
+        qs, qe = cu[b], cu[b + 1]
+        for a in range(qe - qs + 1):
+            want = oracle.recurrence(x.q[qs:qs + a], x.k[qs:qs + a], x.v[qs:qs + a], x.g[qs:qs + a],
+                                     x.beta[qs:qs + a], [0, a], A_log=x.A_log, dt_bias=x.dt_bias,
+                                     lower_bound=x.lower_bound, h0=pool[idx[b]][None])["state"][0]
+            for h in range(x.hv):
+                kg_raw = np.concatenate([f(x.k[qs:qs + a, h // (x.hv // x.hqk)]), f(x.g[qs:qs + a, h])], axis=1)
+                got = chunked.commit_from_records(
+                    pool[idx[b], h], kg_raw, res["corr"][qs:qs + a, h],
+                    None if x.A_log is None else float(x.A_log[h]),
+                    None if x.dt_bias is None else f(x.dt_bias[h]), x.lower_bound)
+                np.testing.assert_allclose(got, want[h], rtol=1e-11, atol=1e-14,
+                                           err_msg=f"request {b} head {h} accepted {a}")
