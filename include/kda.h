@@ -132,6 +132,43 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
                   const int32_t* state_indices, const uint8_t* has_initial_state,
                   int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Checkpoint offsets of kda_chunk_fwd_ex must be multiples of this (the
+ * prefill's chunk length): the walk snapshots states at chunk boundaries. */
+#define KDA_CHECKPOINT_ALIGNMENT 64
+
+/*
+ * kda_chunk_fwd_ex - kda_chunk_fwd plus mid-prefill state snapshots (the
+ * vLLM kda_chunk page's fused_kda_chunk checkpoint_state /
+ * checkpoint_offsets / checkpoint_state_indices).  All other arguments as
+ * kda_chunk_fwd.
+ *   checkpoint_state      fp32 [rows, Hv, 128, 128] destination, or NULL (no
+ *                         snapshots; the offsets and indices must then be NULL).
+ *                         Without indices it is a staging buffer with a row per
+ *                         sequence; with them it may be the paged state cache.
+ *   checkpoint_row_stride floats between rows (multiple of 4, >= Hv*16384)
+ *   checkpoint_rows       rows in checkpoint_state; a destination row >= rows
+ *                         sets KDA_ERR_DEVICE_INDEX and is skipped
+ *   checkpoint_offsets    device int32 [n_seqs]: sequence n's state after
+ *                         checkpoint_offsets[n] of its tokens is written to its
+ *                         row.  0 disables the snapshot; an offset that is not a
+ *                         positive multiple of KDA_CHECKPOINT_ALIGNMENT or
+ *                         exceeds the sequence's length is skipped silently, so
+ *                         callers filter rather than rely on the store.
+ *   checkpoint_state_indices device int32 [n_seqs] destination rows, or NULL
+ *                         (row n); a negative row disables that sequence's
+ *                         snapshot
+ * Writing a snapshot row that the same call also uses as a state cache row
+ * of another sequence is a race.
+ */
+int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seqlens,
+                     int32_t n_seqs, const float* initial_state, float* final_state,
+                     float* state_cache, int64_t slot_stride, int64_t n_slots,
+                     const int32_t* state_indices, const uint8_t* has_initial_state,
+                     float* checkpoint_state, int64_t checkpoint_row_stride,
+                     int64_t checkpoint_rows, const int32_t* checkpoint_offsets,
+                     const int32_t* checkpoint_state_indices, int32_t groups,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that cannot allocate
  * device memory.  The paper has no counterpart; this is a deployment aid.

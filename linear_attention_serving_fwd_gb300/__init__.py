@@ -104,7 +104,8 @@ def chunk_workspace_bytes(n_seqs: int, t_total: int, hv: int, groups: int = 0) -
 def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, lower_bound=-5.0,
                   cu_seqlens=None, n_seqs=None, initial_state=None, output_final_state=False,
                   final_state=None, out=None, state_cache=None, state_indices=None,
-                  has_initial_state=None, groups: int = 0, workspace=None, stream=None):
+                  has_initial_state=None, groups: int = 0, workspace=None, stream=None,
+                  checkpoint_state=None, checkpoint_offsets=None, checkpoint_state_indices=None):
     """Chunked KDA prefill.  Returns (out, final_state or None).
 
     q, k: [T, Hqk, 128] or [B, T, Hqk, 128]; v, g: [T, Hv, 128]; beta:
@@ -112,6 +113,10 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     sequences of T tokens.  ``state_cache`` [slots, Hv, 128, 128] fp32 with
     ``state_indices`` [N] int32 (and optional ``has_initial_state`` [N])
     replaces initial_state / final_state and is updated in place.
+    ``checkpoint_state`` [rows, Hv, 128, 128] fp32 with ``checkpoint_offsets``
+    [N] (and optional ``checkpoint_state_indices`` [N]) receives each
+    sequence's state after its first checkpoint_offsets[n] tokens (a positive
+    multiple of 64 no larger than its length; other offsets are skipped).
     """
     dense_b = q.shape[0] if q.dim() == 4 else None
     q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
@@ -149,11 +154,30 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     ws_bytes = chunk_workspace_bytes(n, T, hv, groups)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    rc = _native.lib().kda_chunk_fwd(
-        ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
-        _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
-        int(groups), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream_handle(stream))
+    ck_stride, ck_rows = 0, 0
+    if checkpoint_state is not None:
+        if checkpoint_offsets is None:
+            raise ValueError("checkpoint_state needs checkpoint_offsets.")
+        if checkpoint_state.dtype != torch.float32:
+            raise TypeError("checkpoint_state must be float32.")
+        if tuple(checkpoint_state.shape[1:]) != (hv, D, D) or checkpoint_state[0].stride() != (D * D, D, 1):
+            raise ValueError("checkpoint_state must be [rows, Hv, 128, 128] with contiguous rows.")
+        ck_stride, ck_rows = checkpoint_state.stride(0), checkpoint_state.shape[0]
+        checkpoint_offsets = checkpoint_offsets.to(torch.int32).contiguous()
+        if checkpoint_state_indices is not None:
+            checkpoint_state_indices = checkpoint_state_indices.to(torch.int32).contiguous()
+        rc = _native.lib().kda_chunk_fwd_ex(
+            ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
+            _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
+            _ptr(checkpoint_state), ck_stride, ck_rows, _ptr(checkpoint_offsets),
+            _ptr(checkpoint_state_indices), int(groups), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    else:
+        rc = _native.lib().kda_chunk_fwd(
+            ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
+            _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
+            int(groups), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
     _native.check(rc)
     del keep
     return out, final_state

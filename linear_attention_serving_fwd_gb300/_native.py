@@ -26,7 +26,7 @@ KDA_DTYPE_FP16 = 1
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_verify",
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
-           "kda_version", "kda_chunk_fwd_noalloc", "kda_commit")
+           "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex")
 
 
 class KdaActivations(ctypes.Structure):
@@ -58,6 +58,8 @@ def _declare(lib):
     lib.kda_chunk_workspace_bytes.restype = SZ
     lib.kda_chunk_fwd.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, I32, P, SZ, P]
     lib.kda_chunk_fwd.restype = ctypes.c_int
+    lib.kda_chunk_fwd_ex.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, P, I64, I64, P, P, I32, P, SZ, P]
+    lib.kda_chunk_fwd_ex.restype = ctypes.c_int
     lib.kda_chunk_fwd_noalloc.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, I32, P]
     lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
     lib.kda_decode.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P]

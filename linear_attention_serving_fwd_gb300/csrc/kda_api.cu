@@ -108,13 +108,14 @@ void fill_common(const kda_activations* x, const __nv_bfloat16*& q, const __nv_b
   b = static_cast<const __nv_bfloat16*>(x->beta);
 }
 
-int check_pool(const float* pool, int64_t slot_stride, int64_t n_slots, int hv, const char* name) {
+int check_pool(const float* pool, int64_t slot_stride, int64_t n_slots, int hv, const char* name,
+               const char* stride_name = "slot_stride") {
   if (!pool) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must not be NULL.", name);
   if (!aligned16(pool)) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned.", name);
-  if (n_slots <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "state pool must contain at least one slot.");
+  if (n_slots <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must contain at least one slot.", name);
   if (slot_stride % 4 != 0 || slot_stride < (int64_t)hv * kda::D * kda::D)
     return fail(KDA_ERR_INVALID_ARGUMENT,
-                "slot_stride must be a multiple of 4 floats and >= Hv*128*128 (got %lld).",
+                "%s must be a multiple of 4 floats and >= Hv*128*128 (got %lld).", stride_name,
                 (long long)slot_stride);
   return KDA_OK;
 }
@@ -247,11 +248,13 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
   return 4 * kda::chunk_workspace_floats(n_seqs, t_total, hv, G, nullptr);
 }
 
-int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
-                  const float* initial_state, float* final_state, float* state_cache,
-                  int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
-                  const uint8_t* has_initial_state, int32_t groups, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
+                        const float* initial_state, float* final_state, float* state_cache,
+                        int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
+                        const uint8_t* has_initial_state, float* checkpoint_state,
+                        int64_t checkpoint_row_stride, int64_t checkpoint_rows,
+                        const int32_t* checkpoint_offsets, const int32_t* checkpoint_state_indices,
+                        int32_t groups, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_activations(x, true);
   if (rc) return rc;
   if (n_seqs <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs must be >= 1.");
@@ -268,6 +271,19 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
   }
   if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
     return fail(KDA_ERR_INVALID_ARGUMENT, "states must be 16-byte aligned.");
+  if (checkpoint_state) {
+    if (!checkpoint_offsets)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoint_state needs checkpoint_offsets.");
+    rc = check_pool(checkpoint_state, checkpoint_row_stride, checkpoint_rows, x->hv, "checkpoint_state",
+                    "checkpoint_row_stride");
+    if (rc) return rc;
+    if (!checkpoint_state_indices && checkpoint_rows < n_seqs)
+      return fail(KDA_ERR_INVALID_ARGUMENT,
+                  "checkpoint_state without checkpoint_state_indices needs a row per sequence "
+                  "(%lld < %d).", (long long)checkpoint_rows, n_seqs);
+  } else if (checkpoint_offsets || checkpoint_state_indices) {
+    return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoint offsets or indices given without checkpoint_state.");
+  }
   const int G = choose_groups(n_seqs, x->t_total, x->hv, groups);
   const size_t need = 4 * kda::chunk_workspace_floats(n_seqs, x->t_total, x->hv, G, nullptr);
   if (!workspace || workspace_bytes < need)
@@ -296,11 +312,36 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
   p.state_indices = state_indices; p.has_init = has_initial_state;
   p.groups = G;
   p.sm_count = device_sm_count();
+  p.ckpt = checkpoint_state; p.ckpt_stride = checkpoint_row_stride; p.ckpt_rows = checkpoint_rows;
+  p.ckpt_off = checkpoint_offsets; p.ckpt_idx = checkpoint_state_indices;
   p.err = err;
   const int lrc = kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream));
   if (lrc == -2) return KDA_ERR_INVALID_ARGUMENT;  // message set by the launcher
   if (lrc != 0) return cuda_fail(cudaGetLastError(), "kda_chunk_fwd launch");
   return ok();
+}
+
+int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
+                  const float* initial_state, float* final_state, float* state_cache,
+                  int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
+                  const uint8_t* has_initial_state, int32_t groups, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  return chunk_common(x, out, cu_seqlens, n_seqs, initial_state, final_state, state_cache, slot_stride,
+                      n_slots, state_indices, has_initial_state, nullptr, 0, 0, nullptr, nullptr, groups,
+                      workspace, workspace_bytes, stream);
+}
+
+int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
+                     const float* initial_state, float* final_state, float* state_cache,
+                     int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
+                     const uint8_t* has_initial_state, float* checkpoint_state,
+                     int64_t checkpoint_row_stride, int64_t checkpoint_rows,
+                     const int32_t* checkpoint_offsets, const int32_t* checkpoint_state_indices,
+                     int32_t groups, void* workspace, size_t workspace_bytes, void* stream) {
+  return chunk_common(x, out, cu_seqlens, n_seqs, initial_state, final_state, state_cache, slot_stride,
+                      n_slots, state_indices, has_initial_state, checkpoint_state, checkpoint_row_stride,
+                      checkpoint_rows, checkpoint_offsets, checkpoint_state_indices, groups, workspace,
+                      workspace_bytes, stream);
 }
 
 static int window_common(const kda_activations* x, void* out, const float* pool, int64_t slot_stride,

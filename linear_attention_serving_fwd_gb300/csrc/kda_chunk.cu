@@ -882,6 +882,23 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     };
     // A failed wait sets ``fail``; the chain stops only at a barrier, all
     // 128 threads together.
+    // mid-prefill snapshot of this sequence: after in-sequence chunk ck_j
+    int ck_j = -1;
+    float* ck_dst = nullptr;
+    if (mode == 0 && p.ckpt) {
+      const int o = p.ckpt_off[n];
+      const int len = seq_eos(p, n) - seq_bos(p, n);
+      const int64_t row = p.ckpt_idx ? (int64_t)p.ckpt_idx[n] : (int64_t)n;
+      if (o > 0 && o % CHUNK == 0 && o <= len && row >= 0) {
+        if (row < p.ckpt_rows) {
+          ck_j = o / CHUNK - 1;
+          ck_dst = p.ckpt + row * p.ckpt_stride + (int64_t)h * D * D;
+        } else if (tid == 0) {
+          set_error(p.err, ERR_INDEX);
+        }
+      }
+    }
+    const int seq_c0 = p.chunk_off[n];
     float dcur = 0.f;
     bool fail = false;
     if (nch > 0) {
@@ -921,6 +938,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         for (int v = 0; v < 16; ++v)
           S[v] = fmaf(dcur, S[v], __uint_as_float(y0[v]) + __uint_as_float(y1[v]) +
                                       (ident ? 0.f : __uint_as_float(y2[v])));
+        if (c0 + it - seq_c0 == ck_j)  // S now holds the state after the snapshot's chunk
+#pragma unroll
+          for (int v = 0; v < 16; ++v) ck_dst[(int64_t)(col0 + 16 * ch + v) * D + k] = S[v];
         if (more) {
           write_s16(ab);
           fence_proxy_async_smem();

@@ -69,6 +69,13 @@ struct ChunkParams {
   float* gM;            // [N, Hv, G, 128, 128]  M_g^T
   float* gB;            // [N, Hv, G, 128, 128]  B_g^T
   float* gS;            // [N, Hv, G, 128, 128]  incoming state of each group (V-first)
+  // mid-prefill snapshots: the state after ckpt_off[n] tokens of sequence n
+  // (a positive multiple of CHUNK, at most its length) goes to row
+  // ckpt_idx[n] (or n) of ckpt; others are skipped
+  float* ckpt;
+  int64_t ckpt_stride, ckpt_rows;
+  const int32_t* ckpt_off;
+  const int32_t* ckpt_idx;
   unsigned* err;        // device error word
 };
 

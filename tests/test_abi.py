@@ -101,6 +101,38 @@ def test_chunk_rules_on_states_and_workspace():
     assert "divisible" in _msg()
 
 
+def _chunk_ex(a, **kw):
+    lib = _native.lib()
+    args = dict(out=FAKE, cu=None, n=1, h0=None, hT=None, cache=None, stride=0, slots=0,
+                idx=None, hi=None, ck=None, ck_stride=0, ck_rows=0, ck_off=None, ck_idx=None,
+                groups=1, ws=FAKE, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return lib.kda_chunk_fwd_ex(ctypes.byref(a), args["out"], args["cu"], args["n"], args["h0"],
+                                args["hT"], args["cache"], args["stride"], args["slots"],
+                                args["idx"], args["hi"], args["ck"], args["ck_stride"],
+                                args["ck_rows"], args["ck_off"], args["ck_idx"], args["groups"],
+                                args["ws"], args["ws_bytes"], args["stream"])
+
+
+def test_checkpoint_argument_rules():
+    a = _acts()
+    row = 4 * 16384
+    assert _chunk_ex(a, ck=FAKE, ck_stride=row, ck_rows=1) == INVALID
+    assert "needs checkpoint_offsets" in _msg()
+    assert _chunk_ex(a, ck_off=FAKE) == INVALID
+    assert "without checkpoint_state" in _msg()
+    assert _chunk_ex(a, ck_idx=FAKE) == INVALID
+    assert "without checkpoint_state" in _msg()
+    assert _chunk_ex(_acts(t_total=128), n=2, ck=FAKE, ck_stride=row, ck_rows=1, ck_off=FAKE) == INVALID
+    assert "row per sequence" in _msg()
+    assert _chunk_ex(a, ck=FAKE, ck_stride=row + 2, ck_rows=1, ck_off=FAKE) == INVALID
+    assert "checkpoint_row_stride" in _msg()
+    assert _chunk_ex(a, ck=FAKE, ck_stride=row, ck_rows=0, ck_off=FAKE, ck_idx=FAKE) == INVALID
+    assert "checkpoint_state must contain" in _msg()
+    assert _chunk_ex(a, ck=FAKE + 4, ck_stride=row, ck_rows=1, ck_off=FAKE) == INVALID
+    assert "checkpoint_state must be 16-byte aligned" in _msg()
+
+
 def test_workspace_query():
     lib = _native.lib()
     assert lib.kda_chunk_workspace_bytes(0, 64, 4, 1) == 0
