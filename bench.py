@@ -44,8 +44,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,verify,commit,varlen,long",
-                    help="comma list of extra workloads: decode, verify, commit, varlen, long")
+    ap.add_argument("--extras", default="decode,verify,commit,decode_steps,varlen,checkpoint,long",
+                    help="comma list of extra workloads: decode, verify, commit, decode_steps, "
+                         "varlen, checkpoint, long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -422,11 +423,52 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                                              "peak_source": f"{pk['src']} HBM copy bandwidth"},
                                 "workload": "256 requests x 4 accepted tokens, Hv=32, 512-slot fp32 pool"}
         del y, pool
+    if "decode_steps" in want:
+        # speculative multi-token decode with a [request, step] slot table:
+        # start from the accepted column's row, store the state after every
+        # token into its own row (64 KB in + 4 x 64 KB out per item)
+        window = 4
+        y = W.decode_batch(256, window, 32, 32, slots=1280, seed=rank, device="cuda",
+                           name="decode_steps_q4")
+        table, acc = W.decode_slot_table(256, window, 1280, seed=rank, device="cuda")
+        pool = y.state_pool
+        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
+
+        def fs():
+            kda.kda_decode_steps(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, table, window,
+                                 num_accepted_tokens=acc, A_log=y.A_log, dt_bias=y.dt_bias, out=out)
+        for _ in range(3):
+            fs()
+        secs = reduce_max(time_device(torch, fs, steps, flush, barrier))
+        items = y.n_seqs * y.hv
+        t = secs / steps
+        nbytes = items * sb * (1 + window) + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
+        gbs = nbytes / t / 1e9
+        res["decode_steps_q4"] = {"tokens_per_s": round(y.t_total * world / t, 1),
+                                  "ms_per_step": round(t * 1e3, 4),
+                                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                                               "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                                               "traffic": None,
+                                               "peak_source": f"{pk['src']} HBM copy bandwidth"},
+                                  "workload": "256 requests x 4 tokens, Hqk=Hv=32, 1280-row fp32 pool, "
+                                              "slot table of 4 rows per request, accepted counts U{1..4}"}
+        del y, pool, table, acc
+        torch.cuda.empty_cache()
     # varlen paged and long-context prefill
-    for name in ("varlen", "long"):
+    for name in ("varlen", "checkpoint", "long"):
         if name not in want:
             continue
-        z = W.workload(name, seed=rank, device="cuda")
+        z = W.workload("long" if name == "long" else "varlen", seed=rank, device="cuda")
+        ck = {}
+        if name == "checkpoint":
+            # one snapshot per sequence at its last 64-aligned midpoint, into
+            # pool rows no sequence of the batch uses (prefix caching)
+            lens = (z.cu_seqlens[1:] - z.cu_seqlens[:-1]).to(torch.int64)
+            used = set(z.state_indices.tolist())
+            spare = [r for r in range(z.state_pool.shape[0]) if r not in used][:z.n_seqs]
+            ck = dict(checkpoint_state=z.state_pool,
+                      checkpoint_offsets=((lens // 2) // 64 * 64).to(torch.int32),
+                      checkpoint_state_indices=torch.tensor(spare, dtype=torch.int32, device="cuda"))
         out = torch.empty((z.t_total, z.hv, D), dtype=torch.bfloat16, device="cuda")
         ws = torch.empty(kda.chunk_workspace_bytes(z.n_seqs, z.t_total, z.hv, 0),
                          dtype=torch.uint8, device="cuda")
@@ -439,7 +481,7 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                 kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
                                   cu_seqlens=z.cu_seqlens, state_cache=z.state_pool,
                                   state_indices=z.state_indices,
-                                  has_initial_state=z.has_initial_state, out=out, workspace=ws)
+                                  has_initial_state=z.has_initial_state, out=out, workspace=ws, **ck)
             else:
                 kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
                                   n_seqs=z.n_seqs, final_state=fin, out=out, workspace=ws)
@@ -452,8 +494,14 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
         tfl = th * flop_per_token_head() / t / 1e12
         res[name] = {"tokens_per_s": round(z.t_total * world / t, 1), "ms_per_step": round(t * 1e3, 3),
                      "tflops": round(tfl, 3), "pct_bf16_peak": round(100 * tfl / pk["bf16"], 2),
-                     "workload": ("8 seqs (U[64,8192] rescaled to 32768), Hqk=8 Hv=32, paged fp32 cache"
-                                  if name == "varlen" else "B=1 T=131072 Hqk=Hv=32, zero initial state")}
+                     "workload": {"varlen": "8 seqs (U[64,8192] rescaled to 32768), Hqk=8 Hv=32, paged fp32 cache",
+                                  "checkpoint": "varlen workload plus one snapshot per sequence at its "
+                                                "64-aligned midpoint into a spare cache row",
+                                  "long": "B=1 T=131072 Hqk=Hv=32, zero initial state"}[name]}
+        if name == "checkpoint":
+            res[name]["snapshot_bytes"] = int((ck["checkpoint_offsets"] > 0).sum().item()) * z.hv * 4 * D * D
+            if "varlen" in res:
+                res[name]["overhead_vs_varlen"] = round(t * 1e3 / res["varlen"]["ms_per_step"] - 1, 4)
         del z, out, ws
         torch.cuda.empty_cache()
     return res

@@ -220,6 +220,35 @@ int kda_decode(const kda_activations* x, void* out, float* state_pool,
                const int32_t* slots, int32_t n_req, int32_t window, void* stream);
 
 /*
+ * kda_decode_steps - kda_decode with a [request, step] slot table and
+ * accepted-token counts: the MATE gated_delta_rule_decode contract for
+ * [B, T] state_indices with num_accepted_tokens (speculative, multi-token
+ * in-place decode).  The page names these arguments and their shape rules;
+ * the reading taken of their meaning is:
+ *   state_indices        device int32 [n_req, indices_stride], indices_stride
+ *                        >= window.  Request b reads its initial state from
+ *                        row state_indices[b][c], c = num_accepted_tokens[b]-1
+ *                        (c = 0 when num_accepted_tokens is NULL), and the
+ *                        state after its token t is written to row
+ *                        state_indices[b][t], t < its length.  A negative row
+ *                        at column c makes b a padding request (zero output,
+ *                        no state traffic); a negative row at column t skips
+ *                        that store.  A row >= n_slots at column c or at any
+ *                        column t < length, or c outside [0, indices_stride),
+ *                        sets KDA_ERR_DEVICE_INDEX and b is treated as padding.
+ *   num_accepted_tokens  device int32 [n_req] or NULL
+ * All other arguments as kda_decode.  Columns that repeat a row are written
+ * in token order, so the row ends holding the later token's state; with
+ * every column of b equal to one slot this is kda_decode.  Rows must not be
+ * shared between requests; the read row may be one of the request's own
+ * write rows (it is read before any store).
+ */
+int kda_decode_steps(const kda_activations* x, void* out, float* state_pool, int64_t slot_stride,
+                     int64_t n_slots, const int32_t* query_start, const int32_t* state_indices,
+                     int64_t indices_stride, const int32_t* num_accepted_tokens, int32_t n_req,
+                     int32_t window, void* stream);
+
+/*
  * kda_verify - windowed speculative verify (1 <= window <= 8): the vLLM
  * kimi_k3 CuTeDSL KdaTcVerify contract with fp32 states.  Same inputs and
  * outputs ``out`` as kda_decode, but the state pool is only read, and per

@@ -7,6 +7,8 @@ every step of the computation runs in the library's CUDA kernels.
 * :func:`kda_chunk_fwd` - chunked prefill (dense, varlen, paged state cache,
   optional chunk-group scan).
 * :func:`kda_decode` - in-place window decode on a paged fp32 state cache.
+* :func:`kda_decode_steps` - window decode with a [request, step] slot table
+  and accepted-token counts (speculative multi-token decode).
 * :func:`kda_verify` - speculative verify (state read only, correction
   records).
 * :func:`kda_device_status` - read (and clear) the device error word.
@@ -22,7 +24,8 @@ from . import _native
 from ._native import KdaError
 
 D = 128
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode", "kda_verify", "kda_commit",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode", "kda_decode_steps", "kda_verify",
+           "kda_commit",
            "kda_device_status", "chunk_workspace_bytes", "KdaError", "library_path"]
 
 
@@ -215,14 +218,23 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, out, A_log=None, dt_bias=None, sc
 
 
 def _window_call(verify, q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log,
-                 dt_bias, scale, lower_bound, out, corr, kg, work_counter, stream):
+                 dt_bias, scale, lower_bound, out, corr, kg, work_counter, stream,
+                 num_accepted_tokens=None):
     a, keep = _activations(_as_tokens(q, "q"), _as_tokens(k, "k"), _as_tokens(v, "v"),
                            _as_tokens(g, "g"), _as_tokens(beta, "beta", heads_dim=False),
                            A_log, dt_bias, scale, lower_bound)
     T, hv = a.t_total, a.hv
-    n_req = slots.numel()
+    table = slots.dim() == 2
+    n_req = slots.shape[0] if table else slots.numel()
     if query_start.dtype != torch.int32 or slots.dtype != torch.int32:
         raise TypeError("query_start and slots must have dtype torch.int32.")
+    if table and verify:
+        raise ValueError("kda_verify takes one slot per request.")
+    if table and slots.stride(1) != 1:
+        raise ValueError("a [n_req, steps] slot table must have contiguous rows.")
+    if num_accepted_tokens is not None:
+        if num_accepted_tokens.dtype != torch.int32 or num_accepted_tokens.numel() != n_req:
+            raise ValueError("num_accepted_tokens must be int32 with one entry per request.")
     if state_pool.dtype != torch.float32:
         raise TypeError("state_pool must be float32.")
     if tuple(state_pool.shape[1:]) != (hv, D, D) or state_pool[0].stride() != (D * D, D, 1):
@@ -240,6 +252,11 @@ def _window_call(verify, q, k, v, g, beta, state_pool, query_start, slots, windo
         rc = lib.kda_verify(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
                             state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
                             _ptr(corr), _ptr(kg), _ptr(work_counter), _stream_handle(stream))
+    elif table:
+        rc = lib.kda_decode_steps(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
+                                  state_pool.shape[0], _ptr(query_start), _ptr(slots),
+                                  slots.stride(0), _ptr(num_accepted_tokens), n_req, window,
+                                  _stream_handle(stream))
     else:
         rc = lib.kda_decode(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
                             state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
@@ -256,6 +273,22 @@ def kda_decode(q, k, v, g, beta, state_pool, query_start, slots, window, *, A_lo
     return _window_call(False, q, k, v, g, beta, state_pool, query_start, slots, window,
                         A_log=A_log, dt_bias=dt_bias, scale=scale, lower_bound=lower_bound,
                         out=out, corr=None, kg=None, work_counter=None, stream=stream)[0]
+
+
+def kda_decode_steps(q, k, v, g, beta, state_pool, query_start, state_indices, window, *,
+                     num_accepted_tokens=None, A_log=None, dt_bias=None, scale=None,
+                     lower_bound=-5.0, out=None, stream=None):
+    """Decode with a [n_req, steps] int32 slot table (steps >= window):
+    request b starts from pool row state_indices[b, num_accepted_tokens[b] - 1]
+    (column 0 without counts) and the state after its token t is stored to
+    row state_indices[b, t] (negative = no store; a negative start row makes
+    b padding).  Returns out."""
+    if state_indices.dim() != 2:
+        raise ValueError("state_indices must be a [n_req, steps] table.")
+    return _window_call(False, q, k, v, g, beta, state_pool, query_start, state_indices, window,
+                        A_log=A_log, dt_bias=dt_bias, scale=scale, lower_bound=lower_bound,
+                        out=out, corr=None, kg=None, work_counter=None, stream=stream,
+                        num_accepted_tokens=num_accepted_tokens)[0]
 
 
 def kda_verify(q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log=None,

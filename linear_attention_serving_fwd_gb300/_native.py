@@ -26,7 +26,8 @@ KDA_DTYPE_FP16 = 1
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_verify",
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
-           "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex")
+           "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
+           "kda_decode_steps")
 
 
 class KdaActivations(ctypes.Structure):
@@ -64,6 +65,8 @@ def _declare(lib):
     lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
     lib.kda_decode.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P]
     lib.kda_decode.restype = ctypes.c_int
+    lib.kda_decode_steps.argtypes = [A, P, P, I64, I64, P, P, I64, P, I32, I32, P]
+    lib.kda_decode_steps.restype = ctypes.c_int
     lib.kda_verify.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P, P, P, P]
     lib.kda_verify.restype = ctypes.c_int
     lib.kda_commit.argtypes = [P, I64, I64, P, P, I32, I32, I32, P, P, P, P, ctypes.c_float, P]

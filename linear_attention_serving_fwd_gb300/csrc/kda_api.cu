@@ -347,15 +347,20 @@ int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seql
 static int window_common(const kda_activations* x, void* out, const float* pool, int64_t slot_stride,
                          int64_t n_slots, const int32_t* query_start, const int32_t* slots,
                          int32_t n_req, int32_t window, bool verify, float* corr, void* kg,
-                         int32_t* counter, void* stream) {
+                         int32_t* counter, void* stream, const int32_t* step_slots = nullptr,
+                         int64_t step_stride = 0, const int32_t* n_accepted = nullptr) {
   int rc = check_activations(x, true);
   if (rc) return rc;
   if (window < 1 || window > kda::MAX_WINDOW)
     return fail(KDA_ERR_INVALID_ARGUMENT, "window must satisfy 1 <= window <= 8 (got %d).", window);
   if (n_req < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_req must be >= 0.");
+  if (step_slots && step_stride < window)
+    return fail(KDA_ERR_INVALID_ARGUMENT,
+                "state_indices needs at least window = %d columns, got %lld.", window,
+                (long long)step_stride);
   if (n_req == 0) return ok();
-  if (!query_start || !slots)
-    return fail(KDA_ERR_INVALID_ARGUMENT, "query_start and slots must not be NULL.");
+  if (!query_start || !(slots || step_slots))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "query_start and state_indices must not be NULL.");
   if (x->t_total > 0 && !out) return fail(KDA_ERR_INVALID_ARGUMENT, "out must not be NULL.");
   rc = check_pool(pool, slot_stride, n_slots, x->hv, "state_pool");
   if (rc) return rc;
@@ -379,6 +384,7 @@ static int window_common(const kda_activations* x, void* out, const float* pool,
   p.pool = const_cast<float*>(pool);
   p.slot_stride = slot_stride; p.n_slots = n_slots;
   p.query_start = query_start; p.slots = slots;
+  p.step_slots = step_slots; p.step_stride = step_stride; p.n_accepted = n_accepted;
   p.n_req = n_req; p.window = window; p.hqk = x->hqk; p.hv = x->hv;
   p.corr = corr; p.kg = static_cast<__nv_bfloat16*>(kg); p.counter = counter;
   p.err = err;
@@ -392,6 +398,17 @@ int kda_decode(const kda_activations* x, void* out, float* state_pool, int64_t s
                int32_t window, void* stream) {
   return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req,
                        window, false, nullptr, nullptr, nullptr, stream);
+}
+
+int kda_decode_steps(const kda_activations* x, void* out, float* state_pool, int64_t slot_stride,
+                     int64_t n_slots, const int32_t* query_start, const int32_t* state_indices,
+                     int64_t indices_stride, const int32_t* num_accepted_tokens, int32_t n_req,
+                     int32_t window, void* stream) {
+  if (!state_indices && n_req > 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "query_start and state_indices must not be NULL.");
+  return window_common(x, out, state_pool, slot_stride, n_slots, query_start, nullptr, n_req, window,
+                       false, nullptr, nullptr, nullptr, stream, state_indices, indices_stride,
+                       num_accepted_tokens);
 }
 
 int kda_verify(const kda_activations* x, void* out, const float* state_pool, int64_t slot_stride,

@@ -18,6 +18,12 @@ struct WindowParams {
   int64_t n_slots;
   const int32_t* query_start;
   const int32_t* slots;
+  // decode with a [n_req, step_stride] slot table (slots unused): the state
+  // is read from row step_slots[b][n_accepted[b] - 1] (column 0 without
+  // n_accepted) and the state after token t goes to row step_slots[b][t]
+  const int32_t* step_slots;
+  int64_t step_stride;
+  const int32_t* n_accepted;
   int n_req, window, hqk, hv;
   float* corr;          // verify: [n_req, Hv, window, 128]
   __nv_bfloat16* kg;    // verify: [n_req, Hv, window, 256]

@@ -10,7 +10,9 @@
 //    two ahead streams in while one runs, and the next item's per-token
 //    scalars (beta, A_log, dt_bias) are loaded into registers a step ahead;
 //  * decode writes the new state back through a third 64 KB buffer and two
-//    bulk stores, so no thread waits on its write;
+//    bulk stores, so no thread waits on its write; with a [request, step]
+//    slot table it reads the row of the last accepted token and also stores
+//    the state after each earlier token of the window, from registers;
 //  * per item, warp t < qlen first turns token t's raw rows into the vectors
 //    every warp needs (L2-normalised k^ and q~, exp(gate), their products)
 //    in shared memory, once;
@@ -56,7 +58,8 @@ static_assert(sizeof(WinSmem) <= 227 * 1024, "window kernel shared memory");
 
 struct ItemInfo {
   int request, head, qs, qlen;
-  int64_t slot;
+  int64_t slot;   // the row the state is read from
+  int64_t wslot;  // decode: the row the state after the last token goes to (< 0: none)
   bool work;  // state is loaded and tokens processed
   bool zero;  // padding request: write zero outputs
   bool bad;   // out-of-range slot or window length (reported, treated as padding)
@@ -68,9 +71,24 @@ __device__ __forceinline__ ItemInfo item_info(const WindowParams& p, int item) {
   r.head = item - r.request * p.hv;
   r.qs = p.query_start[r.request];
   r.qlen = p.query_start[r.request + 1] - r.qs;
-  r.slot = p.slots[r.request];
   const bool bad_len = r.qlen < 0 || r.qlen > p.window;
-  const bool bad_slot = r.slot >= p.n_slots;
+  bool bad_slot;
+  if (p.step_slots) {
+    // slot table: read the column of the last accepted token, write a row
+    // per token (window <= step_stride, so columns t < qlen exist)
+    const int32_t* row = p.step_slots + (int64_t)r.request * p.step_stride;
+    const int col = p.n_accepted ? p.n_accepted[r.request] - 1 : 0;
+    const bool bad_col = col < 0 || col >= p.step_stride;
+    r.slot = bad_col ? -1 : row[col];
+    r.wslot = (!bad_len && r.qlen > 0) ? row[r.qlen - 1] : -1;
+    bad_slot = bad_col || r.slot >= p.n_slots;
+    if (!bad_len)
+      for (int t = 0; t < r.qlen; ++t) bad_slot |= row[t] >= p.n_slots;
+  } else {
+    r.slot = p.slots[r.request];
+    r.wslot = r.slot;
+    bad_slot = r.slot >= p.n_slots;
+  }
   r.work = !bad_len && !bad_slot && r.slot >= 0 && r.qlen > 0;
   r.zero = !bad_len && r.qlen > 0 && !r.work;
   r.bad = bad_len || bad_slot;
@@ -255,6 +273,20 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) S[i][jj] = ffma2(S[i][jj], dv[jj], fmul2(kv[jj], uu));
     }
+    if (!VERIFY && p.step_slots && t + 1 < it.qlen) {
+      // slot table: the state after token t, unless its row is the last
+      // token's (written after the window) or disabled
+      const int64_t row = p.step_slots[(int64_t)it.request * p.step_stride + t];
+      if (row >= 0 && row != it.wslot) {
+        float* dst = p.pool + row * p.slot_stride + (int64_t)h * D * D;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<float4*>(dst + win_row(warp, lane, i) * D + win_chan(lane, j)) =
+                make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y);
+      }
+    }
   }
 }
 
@@ -368,8 +400,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
     }
     if (tid == 0 && it.bad) set_error(p.err, ERR_INDEX);
     __syncthreads();  // input buffer b and the token vectors consumed, sout written
-    if (!VERIFY && tid == 0 && it.work) {
-      float* dst = p.pool + it.slot * p.slot_stride + (int64_t)it.head * D * D;
+    if (!VERIFY && tid == 0 && it.work && it.wslot >= 0) {
+      float* dst = p.pool + it.wslot * p.slot_stride + (int64_t)it.head * D * D;
       bulk_s2g(dst, s.sout, STATE_BYTES / 2);
       bulk_s2g(dst + D * D / 2, s.sout + D * D / 2, STATE_BYTES / 2);
       bulk_commit();

@@ -209,6 +209,18 @@ def decode_batch(n_req: int, window: int, hqk: int, hv: int, *, slots: int = 512
                      window=window, output_final_state=False)
 
 
+def decode_slot_table(n_req: int, steps: int, slots: int, *, seed: int = 0, device="cpu"):
+    """A [n_req, steps] int32 slot table of distinct pool rows (a row per
+    request and decode step, as speculative decode keeps them) drawn from
+    randperm(slots), and per-request accepted-token counts U{1..steps}."""
+    assert n_req * steps <= slots
+    gen = _gen(seed + 7919, device)
+    rows = torch.randperm(slots, generator=gen, device=device)[:n_req * steps]
+    table = rows.to(torch.int32).view(n_req, steps).contiguous()
+    acc = torch.randint(1, steps + 1, (n_req,), generator=gen, device=device, dtype=torch.int32)
+    return table, acc
+
+
 def _cumsum(xs):
     s = 0
     for x in xs:

@@ -185,3 +185,72 @@ def window(x, *, n_threads=0):
             res["corr"][cu[b]:cu[b + 1]] = 0.0
     res["pool"] = pool
     return res
+
+
+def window_steps(x, table, num_accepted=None, *, n_threads=0):
+    """Oracle for ``kda_decode_steps``: decode with a [request, step] slot table.
+
+    Follows the MATE ``gated_delta_rule_decode`` arguments ``state_indices``
+    ([B, T]) and ``num_accepted_tokens`` as read here: request b starts from
+    pool row ``table[b, c]`` with c = num_accepted[b] - 1 (0 without counts),
+    and the state after its token t is stored to row ``table[b, t]``
+    (negative: no store), rows written in token order.  A negative start row
+    makes b padding (zero output, nothing stored).  A start column outside
+    the table, or a row >= the pool size at the start column or at any of
+    b's token columns, flags the call and b is treated as padding.
+
+    Every state is the recurrence itself: the state after token t is the
+    final state of the recurrence run on b's first t + 1 tokens.
+    Returns out [T, Hv, 128], the pool after the call, and ``bad``.
+    """
+    n = x.n_seqs
+    pool0 = x.state_pool.detach().cpu().double().numpy()
+    pool = pool0.copy()
+    n_slots = pool.shape[0]
+    tab = np.asarray(table.cpu().numpy() if hasattr(table, "cpu") else table, dtype=np.int64)
+    na = None
+    if num_accepted is not None:
+        na = np.asarray(num_accepted.cpu().numpy() if hasattr(num_accepted, "cpu") else num_accepted,
+                        dtype=np.int64)
+    cu = np.asarray(x.cu_seqlens.cpu().numpy(), dtype=np.int64)
+    q, k, v, g, beta = (_f32(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    out = np.zeros((int(cu[-1]), x.hv, D))
+    bad = False
+    live = []  # (request, start row, length)
+    for b in range(n):
+        L = int(cu[b + 1] - cu[b])
+        col = int(na[b]) - 1 if na is not None else 0
+        if col < 0 or col >= tab.shape[1]:
+            bad = True
+            continue
+        if L <= 0:
+            continue
+        r0 = int(tab[b, col])
+        if r0 >= n_slots or np.any(tab[b, :L] >= n_slots):
+            bad = True
+            continue
+        if r0 >= 0:
+            live.append((b, r0, L))
+    # one sequence per (request, prefix length): tokens cu[b] .. cu[b] + t
+    sel, starts, h0 = [], [0], []
+    for b, r0, L in live:
+        for t in range(L):
+            sel.extend(range(int(cu[b]), int(cu[b]) + t + 1))
+            starts.append(len(sel))
+            h0.append(pool0[r0])
+    if live:
+        sel = np.asarray(sel)
+        res = recurrence(q[sel], k[sel], v[sel], g[sel], beta[sel], np.asarray(starts),
+                         A_log=x.A_log, dt_bias=x.dt_bias, scale=x.scale,
+                         lower_bound=x.lower_bound, h0=np.stack(h0), n_threads=n_threads)
+        piece = 0
+        for b, r0, L in live:
+            for t in range(L):
+                if t == L - 1:  # the full window: its outputs are the decode's
+                    a, e = starts[piece], starts[piece + 1]
+                    out[int(cu[b]):int(cu[b]) + L] = res["out"][a:e]
+                row = int(tab[b, t])
+                if row >= 0:
+                    pool[row] = res["state"][piece]
+                piece += 1
+    return dict(out=out, pool=pool, bad=bad)

@@ -172,6 +172,25 @@ def test_window_validation(verify):
         assert _window(a, True, ctr=None) == INVALID and "work_counter" in _msg()
 
 
+def test_slot_table_decode_validation():
+    lib = _native.lib()
+    a = _acts()
+
+    def steps(**kw):
+        args = dict(out=FAKE, pool=FAKE, stride=4 * 16384, slots=8, qs=FAKE, tab=FAKE, ts=4,
+                    acc=None, n=2, win=4)
+        args.update(kw)
+        return lib.kda_decode_steps(ctypes.byref(a), args["out"], args["pool"], args["stride"],
+                                    args["slots"], args["qs"], args["tab"], args["ts"], args["acc"],
+                                    args["n"], args["win"], None)
+    assert steps(ts=3) == INVALID and "at least window" in _msg()
+    assert steps(tab=None) == INVALID and "state_indices" in _msg()
+    assert steps(qs=None) == INVALID
+    assert steps(win=9, ts=9) == INVALID and "window" in _msg()
+    assert steps(pool=None) == INVALID and "state_pool" in _msg()
+    assert steps(n=0) == 0  # nothing to do
+
+
 def test_valid_call_without_gpu_reports_cuda_error():
     """Arguments that pass validation reach the CUDA runtime, which on a host
     without a GPU fails cleanly with KDA_ERR_CUDA."""

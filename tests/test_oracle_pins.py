@@ -242,6 +242,49 @@ def test_window_equals_repeated_single_tokens():
     assert np.array_equal(res["pool"][untouched], pool[untouched])
 
 
+def test_slot_table_decode_states_and_reads():
+    """The slot-table decode stores, at each column t, the state after t + 1
+    single-token decodes from the start row (the accepted column), and with
+    every column of a request on one slot it is the in-place window decode."""
+    x = W.decode_batch(5, 4, 2, 4, slots=24, seed=12, qlens=[4, 3, 1, 4, 2], lower_bound=-0.7)
+    pool = x.state_pool.double().numpy().copy()
+    table = np.array([[0, 1, 2, 3], [4, -1, 6, 7], [8, 9, 10, 11], [-1, 12, 13, 14],
+                      [15, 16, -1, -1]], dtype=np.int64)
+    acc = np.array([2, 1, 4, 1, 3])
+    res = oracle.window_steps(x, torch.from_numpy(table), torch.from_numpy(acc))
+    assert not res["bad"]
+    cu = x.cu_seqlens.tolist()
+    written = set()
+    for b in range(5):
+        r0 = table[b, acc[b] - 1]
+        if r0 < 0:
+            assert np.all(res["out"][cu[b]:cu[b + 1]] == 0)
+            continue
+        S = pool[r0][None]
+        for j, t in enumerate(range(cu[b], cu[b + 1])):
+            one = oracle.recurrence(x.q[t:t + 1], x.k[t:t + 1], x.v[t:t + 1], x.g[t:t + 1],
+                                    x.beta[t:t + 1], [0, 1], A_log=x.A_log, dt_bias=x.dt_bias,
+                                    lower_bound=x.lower_bound, h0=S)
+            np.testing.assert_allclose(res["out"][t], one["out"][0], rtol=1e-12, atol=1e-15)
+            S = one["state"]
+            if table[b, j] >= 0:
+                np.testing.assert_allclose(res["pool"][table[b, j]], S[0], rtol=1e-12, atol=1e-15)
+                written.add(int(table[b, j]))
+    untouched = [r for r in range(24) if r not in written]
+    assert np.array_equal(res["pool"][untouched], pool[untouched])
+    # one slot per request in every column: the in-place decode
+    same = np.repeat(x.state_indices.numpy()[:, None], 4, axis=1)
+    a = oracle.window_steps(x, torch.from_numpy(same))
+    w = oracle.window(x)
+    np.testing.assert_allclose(a["out"], w["out"], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(a["pool"], w["pool"], rtol=1e-12, atol=1e-15)
+    # a start column outside the table, or a row past the pool, is flagged
+    assert oracle.window_steps(x, torch.from_numpy(table), torch.from_numpy(acc * 0))["bad"]
+    t2 = table.copy()
+    t2[2, 3] = 24
+    assert oracle.window_steps(x, torch.from_numpy(t2), torch.from_numpy(acc))["bad"]
+
+
 def test_corr_matches_windowed_solve():
     """The correction records U_t equal the windowed forward substitution of
     the verify page (probes p_t = e^{L_t} k^_t against the start state and
