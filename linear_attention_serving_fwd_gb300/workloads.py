@@ -221,6 +221,21 @@ def decode_slot_table(n_req: int, steps: int, slots: int, *, seed: int = 0, devi
     return table, acc
 
 
+def conv_inputs(hqk: int, hv: int, rows: int, positions: int, *, taps: str = "bf16",
+                seed: int = 0, device="cpu"):
+    """Width-4 depthwise conv parameters and state for the raw q/k/v
+    projection bands (C = (2 Hqk + Hv) * 128 channels): weight [C, 4] drawn
+    U(-1/2, 1/2) (the default init of a conv1d with fan-in 4), bf16 or fp32,
+    and a bf16 conv state [rows, positions, C] (token major) of N(0, 1)
+    values, the scale of the projection outputs it holds."""
+    gen = _gen(seed + 104729, device)
+    C = (2 * hqk + hv) * D
+    w = _uniform(gen, (C, 4), -0.5, 0.5, device)
+    w = w.to(torch.bfloat16) if taps == "bf16" else w
+    st = _normal(gen, (rows, positions, C), 1.0, device).to(torch.bfloat16)
+    return w, st
+
+
 def _cumsum(xs):
     s = 0
     for x in xs:
