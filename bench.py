@@ -44,9 +44,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--extras", default="decode,verify,commit,decode_steps,varlen,checkpoint,long",
-                    help="comma list of extra workloads: decode, verify, commit, decode_steps, "
-                         "varlen, checkpoint, long")
+    ap.add_argument("--extras",
+                    default="decode,verify,verify_conv,commit,decode_steps,varlen,checkpoint,prefill_conv,long",
+                    help="comma list of extra workloads: decode, verify, verify_conv, commit, "
+                         "decode_steps, varlen, checkpoint, prefill_conv, long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -355,7 +356,7 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
     # decode / verify on the 256-request batch, H=32, 512-slot pool
     want = set(args.extras.split(","))
     for window in (1, 4):
-        if not ({"decode", "verify", "commit"} & want):
+        if not ({"decode", "verify", "verify_conv", "commit"} & want):
             break
         y = W.workload("decode", window=window, seed=rank, device="cuda")
         pool = y.state_pool
@@ -397,6 +398,35 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                                      else None,
                                      "peak_source": f"{pk['src']} HBM copy bandwidth"},
                         "workload": f"256 requests x window {window}, Hqk=Hv=32, 512-slot fp32 pool"}
+        if "verify_conv" in want and window == 4:
+            # verify on the raw projection bands: width-4 conv + SiLU after the
+            # history at the accepted column, conv state rolled (bf16 taps)
+            w, cst = W.conv_inputs(y.hqk, y.hv, pool.shape[0], window + 2, seed=rank, device="cuda")
+            acc = torch.randint(1, window + 1, (y.n_seqs,), dtype=torch.int32, device="cuda")
+
+            def fv():
+                kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, window,
+                               A_log=y.A_log, dt_bias=y.dt_bias, out=out, corr=corr, kg=kg,
+                               work_counter=counter, conv_weight=w, conv_state=cst,
+                               num_accepted_tokens=acc)
+            for _ in range(3):
+                fv()
+            secs = reduce_max(time_device(torch, fv, steps, flush, barrier))
+            t = secs / steps
+            items = y.n_seqs * y.hv
+            nbytes = (items * sb + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
+                      + y.t_total * y.hv * (4 * D + 4 * D))
+            gbs = nbytes / t / 1e9
+            res["verify_conv_q4"] = {"tokens_per_s": round(y.t_total * world / t, 1),
+                                     "ms_per_step": round(t * 1e3, 4),
+                                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                                                  "peak": pk["hbm"], "unit": "GB/s",
+                                                  "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                                                  "peak_source": f"{pk['src']} HBM copy bandwidth"},
+                                     "workload": "256 requests x window 4, Hqk=Hv=32, 512-slot fp32 pool, "
+                                                 "width-4 conv + SiLU on raw q/k/v (bf16 taps), "
+                                                 "6-position conv state, accepted U{1..4}"}
+            del w, cst, acc
         if "commit" in want and window == 4:
             # rebuild every request's state after all 4 verified tokens from
             # verify's records, in place: 64 KB in + 64 KB out per item
@@ -455,11 +485,24 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
         del y, pool, table, acc
         torch.cuda.empty_cache()
     # varlen paged and long-context prefill
-    for name in ("varlen", "checkpoint", "long"):
+    for name in ("varlen", "checkpoint", "prefill_conv", "long"):
         if name not in want:
             continue
         z = W.workload("long" if name == "long" else "varlen", seed=rank, device="cuda")
         ck = {}
+        q_in, k_in, v_in = z.q, z.k, z.v
+        if name == "prefill_conv":
+            # raw projection bands as strided views of one fused [T, C]
+            # projection; width-4 conv + SiLU (bf16 taps) in the prologue
+            T_, C_ = z.t_total, (2 * z.hqk + z.hv) * D
+            qkv = torch.cat([z.q.reshape(T_, -1), z.k.reshape(T_, -1), z.v.reshape(T_, -1)], dim=1)
+            a_, b_ = z.hqk * D, 2 * z.hqk * D
+            q_in = qkv[:, :a_].view(T_, z.hqk, D)
+            k_in = qkv[:, a_:b_].view(T_, z.hqk, D)
+            v_in = qkv[:, b_:].view(T_, z.hv, D)
+            w_, cst_ = W.conv_inputs(z.hqk, z.hv, z.state_pool.shape[0], 4, seed=rank, device="cuda")
+            ck = dict(conv_weight=w_, conv_state=cst_, conv_state_indices=z.state_indices,
+                      conv_has_initial_state=z.has_initial_state)
         if name == "checkpoint":
             # one snapshot per sequence at its last 64-aligned midpoint, into
             # pool rows no sequence of the batch uses (prefix caching)
@@ -478,7 +521,7 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
 
         def fn():
             if z.state_pool is not None:
-                kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
+                kda.kda_chunk_fwd(q_in, k_in, v_in, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
                                   cu_seqlens=z.cu_seqlens, state_cache=z.state_pool,
                                   state_indices=z.state_indices,
                                   has_initial_state=z.has_initial_state, out=out, workspace=ws, **ck)
@@ -497,7 +540,12 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                      "workload": {"varlen": "8 seqs (U[64,8192] rescaled to 32768), Hqk=8 Hv=32, paged fp32 cache",
                                   "checkpoint": "varlen workload plus one snapshot per sequence at its "
                                                 "64-aligned midpoint into a spare cache row",
+                                  "prefill_conv": "varlen workload on raw q/k/v bands of a fused "
+                                                  "projection: width-4 conv + SiLU (bf16 taps) fused "
+                                                  "into the prologue, conv state updated",
                                   "long": "B=1 T=131072 Hqk=Hv=32, zero initial state"}[name]}
+        if name == "prefill_conv" and "varlen" in res:
+            res[name]["overhead_vs_varlen"] = round(t * 1e3 / res["varlen"]["ms_per_step"] - 1, 4)
         if name == "checkpoint":
             res[name]["snapshot_bytes"] = int((ck["checkpoint_offsets"] > 0).sum().item()) * z.hv * 4 * D * D
             if "varlen" in res:

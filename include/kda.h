@@ -80,6 +80,57 @@ typedef struct kda_activations {
 } kda_activations;
 
 /*
+ * kda_conv - the width-4 depthwise causal conv + SiLU that kda_chunk_fwd_ex
+ * and kda_verify_ex can apply to q, k and v first: the conv arguments of
+ * the vLLM kimi_k3 AMD kda_chunk page's fused_kda_prologue (conv_weight,
+ * conv_state, conv_state_indices, conv_has_initial_state) and the conv path
+ * of the verify page's KdaTcVerify.  q, k and v (kda_activations) are then
+ * the raw bands of the QKV projection.  Channels number the q band, then k,
+ * then v: C = (2*Hqk + Hv)*128, channel = band offset + head*128 + c.  Per
+ * channel, with history inputs h0, h1, h2 (oldest first) before the inputs
+ * x_t:  y_t = SiLU(w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t), rounded
+ * to bf16; with bf16 taps each product is rounded to bf16 and the four are
+ * summed in fp32 in tap order, with fp32 taps the sum is an fp32 fma chain
+ * (the verify page's "stock kernel's order").
+ *
+ *   weight        [C, 4] contiguous, 16-byte aligned: bf16, or fp32 when
+ *                 weight_f32 = 1 (the stock conv1d parameter)
+ *   state         bf16 conv state; element (row, position, channel) at
+ *                 state[row*row_stride + position*pos_stride +
+ *                 channel*chan_stride] (token major [rows, positions, C] or
+ *                 channel major [rows, C, positions], the verify page's
+ *                 conv_dim_first), updated in place by the call
+ *   rows, positions  its extent; prefill needs positions >= 3, verify
+ *                 positions >= window + 2
+ *   state_indices prefill: device int32 [n_seqs], the row of each sequence
+ *                 (negative: zero history and no update; >= rows sets
+ *                 KDA_ERR_DEVICE_INDEX, zero history, no update)
+ *   has_initial_state prefill: device uint8 [n_seqs] or NULL (= all true);
+ *                 0 starts that sequence from a zero history
+ *   num_accepted  verify: device int32 [n_req]; request b's history is at
+ *                 positions num_accepted[b]-1 .. num_accepted[b]+1 of row
+ *                 slots[b] (the verify page's accepted tokens)
+ * Prefill reads the history at positions 0..2 and leaves sequence n's last
+ * three raw inputs there (a sequence shorter than three keeps the tail of
+ * its history in front).  Verify leaves the rolled state: positions 0 and 1
+ * = the two newest history inputs, position 2 + t = raw input t of the
+ * window; an out-of-range num_accepted sets KDA_ERR_DEVICE_INDEX and the
+ * request is treated as padding.  The conv-state update runs as its own
+ * launch after every history has been read.
+ */
+typedef struct kda_conv {
+  const void* weight;
+  int32_t weight_f32;
+  void* state;
+  int64_t row_stride, pos_stride, chan_stride;
+  int64_t rows;
+  int32_t positions;
+  const int32_t* state_indices;
+  const uint8_t* has_initial_state;
+  const int32_t* num_accepted;
+} kda_conv;
+
+/*
  * kda_chunk_workspace_bytes - device scratch needed by kda_chunk_fwd.
  *   n_seqs  number of sequences; t_total total tokens; hv value heads;
  *   groups  chunk groups per sequence for the parallel scan (the same value
@@ -157,6 +208,8 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
  *   checkpoint_state_indices device int32 [n_seqs] destination rows, or NULL
  *                         (row n); a negative row disables that sequence's
  *                         snapshot
+ *   conv                  the conv applied to q, k, v first (see kda_conv),
+ *                         or NULL
  * Writing a snapshot row that the same call also uses as a state cache row
  * of another sequence is a race.
  */
@@ -166,8 +219,8 @@ int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seql
                      const int32_t* state_indices, const uint8_t* has_initial_state,
                      float* checkpoint_state, int64_t checkpoint_row_stride,
                      int64_t checkpoint_rows, const int32_t* checkpoint_offsets,
-                     const int32_t* checkpoint_state_indices, int32_t groups,
-                     void* workspace, size_t workspace_bytes, void* stream);
+                     const int32_t* checkpoint_state_indices, const kda_conv* conv,
+                     int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * kda_chunk_fwd_noalloc - kda_chunk_fwd for callers that cannot allocate
@@ -266,6 +319,22 @@ int kda_verify(const kda_activations* x, void* out, const float* state_pool,
                int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
                const int32_t* slots, int32_t n_req, int32_t window, float* corr,
                void* kg, int32_t* work_counter, void* stream);
+
+/*
+ * kda_verify_ex - kda_verify with the conv path of the verify page
+ * (KdaTcVerify with conv): q, k and v are the raw projection bands, each
+ * request's tokens are convolved (width 4, SiLU, see kda_conv) after the
+ * history at positions num_accepted[b]-1 .. num_accepted[b]+1 of conv row
+ * slots[b] (conv->rows >= n_slots, conv->positions >= window + 2,
+ * conv->num_accepted required), the recurrence runs on the convolved
+ * values, the kg record holds the convolved k, and the conv state is left
+ * rolled.  conv NULL: exactly kda_verify.  The SSM state pool is still only
+ * read.
+ */
+int kda_verify_ex(const kda_activations* x, void* out, const float* state_pool,
+                  int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
+                  const int32_t* slots, int32_t n_req, int32_t window, float* corr,
+                  void* kg, int32_t* work_counter, const kda_conv* conv, void* stream);
 
 /*
  * kda_commit - speculative-decode commit: rebuild each request's state after

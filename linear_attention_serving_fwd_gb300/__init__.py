@@ -100,6 +100,45 @@ def _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound):
     return a, (A_log, dt_bias)  # keep contiguous copies alive
 
 
+def _conv(conv_weight, conv_state, conv_dim_first, hqk, hv, *, state_indices=None,
+          has_initial_state=None, num_accepted=None):
+    """The kda_conv descriptor (or None) and the tensors it points into."""
+    if conv_weight is None and conv_state is None:
+        return None, []
+    if conv_weight is None or conv_state is None:
+        raise ValueError("conv_weight and conv_state must be given together.")
+    C = (2 * hqk + hv) * D
+    w = conv_weight.reshape(C, 4).contiguous()
+    if w.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("conv_weight must be bfloat16 or float32.")
+    if conv_state.dtype != torch.bfloat16 or conv_state.dim() != 3:
+        raise ValueError("conv_state must be a bfloat16 [rows, positions, C] (or [rows, C, positions] "
+                         "with conv_dim_first) tensor.")
+    ch_dim, pos_dim = (1, 2) if conv_dim_first else (2, 1)
+    if conv_state.shape[ch_dim] != C:
+        raise ValueError(f"conv_state needs {C} channels (2 Hqk + Hv bands of 128).")
+    cv = _native.KdaConv()
+    cv.weight, cv.weight_f32 = w.data_ptr(), int(w.dtype == torch.float32)
+    cv.state = conv_state.data_ptr()
+    cv.row_stride, cv.pos_stride = conv_state.stride(0), conv_state.stride(pos_dim)
+    cv.chan_stride = conv_state.stride(ch_dim)
+    cv.rows, cv.positions = conv_state.shape[0], conv_state.shape[pos_dim]
+    keep = [w]
+    if state_indices is not None:
+        state_indices = state_indices.to(torch.int32).contiguous()
+        keep.append(state_indices)
+        cv.state_indices = state_indices.data_ptr()
+    if has_initial_state is not None:
+        has_initial_state = has_initial_state.to(torch.uint8).contiguous()
+        keep.append(has_initial_state)
+        cv.has_initial_state = has_initial_state.data_ptr()
+    if num_accepted is not None:
+        num_accepted = num_accepted.to(torch.int32).contiguous()
+        keep.append(num_accepted)
+        cv.num_accepted = num_accepted.data_ptr()
+    return cv, keep
+
+
 def chunk_workspace_bytes(n_seqs: int, t_total: int, hv: int, groups: int = 0) -> int:
     return int(_native.lib().kda_chunk_workspace_bytes(n_seqs, t_total, hv, groups))
 
@@ -108,7 +147,9 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
                   cu_seqlens=None, n_seqs=None, initial_state=None, output_final_state=False,
                   final_state=None, out=None, state_cache=None, state_indices=None,
                   has_initial_state=None, groups: int = 0, workspace=None, stream=None,
-                  checkpoint_state=None, checkpoint_offsets=None, checkpoint_state_indices=None):
+                  checkpoint_state=None, checkpoint_offsets=None, checkpoint_state_indices=None,
+                  conv_weight=None, conv_state=None, conv_state_indices=None,
+                  conv_has_initial_state=None, conv_dim_first=False):
     """Chunked KDA prefill.  Returns (out, final_state or None).
 
     q, k: [T, Hqk, 128] or [B, T, Hqk, 128]; v, g: [T, Hv, 128]; beta:
@@ -120,6 +161,12 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     [N] (and optional ``checkpoint_state_indices`` [N]) receives each
     sequence's state after its first checkpoint_offsets[n] tokens (a positive
     multiple of 64 no larger than its length; other offsets are skipped).
+    ``conv_weight`` [C, 4] (bf16 or fp32) with ``conv_state`` bf16
+    [rows, positions >= 3, C] (``conv_dim_first``: [rows, C, positions]) and
+    ``conv_state_indices`` [N] makes q, k, v the raw projection bands
+    (C = (2 Hqk + Hv) * 128): they pass a width-4 depthwise conv and SiLU
+    first, and each sequence's conv row is left holding its last three raw
+    inputs.
     """
     dense_b = q.shape[0] if q.dim() == 4 else None
     q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
@@ -158,23 +205,30 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ck_stride, ck_rows = 0, 0
-    if checkpoint_state is not None:
-        if checkpoint_offsets is None:
-            raise ValueError("checkpoint_state needs checkpoint_offsets.")
-        if checkpoint_state.dtype != torch.float32:
-            raise TypeError("checkpoint_state must be float32.")
-        if tuple(checkpoint_state.shape[1:]) != (hv, D, D) or checkpoint_state[0].stride() != (D * D, D, 1):
-            raise ValueError("checkpoint_state must be [rows, Hv, 128, 128] with contiguous rows.")
-        ck_stride, ck_rows = checkpoint_state.stride(0), checkpoint_state.shape[0]
-        checkpoint_offsets = checkpoint_offsets.to(torch.int32).contiguous()
-        if checkpoint_state_indices is not None:
-            checkpoint_state_indices = checkpoint_state_indices.to(torch.int32).contiguous()
+    cv, cv_keep = _conv(conv_weight, conv_state, conv_dim_first, a.hqk, hv,
+                        state_indices=conv_state_indices, has_initial_state=conv_has_initial_state)
+    if cv is not None and conv_state_indices is None:
+        raise ValueError("conv_state needs conv_state_indices.")
+    if checkpoint_state is not None or cv is not None:
+        if checkpoint_state is not None:
+            if checkpoint_offsets is None:
+                raise ValueError("checkpoint_state needs checkpoint_offsets.")
+            if checkpoint_state.dtype != torch.float32:
+                raise TypeError("checkpoint_state must be float32.")
+            if (tuple(checkpoint_state.shape[1:]) != (hv, D, D)
+                    or checkpoint_state[0].stride() != (D * D, D, 1)):
+                raise ValueError("checkpoint_state must be [rows, Hv, 128, 128] with contiguous rows.")
+            ck_stride, ck_rows = checkpoint_state.stride(0), checkpoint_state.shape[0]
+            checkpoint_offsets = checkpoint_offsets.to(torch.int32).contiguous()
+            if checkpoint_state_indices is not None:
+                checkpoint_state_indices = checkpoint_state_indices.to(torch.int32).contiguous()
         rc = _native.lib().kda_chunk_fwd_ex(
             ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
             _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
             _ptr(checkpoint_state), ck_stride, ck_rows, _ptr(checkpoint_offsets),
-            _ptr(checkpoint_state_indices), int(groups), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+            _ptr(checkpoint_state_indices), None if cv is None else ctypes.byref(cv), int(groups),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        del cv_keep
     else:
         rc = _native.lib().kda_chunk_fwd(
             ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
@@ -219,7 +273,7 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, out, A_log=None, dt_bias=None, sc
 
 def _window_call(verify, q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log,
                  dt_bias, scale, lower_bound, out, corr, kg, work_counter, stream,
-                 num_accepted_tokens=None):
+                 num_accepted_tokens=None, conv_weight=None, conv_state=None, conv_dim_first=False):
     a, keep = _activations(_as_tokens(q, "q"), _as_tokens(k, "k"), _as_tokens(v, "v"),
                            _as_tokens(g, "g"), _as_tokens(beta, "beta", heads_dim=False),
                            A_log, dt_bias, scale, lower_bound)
@@ -249,9 +303,20 @@ def _window_call(verify, q, k, v, g, beta, state_pool, query_start, slots, windo
             kg = torch.empty((n_req, hv, window, 2 * D), dtype=q.dtype, device=q.device)
         if work_counter is None:
             work_counter = torch.zeros(1, dtype=torch.int32, device=q.device)
-        rc = lib.kda_verify(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
-                            state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
-                            _ptr(corr), _ptr(kg), _ptr(work_counter), _stream_handle(stream))
+        cv, cv_keep = _conv(conv_weight, conv_state, conv_dim_first, a.hqk, hv,
+                            num_accepted=num_accepted_tokens)
+        if cv is not None:
+            if num_accepted_tokens is None:
+                raise ValueError("verify with a conv needs num_accepted_tokens.")
+            rc = lib.kda_verify_ex(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
+                                   state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
+                                   _ptr(corr), _ptr(kg), _ptr(work_counter), ctypes.byref(cv),
+                                   _stream_handle(stream))
+            del cv_keep
+        else:
+            rc = lib.kda_verify(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
+                                state_pool.shape[0], _ptr(query_start), _ptr(slots), n_req, window,
+                                _ptr(corr), _ptr(kg), _ptr(work_counter), _stream_handle(stream))
     elif table:
         rc = lib.kda_decode_steps(ctypes.byref(a), _ptr(out), _ptr(state_pool), state_pool.stride(0),
                                   state_pool.shape[0], _ptr(query_start), _ptr(slots),
@@ -293,11 +358,20 @@ def kda_decode_steps(q, k, v, g, beta, state_pool, query_start, state_indices, w
 
 def kda_verify(q, k, v, g, beta, state_pool, query_start, slots, window, *, A_log=None,
                dt_bias=None, scale=None, lower_bound=-5.0, out=None, corr=None, kg=None,
-               work_counter=None, stream=None):
-    """Speculative verify (state read only).  Returns (out, corr, kg)."""
+               work_counter=None, stream=None, conv_weight=None, conv_state=None,
+               num_accepted_tokens=None, conv_dim_first=False):
+    """Speculative verify (state read only).  Returns (out, corr, kg).
+
+    With ``conv_weight`` [C, 4] and ``conv_state`` bf16 [slots, positions >=
+    window + 2, C] (``conv_dim_first``: [slots, C, positions]) and
+    ``num_accepted_tokens`` [n_req], q, k, v are the raw projection bands:
+    they pass the width-4 conv + SiLU after the history at positions
+    accepted-1 .. accepted+1 of row slots[b], and the conv state is rolled."""
     return _window_call(True, q, k, v, g, beta, state_pool, query_start, slots, window,
                         A_log=A_log, dt_bias=dt_bias, scale=scale, lower_bound=lower_bound,
-                        out=out, corr=corr, kg=kg, work_counter=work_counter, stream=stream)
+                        out=out, corr=corr, kg=kg, work_counter=work_counter, stream=stream,
+                        num_accepted_tokens=num_accepted_tokens, conv_weight=conv_weight,
+                        conv_state=conv_state, conv_dim_first=conv_dim_first)
 
 
 def kda_commit(state_pool, slots, num_accepted, corr, kg, window, *, A_log=None, dt_bias=None,

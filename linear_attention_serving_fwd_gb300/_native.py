@@ -27,7 +27,7 @@ KDA_DTYPE_FP16 = 1
 EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_verify",
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
            "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
-           "kda_decode_steps")
+           "kda_decode_steps", "kda_verify_ex")
 
 
 class KdaActivations(ctypes.Structure):
@@ -46,6 +46,18 @@ class KdaActivations(ctypes.Structure):
     ]
 
 
+class KdaConv(ctypes.Structure):
+    _fields_ = [
+        ("weight", ctypes.c_void_p), ("weight_f32", ctypes.c_int32),
+        ("state", ctypes.c_void_p),
+        ("row_stride", ctypes.c_int64), ("pos_stride", ctypes.c_int64),
+        ("chan_stride", ctypes.c_int64), ("rows", ctypes.c_int64),
+        ("positions", ctypes.c_int32),
+        ("state_indices", ctypes.c_void_p), ("has_initial_state", ctypes.c_void_p),
+        ("num_accepted", ctypes.c_void_p),
+    ]
+
+
 class KdaError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"[kda status {code}] {msg}")
@@ -59,7 +71,9 @@ def _declare(lib):
     lib.kda_chunk_workspace_bytes.restype = SZ
     lib.kda_chunk_fwd.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, I32, P, SZ, P]
     lib.kda_chunk_fwd.restype = ctypes.c_int
-    lib.kda_chunk_fwd_ex.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, P, I64, I64, P, P, I32, P, SZ, P]
+    CV = ctypes.POINTER(KdaConv)
+    lib.kda_chunk_fwd_ex.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, P, I64, I64, P, P, CV, I32, P,
+                                     SZ, P]
     lib.kda_chunk_fwd_ex.restype = ctypes.c_int
     lib.kda_chunk_fwd_noalloc.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, I32, P]
     lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
@@ -69,6 +83,8 @@ def _declare(lib):
     lib.kda_decode_steps.restype = ctypes.c_int
     lib.kda_verify.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P, P, P, P]
     lib.kda_verify.restype = ctypes.c_int
+    lib.kda_verify_ex.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P, P, P, CV, P]
+    lib.kda_verify_ex.restype = ctypes.c_int
     lib.kda_commit.argtypes = [P, I64, I64, P, P, I32, I32, I32, P, P, P, P, ctypes.c_float, P]
     lib.kda_commit.restype = ctypes.c_int
     lib.kda_last_error.argtypes = []

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
-SOURCES = ["kda_api.cu", "kda_window.cu", "kda_chunk.cu", "kda_noalloc.cu", "kda_commit.cu"]
+SOURCES = ["kda_api.cu", "kda_window.cu", "kda_chunk.cu", "kda_noalloc.cu", "kda_commit.cu", "kda_conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-diag-suppress", "550"]

@@ -248,14 +248,57 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
   return 4 * kda::chunk_workspace_floats(n_seqs, t_total, hv, G, nullptr);
 }
 
+// Host rules of a kda_conv; fills cp (state == nullptr when conv is NULL).
+static int check_conv(const kda_conv* conv, const kda_activations* x, bool verify, int32_t window,
+                      int64_t n_slots, kda::ConvParams& cp) {
+  memset(&cp, 0, sizeof(cp));
+  if (!conv) return KDA_OK;
+  if (!conv->weight || !conv->state)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "conv weight and state must not be NULL.");
+  if (!aligned16(conv->weight)) return fail(KDA_ERR_INVALID_ARGUMENT, "conv weight must be 16-byte aligned.");
+  if (conv->weight_f32 != 0 && conv->weight_f32 != 1)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "conv weight_f32 must be 0 (bf16 taps) or 1 (fp32 taps).");
+  if (conv->rows <= 0 || conv->row_stride <= 0 || conv->pos_stride <= 0 || conv->chan_stride <= 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "conv state rows and strides must be positive.");
+  const int need = verify ? window + 2 : 3;
+  if (conv->positions < need)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "conv state needs at least %d positions (got %d).", need,
+                conv->positions);
+  if (verify) {
+    if (!conv->num_accepted) return fail(KDA_ERR_INVALID_ARGUMENT, "verify with a conv needs num_accepted.");
+    if (conv->rows < n_slots)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "conv state needs a row per state slot (%lld < %lld).",
+                  (long long)conv->rows, (long long)n_slots);
+  } else if (!conv->state_indices) {
+    return fail(KDA_ERR_INVALID_ARGUMENT, "prefill with a conv needs conv state_indices.");
+  }
+  (void)x;
+  cp.w = conv->weight;
+  cp.w_f32 = conv->weight_f32;
+  cp.state = static_cast<__nv_bfloat16*>(conv->state);
+  cp.row_st = conv->row_stride;
+  cp.pos_st = conv->pos_stride;
+  cp.ch_st = conv->chan_stride;
+  cp.rows = conv->rows;
+  cp.positions = conv->positions;
+  cp.idx = conv->state_indices;
+  cp.has_init = conv->has_initial_state;
+  cp.accepted = conv->num_accepted;
+  return KDA_OK;
+}
+
 static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
                         const float* initial_state, float* final_state, float* state_cache,
                         int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
                         const uint8_t* has_initial_state, float* checkpoint_state,
                         int64_t checkpoint_row_stride, int64_t checkpoint_rows,
                         const int32_t* checkpoint_offsets, const int32_t* checkpoint_state_indices,
-                        int32_t groups, void* workspace, size_t workspace_bytes, void* stream) {
+                        const kda_conv* conv, int32_t groups, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   int rc = check_activations(x, true);
+  if (rc) return rc;
+  kda::ConvParams cp;
+  rc = check_conv(conv, x, false, 0, 0, cp);
   if (rc) return rc;
   if (n_seqs <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs must be >= 1.");
   if (!cu_seqlens && x->t_total % n_seqs != 0)
@@ -314,6 +357,7 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
   p.sm_count = device_sm_count();
   p.ckpt = checkpoint_state; p.ckpt_stride = checkpoint_row_stride; p.ckpt_rows = checkpoint_rows;
   p.ckpt_off = checkpoint_offsets; p.ckpt_idx = checkpoint_state_indices;
+  p.conv = cp;
   p.err = err;
   const int lrc = kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream));
   if (lrc == -2) return KDA_ERR_INVALID_ARGUMENT;  // message set by the launcher
@@ -327,8 +371,8 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
                   const uint8_t* has_initial_state, int32_t groups, void* workspace,
                   size_t workspace_bytes, void* stream) {
   return chunk_common(x, out, cu_seqlens, n_seqs, initial_state, final_state, state_cache, slot_stride,
-                      n_slots, state_indices, has_initial_state, nullptr, 0, 0, nullptr, nullptr, groups,
-                      workspace, workspace_bytes, stream);
+                      n_slots, state_indices, has_initial_state, nullptr, 0, 0, nullptr, nullptr, nullptr,
+                      groups, workspace, workspace_bytes, stream);
 }
 
 int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
@@ -337,10 +381,11 @@ int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seql
                      const uint8_t* has_initial_state, float* checkpoint_state,
                      int64_t checkpoint_row_stride, int64_t checkpoint_rows,
                      const int32_t* checkpoint_offsets, const int32_t* checkpoint_state_indices,
-                     int32_t groups, void* workspace, size_t workspace_bytes, void* stream) {
+                     const kda_conv* conv, int32_t groups, void* workspace, size_t workspace_bytes,
+                     void* stream) {
   return chunk_common(x, out, cu_seqlens, n_seqs, initial_state, final_state, state_cache, slot_stride,
                       n_slots, state_indices, has_initial_state, checkpoint_state, checkpoint_row_stride,
-                      checkpoint_rows, checkpoint_offsets, checkpoint_state_indices, groups, workspace,
+                      checkpoint_rows, checkpoint_offsets, checkpoint_state_indices, conv, groups, workspace,
                       workspace_bytes, stream);
 }
 
@@ -348,8 +393,12 @@ static int window_common(const kda_activations* x, void* out, const float* pool,
                          int64_t n_slots, const int32_t* query_start, const int32_t* slots,
                          int32_t n_req, int32_t window, bool verify, float* corr, void* kg,
                          int32_t* counter, void* stream, const int32_t* step_slots = nullptr,
-                         int64_t step_stride = 0, const int32_t* n_accepted = nullptr) {
+                         int64_t step_stride = 0, const int32_t* n_accepted = nullptr,
+                         const kda_conv* conv = nullptr) {
   int rc = check_activations(x, true);
+  if (rc) return rc;
+  kda::ConvParams cp;
+  rc = check_conv(conv, x, true, window, n_slots, cp);
   if (rc) return rc;
   if (window < 1 || window > kda::MAX_WINDOW)
     return fail(KDA_ERR_INVALID_ARGUMENT, "window must satisfy 1 <= window <= 8 (got %d).", window);
@@ -385,6 +434,7 @@ static int window_common(const kda_activations* x, void* out, const float* pool,
   p.slot_stride = slot_stride; p.n_slots = n_slots;
   p.query_start = query_start; p.slots = slots;
   p.step_slots = step_slots; p.step_stride = step_stride; p.n_accepted = n_accepted;
+  p.conv = cp;
   p.n_req = n_req; p.window = window; p.hqk = x->hqk; p.hv = x->hv;
   p.corr = corr; p.kg = static_cast<__nv_bfloat16*>(kg); p.counter = counter;
   p.err = err;
@@ -416,6 +466,14 @@ int kda_verify(const kda_activations* x, void* out, const float* state_pool, int
                int32_t window, float* corr, void* kg, int32_t* work_counter, void* stream) {
   return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req,
                        window, true, corr, kg, work_counter, stream);
+}
+
+int kda_verify_ex(const kda_activations* x, void* out, const float* state_pool, int64_t slot_stride,
+                  int64_t n_slots, const int32_t* query_start, const int32_t* slots, int32_t n_req,
+                  int32_t window, float* corr, void* kg, int32_t* work_counter, const kda_conv* conv,
+                  void* stream) {
+  return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req, window, true,
+                       corr, kg, work_counter, stream, nullptr, 0, nullptr, conv);
 }
 
 int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const int32_t* slots,

@@ -39,6 +39,7 @@
 #include <cuda.h>  // CUtensorMap (types only; the encoder comes via the runtime)
 #include <cudaTypedefs.h>
 
+#include "kda_conv.cuh"
 #include "kda_params.cuh"
 #include "kda_tc.cuh"
 
@@ -158,7 +159,7 @@ constexpr uint32_t P_W = 34816;      // fp32 [32][LDW]  temporary product
 constexpr uint32_t P_A3 = 17408;     // fp16 [128][128] = [[T, 0], [-A_qk T, I]], over A and W
 constexpr uint32_t P_A2 = 50176;     // fp16 [128][64]  = [A_qk ; 0]
 constexpr uint32_t P_B2 = 66560;     // fp16 [64][64]   = T^T
-constexpr uint32_t P_TILES = 75776;  // bf16 [4][64][128]: q, k, g, v of the next item
+constexpr uint32_t P_TILES = 75776;  // bf16 tiles of the next item (below)
 constexpr uint32_t P_WT = 0;         // fp16 w^T, MN-major [k'][r] (over L^{-1} once dead)
 constexpr uint32_t WT_LBO = 128, WT_SBO = 1024;  // its 8-row r groups / 8-column k' groups
 static_assert(P_LI + 64 * LDT * 4 <= P_A && P_A + 64 * LDT * 4 <= P_W, "prologue carve");
@@ -185,7 +186,15 @@ struct __align__(1024) ProSmem {
   uint32_t tmem;
   int abort;
 };
-static_assert(P_TILES + 4 * 64 * D * 2 <= sizeof(ProSmem::XY), "carve fits");
+// The tiles: q, k, v, each HALO rows (the three tokens before the chunk,
+// which a conv reads) then the chunk's 64 rows, then g (64 rows).
+constexpr int HALO = 3;
+constexpr int TILE_QKV = (HALO + CHUNK) * D;  // elements of a q / k / v tile (17,152 bytes)
+static_assert(P_TILES + (3 * TILE_QKV + CHUNK * D) * 2 <= sizeof(ProSmem::XY), "carve fits");
+static_assert((P_TILES + HALO * D * 2) % 128 == 0 && (TILE_QKV * 2) % 128 == 0, "TMA tile alignment");
+// row r (from -HALO) of band x (0 q, 1 k, 2 v) / row r of g
+__device__ __forceinline__ int tile_row(int x, int r) { return x * TILE_QKV + (HALO + r) * D; }
+__device__ __forceinline__ int g_row(int r) { return 3 * TILE_QKV + r * D; }
 
 // item t = chunk * Hv + head
 __device__ __forceinline__ int4 item_meta(const ChunkParams& p, int t) {
@@ -210,18 +219,66 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// One item's q, k, g, v rows (bf16, 64 x 128 each) into ``tiles`` with four
-// tiled TMA loads completing on ``bar`` (one thread).  Tokens past T arrive
-// as zeros; rows past the sequence end hold the next sequence's tokens and
-// readers mask them.
+// One item's q, k, v, g rows (bf16, 64 x 128 each) into ``tiles`` with four
+// tiled TMA loads completing on ``bar`` (one thread).  With a conv the q, k,
+// v boxes start three tokens early (HALO rows: the conv's history inside a
+// sequence; at a sequence start the conv phase replaces them).  Tokens
+// before 0 or past T arrive as zeros; rows past the sequence end hold the
+// next sequence's tokens and readers mask them.
+template <bool CONV>
 __device__ __forceinline__ void load_tiles(const ChunkParams& p, const TileMaps& maps, int4 m,
                                            __nv_bfloat16* tiles, uint64_t* bar) {
   const int h = m.y, bos = m.z, hq = h / (p.hv / p.hqk);
-  mbar_arrive_expect_tx(bar, 4u * 64u * D * 2u);
-  tma_load_3d(tiles + 0 * 64 * D, &maps.q, 0, hq, bos, bar);
-  tma_load_3d(tiles + 1 * 64 * D, &maps.k, 0, hq, bos, bar);
-  tma_load_3d(tiles + 2 * 64 * D, &maps.g, 0, h, bos, bar);
-  tma_load_3d(tiles + 3 * 64 * D, &maps.v, 0, h, bos, bar);
+  constexpr int halo = CONV ? HALO : 0;
+  mbar_arrive_expect_tx(bar, (uint32_t)((3 * (CHUNK + halo) + CHUNK) * D * 2));
+  tma_load_3d(tiles + tile_row(0, -halo), &maps.q, 0, hq, bos - halo, bar);
+  tma_load_3d(tiles + tile_row(1, -halo), &maps.k, 0, hq, bos - halo, bar);
+  tma_load_3d(tiles + tile_row(2, -halo), &maps.v, 0, h, bos - halo, bar);
+  tma_load_3d(tiles + g_row(0), &maps.g, 0, h, bos, bar);
+}
+
+// Width-4 conv + SiLU of the item's q, k, v tiles, in place (conv mode).
+// Thread (channel c, sub-chunk Rq) computes rows 16 Rq .. +15 of the three
+// bands from the raw rows 16 Rq - 3 .. 16 Rq + 15; at a sequence's first
+// chunk the HALO rows are first replaced by the conv state's history
+// (zeros without one).  Ends with a barrier.
+__device__ __forceinline__ void conv_tiles(const ChunkParams& p, __nv_bfloat16* tiles, int c_glob, int h,
+                                        int tid) {
+  const ConvParams& cv = p.conv;
+  const int c = tid & 127, Rq = tid >> 7;
+  int64_t ch[3];
+  conv_channels(p.hqk, p.hv, h, c, ch);
+  if (p.chunk_j[c_glob] == 0 && Rq < 3) {
+    const int n = p.chunk_seq[c_glob];
+    const int row = cv.idx[n];
+    const bool init = row >= 0 && row < cv.rows && (!cv.has_init || cv.has_init[n]);
+    const int64_t chx = Rq == 0 ? ch[0] : (Rq == 1 ? ch[1] : ch[2]);
+    const __nv_bfloat16* src = cv.state + (int64_t)row * cv.row_st + chx * cv.ch_st;
+#pragma unroll
+    for (int i = 0; i < HALO; ++i)
+      tiles[tile_row(Rq, i - HALO) + c] = init ? src[i * cv.pos_st] : __float2bfloat16(0.f);
+  }
+  __syncthreads();
+  __nv_bfloat162 y[3][8];  // outputs, rows in pairs
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    const float4 w = conv_taps(cv, ch[x]);
+    const __nv_bfloat16* col = tiles + tile_row(x, 16 * Rq - HALO) + c;
+    __nv_bfloat16 win[16 + HALO];  // rows 16 Rq - 3 .. 16 Rq + 15
+#pragma unroll
+    for (int i = 0; i < 16 + HALO; ++i) win[i] = col[i * D];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) y[x][i >> 1] = conv_silu2(cv.w_f32, w, win + i);
+  }
+  __syncthreads();  // every raw row read
+#pragma unroll
+  for (int x = 0; x < 3; ++x)
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      tiles[tile_row(x, 16 * Rq + i) + c] = y[x][i >> 1].x;
+      tiles[tile_row(x, 16 * Rq + i + 1) + c] = y[x][i >> 1].y;
+    }
+  __syncthreads();
 }
 
 // The item's raw per-row beta (threads 0..63), dt_bias of channel tid % 128
@@ -240,6 +297,7 @@ __device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m
   return r;
 }
 
+template <bool CONV>
 __global__ void __launch_bounds__(PRO_THREADS, 1)
     kda_prologue_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -259,7 +317,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     fence_mbar_init();
     s.abort = 0;
     s.meta[0] = item_meta(p, blockIdx.x);
-    load_tiles(p, maps, s.meta[0], tiles, &s.tbar);
+    load_tiles<CONV>(p, maps, s.meta[0], tiles, &s.tbar);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -279,6 +337,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     wait_or_abort(&s.tbar, tile_phase, &s.abort, p.err);
     tile_phase ^= 1u;
     __syncthreads();
+    if constexpr (CONV) conv_tiles(p, tiles, c_glob, h, tid);
 
     // ---- phase 1: channel-owner, thread = (channel c, sub-chunk Rq) ----------
     const int c = tid & 127, Rq = tid >> 7;
@@ -292,12 +351,12 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       for (int i = 0; i < 16; i += 2) {
         const int r = 16 * Rq + i;
         const bool in0 = r < len, in1 = r + 1 < len;
-        qv[i] = in0 ? bf2f(tiles[(0 * 64 + r) * D + c]) : 0.f;
-        qv[i + 1] = in1 ? bf2f(tiles[(0 * 64 + r + 1) * D + c]) : 0.f;
-        kv[i] = in0 ? bf2f(tiles[(1 * 64 + r) * D + c]) : 0.f;
-        kv[i + 1] = in1 ? bf2f(tiles[(1 * 64 + r + 1) * D + c]) : 0.f;
-        float2 g = make_float2(in0 ? bf2f(tiles[(2 * 64 + r) * D + c]) : 0.f,
-                               in1 ? bf2f(tiles[(2 * 64 + r + 1) * D + c]) : 0.f);
+        qv[i] = in0 ? bf2f(tiles[tile_row(0, r) + c]) : 0.f;
+        qv[i + 1] = in1 ? bf2f(tiles[tile_row(0, r + 1) + c]) : 0.f;
+        kv[i] = in0 ? bf2f(tiles[tile_row(1, r) + c]) : 0.f;
+        kv[i + 1] = in1 ? bf2f(tiles[tile_row(1, r + 1) + c]) : 0.f;
+        float2 g = make_float2(in0 ? bf2f(tiles[g_row(r) + c]) : 0.f,
+                               in1 ? bf2f(tiles[g_row(r + 1) + c]) : 0.f);
         if (p.has_gate) {  // lower_bound * sigmoid(a (g + dt_bias)), in pairs
           const float2 t = ffma2(ah2, g, adt2);
           const float2 den = fadd2(make_float2(__expf(-t.x), __expf(-t.y)), make_float2(1.f, 1.f));
@@ -308,8 +367,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         lam[i] = acc;
         acc += g.y;
         lam[i + 1] = acc;
-        vw[i >> 1] = pack_half2(in0 ? bf2f(tiles[(3 * 64 + r) * D + c]) : 0.f,
-                                in1 ? bf2f(tiles[(3 * 64 + r + 1) * D + c]) : 0.f);
+        vw[i >> 1] = pack_half2(in0 ? bf2f(tiles[tile_row(2, r) + c]) : 0.f,
+                                in1 ? bf2f(tiles[tile_row(2, r + 1) + c]) : 0.f);
       }
       // v^T of this column: the record's block c / 32, and VT for o_intra
 #pragma unroll
@@ -506,7 +565,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     // the next item's rows stream in behind the carve
     if (has_next) {
       const int4 mn = s.meta[cur ^ 1];
-      if (tid == 96) load_tiles(p, maps, mn, tiles, &s.tbar);  // a warp idle in the diagonal solve
+      if (tid == 96) load_tiles<CONV>(p, maps, mn, tiles, &s.tbar);  // a warp idle in the diagonal solve
       tiles_issued += 1;
       sc = load_scalars(p, mn, tid);
     }
@@ -1147,14 +1206,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// rows of ``heads`` x 128 bf16 per token: dims (128, heads, T), box (128, 1, 64)
+// rows of ``heads`` x 128 bf16 per token: dims (128, heads, T), box (128, 1, rows)
 static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, int64_t st_head,
-                        int64_t st_tok) {
+                        int64_t st_tok, int rows = CHUNK) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)T};
   const cuuint64_t strides[2] = {(cuuint64_t)st_head * 2, (cuuint64_t)st_tok * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)CHUNK};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)rows};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1164,7 +1223,9 @@ static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, in
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   static bool attrs = false;
   if (!attrs) {
-    cudaFuncSetAttribute(kda_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(kda_prologue_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(ProSmem));
+    cudaFuncSetAttribute(kda_prologue_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(ProSmem));
     cudaFuncSetAttribute(kda_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(WalkSmem));
@@ -1193,10 +1254,11 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
   trace_end(stream);
   TileMaps maps;
-  if (!encode_rows(&maps.q, p.q, p.hqk, p.t_total, p.q_sh, p.q_st) ||
-      !encode_rows(&maps.k, p.k, p.hqk, p.t_total, p.k_sh, p.k_st) ||
+  const int qkv_rows = CHUNK + (p.conv.state ? HALO : 0);
+  if (!encode_rows(&maps.q, p.q, p.hqk, p.t_total, p.q_sh, p.q_st, qkv_rows) ||
+      !encode_rows(&maps.k, p.k, p.hqk, p.t_total, p.k_sh, p.k_st, qkv_rows) ||
       !encode_rows(&maps.g, p.g, p.hv, p.t_total, p.g_sh, p.g_st) ||
-      !encode_rows(&maps.v, p.v, p.hv, p.t_total, p.v_sh, p.v_st)) {
+      !encode_rows(&maps.v, p.v, p.hv, p.t_total, p.v_sh, p.v_st, qkv_rows)) {
     set_last_error(KDA_ERR_INVALID_ARGUMENT,
                    "kda_chunk_fwd: q/k/v/g layout cannot be described by a TMA tensor map "
                    "(strides must be positive multiples of 8 elements below 2^39 bytes).");
@@ -1205,8 +1267,14 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   trace_begin("kda_prologue", stream);
   const int items = max_chunks * p.hv;
   const int sms = p.sm_count > 0 ? p.sm_count : 152;
-  kda_prologue_kernel<<<items < sms ? items : sms, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+  const int grid = items < sms ? items : sms;
+  if (p.conv.state)
+    kda_prologue_kernel<true><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+  else
+    kda_prologue_kernel<false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
   trace_end(stream);
+  // the conv history of every sequence has been read: roll the conv state
+  if (p.conv.state && launch_conv_prefill_state(p, stream) != 0) return -1;
   if (p.groups > 1) {
     trace_begin("kda_walk_pass1", stream);
     kda_walk_kernel<<<dim3(2 * D / NB, p.hv, p.n_seqs * p.groups), WALK_THREADS,

@@ -5,6 +5,20 @@
 
 namespace kda {
 
+// Width-4 depthwise conv + SiLU over the raw q/k/v projection bands
+// (state == nullptr: off).  Channel ch of C = (2 Hqk + Hv) * 128 numbers the
+// q band, then k, then v (band offset + head * 128 + c).
+struct ConvParams {
+  const void* w;               // [C, 4] taps, bf16 or fp32 (w_f32)
+  int w_f32;
+  __nv_bfloat16* state;        // element (row, pos, ch) at row*row_st + pos*pos_st + ch*ch_st
+  int64_t row_st, pos_st, ch_st, rows;
+  int positions;
+  const int32_t* idx;          // prefill: [N] state row per sequence (< 0: zero history, no update)
+  const uint8_t* has_init;     // prefill: [N] or null (all rows hold a history)
+  const int32_t* accepted;     // verify: [n_req]; history at positions accepted-1 .. accepted+1
+};
+
 struct WindowParams {
   const __nv_bfloat16 *q, *k, *v, *g, *beta;
   int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh, g_st, g_sh, b_st, b_sh;
@@ -25,6 +39,7 @@ struct WindowParams {
   int64_t step_stride;
   const int32_t* n_accepted;
   int n_req, window, hqk, hv;
+  ConvParams conv;       // verify only
   float* corr;          // verify: [n_req, Hv, window, 128]
   __nv_bfloat16* kg;    // verify: [n_req, Hv, window, 256]
   int32_t* counter;     // verify: ticket counter
@@ -82,6 +97,7 @@ struct ChunkParams {
   int64_t ckpt_stride, ckpt_rows;
   const int32_t* ckpt_off;
   const int32_t* ckpt_idx;
+  ConvParams conv;
   unsigned* err;        // device error word
 };
 
@@ -97,6 +113,8 @@ void set_last_error(int code, const char* msg);
 // Launchers (kernels' translation units); return 0 or -1 (see cudaGetLastError).
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream);
 int launch_commit(const CommitParams& p, cudaStream_t stream);
+int launch_conv_prefill_state(const ChunkParams& p, cudaStream_t stream);
+int launch_conv_roll(const WindowParams& p, cudaStream_t stream);
 size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out);
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream);
 

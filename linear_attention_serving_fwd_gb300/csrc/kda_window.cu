@@ -28,10 +28,15 @@
 //   S <- diag(e^gate) S;  U = beta (v - S^T k^);  S <- S + k^ U^T;  o = S^T q~
 // computed as U = beta (v - S_old^T (e^gate * k^)),
 //             o = S_old^T (e^gate * q~) + U (k^ . q~),  S = e^gate * S_old + k^ U^T.
+// Verify with a conv (the verify page's conv path): q, k, v are the raw
+// projection bands; warp t first convolves token t's rows (width 4, SiLU)
+// with the history at the accepted column, the outputs replace the raw rows,
+// and a small kernel afterwards rolls the conv state.
 // Verify (the vLLM kimi_k3 CuTeDSL verify page, KdaTcVerify) additionally
 // writes corr = U_t and kg = (raw k_t, raw g_t) and never writes the state;
 // its persistent scheduler takes tickets from a caller-zeroed counter and the
 // taker of the last ticket resets it.
+#include "kda_conv.cuh"
 #include "kda_params.cuh"
 
 namespace kda {
@@ -88,6 +93,11 @@ __device__ __forceinline__ ItemInfo item_info(const WindowParams& p, int item) {
     r.slot = p.slots[r.request];
     r.wslot = r.slot;
     bad_slot = r.slot >= p.n_slots;
+  }
+  if (p.conv.state && r.slot >= 0 && !bad_len && r.qlen > 0) {
+    // verify with a conv: its history sits at positions accepted-1 .. +1
+    const int first = p.conv.accepted[r.request] - 1;
+    bad_slot |= first < 0 || first + 3 > p.conv.positions || r.slot >= p.conv.rows;
   }
   r.work = !bad_len && !bad_slot && r.slot >= 0 && r.qlen > 0;
   r.zero = !bad_len && r.qlen > 0 && !r.work;
@@ -177,6 +187,37 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
   if (lane == 0) {
     s.tkq[t] = kq;
     s.tbeta[t] = sigmoidf_(bf2f(ts.beta));
+  }
+}
+
+// Verify with a conv: warp t's conv + SiLU outputs for token t (lane = 4
+// channels of each band: q and k of the head's q/k head, v of the head),
+// from the window's raw rows and, for the taps before the window, the
+// history at positions accepted-1 .. accepted+1 of the slot's conv row.
+__device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo& it,
+                                           const __nv_bfloat16* ibuf, int t, int lane, float y[3][4]) {
+  const ConvParams& cv = p.conv;
+  const int first = cv.accepted[it.request] - 1;
+  int64_t ch[3];
+  conv_channels(p.hqk, p.hv, it.head, 4 * lane, ch);
+  const __nv_bfloat16* hist = cv.state + it.slot * cv.row_st;
+#pragma unroll
+  for (int x = 0; x < 3; ++x) {
+    float win[4][4];  // tap j reads token t - 3 + j
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int tt = t - 3 + j;
+      if (tt >= 0) {
+        load_bf16x4(ibuf + (tt * 4 + x) * D + 4 * lane, win[j]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          win[j][e] = bf2f(hist[(int64_t)(first + 3 + tt) * cv.pos_st + (ch[x] + e) * cv.ch_st]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      y[x][e] = conv_silu(cv.w_f32, conv_taps(cv, ch[x] + e), win[0][e], win[1][e], win[2][e], win[3][e]);
   }
 }
 
@@ -341,14 +382,21 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
   while (cur < items) {
     if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
     bool ok = true;
+    const bool conv = VERIFY && p.conv.state != nullptr;
     float2 S[4][4];
+    float yc[3][4];  // conv outputs of token ``warp`` (verify with a conv)
     if (it.work) {
       ok = mbar_wait_bounded(&s.sbar[b], sphase[b], p.err);
       ok = mbar_wait_bounded(&s.ibar[b], iphase[b], p.err) && ok;
       sphase[b] ^= 1u;
       iphase[b] ^= 1u;
       if (ok) {
-        if (warp < it.qlen) token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        if (warp < it.qlen) {
+          if (conv)
+            conv_token(p, it, s.in[b], warp, lane, yc);
+          else
+            token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -371,6 +419,22 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       }
       if (!VERIFY && tid == 0) bulk_wait<0>();
       return;
+    }
+    if (conv && it.work) {
+      // every raw row has been read: the conv outputs replace them, then
+      // the token vectors come from the convolved rows
+      if (warp < it.qlen) {
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(yc[x][0], yc[x][1]);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(yc[x][2], yc[x][3]);
+          *reinterpret_cast<uint2*>(s.in[b] + (warp * 4 + x) * D + 4 * lane) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+        }
+        __syncwarp();
+        token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+      }
+      __syncthreads();
     }
     const int nn = s.next;
     const ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
@@ -439,6 +503,8 @@ int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
   else
     kda_window_kernel<false><<<grid, WIN_THREADS, sizeof(WinSmem), stream>>>(p);
   trace_end(stream);
+  // verify with a conv: every history has been read, roll the conv state
+  if (verify && p.conv.state && launch_conv_roll(p, stream) != 0) return -1;
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

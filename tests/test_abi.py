@@ -105,12 +105,14 @@ def _chunk_ex(a, **kw):
     lib = _native.lib()
     args = dict(out=FAKE, cu=None, n=1, h0=None, hT=None, cache=None, stride=0, slots=0,
                 idx=None, hi=None, ck=None, ck_stride=0, ck_rows=0, ck_off=None, ck_idx=None,
-                groups=1, ws=FAKE, ws_bytes=1 << 40, stream=None)
+                conv=None, groups=1, ws=FAKE, ws_bytes=1 << 40, stream=None)
     args.update(kw)
     return lib.kda_chunk_fwd_ex(ctypes.byref(a), args["out"], args["cu"], args["n"], args["h0"],
                                 args["hT"], args["cache"], args["stride"], args["slots"],
                                 args["idx"], args["hi"], args["ck"], args["ck_stride"],
-                                args["ck_rows"], args["ck_off"], args["ck_idx"], args["groups"],
+                                args["ck_rows"], args["ck_off"], args["ck_idx"],
+                                None if args["conv"] is None else ctypes.byref(args["conv"]),
+                                args["groups"],
                                 args["ws"], args["ws_bytes"], args["stream"])
 
 
@@ -131,6 +133,35 @@ def test_checkpoint_argument_rules():
     assert "checkpoint_state must contain" in _msg()
     assert _chunk_ex(a, ck=FAKE + 4, ck_stride=row, ck_rows=1, ck_off=FAKE) == INVALID
     assert "checkpoint_state must be 16-byte aligned" in _msg()
+
+
+def _conv_desc(**over):
+    cv = _native.KdaConv()
+    cv.weight, cv.weight_f32, cv.state = FAKE, 0, FAKE
+    cv.row_stride, cv.pos_stride, cv.chan_stride = 10 * 1024, 1024, 1
+    cv.rows, cv.positions = 4, 10
+    cv.state_indices, cv.has_initial_state, cv.num_accepted = FAKE, None, FAKE
+    for k, v in over.items():
+        setattr(cv, k, v)
+    return cv
+
+
+def test_conv_argument_rules():
+    a = _acts()
+    assert _chunk_ex(a, conv=_conv_desc(weight=None)) == INVALID and "conv weight" in _msg()
+    assert _chunk_ex(a, conv=_conv_desc(weight=FAKE + 8)) == INVALID and "16-byte" in _msg()
+    assert _chunk_ex(a, conv=_conv_desc(weight_f32=2)) == INVALID and "weight_f32" in _msg()
+    assert _chunk_ex(a, conv=_conv_desc(positions=2)) == INVALID and "at least 3 positions" in _msg()
+    assert _chunk_ex(a, conv=_conv_desc(state_indices=None)) == INVALID and "state_indices" in _msg()
+    assert _chunk_ex(a, conv=_conv_desc(pos_stride=0)) == INVALID and "positive" in _msg()
+    lib = _native.lib()
+
+    def verify(cv, win=4, slots=4):
+        return lib.kda_verify_ex(ctypes.byref(a), FAKE, FAKE, 4 * 16384, slots, FAKE, FAKE, 2, win,
+                                 FAKE, FAKE, FAKE, ctypes.byref(cv), None)
+    assert verify(_conv_desc(positions=5)) == INVALID and "at least 6 positions" in _msg()
+    assert verify(_conv_desc(num_accepted=None)) == INVALID and "num_accepted" in _msg()
+    assert verify(_conv_desc(), slots=5) == INVALID and "row per state slot" in _msg()
 
 
 def test_workspace_query():
