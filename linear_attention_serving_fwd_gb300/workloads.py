@@ -6,7 +6,9 @@ arithmetic (no gate, no norm, no recurrence), so both sides can share it.
 
 Draw order for every workload is fixed: q, k, v, g, beta, A_log, dt_bias,
 state, lengths, slots.  Draws are fp32 from one seeded generator and are cast
-to bf16 afterwards.  "N(0, s)" means standard deviation s.
+to bf16 afterwards (activations may be cast to fp16 and states to bf16
+instead, ``act_dtype`` / ``state_dtype``, from the same draws).  "N(0, s)"
+means standard deviation s.
 
 Workloads (the shapes and distributions of the chunk_kda / decode pages'
 intended serving traffic):
@@ -108,8 +110,8 @@ def _uniform(gen, shape, lo, hi, device):
     return torch.rand(shape, generator=gen, device=device, dtype=torch.float32) * (hi - lo) + lo
 
 
-def _draw_activations(gen, t_total, hqk, hv, device, g_std=1.0, g_shift=0.0):
-    bf = torch.bfloat16
+def _draw_activations(gen, t_total, hqk, hv, device, g_std=1.0, g_shift=0.0, dtype=torch.bfloat16):
+    bf = dtype  # activation storage: bf16 (default) or fp16, from the same fp32 draws
     q = _normal(gen, (t_total, hqk, D), 1.0, device).to(bf)
     k = _normal(gen, (t_total, hqk, D), 1.0, device).to(bf)
     v = _normal(gen, (t_total, hv, D), 1.0, device).to(bf)
@@ -123,12 +125,13 @@ def _draw_activations(gen, t_total, hqk, hv, device, g_std=1.0, g_shift=0.0):
 def dense_prefill(B: int, T: int, hqk: int, hv: int, *, seed: int = 0, device="cpu",
                   init_state: bool = True, state_std: float = 0.02,
                   lower_bound: float = -5.0, g_shift: float = 0.0,
-                  scale: float = D ** -0.5, name: str = "dense") -> KdaInputs:
+                  scale: float = D ** -0.5, name: str = "dense",
+                  act_dtype=torch.bfloat16, state_dtype=torch.float32) -> KdaInputs:
     """Dense [B, T] prefill flattened to T_tot = B*T tokens."""
     gen = _gen(seed, device)
     q, k, v, g, beta, A_log, dt_bias = _draw_activations(gen, B * T, hqk, hv, device,
-                                                         g_shift=g_shift)
-    h0 = _normal(gen, (B, hv, D, D), state_std, device) if init_state else None
+                                                         g_shift=g_shift, dtype=act_dtype)
+    h0 = _normal(gen, (B, hv, D, D), state_std, device).to(state_dtype) if init_state else None
     cu = torch.arange(0, B + 1, dtype=torch.int32, device=device) * T
     return KdaInputs(name=name, q=q, k=k, v=v, g=g, beta=beta, A_log=A_log,
                      dt_bias=dt_bias, cu_seqlens=cu, B=B, T=T, scale=scale,
@@ -149,8 +152,9 @@ def varlen_paged(lens_or_n, hqk: int, hv: int, *, total: Optional[int] = None,
                  slots: int = 64, seed: int = 0, device="cpu",
                  lower_bound: float = -5.0, g_shift: float = 0.0,
                  state_std: float = 0.02, has_initial=None,
-                 name: str = "varlen") -> KdaInputs:
-    """Varlen prefill on a paged fp32 state cache.
+                 name: str = "varlen", act_dtype=torch.bfloat16,
+                 state_dtype=torch.float32) -> KdaInputs:
+    """Varlen prefill on a paged state cache (fp32 unless ``state_dtype``).
 
     ``lens_or_n`` is either an explicit list of lengths or a sequence count,
     in which case lengths are drawn U[64, 8192] and rescaled to ``total``.
@@ -166,8 +170,8 @@ def varlen_paged(lens_or_n, hqk: int, hv: int, *, total: Optional[int] = None,
         n = len(lens_or_n)
         t_total = int(sum(lens_or_n))
     q, k, v, g, beta, A_log, dt_bias = _draw_activations(gen, t_total, hqk, hv, device,
-                                                         g_shift=g_shift)
-    pool = _normal(gen, (slots, hv, D, D), state_std, device)
+                                                         g_shift=g_shift, dtype=act_dtype)
+    pool = _normal(gen, (slots, hv, D, D), state_std, device).to(state_dtype)
     if isinstance(lens_or_n, int):
         lens = rescaled_lengths(gen, n, total, 64.0, 8192.0, device)
     else:
@@ -187,7 +191,8 @@ def varlen_paged(lens_or_n, hqk: int, hv: int, *, total: Optional[int] = None,
 def decode_batch(n_req: int, window: int, hqk: int, hv: int, *, slots: int = 512,
                  seed: int = 0, device="cpu", qlens=None, null_requests=(),
                  lower_bound: float = -5.0, g_shift: float = 0.0,
-                 state_std: float = 0.02, name: str = "decode") -> KdaInputs:
+                 state_std: float = 0.02, name: str = "decode",
+                 act_dtype=torch.bfloat16, state_dtype=torch.float32) -> KdaInputs:
     """Batched decode / verify: each request has ``window`` new tokens (or
     ``qlens[b]`` <= window), one state slot each, drawn without replacement.
     Requests listed in ``null_requests`` get slot -1 (a padding entry)."""
@@ -197,8 +202,8 @@ def decode_batch(n_req: int, window: int, hqk: int, hv: int, *, slots: int = 512
     assert all(0 <= x <= window for x in qlens)
     t_total = int(sum(qlens))
     q, k, v, g, beta, A_log, dt_bias = _draw_activations(gen, t_total, hqk, hv, device,
-                                                         g_shift=g_shift)
-    pool = _normal(gen, (slots, hv, D, D), state_std, device)
+                                                         g_shift=g_shift, dtype=act_dtype)
+    pool = _normal(gen, (slots, hv, D, D), state_std, device).to(state_dtype)
     idx = torch.randperm(slots, generator=gen, device=device)[:n_req].to(torch.int32)
     for b in null_requests:
         idx[b] = -1

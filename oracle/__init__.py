@@ -123,6 +123,21 @@ def recurrence(q, k, v, g, beta, cu_seqlens, *, A_log=None, dt_bias=None,
     return dict(out=out, state=hT, corr=corr)
 
 
+def round_bf16(a):
+    """fp64 values rounded to bf16 as a kernel holding them in fp32 would:
+    to fp32, then to bf16, each to nearest even (torch's casts)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+    return t.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _is_bf16(t):
+    if t is None:
+        return False
+    import torch
+    return getattr(t, "dtype", None) == torch.bfloat16
+
+
 def prefill(x, *, want_corr=False, n_threads=0):
     """Oracle for ``kda_chunk_fwd`` on a :class:`KdaInputs` batch.
 
@@ -130,6 +145,9 @@ def prefill(x, *, want_corr=False, n_threads=0):
     ``state_pool[state_indices[n]]`` (zero where ``has_initial_state[n]`` is
     false).  Returns out, the final states [N, Hv, 128, 128], and, for the
     paged form, the whole updated pool (final states written to their rows).
+    With bf16 states (the pool or initial state stored as bf16) the states
+    are read widened and the final ones rounded to bf16 once, at the end:
+    the chunk path keeps its state in fp32 across the whole sequence.
     """
     n = x.n_seqs
     h0 = None
@@ -148,6 +166,8 @@ def prefill(x, *, want_corr=False, n_threads=0):
     res = recurrence(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, A_log=x.A_log,
                      dt_bias=x.dt_bias, scale=x.scale, lower_bound=x.lower_bound,
                      h0=h0, want_corr=want_corr, n_threads=n_threads)
+    if _is_bf16(x.state_pool) or _is_bf16(x.initial_state):
+        res["state"] = round_bf16(res["state"])
     if pool is not None:
         idx = x.state_indices.cpu().numpy().astype(np.int64)
         for i in range(n):
@@ -157,6 +177,36 @@ def prefill(x, *, want_corr=False, n_threads=0):
     return res
 
 
+def _token_steps(x, h0, starts, lens, *, bf16, n_threads=0):
+    """Run each live request's tokens one at a time from h0 [R, Hv, 128, 128]
+    (request r's tokens starts[r] .. starts[r] + lens[r] - 1), rounding the
+    carried state to bf16 after every token when ``bf16``: the MATE decode
+    page's bf16 state, stored after each decoded token.  Returns the per
+    token outputs and corrections [T, Hv, 128] and the states after every
+    token, states[t][r] (None past a request's length)."""
+    T, hv = x.t_total, x.hv
+    out = np.zeros((T, hv, D))
+    corr = np.zeros((T, hv, D))
+    S = [h0[r] for r in range(len(starts))]
+    states = []
+    for t in range(max(lens, default=0)):
+        live = [r for r in range(len(starts)) if lens[r] > t]
+        tok = np.asarray([starts[r] + t for r in live])
+        res = recurrence(x.q[tok], x.k[tok], x.v[tok], x.g[tok], x.beta[tok],
+                         np.arange(len(live) + 1), A_log=x.A_log, dt_bias=x.dt_bias,
+                         scale=x.scale, lower_bound=x.lower_bound, h0=np.stack([S[r] for r in live]),
+                         want_corr=True, n_threads=n_threads)
+        out[tok] = res["out"]
+        corr[tok] = res["corr"]
+        st = round_bf16(res["state"]) if bf16 else res["state"]
+        row = [None] * len(starts)
+        for i, r in enumerate(live):
+            S[r] = st[i]
+            row[r] = st[i]
+        states.append(row)
+    return out, corr, states
+
+
 def window(x, *, n_threads=0):
     """Oracle for ``kda_decode`` / ``kda_verify`` on a decode batch.
 
@@ -164,8 +214,11 @@ def window(x, *, n_threads=0):
     ``state_indices[b]``.  A negative slot is a padding entry: zero output,
     no correction records, and its (nonexistent) row untouched.  Returns
     out [T, Hv, 128], corr [T, Hv, 128] (U_t), and the pool after the decode
-    (the verify pool is the input pool, unchanged).
+    (the verify pool is the input pool, unchanged).  A bf16 pool is read
+    widened and the carried state rounded to bf16 after every token.
     """
+    if _is_bf16(x.state_pool):
+        return _window_bf16(x, n_threads=n_threads)
     n = x.n_seqs
     pool = x.state_pool.detach().cpu().double().numpy().copy()
     idx = x.state_indices.cpu().numpy().astype(np.int64)
@@ -187,6 +240,24 @@ def window(x, *, n_threads=0):
     return res
 
 
+def _window_bf16(x, *, n_threads=0):
+    pool = x.state_pool.detach().cpu().double().numpy().copy()
+    idx = x.state_indices.cpu().numpy().astype(np.int64)
+    cu = x.cu_seqlens.cpu().numpy().astype(np.int64)
+    live = [b for b in range(x.n_seqs) if idx[b] >= 0 and cu[b + 1] > cu[b]]
+    h0 = np.stack([pool[idx[b]] for b in live]) if live else np.zeros((0, x.hv, D, D))
+    out, corr, states = _token_steps(x, h0, [int(cu[b]) for b in live],
+                                     [int(cu[b + 1] - cu[b]) for b in live], bf16=True,
+                                     n_threads=n_threads)
+    for b in range(x.n_seqs):
+        if idx[b] < 0:
+            out[cu[b]:cu[b + 1]] = 0.0
+            corr[cu[b]:cu[b + 1]] = 0.0
+    for i, b in enumerate(live):
+        pool[idx[b]] = states[int(cu[b + 1] - cu[b]) - 1][i]
+    return dict(out=out, corr=corr, pool=pool, state=None)
+
+
 def window_steps(x, table, num_accepted=None, *, n_threads=0):
     """Oracle for ``kda_decode_steps``: decode with a [request, step] slot table.
 
@@ -200,7 +271,8 @@ def window_steps(x, table, num_accepted=None, *, n_threads=0):
     b's token columns, flags the call and b is treated as padding.
 
     Every state is the recurrence itself: the state after token t is the
-    final state of the recurrence run on b's first t + 1 tokens.
+    final state of the recurrence run on b's first t + 1 tokens (with a bf16
+    pool: run token by token, the carried state rounded to bf16 after each).
     Returns out [T, Hv, 128], the pool after the call, and ``bad``.
     """
     n = x.n_seqs
@@ -231,6 +303,18 @@ def window_steps(x, table, num_accepted=None, *, n_threads=0):
             continue
         if r0 >= 0:
             live.append((b, r0, L))
+    if _is_bf16(x.state_pool):
+        if live:
+            o, _, states = _token_steps(x, np.stack([pool0[r0] for _, r0, _ in live]),
+                                        [int(cu[b]) for b, _, _ in live], [L for _, _, L in live],
+                                        bf16=True, n_threads=n_threads)
+            for i, (b, r0, L) in enumerate(live):
+                out[int(cu[b]):int(cu[b]) + L] = o[int(cu[b]):int(cu[b]) + L]
+                for t in range(L):
+                    row = int(tab[b, t])
+                    if row >= 0:
+                        pool[row] = states[t][i]
+        return dict(out=out, pool=pool, bad=bad)
     # one sequence per (request, prefix length): tokens cu[b] .. cu[b] + t
     sel, starts, h0 = [], [0], []
     for b, r0, L in live:

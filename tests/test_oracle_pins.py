@@ -285,6 +285,50 @@ def test_slot_table_decode_states_and_reads():
     assert oracle.window_steps(x, torch.from_numpy(t2), torch.from_numpy(acc))["bad"]
 
 
+def test_bf16_state_decode_is_repeated_single_token_decode():
+    """The MATE decode page's bf16 state: a Q-token decode on a bf16 pool
+    equals Q single-token decodes, each widening the stored bf16 row and
+    storing its result back as bf16.  Every stored value is bf16."""
+    x = W.decode_batch(5, 4, 1, 2, slots=9, seed=17, qlens=[4, 2, 3, 0, 4], null_requests=(1,),
+                       lower_bound=-0.7, state_dtype=torch.bfloat16)
+    res = oracle.window(x)
+    pool = x.state_pool.clone()
+    cu = x.cu_seqlens.tolist()
+    idx = x.state_indices.tolist()
+    for b in range(5):
+        if idx[b] < 0:
+            assert np.all(res["out"][cu[b]:cu[b + 1]] == 0)
+            continue
+        for t in range(cu[b], cu[b + 1]):
+            one = oracle.recurrence(x.q[t:t + 1], x.k[t:t + 1], x.v[t:t + 1], x.g[t:t + 1],
+                                    x.beta[t:t + 1], [0, 1], A_log=x.A_log, dt_bias=x.dt_bias,
+                                    lower_bound=x.lower_bound,
+                                    h0=pool[idx[b]].double().numpy()[None])
+            np.testing.assert_allclose(res["out"][t], one["out"][0], rtol=1e-13, atol=1e-16)
+            pool[idx[b]] = torch.from_numpy(one["state"][0]).float().bfloat16()
+    np.testing.assert_array_equal(res["pool"], pool.double().numpy())
+    assert np.array_equal(res["pool"], pool.double().numpy())
+
+
+def test_bf16_state_closed_forms():
+    """beta = 0, gate = 0: a bf16 state is unchanged bit for bit; one token
+    from a zero bf16 state stores bf16(beta k^ v^T)."""
+    x = W.decode_batch(2, 3, 1, 1, slots=3, seed=19, state_dtype=torch.bfloat16)
+    x.beta[:] = -float("inf")
+    x.A_log, x.dt_bias, x.lower_bound = None, None, 0.0
+    x.g[:] = 0
+    res = oracle.window(x)
+    assert np.array_equal(res["pool"], x.state_pool.double().numpy())
+    y = W.decode_batch(1, 1, 1, 1, slots=2, seed=20, state_dtype=torch.bfloat16)
+    y.state_pool[:] = 0
+    res = oracle.window(y)
+    kk, vv = y.k[0, 0].double().numpy(), y.v[0, 0].double().numpy()
+    kh = kk / np.sqrt(kk @ kk + 1e-6)
+    beta = 1 / (1 + np.exp(-float(y.beta[0, 0])))
+    want = torch.from_numpy(beta * np.outer(vv, kh)).float().bfloat16().double().numpy()
+    np.testing.assert_array_equal(res["pool"][int(y.state_indices[0]), 0], want)
+
+
 def test_corr_matches_windowed_solve():
     """The correction records U_t equal the windowed forward substitution of
     the verify page (probes p_t = e^{L_t} k^_t against the start state and
