@@ -45,9 +45,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--extras",
-                    default="decode,verify,verify_conv,commit,decode_steps,varlen,checkpoint,prefill_conv,long",
+                    default="decode,verify,verify_conv,commit,decode_steps,decode_bf16,prefill_fp16,varlen,"
+                            "checkpoint,prefill_conv,long",
                     help="comma list of extra workloads: decode, verify, verify_conv, commit, "
-                         "decode_steps, varlen, checkpoint, prefill_conv, long")
+                         "decode_steps, decode_bf16, prefill_fp16, varlen, checkpoint, prefill_conv, long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -70,9 +71,9 @@ def prefill_bytes_per_token_head(hqk, hv):
 # Sources each kernel is built from: a profiled DRAM traffic figure is only
 # reported while these files are unchanged since the capture.
 KERNEL_SOURCES = {
-    "kda_prologue": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh"],
-    "kda_walk": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh"],
-    "kda_window": ["kda_window.cu", "kda_common.cuh", "kda_params.cuh"],
+    "kda_prologue": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh", "kda_conv.cuh"],
+    "kda_walk": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh", "kda_conv.cuh"],
+    "kda_window": ["kda_window.cu", "kda_common.cuh", "kda_params.cuh", "kda_conv.cuh"],
 }
 
 
@@ -484,6 +485,48 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                                               "slot table of 4 rows per request, accepted counts U{1..4}"}
         del y, pool, table, acc
         torch.cuda.empty_cache()
+    if "decode_bf16" in want:
+        # Q = 1 decode on a bf16 pool (rounded after the token): half the
+        # state bytes of the fp32 pool
+        y = W.decode_batch(256, 1, 32, 32, slots=512, seed=rank, device="cuda", state_dtype=torch.bfloat16,
+                           name="decode_q1_bf16")
+        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
+
+        def fb():
+            kda.kda_decode(y.q, y.k, y.v, y.g, y.beta, y.state_pool, y.cu_seqlens, y.state_indices, 1,
+                           A_log=y.A_log, dt_bias=y.dt_bias, out=out)
+        for _ in range(3):
+            fb()
+        secs = reduce_max(time_device(torch, fb, steps, flush, barrier))
+        t = secs / steps
+        items = y.n_seqs * y.hv
+        nbytes = items * (sb // 2) * 2 + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
+        gbs = nbytes / t / 1e9
+        res["decode_q1_bf16_state"] = {"tokens_per_s": round(y.t_total * world / t, 1),
+                                       "ms_per_step": round(t * 1e3, 4),
+                                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                                                    "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                                                    "traffic": None,
+                                                    "peak_source": f"{pk['src']} HBM copy bandwidth"},
+                                       "workload": "256 requests x window 1, Hqk=Hv=32, 512-slot bf16 pool"}
+        del y, out
+    if "prefill_fp16" in want:
+        # the headline prefill (B=2, T=4096, H=16) with fp16 activations and output
+        z = W.dense_prefill(2, 4096, 16, 16, seed=rank, device="cuda", act_dtype=torch.float16)
+        out = torch.empty((z.t_total, z.hv, D), dtype=torch.float16, device="cuda")
+        fin = torch.empty((2, z.hv, D, D), dtype=torch.float32, device="cuda")
+        ws = torch.empty(kda.chunk_workspace_bytes(2, z.t_total, z.hv, 0), dtype=torch.uint8, device="cuda")
+
+        def ff():
+            kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias, n_seqs=2,
+                              initial_state=z.initial_state, final_state=fin, out=out, workspace=ws)
+        for _ in range(3):
+            ff()
+        secs = reduce_max(time_device(torch, ff, steps, flush, barrier))
+        t = secs / steps
+        res["prefill_fp16"] = {"tokens_per_s": round(z.t_total * world / t, 1), "ms_per_step": round(t * 1e3, 4),
+                               "workload": "B=2 T=4096 Hqk=Hv=16, fp16 q/k/v/g/beta and output, fp32 states"}
+        del z, out, fin, ws
     # varlen paged and long-context prefill
     for name in ("varlen", "checkpoint", "prefill_conv", "long"):
         if name not in want:

@@ -23,11 +23,12 @@
  * strides in elements and the last dimension contiguous (g and beta may be
  * column slices of a fused projection, as the vLLM kimi_k3 AMD kda_chunk page
  * notes for fused_kda_prologue).  Outputs o are [T_tot, Hv, 128] contiguous.
- * Recurrent states are fp32 and V-first: [.., Hv, V=128, K=128] with K
- * contiguous (the decode page's default state_v_first layout, the verify
+ * Recurrent states are fp32 (or bf16, kda_activations.state_bf16) and
+ * V-first: [.., Hv, V=128, K=128] with K contiguous (the decode page's default state_v_first layout, the verify
  * page's [slots, H, V, K] state and fused_kda_chunk's final state).  A paged
- * cache is [slots, Hv, 128, 128] with a caller-chosen slot stride (in floats,
- * a multiple of 4, >= Hv*128*128).
+ * cache is [slots, Hv, 128, 128] with a caller-chosen slot stride (in state
+ * elements, 16-byte rows: a multiple of 4 for fp32, 8 for bf16,
+ * >= Hv*128*128).
  *
  * Ownership.  Every pointer is caller-owned device memory unless stated; the
  * library allocates no device memory and never synchronises inside an entry
@@ -53,7 +54,7 @@ extern "C" {
 typedef enum kda_status {
   KDA_OK = 0,
   KDA_ERR_INVALID_ARGUMENT = 1, /* shape / pointer / size rule broken */
-  KDA_ERR_UNSUPPORTED_DTYPE = 2, /* only bf16 activations are built */
+  KDA_ERR_UNSUPPORTED_DTYPE = 2, /* a dtype outside bf16/fp16 activations */
   KDA_ERR_CUDA = 3,              /* a CUDA runtime call or launch failed */
   KDA_ERR_DEVICE_TIMEOUT = 4,    /* a bounded device wait expired */
   KDA_ERR_DEVICE_INDEX = 5       /* a kernel met a bad slot / length */
@@ -70,13 +71,22 @@ typedef struct kda_activations {
   const void* beta; int64_t beta_stride_tok, beta_stride_head; /* [T, Hv] logits */
   const float* A_log;   /* [Hv] fp32, or NULL (then dt_bias must be NULL)      */
   const float* dt_bias; /* [Hv, 128] fp32 contiguous, or NULL                   */
-  int32_t dtype;        /* KDA_DTYPE_BF16 (KDA_DTYPE_FP16 is rejected)          */
+  int32_t dtype;        /* KDA_DTYPE_BF16 or KDA_DTYPE_FP16: q, k, v, g, beta and
+                           the output o all have this type                      */
   int32_t t_total;      /* total tokens T                                        */
   int32_t hqk, hv;      /* heads; hv % hqk == 0                                  */
   int32_t use_qk_l2norm;/* must be 1: the in-kernel L2 norm of q and k          */
   float scale;          /* q scale applied after the norm (128^-0.5 usual)       */
   float lower_bound;    /* gate lower bound in [-10.5, 0] (-5 usual); unused
                            without A_log                                        */
+  int32_t state_bf16;   /* 0: every recurrent state of the call (initial, final,
+                           cache, pool, snapshots) is fp32; 1: bf16, widened to
+                           fp32 for arithmetic.  Prefill rounds the final state
+                           (and snapshots) once; decode and verify round the
+                           carried state after every token, as repeated
+                           single-token decode would (the MATE decode page's
+                           bf16 state).  Strides then count bf16 elements and
+                           must be multiples of 8 (16-byte rows).              */
 } kda_activations;
 
 /*
@@ -142,7 +152,7 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
 
 /*
  * kda_chunk_fwd - chunked prefill (chunk = 64): the MATE chunk_kda contract
- * restricted to fp32 states, and the vLLM kimi_k3 AMD fused_kda_prologue +
+ * with fp32 or bf16 states, and the vLLM kimi_k3 AMD fused_kda_prologue +
  * fused_kda_chunk pair (including the paged-cache form and the chunk-group
  * parallel scan of _chunk_groups / _kda_group_workspace).
  *
@@ -151,15 +161,15 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
  *   cu_seqlens     device int32 [n_seqs + 1] token offsets (0, .., T), or
  *                  NULL for n_seqs dense sequences of T / n_seqs tokens
  *   n_seqs         number of sequences (>= 1)
- *   initial_state  [n_seqs, Hv, 128, 128] fp32 or NULL (zero start)
- *   final_state    [n_seqs, Hv, 128, 128] fp32 or NULL (not returned)
- *   state_cache    [slots, Hv, 128, 128] fp32 paged cache, or NULL.  When
+ *   initial_state  [n_seqs, Hv, 128, 128] state dtype, or NULL (zero start)
+ *   final_state    [n_seqs, Hv, 128, 128] state dtype, or NULL (not returned)
+ *   state_cache    [slots, Hv, 128, 128] paged cache (state dtype), or NULL.  When
  *                  given, sequence n starts from row state_indices[n] (zero
  *                  when has_initial_state[n] == 0) and its final state is
  *                  written back to that row; initial_state and final_state
  *                  must then be NULL.  A negative row skips the state I/O of
  *                  that sequence (zero start, final state dropped).
- *   slot_stride    floats between cache rows (multiple of 4, >= Hv*16384)
+ *   slot_stride    elements between cache rows (16-byte rows, >= Hv*16384)
  *   n_slots        rows in the cache; a row >= n_slots sets
  *                  KDA_ERR_DEVICE_INDEX in the device error word and is skipped
  *   state_indices  device int32 [n_seqs]
@@ -178,8 +188,8 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
  * lower_bound >= -10.5, which is enforced).
  */
 int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens,
-                  int32_t n_seqs, const float* initial_state, float* final_state,
-                  float* state_cache, int64_t slot_stride, int64_t n_slots,
+                  int32_t n_seqs, const void* initial_state, void* final_state,
+                  void* state_cache, int64_t slot_stride, int64_t n_slots,
                   const int32_t* state_indices, const uint8_t* has_initial_state,
                   int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -192,11 +202,11 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
  * vLLM kda_chunk page's fused_kda_chunk checkpoint_state /
  * checkpoint_offsets / checkpoint_state_indices).  All other arguments as
  * kda_chunk_fwd.
- *   checkpoint_state      fp32 [rows, Hv, 128, 128] destination, or NULL (no
+ *   checkpoint_state      [rows, Hv, 128, 128] (state dtype) destination, or NULL (no
  *                         snapshots; the offsets and indices must then be NULL).
  *                         Without indices it is a staging buffer with a row per
  *                         sequence; with them it may be the paged state cache.
- *   checkpoint_row_stride floats between rows (multiple of 4, >= Hv*16384)
+ *   checkpoint_row_stride elements between rows (16-byte rows, >= Hv*16384)
  *   checkpoint_rows       rows in checkpoint_state; a destination row >= rows
  *                         sets KDA_ERR_DEVICE_INDEX and is skipped
  *   checkpoint_offsets    device int32 [n_seqs]: sequence n's state after
@@ -214,10 +224,10 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
  * of another sequence is a race.
  */
 int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seqlens,
-                     int32_t n_seqs, const float* initial_state, float* final_state,
-                     float* state_cache, int64_t slot_stride, int64_t n_slots,
+                     int32_t n_seqs, const void* initial_state, void* final_state,
+                     void* state_cache, int64_t slot_stride, int64_t n_slots,
                      const int32_t* state_indices, const uint8_t* has_initial_state,
-                     float* checkpoint_state, int64_t checkpoint_row_stride,
+                     void* checkpoint_state, int64_t checkpoint_row_stride,
                      int64_t checkpoint_rows, const int32_t* checkpoint_offsets,
                      const int32_t* checkpoint_state_indices, const kda_conv* conv,
                      int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
@@ -243,23 +253,23 @@ int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seql
  * on it: serialise them.  Allocates nothing (no cudaMalloc / cudaFree).
  */
 int kda_chunk_fwd_noalloc(const kda_activations* x, void* out, const int32_t* cu_seqlens,
-                          int32_t n_seqs, const float* initial_state, float* final_state,
-                          float* state_cache, int64_t slot_stride, int64_t n_slots,
+                          int32_t n_seqs, const void* initial_state, void* final_state,
+                          void* state_cache, int64_t slot_stride, int64_t n_slots,
                           const int32_t* state_indices, const uint8_t* has_initial_state,
                           int32_t groups, void* stream);
 
 /*
  * kda_decode - in-place decode of a short window (1 <= window <= 8 tokens per
- * request) on a paged fp32 state cache: the MATE gated_delta_rule_decode
- * contract for fp32 V-first states with in-kernel gate, lower bound, beta
+ * request) on a paged state cache: the MATE gated_delta_rule_decode
+ * contract for fp32 or bf16 V-first states with in-kernel gate, lower bound, beta
  * sigmoid and q/k L2 norm, continuous batching by slot.
  *
  *   x            activations; x->t_total = query_start[n_req]
  *   out          [T, Hv, 128] bf16, written (zero for padding requests)
- *   state_pool   [n_slots, Hv, 128, 128] fp32, read and updated in place:
+ *   state_pool   [n_slots, Hv, 128, 128] (state dtype), read and updated in place:
  *                request b's row state_indices[b] ends holding the state
  *                after all of its tokens
- *   slot_stride  floats between rows (multiple of 4, >= Hv*16384)
+ *   slot_stride  elements between rows (16-byte rows, >= Hv*16384)
  *   query_start  device int32 [n_req + 1]; request b owns tokens
  *                query_start[b] .. query_start[b+1]-1, at most ``window``
  *   slots        device int32 [n_req]; a negative slot is a padding entry
@@ -268,7 +278,7 @@ int kda_chunk_fwd_noalloc(const kda_activations* x, void* out, const int32_t* cu
  *                and is treated as padding
  * Requests must use distinct slots (two requests on one row race).
  */
-int kda_decode(const kda_activations* x, void* out, float* state_pool,
+int kda_decode(const kda_activations* x, void* out, void* state_pool,
                int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
                const int32_t* slots, int32_t n_req, int32_t window, void* stream);
 
@@ -296,26 +306,26 @@ int kda_decode(const kda_activations* x, void* out, float* state_pool,
  * shared between requests; the read row may be one of the request's own
  * write rows (it is read before any store).
  */
-int kda_decode_steps(const kda_activations* x, void* out, float* state_pool, int64_t slot_stride,
+int kda_decode_steps(const kda_activations* x, void* out, void* state_pool, int64_t slot_stride,
                      int64_t n_slots, const int32_t* query_start, const int32_t* state_indices,
                      int64_t indices_stride, const int32_t* num_accepted_tokens, int32_t n_req,
                      int32_t window, void* stream);
 
 /*
  * kda_verify - windowed speculative verify (1 <= window <= 8): the vLLM
- * kimi_k3 CuTeDSL KdaTcVerify contract with fp32 states.  Same inputs and
+ * kimi_k3 CuTeDSL KdaTcVerify contract with fp32 or bf16 states.  Same inputs and
  * outputs ``out`` as kda_decode, but the state pool is only read, and per
  * request b, value head h and window position t < qlen it records
  *   corr [n_req, Hv, window, 128] fp32 : the correction U_t (the delta-rule
  *        term beta_t (v_t - S_{t-1}^T k^_t) of token t)
- *   kg   [n_req, Hv, window, 256] bf16 : raw k_t (its query/key head) then
- *        raw g_t, as loaded
+ *   kg   [n_req, Hv, window, 256] activation dtype : raw k_t (its
+ *        query/key head) then raw g_t, as loaded
  * from which the accepted prefix's state can be rebuilt.  Entries t >= qlen
  * and padding requests are not written.
  *   work_counter  device int32[1], zero on entry; the launch's persistent
  *                 scheduler takes tickets from it and leaves it zero.
  */
-int kda_verify(const kda_activations* x, void* out, const float* state_pool,
+int kda_verify(const kda_activations* x, void* out, const void* state_pool,
                int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
                const int32_t* slots, int32_t n_req, int32_t window, float* corr,
                void* kg, int32_t* work_counter, void* stream);
@@ -331,7 +341,7 @@ int kda_verify(const kda_activations* x, void* out, const float* state_pool,
  * rolled.  conv NULL: exactly kda_verify.  The SSM state pool is still only
  * read.
  */
-int kda_verify_ex(const kda_activations* x, void* out, const float* state_pool,
+int kda_verify_ex(const kda_activations* x, void* out, const void* state_pool,
                   int64_t slot_stride, int64_t n_slots, const int32_t* query_start,
                   const int32_t* slots, int32_t n_req, int32_t window, float* corr,
                   void* kg, int32_t* work_counter, const kda_conv* conv, void* stream);
@@ -366,6 +376,19 @@ int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const in
                const int32_t* num_accepted, int32_t n_req, int32_t hv, int32_t window,
                const float* corr, const void* kg, const float* A_log, const float* dt_bias,
                float lower_bound, void* stream);
+
+/*
+ * kda_commit_ex - kda_commit for the dtype variants of kda_verify: the pool
+ * holds bf16 rows when state_bf16 = 1 (S_0 widened, S_a computed in fp32
+ * and rounded once), and the kg record holds fp16 raw k and g when
+ * kg_fp16 = 1 (a verify with KDA_DTYPE_FP16 activations).  slot_stride is
+ * then in bf16 elements (a multiple of 8).  state_bf16 = kg_fp16 = 0 is
+ * kda_commit.
+ */
+int kda_commit_ex(void* state_pool, int64_t slot_stride, int64_t n_slots, const int32_t* slots,
+                  const int32_t* num_accepted, int32_t n_req, int32_t hv, int32_t window,
+                  const float* corr, const void* kg, const float* A_log, const float* dt_bias,
+                  float lower_bound, int32_t state_bf16, int32_t kg_fp16, void* stream);
 
 /* Thread-local text of the last error returned on this thread ("" if none). */
 const char* kda_last_error(void);

@@ -56,6 +56,23 @@ def _as_tokens(x: torch.Tensor, name: str, heads_dim: bool = True) -> torch.Tens
     return x
 
 
+_STATE_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def _state_bf16(*states) -> int:
+    """0 for fp32 recurrent states, 1 for bf16; every given state tensor of
+    a call must have the same dtype."""
+    kinds = {t.dtype for t in states if t is not None}
+    if not kinds:
+        return 0
+    if len(kinds) > 1:
+        raise TypeError("all recurrent states of a call must share one dtype.")
+    dt = kinds.pop()
+    if dt not in _STATE_DTYPES:
+        raise TypeError(f"recurrent states must be float32 or bfloat16 (got {dt}).")
+    return _STATE_DTYPES[dt]
+
+
 def _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound):
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         if not t.is_cuda:
@@ -97,6 +114,7 @@ def _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound):
     a.use_qk_l2norm = 1
     a.scale = D ** -0.5 if scale is None else float(scale)
     a.lower_bound = float(lower_bound)
+    a.state_bf16 = 0  # set by the caller from its state tensors
     return a, (A_log, dt_bias)  # keep contiguous copies alive
 
 
@@ -153,11 +171,14 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     """Chunked KDA prefill.  Returns (out, final_state or None).
 
     q, k: [T, Hqk, 128] or [B, T, Hqk, 128]; v, g: [T, Hv, 128]; beta:
-    [T, Hv] logits; bf16.  Dense [B, T] input without ``cu_seqlens`` runs B
-    sequences of T tokens.  ``state_cache`` [slots, Hv, 128, 128] fp32 with
+    [T, Hv] logits; bf16 or fp16 (o has the same dtype).  Dense [B, T] input
+    without ``cu_seqlens`` runs B sequences of T tokens.  Recurrent states
+    (initial_state, final_state, state_cache, checkpoint_state) are all fp32
+    or all bf16; a bf16 final state is rounded once at the end.
+    ``state_cache`` [slots, Hv, 128, 128] with
     ``state_indices`` [N] int32 (and optional ``has_initial_state`` [N])
     replaces initial_state / final_state and is updated in place.
-    ``checkpoint_state`` [rows, Hv, 128, 128] fp32 with ``checkpoint_offsets``
+    ``checkpoint_state`` [rows, Hv, 128, 128] with ``checkpoint_offsets``
     [N] (and optional ``checkpoint_state_indices`` [N]) receives each
     sequence's state after its first checkpoint_offsets[n] tokens (a positive
     multiple of 64 no larger than its length; other offsets are skipped).
@@ -195,11 +216,11 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
         slot_stride, n_slots = state_cache.stride(0), state_cache.shape[0]
         if tuple(state_cache.shape[1:]) != (hv, D, D) or state_cache[0].stride() != (D * D, D, 1):
             raise ValueError("state_cache must be [slots, Hv, 128, 128] with contiguous rows.")
+    a.state_bf16 = _state_bf16(initial_state, final_state, state_cache, checkpoint_state)
     if output_final_state and final_state is None:
-        final_state = torch.empty((n, hv, D, D), dtype=torch.float32, device=q.device)
+        final_state = torch.empty((n, hv, D, D), dtype=torch.bfloat16 if a.state_bf16 else torch.float32,
+                                  device=q.device)
     if initial_state is not None:
-        if initial_state.dtype != torch.float32:
-            raise TypeError("initial_state must be float32.")
         initial_state = initial_state.contiguous()
     ws_bytes = chunk_workspace_bytes(n, T, hv, groups)
     if workspace is None:
@@ -213,8 +234,6 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
         if checkpoint_state is not None:
             if checkpoint_offsets is None:
                 raise ValueError("checkpoint_state needs checkpoint_offsets.")
-            if checkpoint_state.dtype != torch.float32:
-                raise TypeError("checkpoint_state must be float32.")
             if (tuple(checkpoint_state.shape[1:]) != (hv, D, D)
                     or checkpoint_state[0].stride() != (D * D, D, 1)):
                 raise ValueError("checkpoint_state must be [rows, Hv, 128, 128] with contiguous rows.")
@@ -262,6 +281,7 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, out, A_log=None, dt_bias=None, sc
     slot_stride, n_slots = 0, 0
     if state_cache is not None:
         slot_stride, n_slots = state_cache.stride(0), state_cache.shape[0]
+    a.state_bf16 = _state_bf16(initial_state, final_state, state_cache)
     rc = _native.lib().kda_chunk_fwd_noalloc(
         ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state), _ptr(final_state),
         _ptr(state_cache), slot_stride, n_slots, _ptr(state_indices), _ptr(has_initial_state),
@@ -289,8 +309,7 @@ def _window_call(verify, q, k, v, g, beta, state_pool, query_start, slots, windo
     if num_accepted_tokens is not None:
         if num_accepted_tokens.dtype != torch.int32 or num_accepted_tokens.numel() != n_req:
             raise ValueError("num_accepted_tokens must be int32 with one entry per request.")
-    if state_pool.dtype != torch.float32:
-        raise TypeError("state_pool must be float32.")
+    a.state_bf16 = _state_bf16(state_pool)
     if tuple(state_pool.shape[1:]) != (hv, D, D) or state_pool[0].stride() != (D * D, D, 1):
         raise ValueError("state_pool must be [slots, Hv, 128, 128] with contiguous rows.")
     if out is None:
@@ -382,8 +401,7 @@ def kda_commit(state_pool, slots, num_accepted, corr, kg, window, *, A_log=None,
     parameters).  Returns the pool."""
     if slots.dtype != torch.int32 or num_accepted.dtype != torch.int32:
         raise TypeError("slots and num_accepted must have dtype torch.int32.")
-    if state_pool.dtype != torch.float32:
-        raise TypeError("state_pool must be float32.")
+    state_bf16 = _state_bf16(state_pool)
     hv = state_pool.shape[1]
     if tuple(state_pool.shape[1:]) != (hv, D, D) or state_pool[0].stride() != (D * D, D, 1):
         raise ValueError("state_pool must be [slots, Hv, 128, 128] with contiguous rows.")
@@ -392,16 +410,18 @@ def kda_commit(state_pool, slots, num_accepted, corr, kg, window, *, A_log=None,
         raise ValueError("num_accepted must have one entry per request.")
     if tuple(corr.shape) != (n_req, hv, window, D) or corr.dtype != torch.float32 or not corr.is_contiguous():
         raise ValueError("corr must be a contiguous float32 [n_req, Hv, window, 128] tensor.")
-    if tuple(kg.shape) != (n_req, hv, window, 2 * D) or kg.dtype != torch.bfloat16 or not kg.is_contiguous():
-        raise ValueError("kg must be a contiguous bfloat16 [n_req, Hv, window, 256] tensor.")
+    if (tuple(kg.shape) != (n_req, hv, window, 2 * D) or kg.dtype not in (torch.bfloat16, torch.float16)
+            or not kg.is_contiguous()):
+        raise ValueError("kg must be a contiguous bfloat16 / float16 [n_req, Hv, window, 256] tensor.")
     keep = []
     if A_log is not None:
         A_log = A_log.detach().float().contiguous()
         dt_bias = dt_bias.detach().float().contiguous()
         keep = [A_log, dt_bias]
-    rc = _native.lib().kda_commit(_ptr(state_pool), state_pool.stride(0), state_pool.shape[0], _ptr(slots),
-                                  _ptr(num_accepted), n_req, hv, window, _ptr(corr), _ptr(kg),
-                                  _ptr(A_log), _ptr(dt_bias), float(lower_bound), _stream_handle(stream))
+    rc = _native.lib().kda_commit_ex(_ptr(state_pool), state_pool.stride(0), state_pool.shape[0],
+                                     _ptr(slots), _ptr(num_accepted), n_req, hv, window, _ptr(corr),
+                                     _ptr(kg), _ptr(A_log), _ptr(dt_bias), float(lower_bound), state_bf16,
+                                     int(kg.dtype == torch.float16), _stream_handle(stream))
     _native.check(rc)
     del keep
     return state_pool

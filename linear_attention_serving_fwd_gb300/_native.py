@@ -27,7 +27,7 @@ KDA_DTYPE_FP16 = 1
 EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_verify",
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
            "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
-           "kda_decode_steps", "kda_verify_ex")
+           "kda_decode_steps", "kda_verify_ex", "kda_commit_ex")
 
 
 class KdaActivations(ctypes.Structure):
@@ -43,6 +43,7 @@ class KdaActivations(ctypes.Structure):
         ("hqk", ctypes.c_int32), ("hv", ctypes.c_int32),
         ("use_qk_l2norm", ctypes.c_int32),
         ("scale", ctypes.c_float), ("lower_bound", ctypes.c_float),
+        ("state_bf16", ctypes.c_int32),
     ]
 
 
@@ -87,6 +88,8 @@ def _declare(lib):
     lib.kda_verify_ex.restype = ctypes.c_int
     lib.kda_commit.argtypes = [P, I64, I64, P, P, I32, I32, I32, P, P, P, P, ctypes.c_float, P]
     lib.kda_commit.restype = ctypes.c_int
+    lib.kda_commit_ex.argtypes = [P, I64, I64, P, P, I32, I32, I32, P, P, P, P, ctypes.c_float, I32, I32, P]
+    lib.kda_commit_ex.restype = ctypes.c_int
     lib.kda_last_error.argtypes = []
     lib.kda_last_error.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [P, I32]

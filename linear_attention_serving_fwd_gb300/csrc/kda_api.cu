@@ -56,10 +56,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Rules shared by all entry points.
 int check_activations(const kda_activations* x, bool need_rows_aligned) {
   if (!x) return fail(KDA_ERR_INVALID_ARGUMENT, "activations must not be NULL.");
-  if (x->dtype == KDA_DTYPE_FP16)
-    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "only bfloat16 q/k/v/g/beta are built (got float16).");
-  if (x->dtype != KDA_DTYPE_BF16)
-    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "q/k/v/g/beta dtype must be bfloat16.");
+  if (x->dtype != KDA_DTYPE_BF16 && x->dtype != KDA_DTYPE_FP16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "q/k/v/g/beta dtype must be bfloat16 or float16 (got %d).",
+                x->dtype);
+  if (x->state_bf16 != 0 && x->state_bf16 != 1)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "state_bf16 must be 0 (fp32 states) or 1 (bf16 states).");
   if (x->hqk <= 0 || x->hv <= 0)
     return fail(KDA_ERR_INVALID_ARGUMENT, "head counts must be positive (hqk=%d, hv=%d).", x->hqk, x->hv);
   if (x->hv % x->hqk != 0)
@@ -108,15 +109,18 @@ void fill_common(const kda_activations* x, const __nv_bfloat16*& q, const __nv_b
   b = static_cast<const __nv_bfloat16*>(x->beta);
 }
 
-int check_pool(const float* pool, int64_t slot_stride, int64_t n_slots, int hv, const char* name,
+// Rows of states (fp32, or bf16 with ``bf16``): the stride counts elements
+// and keeps rows 16-byte aligned for the bulk copies.
+int check_pool(const void* pool, int64_t slot_stride, int64_t n_slots, int hv, bool bf16, const char* name,
                const char* stride_name = "slot_stride") {
   if (!pool) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must not be NULL.", name);
   if (!aligned16(pool)) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned.", name);
   if (n_slots <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "%s must contain at least one slot.", name);
-  if (slot_stride % 4 != 0 || slot_stride < (int64_t)hv * kda::D * kda::D)
+  const int64_t unit = bf16 ? 8 : 4;
+  if (slot_stride % unit != 0 || slot_stride < (int64_t)hv * kda::D * kda::D)
     return fail(KDA_ERR_INVALID_ARGUMENT,
-                "%s must be a multiple of 4 floats and >= Hv*128*128 (got %lld).", stride_name,
-                (long long)slot_stride);
+                "%s must be a multiple of %lld elements and >= Hv*128*128 (got %lld).", stride_name,
+                (long long)unit, (long long)slot_stride);
   return KDA_OK;
 }
 
@@ -253,6 +257,8 @@ static int check_conv(const kda_conv* conv, const kda_activations* x, bool verif
                       int64_t n_slots, kda::ConvParams& cp) {
   memset(&cp, 0, sizeof(cp));
   if (!conv) return KDA_OK;
+  if (x->dtype != KDA_DTYPE_BF16)
+    return fail(KDA_ERR_UNSUPPORTED_DTYPE, "the conv path takes bfloat16 activations (the conv state is bf16).");
   if (!conv->weight || !conv->state)
     return fail(KDA_ERR_INVALID_ARGUMENT, "conv weight and state must not be NULL.");
   if (!aligned16(conv->weight)) return fail(KDA_ERR_INVALID_ARGUMENT, "conv weight must be 16-byte aligned.");
@@ -272,7 +278,6 @@ static int check_conv(const kda_conv* conv, const kda_activations* x, bool verif
   } else if (!conv->state_indices) {
     return fail(KDA_ERR_INVALID_ARGUMENT, "prefill with a conv needs conv state_indices.");
   }
-  (void)x;
   cp.w = conv->weight;
   cp.w_f32 = conv->weight_f32;
   cp.state = static_cast<__nv_bfloat16*>(conv->state);
@@ -288,9 +293,9 @@ static int check_conv(const kda_conv* conv, const kda_activations* x, bool verif
 }
 
 static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
-                        const float* initial_state, float* final_state, float* state_cache,
+                        const void* initial_state, void* final_state, void* state_cache,
                         int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
-                        const uint8_t* has_initial_state, float* checkpoint_state,
+                        const uint8_t* has_initial_state, void* checkpoint_state,
                         int64_t checkpoint_row_stride, int64_t checkpoint_rows,
                         const int32_t* checkpoint_offsets, const int32_t* checkpoint_state_indices,
                         const kda_conv* conv, int32_t groups, void* workspace, size_t workspace_bytes,
@@ -309,7 +314,7 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
     if (initial_state || final_state)
       return fail(KDA_ERR_INVALID_ARGUMENT, "state_cache replaces initial_state/final_state.");
     if (!state_indices) return fail(KDA_ERR_INVALID_ARGUMENT, "state_cache needs state_indices.");
-    rc = check_pool(state_cache, slot_stride, n_slots, x->hv, "state_cache");
+    rc = check_pool(state_cache, slot_stride, n_slots, x->hv, x->state_bf16, "state_cache");
     if (rc) return rc;
   }
   if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
@@ -317,7 +322,8 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
   if (checkpoint_state) {
     if (!checkpoint_offsets)
       return fail(KDA_ERR_INVALID_ARGUMENT, "checkpoint_state needs checkpoint_offsets.");
-    rc = check_pool(checkpoint_state, checkpoint_row_stride, checkpoint_rows, x->hv, "checkpoint_state",
+    rc = check_pool(checkpoint_state, checkpoint_row_stride, checkpoint_rows, x->hv, x->state_bf16,
+                    "checkpoint_state",
                     "checkpoint_row_stride");
     if (rc) return rc;
     if (!checkpoint_state_indices && checkpoint_rows < n_seqs)
@@ -350,6 +356,7 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
   p.dense_len = cu_seqlens ? 0 : x->t_total / n_seqs;
   p.cu_seqlens = cu_seqlens;
   p.out = static_cast<__nv_bfloat16*>(out);
+  p.in_fp16 = x->dtype == KDA_DTYPE_FP16; p.state_bf16 = x->state_bf16;
   p.h0 = initial_state; p.hT = final_state; p.cache = state_cache;
   p.slot_stride = slot_stride; p.n_slots = n_slots;
   p.state_indices = state_indices; p.has_init = has_initial_state;
@@ -366,7 +373,7 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
 }
 
 int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
-                  const float* initial_state, float* final_state, float* state_cache,
+                  const void* initial_state, void* final_state, void* state_cache,
                   int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
                   const uint8_t* has_initial_state, int32_t groups, void* workspace,
                   size_t workspace_bytes, void* stream) {
@@ -376,9 +383,9 @@ int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens
 }
 
 int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
-                     const float* initial_state, float* final_state, float* state_cache,
+                     const void* initial_state, void* final_state, void* state_cache,
                      int64_t slot_stride, int64_t n_slots, const int32_t* state_indices,
-                     const uint8_t* has_initial_state, float* checkpoint_state,
+                     const uint8_t* has_initial_state, void* checkpoint_state,
                      int64_t checkpoint_row_stride, int64_t checkpoint_rows,
                      const int32_t* checkpoint_offsets, const int32_t* checkpoint_state_indices,
                      const kda_conv* conv, int32_t groups, void* workspace, size_t workspace_bytes,
@@ -389,7 +396,7 @@ int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seql
                       workspace_bytes, stream);
 }
 
-static int window_common(const kda_activations* x, void* out, const float* pool, int64_t slot_stride,
+static int window_common(const kda_activations* x, void* out, const void* pool, int64_t slot_stride,
                          int64_t n_slots, const int32_t* query_start, const int32_t* slots,
                          int32_t n_req, int32_t window, bool verify, float* corr, void* kg,
                          int32_t* counter, void* stream, const int32_t* step_slots = nullptr,
@@ -411,7 +418,7 @@ static int window_common(const kda_activations* x, void* out, const float* pool,
   if (!query_start || !(slots || step_slots))
     return fail(KDA_ERR_INVALID_ARGUMENT, "query_start and state_indices must not be NULL.");
   if (x->t_total > 0 && !out) return fail(KDA_ERR_INVALID_ARGUMENT, "out must not be NULL.");
-  rc = check_pool(pool, slot_stride, n_slots, x->hv, "state_pool");
+  rc = check_pool(pool, slot_stride, n_slots, x->hv, x->state_bf16, "state_pool");
   if (rc) return rc;
   if (verify && (!corr || !kg || !counter))
     return fail(KDA_ERR_INVALID_ARGUMENT, "verify needs corr, kg and work_counter.");
@@ -430,7 +437,8 @@ static int window_common(const kda_activations* x, void* out, const float* pool,
   p.A_log = x->A_log; p.dt_bias = x->dt_bias; p.has_gate = x->A_log != nullptr;
   p.scale = x->scale; p.lower_bound = x->lower_bound;
   p.out = static_cast<__nv_bfloat16*>(out);
-  p.pool = const_cast<float*>(pool);
+  p.pool = const_cast<void*>(pool);
+  p.in_fp16 = x->dtype == KDA_DTYPE_FP16; p.state_bf16 = x->state_bf16;
   p.slot_stride = slot_stride; p.n_slots = n_slots;
   p.query_start = query_start; p.slots = slots;
   p.step_slots = step_slots; p.step_stride = step_stride; p.n_accepted = n_accepted;
@@ -443,14 +451,14 @@ static int window_common(const kda_activations* x, void* out, const float* pool,
   return ok();
 }
 
-int kda_decode(const kda_activations* x, void* out, float* state_pool, int64_t slot_stride,
+int kda_decode(const kda_activations* x, void* out, void* state_pool, int64_t slot_stride,
                int64_t n_slots, const int32_t* query_start, const int32_t* slots, int32_t n_req,
                int32_t window, void* stream) {
   return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req,
                        window, false, nullptr, nullptr, nullptr, stream);
 }
 
-int kda_decode_steps(const kda_activations* x, void* out, float* state_pool, int64_t slot_stride,
+int kda_decode_steps(const kda_activations* x, void* out, void* state_pool, int64_t slot_stride,
                      int64_t n_slots, const int32_t* query_start, const int32_t* state_indices,
                      int64_t indices_stride, const int32_t* num_accepted_tokens, int32_t n_req,
                      int32_t window, void* stream) {
@@ -461,14 +469,14 @@ int kda_decode_steps(const kda_activations* x, void* out, float* state_pool, int
                        num_accepted_tokens);
 }
 
-int kda_verify(const kda_activations* x, void* out, const float* state_pool, int64_t slot_stride,
+int kda_verify(const kda_activations* x, void* out, const void* state_pool, int64_t slot_stride,
                int64_t n_slots, const int32_t* query_start, const int32_t* slots, int32_t n_req,
                int32_t window, float* corr, void* kg, int32_t* work_counter, void* stream) {
   return window_common(x, out, state_pool, slot_stride, n_slots, query_start, slots, n_req,
                        window, true, corr, kg, work_counter, stream);
 }
 
-int kda_verify_ex(const kda_activations* x, void* out, const float* state_pool, int64_t slot_stride,
+int kda_verify_ex(const kda_activations* x, void* out, const void* state_pool, int64_t slot_stride,
                   int64_t n_slots, const int32_t* query_start, const int32_t* slots, int32_t n_req,
                   int32_t window, float* corr, void* kg, int32_t* work_counter, const kda_conv* conv,
                   void* stream) {
@@ -480,6 +488,16 @@ int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const in
                const int32_t* num_accepted, int32_t n_req, int32_t hv, int32_t window,
                const float* corr, const void* kg, const float* A_log, const float* dt_bias,
                float lower_bound, void* stream) {
+  return kda_commit_ex(state_pool, slot_stride, n_slots, slots, num_accepted, n_req, hv, window, corr, kg,
+                       A_log, dt_bias, lower_bound, 0, 0, stream);
+}
+
+int kda_commit_ex(void* state_pool, int64_t slot_stride, int64_t n_slots, const int32_t* slots,
+                  const int32_t* num_accepted, int32_t n_req, int32_t hv, int32_t window,
+                  const float* corr, const void* kg, const float* A_log, const float* dt_bias,
+                  float lower_bound, int32_t state_bf16, int32_t kg_fp16, void* stream) {
+  if ((state_bf16 != 0 && state_bf16 != 1) || (kg_fp16 != 0 && kg_fp16 != 1))
+    return fail(KDA_ERR_INVALID_ARGUMENT, "state_bf16 and kg_fp16 must be 0 or 1.");
   if (window < 1 || window > kda::MAX_WINDOW)
     return fail(KDA_ERR_INVALID_ARGUMENT, "window must satisfy 1 <= window <= 8 (got %d).", window);
   if (n_req < 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_req must be >= 0.");
@@ -495,7 +513,7 @@ int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const in
   if (A_log && !aligned16(dt_bias)) return fail(KDA_ERR_INVALID_ARGUMENT, "dt_bias must be 16-byte aligned.");
   if (A_log && !(lower_bound <= 0.f && lower_bound >= -10.5f))
     return fail(KDA_ERR_INVALID_ARGUMENT, "lower_bound must lie in [-10.5, 0] (got %g).", (double)lower_bound);
-  int rc = check_pool(state_pool, slot_stride, n_slots, hv, "state_pool");
+  int rc = check_pool(state_pool, slot_stride, n_slots, hv, state_bf16, "state_pool");
   if (rc) return rc;
   if ((int64_t)n_req * hv > 0x7fffffff)
     return fail(KDA_ERR_INVALID_ARGUMENT, "n_req * Hv exceeds 2^31.");
@@ -504,6 +522,7 @@ int kda_commit(float* state_pool, int64_t slot_stride, int64_t n_slots, const in
   kda::CommitParams p;
   memset(&p, 0, sizeof(p));
   p.pool = state_pool; p.slot_stride = slot_stride; p.n_slots = n_slots;
+  p.state_bf16 = state_bf16; p.kg_fp16 = kg_fp16;
   p.slots = slots; p.accepted = num_accepted;
   p.corr = corr; p.kg = static_cast<const __nv_bfloat16*>(kg);
   p.A_log = A_log; p.dt_bias = dt_bias; p.lower_bound = lower_bound; p.has_gate = A_log != nullptr;

@@ -297,7 +297,7 @@ __device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m
   return r;
 }
 
-template <bool CONV>
+template <bool CONV, bool FP16>
 __global__ void __launch_bounds__(PRO_THREADS, 1)
     kda_prologue_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     const int c_glob = meta.x, h = meta.y, len = meta.w;
     const float a_h = p.has_gate ? __expf(sc.alog) : 0.f;
     const float dt = sc.dt;
-    if (tid < 64) s.beta[tid] = tid < len ? sigmoidf_(bf2f(sc.beta)) : 0.f;
+    if (tid < 64) s.beta[tid] = tid < len ? sigmoidf_(act_f<FP16>(sc.beta)) : 0.f;
     unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
     // ---- phase 0: this item's tiles (issued during the previous item) -------
     wait_or_abort(&s.tbar, tile_phase, &s.abort, p.err);
@@ -351,12 +351,12 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       for (int i = 0; i < 16; i += 2) {
         const int r = 16 * Rq + i;
         const bool in0 = r < len, in1 = r + 1 < len;
-        qv[i] = in0 ? bf2f(tiles[tile_row(0, r) + c]) : 0.f;
-        qv[i + 1] = in1 ? bf2f(tiles[tile_row(0, r + 1) + c]) : 0.f;
-        kv[i] = in0 ? bf2f(tiles[tile_row(1, r) + c]) : 0.f;
-        kv[i + 1] = in1 ? bf2f(tiles[tile_row(1, r + 1) + c]) : 0.f;
-        float2 g = make_float2(in0 ? bf2f(tiles[g_row(r) + c]) : 0.f,
-                               in1 ? bf2f(tiles[g_row(r + 1) + c]) : 0.f);
+        qv[i] = in0 ? act_f<FP16>(tiles[tile_row(0, r) + c]) : 0.f;
+        qv[i + 1] = in1 ? act_f<FP16>(tiles[tile_row(0, r + 1) + c]) : 0.f;
+        kv[i] = in0 ? act_f<FP16>(tiles[tile_row(1, r) + c]) : 0.f;
+        kv[i + 1] = in1 ? act_f<FP16>(tiles[tile_row(1, r + 1) + c]) : 0.f;
+        float2 g = make_float2(in0 ? act_f<FP16>(tiles[g_row(r) + c]) : 0.f,
+                               in1 ? act_f<FP16>(tiles[g_row(r + 1) + c]) : 0.f);
         if (p.has_gate) {  // lower_bound * sigmoid(a (g + dt_bias)), in pairs
           const float2 t = ffma2(ah2, g, adt2);
           const float2 den = fadd2(make_float2(__expf(-t.x), __expf(-t.y)), make_float2(1.f, 1.f));
@@ -367,8 +367,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         lam[i] = acc;
         acc += g.y;
         lam[i + 1] = acc;
-        vw[i >> 1] = pack_half2(in0 ? bf2f(tiles[tile_row(2, r) + c]) : 0.f,
-                                in1 ? bf2f(tiles[tile_row(2, r + 1) + c]) : 0.f);
+        vw[i >> 1] = pack_half2(in0 ? act_f<FP16>(tiles[tile_row(2, r) + c]) : 0.f,
+                                in1 ? act_f<FP16>(tiles[tile_row(2, r + 1) + c]) : 0.f);
       }
       // v^T of this column: the record's block c / 32, and VT for o_intra
 #pragma unroll
@@ -837,24 +837,38 @@ struct __align__(1024) WalkSmem {
 };
 static_assert(sizeof(WalkSmem) <= 227 * 1024, "walk shared memory");
 
-__device__ __forceinline__ const float* initial_state(const ChunkParams& p, int n, int h) {
+// Element offset of sequence n's head-h initial / final state in
+// init_base(p) / final_base(p) (the paged cache, or h0 / hT), or -1 for none.
+// Elements are fp32, or bf16 with p.state_bf16.
+__device__ __forceinline__ int64_t initial_state_off(const ChunkParams& p, int n, int h) {
   if (p.cache) {
     const int64_t slot = p.state_indices[n];
-    if (slot < 0) return nullptr;
-    if (slot >= p.n_slots) { set_error(p.err, ERR_INDEX); return nullptr; }
-    if (p.has_init && !p.has_init[n]) return nullptr;
-    return p.cache + slot * p.slot_stride + (int64_t)h * D * D;
+    if (slot < 0) return -1;
+    if (slot >= p.n_slots) { set_error(p.err, ERR_INDEX); return -1; }
+    if (p.has_init && !p.has_init[n]) return -1;
+    return slot * p.slot_stride + (int64_t)h * D * D;
   }
-  return p.h0 ? p.h0 + ((int64_t)n * p.hv + h) * D * D : nullptr;
+  return p.h0 ? ((int64_t)n * p.hv + h) * D * D : -1;
 }
-
-__device__ __forceinline__ float* final_state(const ChunkParams& p, int n, int h) {
+__device__ __forceinline__ int64_t final_state_off(const ChunkParams& p, int n, int h) {
   if (p.cache) {
     const int64_t slot = p.state_indices[n];
-    if (slot < 0 || slot >= p.n_slots) return nullptr;
-    return p.cache + slot * p.slot_stride + (int64_t)h * D * D;
+    if (slot < 0 || slot >= p.n_slots) return -1;
+    return slot * p.slot_stride + (int64_t)h * D * D;
   }
-  return p.hT ? p.hT + ((int64_t)n * p.hv + h) * D * D : nullptr;
+  return p.hT ? ((int64_t)n * p.hv + h) * D * D : -1;
+}
+__device__ __forceinline__ const void* init_base(const ChunkParams& p) { return p.cache ? p.cache : p.h0; }
+__device__ __forceinline__ void* final_base(const ChunkParams& p) { return p.cache ? p.cache : p.hT; }
+__device__ __forceinline__ float state_load(const ChunkParams& p, const void* base, int64_t i) {
+  return p.state_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i])
+                      : static_cast<const float*>(base)[i];
+}
+__device__ __forceinline__ void state_store(const ChunkParams& p, void* base, int64_t i, float x) {
+  if (p.state_bf16)
+    static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+  else
+    static_cast<float*>(base)[i] = x;
 }
 
 __device__ __forceinline__ void group_range(const ChunkParams& p, int n, int gidx, int& c0, int& c1) {
@@ -913,14 +927,17 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     const int half = tid == 0 ? 0 : (tid == 32 ? 1 : -1);
     float S[16];
     {
-      const float* src = nullptr;
-      if (mode == 0) src = (p.groups > 1) ? p.gS + plane : initial_state(p, n, h);
+      // pass two of a group scan starts from the composed state (fp32); a
+      // serial walk from the sequence's initial state (state dtype)
+      const float* gsrc = (mode == 0 && p.groups > 1) ? p.gS + plane : nullptr;
+      const int64_t ioff = (mode == 0 && p.groups == 1) ? initial_state_off(p, n, h) : -1;
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
         const int col = col0 + 16 * ch + v;
         float x = 0.f;
         if (mode == 1) x = (ident && k == col) ? 1.f : 0.f;
-        else if (src) x = src[(int64_t)col * D + k];
+        else if (gsrc) x = gsrc[(int64_t)col * D + k];
+        else if (ioff >= 0) x = state_load(p, init_base(p), ioff + (int64_t)col * D + k);
         S[v] = x;
       }
     }
@@ -943,7 +960,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     // 128 threads together.
     // mid-prefill snapshot of this sequence: after in-sequence chunk ck_j
     int ck_j = -1;
-    float* ck_dst = nullptr;
+    int64_t ck_off = 0;
     if (mode == 0 && p.ckpt) {
       const int o = p.ckpt_off[n];
       const int len = seq_eos(p, n) - seq_bos(p, n);
@@ -951,7 +968,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       if (o > 0 && o % CHUNK == 0 && o <= len && row >= 0) {
         if (row < p.ckpt_rows) {
           ck_j = o / CHUNK - 1;
-          ck_dst = p.ckpt + row * p.ckpt_stride + (int64_t)h * D * D;
+          ck_off = row * p.ckpt_stride + (int64_t)h * D * D;
         } else if (tid == 0) {
           set_error(p.err, ERR_INDEX);
         }
@@ -999,7 +1016,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
                                       (ident ? 0.f : __uint_as_float(y2[v])));
         if (c0 + it - seq_c0 == ck_j)  // S now holds the state after the snapshot's chunk
 #pragma unroll
-          for (int v = 0; v < 16; ++v) ck_dst[(int64_t)(col0 + 16 * ch + v) * D + k] = S[v];
+          for (int v = 0; v < 16; ++v) state_store(p, p.ckpt, ck_off + (int64_t)(col0 + 16 * ch + v) * D + k, S[v]);
         if (more) {
           write_s16(ab);
           fence_proxy_async_smem();
@@ -1015,12 +1032,20 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       }
       dcur = dnext;
     }
-    float* dst = nullptr;  // end state of this column block, V-first rows col0..
-    if (mode == 1) dst = (ident ? p.gM : p.gB) + plane;
-    else if (p.groups == 1) dst = final_state(p, n, h);
-    if (dst && !s.abort)
+    // end state of this column block, V-first rows col0..: the group scan's
+    // operators (fp32), or the sequence's final state (state dtype)
+    if (!s.abort) {
+      if (mode == 1) {
+        float* dst = (ident ? p.gM : p.gB) + plane;
 #pragma unroll
-      for (int v = 0; v < 16; ++v) dst[(int64_t)(col0 + 16 * ch + v) * D + k] = S[v];
+        for (int v = 0; v < 16; ++v) dst[(int64_t)(col0 + 16 * ch + v) * D + k] = S[v];
+      } else if (p.groups == 1) {
+        const int64_t fo = final_state_off(p, n, h);
+        if (fo >= 0)
+#pragma unroll
+          for (int v = 0; v < 16; ++v) state_store(p, final_base(p), fo + (int64_t)(col0 + 16 * ch + v) * D + k, S[v]);
+      }
+    }
   } else if (warp < 12) {
     // ---------------- output rows: O[b] lanes 16 q .. 16 q + 15 --------------
     const int q = warp - 8, r = 16 * q + (lane & 15);
@@ -1049,8 +1074,8 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float2 f = __bfloat1622float2(ib[u]);
-            __nv_bfloat162 t = __floats2bfloat162_rn(o[8 * j + 2 * u] + f.x, o[8 * j + 2 * u + 1] + f.y);
-            wp[u] = *reinterpret_cast<uint32_t*>(&t);
+            const float a0 = o[8 * j + 2 * u] + f.x, a1 = o[8 * j + 2 * u + 1] + f.y;
+            wp[u] = p.in_fp16 ? act_pack2<true>(a0, a1) : act_pack2<false>(a0, a1);
           }
           *reinterpret_cast<uint4*>(dst + 8 * j) = w;
         }
@@ -1148,8 +1173,9 @@ __global__ void __launch_bounds__(COMPOSE_THREADS, 1) kda_compose_kernel(ChunkPa
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int tid = threadIdx.x;
   const int v0 = vb * NB;
-  const float* src = initial_state(p, n, h);
-  for (int e = tid; e < NB * D; e += COMPOSE_THREADS) St[e] = src ? src[(int64_t)v0 * D + e] : 0.f;
+  const int64_t ioff = initial_state_off(p, n, h);
+  for (int e = tid; e < NB * D; e += COMPOSE_THREADS)
+    St[e] = ioff >= 0 ? state_load(p, init_base(p), ioff + (int64_t)v0 * D + e) : 0.f;
   __syncthreads();
   for (int gi = 0; gi < p.groups; ++gi) {
     const int64_t plane = (((int64_t)n * p.hv + h) * p.groups + gi) * D * D;
@@ -1170,9 +1196,9 @@ __global__ void __launch_bounds__(COMPOSE_THREADS, 1) kda_compose_kernel(ChunkPa
     for (int j2 = 0; j2 < 16; ++j2) St[v * D + kq + 8 * j2] = acc[j2];
     __syncthreads();
   }
-  float* dst = final_state(p, n, h);
-  if (dst)
-    for (int e = tid; e < NB * D; e += COMPOSE_THREADS) dst[(int64_t)v0 * D + e] = St[e];
+  const int64_t fo = final_state_off(p, n, h);
+  if (fo >= 0)
+    for (int e = tid; e < NB * D; e += COMPOSE_THREADS) state_store(p, final_base(p), fo + (int64_t)v0 * D + e, St[e]);
 }
 
 // --------------------------------------------------------------------------
@@ -1208,14 +1234,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // rows of ``heads`` x 128 bf16 per token: dims (128, heads, T), box (128, 1, rows)
 static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, int64_t st_head,
-                        int64_t st_tok, int rows = CHUNK) {
+                        int64_t st_tok, bool fp16, int rows = CHUNK) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)T};
   const cuuint64_t strides[2] = {(cuuint64_t)st_head * 2, (cuuint64_t)st_tok * 2};
   const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)rows};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1223,9 +1249,11 @@ static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, in
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   static bool attrs = false;
   if (!attrs) {
-    cudaFuncSetAttribute(kda_prologue_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(kda_prologue_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(ProSmem));
-    cudaFuncSetAttribute(kda_prologue_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(kda_prologue_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(ProSmem));
+    cudaFuncSetAttribute(kda_prologue_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(ProSmem));
     cudaFuncSetAttribute(kda_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(WalkSmem));
@@ -1255,10 +1283,11 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   trace_end(stream);
   TileMaps maps;
   const int qkv_rows = CHUNK + (p.conv.state ? HALO : 0);
-  if (!encode_rows(&maps.q, p.q, p.hqk, p.t_total, p.q_sh, p.q_st, qkv_rows) ||
-      !encode_rows(&maps.k, p.k, p.hqk, p.t_total, p.k_sh, p.k_st, qkv_rows) ||
-      !encode_rows(&maps.g, p.g, p.hv, p.t_total, p.g_sh, p.g_st) ||
-      !encode_rows(&maps.v, p.v, p.hv, p.t_total, p.v_sh, p.v_st, qkv_rows)) {
+  const bool f16 = p.in_fp16 != 0;
+  if (!encode_rows(&maps.q, p.q, p.hqk, p.t_total, p.q_sh, p.q_st, f16, qkv_rows) ||
+      !encode_rows(&maps.k, p.k, p.hqk, p.t_total, p.k_sh, p.k_st, f16, qkv_rows) ||
+      !encode_rows(&maps.g, p.g, p.hv, p.t_total, p.g_sh, p.g_st, f16) ||
+      !encode_rows(&maps.v, p.v, p.hv, p.t_total, p.v_sh, p.v_st, f16, qkv_rows)) {
     set_last_error(KDA_ERR_INVALID_ARGUMENT,
                    "kda_chunk_fwd: q/k/v/g layout cannot be described by a TMA tensor map "
                    "(strides must be positive multiples of 8 elements below 2^39 bytes).");
@@ -1268,10 +1297,12 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   const int items = max_chunks * p.hv;
   const int sms = p.sm_count > 0 ? p.sm_count : 152;
   const int grid = items < sms ? items : sms;
-  if (p.conv.state)
-    kda_prologue_kernel<true><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+  if (p.conv.state)  // bf16 activations only (checked by the API layer)
+    kda_prologue_kernel<true, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+  else if (p.in_fp16)
+    kda_prologue_kernel<false, true><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
   else
-    kda_prologue_kernel<false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+    kda_prologue_kernel<false, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
   trace_end(stream);
   // the conv history of every sequence has been read: roll the conv state
   if (p.conv.state && launch_conv_prefill_state(p, stream) != 0) return -1;

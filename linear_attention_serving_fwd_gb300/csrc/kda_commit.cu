@@ -52,12 +52,20 @@ __device__ __forceinline__ CommitItem commit_item(const CommitParams& p, int ite
   return r;
 }
 
+// A state row's bytes (fp32 or bf16 elements).
+template <bool SBF16>
+__device__ __forceinline__ unsigned char* cm_state_row(const CommitParams& p, int64_t slot, int head) {
+  return static_cast<unsigned char*>(p.pool) + (slot * p.slot_stride + (int64_t)head * D * D) * (SBF16 ? 2 : 4);
+}
+
+template <bool SBF16>
 __device__ __forceinline__ void commit_issue_state(const CommitParams& p, const CommitItem& it, float* sbuf,
                                                    uint64_t* bar) {
-  const float* src = p.pool + it.slot * p.slot_stride + (int64_t)it.head * D * D;
-  mbar_arrive_expect_tx(bar, CM_STATE);
-  bulk_g2s(sbuf, src, CM_STATE / 2, bar);
-  bulk_g2s(sbuf + D * D / 2, src + D * D / 2, CM_STATE / 2, bar);
+  constexpr int bytes = SBF16 ? CM_STATE / 2 : CM_STATE;
+  const unsigned char* src = cm_state_row<SBF16>(p, it.slot, it.head);
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_g2s(sbuf, src, bytes / 2, bar);
+  bulk_g2s(reinterpret_cast<unsigned char*>(sbuf) + bytes / 2, src + bytes / 2, bytes / 2, bar);
 }
 
 __device__ __forceinline__ void commit_issue_records(const CommitParams& p, const CommitItem& it, float* cbuf,
@@ -73,6 +81,7 @@ __device__ __forceinline__ void commit_issue_records(const CommitParams& p, cons
 __device__ __forceinline__ int cm_row(int warp, int lane, int i) { return 8 * warp + 4 * (lane >> 4) + i; }
 __device__ __forceinline__ int cm_chan(int lane, int j) { return 4 * (lane & 15) + 64 * j; }
 
+template <bool SBF16>
 __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   CommitSmem& s = *reinterpret_cast<CommitSmem*>(smem_raw);
@@ -91,11 +100,11 @@ __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitP
   CommitItem itn = nxt < items ? commit_item(p, nxt) : CommitItem{};
   if (tid == 0) {
     if (it.work) {
-      commit_issue_state(p, it, s.state[0], &s.sbar[0]);
+      commit_issue_state<SBF16>(p, it, s.state[0], &s.sbar[0]);
       commit_issue_records(p, it, s.corr[0], s.kg[0], &s.rbar[0]);
     }
     if (itn.work) {
-      commit_issue_state(p, itn, s.state[1], &s.sbar[1]);
+      commit_issue_state<SBF16>(p, itn, s.state[1], &s.sbar[1]);
       commit_issue_records(p, itn, s.corr[1], s.kg[1], &s.rbar[1]);
     }
   }
@@ -117,8 +126,13 @@ __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitP
           // token t = warp: k^_t and the gate, lane = 4 channels
           const __nv_bfloat16* kr = s.kg[b] + warp * 2 * D;
           float kv[4], gv[4];
-          load_bf16x4(kr + 4 * lane, kv);
-          load_bf16x4(kr + D + 4 * lane, gv);
+          if (p.kg_fp16) {
+            load_act4<true>(kr + 4 * lane, kv);
+            load_act4<true>(kr + D + 4 * lane, gv);
+          } else {
+            load_act4<false>(kr + 4 * lane, kv);
+            load_act4<false>(kr + D + 4 * lane, gv);
+          }
           const float rk = rsqrtf(warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]) +
                                   1e-6f);
           float4 dt = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -140,8 +154,15 @@ __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitP
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const float4 x4 =
-                *reinterpret_cast<const float4*>(s.state[b] + cm_row(warp, lane, i) * D + cm_chan(lane, j));
+            float4 x4;
+            if constexpr (SBF16) {
+              float v[4];
+              load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(s.state[b]) + cm_row(warp, lane, i) * D +
+                              cm_chan(lane, j), v);
+              x4 = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+              x4 = *reinterpret_cast<const float4*>(s.state[b] + cm_row(warp, lane, i) * D + cm_chan(lane, j));
+            }
             S[i][2 * j] = make_float2(x4.x, x4.y);
             S[i][2 * j + 1] = make_float2(x4.z, x4.w);
           }
@@ -158,7 +179,7 @@ __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitP
       return;
     }
     // state buffer b is in registers: the item after next may stream into it
-    if (tid == 0 && it2.work) commit_issue_state(p, it2, s.state[b], &s.sbar[b]);
+    if (tid == 0 && it2.work) commit_issue_state<SBF16>(p, it2, s.state[b], &s.sbar[b]);
     if (it.work) {
       if (tid < D) {
         // channel k = tid: L_t, e^{L_a} and the weights e^{L_a - L_t} k^_t
@@ -210,18 +231,29 @@ __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitP
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-          *reinterpret_cast<float4*>(s.sout + cm_row(warp, lane, i) * D + cm_chan(lane, j)) =
-              make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y);
+        for (int j = 0; j < 2; ++j) {
+          const int o = cm_row(warp, lane, i) * D + cm_chan(lane, j);
+          if constexpr (SBF16) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(S[i][2 * j].x, S[i][2 * j].y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(S[i][2 * j + 1].x, S[i][2 * j + 1].y);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(s.sout) + o) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+          } else {
+            *reinterpret_cast<float4*>(s.sout + o) =
+                make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y);
+          }
+        }
       fence_proxy_async_smem();
     }
     if (tid == 0 && it.bad) set_error(p.err, ERR_INDEX);
     __syncthreads();  // records of buffer b consumed, sout written
     if (tid == 0) {
       if (it.work) {
-        float* dst = p.pool + it.slot * p.slot_stride + (int64_t)it.head * D * D;
-        bulk_s2g(dst, s.sout, CM_STATE / 2);
-        bulk_s2g(dst + D * D / 2, s.sout + D * D / 2, CM_STATE / 2);
+        constexpr int bytes = SBF16 ? CM_STATE / 2 : CM_STATE;
+        unsigned char* dst = cm_state_row<SBF16>(p, it.slot, it.head);
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(s.sout);
+        bulk_s2g(dst, src, bytes / 2);
+        bulk_s2g(dst + bytes / 2, src + bytes / 2, bytes / 2);
         bulk_commit();
         stored = true;
       }
@@ -242,14 +274,19 @@ int launch_commit(const CommitParams& p, cudaStream_t stream) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(kda_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(kda_commit_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(CommitSmem));
+    cudaFuncSetAttribute(kda_commit_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(CommitSmem));
   }
   const int items = p.n_req * p.hv;
   if (items == 0) return 0;
   const int grid = items < num_sms ? items : num_sms;
   trace_begin("kda_commit", stream);
-  kda_commit_kernel<<<grid, CM_THREADS, sizeof(CommitSmem), stream>>>(p);
+  if (p.state_bf16)
+    kda_commit_kernel<true><<<grid, CM_THREADS, sizeof(CommitSmem), stream>>>(p);
+  else
+    kda_commit_kernel<false><<<grid, CM_THREADS, sizeof(CommitSmem), stream>>>(p);
   trace_end(stream);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

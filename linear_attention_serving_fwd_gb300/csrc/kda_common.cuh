@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,6 +36,38 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) { atomic
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Activations are 16-bit storage read through __nv_bfloat16 pointers: bf16,
+// or fp16 bits when the call's activations are fp16.
+template <bool FP16>
+__device__ __forceinline__ float act_f(__nv_bfloat16 x) {
+  if constexpr (FP16) {
+    return __half2float(*reinterpret_cast<const __half*>(&x));
+  } else {
+    return __bfloat162float(x);
+  }
+}
+__device__ __forceinline__ float act_f(__nv_bfloat16 x, bool fp16) {
+  return fp16 ? act_f<true>(x) : act_f<false>(x);
+}
+// two fp32 values rounded to the activation type, as 32 bits
+template <bool FP16>
+__device__ __forceinline__ uint32_t act_pack2(float a, float b) {
+  if constexpr (FP16) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+__device__ __forceinline__ __nv_bfloat16 act_from_f(float x, bool fp16) {
+  if (fp16) {
+    const __half h = __float2half_rn(x);
+    return *reinterpret_cast<const __nv_bfloat16*>(&h);
+  }
+  return __float2bfloat16_rn(x);
+}
+
 // Four consecutive bf16 (8 bytes, 8-byte aligned) to fp32.
 __device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float out[4]) {
   uint2 raw = *reinterpret_cast<const uint2*>(p);
@@ -42,6 +75,25 @@ __device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float out[4]
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
   float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
   out[0] = fa.x; out[1] = fa.y; out[2] = fb.x; out[3] = fb.y;
+}
+// Four consecutive activations (8 bytes, 8-byte aligned) to fp32.
+template <bool FP16>
+__device__ __forceinline__ void load_act4(const __nv_bfloat16* p, float out[4]) {
+  if constexpr (FP16) {
+    uint2 raw = *reinterpret_cast<const uint2*>(p);
+    const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    out[0] = fa.x; out[1] = fa.y; out[2] = fb.x; out[3] = fb.y;
+  } else {
+    load_bf16x4(p, out);
+  }
+}
+
+// Four fp32 values rounded to bf16 and back (a bf16 state's storage).
+__device__ __forceinline__ float4 round_bf16x4(float4 x) {
+  const float2 a = __bfloat1622float2(__floats2bfloat162_rn(x.x, x.y));
+  const float2 b = __bfloat1622float2(__floats2bfloat162_rn(x.z, x.w));
+  return make_float4(a.x, a.y, b.x, b.y);
 }
 
 __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float v[4]) {

@@ -60,8 +60,8 @@ int scratch_for_current_device(void** out) {
 
 extern "C" int kda_chunk_fwd_noalloc(const kda_activations* x, void* out,
                                      const int32_t* cu_seqlens, int32_t n_seqs,
-                                     const float* initial_state, float* final_state,
-                                     float* state_cache, int64_t slot_stride, int64_t n_slots,
+                                     const void* initial_state, void* final_state,
+                                     void* state_cache, int64_t slot_stride, int64_t n_slots,
                                      const int32_t* state_indices,
                                      const uint8_t* has_initial_state, int32_t groups,
                                      void* stream) {

@@ -26,8 +26,8 @@ struct WindowParams {
   const float* dt_bias;
   float scale, lower_bound;
   int has_gate;
-  __nv_bfloat16* out;  // [T, Hv, 128]
-  float* pool;         // [n_slots, Hv, 128, 128] (read only for verify)
+  __nv_bfloat16* out;  // [T, Hv, 128], activation dtype
+  void* pool;          // [n_slots, Hv, 128, 128] fp32 or bf16 (read only for verify)
   int64_t slot_stride;
   int64_t n_slots;
   const int32_t* query_start;
@@ -40,6 +40,7 @@ struct WindowParams {
   const int32_t* n_accepted;
   int n_req, window, hqk, hv;
   ConvParams conv;       // verify only
+  int in_fp16, state_bf16;  // activation / state dtypes
   float* corr;          // verify: [n_req, Hv, window, 128]
   __nv_bfloat16* kg;    // verify: [n_req, Hv, window, 256]
   int32_t* counter;     // verify: ticket counter
@@ -47,12 +48,13 @@ struct WindowParams {
 };
 
 struct CommitParams {
-  float* pool;                 // [n_slots, Hv, 128, 128] fp32, rewritten in place
+  void* pool;                  // [n_slots, Hv, 128, 128] fp32 or bf16, rewritten in place
   int64_t slot_stride, n_slots;
   const int32_t* slots;        // [n_req]
   const int32_t* accepted;     // [n_req] accepted prefix length a
   const float* corr;           // [n_req, Hv, window, 128] U_t from kda_verify
   const __nv_bfloat16* kg;     // [n_req, Hv, window, 256] raw k_t, raw g_t from kda_verify
+  int state_bf16, kg_fp16;
   const float* A_log;
   const float* dt_bias;
   float lower_bound;
@@ -71,10 +73,11 @@ struct ChunkParams {
   int t_total, hqk, hv, n_seqs;
   int dense_len;               // > 0: dense sequences of this length (no cu_seqlens)
   const int32_t* cu_seqlens;   // [N+1] or null
-  __nv_bfloat16* out;
-  const float* h0;             // [N, Hv, 128, 128] or null
-  float* hT;                   // [N, Hv, 128, 128] or null
-  float* cache;                // paged cache or null
+  __nv_bfloat16* out;          // activation dtype
+  int in_fp16, state_bf16;     // activation / state dtypes
+  const void* h0;              // [N, Hv, 128, 128] state dtype, or null
+  void* hT;                    // [N, Hv, 128, 128] or null
+  void* cache;                 // paged cache or null
   int64_t slot_stride, n_slots;
   const int32_t* state_indices;
   const uint8_t* has_init;
@@ -93,7 +96,7 @@ struct ChunkParams {
   // mid-prefill snapshots: the state after ckpt_off[n] tokens of sequence n
   // (a positive multiple of CHUNK, at most its length) goes to row
   // ckpt_idx[n] (or n) of ckpt; others are skipped
-  float* ckpt;
+  void* ckpt;                   // state dtype
   int64_t ckpt_stride, ckpt_rows;
   const int32_t* ckpt_off;
   const int32_t* ckpt_idx;

@@ -105,14 +105,44 @@ __device__ __forceinline__ ItemInfo item_info(const WindowParams& p, int item) {
   return r;
 }
 
-// Bulk copies of an item (one thread): the state into sbuf on sbar, the
-// window's q/k/v/g rows into ibuf on ibar.
+// A state row's bytes: fp32 or bf16 elements.
+template <bool SBF16>
+__device__ __forceinline__ unsigned char* state_row(const WindowParams& p, int64_t slot, int head) {
+  return static_cast<unsigned char*>(p.pool) + (slot * p.slot_stride + (int64_t)head * D * D) * (SBF16 ? 2 : 4);
+}
+
+// Bulk copy of an item's state into sbuf on sbar (one thread).
+template <bool SBF16>
 __device__ __forceinline__ void issue_state(const WindowParams& p, const ItemInfo& it, float* sbuf,
                                             uint64_t* sbar) {
-  const float* src = p.pool + it.slot * p.slot_stride + (int64_t)it.head * D * D;
-  mbar_arrive_expect_tx(sbar, STATE_BYTES);
-  bulk_g2s(sbuf, src, STATE_BYTES / 2, sbar);
-  bulk_g2s(sbuf + D * D / 2, src + D * D / 2, STATE_BYTES / 2, sbar);
+  constexpr int bytes = SBF16 ? STATE_BYTES / 2 : STATE_BYTES;
+  const unsigned char* src = state_row<SBF16>(p, it.slot, it.head);
+  mbar_arrive_expect_tx(sbar, bytes);
+  bulk_g2s(sbuf, src, bytes / 2, sbar);
+  bulk_g2s(reinterpret_cast<unsigned char*>(sbuf) + bytes / 2, src + bytes / 2, bytes / 2, sbar);
+}
+
+// Four state values of row ``row``, channels ``chan``.. from a staged state
+// (fp32, or bf16 widened).
+template <bool SBF16>
+__device__ __forceinline__ float4 state_ld4(const float* sbuf, int row, int chan) {
+  if constexpr (SBF16) {
+    float v[4];
+    load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(sbuf) + row * D + chan, v);
+    return make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    return *reinterpret_cast<const float4*>(sbuf + row * D + chan);
+  }
+}
+template <bool SBF16>
+__device__ __forceinline__ void state_st4(void* base, int row, int chan, float4 x) {
+  if constexpr (SBF16) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(base) + row * D + chan) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(base) + row * D + chan) = x;
+  }
 }
 
 // The window's q/k/v/g rows, one bulk copy per lane of the calling warp.
@@ -157,12 +187,13 @@ __device__ __forceinline__ TokenScalars load_token_scalars(const WindowParams& p
 }
 
 // Token t's per-channel vectors, computed by one warp (lane = 4 channels).
+template <bool FP16>
 __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s, const TokenScalars& ts,
                                               const __nv_bfloat16* rowp, int t, int lane) {
   float qv[4], kv[4], gv[4];
-  load_bf16x4(rowp + 0 * D + 4 * lane, qv);
-  load_bf16x4(rowp + 1 * D + 4 * lane, kv);
-  load_bf16x4(rowp + 3 * D + 4 * lane, gv);
+  load_act4<FP16>(rowp + 0 * D + 4 * lane, qv);
+  load_act4<FP16>(rowp + 1 * D + 4 * lane, kv);
+  load_act4<FP16>(rowp + 3 * D + 4 * lane, gv);
   const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
   const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
   const float rq = rsqrtf(sq + 1e-6f) * p.scale, rk = rsqrtf(sk + 1e-6f);
@@ -186,7 +217,7 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
   *reinterpret_cast<float4*>(&s.tkh[t][4 * lane]) = make_float4(kh[0], kh[1], kh[2], kh[3]);
   if (lane == 0) {
     s.tkq[t] = kq;
-    s.tbeta[t] = sigmoidf_(bf2f(ts.beta));
+    s.tbeta[t] = sigmoidf_(act_f<FP16>(ts.beta));
   }
 }
 
@@ -228,7 +259,7 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
 __device__ __forceinline__ int win_row(int warp, int lane, int i) { return 8 * warp + 4 * (lane >> 4) + i; }
 __device__ __forceinline__ int win_chan(int lane, int j) { return 4 * (lane & 15) + 64 * j; }
 
-template <bool VERIFY>
+template <bool VERIFY, bool SBF16, bool FP16>
 __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, const ItemInfo& it,
                                            float2 (&S)[4][4], const __nv_bfloat16* ibuf, int warp,
                                            int lane) {
@@ -282,12 +313,12 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
     }
     const float mine = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
     // lanes with m < 4: U of row m; lanes with m >= 4: the output of row m - 4
-    const float vval = bf2f(ibuf[t * 4 * D + 2 * D + my_row]);
+    const float vval = act_f<FP16>(ibuf[t * 4 * D + 2 * D + my_row]);
     const float U = beta * (vval - mine);
     const int half = lane & 16;
     const float Urow = __shfl_sync(0xffffffffu, U, half | (2 * (m & 3)));
     if (m >= 4) {
-      if ((lane & 1) == 0) p.out[(tok * p.hv + h) * D + my_row] = __float2bfloat16_rn(mine + Urow * kq);
+      if ((lane & 1) == 0) p.out[(tok * p.hv + h) * D + my_row] = act_from_f(mine + Urow * kq, FP16);
     } else if (VERIFY && (lane & 1) == 0) {
       p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + my_row] = U;
     }
@@ -314,24 +345,37 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) S[i][jj] = ffma2(S[i][jj], dv[jj], fmul2(kv[jj], uu));
     }
+    if constexpr (SBF16) {
+      // a bf16 state is stored after every token: the next token starts
+      // from the rounded state, as repeated single-token decode would
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float4 r = round_bf16x4(make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x,
+                                                    S[i][2 * j + 1].y));
+          S[i][2 * j] = make_float2(r.x, r.y);
+          S[i][2 * j + 1] = make_float2(r.z, r.w);
+        }
+    }
     if (!VERIFY && p.step_slots && t + 1 < it.qlen) {
       // slot table: the state after token t, unless its row is the last
       // token's (written after the window) or disabled
       const int64_t row = p.step_slots[(int64_t)it.request * p.step_stride + t];
       if (row >= 0 && row != it.wslot) {
-        float* dst = p.pool + row * p.slot_stride + (int64_t)h * D * D;
+        void* dst = state_row<SBF16>(p, row, h);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            *reinterpret_cast<float4*>(dst + win_row(warp, lane, i) * D + win_chan(lane, j)) =
-                make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y);
+            state_st4<SBF16>(dst, win_row(warp, lane, i), win_chan(lane, j),
+                             make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y));
       }
     }
   }
 }
 
-template <bool VERIFY>
+template <bool VERIFY, bool SBF16, bool FP16>
 __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const WindowParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   WinSmem& s = *reinterpret_cast<WinSmem*>(smem_raw);
@@ -367,7 +411,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       if (its[b] < items) {
         const ItemInfo ii = item_info(p, its[b]);
         if (ii.work) {
-          if (lane == 0) issue_state(p, ii, s.state[b], &s.sbar[b]);
+          if (lane == 0) issue_state<SBF16>(p, ii, s.state[b], &s.sbar[b]);
           issue_inputs(p, ii, s.in[b], &s.ibar[b], lane);
         }
       }
@@ -382,7 +426,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
   while (cur < items) {
     if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
     bool ok = true;
-    const bool conv = VERIFY && p.conv.state != nullptr;
+    const bool conv = VERIFY && !FP16 && p.conv.state != nullptr;  // conv: bf16 activations only
     float2 S[4][4];
     float yc[3][4];  // conv outputs of token ``warp`` (verify with a conv)
     if (it.work) {
@@ -395,14 +439,13 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
           if (conv)
             conv_token(p, it, s.in[b], warp, lane, yc);
           else
-            token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+            token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const float4 x4 = *reinterpret_cast<const float4*>(s.state[b] + win_row(warp, lane, i) * D +
-                                                               win_chan(lane, j));
+            const float4 x4 = state_ld4<SBF16>(s.state[b], win_row(warp, lane, i), win_chan(lane, j));
             S[i][2 * j] = make_float2(x4.x, x4.y);
             S[i][2 * j + 1] = make_float2(x4.z, x4.w);
           }
@@ -432,17 +475,17 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
               make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
         }
         __syncwarp();
-        token_vectors(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
       }
       __syncthreads();
     }
     const int nn = s.next;
     const ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
-    if (tid == 0 && nn < items && it2.work) issue_state(p, it2, s.state[b], &s.sbar[b]);
+    if (tid == 0 && nn < items && it2.work) issue_state<SBF16>(p, it2, s.state[b], &s.sbar[b]);
     // the next item's scalars, used a step from now
     const TokenScalars ts_next = load_token_scalars(p, itn, warp, lane);
     if (it.work) {
-      run_tokens<VERIFY>(p, s, it, S, s.in[b], warp, lane);
+      run_tokens<VERIFY, SBF16, FP16>(p, s, it, S, s.in[b], warp, lane);
       if (!VERIFY) {
         // the previous item's bulk store has read sout by now (a whole item
         // ago); confirm it before anyone overwrites sout
@@ -452,8 +495,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            *reinterpret_cast<float4*>(s.sout + win_row(warp, lane, i) * D + win_chan(lane, j)) =
-                make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y);
+            state_st4<SBF16>(s.sout, win_row(warp, lane, i), win_chan(lane, j),
+                             make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y));
         fence_proxy_async_smem();
       }
     } else if (it.zero) {
@@ -465,9 +508,11 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
     if (tid == 0 && it.bad) set_error(p.err, ERR_INDEX);
     __syncthreads();  // input buffer b and the token vectors consumed, sout written
     if (!VERIFY && tid == 0 && it.work && it.wslot >= 0) {
-      float* dst = p.pool + it.wslot * p.slot_stride + (int64_t)it.head * D * D;
-      bulk_s2g(dst, s.sout, STATE_BYTES / 2);
-      bulk_s2g(dst + D * D / 2, s.sout + D * D / 2, STATE_BYTES / 2);
+      constexpr int bytes = SBF16 ? STATE_BYTES / 2 : STATE_BYTES;
+      unsigned char* dst = state_row<SBF16>(p, it.wslot, it.head);
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(s.sout);
+      bulk_s2g(dst, src, bytes / 2);
+      bulk_s2g(dst + bytes / 2, src + bytes / 2, bytes / 2);
       bulk_commit();
       stored = true;
     }
@@ -483,25 +528,39 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
 }
 
 // Host-side launcher (called from the API layer after validation).
+template <bool VERIFY, bool SBF16, bool FP16>
+static void launch_window_t(const WindowParams& p, int grid, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(WinSmem));
+    attr = true;
+  }
+  kda_window_kernel<VERIFY, SBF16, FP16><<<grid, WIN_THREADS, sizeof(WinSmem), stream>>>(p);
+}
+
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
   static int num_sms = 0;
   if (num_sms == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(kda_window_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(WinSmem));
-    cudaFuncSetAttribute(kda_window_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(WinSmem));
   }
   const int items = p.n_req * p.hv;
   if (items == 0) return 0;
   const int grid = items < num_sms ? items : num_sms;
+  const int variant = (verify ? 4 : 0) + (p.state_bf16 ? 2 : 0) + (p.in_fp16 ? 1 : 0);
   trace_begin(verify ? "kda_verify_window" : "kda_decode_window", stream);
-  if (verify)
-    kda_window_kernel<true><<<grid, WIN_THREADS, sizeof(WinSmem), stream>>>(p);
-  else
-    kda_window_kernel<false><<<grid, WIN_THREADS, sizeof(WinSmem), stream>>>(p);
+  switch (variant) {
+    case 0: launch_window_t<false, false, false>(p, grid, stream); break;
+    case 1: launch_window_t<false, false, true>(p, grid, stream); break;
+    case 2: launch_window_t<false, true, false>(p, grid, stream); break;
+    case 3: launch_window_t<false, true, true>(p, grid, stream); break;
+    case 4: launch_window_t<true, false, false>(p, grid, stream); break;
+    case 5: launch_window_t<true, false, true>(p, grid, stream); break;
+    case 6: launch_window_t<true, true, false>(p, grid, stream); break;
+    default: launch_window_t<true, true, true>(p, grid, stream); break;
+  }
   trace_end(stream);
   // verify with a conv: every history has been read, roll the conv state
   if (verify && p.conv.state && launch_conv_roll(p, stream) != 0) return -1;

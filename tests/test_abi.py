@@ -67,8 +67,8 @@ def _msg():
 
 
 @pytest.mark.parametrize("over,code,text", [
-    (dict(dtype=1), DTYPE, "bfloat16"),
-    (dict(dtype=7), DTYPE, "bfloat16"),
+    (dict(dtype=7), DTYPE, "bfloat16 or float16"),
+    (dict(state_bf16=2), INVALID, "state_bf16"),
     (dict(hv=3), INVALID, "GVA requires"),
     (dict(hqk=0), INVALID, "positive"),
     (dict(A_log=None), INVALID, "provided together"),
@@ -92,6 +92,9 @@ def test_chunk_rules_on_states_and_workspace():
     assert "needs state_indices" in _msg()
     assert _chunk(a, cache=FAKE, idx=FAKE, stride=4 * 16384 + 2, slots=3) == INVALID
     assert "slot_stride" in _msg()
+    # bf16 states: 16-byte rows need strides in multiples of 8 elements
+    assert _chunk(_acts(state_bf16=1), cache=FAKE, idx=FAKE, stride=4 * 16384 + 4, slots=3) == INVALID
+    assert "multiple of 8" in _msg()
     assert _chunk(a, cache=FAKE, idx=FAKE, stride=4 * 16384, slots=0) == INVALID
     assert "at least one slot" in _msg()
     assert _chunk(a, ws_bytes=16) == INVALID
@@ -154,6 +157,7 @@ def test_conv_argument_rules():
     assert _chunk_ex(a, conv=_conv_desc(positions=2)) == INVALID and "at least 3 positions" in _msg()
     assert _chunk_ex(a, conv=_conv_desc(state_indices=None)) == INVALID and "state_indices" in _msg()
     assert _chunk_ex(a, conv=_conv_desc(pos_stride=0)) == INVALID and "positive" in _msg()
+    assert _chunk_ex(_acts(dtype=1), conv=_conv_desc()) == DTYPE and "bfloat16 activations" in _msg()
     lib = _native.lib()
 
     def verify(cv, win=4, slots=4):
@@ -258,3 +262,11 @@ def test_commit_validation():
     assert _commit(lb=-11.0) == INVALID and "lower_bound" in _msg()
     assert _commit(pool=None) == INVALID and "state_pool" in _msg()
     assert _commit(slots=0) == INVALID and "at least one slot" in _msg()
+    lib = _native.lib()
+
+    def commit_ex(sb, kf, stride=4 * 16384):
+        return lib.kda_commit_ex(FAKE, stride, 8, FAKE, FAKE, 2, 4, 4, FAKE, FAKE, FAKE, FAKE, -5.0, sb, kf,
+                                 None)
+    assert commit_ex(2, 0) == INVALID and "state_bf16 and kg_fp16" in _msg()
+    assert commit_ex(0, 3) == INVALID and "state_bf16 and kg_fp16" in _msg()
+    assert commit_ex(1, 0, stride=4 * 16384 + 4) == INVALID and "multiple of 8" in _msg()
