@@ -598,26 +598,28 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
     return res
 
 
-def cpu_baseline(x, n_heads=16, n_tokens=4096):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload:
-    sequence 0, ``n_heads`` heads, its first ``n_tokens`` tokens."""
+def cpu_baseline(x, min_seconds=10.0, max_reps=200):
+    """The fp64 oracle, as it stands, on the whole dense workload (every
+    sequence and head), repeated until ``min_seconds`` of wall time."""
     import oracle
-    sl = slice(0, n_tokens)
-    h = slice(0, n_heads)
-    q, k = x.q[sl, h].cpu(), x.k[sl, h].cpu()
-    v, g, b = x.v[sl, h].cpu(), x.g[sl, h].cpu(), x.beta[sl, h].cpu()
-    A_log, dt = x.A_log[h].cpu(), x.dt_bias[h].cpu()
-    h0 = x.initial_state[0:1, h].cpu() if x.initial_state is not None else None
+    q, k, v, g, b = (t.cpu() for t in (x.q, x.k, x.v, x.g, x.beta))
+    A_log, dt = x.A_log.cpu(), x.dt_bias.cpu()
+    h0 = x.initial_state.cpu() if x.initial_state is not None else None
+    cu = x.cu_seqlens.cpu()
     threads = os.cpu_count() or 1
+    reps = 0
     t0 = time.perf_counter()
-    oracle.recurrence(q, k, v, g, b, [0, n_tokens], A_log=A_log, dt_bias=dt,
-                      lower_bound=x.lower_bound, h0=h0, n_threads=threads)
-    dt_s = time.perf_counter() - t0
-    th_per_s = n_heads * n_tokens / dt_s
-    return {"value": round(th_per_s / x.hv, 2), "unit": "tokens/s", "cores": threads,
+    while True:
+        oracle.recurrence(q, k, v, g, b, cu, A_log=A_log, dt_bias=dt, lower_bound=x.lower_bound,
+                          h0=h0, want_out=True, want_state=True, n_threads=threads)
+        reps += 1
+        dt_s = time.perf_counter() - t0
+        if dt_s >= min_seconds or reps >= max_reps:
+            break
+    return {"value": round(x.t_total * reps / dt_s, 2), "unit": "tokens/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt_s, 3),
-            "sample": f"sequence 0, heads 0..{n_heads - 1}, tokens 0..{n_tokens - 1} of the dense "
-                      f"workload (fp64 token recurrence, OpenMP); token-heads/s divided by Hv={x.hv}"}
+            "sample": f"the whole dense workload ({x.n_seqs} x {x.t_total // x.n_seqs} tokens, Hv={x.hv}) "
+                      f"{reps} times (fp64 token recurrence, OpenMP over sequence, head and value block)"}
 
 
 # ---------------------------------------------------------------------------
@@ -629,11 +631,10 @@ def run_reference(args):
     import oracle
     from linear_attention_serving_fwd_gb300 import workloads as W
     w = WORKLOAD
-    # bounded sample per step: 2 heads x 1024 tokens of sequence 0
-    nh, nt = 2, 1024
-    x = W.dense_prefill(1, nt, nh, nh, seed=0)
+    # one step = the whole dense workload (every sequence and head)
+    x = W.dense_prefill(w["B"], w["T"], w["hqk"], w["hv"], seed=0)
     threads = os.cpu_count() or 1
-    args_ = (x.q, x.k, x.v, x.g, x.beta, [0, nt])
+    args_ = (x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens)
     kw = dict(A_log=x.A_log, dt_bias=x.dt_bias, lower_bound=x.lower_bound,
               h0=x.initial_state, n_threads=threads)
     for _ in range(max(1, args.warmup)):
@@ -642,9 +643,9 @@ def run_reference(args):
     for _ in range(args.steps):
         oracle.recurrence(*args_, **kw)
     secs = time.perf_counter() - t0
-    value = nh * nt * args.steps / secs / w["hv"]
-    sample = (f"per step: {nh} heads x {nt} tokens of one dense sequence (fp64 token "
-              f"recurrence, OpenMP, {threads} threads); token-heads/s divided by Hv={w['hv']}")
+    value = x.t_total * args.steps / secs
+    sample = (f"per step: the whole dense workload ({w['B']} x {w['T']} tokens, Hv={w['hv']}; fp64 token "
+              f"recurrence, OpenMP, {threads} threads)")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
