@@ -684,10 +684,12 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated) ----------------
+    // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated); R = kg^T T
+    // (A = kg^T) into columns 128.., read while phase 6 runs
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
+      tc::mma_kloop(tmem + 128, smem_u32(s.KG), smem_u32(B2), 128, 64, 64, 0, false);
       tc::mma_commit(&s.bar);
     }
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
@@ -710,11 +712,28 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     __syncthreads();
 
     // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA): w^T to shared memory
-    // (MN-major B operand of P), qg' to the record
+    // (MN-major B operand of P), qg' to the record; -o_intra = (-A_qk T) v
+    // (A = A3's rows 64.., M = 64: row r at lane r % 16 + 32 (r / 16)) into
+    // columns 256.., read while phase 7 runs.  Meanwhile R goes to the record.
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop(tmem, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
+      tc::mma_run<4>(tmem + 256, tc::smem_desc(smem_u32(A3) + 1024, 2048, 128),
+                     tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096, tc::idesc_f16(64, 128, 0), false);
       tc::mma_commit(&s.bar);
+    }
+    {
+      tc::fence_after_sync();
+      const int k = 32 * (warp & 3) + lane, cq = warp >> 2;
+      float b[16];
+      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 128 + 16 * cq), b);
+      uint32_t rv[8];
+#pragma unroll
+      for (int t = 0; t < 16; t += 2) rv[t >> 1] = pack_half2(b[t], b[t + 1]);
+#pragma unroll
+      for (int g8 = 0; g8 < 2; ++g8)
+        *reinterpret_cast<uint4*>(wsb + CH_R + tc::kmajor_offset(k, 16 * cq + 8 * g8, 128)) =
+            make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
     }
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
@@ -741,15 +760,32 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- phase 7: P = -kg^T w, R = kg^T T (A = kg^T) and -o_intra =
-    // (-A_qk T) v (A = A3's rows 64.., M = 64: row r at lane r % 16 + 32 (r / 16))
+    // ---- phase 7: P = -kg^T w (A = kg^T, B = w^T MN-major); meanwhile
+    // -o_intra goes to the record
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop_bmn(tmem, smem_u32(s.KG), smem_u32(WT), 128, 128, 64, WT_LBO, WT_SBO, false);
-      tc::mma_kloop(tmem + 128, smem_u32(s.KG), smem_u32(B2), 128, 64, 64, 0, false);
-      tc::mma_run<4>(tmem + 256, tc::smem_desc(smem_u32(A3) + 1024, 2048, 128),
-                     tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096, tc::idesc_f16(64, 128, 0), false);
       tc::mma_commit(&s.bar);
+    }
+    {
+      tc::fence_after_sync();
+      // o_intra, value block cq: lanes 0..15 of the warp hold rows 16 (warp & 3) + lane
+      const int cq = warp >> 2;
+      float a[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 256 + 32 * cq), a);
+      if (lane < 16) {
+        const int r = 16 * (warp & 3) + lane;
+        uint32_t ov[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(-a[t], -a[t + 1]);
+          ov[t >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(wsb + CH_OI + cq * OI_BLOCK + r * 64 + 16 * g8) =
+              make_uint4(ov[4 * g8], ov[4 * g8 + 1], ov[4 * g8 + 2], ov[4 * g8 + 3]);
+      }
     }
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
@@ -765,30 +801,6 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       for (int g8 = 0; g8 < 4; ++g8)
         *reinterpret_cast<uint4*>(wsb + CH_P + tc::kmajor_offset(k, 32 * cq + 8 * g8, 128)) =
             make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
-      float b[16];
-      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 128 + 16 * cq), b);
-      uint32_t rv[8];
-#pragma unroll
-      for (int t = 0; t < 16; t += 2) rv[t >> 1] = pack_half2(b[t], b[t + 1]);
-#pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8)
-        *reinterpret_cast<uint4*>(wsb + CH_R + tc::kmajor_offset(k, 16 * cq + 8 * g8, 128)) =
-            make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
-      // o_intra, value block cq: lanes 0..15 of the warp hold rows 16 (warp & 3) + lane
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 256 + 32 * cq), a);
-      if (lane < 16) {
-        const int r = 16 * (warp & 3) + lane;
-        uint32_t ov[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(-a[t], -a[t + 1]);
-          ov[t >> 1] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-#pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(wsb + CH_OI + cq * OI_BLOCK + r * 64 + 16 * g8) =
-              make_uint4(ov[4 * g8], ov[4 * g8 + 1], ov[4 * g8 + 2], ov[4 * g8 + 3]);
-      }
     }
     tc::fence_before_sync();
     __syncthreads();
