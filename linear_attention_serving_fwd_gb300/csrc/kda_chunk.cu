@@ -452,18 +452,18 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         const float2 iE = make_float2(__expf(mR - lam[i]), __expf(mR - lam[i + 1]));
         const float2 kh = make_float2(kv[i], kv[i + 1]), qh = make_float2(qv[i], qv[i + 1]);
         const float2 xk = fmul2(kh, E), xq = fmul2(qh, E), y = fmul2(kh, iE);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32(xk.x);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r + 1, c, 128)) = tc::to_tf32(xk.y);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32(xq.x);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(65 + r, c, 128)) = tc::to_tf32(xq.y);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32_int(xk.x);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r + 1, c, 128)) = tc::to_tf32_int(xk.y);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32_int(xq.x);
+        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(65 + r, c, 128)) = tc::to_tf32_int(xq.y);
 #pragma unroll
         for (int R2 = 0; R2 < 4; ++R2)
           if (R2 >= Rq) {
             const float2 yf = fmul2(y, make_float2(F[R2], F[R2]));
             *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
-                tc::to_tf32(yf.x);
+                tc::to_tf32_int(yf.x);
             *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r + 1, c, YROWS)) =
-                tc::to_tf32(yf.y);
+                tc::to_tf32_int(yf.y);
           }
       }
       fence_proxy_async_smem();

@@ -86,6 +86,14 @@ __device__ __forceinline__ float to_tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
 }
+// The same rounding on the integer pipe, for finite x below 2^128 - 2^115:
+// tf32 keeps 10 of fp32's 23 fraction bits, so adding half of the dropped
+// 13-bit field (0x1000) to the sign-magnitude pattern rounds the magnitude
+// half up (ties away from zero; a carry correctly bumps the exponent), and
+// the mask clears the dropped bits.
+__device__ __forceinline__ float to_tf32_int(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
 
 // --- TMEM allocation (one full warp executes these) -----------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
