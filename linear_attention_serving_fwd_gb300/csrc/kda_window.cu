@@ -55,6 +55,7 @@ struct __align__(128) WinSmem {
   float tkh[MAX_WINDOW][D];   // k^
   float tbeta[MAX_WINDOW];
   float tkq[MAX_WINDOW];      // k^ . q~
+  float cc[4][4], dd[4][4];   // windowed solve: coupling scalars c_tj, d_tj
   uint64_t sbar[2], ibar[2];
   int next;
 };
@@ -375,6 +376,225 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
   }
 }
 
+// Windowed solve of a 2..4-token window on an fp32 state (the verify page's
+// probes and coupling scalars, KdaTcVerify steps 2-4), replacing the token
+// loop: with P_t = prod_{i <= t} e^{gate_i} and r_{j,t} = k^_j prod_{i=j+1..t}
+// e^{gate_i} (per channel, every factor <= 1),
+//   U_t = beta_t (v_t - S0^T (P_t k^_t) - sum_{j<t} (r_{j,t} . k^_t) U_j)
+//   o_t = S0^T (P_t q~_t) + sum_{j<=t} (r_{j,t} . q~_t) U_j
+//   S   = P_{Q-1} * S0 + sum_j r_{j,Q-1} U_j^T
+// so the state is read once for all 2Q probes and updated once.  Every
+// thread takes part (it holds the state rows of the token loop's layout).
+template <bool VERIFY, bool FP16>
+__device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, const ItemInfo& it,
+                                             float2 (&S)[4][4], const __nv_bfloat16* ibuf,
+                                             const TokenScalars& ts, int tid, int warp, int lane) {
+  constexpr int QW = 4;
+  const int Q = it.qlen, h = it.head;
+  float* z = &s.tp[0][0];  // tp, tr, tdec, tkh: 16 KB of contiguous scratch
+  float* khat = z;
+  float* qtil = z + QW * D;
+  float* dec = z + 2 * QW * D;
+  float* kG = z + 3 * QW * D;
+  float* qG = z + 4 * QW * D;
+  float* wv = z + 5 * QW * D;
+  float* eGQ = z + 6 * QW * D;
+  float* pb = z;           // S0^T kG_t, over khat once the couplings are done
+  float* pa = z + QW * D;  // S0^T qG_t, over qtil
+  float* U = z + 2 * QW * D;  // over dec
+  const int c0 = 4 * lane;
+  // (1) warp t < Q: k^_t, q~_t, e^{gate_t}, beta_t (and verify's kg record)
+  if (warp < Q) {
+    const __nv_bfloat16* rowp = ibuf + warp * 4 * D;
+    float qv[4], kv[4], gv[4];
+    load_act4<FP16>(rowp + 0 * D + c0, qv);
+    load_act4<FP16>(rowp + 1 * D + c0, kv);
+    load_act4<FP16>(rowp + 3 * D + c0, gv);
+    const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
+    const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
+    const float rq = rsqrtf(sq + 1e-6f) * p.scale, rk = rsqrtf(sk + 1e-6f);
+    const float a = p.has_gate ? __expf(ts.alog) : 0.f;
+    const float dt[4] = {ts.dt.x, ts.dt.y, ts.dt.z, ts.dt.w};
+    float dv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float gate = p.has_gate ? p.lower_bound * sigmoidf_(a * (gv[j] + dt[j])) : gv[j];
+      dv[j] = __expf(gate);
+    }
+    *reinterpret_cast<float4*>(khat + warp * D + c0) = make_float4(kv[0] * rk, kv[1] * rk, kv[2] * rk, kv[3] * rk);
+    *reinterpret_cast<float4*>(qtil + warp * D + c0) = make_float4(qv[0] * rq, qv[1] * rq, qv[2] * rq, qv[3] * rq);
+    *reinterpret_cast<float4*>(dec + warp * D + c0) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+    if (lane == 0) s.tbeta[warp] = sigmoidf_(act_f<FP16>(ts.beta));
+    if (VERIFY) {
+      __nv_bfloat16* dst = p.kg + (((int64_t)it.request * p.hv + h) * p.window + warp) * 2 * D;
+      *reinterpret_cast<uint2*>(dst + c0) = *reinterpret_cast<const uint2*>(rowp + 1 * D + c0);
+      *reinterpret_cast<uint2*>(dst + D + c0) = *reinterpret_cast<const uint2*>(rowp + 3 * D + c0);
+    }
+  }
+  __syncthreads();
+  // (2) warp j: P_j k^_j, P_j q~_j (zero for j >= Q), the chain r_{j,t},
+  // its couplings with tokens t >= j, and r_{j,Q-1}
+  if (warp < QW) {
+    const int j = warp;
+    if (j < Q) {
+      float4 P = make_float4(1.f, 1.f, 1.f, 1.f);
+      for (int i = 0; i <= j; ++i) {
+        const float4 d4 = *reinterpret_cast<const float4*>(dec + i * D + c0);
+        P = make_float4(P.x * d4.x, P.y * d4.y, P.z * d4.z, P.w * d4.w);
+      }
+      const float4 kj = *reinterpret_cast<const float4*>(khat + j * D + c0);
+      const float4 qj = *reinterpret_cast<const float4*>(qtil + j * D + c0);
+      *reinterpret_cast<float4*>(kG + j * D + c0) = make_float4(kj.x * P.x, kj.y * P.y, kj.z * P.z, kj.w * P.w);
+      *reinterpret_cast<float4*>(qG + j * D + c0) = make_float4(qj.x * P.x, qj.y * P.y, qj.z * P.z, qj.w * P.w);
+      if (j == Q - 1) *reinterpret_cast<float4*>(eGQ + c0) = P;
+      float4 r = kj;
+      float dsum[QW], csum[QW];
+#pragma unroll
+      for (int t = 0; t < QW; ++t) {
+        dsum[t] = 0.f;
+        csum[t] = 0.f;
+        if (t >= j && t < Q) {
+          if (t > j) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dec + t * D + c0);
+            r = make_float4(r.x * d4.x, r.y * d4.y, r.z * d4.z, r.w * d4.w);
+          }
+          const float4 qt = *reinterpret_cast<const float4*>(qtil + t * D + c0);
+          const float4 kt = *reinterpret_cast<const float4*>(khat + t * D + c0);
+          dsum[t] = r.x * qt.x + r.y * qt.y + r.z * qt.z + r.w * qt.w;
+          csum[t] = r.x * kt.x + r.y * kt.y + r.z * kt.z + r.w * kt.w;
+        }
+      }
+      *reinterpret_cast<float4*>(wv + j * D + c0) = r;
+      // reduce-scatter of the 8 sums over the warp (halving by lane bits
+      // 4, 3, 2, then bits 1 and 0 summed): lanes with bits 1..0 clear end
+      // with entry 4 b4 + 2 b3 + b2 of (d_0..d_3, c_0..c_3)
+      float y[8] = {dsum[0], dsum[1], dsum[2], dsum[3], csum[0], csum[1], csum[2], csum[3]};
+#pragma unroll
+      for (int lvl = 0; lvl < 3; ++lvl) {
+        const int m = 16 >> lvl, n = 4 >> lvl;
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q < n) {
+            const float send = up ? y[q] : y[q + n], keep = up ? y[q + n] : y[q];
+            y[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+      }
+      y[0] += __shfl_xor_sync(0xffffffffu, y[0], 2);
+      y[0] += __shfl_xor_sync(0xffffffffu, y[0], 1);
+      if ((lane & 3) == 0) {
+        const int e = 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+        if (e < 4)
+          s.dd[e][j] = y[0];
+        else
+          s.cc[e - 4][j] = y[0];
+      }
+    } else {
+      *reinterpret_cast<float4*>(kG + j * D + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(qG + j * D + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __syncthreads();
+  // (3) probes, keys then queries: this thread's 4 rows x 8 channels
+  // against the 4 vectors; x[4 i + t] = row i . vec_t, reduce-scattered over
+  // the half warp's 16 lanes (halving by lane bits 3, 2, 1, 0) so that lane
+  // (b3 b2 b1 b0) ends with row 2 b3 + b2, token 2 b1 + b0
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const float* vecs = half == 0 ? kG : qG;
+    float x[16];
+#pragma unroll
+    for (int t = 0; t < QW; ++t) {
+      float2 w2[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float4 w4 = *reinterpret_cast<const float4*>(vecs + t * D + win_chan(lane, j));
+        w2[2 * j] = make_float2(w4.x, w4.y);
+        w2[2 * j + 1] = make_float2(w4.z, w4.w);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float2 acc = fmul2(S[i][0], w2[0]);
+#pragma unroll
+        for (int jj = 1; jj < 4; ++jj) acc = ffma2(S[i][jj], w2[jj], acc);
+        x[4 * i + t] = acc.x + acc.y;
+      }
+    }
+#pragma unroll
+    for (int lvl = 0; lvl < 4; ++lvl) {
+      const int m = 8 >> lvl, n = 8 >> lvl;  // lane mask, half of the live entries
+      const bool up = (lane & m) != 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (q < n) {
+          const float send = up ? x[q] : x[q + n], keep = up ? x[q + n] : x[q];
+          x[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+    }
+    const int l = lane & 15;
+    const int i = 2 * ((l >> 3) & 1) + ((l >> 2) & 1), t = 2 * ((l >> 1) & 1) + (l & 1);
+    (half == 0 ? pb : pa)[t * D + win_row(warp, lane, i)] = x[0];
+  }
+  __syncthreads();
+  // (4) thread v < 128: forward substitution for row v, outputs, records
+  if (tid < D) {
+    const int v = tid;
+    float u[QW];
+#pragma unroll
+    for (int t = 0; t < QW; ++t) {
+      u[t] = 0.f;
+      if (t < Q) {
+        float acc = act_f<FP16>(ibuf[t * 4 * D + 2 * D + v]) - pb[t * D + v];
+#pragma unroll
+        for (int j = 0; j < t; ++j) acc -= s.cc[t][j] * u[j];
+        u[t] = s.tbeta[t] * acc;
+        float o = pa[t * D + v];
+#pragma unroll
+        for (int j = 0; j <= t; ++j) o += s.dd[t][j] * u[j];
+        p.out[((int64_t)(it.qs + t) * p.hv + h) * D + v] = act_from_f(o, FP16);
+        if (VERIFY) p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + v] = u[t];
+        U[t * D + v] = u[t];
+      }
+    }
+  }
+  if (!VERIFY) {
+    __syncthreads();
+    // (5) S = P_{Q-1} * S0 + sum_t r_{t,Q-1} U_t^T
+    float2 e2[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float4 e4 = *reinterpret_cast<const float4*>(eGQ + win_chan(lane, j));
+      e2[2 * j] = make_float2(e4.x, e4.y);
+      e2[2 * j + 1] = make_float2(e4.z, e4.w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) S[i][jj] = fmul2(S[i][jj], e2[jj]);
+#pragma unroll
+    for (int t = 0; t < QW; ++t) {
+      if (t < Q) {
+        float2 w2[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wv + t * D + win_chan(lane, j));
+          w2[2 * j] = make_float2(w4.x, w4.y);
+          w2[2 * j + 1] = make_float2(w4.z, w4.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float ut = U[t * D + win_row(warp, lane, i)];
+          const float2 uu = make_float2(ut, ut);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) S[i][jj] = ffma2(w2[jj], uu, S[i][jj]);
+        }
+      }
+    }
+  }
+}
+
 template <bool VERIFY, bool SBF16, bool FP16>
 __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const WindowParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -427,6 +647,10 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
     if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
     bool ok = true;
     const bool conv = VERIFY && !FP16 && p.conv.state != nullptr;  // conv: bf16 activations only
+    // verify of 2..4 tokens on an fp32 state: the windowed solve (measured
+    // faster than the token loop there; for decode, whose rank-Q update and
+    // write-back follow, the token loop measured faster)
+    const bool windowed = VERIFY && !SBF16 && it.qlen >= 2 && it.qlen <= 4;
     float2 S[4][4];
     float yc[3][4];  // conv outputs of token ``warp`` (verify with a conv)
     if (it.work) {
@@ -438,7 +662,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
         if (warp < it.qlen) {
           if (conv)
             conv_token(p, it, s.in[b], warp, lane, yc);
-          else
+          else if (!windowed)
             token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
         }
 #pragma unroll
@@ -475,7 +699,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
               make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
         }
         __syncwarp();
-        token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        if (!windowed) token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
       }
       __syncthreads();
     }
@@ -485,7 +709,10 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
     // the next item's scalars, used a step from now
     const TokenScalars ts_next = load_token_scalars(p, itn, warp, lane);
     if (it.work) {
-      run_tokens<VERIFY, SBF16, FP16>(p, s, it, S, s.in[b], warp, lane);
+      if (windowed)
+        window_solve<VERIFY, FP16>(p, s, it, S, s.in[b], ts, tid, warp, lane);
+      else
+        run_tokens<VERIFY, SBF16, FP16>(p, s, it, S, s.in[b], warp, lane);
       if (!VERIFY) {
         // the previous item's bulk store has read sout by now (a whole item
         // ago); confirm it before anyone overwrites sout

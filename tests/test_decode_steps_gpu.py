@@ -60,7 +60,9 @@ def test_slot_table_small():
 
 def test_slot_table_without_counts_and_repeated_rows():
     """No counts: start from column 0.  A row repeated across columns ends
-    with the later token's state; all columns on one slot equal kda_decode."""
+    with the later token's state; all columns on one slot give kda_decode's
+    result (within tolerance: the slot table runs token by token, the
+    in-place decode of a 2..4-token window runs the windowed solve)."""
     import linear_attention_serving_fwd_gb300 as kda
     x = W.decode_batch(6, 4, 2, 2, slots=30, seed=22, qlens=[4, 4, 2, 3, 1, 4], lower_bound=-0.6)
     table, _ = W.decode_slot_table(6, 4, 30, seed=22)
@@ -76,7 +78,14 @@ def test_slot_table_without_counts_and_repeated_rows():
     out_d = kda.kda_decode(xd.q, xd.k, xd.v, xd.g, xd.beta, pool_d, xd.cu_seqlens, xd.state_indices,
                            x.window, A_log=xd.A_log, dt_bias=xd.dt_bias, lower_bound=x.lower_bound)
     torch.cuda.synchronize()
-    assert torch.equal(out_s, out_d) and torch.equal(pool_s, pool_d)
+    ref_d = oracle.window(x)
+    check_out(out_s, ref_d["out"], "slot table, one slot per request")
+    check_out(out_d, ref_d["out"], "kda_decode")
+    live = x.state_indices.tolist()
+    check_state(pool_s[live], ref_d["pool"][live], "slot table rows")
+    check_state(pool_d[live], ref_d["pool"][live], "kda_decode rows")
+    assert torch.equal(pool_s[[r for r in range(30) if r not in live]],
+                       pool_d[[r for r in range(30) if r not in live]])
     assert kda.kda_device_status(clear=True) == 0
 
 
