@@ -146,7 +146,7 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 // --------------------------------------------------------------------------
 constexpr int PRO_THREADS = 512;
 constexpr int LDT = 68;  // row stride (floats) of the 64 x 64 fp32 matrices (16-byte rows)
-constexpr int LDW = 33;  // row stride of the 32 x 32 fp32 temporary
+constexpr int LDW = 34;  // row stride of the 32 x 32 fp32 temporary (8-byte column pairs)
 constexpr int YROWS = 160;  // rows of the stacked Y operand
 
 // first row of Y_R in the stacked operand = its first TMEM accumulator column
@@ -590,69 +590,81 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       for (int i = 0; i < 16; ++i) Li[(b0 + i) * LDT + b0 + jc] = x[i];
     }
     __syncthreads();
-    {
-      // 16-row pairs (a, b) = (2P, 2P + 1): W = A_ba L^{-1}_aa
-      const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
+    // 16-row pairs (a, b) = (2P, 2P + 1): thread (P, row i, column pair jp)
+    // of the first 256 threads computes two entries
+    if (tid < 256) {
+      // W = A_ba L^{-1}_aa
+      const int P = tid >> 7, i = (tid >> 3) & 15, j0 = 2 * (tid & 7);
       const int a0 = 32 * P, b0 = 32 * P + 16;
-      float s0 = 0.f, s1 = 0.f;
+      float2 r = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 16; m += 2) {
-        s0 += Af[(b0 + i) * LDT + a0 + m] * Li[(a0 + m) * LDT + a0 + jc];
-        s1 += Af[(b0 + i) * LDT + a0 + m + 1] * Li[(a0 + m + 1) * LDT + a0 + jc];
+      for (int m = 0; m < 16; m += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(&Af[(b0 + i) * LDT + a0 + m]);
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          r = ffma2(make_float2(xs[u], xs[u]), *reinterpret_cast<const float2*>(&Li[(a0 + m + u) * LDT + a0 + j0]), r);
       }
-      Wt[(16 * P + i) * LDW + jc] = s0 + s1;
+      *reinterpret_cast<float2*>(&Wt[(16 * P + i) * LDW + j0]) = r;
     }
     __syncthreads();
-    {
+    if (tid < 256) {
       // L^{-1}_ba = - L^{-1}_bb W
-      const int P = tid >> 8, i = (tid >> 4) & 15, jc = tid & 15;
+      const int P = tid >> 7, i = (tid >> 3) & 15, j0 = 2 * (tid & 7);
       const int a0 = 32 * P, b0 = 32 * P + 16;
-      float s0 = 0.f, s1 = 0.f;
+      float2 r = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 16; m += 2) {
-        s0 += Li[(b0 + i) * LDT + b0 + m] * Wt[(16 * P + m) * LDW + jc];
-        s1 += Li[(b0 + i) * LDT + b0 + m + 1] * Wt[(16 * P + m + 1) * LDW + jc];
+      for (int m = 0; m < 16; m += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(&Li[(b0 + i) * LDT + b0 + m]);
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          r = ffma2(make_float2(xs[u], xs[u]), *reinterpret_cast<const float2*>(&Wt[(16 * P + m + u) * LDW + j0]), r);
       }
-      Li[(b0 + i) * LDT + a0 + jc] = -(s0 + s1);
+      *reinterpret_cast<float2*>(&Li[(b0 + i) * LDT + a0 + j0]) = make_float2(-r.x, -r.y);
     }
     __syncthreads();
-    // 32-row halves: warp = rows (2 warp, 2 warp + 1), lane = column; the
-    // column of the right factor sits in registers, the rows of the left one
-    // are read as 16-byte broadcasts
-    {
+    // 32-row halves: thread (row pair rp, column pair cp) of the first 256
+    // threads computes a 2 x 2 tile; the left factor's rows are 16-byte
+    // broadcasts, the right factor's column pairs 8-byte loads
+    if (tid < 256) {
       // W = A_{[32,64) [0,32)} L^{-1}_{[0,32) [0,32)}
-      float col[32];
-#pragma unroll
-      for (int m = 0; m < 32; ++m) col[m] = Li[m * LDT + lane];
-      const int i0 = 2 * warp;
-      float s0 = 0.f, s1 = 0.f;
+      const int i0 = 2 * (tid >> 4), j0 = 2 * (tid & 15);
+      float2 r0 = make_float2(0.f, 0.f), r1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 32; m += 4) {
         const float4 x = *reinterpret_cast<const float4*>(&Af[(32 + i0) * LDT + m]);
         const float4 z = *reinterpret_cast<const float4*>(&Af[(33 + i0) * LDT + m]);
-        s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
-        s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
+        const float xs[4] = {x.x, x.y, x.z, x.w}, zs[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 c2 = *reinterpret_cast<const float2*>(&Li[(m + u) * LDT + j0]);
+          r0 = ffma2(make_float2(xs[u], xs[u]), c2, r0);
+          r1 = ffma2(make_float2(zs[u], zs[u]), c2, r1);
+        }
       }
-      Wt[i0 * LDW + lane] = s0;
-      Wt[(i0 + 1) * LDW + lane] = s1;
+      *reinterpret_cast<float2*>(&Wt[i0 * LDW + j0]) = r0;
+      *reinterpret_cast<float2*>(&Wt[(i0 + 1) * LDW + j0]) = r1;
     }
     __syncthreads();
-    {
+    if (tid < 256) {
       // L^{-1}_{[32,64) [0,32)} = - L^{-1}_{[32,64) [32,64)} W
-      float col[32];
-#pragma unroll
-      for (int m = 0; m < 32; ++m) col[m] = Wt[m * LDW + lane];
-      const int i0 = 2 * warp;
-      float s0 = 0.f, s1 = 0.f;
+      const int i0 = 2 * (tid >> 4), j0 = 2 * (tid & 15);
+      float2 r0 = make_float2(0.f, 0.f), r1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 32; m += 4) {
         const float4 x = *reinterpret_cast<const float4*>(&Li[(32 + i0) * LDT + 32 + m]);
         const float4 z = *reinterpret_cast<const float4*>(&Li[(33 + i0) * LDT + 32 + m]);
-        s0 = fmaf(x.x, col[m], fmaf(x.y, col[m + 1], fmaf(x.z, col[m + 2], fmaf(x.w, col[m + 3], s0))));
-        s1 = fmaf(z.x, col[m], fmaf(z.y, col[m + 1], fmaf(z.z, col[m + 2], fmaf(z.w, col[m + 3], s1))));
+        const float xs[4] = {x.x, x.y, x.z, x.w}, zs[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 c2 = *reinterpret_cast<const float2*>(&Wt[(m + u) * LDW + j0]);
+          r0 = ffma2(make_float2(xs[u], xs[u]), c2, r0);
+          r1 = ffma2(make_float2(zs[u], zs[u]), c2, r1);
+        }
       }
-      Li[(32 + i0) * LDT + lane] = -s0;
-      Li[(33 + i0) * LDT + lane] = -s1;
+      *reinterpret_cast<float2*>(&Li[(32 + i0) * LDT + j0]) = make_float2(-r0.x, -r0.y);
+      *reinterpret_cast<float2*>(&Li[(33 + i0) * LDT + j0]) = make_float2(-r1.x, -r1.y);
     }
     __syncthreads();
 
