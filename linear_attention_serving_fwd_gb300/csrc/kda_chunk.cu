@@ -174,9 +174,9 @@ struct __align__(1024) ProSmem {
   unsigned char KG[16384];  // fp16 kg^T, K-major [k][r]
   unsigned char VT[16384];  // fp16 v^T, K-major [v][r] (K groups 2048 bytes apart)
   float ref[4][128];        // m_R = Lam at row 16R + 7
-  float qtot[4][128];       // gate sum of each sub-chunk
-  float ssk[4][64];         // |k_r|^2 partial per group of 32 channels
-  float ssq[4][64];
+  float qtot[8][128];       // gate sum of each 8-row half sub-chunk
+  float ssk[2][64];         // |k_r|^2 partial per group of 64 channels
+  float ssq[2][64];
   float lamc[128];          // Lam at row 63
   float rk[64], rq[64];     // 1/|k_r| and scale/|q_r|
   float beta[64];
@@ -285,14 +285,15 @@ __device__ __forceinline__ void conv_tiles(const ChunkParams& p, __nv_bfloat16* 
 // and A_log: loaded early, consumed at the item's start.
 struct ItemScalars {
   __nv_bfloat16 beta;
-  float dt, alog;
+  float2 dt;  // dt_bias of the thread's channel pair 2 (tid % 64), + 1
+  float alog;
 };
 __device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m, int tid) {
   ItemScalars r;
   const int h = m.y, bos = m.z, len = m.w;
   r.beta = (tid < 64 && tid < len) ? p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh]
                                    : __float2bfloat16(0.f);
-  r.dt = p.has_gate ? p.dt_bias[h * D + (tid & 127)] : 0.f;
+  r.dt = p.has_gate ? *reinterpret_cast<const float2*>(p.dt_bias + h * D + 2 * (tid & 63)) : make_float2(0.f, 0.f);
   r.alog = p.has_gate ? p.A_log[h] : 0.f;
   return r;
 }
@@ -330,7 +331,6 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     const int4 meta = s.meta[cur];
     const int c_glob = meta.x, h = meta.y, len = meta.w;
     const float a_h = p.has_gate ? __expf(sc.alog) : 0.f;
-    const float dt = sc.dt;
     if (tid < 64) s.beta[tid] = tid < len ? sigmoidf_(act_f<FP16>(sc.beta)) : 0.f;
     unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
     // ---- phase 0: this item's tiles (issued during the previous item) -------
@@ -339,132 +339,145 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     __syncthreads();
     if constexpr (CONV) conv_tiles(p, tiles, c_glob, h, tid);
 
-    // ---- phase 1: channel-owner, thread = (channel c, sub-chunk Rq) ----------
-    const int c = tid & 127, Rq = tid >> 7;
-    float lam[16], kv[16], qv[16];
+    // ---- phase 1: thread = (channel pair: channels c, c + 1 with c = 2 cp;
+    // rows 8 hs .. 8 hs + 7, half hh of sub-chunk Rq = hs / 2) ------------------
+    const int cp = tid & 63, hs = tid >> 6, Rq = hs >> 1, hh = hs & 1;
+    const int c = 2 * cp;
+    float2 lam[8], kv[8], qv[8];  // per row, the two channels
     {
-      float acc = 0.f;
-      uint32_t vw[8];  // v column c as packed fp16 pairs (rows 2i, 2i+1)
-      const float2 ah2 = make_float2(a_h, a_h), adt2 = make_float2(a_h * dt, a_h * dt);
-      // rows in pairs; rows at or past ``len`` belong to the next sequence
+      float2 acc = make_float2(0.f, 0.f);
+      uint32_t vw[2][4];  // v of channels c and c + 1 as fp16 pairs along rows
+      const float2 ah2 = make_float2(a_h, a_h), adt2 = make_float2(a_h * sc.dt.x, a_h * sc.dt.y);
+      const float2 zero2 = make_float2(0.f, 0.f);
+      // rows at or past ``len`` belong to the next sequence
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const int r = 16 * Rq + i;
-        const bool in0 = r < len, in1 = r + 1 < len;
-        qv[i] = in0 ? act_f<FP16>(tiles[tile_row(0, r) + c]) : 0.f;
-        qv[i + 1] = in1 ? act_f<FP16>(tiles[tile_row(0, r + 1) + c]) : 0.f;
-        kv[i] = in0 ? act_f<FP16>(tiles[tile_row(1, r) + c]) : 0.f;
-        kv[i + 1] = in1 ? act_f<FP16>(tiles[tile_row(1, r + 1) + c]) : 0.f;
-        float2 g = make_float2(in0 ? act_f<FP16>(tiles[g_row(r) + c]) : 0.f,
-                               in1 ? act_f<FP16>(tiles[g_row(r + 1) + c]) : 0.f);
-        if (p.has_gate) {  // lower_bound * sigmoid(a (g + dt_bias)), in pairs
-          const float2 t = ffma2(ah2, g, adt2);
-          const float2 den = fadd2(make_float2(__expf(-t.x), __expf(-t.y)), make_float2(1.f, 1.f));
-          g = make_float2(in0 ? __fdividef(p.lower_bound, den.x) : 0.f,
-                          in1 ? __fdividef(p.lower_bound, den.y) : 0.f);
+      for (int i = 0; i < 8; i += 2) {
+        float2 vv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = 8 * hs + i + e;
+          const bool in = r < len;
+          qv[i + e] = in ? act_f2<FP16>(tiles + tile_row(0, r) + c) : zero2;
+          kv[i + e] = in ? act_f2<FP16>(tiles + tile_row(1, r) + c) : zero2;
+          float2 g = in ? act_f2<FP16>(tiles + g_row(r) + c) : zero2;
+          if (p.has_gate) {  // lower_bound * sigmoid(a (g + dt_bias)), both channels
+            const float2 t = ffma2(ah2, g, adt2);
+            const float2 den = fadd2(make_float2(__expf(-t.x), __expf(-t.y)), make_float2(1.f, 1.f));
+            g = in ? make_float2(__fdividef(p.lower_bound, den.x), __fdividef(p.lower_bound, den.y)) : zero2;
+          }
+          acc = fadd2(acc, g);
+          lam[i + e] = acc;
+          vv[e] = in ? act_f2<FP16>(tiles + tile_row(2, r) + c) : zero2;
         }
-        acc += g.x;
-        lam[i] = acc;
-        acc += g.y;
-        lam[i + 1] = acc;
-        vw[i >> 1] = pack_half2(in0 ? act_f<FP16>(tiles[tile_row(2, r) + c]) : 0.f,
-                                in1 ? act_f<FP16>(tiles[tile_row(2, r + 1) + c]) : 0.f);
+        vw[0][i >> 1] = pack_half2(vv[0].x, vv[1].x);
+        vw[1][i >> 1] = pack_half2(vv[0].y, vv[1].y);
       }
-      // v^T of this column: the record's block c / 32, and VT for o_intra
+      // v^T of the two channels: the record's block c / 32, and VT for o_intra
 #pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8) {
-        const uint4 v4 = make_uint4(vw[4 * g8], vw[4 * g8 + 1], vw[4 * g8 + 2], vw[4 * g8 + 3]);
-        *reinterpret_cast<uint4*>(wsb + CH_V16 + (c >> 5) * VB_BYTES +
-                                  tc::kmajor_offset_lbo(c & 31, 16 * Rq + 8 * g8, VB_LBO)) = v4;
-        *reinterpret_cast<uint4*>(s.VT + tc::kmajor_offset(c, 16 * Rq + 8 * g8, 128)) = v4;
+      for (int e = 0; e < 2; ++e) {
+        const int ch = c + e;
+        const uint4 v4 = make_uint4(vw[e][0], vw[e][1], vw[e][2], vw[e][3]);
+        *reinterpret_cast<uint4*>(wsb + CH_V16 + (ch >> 5) * VB_BYTES +
+                                  tc::kmajor_offset_lbo(ch & 31, 8 * hs, VB_LBO)) = v4;
+        *reinterpret_cast<uint4*>(s.VT + tc::kmajor_offset(ch, 8 * hs, 128)) = v4;
       }
-      s.qtot[Rq][c] = acc;
-      // row norms: reduce-scatter the 16 per-row partials over the warp's 32
-      // channels (row = lane % 16), then the four channel groups meet in smem
-      float pk[16], pq[16];
+      *reinterpret_cast<float2*>(&s.qtot[hs][c]) = acc;
+      // row norms: the 8 per-row partials reduce-scatter over the warp's 64
+      // channels (halving by lane bits 4, 3, 2; bits 1, 0 summed): lanes with
+      // bits 1..0 clear hold row 4 b4 + 2 b3 + b2; the two channel halves
+      // meet in shared memory
+      float pk[8], pq[8];
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const float2 k2 = make_float2(kv[i], kv[i + 1]), q2 = make_float2(qv[i], qv[i + 1]);
-        const float2 kk = fmul2(k2, k2), qq = fmul2(q2, q2);
-        pk[i] = kk.x; pk[i + 1] = kk.y;
-        pq[i] = qq.x; pq[i + 1] = qq.y;
+      for (int i = 0; i < 8; ++i) {
+        pk[i] = kv[i].x * kv[i].x + kv[i].y * kv[i].y;
+        pq[i] = qv[i].x * qv[i].x + qv[i].y * qv[i].y;
       }
 #pragma unroll
-      for (int sh = 8; sh >= 1; sh >>= 1) {
-        const bool up = (lane & sh) != 0;
+      for (int lvl = 0; lvl < 3; ++lvl) {
+        const int m = 16 >> lvl, n = 4 >> lvl;
+        const bool up = (lane & m) != 0;
 #pragma unroll
-        for (int m = 0; m < sh; ++m) {
-          const float sk = up ? pk[m] : pk[m + sh], kk = up ? pk[m + sh] : pk[m];
-          const float sq = up ? pq[m] : pq[m + sh], qq = up ? pq[m + sh] : pq[m];
-          pk[m] = kk + __shfl_xor_sync(0xffffffffu, sk, sh);
-          pq[m] = qq + __shfl_xor_sync(0xffffffffu, sq, sh);
+        for (int q = 0; q < 4; ++q) {
+          if (q < n) {
+            const float sk = up ? pk[q] : pk[q + n], kk = up ? pk[q + n] : pk[q];
+            const float sq = up ? pq[q] : pq[q + n], qq = up ? pq[q + n] : pq[q];
+            pk[q] = kk + __shfl_xor_sync(0xffffffffu, sk, m);
+            pq[q] = qq + __shfl_xor_sync(0xffffffffu, sq, m);
+          }
         }
       }
-      pk[0] += __shfl_xor_sync(0xffffffffu, pk[0], 16);
-      pq[0] += __shfl_xor_sync(0xffffffffu, pq[0], 16);
-      if (lane < 16) {
-        s.ssk[c >> 5][16 * Rq + lane] = pk[0];
-        s.ssq[c >> 5][16 * Rq + lane] = pq[0];
+#pragma unroll
+      for (int m = 2; m >= 1; m >>= 1) {
+        pk[0] += __shfl_xor_sync(0xffffffffu, pk[0], m);
+        pq[0] += __shfl_xor_sync(0xffffffffu, pq[0], m);
+      }
+      if ((lane & 3) == 0) {
+        const int row = 8 * hs + 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+        s.ssk[cp >> 5][row] = pk[0];
+        s.ssq[cp >> 5][row] = pq[0];
       }
     }
     __syncthreads();
-    float mR;  // Lam at row 16 Rq + 7
+    float2 mR;  // Lam at row 16 Rq + 7, the sub-chunk's reference
     {
-      float off = 0.f;
-      for (int R2 = 0; R2 < Rq; ++R2) off += s.qtot[R2][c];
+      float2 off = make_float2(0.f, 0.f);
+      for (int h2 = 0; h2 < hs; ++h2) off = fadd2(off, *reinterpret_cast<const float2*>(&s.qtot[h2][c]));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) lam[i] += off;
-      mR = lam[7];
-      s.ref[Rq][c] = mR;
-      if (Rq == 3) {
-        s.lamc[c] = lam[15];
-        reinterpret_cast<float*>(wsb + CH_D)[c] = __expf(lam[15]);
+      for (int i = 0; i < 8; ++i) lam[i] = fadd2(lam[i], off);
+      // the first half holds row 16 Rq + 7 itself; the second half starts after it
+      mR = hh == 0 ? lam[7] : off;
+      if (hh == 0) *reinterpret_cast<float2*>(&s.ref[Rq][c]) = mR;
+      if (hs == 7) {
+        *reinterpret_cast<float2*>(&s.lamc[c]) = lam[7];
+        *reinterpret_cast<float2*>(wsb + CH_D + 4 * c) = make_float2(__expf(lam[7].x), __expf(lam[7].y));
       }
       if (tid < 64) {
-        const float sk = s.ssk[0][tid] + s.ssk[1][tid] + s.ssk[2][tid] + s.ssk[3][tid];
-        const float sq = s.ssq[0][tid] + s.ssq[1][tid] + s.ssq[2][tid] + s.ssq[3][tid];
+        const float sk = s.ssk[0][tid] + s.ssk[1][tid];
+        const float sq = s.ssq[0][tid] + s.ssq[1][tid];
         s.rk[tid] = rsqrtf(sk + 1e-6f);
         s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
       }
     }
     __syncthreads();
     {
-      const float lamC = s.lamc[c];
-      float F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
+      const float2 lamC = *reinterpret_cast<const float2*>(&s.lamc[c]);
+      float2 F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
 #pragma unroll
-      for (int R2 = 0; R2 < 4; ++R2) F[R2] = R2 > Rq ? __expf(s.ref[R2][c] - mR) : 1.f;
-      // normalised keys and queries (the row norms are the warp's: 16-byte
-      // broadcasts)
-#pragma unroll
-      for (int i4 = 0; i4 < 16; i4 += 4) {
-        const float4 r4 = *reinterpret_cast<const float4*>(&s.rk[16 * Rq + i4]);
-        const float4 q4 = *reinterpret_cast<const float4*>(&s.rq[16 * Rq + i4]);
-        kv[i4] *= r4.x; kv[i4 + 1] *= r4.y; kv[i4 + 2] *= r4.z; kv[i4 + 3] *= r4.w;
-        qv[i4] *= q4.x; qv[i4 + 1] *= q4.y; qv[i4 + 2] *= q4.z; qv[i4 + 3] *= q4.w;
+      for (int R2 = 0; R2 < 4; ++R2) {
+        const float2 m2 = *reinterpret_cast<const float2*>(&s.ref[R2][c]);
+        F[R2] = R2 > Rq ? make_float2(__expf(m2.x - mR.x), __expf(m2.y - mR.y)) : make_float2(1.f, 1.f);
       }
-      // X and Y first (rows in pairs, packed fp32x2 products): the A_kk /
-      // A_qk product starts on them while the B3 / KG operands are built
+      // normalised keys and queries (the row norms: 16-byte broadcasts)
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const int r = 16 * Rq + i;
+      for (int i4 = 0; i4 < 8; i4 += 4) {
+        const float4 r4 = *reinterpret_cast<const float4*>(&s.rk[8 * hs + i4]);
+        const float4 q4 = *reinterpret_cast<const float4*>(&s.rq[8 * hs + i4]);
+        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          kv[i4 + u] = fmul2(kv[i4 + u], make_float2(rr[u], rr[u]));
+          qv[i4 + u] = fmul2(qv[i4 + u], make_float2(qq[u], qq[u]));
+        }
+      }
+      // X and Y first (8-byte pairs of tf32 along the channels): the A_kk /
+      // A_qk product starts on them while the B3 / KG operands are built
+      auto tf32x2 = [](float2 v) {
+        return make_uint2(__float_as_uint(tc::to_tf32_int(v.x)), __float_as_uint(tc::to_tf32_int(v.y)));
+      };
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = 8 * hs + i;
         // e^{Lam - m} and e^{m - Lam}, both within e^{+-84}
-        const float2 E = make_float2(__expf(lam[i] - mR), __expf(lam[i + 1] - mR));
-        const float2 iE = make_float2(__expf(mR - lam[i]), __expf(mR - lam[i + 1]));
-        const float2 kh = make_float2(kv[i], kv[i + 1]), qh = make_float2(qv[i], qv[i + 1]);
-        const float2 xk = fmul2(kh, E), xq = fmul2(qh, E), y = fmul2(kh, iE);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r, c, 128)) = tc::to_tf32_int(xk.x);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(r + 1, c, 128)) = tc::to_tf32_int(xk.y);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tc::to_tf32_int(xq.x);
-        *reinterpret_cast<float*>(s.XY + tc::sw128_offset32(65 + r, c, 128)) = tc::to_tf32_int(xq.y);
+        const float2 E = make_float2(__expf(lam[i].x - mR.x), __expf(lam[i].y - mR.y));
+        const float2 iE = make_float2(__expf(mR.x - lam[i].x), __expf(mR.y - lam[i].y));
+        const float2 xk = fmul2(kv[i], E), xq = fmul2(qv[i], E), y = fmul2(kv[i], iE);
+        *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(r, c, 128)) = tf32x2(xk);
+        *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tf32x2(xq);
 #pragma unroll
         for (int R2 = 0; R2 < 4; ++R2)
-          if (R2 >= Rq) {
-            const float2 yf = fmul2(y, make_float2(F[R2], F[R2]));
-            *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
-                tc::to_tf32_int(yf.x);
-            *reinterpret_cast<float*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r + 1, c, YROWS)) =
-                tc::to_tf32_int(yf.y);
-          }
+          if (R2 >= Rq)
+            *reinterpret_cast<uint2*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
+                tf32x2(fmul2(y, F[R2]));
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -478,27 +491,35 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
       // meanwhile: Kg = k^ e^{Lam}, qg = q~ e^{Lam}, kg = k^ e^{Lam_C - Lam}
       // (each factor at most 1: an underflow only drops a term below e^{-87})
-      uint32_t kgw[8], Kgx[8], qgx[8];  // packed fp16 pairs along rows
+      uint32_t Kgx[2][4], qgx[2][4], kgw[2][4];  // per channel, fp16 pairs along rows
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const float2 eL = make_float2(__expf(lam[i]), __expf(lam[i + 1]));
-        const float2 eC = make_float2(__expf(lamC - lam[i]), __expf(lamC - lam[i + 1]));
-        const float2 kh = make_float2(kv[i], kv[i + 1]), qh = make_float2(qv[i], qv[i + 1]);
-        const float2 Kg2 = fmul2(kh, eL), qg2 = fmul2(qh, eL), kg2 = fmul2(kh, eC);
-        kgw[i >> 1] = pack_half2(kg2.x, kg2.y);
-        Kgx[i >> 1] = pack_half2(Kg2.x, Kg2.y);
-        qgx[i >> 1] = pack_half2(qg2.x, qg2.y);
+      for (int i = 0; i < 8; i += 2) {
+        float2 Kg2[2], qg2[2], kg2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float2 eL = make_float2(__expf(lam[i + e].x), __expf(lam[i + e].y));
+          const float2 eC = make_float2(__expf(lamC.x - lam[i + e].x), __expf(lamC.y - lam[i + e].y));
+          Kg2[e] = fmul2(kv[i + e], eL);
+          qg2[e] = fmul2(qv[i + e], eL);
+          kg2[e] = fmul2(kv[i + e], eC);
+        }
+        Kgx[0][i >> 1] = pack_half2(Kg2[0].x, Kg2[1].x);
+        Kgx[1][i >> 1] = pack_half2(Kg2[0].y, Kg2[1].y);
+        qgx[0][i >> 1] = pack_half2(qg2[0].x, qg2[1].x);
+        qgx[1][i >> 1] = pack_half2(qg2[0].y, qg2[1].y);
+        kgw[0][i >> 1] = pack_half2(kg2[0].x, kg2[1].x);
+        kgw[1][i >> 1] = pack_half2(kg2[0].y, kg2[1].y);
       }
       // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KG [k = c][K = r]
 #pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8) {
-        const int r0 = 16 * Rq + 8 * g8;
-        *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, r0, 128)) =
-            make_uint4(Kgx[4 * g8], Kgx[4 * g8 + 1], Kgx[4 * g8 + 2], Kgx[4 * g8 + 3]);
-        *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(c, 64 + r0, 128)) =
-            make_uint4(qgx[4 * g8], qgx[4 * g8 + 1], qgx[4 * g8 + 2], qgx[4 * g8 + 3]);
-        *reinterpret_cast<uint4*>(s.KG + tc::kmajor_offset(c, r0, 128)) =
-            make_uint4(kgw[4 * g8], kgw[4 * g8 + 1], kgw[4 * g8 + 2], kgw[4 * g8 + 3]);
+      for (int e = 0; e < 2; ++e) {
+        const int ch = c + e, r0 = 8 * hs;
+        *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(ch, r0, 128)) =
+            make_uint4(Kgx[e][0], Kgx[e][1], Kgx[e][2], Kgx[e][3]);
+        *reinterpret_cast<uint4*>(s.B3 + tc::kmajor_offset(ch, 64 + r0, 128)) =
+            make_uint4(qgx[e][0], qgx[e][1], qgx[e][2], qgx[e][3]);
+        *reinterpret_cast<uint4*>(s.KG + tc::kmajor_offset(ch, r0, 128)) =
+            make_uint4(kgw[e][0], kgw[e][1], kgw[e][2], kgw[e][3]);
       }
       fence_proxy_async_smem();
     }

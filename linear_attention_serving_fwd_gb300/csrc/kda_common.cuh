@@ -76,6 +76,17 @@ __device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float out[4]
   float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
   out[0] = fa.x; out[1] = fa.y; out[2] = fb.x; out[3] = fb.y;
 }
+// Two consecutive activations (4 bytes, 4-byte aligned) to fp32.
+template <bool FP16>
+__device__ __forceinline__ float2 act_f2(const __nv_bfloat16* p) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+  if constexpr (FP16) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  } else {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  }
+}
+
 // Four consecutive activations (8 bytes, 8-byte aligned) to fp32.
 template <bool FP16>
 __device__ __forceinline__ void load_act4(const __nv_bfloat16* p, float out[4]) {
