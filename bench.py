@@ -14,8 +14,8 @@ Multi-GPU (torchrun): one replica per rank, no collective in the data path
 ("weak" scaling); a barrier brackets the timed region and the slowest rank's
 time is used.
 
-``--impl reference`` times the fp64 CPU oracle on a bounded sample per step
-on this host's cores (rank 0 only) and prints the same keys.
+``--impl reference`` times the fp64 CPU oracle on the whole dense workload
+per step on this host's cores (rank 0 only) and prints the same keys.
 """
 from __future__ import annotations
 
@@ -250,7 +250,7 @@ def run_ours(args, rank, world, barrier, reduce_max):
     secs = reduce_max(secs)
     ms_per_step = secs / args.steps * 1e3
     tokens = n * w["T"] * world
-    value = tokens * args.steps / secs
+    value = weak_scaling_value(n * w["T"], args.steps, world, secs)
     th = n * w["T"] * w["hv"]
     tflops = th * flop_per_token_head() * args.steps * world / secs / 1e12
 
@@ -660,6 +660,35 @@ def run_reference(args):
     }
 
 
+def collectives(world, backend="nccl"):
+    """The job's (barrier, reduce_max) over its ``world`` ranks: the barrier
+    that brackets the timed region and the slowest rank's seconds.  One rank:
+    no-ops.  The process group (nccl on GPUs; gloo for the CPU tests) is
+    created here if the launcher has not made one."""
+    if world <= 1:
+        return (lambda: None), (lambda s: s)
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend)
+    dev = "cuda" if backend == "nccl" else "cpu"
+
+    def barrier():
+        dist.barrier()
+
+    def reduce_max(s):
+        t = torch.tensor([s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return barrier, reduce_max
+
+
+def weak_scaling_value(units_per_rank, steps, world, max_seconds):
+    """Whole-job throughput of ``world`` replicas that each processed
+    ``units_per_rank`` per step for ``steps`` steps, timed by the slowest."""
+    return units_per_rank * world * steps / max_seconds
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -669,20 +698,9 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     import torch
-    barrier = lambda: None
-    reduce_max = lambda s: s
     if world > 1:
-        import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-        dist.init_process_group("nccl")
-
-        def barrier():
-            dist.barrier()
-
-        def reduce_max(s):
-            t = torch.tensor([s], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
+    barrier, reduce_max = collectives(world, "nccl")
     line = run_ours(args, rank, world, barrier, reduce_max)
     if rank == 0:
         print(json.dumps(line), flush=True)
