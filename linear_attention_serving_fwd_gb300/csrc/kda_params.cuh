@@ -17,6 +17,8 @@ struct ConvParams {
   const int32_t* idx;          // prefill: [N] state row per sequence (< 0: zero history, no update)
   const uint8_t* has_init;     // prefill: [N] or null (all rows hold a history)
   const int32_t* accepted;     // verify: [n_req]; history at positions accepted-1 .. accepted+1
+  int bulk;                    // verify: token-major state and 16-byte rows: taps and history
+                               // are staged into shared memory by bulk copies with the inputs
 };
 
 struct WindowParams {

@@ -146,12 +146,34 @@ __device__ __forceinline__ void state_st4(void* base, int row, int chan, float4 
   }
 }
 
-// The window's q/k/v/g rows, one bulk copy per lane of the calling warp.
+// Verify with a staged conv: each item's taps (3 bands x 128 channels) and
+// the three history positions of its 3 bands, per input buffer.
+constexpr int CONV_TAPS_BYTES = 3 * 2048;                  // room for fp32 taps
+constexpr int CONV_STAGE_BYTES = CONV_TAPS_BYTES + 9 * 256;  // + bf16 history
+
+// The window's q/k/v/g rows, one bulk copy per lane of the calling warp (and,
+// for a staged conv, the item's taps and history into ``stage``).
 __device__ __forceinline__ void issue_inputs(const WindowParams& p, const ItemInfo& it,
-                                             __nv_bfloat16* ibuf, uint64_t* ibar, int lane) {
+                                             __nv_bfloat16* ibuf, uint64_t* ibar, int lane,
+                                             unsigned char* stage = nullptr) {
   const int hq = it.head / (p.hv / p.hqk);
-  if (lane == 0) mbar_arrive_expect_tx(ibar, it.qlen * 4 * ROW_BYTES);
+  const bool conv = stage != nullptr;
+  const int tap_bytes = D * (p.conv.w_f32 ? 16 : 8);
+  if (lane == 0) mbar_arrive_expect_tx(ibar, it.qlen * 4 * ROW_BYTES + (conv ? 3 * tap_bytes + 9 * 256 : 0));
   __syncwarp();
+  if (conv && lane < 12) {
+    int64_t ch[3];
+    conv_channels(p.hqk, p.hv, it.head, 0, ch);
+    if (lane < 3) {
+      const unsigned char* w = static_cast<const unsigned char*>(p.conv.w) + ch[lane] * (tap_bytes / D);
+      bulk_g2s(stage + lane * 2048, w, tap_bytes, ibar);
+    } else {
+      const int x = (lane - 3) / 3, i = (lane - 3) % 3;
+      const int first = p.conv.accepted[it.request] - 1;
+      const __nv_bfloat16* h = p.conv.state + it.slot * p.conv.row_st + (int64_t)(first + i) * p.conv.pos_st + ch[x];
+      bulk_g2s(stage + CONV_TAPS_BYTES + (x * 3 + i) * 256, h, 256, ibar);
+    }
+  }
   if (lane < 4 * it.qlen) {
     const int t = lane >> 2, which = lane & 3;
     const int64_t tok = it.qs + t;
@@ -227,7 +249,8 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
 // from the window's raw rows and, for the taps before the window, the
 // history at positions accepted-1 .. accepted+1 of the slot's conv row.
 __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo& it,
-                                           const __nv_bfloat16* ibuf, int t, int lane, float y[3][4]) {
+                                           const __nv_bfloat16* ibuf, const unsigned char* stage, int t,
+                                           int lane, float y[3][4]) {
   const ConvParams& cv = p.conv;
   const int first = cv.accepted[it.request] - 1;
   int64_t ch[3];
@@ -241,6 +264,9 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
       const int tt = t - 3 + j;
       if (tt >= 0) {
         load_bf16x4(ibuf + (tt * 4 + x) * D + 4 * lane, win[j]);
+      } else if (cv.bulk) {  // staged history position first + 3 + tt
+        load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + CONV_TAPS_BYTES + (x * 3 + 3 + tt) * 256) +
+                        4 * lane, win[j]);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -248,8 +274,21 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
       }
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      y[x][e] = conv_silu(cv.w_f32, conv_taps(cv, ch[x] + e), win[0][e], win[1][e], win[2][e], win[3][e]);
+    for (int e = 0; e < 4; ++e) {
+      float4 w;
+      if (cv.bulk) {
+        if (cv.w_f32) {
+          w = *reinterpret_cast<const float4*>(stage + x * 2048 + (4 * lane + e) * 16);
+        } else {
+          float t4[4];
+          load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + x * 2048 + (4 * lane + e) * 8), t4);
+          w = make_float4(t4[0], t4[1], t4[2], t4[3]);
+        }
+      } else {
+        w = conv_taps(cv, ch[x] + e);
+      }
+      y[x][e] = conv_silu(cv.w_f32, w, win[0][e], win[1][e], win[2][e], win[3][e]);
+    }
   }
 }
 
@@ -595,6 +634,13 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
   }
 }
 
+// The staging area of input buffer b for a verify with a staged conv (the
+// state write-back buffer, unused by verify), else none.
+__device__ __forceinline__ unsigned char* conv_stage(const WindowParams& p, WinSmem& s, int b) {
+  return (p.conv.state && p.conv.bulk) ? reinterpret_cast<unsigned char*>(s.sout) + b * CONV_STAGE_BYTES : nullptr;
+}
+static_assert(2 * CONV_STAGE_BYTES <= (int)sizeof(float) * D * D, "conv staging fits the write-back buffer");
+
 template <bool VERIFY, bool SBF16, bool FP16>
 __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const WindowParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -632,7 +678,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
         const ItemInfo ii = item_info(p, its[b]);
         if (ii.work) {
           if (lane == 0) issue_state<SBF16>(p, ii, s.state[b], &s.sbar[b]);
-          issue_inputs(p, ii, s.in[b], &s.ibar[b], lane);
+          issue_inputs(p, ii, s.in[b], &s.ibar[b], lane, conv_stage(p, s, b));
         }
       }
     }
@@ -661,7 +707,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       if (ok) {
         if (warp < it.qlen) {
           if (conv)
-            conv_token(p, it, s.in[b], warp, lane, yc);
+            conv_token(p, it, s.in[b], reinterpret_cast<const unsigned char*>(s.sout) + b * CONV_STAGE_BYTES,
+                       warp, lane, yc);
           else if (!windowed)
             token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
         }
@@ -743,7 +790,7 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       bulk_commit();
       stored = true;
     }
-    if (warp == 1 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane);
+    if (warp == 1 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane, conv_stage(p, s, b));
     ts = ts_next;
     cur = nxt;
     nxt = nn;
