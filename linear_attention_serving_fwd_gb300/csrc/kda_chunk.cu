@@ -68,6 +68,23 @@ __device__ __forceinline__ int seq_eos(const ChunkParams& p, int n) {
   return p.cu_seqlens ? p.cu_seqlens[n + 1] : (n + 1) * p.dense_len;
 }
 
+// Chunk tables.  With cu_seqlens they are built on the device by
+// kda_chunk_index_kernel; dense sequences of dense_len tokens have them in
+// closed form (ceil(dense_len / 64) chunks each), and that launch is skipped.
+__device__ __forceinline__ int dense_chunks(const ChunkParams& p) { return (p.dense_len + CHUNK - 1) / CHUNK; }
+__device__ __forceinline__ int num_chunks_of(const ChunkParams& p) {
+  return p.cu_seqlens ? *p.n_chunks : p.n_seqs * dense_chunks(p);
+}
+__device__ __forceinline__ int chunk_off_of(const ChunkParams& p, int n) {
+  return p.cu_seqlens ? p.chunk_off[n] : n * dense_chunks(p);
+}
+__device__ __forceinline__ int chunk_seq_of(const ChunkParams& p, int c) {
+  return p.cu_seqlens ? p.chunk_seq[c] : c / dense_chunks(p);
+}
+__device__ __forceinline__ int chunk_j_of(const ChunkParams& p, int c) {
+  return p.cu_seqlens ? p.chunk_j[c] : c % dense_chunks(p);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -199,8 +216,8 @@ __device__ __forceinline__ int g_row(int r) { return 3 * TILE_QKV + r * D; }
 // item t = chunk * Hv + head
 __device__ __forceinline__ int4 item_meta(const ChunkParams& p, int t) {
   const int c = t / p.hv, h = t - c * p.hv;
-  const int n = p.chunk_seq[c];
-  const int bos = seq_bos(p, n) + p.chunk_j[c] * CHUNK;
+  const int n = chunk_seq_of(p, c);
+  const int bos = seq_bos(p, n) + chunk_j_of(p, c) * CHUNK;
   return make_int4(c, h, bos, min(CHUNK, seq_eos(p, n) - bos));
 }
 
@@ -248,8 +265,8 @@ __device__ __forceinline__ void conv_tiles(const ChunkParams& p, __nv_bfloat16* 
   const int c = tid & 127, Rq = tid >> 7;
   int64_t ch[3];
   conv_channels(p.hqk, p.hv, h, c, ch);
-  if (p.chunk_j[c_glob] == 0 && Rq < 3) {
-    const int n = p.chunk_seq[c_glob];
+  if (chunk_j_of(p, c_glob) == 0 && Rq < 3) {
+    const int n = chunk_seq_of(p, c_glob);
     const int row = cv.idx[n];
     const bool init = row >= 0 && row < cv.rows && (!cv.has_init || cv.has_init[n]);
     const int64_t chx = Rq == 0 ? ch[0] : (Rq == 1 ? ch[1] : ch[2]);
@@ -304,7 +321,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   ProSmem& s = *reinterpret_cast<ProSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = *p.n_chunks * p.hv;
+  const int n_items = num_chunks_of(p) * p.hv;
   if ((int)blockIdx.x >= n_items) return;
   __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.XY + P_TILES);
 
@@ -917,7 +934,7 @@ __device__ __forceinline__ void state_store(const ChunkParams& p, void* base, in
 }
 
 __device__ __forceinline__ void group_range(const ChunkParams& p, int n, int gidx, int& c0, int& c1) {
-  const int base = p.chunk_off[n], nc = p.chunk_off[n + 1] - base;
+  const int base = chunk_off_of(p, n), nc = chunk_off_of(p, n + 1) - base;
   const int per = (nc + p.groups - 1) / p.groups;
   c0 = base + min(nc, gidx * per);
   c1 = base + min(nc, (gidx + 1) * per);
@@ -1019,7 +1036,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         }
       }
     }
-    const int seq_c0 = p.chunk_off[n];
+    const int seq_c0 = chunk_off_of(p, n);
     float dcur = 0.f;
     bool fail = false;
     if (nch > 0) {
@@ -1106,9 +1123,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.o_done[ob]);  // O[ob] and b[ob] read
-      const int c = c0 + it, n_ = p.chunk_seq[c];
-      const int bos = seq_bos(p, n_) + p.chunk_j[c] * CHUNK;
-      const int len = min(CHUNK, seq_eos(p, n_) - bos);
+      // every chunk of this walk belongs to sequence n
+      const int bos = seq_bos(p, n) + (c0 + it - chunk_off_of(p, n)) * CHUNK;
+      const int len = min(CHUNK, seq_eos(p, n) - bos);
       if (lane < 16 && r < len) {
         __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D + col0;
 #pragma unroll
@@ -1323,9 +1340,11 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     p.gB = fw + plane;
     p.gS = fw + 2 * plane;
   }
-  trace_begin("kda_chunk_index", stream);
-  kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
-  trace_end(stream);
+  if (p.cu_seqlens) {  // dense sequences have closed-form chunk tables
+    trace_begin("kda_chunk_index", stream);
+    kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
+    trace_end(stream);
+  }
   TileMaps maps;
   const int qkv_rows = CHUNK + (p.conv.state ? HALO : 0);
   const bool f16 = p.in_fp16 != 0;

@@ -62,8 +62,10 @@ def test_prologue_records_match_chunk_form(T, lb):
     xd = x.to("cuda")
     ws_bytes = kda.chunk_workspace_bytes(1, T, 2, 1)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    # cu_seqlens: the device-built chunk table (dense calls use closed-form tables)
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
     kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, A_log=xd.A_log, dt_bias=xd.dt_bias,
-                      lower_bound=lb, n_seqs=1, output_final_state=True, groups=1, workspace=ws)
+                      lower_bound=lb, cu_seqlens=cu, output_final_state=True, groups=1, workspace=ws)
     torch.cuda.synchronize()
     assert kda.kda_device_status(clear=True) == 0
     raw = ws.cpu().numpy()

@@ -96,11 +96,21 @@ def test_verify_matches_oracle_and_leaves_state(window):
 
 
 def test_verify_equals_decode_outputs_and_padding():
+    """Verify and decode give the same outputs (verify runs the windowed solve
+    for 2..4 tokens, decode the token loop: both within the output tolerance
+    of the oracle, zeros on the padding), and verify leaves the pool as it
+    was."""
     x = W.decode_batch(9, 4, 1, 2, slots=12, seed=5, qlens=[4, 3, 4, 0, 1, 4, 2, 4, 4],
                        null_requests=(4, 7), lower_bound=-0.3)
+    ref = oracle.window(x)
     dec = _run_decode(x)
     ver = _run_decode(x, verify=True)
-    assert torch.equal(dec["out"], ver["out"])
+    check_out(ver["out"], ref["out"], "verify out")
+    check_out(dec["out"], ref["out"], "decode out")
+    cu = x.cu_seqlens.tolist()
+    for b in (4, 7):  # padding: zeros from both
+        assert torch.count_nonzero(ver["out"][cu[b]:cu[b + 1]]) == 0
+        assert torch.count_nonzero(dec["out"][cu[b]:cu[b + 1]]) == 0
     assert torch.equal(ver["pool"].cpu(), x.state_pool)
     _status_clean()
 
