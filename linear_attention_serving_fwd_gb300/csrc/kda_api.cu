@@ -289,8 +289,10 @@ static int check_conv(const kda_conv* conv, const kda_activations* x, bool verif
   cp.idx = conv->state_indices;
   cp.has_init = conv->has_initial_state;
   cp.accepted = conv->num_accepted;
-  cp.bulk = verify && conv->chan_stride == 1 && conv->pos_stride % 8 == 0 && conv->row_stride % 8 == 0 &&
-            aligned16(conv->state);
+  // staged by bulk copies (verify): bf16 taps and a token-major state with
+  // 16-byte aligned rows and positions
+  cp.bulk = verify && !conv->weight_f32 && aligned16(conv->weight) && conv->chan_stride == 1 &&
+            conv->pos_stride % 8 == 0 && conv->row_stride % 8 == 0 && aligned16(conv->state);
   return KDA_OK;
 }
 

@@ -3,27 +3,31 @@
 //
 // Design (memory bound: each (request, head) moves its 64 KB V-first state
 // once in, and for decode once out):
-//  * persistent grid, one CTA per SM, 512 threads = 16 warps;
-//  * two 64 KB state buffers filled by 1-D bulk async copies (TMA engine)
-//    completing on mbarriers, plus two small buffers for the window's
-//    q/k/v/g rows (issued by the lanes of one warp); the state of the item
-//    two ahead streams in while one runs, and the next item's per-token
-//    scalars (beta, A_log, dt_bias) are loaded into registers a step ahead;
-//  * decode writes the new state back through a third 64 KB buffer and two
-//    bulk stores, so no thread waits on its write; with a [request, step]
-//    slot table it reads the row of the last accepted token and also stores
-//    the state after each earlier token of the window, from registers;
+//  * persistent grid; every state and q/k/v/g row arrives by 1-D bulk async
+//    copies (TMA engine) completing on mbarriers, and the next item's
+//    per-token scalars (beta, A_log, dt_bias) are loaded a step ahead;
+//  * two layouts by the state rows WR a thread holds (rows of S^T, 8 key
+//    channels each, so the state lives in 8 WR registers per thread and a
+//    row's dot products reduce over the 16 lanes of a half warp):
+//    - WR = 8 (verify, and decode of windows longer than one token): 256
+//      threads, two CTAs per SM, one state buffer each; the next item's
+//      state streams in while one runs, and the other CTA's work hides each
+//      item's latency chain; decode stores the new state from registers;
+//    - WR = 4 (decode of one token, which only moves bytes): 512 threads,
+//      one CTA per SM, two state buffers (the state two items ahead streams
+//      in) and a third for the write-back, which leaves by two bulk stores
+//      so no thread waits on it;
+//  * with a [request, step] slot table decode reads the row of the last
+//    accepted token and also stores the state after each earlier token of
+//    the window, from registers;
 //  * per item, warp t < qlen first turns token t's raw rows into the vectors
 //    every warp needs (L2-normalised k^ and q~, exp(gate), their products)
 //    in shared memory, once;
-//  * warp w owns state rows v = 8w..8w+7 (rows of S^T); each half warp
-//    holds four of them and lane L key channels 8 (L % 16)..+7, so the state
-//    lives in 32 registers per thread and a row's dot products reduce over
-//    16 lanes;
-//  * per token, the 8 dot products of a half warp (its rows with
+//  * per token, the 2 WR dot products of a half warp (its rows with
 //    exp(gate) * k^ and with exp(gate) * q~) are reduced by one
-//    recursive-halving reduce-scatter, after which lane pairs hold one row's
-//    correction U or output; products use packed fp32x2 FMAs.
+//    recursive-halving reduce-scatter, after which a lane (WR = 8) or lane
+//    pair (WR = 4) holds one row's correction U or output; products use
+//    packed fp32x2 FMAs.
 // Token order inside the window follows the recurrence exactly:
 //   S <- diag(e^gate) S;  U = beta (v - S^T k^);  S <- S + k^ U^T;  o = S^T q~
 // computed as U = beta (v - S_old^T (e^gate * k^)),
@@ -41,13 +45,24 @@
 
 namespace kda {
 
-constexpr int WIN_THREADS = 512;
+// Two thread layouts, by the state rows WR a thread holds (8 key channels
+// each): WR = 8, 256 threads, two CTAs per SM with one state buffer each;
+// WR = 4, 512 threads, one CTA per SM with two state buffers and a
+// write-back staging buffer (decode of one token, where the kernel only
+// moves bytes and wants the most of them in flight).
+template <int WR>
+__host__ __device__ constexpr int win_threads() { return 2048 / WR; }
 constexpr int STATE_BYTES = D * D * 4;                // 65536
 constexpr int ROW_BYTES = D * 2;                      // one bf16 row of 128
 
+// Verify with a staged conv (token-major conv state, bf16 taps): each item's
+// taps (3 bands x 128 channels x 4) and the three history positions of its
+// 3 bands, per input buffer.
+constexpr int CONV_TAPS_BYTES = 3 * 1024;
+constexpr int CONV_STAGE_BYTES = CONV_TAPS_BYTES + 9 * 256;
+
 struct __align__(128) WinSmem {
-  float state[2][D * D];
-  float sout[D * D];  // decode: the new state, written back by bulk stores
+  float state[D * D];  // the next item's state streams in while this one runs
   __nv_bfloat16 in[2][MAX_WINDOW * 4 * D];
   float tp[MAX_WINDOW][D];    // e^gate * k^
   float tr[MAX_WINDOW][D];    // e^gate * q~
@@ -60,7 +75,13 @@ struct __align__(128) WinSmem {
   int next;
 };
 
-static_assert(sizeof(WinSmem) <= 227 * 1024, "window kernel shared memory");
+// Past the block: WR = 8, the two conv staging areas; WR = 4, the second
+// state buffer and the write-back staging buffer.
+constexpr int EXTRA_WR8 = 2 * CONV_STAGE_BYTES;
+constexpr int EXTRA_WR4 = 2 * STATE_BYTES;
+// two WR = 8 CTAs (each with its 1 KB reserve) share an SM's 228 KB
+static_assert(2 * (sizeof(WinSmem) + EXTRA_WR8 + 1024) <= 228 * 1024, "two window CTAs per SM");
+static_assert(sizeof(WinSmem) + EXTRA_WR4 <= 227 * 1024, "a WR = 4 window CTA fits");
 
 struct ItemInfo {
   int request, head, qs, qlen;
@@ -146,11 +167,6 @@ __device__ __forceinline__ void state_st4(void* base, int row, int chan, float4 
   }
 }
 
-// Verify with a staged conv: each item's taps (3 bands x 128 channels) and
-// the three history positions of its 3 bands, per input buffer.
-constexpr int CONV_TAPS_BYTES = 3 * 2048;                  // room for fp32 taps
-constexpr int CONV_STAGE_BYTES = CONV_TAPS_BYTES + 9 * 256;  // + bf16 history
-
 // The window's q/k/v/g rows, one bulk copy per lane of the calling warp (and,
 // for a staged conv, the item's taps and history into ``stage``).
 __device__ __forceinline__ void issue_inputs(const WindowParams& p, const ItemInfo& it,
@@ -158,7 +174,7 @@ __device__ __forceinline__ void issue_inputs(const WindowParams& p, const ItemIn
                                              unsigned char* stage = nullptr) {
   const int hq = it.head / (p.hv / p.hqk);
   const bool conv = stage != nullptr;
-  const int tap_bytes = D * (p.conv.w_f32 ? 16 : 8);
+  constexpr int tap_bytes = D * 8;  // bf16 taps
   if (lane == 0) mbar_arrive_expect_tx(ibar, it.qlen * 4 * ROW_BYTES + (conv ? 3 * tap_bytes + 9 * 256 : 0));
   __syncwarp();
   if (conv && lane < 12) {
@@ -166,7 +182,7 @@ __device__ __forceinline__ void issue_inputs(const WindowParams& p, const ItemIn
     conv_channels(p.hqk, p.hv, it.head, 0, ch);
     if (lane < 3) {
       const unsigned char* w = static_cast<const unsigned char*>(p.conv.w) + ch[lane] * (tap_bytes / D);
-      bulk_g2s(stage + lane * 2048, w, tap_bytes, ibar);
+      bulk_g2s(stage + lane * 1024, w, tap_bytes, ibar);
     } else {
       const int x = (lane - 3) / 3, i = (lane - 3) % 3;
       const int first = p.conv.accepted[it.request] - 1;
@@ -276,14 +292,10 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float4 w;
-      if (cv.bulk) {
-        if (cv.w_f32) {
-          w = *reinterpret_cast<const float4*>(stage + x * 2048 + (4 * lane + e) * 16);
-        } else {
-          float t4[4];
-          load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + x * 2048 + (4 * lane + e) * 8), t4);
-          w = make_float4(t4[0], t4[1], t4[2], t4[3]);
-        }
+      if (cv.bulk) {  // staged bf16 taps
+        float t4[4];
+        load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + x * 1024 + (4 * lane + e) * 8), t4);
+        w = make_float4(t4[0], t4[1], t4[2], t4[3]);
       } else {
         w = conv_taps(cv, ch[x] + e);
       }
@@ -292,37 +304,47 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
   }
 }
 
-// Thread (warp w, lane L) holds state rows v = 8w + 4 (L / 16) + i, i < 4,
+// Thread (warp w, lane L) holds state rows v = 2 WR w + WR (L / 16) + i, i < WR,
 // at key channels 4 (L % 16) + 64 j .. + 3, j < 2, as float2 pairs S[i][jj]
 // (jj = 2 j, 2 j + 1): each row's dot products reduce over the 16 lanes of
 // a half warp, and a half warp's 16-byte accesses to a row are contiguous.
-__device__ __forceinline__ int win_row(int warp, int lane, int i) { return 8 * warp + 4 * (lane >> 4) + i; }
+template <int WR>
+__device__ __forceinline__ int win_row(int warp, int lane, int i) { return 2 * WR * warp + WR * (lane >> 4) + i; }
 __device__ __forceinline__ int win_chan(int lane, int j) { return 4 * (lane & 15) + 64 * j; }
 
-template <bool VERIFY, bool SBF16, bool FP16>
+__device__ __forceinline__ void load_pairs(const float* vec, int lane, float2 (&v)[4]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float4 x4 = *reinterpret_cast<const float4*>(vec + win_chan(lane, j));
+    v[2 * j] = make_float2(x4.x, x4.y);
+    v[2 * j + 1] = make_float2(x4.z, x4.w);
+  }
+}
+
+template <bool VERIFY, bool SBF16, bool FP16, int WR>
 __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, const ItemInfo& it,
-                                           float2 (&S)[4][4], const __nv_bfloat16* ibuf, int warp,
+                                           float2 (&S)[WR][4], const __nv_bfloat16* ibuf, int warp,
                                            int lane) {
   const int h = it.head;
-  const int m = (lane & 15) >> 1;            // the value this lane pair ends with
-  const int my_row = win_row(warp, lane, m & 3);
+  // the 2 WR sums of a half warp are reduce-scattered over its 16 lanes by
+  // L halvings (lane bits 3, 2, ..), then the last 4 - L lane bits summed
+  constexpr int L = WR == 8 ? 4 : 3;
+  constexpr int SH = 4 - L;
+  const int e = (lane & 15) >> SH;           // the sum this lane ends with
+  const int ei = e & (WR - 1);               // its row; e < WR: row . (e^gate k^), else row . (e^gate q~)
+  const bool lead = (lane & ((1 << SH) - 1)) == 0;
+  const int my_row = win_row<WR>(warp, lane, ei);
+  const int half = lane & 16;
   for (int t = 0; t < it.qlen; ++t) {
     const int64_t tok = it.qs + t;
     float2 pv[4], rv[4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float4 p4 = *reinterpret_cast<const float4*>(&s.tp[t][win_chan(lane, j)]);
-      const float4 r4 = *reinterpret_cast<const float4*>(&s.tr[t][win_chan(lane, j)]);
-      pv[2 * j] = make_float2(p4.x, p4.y);
-      pv[2 * j + 1] = make_float2(p4.z, p4.w);
-      rv[2 * j] = make_float2(r4.x, r4.y);
-      rv[2 * j + 1] = make_float2(r4.z, r4.w);
-    }
+    load_pairs(s.tp[t], lane, pv);
+    load_pairs(s.tr[t], lane, rv);
     const float beta = s.tbeta[t], kq = s.tkq[t];
-    // x[i]: row i . (e^gate k^), x[4 + i]: row i . (e^gate q~), over this lane's 8 channels
-    float x[8];
+    // x[i]: row i . (e^gate k^), x[WR + i]: row i . (e^gate q~), over this lane's 8 channels
+    float x[2 * WR];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < WR; ++i) {
       float2 a = fmul2(S[i][0], pv[0]), bq = fmul2(S[i][0], rv[0]);
 #pragma unroll
       for (int jj = 1; jj < 4; ++jj) {
@@ -330,37 +352,32 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
         bq = ffma2(S[i][jj], rv[jj], bq);
       }
       x[i] = a.x + a.y;
-      x[4 + i] = bq.x + bq.y;
-    }
-    // reduce-scatter of 8 sums over the half warp's 16 lanes: lane pair
-    // (2 m, 2 m + 1) of the half ends with value m
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const bool up = (lane & 8) != 0;
-      const float send = up ? x[q] : x[q + 4], keep = up ? x[q + 4] : x[q];
-      x[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      x[WR + i] = bq.x + bq.y;
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const bool up = (lane & 4) != 0;
-      const float send = up ? x[q] : x[q + 2], keep = up ? x[q + 2] : x[q];
-      x[q] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    for (int lvl = 0; lvl < L; ++lvl) {
+      const int m = 8 >> lvl, n = WR >> lvl;
+      const bool up = (lane & m) != 0;
+#pragma unroll
+      for (int q = 0; q < WR; ++q) {
+        if (q < n) {
+          const float send = up ? x[q] : x[q + n], keep = up ? x[q + n] : x[q];
+          x[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
     }
-    {
-      const bool up = (lane & 2) != 0;
-      const float send = up ? x[0] : x[1], keep = up ? x[1] : x[0];
-      x[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    const float mine = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
-    // lanes with m < 4: U of row m; lanes with m >= 4: the output of row m - 4
+    if (SH) x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+    const float mine = x[0];
+    // sums e < WR: U of row e; e >= WR: the output of row e - WR
     const float vval = act_f<FP16>(ibuf[t * 4 * D + 2 * D + my_row]);
     const float U = beta * (vval - mine);
-    const int half = lane & 16;
-    const float Urow = __shfl_sync(0xffffffffu, U, half | (2 * (m & 3)));
-    if (m >= 4) {
-      if ((lane & 1) == 0) p.out[(tok * p.hv + h) * D + my_row] = act_from_f(mine + Urow * kq, FP16);
-    } else if (VERIFY && (lane & 1) == 0) {
-      p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + my_row] = U;
+    const float Urow = __shfl_sync(0xffffffffu, U, half | (ei << SH));
+    if (lead) {
+      if (e >= WR) {
+        p.out[(tok * p.hv + h) * D + my_row] = act_from_f(mine + Urow * kq, FP16);
+      } else if (VERIFY) {
+        p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + my_row] = U;
+      }
     }
     if (VERIFY && warp == 0) {
       __nv_bfloat16* dst = p.kg + (((int64_t)it.request * p.hv + h) * p.window + t) * 2 * D;
@@ -369,18 +386,11 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
       *reinterpret_cast<uint2*>(dst + D + 4 * lane) = *reinterpret_cast<const uint2*>(rowp + 3 * D + 4 * lane);
     }
     float2 dv[4], kv[4];
+    load_pairs(s.tdec[t], lane, dv);
+    load_pairs(s.tkh[t], lane, kv);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float4 d4 = *reinterpret_cast<const float4*>(&s.tdec[t][win_chan(lane, j)]);
-      const float4 k4 = *reinterpret_cast<const float4*>(&s.tkh[t][win_chan(lane, j)]);
-      dv[2 * j] = make_float2(d4.x, d4.y);
-      dv[2 * j + 1] = make_float2(d4.z, d4.w);
-      kv[2 * j] = make_float2(k4.x, k4.y);
-      kv[2 * j + 1] = make_float2(k4.z, k4.w);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float Ui = __shfl_sync(0xffffffffu, U, half | (2 * i));
+    for (int i = 0; i < WR; ++i) {
+      const float Ui = __shfl_sync(0xffffffffu, U, half | (i << SH));
       const float2 uu = make_float2(Ui, Ui);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) S[i][jj] = ffma2(S[i][jj], dv[jj], fmul2(kv[jj], uu));
@@ -389,7 +399,7 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
       // a bf16 state is stored after every token: the next token starts
       // from the rounded state, as repeated single-token decode would
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < WR; ++i)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const float4 r = round_bf16x4(make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x,
@@ -405,10 +415,10 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
       if (row >= 0 && row != it.wslot) {
         void* dst = state_row<SBF16>(p, row, h);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < WR; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            state_st4<SBF16>(dst, win_row(warp, lane, i), win_chan(lane, j),
+            state_st4<SBF16>(dst, win_row<WR>(warp, lane, i), win_chan(lane, j),
                              make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y));
       }
     }
@@ -424,9 +434,9 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
 //   S   = P_{Q-1} * S0 + sum_j r_{j,Q-1} U_j^T
 // so the state is read once for all 2Q probes and updated once.  Every
 // thread takes part (it holds the state rows of the token loop's layout).
-template <bool VERIFY, bool FP16>
+template <bool FP16, int WR>
 __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, const ItemInfo& it,
-                                             float2 (&S)[4][4], const __nv_bfloat16* ibuf,
+                                             const float2 (&S)[WR][4], const __nv_bfloat16* ibuf,
                                              const TokenScalars& ts, int tid, int warp, int lane) {
   constexpr int QW = 4;
   const int Q = it.qlen, h = it.head;
@@ -436,11 +446,8 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
   float* dec = z + 2 * QW * D;
   float* kG = z + 3 * QW * D;
   float* qG = z + 4 * QW * D;
-  float* wv = z + 5 * QW * D;
-  float* eGQ = z + 6 * QW * D;
   float* pb = z;           // S0^T kG_t, over khat once the couplings are done
   float* pa = z + QW * D;  // S0^T qG_t, over qtil
-  float* U = z + 2 * QW * D;  // over dec
   const int c0 = 4 * lane;
   // (1) warp t < Q: k^_t, q~_t, e^{gate_t}, beta_t (and verify's kg record)
   if (warp < Q) {
@@ -464,15 +471,15 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
     *reinterpret_cast<float4*>(qtil + warp * D + c0) = make_float4(qv[0] * rq, qv[1] * rq, qv[2] * rq, qv[3] * rq);
     *reinterpret_cast<float4*>(dec + warp * D + c0) = make_float4(dv[0], dv[1], dv[2], dv[3]);
     if (lane == 0) s.tbeta[warp] = sigmoidf_(act_f<FP16>(ts.beta));
-    if (VERIFY) {
+    {  // verify's kg record
       __nv_bfloat16* dst = p.kg + (((int64_t)it.request * p.hv + h) * p.window + warp) * 2 * D;
       *reinterpret_cast<uint2*>(dst + c0) = *reinterpret_cast<const uint2*>(rowp + 1 * D + c0);
       *reinterpret_cast<uint2*>(dst + D + c0) = *reinterpret_cast<const uint2*>(rowp + 3 * D + c0);
     }
   }
   __syncthreads();
-  // (2) warp j: P_j k^_j, P_j q~_j (zero for j >= Q), the chain r_{j,t},
-  // its couplings with tokens t >= j, and r_{j,Q-1}
+  // (2) warp j: P_j k^_j, P_j q~_j (zero for j >= Q), the chain r_{j,t}
+  // and its couplings with tokens t >= j
   if (warp < QW) {
     const int j = warp;
     if (j < Q) {
@@ -485,7 +492,6 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
       const float4 qj = *reinterpret_cast<const float4*>(qtil + j * D + c0);
       *reinterpret_cast<float4*>(kG + j * D + c0) = make_float4(kj.x * P.x, kj.y * P.y, kj.z * P.z, kj.w * P.w);
       *reinterpret_cast<float4*>(qG + j * D + c0) = make_float4(qj.x * P.x, qj.y * P.y, qj.z * P.z, qj.w * P.w);
-      if (j == Q - 1) *reinterpret_cast<float4*>(eGQ + c0) = P;
       float4 r = kj;
       float dsum[QW], csum[QW];
 #pragma unroll
@@ -503,7 +509,6 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
           csum[t] = r.x * kt.x + r.y * kt.y + r.z * kt.z + r.w * kt.w;
         }
       }
-      *reinterpret_cast<float4*>(wv + j * D + c0) = r;
       // reduce-scatter of the 8 sums over the warp (halving by lane bits
       // 4, 3, 2, then bits 1 and 0 summed): lanes with bits 1..0 clear end
       // with entry 4 b4 + 2 b3 + b2 of (d_0..d_3, c_0..c_3)
@@ -535,46 +540,45 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
     }
   }
   __syncthreads();
-  // (3) probes, keys then queries: this thread's 4 rows x 8 channels
-  // against the 4 vectors; x[4 i + t] = row i . vec_t, reduce-scattered over
-  // the half warp's 16 lanes (halving by lane bits 3, 2, 1, 0) so that lane
-  // (b3 b2 b1 b0) ends with row 2 b3 + b2, token 2 b1 + b0
+  // (3) probes, keys then queries, TP = 16 / WR tokens at a time: this
+  // thread's WR rows x 8 channels against those tokens' vectors;
+  // x[TP i + u] = row i . vec_{t0+u}, reduce-scattered over the half warp's
+  // 16 lanes (halving by lane bits 3, 2, 1, 0) so that lane e of the half
+  // ends with x[e]: row e / TP, token t0 + e % TP
+  constexpr int TP = 16 / WR;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const float* vecs = half == 0 ? kG : qG;
-    float x[16];
 #pragma unroll
-    for (int t = 0; t < QW; ++t) {
-      float2 w2[4];
+    for (int t0 = 0; t0 < QW; t0 += TP) {
+      float x[16];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float4 w4 = *reinterpret_cast<const float4*>(vecs + t * D + win_chan(lane, j));
-        w2[2 * j] = make_float2(w4.x, w4.y);
-        w2[2 * j + 1] = make_float2(w4.z, w4.w);
-      }
+      for (int u = 0; u < TP; ++u) {
+        float2 w2[4];
+        load_pairs(vecs + (t0 + u) * D, lane, w2);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 acc = fmul2(S[i][0], w2[0]);
+        for (int i = 0; i < WR; ++i) {
+          float2 acc = fmul2(S[i][0], w2[0]);
 #pragma unroll
-        for (int jj = 1; jj < 4; ++jj) acc = ffma2(S[i][jj], w2[jj], acc);
-        x[4 * i + t] = acc.x + acc.y;
-      }
-    }
-#pragma unroll
-    for (int lvl = 0; lvl < 4; ++lvl) {
-      const int m = 8 >> lvl, n = 8 >> lvl;  // lane mask, half of the live entries
-      const bool up = (lane & m) != 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (q < n) {
-          const float send = up ? x[q] : x[q + n], keep = up ? x[q + n] : x[q];
-          x[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          for (int jj = 1; jj < 4; ++jj) acc = ffma2(S[i][jj], w2[jj], acc);
+          x[TP * i + u] = acc.x + acc.y;
         }
       }
+#pragma unroll
+      for (int lvl = 0; lvl < 4; ++lvl) {
+        const int m = 8 >> lvl;
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q < m) {
+            const float send = up ? x[q] : x[q + m], keep = up ? x[q + m] : x[q];
+            x[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+      }
+      const int e = lane & 15;
+      (half == 0 ? pb : pa)[(t0 + e % TP) * D + win_row<WR>(warp, lane, e / TP)] = x[0];
     }
-    const int l = lane & 15;
-    const int i = 2 * ((l >> 3) & 1) + ((l >> 2) & 1), t = 2 * ((l >> 1) & 1) + (l & 1);
-    (half == 0 ? pb : pa)[t * D + win_row(warp, lane, i)] = x[0];
   }
   __syncthreads();
   // (4) thread v < 128: forward substitution for row v, outputs, records
@@ -593,58 +597,33 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
 #pragma unroll
         for (int j = 0; j <= t; ++j) o += s.dd[t][j] * u[j];
         p.out[((int64_t)(it.qs + t) * p.hv + h) * D + v] = act_from_f(o, FP16);
-        if (VERIFY) p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + v] = u[t];
-        U[t * D + v] = u[t];
-      }
-    }
-  }
-  if (!VERIFY) {
-    __syncthreads();
-    // (5) S = P_{Q-1} * S0 + sum_t r_{t,Q-1} U_t^T
-    float2 e2[4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float4 e4 = *reinterpret_cast<const float4*>(eGQ + win_chan(lane, j));
-      e2[2 * j] = make_float2(e4.x, e4.y);
-      e2[2 * j + 1] = make_float2(e4.z, e4.w);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) S[i][jj] = fmul2(S[i][jj], e2[jj]);
-#pragma unroll
-    for (int t = 0; t < QW; ++t) {
-      if (t < Q) {
-        float2 w2[4];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float4 w4 = *reinterpret_cast<const float4*>(wv + t * D + win_chan(lane, j));
-          w2[2 * j] = make_float2(w4.x, w4.y);
-          w2[2 * j + 1] = make_float2(w4.z, w4.w);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float ut = U[t * D + win_row(warp, lane, i)];
-          const float2 uu = make_float2(ut, ut);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) S[i][jj] = ffma2(w2[jj], uu, S[i][jj]);
-        }
+        p.corr[(((int64_t)it.request * p.hv + h) * p.window + t) * D + v] = u[t];
       }
     }
   }
 }
 
-// The staging area of input buffer b for a verify with a staged conv (the
-// state write-back buffer, unused by verify), else none.
-__device__ __forceinline__ unsigned char* conv_stage(const WindowParams& p, WinSmem& s, int b) {
-  return (p.conv.state && p.conv.bulk) ? reinterpret_cast<unsigned char*>(s.sout) + b * CONV_STAGE_BYTES : nullptr;
+// The staging area of input buffer b for a verify with a staged conv, else
+// none.
+__device__ __forceinline__ unsigned char* conv_stage(const WindowParams& p, unsigned char* extra, int b) {
+  return (p.conv.state && p.conv.bulk) ? extra + b * CONV_STAGE_BYTES : nullptr;
 }
-static_assert(2 * CONV_STAGE_BYTES <= (int)sizeof(float) * D * D, "conv staging fits the write-back buffer");
 
-template <bool VERIFY, bool SBF16, bool FP16>
-__global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const WindowParams p) {
+// WR = 8: one state buffer, the next item's state streams in while an item
+// runs; the new state is stored from registers.  WR = 4 (decode only): two
+// state buffers, the state two items ahead streams in, and the new state
+// leaves through a staging buffer by two bulk stores, so no thread waits on
+// its write.
+template <bool VERIFY, bool SBF16, bool FP16, int WR>
+__global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window_kernel(const WindowParams p) {
+  static_assert(WR == 8 || (WR == 4 && !VERIFY), "verify runs the WR = 8 layout");
+  constexpr int NBUF = WR == 8 ? 1 : 2;
+  constexpr int THREADS = win_threads<WR>();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   WinSmem& s = *reinterpret_cast<WinSmem*>(smem_raw);
+  unsigned char* const extra = smem_raw + sizeof(WinSmem);
+  auto state_buf = [&](int k) -> float* { return k == 0 ? s.state : reinterpret_cast<float*>(extra); };
+  float* const sout = reinterpret_cast<float*>(extra + STATE_BYTES);  // WR = 4
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = p.n_req * p.hv;
   const int ctas = gridDim.x;
@@ -677,8 +656,8 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       if (its[b] < items) {
         const ItemInfo ii = item_info(p, its[b]);
         if (ii.work) {
-          if (lane == 0) issue_state<SBF16>(p, ii, s.state[b], &s.sbar[b]);
-          issue_inputs(p, ii, s.in[b], &s.ibar[b], lane, conv_stage(p, s, b));
+          if (b < NBUF && lane == 0) issue_state<SBF16>(p, ii, state_buf(b), &s.sbar[b]);
+          issue_inputs(p, ii, s.in[b], &s.ibar[b], lane, conv_stage(p, extra, b));
         }
       }
     }
@@ -687,52 +666,60 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
   ItemInfo itn = nxt < items ? item_info(p, nxt) : ItemInfo{};
   TokenScalars ts = load_token_scalars(p, it, warp, lane);
   uint32_t sphase[2] = {0u, 0u}, iphase[2] = {0u, 0u};
-  int b = 0;
-  bool stored = false;  // a bulk state store is in flight from sout
+  int b = 0, sb = 0;  // input buffer, state buffer
+  bool stored = false;  // WR = 4: a bulk state store is in flight from sout
   while (cur < items) {
     if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
     bool ok = true;
     const bool conv = VERIFY && !FP16 && p.conv.state != nullptr;  // conv: bf16 activations only
     // verify of 2..4 tokens on an fp32 state: the windowed solve (measured
-    // faster than the token loop there; for decode, whose rank-Q update and
+    // faster than the token loop there; for decode, whose update and
     // write-back follow, the token loop measured faster)
     const bool windowed = VERIFY && !SBF16 && it.qlen >= 2 && it.qlen <= 4;
-    float2 S[4][4];
+    float2 S[WR][4];
     float yc[3][4];  // conv outputs of token ``warp`` (verify with a conv)
     if (it.work) {
-      ok = mbar_wait_bounded(&s.sbar[b], sphase[b], p.err);
+      ok = mbar_wait_bounded(&s.sbar[sb], sphase[sb], p.err);
       ok = mbar_wait_bounded(&s.ibar[b], iphase[b], p.err) && ok;
-      sphase[b] ^= 1u;
+      sphase[sb] ^= 1u;
       iphase[b] ^= 1u;
       if (ok) {
         if (warp < it.qlen) {
           if (conv)
-            conv_token(p, it, s.in[b], reinterpret_cast<const unsigned char*>(s.sout) + b * CONV_STAGE_BYTES,
-                       warp, lane, yc);
+            conv_token(p, it, s.in[b], extra + b * CONV_STAGE_BYTES, warp, lane, yc);
           else if (!windowed)
             token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
         }
+        const float* sbuf = state_buf(sb);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < WR; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const float4 x4 = state_ld4<SBF16>(s.state[b], win_row(warp, lane, i), win_chan(lane, j));
+            const float4 x4 = state_ld4<SBF16>(sbuf, win_row<WR>(warp, lane, i), win_chan(lane, j));
             S[i][2 * j] = make_float2(x4.x, x4.y);
             S[i][2 * j + 1] = make_float2(x4.z, x4.w);
           }
       }
     }
-    // state buffer b read, token vectors written, the next ticket published
+    // the state buffer read, token vectors written, the next ticket published
     if (__syncthreads_or(!ok)) {
       // a copy never landed (error word set): wait, bounded, for the copies
-      // still in flight into the other buffer, and for the last state store,
-      // before leaving
-      if (tid == 0 && nxt < items && item_info(p, nxt).work) {
-        mbar_wait_bounded(&s.sbar[b ^ 1], sphase[b ^ 1], p.err);
+      // still in flight (the next item's inputs, and with two state buffers
+      // its state), then leave
+      if (tid == 0 && itn.work) {
         mbar_wait_bounded(&s.ibar[b ^ 1], iphase[b ^ 1], p.err);
+        if (NBUF == 2) mbar_wait_bounded(&s.sbar[sb ^ 1], sphase[sb ^ 1], p.err);
       }
-      if (!VERIFY && tid == 0) bulk_wait<0>();
+      if (WR == 4 && tid == 0) bulk_wait<0>();
       return;
+    }
+    const int nn = s.next;
+    const ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
+    // the freed state buffer takes the state of the item after this one (one
+    // buffer) or of the item after that (two buffers)
+    if (tid == 0) {
+      const ItemInfo& ahead = NBUF == 2 ? it2 : itn;
+      if (ahead.work) issue_state<SBF16>(p, ahead, state_buf(sb), &s.sbar[sb]);
     }
     if (conv && it.work) {
       // every raw row has been read: the conv outputs replace them, then
@@ -750,67 +737,81 @@ __global__ void __launch_bounds__(WIN_THREADS, 1) kda_window_kernel(const Window
       }
       __syncthreads();
     }
-    const int nn = s.next;
-    const ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
-    if (tid == 0 && nn < items && it2.work) issue_state<SBF16>(p, it2, s.state[b], &s.sbar[b]);
     // the next item's scalars, used a step from now
     const TokenScalars ts_next = load_token_scalars(p, itn, warp, lane);
     if (it.work) {
-      if (windowed)
-        window_solve<VERIFY, FP16>(p, s, it, S, s.in[b], ts, tid, warp, lane);
-      else
-        run_tokens<VERIFY, SBF16, FP16>(p, s, it, S, s.in[b], warp, lane);
-      if (!VERIFY) {
-        // the previous item's bulk store has read sout by now (a whole item
-        // ago); confirm it before anyone overwrites sout
-        if (tid == 0 && stored) bulk_wait_read<0>();
-        __syncthreads();
+      bool solved = false;
+      if constexpr (VERIFY) {
+        if (windowed) {
+          window_solve<FP16, WR>(p, s, it, S, s.in[b], ts, tid, warp, lane);
+          solved = true;
+        }
+      }
+      if (!solved) run_tokens<VERIFY, SBF16, FP16, WR>(p, s, it, S, s.in[b], warp, lane);
+      if (!VERIFY && it.wslot >= 0) {
+        // the state after the last token: WR = 8 straight from registers,
+        // each half warp storing 256 contiguous bytes of a row per
+        // instruction; WR = 4 into sout, once the previous item's bulk store
+        // has read it (issued a whole item ago)
+        void* dst = state_row<SBF16>(p, it.wslot, it.head);
+        if (WR == 4) {
+          if (tid == 0 && stored) bulk_wait_read<0>();
+          __syncthreads();
+          dst = sout;
+        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < WR; ++i)
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            state_st4<SBF16>(s.sout, win_row(warp, lane, i), win_chan(lane, j),
+            state_st4<SBF16>(dst, win_row<WR>(warp, lane, i), win_chan(lane, j),
                              make_float4(S[i][2 * j].x, S[i][2 * j].y, S[i][2 * j + 1].x, S[i][2 * j + 1].y));
-        fence_proxy_async_smem();
+        if (WR == 4) fence_proxy_async_smem();
       }
     } else if (it.zero) {
-      for (int e = tid; e < it.qlen * D; e += WIN_THREADS) {
+      for (int e = tid; e < it.qlen * D; e += THREADS) {
         const int t = e / D, c = e - t * D;
         p.out[((int64_t)(it.qs + t) * p.hv + it.head) * D + c] = __float2bfloat16_rn(0.f);
       }
     }
     if (tid == 0 && it.bad) set_error(p.err, ERR_INDEX);
     __syncthreads();  // input buffer b and the token vectors consumed, sout written
-    if (!VERIFY && tid == 0 && it.work && it.wslot >= 0) {
+    if (WR == 4 && !VERIFY && tid == 0 && it.work && it.wslot >= 0) {
       constexpr int bytes = SBF16 ? STATE_BYTES / 2 : STATE_BYTES;
       unsigned char* dst = state_row<SBF16>(p, it.wslot, it.head);
-      const unsigned char* src = reinterpret_cast<const unsigned char*>(s.sout);
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(sout);
       bulk_s2g(dst, src, bytes / 2);
       bulk_s2g(dst + bytes / 2, src + bytes / 2, bytes / 2);
       bulk_commit();
       stored = true;
     }
-    if (warp == 1 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane, conv_stage(p, s, b));
+    if (warp == 1 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane, conv_stage(p, extra, b));
     ts = ts_next;
     cur = nxt;
     nxt = nn;
     it = itn;
     itn = it2;
     b ^= 1;
+    if (NBUF == 2) sb ^= 1;
   }
-  if (!VERIFY && tid == 0) bulk_wait<0>();  // the last state store has landed
+  if (WR == 4 && tid == 0) bulk_wait<0>();  // the last state store has landed
 }
 
 // Host-side launcher (called from the API layer after validation).
-template <bool VERIFY, bool SBF16, bool FP16>
-static void launch_window_t(const WindowParams& p, int grid, cudaStream_t stream) {
+template <bool VERIFY, bool SBF16, bool FP16, int WR>
+static void launch_window_t(const WindowParams& p, int num_sms, cudaStream_t stream) {
+  constexpr int smem = (int)sizeof(WinSmem) + (WR == 8 ? EXTRA_WR8 : EXTRA_WR4);
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(WinSmem));
+    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     attr = true;
   }
-  kda_window_kernel<VERIFY, SBF16, FP16><<<grid, WIN_THREADS, sizeof(WinSmem), stream>>>(p);
+  const int items = p.n_req * p.hv;
+  const int slots = (WR == 8 ? 2 : 1) * num_sms;  // resident CTAs
+  const int grid = items < slots ? items : slots;
+  kda_window_kernel<VERIFY, SBF16, FP16, WR><<<grid, win_threads<WR>(), smem, stream>>>(p);
 }
 
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
@@ -822,18 +823,25 @@ int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
   }
   const int items = p.n_req * p.hv;
   if (items == 0) return 0;
-  const int grid = items < num_sms ? items : num_sms;
-  const int variant = (verify ? 4 : 0) + (p.state_bf16 ? 2 : 0) + (p.in_fp16 ? 1 : 0);
+  // decode of one token per request moves the state with almost no compute:
+  // the WR = 4 layout keeps the most bytes in flight (measured faster
+  // there); longer windows and verify overlap two CTAs' compute (WR = 8)
+  const bool wr4 = !verify && p.window == 1;
+  const int variant = (wr4 ? 8 : 0) + (verify ? 4 : 0) + (p.state_bf16 ? 2 : 0) + (p.in_fp16 ? 1 : 0);
   trace_begin(verify ? "kda_verify_window" : "kda_decode_window", stream);
   switch (variant) {
-    case 0: launch_window_t<false, false, false>(p, grid, stream); break;
-    case 1: launch_window_t<false, false, true>(p, grid, stream); break;
-    case 2: launch_window_t<false, true, false>(p, grid, stream); break;
-    case 3: launch_window_t<false, true, true>(p, grid, stream); break;
-    case 4: launch_window_t<true, false, false>(p, grid, stream); break;
-    case 5: launch_window_t<true, false, true>(p, grid, stream); break;
-    case 6: launch_window_t<true, true, false>(p, grid, stream); break;
-    default: launch_window_t<true, true, true>(p, grid, stream); break;
+    case 0: launch_window_t<false, false, false, 8>(p, num_sms, stream); break;
+    case 1: launch_window_t<false, false, true, 8>(p, num_sms, stream); break;
+    case 2: launch_window_t<false, true, false, 8>(p, num_sms, stream); break;
+    case 3: launch_window_t<false, true, true, 8>(p, num_sms, stream); break;
+    case 4: launch_window_t<true, false, false, 8>(p, num_sms, stream); break;
+    case 5: launch_window_t<true, false, true, 8>(p, num_sms, stream); break;
+    case 6: launch_window_t<true, true, false, 8>(p, num_sms, stream); break;
+    case 7: launch_window_t<true, true, true, 8>(p, num_sms, stream); break;
+    case 8: launch_window_t<false, false, false, 4>(p, num_sms, stream); break;
+    case 9: launch_window_t<false, false, true, 4>(p, num_sms, stream); break;
+    case 10: launch_window_t<false, true, false, 4>(p, num_sms, stream); break;
+    default: launch_window_t<false, true, true, 4>(p, num_sms, stream); break;
   }
   trace_end(stream);
   // verify with a conv: every history has been read, roll the conv state
