@@ -266,7 +266,7 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
 // history at positions accepted-1 .. accepted+1 of the slot's conv row.
 __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo& it,
                                            const __nv_bfloat16* ibuf, const unsigned char* stage, int t,
-                                           int lane, float y[3][4]) {
+                                           int lane, uint2 (&y)[3]) {
   const ConvParams& cv = p.conv;
   const int first = cv.accepted[it.request] - 1;
   int64_t ch[3];
@@ -289,6 +289,7 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
           win[j][e] = bf2f(hist[(int64_t)(first + 3 + tt) * cv.pos_st + (ch[x] + e) * cv.ch_st]);
       }
     }
+    float ye[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float4 w;
@@ -299,8 +300,11 @@ __device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo
       } else {
         w = conv_taps(cv, ch[x] + e);
       }
-      y[x][e] = conv_silu(cv.w_f32, w, win[0][e], win[1][e], win[2][e], win[3][e]);
+      ye[e] = conv_silu(cv.w_f32, w, win[0][e], win[1][e], win[2][e], win[3][e]);
     }
+    // rounded to bf16 at once (the convolved rows replace the raw bf16 rows)
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(ye[0], ye[1]), hi = __floats2bfloat162_rn(ye[2], ye[3]);
+    y[x] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
   }
 }
 
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
     // write-back follow, the token loop measured faster)
     const bool windowed = VERIFY && !SBF16 && it.qlen >= 2 && it.qlen <= 4;
     float2 S[WR][4];
-    float yc[3][4];  // conv outputs of token ``warp`` (verify with a conv)
+    uint2 yc[3];  // bf16 conv outputs of token ``warp`` (verify with a conv)
     if (it.work) {
       ok = mbar_wait_bounded(&s.sbar[sb], sphase[sb], p.err);
       ok = mbar_wait_bounded(&s.ibar[b], iphase[b], p.err) && ok;
@@ -726,12 +730,7 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
       // the token vectors come from the convolved rows
       if (warp < it.qlen) {
 #pragma unroll
-        for (int x = 0; x < 3; ++x) {
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(yc[x][0], yc[x][1]);
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(yc[x][2], yc[x][3]);
-          *reinterpret_cast<uint2*>(s.in[b] + (warp * 4 + x) * D + 4 * lane) =
-              make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-        }
+        for (int x = 0; x < 3; ++x) *reinterpret_cast<uint2*>(s.in[b] + (warp * 4 + x) * D + 4 * lane) = yc[x];
         __syncwarp();
         if (!windowed) token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
       }
