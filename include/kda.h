@@ -259,6 +259,57 @@ int kda_chunk_fwd_noalloc(const kda_activations* x, void* out, const int32_t* cu
                           int32_t groups, void* stream);
 
 /*
+ * kda_chunk_fwd_host - kda_chunk_fwd on activations, output and states in
+ * HOST memory: the library moves them and overlaps the moves with the
+ * prefill.  The paper has no counterpart; it is the serving form of chunked
+ * prefill (the MATE chunk_kda contract cut into segments).
+ *
+ * Each sequence is cut into segments of segment_tokens tokens (the last one
+ * shorter); call j runs segment j of every sequence still active as one
+ * varlen prefill on device mirrors in the workspace, the fp32 state carried
+ * from call to call.  Segments are multiples of the 64-token chunk, so the
+ * chunks are those of an uncut prefill.  Three library streams copy the
+ * rows in, compute and copy the outputs out, so call j computes while call
+ * j + 1's rows arrive and call j - 1's outputs leave; the work is ordered
+ * after earlier work on ``stream`` and ``stream`` waits for all of it.
+ *
+ *   x               q, k, v, g, beta, A_log, dt_bias are host pointers
+ *                   (page-locked memory lets the copies overlap; pageable
+ *                   memory works, without overlap).  Heads contiguous within
+ *                   a token (q/k/v/g head stride 128, beta head stride 1);
+ *                   any token stride that covers a token's heads.
+ *                   state_bf16 must be 0.
+ *   out             host [T, Hv, 128] contiguous, x->dtype, written
+ *   cu_seqlens      host int32 [n_seqs + 1] (0 .. T, non-decreasing), or
+ *                   NULL for n_seqs dense sequences of T / n_seqs tokens
+ *   initial_state   host fp32 [n_seqs, Hv, 128, 128], or NULL (zero start)
+ *   final_state     host fp32 [n_seqs, Hv, 128, 128], or NULL (dropped)
+ *   segment_tokens  a positive multiple of 64, or <= 0: about a quarter of
+ *                   the longest sequence, between 256 and 4096
+ *   groups          as kda_chunk_fwd, per call
+ *   workspace       device memory of at least
+ *                   kda_chunk_fwd_host_workspace_bytes(..) bytes: the
+ *                   mirrors of the inputs and the output, the carried states
+ *                   and each call's prefill scratch
+ *   stream          cudaStream_t
+ * The host buffers must stay valid, and the workspace untouched, until
+ * ``stream`` reaches the end of this call's work.  Calls on one device share
+ * the library streams and one page-locked table buffer, which a call reuses
+ * only after the previous call's tables reached the device (it waits on the
+ * host for that); not for stream capture.  Device-side rules and error
+ * words as kda_chunk_fwd.
+ */
+int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
+                       const float* initial_state, float* final_state, int32_t segment_tokens,
+                       int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
+
+/* kda_chunk_fwd_host_workspace_bytes - the workspace kda_chunk_fwd_host needs
+ * for these arguments (the same x, cu_seqlens, n_seqs, segment_tokens and
+ * groups); 0 when they are invalid (kda_last_error says why). */
+size_t kda_chunk_fwd_host_workspace_bytes(const kda_activations* x, const int32_t* cu_seqlens,
+                                          int32_t n_seqs, int32_t segment_tokens, int32_t groups);
+
+/*
  * kda_decode - in-place decode of a short window (1 <= window <= 8 tokens per
  * request) on a paged state cache: the MATE gated_delta_rule_decode
  * contract for fp32 or bf16 V-first states with in-kernel gate, lower bound, beta

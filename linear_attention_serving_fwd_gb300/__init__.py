@@ -24,9 +24,9 @@ from . import _native
 from ._native import KdaError
 
 D = 128
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_decode", "kda_decode_steps", "kda_verify",
-           "kda_commit",
-           "kda_device_status", "chunk_workspace_bytes", "KdaError", "library_path"]
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_host", "kda_decode", "kda_decode_steps",
+           "kda_verify", "kda_commit", "kda_device_status", "chunk_workspace_bytes",
+           "chunk_fwd_host_workspace_bytes", "KdaError", "library_path"]
 
 
 def library_path() -> str:
@@ -73,9 +73,11 @@ def _state_bf16(*states) -> int:
     return _STATE_DTYPES[dt]
 
 
-def _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound):
+def _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound, host=False):
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
-        if not t.is_cuda:
+        if host and t.is_cuda:
+            raise ValueError(f"{name} must be a host (CPU) tensor.")
+        if not host and not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor.")
     if q.dtype == torch.float16:
         dtype = _native.KDA_DTYPE_FP16
@@ -257,6 +259,88 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     _native.check(rc)
     del keep
     return out, final_state
+
+
+def kda_chunk_fwd_host(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, lower_bound=-5.0,
+                       cu_seqlens=None, n_seqs=None, initial_state=None, output_final_state=False,
+                       final_state=None, out=None, segment_tokens: int = 0, groups: int = 0,
+                       workspace=None, device=None, stream=None):
+    """Chunked prefill on host (CPU) tensors; returns (out, final_state or None),
+    both host tensors.
+
+    The same shapes and rules as ``kda_chunk_fwd`` with every tensor in host
+    memory (``cu_seqlens`` an int32 CPU tensor; A_log, dt_bias, states fp32
+    CPU tensors).  The library copies segments of ``segment_tokens`` tokens
+    of every sequence to the GPU, runs them as chunked prefill with the
+    state carried between segments, and copies the outputs back, the copies
+    overlapping the kernels when the host tensors are page-locked
+    (``pin_memory()``; ``out`` and ``final_state`` are allocated page-locked
+    when not given).  ``workspace`` is a uint8 CUDA tensor of at least
+    ``chunk_fwd_host_workspace_bytes(..)`` bytes, allocated on ``device``
+    when not given.  The call returns once the work is queued on ``stream``:
+    synchronise it before reading ``out``.
+    """
+    dense_b = q.shape[0] if q.dim() == 4 else None
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
+    v, g = _as_tokens(v, "v"), _as_tokens(g, "g")
+    beta = _as_tokens(beta, "beta", heads_dim=False)
+    if any(t is not None and t.is_cuda for t in (A_log, dt_bias)):
+        raise ValueError("A_log and dt_bias must be CPU tensors.")
+    a, keep = _activations(q, k, v, g, beta, A_log, dt_bias, scale, lower_bound, host=True)
+    T, hv = q.shape[0], v.shape[1]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.is_cuda:
+            raise TypeError("cu_seqlens must be an int32 CPU tensor.")
+        cu_seqlens = cu_seqlens.contiguous()
+        n = cu_seqlens.numel() - 1
+    else:
+        n = n_seqs if n_seqs is not None else (dense_b if dense_b is not None else 1)
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is not None and (t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != (n, hv, D, D)
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous fp32 CPU tensor [N, Hv, 128, 128].")
+    if out is None:
+        out = torch.empty((T, hv, D), dtype=q.dtype).pin_memory()
+    elif out.is_cuda or tuple(out.shape) != (T, hv, D) or not out.is_contiguous() or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous CPU tensor [T, Hv, 128] of the input dtype.")
+    if output_final_state and final_state is None:
+        final_state = torch.empty((n, hv, D, D), dtype=torch.float32).pin_memory()
+    lib = _native.lib()
+    need = int(lib.kda_chunk_fwd_host_workspace_bytes(ctypes.byref(a), _ptr(cu_seqlens), n,
+                                                      int(segment_tokens), int(groups)))
+    if need == 0:
+        raise _native.KdaError(_native.KDA_ERR_INVALID_ARGUMENT, lib.kda_last_error().decode())
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8,
+                                device=device if device is not None else torch.cuda.current_device())
+    elif not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor.")
+    with torch.cuda.device(workspace.device):
+        rc = lib.kda_chunk_fwd_host(ctypes.byref(a), _ptr(out), _ptr(cu_seqlens), n, _ptr(initial_state),
+                                    _ptr(final_state), int(segment_tokens), int(groups), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _native.check(rc)
+    del keep
+    return out, final_state
+
+
+def chunk_fwd_host_workspace_bytes(q, k, v, g, beta, *, A_log=None, dt_bias=None, cu_seqlens=None,
+                                   n_seqs=None, segment_tokens: int = 0, groups: int = 0) -> int:
+    """Workspace bytes ``kda_chunk_fwd_host`` needs for these host tensors."""
+    dense_b = q.shape[0] if q.dim() == 4 else None
+    q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
+    v, g = _as_tokens(v, "v"), _as_tokens(g, "g")
+    beta = _as_tokens(beta, "beta", heads_dim=False)
+    a, keep = _activations(q, k, v, g, beta, A_log, dt_bias, None, -5.0, host=True)
+    n = (cu_seqlens.numel() - 1 if cu_seqlens is not None
+         else n_seqs if n_seqs is not None else (dense_b if dense_b is not None else 1))
+    lib = _native.lib()
+    need = int(lib.kda_chunk_fwd_host_workspace_bytes(ctypes.byref(a), _ptr(cu_seqlens), n,
+                                                      int(segment_tokens), int(groups)))
+    del keep
+    if need == 0:
+        raise _native.KdaError(_native.KDA_ERR_INVALID_ARGUMENT, lib.kda_last_error().decode())
+    return need
 
 
 def kda_chunk_fwd_noalloc(q, k, v, g, beta, *, out, A_log=None, dt_bias=None, scale=None,

@@ -27,7 +27,8 @@ KDA_DTYPE_FP16 = 1
 EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_verify",
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
            "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
-           "kda_decode_steps", "kda_verify_ex", "kda_commit_ex")
+           "kda_decode_steps", "kda_verify_ex", "kda_commit_ex", "kda_chunk_fwd_host",
+           "kda_chunk_fwd_host_workspace_bytes")
 
 
 class KdaActivations(ctypes.Structure):
@@ -78,6 +79,10 @@ def _declare(lib):
     lib.kda_chunk_fwd_ex.restype = ctypes.c_int
     lib.kda_chunk_fwd_noalloc.argtypes = [A, P, P, I32, P, P, P, I64, I64, P, P, I32, P]
     lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_chunk_fwd_host.argtypes = [A, P, P, I32, P, P, I32, I32, P, SZ, P]
+    lib.kda_chunk_fwd_host.restype = ctypes.c_int
+    lib.kda_chunk_fwd_host_workspace_bytes.argtypes = [A, P, I32, I32, I32]
+    lib.kda_chunk_fwd_host_workspace_bytes.restype = SZ
     lib.kda_decode.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode_steps.argtypes = [A, P, P, I64, I64, P, P, I64, P, I32, I32, P]

@@ -2,6 +2,7 @@
 // (the shape, dtype and pairing rules of the MATE chunk_kda /
 // gated_delta_rule_decode validation and of the vLLM fused_kda_chunk cache
 // rules), the per-device error word, and the kernel launches.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -398,6 +399,329 @@ int kda_chunk_fwd_ex(const kda_activations* x, void* out, const int32_t* cu_seql
                       n_slots, state_indices, has_initial_state, checkpoint_state, checkpoint_row_stride,
                       checkpoint_rows, checkpoint_offsets, checkpoint_state_indices, conv, groups, workspace,
                       workspace_bytes, stream);
+}
+
+// --- prefill from host memory ---------------------------------------------
+// Chunked prefill in the serving sense: each sequence is cut into segments of
+// L tokens (a multiple of the 64-token chunk, so the kernels' chunks are the
+// ones an uncut prefill forms), and call j runs segment j of every sequence
+// still active as one varlen prefill, the fp32 state carried from call to
+// call in a state-cache table in the workspace.  Three streams: copy-in
+// (host to device mirrors), compute, copy-out; call j computes while call
+// j + 1's rows arrive and call j - 1's outputs leave.
+namespace {
+
+constexpr size_t HOST_ALIGN = 256;
+size_t align_up(size_t n) { return (n + HOST_ALIGN - 1) / HOST_ALIGN * HOST_ALIGN; }
+
+struct HostPlan {
+  int L = 0, n_calls = 0;
+  bool dense = false;                      // n_seqs sequences of t_total / n_seqs tokens
+  std::vector<int64_t> start, len;         // per sequence, host rows
+  std::vector<int32_t> call_n, call_rows;  // per call: sequences, tokens
+  std::vector<int64_t> call_row;           // per call: first row in the device mirrors
+  std::vector<uint8_t> call_dense;         // the call's pieces are equally long
+  std::vector<int64_t> call_meta;          // per call: int32 offset of its cu_seqlens, then indices
+  std::vector<size_t> call_ws;             // per call: chunk workspace bytes
+  size_t meta_ints = 0;
+  size_t off_q = 0, off_k = 0, off_v = 0, off_g = 0, off_b = 0, off_o = 0, off_cache = 0, off_alog = 0,
+         off_dt = 0, off_meta = 0, off_ws = 0, total = 0;
+};
+
+// Validates a host-memory prefill and lays out its calls and workspace.
+int plan_host(const kda_activations* x, const int32_t* cu, int32_t n_seqs, int32_t segment,
+              int32_t groups, HostPlan& P) {
+  int rc = check_activations(x, false);
+  if (rc) return rc;
+  if (x->state_bf16 != 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "the host-memory prefill carries fp32 states only (state_bf16 = 0).");
+  if (n_seqs <= 0) return fail(KDA_ERR_INVALID_ARGUMENT, "n_seqs must be >= 1.");
+  if (segment > 0 && segment % kda::CHUNK != 0)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "segment_tokens must be a positive multiple of %d (got %d).",
+                kda::CHUNK, segment);
+  const int64_t T = x->t_total, hqk = x->hqk, hv = x->hv, D = kda::D;
+  if (T > 0) {
+    if ((hqk > 1 && (x->q_stride_head != D || x->k_stride_head != D)) ||
+        (hv > 1 && (x->v_stride_head != D || x->g_stride_head != D)) || (hv > 1 && x->beta_stride_head != 1))
+      return fail(KDA_ERR_INVALID_ARGUMENT,
+                  "host rows need contiguous heads (q/k/v/g head stride 128, beta head stride 1).");
+    if (x->q_stride_tok < hqk * D || x->k_stride_tok < hqk * D || x->v_stride_tok < hv * D ||
+        x->g_stride_tok < hv * D || x->beta_stride_tok < hv)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "host token strides must cover a token's heads.");
+  }
+  P.start.assign(n_seqs, 0);
+  P.len.assign(n_seqs, 0);
+  P.dense = cu == nullptr;
+  if (cu) {
+    if (cu[0] != 0 || cu[n_seqs] != T)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must run from 0 to t_total.");
+    for (int b = 0; b < n_seqs; ++b) {
+      if (cu[b + 1] < cu[b]) return fail(KDA_ERR_INVALID_ARGUMENT, "cu_seqlens must be non-decreasing.");
+      P.start[b] = cu[b];
+      P.len[b] = cu[b + 1] - cu[b];
+    }
+  } else {
+    if (T % n_seqs != 0)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "dense mode (no cu_seqlens) needs t_total divisible by n_seqs.");
+    for (int b = 0; b < n_seqs; ++b) {
+      P.start[b] = (T / n_seqs) * b;
+      P.len[b] = T / n_seqs;
+    }
+  }
+  int64_t max_len = 0;
+  for (int64_t l : P.len) max_len = l > max_len ? l : max_len;
+  // by default about four segments of the longest sequence, 256 .. 4096
+  // tokens (B=2 x 4096 tokens, H=16 on GB300: 1.13 ms at one segment,
+  // 0.95 at two, 0.89 at four, 0.90 at eight, 1.01 at sixteen)
+  int64_t L = segment;
+  if (L <= 0) {
+    L = (max_len / 4 + kda::CHUNK - 1) / kda::CHUNK * kda::CHUNK;
+    L = L < 256 ? 256 : (L > 4096 ? 4096 : L);
+  }
+  P.L = (int)L;
+  P.n_calls = (int)((max_len + L - 1) / L);
+  int64_t row = 0;
+  for (int j = 0; j < P.n_calls; ++j) {
+    int32_t n = 0, rows = 0;
+    int64_t first = -1;
+    bool eq = true;
+    for (int b = 0; b < n_seqs; ++b) {
+      if (P.len[b] <= j * L) continue;
+      const int64_t piece = std::min<int64_t>(L, P.len[b] - j * L);
+      if (first < 0) first = piece;
+      eq &= piece == first;
+      ++n;
+      rows += (int32_t)piece;
+    }
+    P.call_n.push_back(n);
+    P.call_rows.push_back(rows);
+    P.call_row.push_back(row);
+    P.call_dense.push_back(eq);
+    P.call_meta.push_back((int64_t)P.meta_ints);
+    P.meta_ints += 2 * (size_t)n + 1;
+    const int G = choose_groups(n, rows, x->hv, groups);
+    P.call_ws.push_back(4 * kda::chunk_workspace_floats(n, rows, x->hv, G, nullptr));
+    row += rows;
+  }
+  const size_t es = 2;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+  P.off_q = take(T * hqk * D * es);
+  P.off_k = take(T * hqk * D * es);
+  P.off_v = take(T * hv * D * es);
+  P.off_g = take(T * hv * D * es);
+  P.off_b = take(T * hv * es);
+  P.off_o = take(T * hv * D * es);
+  P.off_cache = take((size_t)n_seqs * hv * D * D * 4);
+  P.off_alog = take(x->A_log ? hv * 4 : 0);
+  P.off_dt = take(x->A_log ? hv * D * 4 : 0);
+  P.off_meta = take(P.meta_ints * 4);
+  size_t ws = 0;
+  for (size_t w : P.call_ws) ws = w > ws ? w : ws;
+  P.off_ws = take(ws);
+  P.total = o;
+  return KDA_OK;
+}
+
+struct HostCtx {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> ev;
+  int32_t* meta = nullptr;  // page-locked staging of the call tables
+  size_t meta_cap = 0;      // ints
+  cudaEvent_t meta_done = nullptr;
+  bool meta_used = false;
+};
+HostCtx g_host_ctx[64];
+
+int host_ctx_ready(HostCtx& c, size_t events, size_t meta_ints) {
+  cudaError_t e = cudaSuccess;
+  if (!c.ready) {
+    if ((e = cudaStreamCreateWithFlags(&c.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&c.s_comp, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&c.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c.meta_done, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e, "host prefill streams");
+    c.ready = true;
+  }
+  while (c.ev.size() < events) {
+    cudaEvent_t ev = nullptr;
+    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e, "host prefill events");
+    c.ev.push_back(ev);
+  }
+  // the previous call's tables have left the staging buffer
+  if (c.meta_used && (e = cudaEventSynchronize(c.meta_done)) != cudaSuccess)
+    return cuda_fail(e, "host prefill tables");
+  if (meta_ints > c.meta_cap) {
+    if (c.meta) cudaFreeHost(c.meta);
+    c.meta = nullptr;
+    c.meta_cap = 0;
+    const size_t cap = meta_ints < 1024 ? 1024 : 2 * meta_ints;
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c.meta), cap * 4, cudaHostAllocDefault)) != cudaSuccess)
+      return cuda_fail(e, "host prefill tables");
+    c.meta_cap = cap;
+  }
+  return KDA_OK;
+}
+
+// rows x row_bytes from a strided source to a packed destination
+cudaError_t copy_rows(void* dst, const void* src, size_t row_bytes, size_t src_pitch, size_t rows,
+                      cudaMemcpyKind kind, cudaStream_t s) {
+  if (rows == 0 || row_bytes == 0) return cudaSuccess;
+  if (src_pitch == row_bytes) return cudaMemcpyAsync(dst, src, row_bytes * rows, kind, s);
+  return cudaMemcpy2DAsync(dst, row_bytes, src, src_pitch, row_bytes, rows, kind, s);
+}
+
+}  // namespace
+
+size_t kda_chunk_fwd_host_workspace_bytes(const kda_activations* x, const int32_t* cu_seqlens,
+                                          int32_t n_seqs, int32_t segment_tokens, int32_t groups) {
+  HostPlan P;
+  if (plan_host(x, cu_seqlens, n_seqs, segment_tokens, groups, P) != KDA_OK) return 0;
+  return P.total + HOST_ALIGN;
+}
+
+int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,
+                       const float* initial_state, float* final_state, int32_t segment_tokens,
+                       int32_t groups, void* workspace, size_t workspace_bytes, void* stream) {
+  HostPlan P;
+  int rc = plan_host(x, cu_seqlens, n_seqs, segment_tokens, groups, P);
+  if (rc) return rc;
+  if (x->t_total > 0 && !out) return fail(KDA_ERR_INVALID_ARGUMENT, "out must not be NULL.");
+  if (!workspace || workspace_bytes < P.total + HOST_ALIGN)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "workspace needs %zu bytes (got %zu).", P.total + HOST_ALIGN,
+                workspace ? workspace_bytes : (size_t)0);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(KDA_ERR_CUDA, "device ordinal %d out of range.", dev);
+  HostCtx& c = g_host_ctx[dev];
+  std::lock_guard<std::mutex> lock(c.mu);
+  rc = host_ctx_ready(c, 2 * (size_t)P.n_calls + 3, P.meta_ints);
+  if (rc) return rc;
+  const int64_t hqk = x->hqk, hv = x->hv, D = kda::D, es = 2;
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(workspace) + HOST_ALIGN - 1) / HOST_ALIGN * HOST_ALIGN);
+  float* cache = reinterpret_cast<float*>(base + P.off_cache);
+  const size_t state_bytes = (size_t)n_seqs * hv * D * D * 4;
+  // the call tables: cu_seqlens of the packed call, then its sequences' cache rows
+  for (int j = 0; j < P.n_calls; ++j) {
+    int32_t* cu = c.meta + P.call_meta[j];
+    int32_t* idx = cu + P.call_n[j] + 1;
+    int n = 0, acc = 0;
+    cu[0] = 0;
+    for (int b = 0; b < n_seqs; ++b) {
+      if (P.len[b] <= (int64_t)j * P.L) continue;
+      acc += (int)std::min<int64_t>(P.L, P.len[b] - (int64_t)j * P.L);
+      idx[n] = b;
+      cu[++n] = acc;
+    }
+  }
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  cudaEvent_t ev_start = c.ev[0], ev_end = c.ev[1], ev_init = c.ev[2];
+  auto step = [&](cudaError_t r, const char* what) {
+    if (r != cudaSuccess && rc == KDA_OK) rc = cuda_fail(r, what);
+    return rc == KDA_OK;
+  };
+  step(cudaEventRecord(ev_start, user), "cudaEventRecord");
+  for (cudaStream_t s : {c.s_in, c.s_comp, c.s_out}) step(cudaStreamWaitEvent(s, ev_start, 0), "cudaStreamWaitEvent");
+  if (rc) return rc;
+  if (P.meta_ints)
+    step(cudaMemcpyAsync(base + P.off_meta, c.meta, P.meta_ints * 4, cudaMemcpyHostToDevice, c.s_in), "tables");
+  step(cudaEventRecord(c.meta_done, c.s_in), "cudaEventRecord");
+  c.meta_used = true;
+  if (x->A_log) {
+    step(cudaMemcpyAsync(base + P.off_alog, x->A_log, hv * 4, cudaMemcpyHostToDevice, c.s_in), "A_log");
+    step(cudaMemcpyAsync(base + P.off_dt, x->dt_bias, hv * D * 4, cudaMemcpyHostToDevice, c.s_in), "dt_bias");
+  }
+  if (initial_state)
+    step(cudaMemcpyAsync(cache, initial_state, state_bytes, cudaMemcpyHostToDevice, c.s_in), "initial_state");
+  else
+    step(cudaMemsetAsync(cache, 0, state_bytes, c.s_in), "zero initial state");
+
+  struct Band { const void* host; int64_t tok_stride, width; size_t off; };
+  const Band bands[5] = {{x->q, x->q_stride_tok, hqk * D, P.off_q}, {x->k, x->k_stride_tok, hqk * D, P.off_k},
+                         {x->v, x->v_stride_tok, hv * D, P.off_v}, {x->g, x->g_stride_tok, hv * D, P.off_g},
+                         {x->beta, x->beta_stride_tok, hv, P.off_b}};
+  const int64_t out_row = hv * D * es;
+  for (int j = 0; j < P.n_calls && rc == KDA_OK; ++j) {
+    cudaEvent_t ev_in = c.ev[3 + 2 * j], ev_comp = c.ev[4 + 2 * j];
+    const int64_t jL = (int64_t)j * P.L;
+    const int64_t piece0 = std::min<int64_t>(P.L, P.len[0] - jL);
+    // copy in: a dense call's pieces are evenly spaced, one 2-D copy per band
+    for (const Band& bd : bands) {
+      const size_t rb = bd.width * es, pitch = bd.tok_stride * es;
+      unsigned char* dst = base + bd.off + P.call_row[j] * rb;
+      if (P.dense && pitch == rb && (size_t)P.len[0] * rb < ((size_t)1 << 31)) {
+        const size_t w = piece0 * rb;
+        step(cudaMemcpy2DAsync(dst, w, static_cast<const unsigned char*>(bd.host) + jL * rb, P.len[0] * rb, w,
+                               P.call_n[j], cudaMemcpyHostToDevice, c.s_in), "copy in");
+        continue;
+      }
+      for (int b = 0; b < n_seqs; ++b) {
+        if (P.len[b] <= jL) continue;
+        const int64_t piece = std::min<int64_t>(P.L, P.len[b] - jL);
+        step(copy_rows(dst, static_cast<const unsigned char*>(bd.host) + (P.start[b] + jL) * pitch, rb, pitch,
+                       piece, cudaMemcpyHostToDevice, c.s_in), "copy in");
+        dst += piece * rb;
+      }
+    }
+    step(cudaEventRecord(ev_in, c.s_in), "cudaEventRecord");
+    step(cudaStreamWaitEvent(c.s_comp, ev_in, 0), "cudaStreamWaitEvent");
+    if (rc) break;
+    // compute: the packed call against the cache rows of its sequences
+    kda_activations xd = *x;
+    xd.q = base + P.off_q + P.call_row[j] * hqk * D * es;
+    xd.k = base + P.off_k + P.call_row[j] * hqk * D * es;
+    xd.v = base + P.off_v + P.call_row[j] * hv * D * es;
+    xd.g = base + P.off_g + P.call_row[j] * hv * D * es;
+    xd.beta = base + P.off_b + P.call_row[j] * hv * es;
+    xd.q_stride_tok = xd.k_stride_tok = hqk * D;
+    xd.v_stride_tok = xd.g_stride_tok = hv * D;
+    xd.q_stride_head = xd.k_stride_head = xd.v_stride_head = xd.g_stride_head = D;
+    xd.beta_stride_tok = hv;
+    xd.beta_stride_head = 1;
+    xd.A_log = x->A_log ? reinterpret_cast<const float*>(base + P.off_alog) : nullptr;
+    xd.dt_bias = x->A_log ? reinterpret_cast<const float*>(base + P.off_dt) : nullptr;
+    xd.t_total = P.call_rows[j];
+    const int32_t* mcu = reinterpret_cast<const int32_t*>(base + P.off_meta) + P.call_meta[j];
+    unsigned char* out_dev = base + P.off_o + P.call_row[j] * out_row;
+    rc = chunk_common(&xd, out_dev, P.call_dense[j] ? nullptr : mcu, P.call_n[j], nullptr, nullptr, cache,
+                      hv * D * D, n_seqs, mcu + P.call_n[j] + 1, nullptr, nullptr, 0, 0, nullptr, nullptr,
+                      nullptr, groups, base + P.off_ws, P.call_ws[j], c.s_comp);
+    step(cudaEventRecord(ev_comp, c.s_comp), "cudaEventRecord");
+    step(cudaStreamWaitEvent(c.s_out, ev_comp, 0), "cudaStreamWaitEvent");
+    if (rc) break;
+    // copy out: the call's output rows back to their tokens
+    if (P.dense && (size_t)P.len[0] * out_row < ((size_t)1 << 31)) {
+      const size_t w = piece0 * out_row;
+      step(cudaMemcpy2DAsync(static_cast<unsigned char*>(out) + jL * out_row, P.len[0] * out_row, out_dev, w, w,
+                             P.call_n[j], cudaMemcpyDeviceToHost, c.s_out), "copy out");
+      continue;
+    }
+    for (int b = 0; b < n_seqs; ++b) {
+      if (P.len[b] <= jL) continue;
+      const int64_t piece = std::min<int64_t>(P.L, P.len[b] - jL);
+      step(cudaMemcpyAsync(static_cast<unsigned char*>(out) + (P.start[b] + jL) * out_row, out_dev,
+                           piece * out_row, cudaMemcpyDeviceToHost, c.s_out), "copy out");
+      out_dev += piece * out_row;
+    }
+  }
+  // join: copy-out after every copy-in and compute, the caller's stream after copy-out
+  const int keep = rc;
+  rc = KDA_OK;
+  step(cudaEventRecord(ev_init, c.s_in), "cudaEventRecord");
+  step(cudaStreamWaitEvent(c.s_out, ev_init, 0), "cudaStreamWaitEvent");
+  if (keep == KDA_OK && final_state)
+    step(cudaMemcpyAsync(final_state, cache, state_bytes, cudaMemcpyDeviceToHost, c.s_out), "final_state");
+  step(cudaEventRecord(ev_end, c.s_comp), "cudaEventRecord");
+  step(cudaStreamWaitEvent(c.s_out, ev_end, 0), "cudaStreamWaitEvent");
+  step(cudaEventRecord(ev_end, c.s_out), "cudaEventRecord");
+  step(cudaStreamWaitEvent(user, ev_end, 0), "cudaStreamWaitEvent");
+  if (keep != KDA_OK) return keep;
+  return rc == KDA_OK ? ok() : rc;
 }
 
 static int window_common(const kda_activations* x, void* out, const void* pool, int64_t slot_stride,

@@ -270,3 +270,34 @@ def test_commit_validation():
     assert commit_ex(2, 0) == INVALID and "state_bf16 and kg_fp16" in _msg()
     assert commit_ex(0, 3) == INVALID and "state_bf16 and kg_fp16" in _msg()
     assert commit_ex(1, 0, stride=4 * 16384 + 4) == INVALID and "multiple of 8" in _msg()
+
+
+def _host_call(a, cu=None, n=1, segment=0, ws_bytes=1 << 40):
+    lib = _native.lib()
+    return lib.kda_chunk_fwd_host(ctypes.byref(a), FAKE, cu, n, None, None, segment, 0, FAKE, ws_bytes, None)
+
+
+def test_host_prefill_validation():
+    """The host-memory prefill's own rules, checked before any CUDA call."""
+    lib = _native.lib()
+    a = _acts(t_total=128)
+    assert _host_call(a, segment=100) == INVALID and "segment_tokens" in _msg()
+    assert _host_call(_acts(t_total=128, state_bf16=1)) == INVALID and "fp32 states" in _msg()
+    assert _host_call(_acts(t_total=128, q_stride_head=256, q_stride_tok=512)) == INVALID
+    assert "contiguous heads" in _msg()
+    assert _host_call(_acts(t_total=128, v_stride_tok=128)) == INVALID and "token strides" in _msg()
+    bad = (ctypes.c_int32 * 3)(0, 100, 90)
+    assert _host_call(_acts(t_total=90), cu=bad, n=2) == INVALID and "non-decreasing" in _msg()
+    short = (ctypes.c_int32 * 3)(0, 10, 80)
+    assert _host_call(_acts(t_total=90), cu=short, n=2) == INVALID and "0 to t_total" in _msg()
+    assert _host_call(_acts(t_total=129), n=2) == INVALID and "divisible" in _msg()
+    assert _host_call(a, ws_bytes=64) == INVALID and "workspace needs" in _msg()
+    # the size query: mirrors of every band and the output, the carried
+    # states, per-call tables and one call's prefill scratch
+    cu = (ctypes.c_int32 * 3)(0, 100, 128)
+    need = lib.kda_chunk_fwd_host_workspace_bytes(ctypes.byref(a), cu, 2, 64, 0)
+    T, hqk, hv = 128, 2, 4
+    mirrors = T * (2 * hqk + 3 * hv) * 128 * 2 + T * hv * 2
+    assert need > mirrors + 2 * hv * 128 * 128 * 4
+    assert lib.kda_chunk_fwd_host_workspace_bytes(ctypes.byref(a), cu, 2, 100, 0) == 0
+    assert "segment_tokens" in _msg()
