@@ -108,8 +108,8 @@ def _decode(x, verify=False, table=None, acc=None):
     return out, pool, corr, kg
 
 
-@pytest.mark.parametrize("act,state,window", [(F16, F32, 4), (BF16, BF16, 1), (BF16, BF16, 4),
-                                              (F16, BF16, 8)])
+@pytest.mark.parametrize("act,state,window", [(F16, F32, 1), (F16, F32, 4), (BF16, BF16, 1), (BF16, BF16, 4),
+                                              (F16, BF16, 1), (F16, BF16, 8)])
 def test_decode_dtypes(act, state, window):
     qlens = [window, 1, 0, max(1, window - 1), window, 2 if window > 1 else 1]
     x = W.decode_batch(6, window, 2, 4, slots=17, seed=43 + window, qlens=qlens, null_requests=(4,),
