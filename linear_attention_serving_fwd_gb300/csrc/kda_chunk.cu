@@ -345,6 +345,9 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   uint32_t bar_phase = 0, tile_phase = 0, tiles_issued = 1;
   int cur = 0;
   for (int t = blockIdx.x; t < n_items; t += gridDim.x, cur ^= 1) {
+    // this CTA's last item: the walk may start its setup on the SMs that
+    // finish first (it waits for this grid before reading any record)
+    if (t + (int)gridDim.x >= n_items) griddep_launch_dependents();
     const int4 meta = s.meta[cur];
     const int c_glob = meta.x, h = meta.y, len = meta.w;
     const float a_h = p.has_gate ? __expf(sc.alog) : 0.f;
@@ -989,9 +992,12 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     const int half = tid == 0 ? 0 : (tid == 32 ? 1 : -1);
     float S[16];
     {
-      // pass two of a group scan starts from the composed state (fp32); a
-      // serial walk from the sequence's initial state (state dtype)
+      // pass two of a group scan starts from the composed state (fp32),
+      // written by the kernel before this one; a serial walk from the
+      // sequence's initial state (state dtype), which no kernel of this call
+      // writes, so it is read before the wait
       const float* gsrc = (mode == 0 && p.groups > 1) ? p.gS + plane : nullptr;
+      if (gsrc) griddep_wait();
       const int64_t ioff = (mode == 0 && p.groups == 1) ? initial_state_off(p, n, h) : -1;
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
@@ -1002,6 +1008,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         else if (ioff >= 0) x = state_load(p, init_base(p), ioff + (int64_t)col * D + k);
         S[v] = x;
       }
+      if (!gsrc) griddep_wait();
     }
     // fp16 S^T block: thread (k, ch) writes its 16 columns as two 8-column chunks
     auto write_s16 = [&](int sb) {
@@ -1110,6 +1117,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     }
   } else if (warp < 12) {
     // ---------------- output rows: O[b] lanes 16 q .. 16 q + 15 --------------
+    griddep_wait();
     const int q = warp - 8, r = 16 * q + (lane & 15);
     for (int it = 0; outp && it < nch; ++it) {
       const int ob = it & 1;
@@ -1145,7 +1153,10 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     }
   } else if (warp == 12) {
     // ---------------- loaders: lane 0 the chain's part, lane 16 the output's;
-    // each also warms L2 with the record it will load LOOKAHEAD chunks later
+    // each also warms L2 with the record it will load LOOKAHEAD chunks later.
+    // The records come from the kernel before this one, which may still be
+    // finishing under a programmatic launch.
+    griddep_wait();
     constexpr int LOOKAHEAD = 4;
     if (lane == 0) {
       for (int it = 0; it < nch; ++it) {
@@ -1179,6 +1190,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
     }
   } else if (!ident) {
     // ---------------- R v one chunk ahead, and qg' S ----------------
+    griddep_wait();
     if (lane == 0) {
       auto issue_rv = [&](int it) {  // RV[it & 1] = R_it v_it
         const int ab = it % 3;
@@ -1370,10 +1382,25 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   trace_end(stream);
   // the conv history of every sequence has been read: roll the conv state
   if (p.conv.state && launch_conv_prefill_state(p, stream) != 0) return -1;
+  // the walks are launched programmatically: a walk CTA sets up (TMEM,
+  // barriers, its initial state) while the kernel before it finishes, and
+  // waits for that kernel before its first read of what it wrote
+  auto launch_walk = [&](dim3 grid, int mode) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(WALK_THREADS);
+    cfg.dynamicSmemBytes = sizeof(WalkSmem);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_walk_kernel, p, mode);
+  };
   if (p.groups > 1) {
     trace_begin("kda_walk_pass1", stream);
-    kda_walk_kernel<<<dim3(2 * D / NB, p.hv, p.n_seqs * p.groups), WALK_THREADS,
-                      sizeof(WalkSmem), stream>>>(p, 1);
+    if (launch_walk(dim3(2 * D / NB, p.hv, p.n_seqs * p.groups), 1) != cudaSuccess) return -1;
     trace_end(stream);
     trace_begin("kda_group_compose", stream);
     kda_compose_kernel<<<dim3(D / NB, p.hv, p.n_seqs), COMPOSE_THREADS,
@@ -1381,8 +1408,7 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     trace_end(stream);
   }
   trace_begin("kda_walk", stream);
-  kda_walk_kernel<<<dim3(D / NB, p.hv, p.n_seqs * p.groups), WALK_THREADS, sizeof(WalkSmem),
-                    stream>>>(p, 0);
+  if (launch_walk(dim3(D / NB, p.hv, p.n_seqs * p.groups), 0) != cudaSuccess) return -1;
   trace_end(stream);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
