@@ -296,14 +296,4 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Programmatic dependent launch.  griddep_launch_dependents: this CTA lets the
-// next kernel of the stream (launched with programmatic stream serialization)
-// be scheduled once every CTA of this grid has said so or exited.
-// griddep_wait: wait until the kernels this one depends on have completed and
-// their memory is visible (returns at once without a programmatic launch).
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 }  // namespace kda
