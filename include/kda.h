@@ -284,8 +284,11 @@ int kda_chunk_fwd_noalloc(const kda_activations* x, void* out, const int32_t* cu
  *                   NULL for n_seqs dense sequences of T / n_seqs tokens
  *   initial_state   host fp32 [n_seqs, Hv, 128, 128], or NULL (zero start)
  *   final_state     host fp32 [n_seqs, Hv, 128, 128], or NULL (dropped)
- *   segment_tokens  a positive multiple of 64, or <= 0: about a quarter of
- *                   the longest sequence, between 256 and 4096
+ *   segment_tokens  a positive multiple of 64: segments of that length; or
+ *                   <= 0: segments shrinking towards the end (from the end
+ *                   256, 256, 512, 1024, .. doubling up to 4096 tokens, the
+ *                   first taking the rest), so the last call, which no copy
+ *                   hides, is short
  *   groups          as kda_chunk_fwd, per call
  *   workspace       device memory of at least
  *                   kda_chunk_fwd_host_workspace_bytes(..) bytes: the

@@ -415,7 +415,8 @@ constexpr size_t HOST_ALIGN = 256;
 size_t align_up(size_t n) { return (n + HOST_ALIGN - 1) / HOST_ALIGN * HOST_ALIGN; }
 
 struct HostPlan {
-  int L = 0, n_calls = 0;
+  int n_calls = 0;
+  std::vector<int64_t> bnd;                // call j covers tokens bnd[j] .. bnd[j+1] of each sequence
   bool dense = false;                      // n_seqs sequences of t_total / n_seqs tokens
   std::vector<int64_t> start, len;         // per sequence, host rows
   std::vector<int32_t> call_n, call_rows;  // per call: sequences, tokens
@@ -470,24 +471,39 @@ int plan_host(const kda_activations* x, const int32_t* cu, int32_t n_seqs, int32
   }
   int64_t max_len = 0;
   for (int64_t l : P.len) max_len = l > max_len ? l : max_len;
-  // by default about four segments of the longest sequence, 256 .. 4096
-  // tokens (B=2 x 4096 tokens, H=16 on GB300: 1.13 ms at one segment,
-  // 0.95 at two, 0.89 at four, 0.90 at eight, 1.01 at sixteen)
-  int64_t L = segment;
-  if (L <= 0) {
-    L = (max_len / 4 + kda::CHUNK - 1) / kda::CHUNK * kda::CHUNK;
-    L = L < 256 ? 256 : (L > 4096 ? 4096 : L);
+  // Segment boundaries.  Given a length: uniform.  By default: shrinking
+  // towards the end, so that the last call's prefill and output copy, the
+  // part no later copy hides, are short, while each call's prefill still
+  // fits under the next call's copy-in (a prefill segment here runs about
+  // twice as fast as the host link delivers its rows): from the end 256,
+  // 256, 512, 1024, ... doubling up to 4096 tokens, the first segment taking
+  // the rest.  (B=2 x 4096 tokens, H=16 on GB300: 1.13 ms a step as one
+  // segment, 0.89 in four of 1024.)
+  P.bnd.assign(1, 0);
+  if (segment > 0) {
+    for (int64_t b = segment; b - segment < max_len; b += segment) P.bnd.push_back(b);
+  } else if (max_len > 0) {
+    std::vector<int64_t> tail;  // segment lengths from the end
+    int64_t covered = 0, next = 256;
+    while (covered < max_len) {
+      tail.push_back(next);
+      covered += next;
+      if (tail.size() >= 2) next = std::min<int64_t>(2 * next, 4096);
+    }
+    for (size_t i = tail.size(); i-- > 0;) P.bnd.push_back(P.bnd.back() + tail[i]);
+    // the first segment shrinks to what the sequence leaves, in whole chunks
+    const int64_t over = (P.bnd.back() - max_len) / kda::CHUNK * kda::CHUNK;
+    for (size_t i = 1; i < P.bnd.size(); ++i) P.bnd[i] -= over;
   }
-  P.L = (int)L;
-  P.n_calls = (int)((max_len + L - 1) / L);
+  P.n_calls = (int)P.bnd.size() - 1;
   int64_t row = 0;
   for (int j = 0; j < P.n_calls; ++j) {
     int32_t n = 0, rows = 0;
     int64_t first = -1;
     bool eq = true;
     for (int b = 0; b < n_seqs; ++b) {
-      if (P.len[b] <= j * L) continue;
-      const int64_t piece = std::min<int64_t>(L, P.len[b] - j * L);
+      if (P.len[b] <= P.bnd[j]) continue;
+      const int64_t piece = std::min<int64_t>(P.bnd[j + 1], P.len[b]) - P.bnd[j];
       if (first < 0) first = piece;
       eq &= piece == first;
       ++n;
@@ -613,8 +629,8 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
     int n = 0, acc = 0;
     cu[0] = 0;
     for (int b = 0; b < n_seqs; ++b) {
-      if (P.len[b] <= (int64_t)j * P.L) continue;
-      acc += (int)std::min<int64_t>(P.L, P.len[b] - (int64_t)j * P.L);
+      if (P.len[b] <= P.bnd[j]) continue;
+      acc += (int)(std::min<int64_t>(P.bnd[j + 1], P.len[b]) - P.bnd[j]);
       idx[n] = b;
       cu[++n] = acc;
     }
@@ -648,8 +664,8 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
   const int64_t out_row = hv * D * es;
   for (int j = 0; j < P.n_calls && rc == KDA_OK; ++j) {
     cudaEvent_t ev_in = c.ev[3 + 2 * j], ev_comp = c.ev[4 + 2 * j];
-    const int64_t jL = (int64_t)j * P.L;
-    const int64_t piece0 = std::min<int64_t>(P.L, P.len[0] - jL);
+    const int64_t jL = P.bnd[j], jR = P.bnd[j + 1];
+    const int64_t piece0 = std::min<int64_t>(jR, P.len[0]) - jL;
     // copy in: a dense call's pieces are evenly spaced, one 2-D copy per band
     for (const Band& bd : bands) {
       const size_t rb = bd.width * es, pitch = bd.tok_stride * es;
@@ -662,7 +678,7 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
       }
       for (int b = 0; b < n_seqs; ++b) {
         if (P.len[b] <= jL) continue;
-        const int64_t piece = std::min<int64_t>(P.L, P.len[b] - jL);
+        const int64_t piece = std::min<int64_t>(jR, P.len[b]) - jL;
         step(copy_rows(dst, static_cast<const unsigned char*>(bd.host) + (P.start[b] + jL) * pitch, rb, pitch,
                        piece, cudaMemcpyHostToDevice, c.s_in), "copy in");
         dst += piece * rb;
@@ -703,7 +719,7 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
     }
     for (int b = 0; b < n_seqs; ++b) {
       if (P.len[b] <= jL) continue;
-      const int64_t piece = std::min<int64_t>(P.L, P.len[b] - jL);
+      const int64_t piece = std::min<int64_t>(jR, P.len[b]) - jL;
       step(cudaMemcpyAsync(static_cast<unsigned char*>(out) + (P.start[b] + jL) * out_row, out_dev,
                            piece * out_row, cudaMemcpyDeviceToHost, c.s_out), "copy out");
       out_dev += piece * out_row;
