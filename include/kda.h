@@ -297,9 +297,10 @@ int kda_chunk_fwd_noalloc(const kda_activations* x, void* out, const int32_t* cu
  *   stream          cudaStream_t
  * The host buffers must stay valid, and the workspace untouched, until
  * ``stream`` reaches the end of this call's work.  Calls on one device share
- * the library streams and one page-locked table buffer, which a call reuses
- * only after the previous call's tables reached the device (it waits on the
- * host for that); not for stream capture.  Device-side rules and error
+ * the library streams and one page-locked buffer, in which a call stages its
+ * call tables, A_log, dt_bias and beta rows for a single copy; a call reuses
+ * it only after the previous call's block reached the device (it waits on
+ * the host for that); not for stream capture.  Device-side rules and error
  * words as kda_chunk_fwd.
  */
 int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_seqlens, int32_t n_seqs,

@@ -425,8 +425,11 @@ struct HostPlan {
   std::vector<int64_t> call_meta;          // per call: int32 offset of its cu_seqlens, then indices
   std::vector<size_t> call_ws;             // per call: chunk workspace bytes
   size_t meta_ints = 0;
-  size_t off_q = 0, off_k = 0, off_v = 0, off_g = 0, off_b = 0, off_o = 0, off_cache = 0, off_alog = 0,
-         off_dt = 0, off_meta = 0, off_ws = 0, total = 0;
+  // the table block, staged page-locked on the host and moved by one copy:
+  // call tables (int32), A_log, dt_bias, beta of every call (call-major)
+  size_t tab_alog = 0, tab_dt = 0, tab_beta = 0, tab_bytes = 0;
+  size_t off_q = 0, off_k = 0, off_v = 0, off_g = 0, off_o = 0, off_cache = 0, off_tab = 0, off_ws = 0,
+         total = 0;
 };
 
 // Validates a host-memory prefill and lays out its calls and workspace.
@@ -526,12 +529,13 @@ int plan_host(const kda_activations* x, const int32_t* cu, int32_t n_seqs, int32
   P.off_k = take(T * hqk * D * es);
   P.off_v = take(T * hv * D * es);
   P.off_g = take(T * hv * D * es);
-  P.off_b = take(T * hv * es);
   P.off_o = take(T * hv * D * es);
   P.off_cache = take((size_t)n_seqs * hv * D * D * 4);
-  P.off_alog = take(x->A_log ? hv * 4 : 0);
-  P.off_dt = take(x->A_log ? hv * D * 4 : 0);
-  P.off_meta = take(P.meta_ints * 4);
+  P.tab_alog = align_up(P.meta_ints * 4);
+  P.tab_dt = align_up(P.tab_alog + (x->A_log ? hv * 4 : 0));
+  P.tab_beta = align_up(P.tab_dt + (x->A_log ? hv * D * 4 : 0));
+  P.tab_bytes = P.tab_beta + T * hv * es;
+  P.off_tab = take(P.tab_bytes);
   size_t ws = 0;
   for (size_t w : P.call_ws) ws = w > ws ? w : ws;
   P.off_ws = take(ws);
@@ -544,14 +548,14 @@ struct HostCtx {
   bool ready = false;
   cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
   std::vector<cudaEvent_t> ev;
-  int32_t* meta = nullptr;  // page-locked staging of the call tables
-  size_t meta_cap = 0;      // ints
+  unsigned char* meta = nullptr;  // page-locked staging of the table block
+  size_t meta_cap = 0;            // bytes
   cudaEvent_t meta_done = nullptr;
   bool meta_used = false;
 };
 HostCtx g_host_ctx[64];
 
-int host_ctx_ready(HostCtx& c, size_t events, size_t meta_ints) {
+int host_ctx_ready(HostCtx& c, size_t events, size_t meta_bytes) {
   cudaError_t e = cudaSuccess;
   if (!c.ready) {
     if ((e = cudaStreamCreateWithFlags(&c.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
@@ -570,12 +574,12 @@ int host_ctx_ready(HostCtx& c, size_t events, size_t meta_ints) {
   // the previous call's tables have left the staging buffer
   if (c.meta_used && (e = cudaEventSynchronize(c.meta_done)) != cudaSuccess)
     return cuda_fail(e, "host prefill tables");
-  if (meta_ints > c.meta_cap) {
+  if (meta_bytes > c.meta_cap) {
     if (c.meta) cudaFreeHost(c.meta);
     c.meta = nullptr;
     c.meta_cap = 0;
-    const size_t cap = meta_ints < 1024 ? 1024 : 2 * meta_ints;
-    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c.meta), cap * 4, cudaHostAllocDefault)) != cudaSuccess)
+    const size_t cap = meta_bytes < 4096 ? 4096 : 2 * meta_bytes;
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c.meta), cap, cudaHostAllocDefault)) != cudaSuccess)
       return cuda_fail(e, "host prefill tables");
     c.meta_cap = cap;
   }
@@ -615,7 +619,7 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
   if (dev < 0 || dev >= 64) return fail(KDA_ERR_CUDA, "device ordinal %d out of range.", dev);
   HostCtx& c = g_host_ctx[dev];
   std::lock_guard<std::mutex> lock(c.mu);
-  rc = host_ctx_ready(c, 2 * (size_t)P.n_calls + 3, P.meta_ints);
+  rc = host_ctx_ready(c, 2 * (size_t)P.n_calls + 3, P.tab_bytes);
   if (rc) return rc;
   const int64_t hqk = x->hqk, hv = x->hv, D = kda::D, es = 2;
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -624,7 +628,7 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
   const size_t state_bytes = (size_t)n_seqs * hv * D * D * 4;
   // the call tables: cu_seqlens of the packed call, then its sequences' cache rows
   for (int j = 0; j < P.n_calls; ++j) {
-    int32_t* cu = c.meta + P.call_meta[j];
+    int32_t* cu = reinterpret_cast<int32_t*>(c.meta) + P.call_meta[j];
     int32_t* idx = cu + P.call_n[j] + 1;
     int n = 0, acc = 0;
     cu[0] = 0;
@@ -644,29 +648,48 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
   step(cudaEventRecord(ev_start, user), "cudaEventRecord");
   for (cudaStream_t s : {c.s_in, c.s_comp, c.s_out}) step(cudaStreamWaitEvent(s, ev_start, 0), "cudaStreamWaitEvent");
   if (rc) return rc;
-  if (P.meta_ints)
-    step(cudaMemcpyAsync(base + P.off_meta, c.meta, P.meta_ints * 4, cudaMemcpyHostToDevice, c.s_in), "tables");
+  // the gate parameters and every call's beta rows (call-major) join the
+  // tables: each copy costs the copy engine a few microseconds on top of
+  // its bytes, so the small ones travel as one
+  if (x->A_log) {
+    memcpy(c.meta + P.tab_alog, x->A_log, hv * 4);
+    memcpy(c.meta + P.tab_dt, x->dt_bias, hv * D * 4);
+  }
+  {
+    const size_t rb = hv * es, pitch = x->beta_stride_tok * es;
+    unsigned char* dst = c.meta + P.tab_beta;
+    for (int j = 0; j < P.n_calls; ++j)
+      for (int b = 0; b < n_seqs; ++b) {
+        if (P.len[b] <= P.bnd[j]) continue;
+        const int64_t piece = std::min<int64_t>(P.bnd[j + 1], P.len[b]) - P.bnd[j];
+        const unsigned char* src = static_cast<const unsigned char*>(x->beta) + (P.start[b] + P.bnd[j]) * pitch;
+        if (pitch == rb) {
+          memcpy(dst, src, piece * rb);
+          dst += piece * rb;
+        } else {
+          for (int64_t r = 0; r < piece; ++r, dst += rb) memcpy(dst, src + r * pitch, rb);
+        }
+      }
+  }
+  if (P.tab_bytes)
+    step(cudaMemcpyAsync(base + P.off_tab, c.meta, P.tab_bytes, cudaMemcpyHostToDevice, c.s_in), "tables");
   step(cudaEventRecord(c.meta_done, c.s_in), "cudaEventRecord");
   c.meta_used = true;
-  if (x->A_log) {
-    step(cudaMemcpyAsync(base + P.off_alog, x->A_log, hv * 4, cudaMemcpyHostToDevice, c.s_in), "A_log");
-    step(cudaMemcpyAsync(base + P.off_dt, x->dt_bias, hv * D * 4, cudaMemcpyHostToDevice, c.s_in), "dt_bias");
-  }
   if (initial_state)
     step(cudaMemcpyAsync(cache, initial_state, state_bytes, cudaMemcpyHostToDevice, c.s_in), "initial_state");
   else
     step(cudaMemsetAsync(cache, 0, state_bytes, c.s_in), "zero initial state");
 
   struct Band { const void* host; int64_t tok_stride, width; size_t off; };
-  const Band bands[5] = {{x->q, x->q_stride_tok, hqk * D, P.off_q}, {x->k, x->k_stride_tok, hqk * D, P.off_k},
-                         {x->v, x->v_stride_tok, hv * D, P.off_v}, {x->g, x->g_stride_tok, hv * D, P.off_g},
-                         {x->beta, x->beta_stride_tok, hv, P.off_b}};
+  const Band bands[4] = {{x->q, x->q_stride_tok, hqk * D, P.off_q}, {x->k, x->k_stride_tok, hqk * D, P.off_k},
+                         {x->v, x->v_stride_tok, hv * D, P.off_v}, {x->g, x->g_stride_tok, hv * D, P.off_g}};
   const int64_t out_row = hv * D * es;
   for (int j = 0; j < P.n_calls && rc == KDA_OK; ++j) {
     cudaEvent_t ev_in = c.ev[3 + 2 * j], ev_comp = c.ev[4 + 2 * j];
     const int64_t jL = P.bnd[j], jR = P.bnd[j + 1];
     const int64_t piece0 = std::min<int64_t>(jR, P.len[0]) - jL;
-    // copy in: a dense call's pieces are evenly spaced, one 2-D copy per band
+    // copy in (q, k, v, g; beta came with the tables): a dense call's pieces
+    // are evenly spaced, one 2-D copy per band
     for (const Band& bd : bands) {
       const size_t rb = bd.width * es, pitch = bd.tok_stride * es;
       unsigned char* dst = base + bd.off + P.call_row[j] * rb;
@@ -693,16 +716,16 @@ int kda_chunk_fwd_host(const kda_activations* x, void* out, const int32_t* cu_se
     xd.k = base + P.off_k + P.call_row[j] * hqk * D * es;
     xd.v = base + P.off_v + P.call_row[j] * hv * D * es;
     xd.g = base + P.off_g + P.call_row[j] * hv * D * es;
-    xd.beta = base + P.off_b + P.call_row[j] * hv * es;
+    xd.beta = base + P.off_tab + P.tab_beta + P.call_row[j] * hv * es;
     xd.q_stride_tok = xd.k_stride_tok = hqk * D;
     xd.v_stride_tok = xd.g_stride_tok = hv * D;
     xd.q_stride_head = xd.k_stride_head = xd.v_stride_head = xd.g_stride_head = D;
     xd.beta_stride_tok = hv;
     xd.beta_stride_head = 1;
-    xd.A_log = x->A_log ? reinterpret_cast<const float*>(base + P.off_alog) : nullptr;
-    xd.dt_bias = x->A_log ? reinterpret_cast<const float*>(base + P.off_dt) : nullptr;
+    xd.A_log = x->A_log ? reinterpret_cast<const float*>(base + P.off_tab + P.tab_alog) : nullptr;
+    xd.dt_bias = x->A_log ? reinterpret_cast<const float*>(base + P.off_tab + P.tab_dt) : nullptr;
     xd.t_total = P.call_rows[j];
-    const int32_t* mcu = reinterpret_cast<const int32_t*>(base + P.off_meta) + P.call_meta[j];
+    const int32_t* mcu = reinterpret_cast<const int32_t*>(base + P.off_tab) + P.call_meta[j];
     unsigned char* out_dev = base + P.off_o + P.call_row[j] * out_row;
     rc = chunk_common(&xd, out_dev, P.call_dense[j] ? nullptr : mcu, P.call_n[j], nullptr, nullptr, cache,
                       hv * D * D, n_seqs, mcu + P.call_n[j] + 1, nullptr, nullptr, 0, 0, nullptr, nullptr,
