@@ -95,3 +95,30 @@ def test_full_dense_workload_matches_device_path():
     assert torch.allclose(oh, od, rtol=2e-2, atol=2e-3), float((oh - od).abs().max())
     rel = float((fin_h - fin_d.cpu()).norm() / fin_d.norm().cpu())
     assert rel < 1e-4, rel
+
+
+def test_fp16_activations_default_segments():
+    """fp16 q/k/v/g/beta and output through the default (shrinking)
+    segments: one sequence of 300 tokens runs as segments of 64 and 236
+    tokens (a 256-token segment cut short by the sequence's end)."""
+    x = W.dense_prefill(1, 300, 2, 2, seed=8, lower_bound=-0.3, state_std=0.2, act_dtype=torch.float16)
+    ref = oracle.prefill(x)
+    out, fin = _host(x, segment=0, dense=True)
+    assert out.dtype == torch.float16
+    check_out(out, ref["out"], "host fp16 out")
+    check_state(fin, ref["state"], "host fp16 final state")
+
+
+def test_empty_batch_returns_initial_states():
+    """Every sequence empty: no segment call runs; the final states are the
+    initial ones and the output is empty."""
+    import linear_attention_serving_fwd_gb300 as kda
+    x = W.dense_prefill(2, 64, 1, 2, seed=9)
+    e = lambda t: t[:0].pin_memory()
+    h0 = x.initial_state.contiguous().pin_memory()
+    out, fin = kda.kda_chunk_fwd_host(e(x.q), e(x.k), e(x.v), e(x.g), e(x.beta), A_log=x.A_log,
+                                      dt_bias=x.dt_bias, cu_seqlens=torch.zeros(3, dtype=torch.int32),
+                                      initial_state=h0, output_final_state=True)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 2, 128)
+    assert torch.equal(fin, h0)
