@@ -613,20 +613,25 @@ __device__ __forceinline__ unsigned char* conv_stage(const WindowParams& p, unsi
   return (p.conv.state && p.conv.bulk) ? extra + b * CONV_STAGE_BYTES : nullptr;
 }
 
-// WR = 8: one state buffer, the next item's state streams in while an item
-// runs; the new state is stored from registers.  WR = 4 (decode only): two
-// state buffers, the state two items ahead streams in, and the new state
-// leaves through a staging buffer by two bulk stores, so no thread waits on
-// its write.
-template <bool VERIFY, bool SBF16, bool FP16, int WR>
+// WR = 8: one fp32 state buffer, the next item's state streams in while an
+// item runs; a bf16 state is half the size, so for one-token windows (which
+// wait on bytes, not on compute) the buffer holds two and the state two
+// items ahead streams in.  The new state is stored from registers.
+// WR = 4 (decode only): two state buffers, the state two items ahead streams
+// in, and the new state leaves through a staging buffer by two bulk stores,
+// so no thread waits on its write.
+template <bool VERIFY, bool SBF16, bool FP16, int WR, int NBUF>
 __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window_kernel(const WindowParams p) {
   static_assert(WR == 8 || (WR == 4 && !VERIFY), "verify runs the WR = 8 layout");
-  constexpr int NBUF = WR == 8 ? 1 : 2;
+  static_assert((WR == 4 && NBUF == 2) || (WR == 8 && (NBUF == 1 || SBF16)), "state buffers of the layout");
   constexpr int THREADS = win_threads<WR>();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   WinSmem& s = *reinterpret_cast<WinSmem*>(smem_raw);
   unsigned char* const extra = smem_raw + sizeof(WinSmem);
-  auto state_buf = [&](int k) -> float* { return k == 0 ? s.state : reinterpret_cast<float*>(extra); };
+  auto state_buf = [&](int k) -> float* {
+    if (WR == 8) return s.state + k * (D * D / 2);  // bf16: two states in the buffer
+    return k == 0 ? s.state : reinterpret_cast<float*>(extra);
+  };
   float* const sout = reinterpret_cast<float*>(extra + STATE_BYTES);  // WR = 4
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = p.n_req * p.hv;
@@ -796,21 +801,21 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
 }
 
 // Host-side launcher (called from the API layer after validation).
-template <bool VERIFY, bool SBF16, bool FP16, int WR>
+template <bool VERIFY, bool SBF16, bool FP16, int WR, int NBUF = (WR == 4 ? 2 : 1)>
 static void launch_window_t(const WindowParams& p, int num_sms, cudaStream_t stream) {
   constexpr int smem = (int)sizeof(WinSmem) + (WR == 8 ? EXTRA_WR8 : EXTRA_WR4);
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR>,
+    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR, NBUF>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR>,
+    cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR, NBUF>,
                          cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     attr = true;
   }
   const int items = p.n_req * p.hv;
   const int slots = (WR == 8 ? 2 : 1) * num_sms;  // resident CTAs
   const int grid = items < slots ? items : slots;
-  kda_window_kernel<VERIFY, SBF16, FP16, WR><<<grid, win_threads<WR>(), smem, stream>>>(p);
+  kda_window_kernel<VERIFY, SBF16, FP16, WR, NBUF><<<grid, win_threads<WR>(), smem, stream>>>(p);
 }
 
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
@@ -822,13 +827,15 @@ int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
   }
   const int items = p.n_req * p.hv;
   if (items == 0) return 0;
-  // decode of one token per request moves the state with almost no compute:
-  // the WR = 4 layout keeps the most bytes in flight (measured faster
-  // there); longer windows and verify overlap two CTAs' compute (WR = 8)
-  const bool wr4 = !verify && p.window == 1;
-  const int variant = (wr4 ? 8 : 0) + (verify ? 4 : 0) + (p.state_bf16 ? 2 : 0) + (p.in_fp16 ? 1 : 0);
+  // decode of one token per request moves the state with almost no
+  // compute: fp32 states run the WR = 4 layout, which keeps the most bytes
+  // in flight; bf16 states (half the bytes) run two CTAs per SM with two
+  // states in each CTA's buffer (0.157 -> 0.136 ms for 8192 items).  Longer
+  // windows and verify overlap two CTAs' compute with one buffer each (WR = 8).
+  const int variant = (verify ? 4 : 0) + (p.state_bf16 ? 2 : 0) + (p.in_fp16 ? 1 : 0);
+  const bool one = !verify && p.window == 1;
   trace_begin(verify ? "kda_verify_window" : "kda_decode_window", stream);
-  switch (variant) {
+  switch (one ? 8 + variant : variant) {
     case 0: launch_window_t<false, false, false, 8>(p, num_sms, stream); break;
     case 1: launch_window_t<false, false, true, 8>(p, num_sms, stream); break;
     case 2: launch_window_t<false, true, false, 8>(p, num_sms, stream); break;
@@ -839,8 +846,8 @@ int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
     case 7: launch_window_t<true, true, true, 8>(p, num_sms, stream); break;
     case 8: launch_window_t<false, false, false, 4>(p, num_sms, stream); break;
     case 9: launch_window_t<false, false, true, 4>(p, num_sms, stream); break;
-    case 10: launch_window_t<false, true, false, 4>(p, num_sms, stream); break;
-    default: launch_window_t<false, true, true, 4>(p, num_sms, stream); break;
+    case 10: launch_window_t<false, true, false, 8, 2>(p, num_sms, stream); break;
+    default: launch_window_t<false, true, true, 8, 2>(p, num_sms, stream); break;
   }
   trace_end(stream);
   // verify with a conv: every history has been read, roll the conv state
