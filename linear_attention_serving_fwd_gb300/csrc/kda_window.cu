@@ -1,5 +1,5 @@
-// Decode (in place) and speculative verify (read only) over a paged fp32
-// state cache, window Q <= 8 tokens per request.
+// Decode (in place) and speculative verify (read only) over a paged fp32 or
+// bf16 state cache, window Q <= 8 tokens per request.
 //
 // Design (memory bound: each (request, head) moves its 64 KB V-first state
 // once in, and for decode once out):
@@ -9,11 +9,13 @@
 //  * two layouts by the state rows WR a thread holds (rows of S^T, 8 key
 //    channels each, so the state lives in 8 WR registers per thread and a
 //    row's dot products reduce over the 16 lanes of a half warp):
-//    - WR = 8 (verify, and decode of windows longer than one token): 256
-//      threads, two CTAs per SM, one state buffer each; the next item's
-//      state streams in while one runs, and the other CTA's work hides each
+//    - WR = 8 (verify, decode of windows longer than one token, and
+//      one-token decode on bf16 states): 256 threads, two CTAs per SM, one
+//      64 KB state buffer each; the next item's state streams in while one
+//      runs (for one-token bf16 decode the buffer holds two states and the
+//      one two items ahead streams in), and the other CTA's work hides each
 //      item's latency chain; decode stores the new state from registers;
-//    - WR = 4 (decode of one token, which only moves bytes): 512 threads,
+//    - WR = 4 (one-token decode on fp32 states, which only moves bytes): 512 threads,
 //      one CTA per SM, two state buffers (the state two items ahead streams
 //      in) and a third for the write-back, which leaves by two bulk stores
 //      so no thread waits on it;
@@ -48,8 +50,8 @@ namespace kda {
 // Two thread layouts, by the state rows WR a thread holds (8 key channels
 // each): WR = 8, 256 threads, two CTAs per SM with one state buffer each;
 // WR = 4, 512 threads, one CTA per SM with two state buffers and a
-// write-back staging buffer (decode of one token, where the kernel only
-// moves bytes and wants the most of them in flight).
+// write-back staging buffer (one-token decode on fp32 states, where the
+// kernel only moves bytes and wants the most of them in flight).
 template <int WR>
 __host__ __device__ constexpr int win_threads() { return 2048 / WR; }
 constexpr int STATE_BYTES = D * D * 4;                // 65536
