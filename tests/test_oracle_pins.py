@@ -55,7 +55,8 @@ def test_gate_golden_values():
         h0 = np.random.default_rng(1).uniform(0.5, 1.5, (1, 1, D, D))
         res = oracle.recurrence(q, k, v, g, b, [0, 1], A_log=A_log, dt_bias=dt,
                                 lower_bound=case["lower_bound"], h0=h0)
-        gate = np.log(res["state"][0, 0] / h0[0, 0])
+        with np.errstate(invalid="ignore", divide="ignore"):  # a planted mistake may give a negative ratio
+            gate = np.log(res["state"][0, 0] / h0[0, 0])
         np.testing.assert_allclose(gate, case["expected_gate"], atol=fx["tolerance"], rtol=0)
 
 
