@@ -35,9 +35,10 @@
 // computed as U = beta (v - S_old^T (e^gate * k^)),
 //             o = S_old^T (e^gate * q~) + U (k^ . q~),  S = e^gate * S_old + k^ U^T.
 // Verify with a conv (the verify page's conv path): q, k, v are the raw
-// projection bands; warp t first convolves token t's rows (width 4, SiLU)
-// with the history at the accepted column, the outputs replace the raw rows,
-// and a small kernel afterwards rolls the conv state.
+// projection bands; each token's rows are first convolved (width 4, SiLU)
+// with the history at the accepted column, by two warps (half the channels
+// each), the outputs replace the raw rows, and a small kernel afterwards
+// rolls the conv state.
 // Verify (the vLLM kimi_k3 CuTeDSL verify page, KdaTcVerify) additionally
 // writes corr = U_t and kg = (raw k_t, raw g_t) and never writes the state;
 // its persistent scheduler takes tickets from a caller-zeroed counter and the
@@ -262,51 +263,52 @@ __device__ __forceinline__ void token_vectors(const WindowParams& p, WinSmem& s,
   }
 }
 
-// Verify with a conv: warp t's conv + SiLU outputs for token t (lane = 4
-// channels of each band: q and k of the head's q/k head, v of the head),
-// from the window's raw rows and, for the taps before the window, the
-// history at positions accepted-1 .. accepted+1 of the slot's conv row.
-__device__ __forceinline__ void conv_token(const WindowParams& p, const ItemInfo& it,
-                                           const __nv_bfloat16* ibuf, const unsigned char* stage, int t,
-                                           int lane, uint2 (&y)[3]) {
+// Verify with a conv: the conv + SiLU outputs of token t for channels c, c+1
+// of each band (q and k of the head's q/k head, v of the head), from the
+// window's raw rows and, for the taps before the window, the history at
+// positions accepted-1 .. accepted+1 of the slot's conv row; rounded to bf16
+// (the convolved rows replace the raw bf16 rows).  The 2 qlen units (token,
+// half of the 128 channels) are spread over the CTA's warps.
+__device__ __forceinline__ void conv_unit(const WindowParams& p, const ItemInfo& it,
+                                          const __nv_bfloat16* ibuf, const unsigned char* stage, int t,
+                                          int c, uint32_t (&y)[3]) {
   const ConvParams& cv = p.conv;
   const int first = cv.accepted[it.request] - 1;
   int64_t ch[3];
-  conv_channels(p.hqk, p.hv, it.head, 4 * lane, ch);
+  conv_channels(p.hqk, p.hv, it.head, c, ch);
   const __nv_bfloat16* hist = cv.state + it.slot * cv.row_st;
 #pragma unroll
   for (int x = 0; x < 3; ++x) {
-    float win[4][4];  // tap j reads token t - 3 + j
+    float2 win[4];  // tap j reads token t - 3 + j
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int tt = t - 3 + j;
       if (tt >= 0) {
-        load_bf16x4(ibuf + (tt * 4 + x) * D + 4 * lane, win[j]);
+        win[j] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(ibuf + (tt * 4 + x) * D + c));
       } else if (cv.bulk) {  // staged history position first + 3 + tt
-        load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + CONV_TAPS_BYTES + (x * 3 + 3 + tt) * 256) +
-                        4 * lane, win[j]);
+        win[j] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+            reinterpret_cast<const __nv_bfloat16*>(stage + CONV_TAPS_BYTES + (x * 3 + 3 + tt) * 256) + c));
       } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          win[j][e] = bf2f(hist[(int64_t)(first + 3 + tt) * cv.pos_st + (ch[x] + e) * cv.ch_st]);
+        const __nv_bfloat16* h = hist + (int64_t)(first + 3 + tt) * cv.pos_st;
+        win[j] = make_float2(bf2f(h[ch[x] * cv.ch_st]), bf2f(h[(ch[x] + 1) * cv.ch_st]));
       }
     }
-    float ye[4];
+    float ye[2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 2; ++e) {
       float4 w;
       if (cv.bulk) {  // staged bf16 taps
         float t4[4];
-        load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + x * 1024 + (4 * lane + e) * 8), t4);
+        load_bf16x4(reinterpret_cast<const __nv_bfloat16*>(stage + x * 1024 + (c + e) * 8), t4);
         w = make_float4(t4[0], t4[1], t4[2], t4[3]);
       } else {
         w = conv_taps(cv, ch[x] + e);
       }
-      ye[e] = conv_silu(cv.w_f32, w, win[0][e], win[1][e], win[2][e], win[3][e]);
+      ye[e] = conv_silu(cv.w_f32, w, e ? win[0].y : win[0].x, e ? win[1].y : win[1].x,
+                        e ? win[2].y : win[2].x, e ? win[3].y : win[3].x);
     }
-    // rounded to bf16 at once (the convolved rows replace the raw bf16 rows)
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(ye[0], ye[1]), hi = __floats2bfloat162_rn(ye[2], ye[3]);
-    y[x] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    const __nv_bfloat162 yy = __floats2bfloat162_rn(ye[0], ye[1]);
+    y[x] = *reinterpret_cast<const uint32_t*>(&yy);
   }
 }
 
@@ -688,18 +690,22 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
     // write-back follow, the token loop measured faster)
     const bool windowed = VERIFY && !SBF16 && it.qlen >= 2 && it.qlen <= 4;
     float2 S[WR][4];
-    uint2 yc[3];  // bf16 conv outputs of token ``warp`` (verify with a conv)
+    uint32_t yc[2][3];  // verify with a conv: this warp's units' bf16 outputs
     if (it.work) {
       ok = mbar_wait_bounded(&s.sbar[sb], sphase[sb], p.err);
       ok = mbar_wait_bounded(&s.ibar[b], iphase[b], p.err) && ok;
       sphase[sb] ^= 1u;
       iphase[b] ^= 1u;
       if (ok) {
-        if (warp < it.qlen) {
-          if (conv)
-            conv_token(p, it, s.in[b], extra + b * CONV_STAGE_BYTES, warp, lane, yc);
-          else if (!windowed)
-            token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        if (conv) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int u = warp + 8 * k;  // unit: token u / 2, channels 64 (u % 2) + 2 lane ..
+            if (u < 2 * it.qlen)
+              conv_unit(p, it, s.in[b], extra + b * CONV_STAGE_BYTES, u >> 1, 64 * (u & 1) + 2 * lane, yc[k]);
+          }
+        } else if (warp < it.qlen && !windowed) {
+          token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
         }
         const float* sbuf = state_buf(sb);
 #pragma unroll
@@ -735,13 +741,19 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
     if (conv && it.work) {
       // every raw row has been read: the conv outputs replace them, then
       // the token vectors come from the convolved rows
-      if (warp < it.qlen) {
 #pragma unroll
-        for (int x = 0; x < 3; ++x) *reinterpret_cast<uint2*>(s.in[b] + (warp * 4 + x) * D + 4 * lane) = yc[x];
-        __syncwarp();
-        if (!windowed) token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+      for (int k = 0; k < 2; ++k) {
+        const int u = warp + 8 * k;
+        if (u < 2 * it.qlen)
+#pragma unroll
+          for (int x = 0; x < 3; ++x)
+            *reinterpret_cast<uint32_t*>(s.in[b] + ((u >> 1) * 4 + x) * D + 64 * (u & 1) + 2 * lane) = yc[k][x];
       }
       __syncthreads();
+      if (!windowed) {
+        if (warp < it.qlen) token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        __syncthreads();
+      }
     }
     // the next item's scalars, used a step from now
     const TokenScalars ts_next = load_token_scalars(p, itn, warp, lane);

@@ -153,6 +153,15 @@ def test_verify_conv_small(taps, dim_first):
     _verify_case(x, taps, dim_first, acc, positions=6)
 
 
+def test_verify_conv_window8():
+    """Windows of up to 8 tokens: 16 (token, channel-half) conv units on the
+    CTA's 8 warps, two per warp; accepted counts up to 8 on a 10-position
+    conv row."""
+    x = W.decode_batch(4, 8, 2, 4, slots=8, seed=35, qlens=[8, 5, 1, 7], lower_bound=-0.6)
+    acc = torch.tensor([1, 8, 3, 6], dtype=torch.int32)
+    _verify_case(x, "bf16", False, acc, positions=10)
+
+
 def test_verify_conv_serving_batch():
     """256 requests x 4 tokens, Hqk=Hv=32, 512-slot pool, accepted counts
     U{1..4}, bf16 taps, token-major conv state of window + 2 positions."""
