@@ -120,6 +120,15 @@ typedef struct kda_activations {
  *   num_accepted  verify: device int32 [n_req]; request b's history is at
  *                 positions num_accepted[b]-1 .. num_accepted[b]+1 of row
  *                 slots[b] (the verify page's accepted tokens)
+ *   scratch, scratch_bytes  prefill: device memory of at least
+ *                 kda_conv_scratch_bytes(t_total, Hqk, Hv) bytes, 16-byte
+ *                 aligned, or NULL.  With it the conv runs once per (token,
+ *                 channel) in a pass of its own that writes the convolved
+ *                 bands there, and the prefill reads them; without it each
+ *                 (chunk, head) item of the prefill convolves its own rows
+ *                 (so under GVA every v-head of a q/k head convolves the q/k
+ *                 rows again).  The results are the same.  Verify: must be
+ *                 NULL.
  * Prefill reads the history at positions 0..2 and leaves sequence n's last
  * three raw inputs there (a sequence shorter than three keeps the tail of
  * its history in front).  Verify leaves the rolled state: positions 0 and 1
@@ -138,7 +147,14 @@ typedef struct kda_conv {
   const int32_t* state_indices;
   const uint8_t* has_initial_state;
   const int32_t* num_accepted;
+  void* scratch;
+  size_t scratch_bytes;
 } kda_conv;
+
+/* kda_conv_scratch_bytes - the conv scratch a prefill of t_total tokens with
+ * Hqk q/k heads and Hv v heads can take: (2*Hqk + Hv)*128 bf16 values a
+ * token.  Returns 0 on invalid sizes. */
+size_t kda_conv_scratch_bytes(int32_t t_total, int32_t hqk, int32_t hv);
 
 /*
  * kda_chunk_workspace_bytes - device scratch needed by kda_chunk_fwd.

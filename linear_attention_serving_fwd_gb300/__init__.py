@@ -26,7 +26,7 @@ from ._native import KdaError
 D = 128
 __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_host", "kda_decode", "kda_decode_steps",
            "kda_verify", "kda_commit", "kda_device_status", "chunk_workspace_bytes",
-           "chunk_fwd_host_workspace_bytes", "KdaError", "library_path"]
+           "chunk_fwd_host_workspace_bytes", "conv_scratch_bytes", "KdaError", "library_path"]
 
 
 def library_path() -> str:
@@ -159,6 +159,11 @@ def _conv(conv_weight, conv_state, conv_dim_first, hqk, hv, *, state_indices=Non
     return cv, keep
 
 
+def conv_scratch_bytes(t_total: int, hqk: int, hv: int) -> int:
+    """Bytes of the optional conv scratch of a prefill with a conv."""
+    return int(_native.lib().kda_conv_scratch_bytes(t_total, hqk, hv))
+
+
 def chunk_workspace_bytes(n_seqs: int, t_total: int, hv: int, groups: int = 0) -> int:
     return int(_native.lib().kda_chunk_workspace_bytes(n_seqs, t_total, hv, groups))
 
@@ -169,7 +174,7 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
                   has_initial_state=None, groups: int = 0, workspace=None, stream=None,
                   checkpoint_state=None, checkpoint_offsets=None, checkpoint_state_indices=None,
                   conv_weight=None, conv_state=None, conv_state_indices=None,
-                  conv_has_initial_state=None, conv_dim_first=False):
+                  conv_has_initial_state=None, conv_dim_first=False, conv_scratch=True):
     """Chunked KDA prefill.  Returns (out, final_state or None).
 
     q, k: [T, Hqk, 128] or [B, T, Hqk, 128]; v, g: [T, Hv, 128]; beta:
@@ -189,7 +194,10 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     ``conv_state_indices`` [N] makes q, k, v the raw projection bands
     (C = (2 Hqk + Hv) * 128): they pass a width-4 depthwise conv and SiLU
     first, and each sequence's conv row is left holding its last three raw
-    inputs.
+    inputs.  ``conv_scratch`` (True: allocated here; or a uint8 CUDA tensor of
+    ``conv_scratch_bytes(T, Hqk, Hv)``) lets the conv run once per (token,
+    channel) in its own pass; False makes each prologue item convolve its
+    own rows.  Both give the same results.
     """
     dense_b = q.shape[0] if q.dim() == 4 else None
     q, k = _as_tokens(q, "q"), _as_tokens(k, "k")
@@ -232,6 +240,11 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
                         state_indices=conv_state_indices, has_initial_state=conv_has_initial_state)
     if cv is not None and conv_state_indices is None:
         raise ValueError("conv_state needs conv_state_indices.")
+    if cv is not None and conv_scratch is not False and conv_scratch is not None:
+        if conv_scratch is True:
+            conv_scratch = torch.empty(conv_scratch_bytes(T, a.hqk, hv), dtype=torch.uint8, device=q.device)
+        cv.scratch, cv.scratch_bytes = conv_scratch.data_ptr(), conv_scratch.numel() * conv_scratch.element_size()
+        cv_keep.append(conv_scratch)
     if checkpoint_state is not None or cv is not None:
         if checkpoint_state is not None:
             if checkpoint_offsets is None:

@@ -28,7 +28,7 @@ EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_veri
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
            "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
            "kda_decode_steps", "kda_verify_ex", "kda_commit_ex", "kda_chunk_fwd_host",
-           "kda_chunk_fwd_host_workspace_bytes")
+           "kda_chunk_fwd_host_workspace_bytes", "kda_conv_scratch_bytes")
 
 
 class KdaActivations(ctypes.Structure):
@@ -57,6 +57,7 @@ class KdaConv(ctypes.Structure):
         ("positions", ctypes.c_int32),
         ("state_indices", ctypes.c_void_p), ("has_initial_state", ctypes.c_void_p),
         ("num_accepted", ctypes.c_void_p),
+        ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t),
     ]
 
 
@@ -83,6 +84,8 @@ def _declare(lib):
     lib.kda_chunk_fwd_host.restype = ctypes.c_int
     lib.kda_chunk_fwd_host_workspace_bytes.argtypes = [A, P, I32, I32, I32]
     lib.kda_chunk_fwd_host_workspace_bytes.restype = SZ
+    lib.kda_conv_scratch_bytes.argtypes = [I32, I32, I32]
+    lib.kda_conv_scratch_bytes.restype = SZ
     lib.kda_decode.argtypes = [A, P, P, I64, I64, P, P, I32, I32, P]
     lib.kda_decode.restype = ctypes.c_int
     lib.kda_decode_steps.argtypes = [A, P, P, I64, I64, P, P, I64, P, I32, I32, P]

@@ -247,6 +247,11 @@ const char* kda_version(void) { return "kda-gb300 0.1 sm_103a"; }
 
 const char* kda_last_error(void) { return g_last_error.c_str(); }
 
+size_t kda_conv_scratch_bytes(int32_t t_total, int32_t hqk, int32_t hv) {
+  if (t_total < 0 || hqk <= 0 || hv <= 0) return 0;
+  return (size_t)t_total * (2 * (size_t)hqk + hv) * kda::D * 2;
+}
+
 size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, int32_t groups) {
   if (n_seqs <= 0 || t_total < 0 || hv <= 0) return 0;
   const int G = choose_groups(n_seqs, t_total, hv, groups);
@@ -276,8 +281,15 @@ static int check_conv(const kda_conv* conv, const kda_activations* x, bool verif
     if (conv->rows < n_slots)
       return fail(KDA_ERR_INVALID_ARGUMENT, "conv state needs a row per state slot (%lld < %lld).",
                   (long long)conv->rows, (long long)n_slots);
+    if (conv->scratch) return fail(KDA_ERR_INVALID_ARGUMENT, "verify takes no conv scratch.");
   } else if (!conv->state_indices) {
     return fail(KDA_ERR_INVALID_ARGUMENT, "prefill with a conv needs conv state_indices.");
+  } else if (conv->scratch) {
+    const size_t need_s = kda_conv_scratch_bytes(x->t_total, x->hqk, x->hv);
+    if (conv->scratch_bytes < need_s)
+      return fail(KDA_ERR_INVALID_ARGUMENT, "conv scratch needs %zu bytes (got %zu).", need_s,
+                  conv->scratch_bytes);
+    if (!aligned16(conv->scratch)) return fail(KDA_ERR_INVALID_ARGUMENT, "conv scratch must be 16-byte aligned.");
   }
   cp.w = conv->weight;
   cp.w_f32 = conv->weight_f32;
@@ -370,6 +382,7 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
   p.ckpt = checkpoint_state; p.ckpt_stride = checkpoint_row_stride; p.ckpt_rows = checkpoint_rows;
   p.ckpt_off = checkpoint_offsets; p.ckpt_idx = checkpoint_state_indices;
   p.conv = cp;
+  p.conv_out = conv ? static_cast<__nv_bfloat16*>(conv->scratch) : nullptr;
   p.err = err;
   const int lrc = kda::launch_chunk(p, workspace, static_cast<cudaStream_t>(stream));
   if (lrc == -2) return KDA_ERR_INVALID_ARGUMENT;  // message set by the launcher

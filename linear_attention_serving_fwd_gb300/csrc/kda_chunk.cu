@@ -1357,13 +1357,28 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
     trace_end(stream);
   }
+  // a conv with a scratch buffer: convolve every (token, channel) once, then
+  // run the plain prologue on the convolved bands (pp); the conv state update
+  // below still reads the raw bands of p
+  ChunkParams pp = p;
+  if (p.conv.state && p.conv_out) {
+    if (launch_conv_prefill(p, stream) != 0) return -1;
+    const int64_t qk = (int64_t)p.hqk * D;
+    pp.q = p.conv_out;
+    pp.k = p.conv_out + (int64_t)p.t_total * qk;
+    pp.v = p.conv_out + 2 * (int64_t)p.t_total * qk;
+    pp.q_st = pp.k_st = qk;
+    pp.v_st = (int64_t)p.hv * D;
+    pp.q_sh = pp.k_sh = pp.v_sh = D;
+    pp.conv.state = nullptr;
+  }
   TileMaps maps;
-  const int qkv_rows = CHUNK + (p.conv.state ? HALO : 0);
-  const bool f16 = p.in_fp16 != 0;
-  if (!encode_rows(&maps.q, p.q, p.hqk, p.t_total, p.q_sh, p.q_st, f16, qkv_rows) ||
-      !encode_rows(&maps.k, p.k, p.hqk, p.t_total, p.k_sh, p.k_st, f16, qkv_rows) ||
-      !encode_rows(&maps.g, p.g, p.hv, p.t_total, p.g_sh, p.g_st, f16) ||
-      !encode_rows(&maps.v, p.v, p.hv, p.t_total, p.v_sh, p.v_st, f16, qkv_rows)) {
+  const int qkv_rows = CHUNK + (pp.conv.state ? HALO : 0);
+  const bool f16 = pp.in_fp16 != 0;
+  if (!encode_rows(&maps.q, pp.q, pp.hqk, pp.t_total, pp.q_sh, pp.q_st, f16, qkv_rows) ||
+      !encode_rows(&maps.k, pp.k, pp.hqk, pp.t_total, pp.k_sh, pp.k_st, f16, qkv_rows) ||
+      !encode_rows(&maps.g, pp.g, pp.hv, pp.t_total, pp.g_sh, pp.g_st, f16) ||
+      !encode_rows(&maps.v, pp.v, pp.hv, pp.t_total, pp.v_sh, pp.v_st, f16, qkv_rows)) {
     set_last_error(KDA_ERR_INVALID_ARGUMENT,
                    "kda_chunk_fwd: q/k/v/g layout cannot be described by a TMA tensor map "
                    "(strides must be positive multiples of 8 elements below 2^39 bytes).");
@@ -1373,12 +1388,12 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   const int items = max_chunks * p.hv;
   const int sms = p.sm_count > 0 ? p.sm_count : 152;
   const int grid = items < sms ? items : sms;
-  if (p.conv.state)  // bf16 activations only (checked by the API layer)
-    kda_prologue_kernel<true, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
-  else if (p.in_fp16)
-    kda_prologue_kernel<false, true><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+  if (pp.conv.state)  // bf16 activations only (checked by the API layer)
+    kda_prologue_kernel<true, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(pp, maps);
+  else if (pp.in_fp16)
+    kda_prologue_kernel<false, true><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(pp, maps);
   else
-    kda_prologue_kernel<false, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(p, maps);
+    kda_prologue_kernel<false, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(pp, maps);
   trace_end(stream);
   // the conv history of every sequence has been read: roll the conv state
   if (p.conv.state && launch_conv_prefill_state(p, stream) != 0) return -1;

@@ -103,6 +103,9 @@ struct ChunkParams {
   const int32_t* ckpt_off;
   const int32_t* ckpt_idx;
   ConvParams conv;
+  __nv_bfloat16* conv_out;     // prefill with a conv: the convolved q, k, v bands ([T, Hqk, 128]
+                               // twice, then [T, Hv, 128]), or null (each prologue item
+                               // convolves its own tiles)
   unsigned* err;        // device error word
 };
 
@@ -119,6 +122,7 @@ void set_last_error(int code, const char* msg);
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream);
 int launch_commit(const CommitParams& p, cudaStream_t stream);
 int launch_conv_prefill_state(const ChunkParams& p, cudaStream_t stream);
+int launch_conv_prefill(const ChunkParams& p, cudaStream_t stream);
 int launch_conv_roll(const WindowParams& p, cudaStream_t stream);
 size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out);
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream);

@@ -166,6 +166,15 @@ def test_conv_argument_rules():
     assert verify(_conv_desc(positions=5)) == INVALID and "at least 6 positions" in _msg()
     assert verify(_conv_desc(num_accepted=None)) == INVALID and "num_accepted" in _msg()
     assert verify(_conv_desc(), slots=5) == INVALID and "row per state slot" in _msg()
+    assert verify(_conv_desc(scratch=FAKE, scratch_bytes=1 << 30)) == INVALID and "no conv scratch" in _msg()
+    # the optional prefill scratch: (2 Hqk + Hv) x 128 bf16 values a token
+    need = lib.kda_conv_scratch_bytes(64, 2, 4)
+    assert need == 64 * (2 * 2 + 4) * 128 * 2
+    assert _chunk_ex(a, conv=_conv_desc(scratch=FAKE, scratch_bytes=need - 2)) == INVALID
+    assert "conv scratch needs" in _msg()
+    assert _chunk_ex(a, conv=_conv_desc(scratch=FAKE + 8, scratch_bytes=need)) == INVALID
+    assert "conv scratch must be 16-byte aligned" in _msg()
+    assert lib.kda_conv_scratch_bytes(64, 0, 4) == 0
 
 
 def test_workspace_query():

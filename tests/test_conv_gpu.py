@@ -51,7 +51,7 @@ def _conv_inputs(x, dense_bands=False):
     return (qkv[:, :a].view(T, hqk, 128), qkv[:, a:b].view(T, hqk, 128), qkv[:, b:].view(T, hv, 128))
 
 
-def _prefill_case(x, taps, dim_first, cidx, chas, groups=1, fused=False, positions=4):
+def _prefill_case(x, taps, dim_first, cidx, chas, groups=1, fused=False, positions=4, scratch=True):
     import linear_attention_serving_fwd_gb300 as kda
     w, st = W.conv_inputs(x.hqk, x.hv, x.state_pool.shape[0], positions, taps=taps, seed=x.t_total)
     (q2, k2, v2), st_ref = oconv.prefill(x.q, x.k, x.v, x.cu_seqlens, w, taps, st, cidx, chas)
@@ -68,7 +68,7 @@ def _prefill_case(x, taps, dim_first, cidx, chas, groups=1, fused=False, positio
                                conv_weight=w.to("cuda"), conv_state=cst,
                                conv_state_indices=cidx.to("cuda"),
                                conv_has_initial_state=None if chas is None else chas.to("cuda"),
-                               conv_dim_first=dim_first)
+                               conv_dim_first=dim_first, conv_scratch=scratch)
     torch.cuda.synchronize()
     assert kda.kda_device_status(clear=True) == 0
     check_out(out, ref["out"], "conv prefill out")
@@ -77,26 +77,50 @@ def _prefill_case(x, taps, dim_first, cidx, chas, groups=1, fused=False, positio
     np.testing.assert_array_equal(_token_major(cst, dim_first), st_ref, err_msg="conv state")
 
 
+@pytest.mark.parametrize("scratch", [True, False])
 @pytest.mark.parametrize("taps,dim_first", [("bf16", False), ("f32", True), ("bf16", True)])
-def test_prefill_conv_small(taps, dim_first):
+def test_prefill_conv_small(taps, dim_first, scratch):
     """Ragged sequences (lengths 1 and 2 below the conv history, chunk
     multiples, a 300-token chain), conv rows without history, a sequence
-    with no conv row."""
+    with no conv row; the conv in its own pass (scratch) or in each
+    prologue item."""
     x = W.varlen_paged([70, 1, 2, 129, 64, 5, 300], 2, 4, slots=9, seed=31, lower_bound=-0.4,
                        has_initial=[1, 0, 1, 1, 1, 0, 1])
     cidx = x.state_indices.clone()
     cidx[4] = -1
     chas = torch.tensor([1, 1, 0, 1, 1, 1, 0], dtype=torch.uint8)
-    _prefill_case(x, taps, dim_first, cidx, chas)
+    _prefill_case(x, taps, dim_first, cidx, chas, scratch=scratch)
 
 
-def test_prefill_conv_group_scan_and_fused_bands():
+@pytest.mark.parametrize("scratch", [True, False])
+def test_prefill_conv_group_scan_and_fused_bands(scratch):
     """The chunk-group scan on convolved inputs, with q/k/v as strided views
     of one fused projection and a longer conv state row."""
     x = W.varlen_paged([700, 64, 1300], 1, 2, slots=5, seed=33, lower_bound=-0.1,
                        has_initial=[1, 1, 0])
     cidx = torch.tensor([3, 0, 4], dtype=torch.int32)
-    _prefill_case(x, "f32", False, cidx, None, groups=4, fused=True, positions=6)
+    _prefill_case(x, "f32", False, cidx, None, groups=4, fused=True, positions=6, scratch=scratch)
+
+
+def test_prefill_conv_paths_agree_bitwise():
+    """The conv in its own pass and the conv in each prologue item evaluate
+    the same roundings in the same order: bit-identical outputs, states and
+    conv rows on the varlen workload's shapes (GVA 4)."""
+    import linear_attention_serving_fwd_gb300 as kda
+    x = W.varlen_paged([300, 1000, 7, 700], 2, 8, slots=6, seed=37, lower_bound=-0.3).to("cuda")
+    w, st = W.conv_inputs(x.hqk, x.hv, 6, 4, taps="bf16", seed=37, device="cuda")
+    res = []
+    for scratch in (True, False):
+        pool, cst = x.state_pool.clone(), st.clone()
+        out, _ = kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, A_log=x.A_log, dt_bias=x.dt_bias,
+                                   cu_seqlens=x.cu_seqlens, state_cache=pool, state_indices=x.state_indices,
+                                   conv_weight=w, conv_state=cst, conv_state_indices=x.state_indices,
+                                   conv_scratch=scratch)
+        res.append((out, pool, cst))
+    torch.cuda.synchronize()
+    assert kda.kda_device_status(clear=True) == 0
+    for a, b, what in zip(res[0], res[1], ("out", "state cache", "conv state")):
+        assert torch.equal(a, b), what
 
 
 def test_prefill_conv_varlen_full():
