@@ -546,7 +546,7 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
         q_in, k_in, v_in = z.q, z.k, z.v
         if name == "prefill_conv":
             # raw projection bands as strided views of one fused [T, C]
-            # projection; width-4 conv + SiLU (bf16 taps) in the prologue
+            # projection; width-4 conv + SiLU (bf16 taps) before the prologue
             T_, C_ = z.t_total, (2 * z.hqk + z.hv) * D
             qkv = torch.cat([z.q.reshape(T_, -1), z.k.reshape(T_, -1), z.v.reshape(T_, -1)], dim=1)
             a_, b_ = z.hqk * D, 2 * z.hqk * D
@@ -594,8 +594,8 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                                   "checkpoint": "varlen workload plus one snapshot per sequence at its "
                                                 "64-aligned midpoint into a spare cache row",
                                   "prefill_conv": "varlen workload on raw q/k/v bands of a fused "
-                                                  "projection: width-4 conv + SiLU (bf16 taps) fused "
-                                                  "into the prologue, conv state updated",
+                                                  "projection: width-4 conv + SiLU (bf16 taps) in a "
+                                                  "pass of its own into a conv scratch, conv state updated",
                                   "long": "B=1 T=131072 Hqk=Hv=32, zero initial state"}[name]}
         if name == "prefill_conv" and "varlen" in res:
             res[name]["overhead_vs_varlen"] = round(t * 1e3 / res["varlen"]["ms_per_step"] - 1, 4)
