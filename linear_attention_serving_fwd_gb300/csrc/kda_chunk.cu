@@ -1079,6 +1079,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         tc::tmem_ld16_async(lanes + T_Y + 64, y1);
         if (!ident) tc::tmem_ld16_async(lanes + T_RV, y2);
         tc::tmem_wait_ld();
+        tc::tmem_regs(y0);
+        tc::tmem_regs(y1);
+        if (!ident) tc::tmem_regs(y2);
 #pragma unroll
         for (int v = 0; v < 16; ++v)
           S[v] = fmaf(dcur, S[v], __uint_as_float(y0[v]) + __uint_as_float(y1[v]) +

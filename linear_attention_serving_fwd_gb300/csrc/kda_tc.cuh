@@ -237,6 +237,30 @@ __device__ __forceinline__ void mma_kloop_tf32_sw128(uint32_t d_tmem, uint32_t a
 }
 
 // --- TMEM -> registers -------------------------------------------------------
+// tcgen05.ld writes its registers asynchronously: they hold the data only
+// after tcgen05.wait::ld.  The wait is a separate asm statement with no
+// register operands, so on its own nothing keeps the compiler from moving a
+// use of the loaded registers above it.  tmem_regs ties them to the wait: an
+// empty volatile asm that reads and writes every register, placed after the
+// wait (volatile asm statements keep their order), on which every later use
+// depends.
+__device__ __forceinline__ void tmem_regs(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]));
+}
+__device__ __forceinline__ void tmem_regs(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]));
+  asm volatile(""
+               : "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
 // lane (taddr.lane + i), columns taddr.col .. +31.  The warp may only touch
 // its own 32-lane sub-partition (warp id % 4).
@@ -253,12 +277,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tmem_regs(r);
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// tmem_ld32 without the wait: issue several, then tmem_wait_ld() once before
-// using any of them.
+// tmem_ld32 without the wait: issue several, then tmem_wait_ld() once and
+// tmem_regs() on each array before using any of them.
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -294,6 +319,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tmem_regs(r);
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }

@@ -135,3 +135,34 @@ def test_long_prefill_sampled(groups):
                                 A_log=x.A_log[h:h + 1], dt_bias=x.dt_bias[h:h + 1])
         check_out(out[:, h:h + 1], ref["out"], f"long head {h}")
         check_state(fin[:, h:h + 1], ref["state"], f"long head {h} state")
+
+
+def test_dense_prefill_repeats_bit_identical():
+    """The prefill is deterministic: 64 repeats of the timed dense workload
+    (B=2, T=4096, H=16), half of them after an L2 flush, give bit-identical
+    outputs and final states.  A use of tcgen05.ld registers before
+    tcgen05.wait::ld showed up here once in about 400 runs."""
+    import linear_attention_serving_fwd_gb300 as kda
+    x = W.workload("dense").to("cuda")
+    T, hv, n = x.t_total, x.hv, x.n_seqs
+    ws = torch.empty(kda.chunk_workspace_bytes(n, T, hv, 0), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    outs = torch.empty((8, T, hv, 128), dtype=torch.bfloat16, device="cuda")
+    fins = torch.empty((8, n, hv, 128, 128), dtype=torch.float32, device="cuda")
+
+    def run(k):
+        kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, A_log=x.A_log, dt_bias=x.dt_bias, scale=x.scale,
+                          lower_bound=x.lower_bound, n_seqs=n, initial_state=x.initial_state,
+                          final_state=fins[k], out=outs[k], workspace=ws)
+    run(0)
+    torch.cuda.synchronize()
+    ref_o, ref_f = outs[0].clone(), fins[0].clone()
+    for i in range(64):
+        if i % 2:
+            flush.fill_(i & 255)
+        run(i % 8)
+        if i % 8 == 7:
+            torch.cuda.synchronize()
+            for k in range(8):
+                assert torch.equal(outs[k], ref_o) and torch.equal(fins[k], ref_f), f"repeat {i - 7 + k} differs"
+    assert kda.kda_device_status(clear=True) == 0
