@@ -122,3 +122,13 @@ def test_empty_batch_returns_initial_states():
     torch.cuda.synchronize()
     assert out.shape == (0, 2, 128)
     assert torch.equal(fin, h0)
+
+
+def test_group_scan_inside_segment_calls():
+    """Each 256-token segment call runs the chunk-group scan (G = 4) on its
+    pieces, the state carried between calls through the cache table."""
+    x = _varlen_with_initial([700, 1300, 64], 1, 2, seed=42, lower_bound=-0.1, state_std=0.2)
+    ref = oracle.prefill(x)
+    out, fin = _host(x, segment=256, groups=4)
+    check_out(out, ref["out"], "host group-scan out")
+    check_state(fin, ref["state"], "host group-scan final state")
