@@ -1,21 +1,25 @@
 #!/usr/bin/env python
 """KDA forward-path benchmark on GB300.  Prints ONE JSON line (rank 0).
 
-A step is one chunked prefill (``kda_chunk_fwd``) of the dense serving
-workload B=2, T=4096, Hqk=Hv=16, D=128 (bf16 activations, fp32 initial state
-read, fp32 final state written), inputs resident in HBM; L2 is flushed (a
-256 MB write) before every timed step and the flush is outside the events.
-The same line carries the decode / verify / varlen / long-context results
-under ``extras``, the dominant kernel's roofline, the end-to-end number
-through the public API with pinned host buffers, and the CPU oracle timed on
-this host as a reported baseline.
+A step is one chunked prefill (``kda_chunk_fwd``) of the long-context
+workload B=1, T=131072, Hqk=Hv=32, D=128 (bf16 activations, zero initial
+state, fp32 final state written; 2048 chunks of 64 per head), the largest
+single-GPU prefill configuration, with inputs resident in HBM.  Its inputs
+(4.3 GB) are larger than L2, so no flush runs between steps.  The same line
+carries the dominant kernel's roofline (and the walk's), the end-to-end
+number through the public host-memory call, the CPU oracle timed on this
+host as a reported baseline, and under ``extras`` the dense and varlen
+prefills (each with its own roofline; L2 flushed before every step), the
+chunk-group counts on the long workload, and decode / verify / commit.
 
 Multi-GPU (torchrun): one replica per rank, no collective in the data path
 ("weak" scaling); a barrier brackets the timed region and the slowest rank's
 time is used.
 
-``--impl reference`` times the fp64 CPU oracle on the whole dense workload
-per step on this host's cores (rank 0 only) and prints the same keys.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (two of the 32 heads over the whole sequence per step, scaled
+to the workload's tokens) on this host's cores (rank 0 only) and prints the
+same keys.
 """
 from __future__ import annotations
 
@@ -33,31 +37,40 @@ sys.path.insert(0, ROOT)
 
 D = 128
 CHUNK = 64
-WORKLOAD = dict(name="dense", B=2, T=4096, hqk=16, hv=16)
+WORKLOAD = dict(name="long", B=1, T=131072, hqk=32, hv=32)
 METRIC = "chunk_kda prefill tokens/s"
+REF_SAMPLE_HEADS = 2  # heads of the workload the reference arm's step runs
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--extras",
-                    default="decode,verify,verify_conv,commit,decode_steps,decode_bf16,prefill_fp16,varlen,"
-                            "checkpoint,prefill_conv,long",
-                    help="comma list of extra workloads: decode, verify, verify_conv, commit, "
-                         "decode_steps, decode_bf16, prefill_fp16, varlen, checkpoint, prefill_conv, long")
+                    default="dense,varlen,groups,checkpoint,prefill_conv,prefill_fp16,commit,decode_steps,"
+                            "decode_bf16,verify_conv,verify,decode",
+                    help="comma list of extra workloads: dense, varlen, groups, checkpoint, prefill_conv, "
+                         "prefill_fp16, commit, decode_steps, decode_bf16, verify_conv, verify, decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
 
 def workload_desc():
     w = WORKLOAD
-    return (f"dense prefill B={w['B']} T={w['T']} Hqk={w['hqk']} Hv={w['hv']} D=128, bf16 "
-            f"q/k/v/g/beta, fp32 initial state N(0,0.02), final state returned, "
-            f"lower_bound=-5, A_log=log U[1,16], dt_bias N(0,0.1)")
+    return (f"long-context prefill B={w['B']} T={w['T']} Hqk={w['hqk']} Hv={w['hv']} D=128, bf16 "
+            f"q/k/v/g/beta N(0,1), zero initial state, final state returned, lower_bound=-5, "
+            f"A_log=log U[1,16], dt_bias N(0,0.1)")
+
+
+def config_dict(replicas):
+    """The workload's config; both arms print this same dict."""
+    w = WORKLOAD
+    return {"workload": workload_desc(), "global_batch": w["B"] * replicas, "seq_len": w["T"],
+            "heads": f"Hqk={w['hqk']} Hv={w['hv']}"}
 
 
 def flop_per_token_head():
@@ -86,15 +99,16 @@ def sources_sha256(kernel):
     return h.hexdigest()
 
 
-def profiled_traffic(kernel):
-    """DRAM bytes per launch (read + write) from the committed ncu summary in
-    profiles/, or None when the kernel's sources changed since the capture."""
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch (read + write) of ``kernel`` on ``workload`` from
+    the committed ncu summary in profiles/, or None when the kernel's sources
+    changed since the capture."""
     import re
     path = os.path.join(ROOT, "profiles", "dram_traffic.md")
     try:
         text = open(path).read()
         block = re.search(r"```json\n(.*?)\n```", text, re.S).group(1)
-        rec = json.loads(block).get(kernel)
+        rec = json.loads(block).get(f"{kernel}@{workload}")
     except Exception:
         return None
     if not rec or rec.get("sources_sha256") != sources_sha256(kernel):
@@ -210,19 +224,53 @@ def preroll(torch, fn, seconds=1.0):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def prefill_kernels(torch, step, steps, flush, barrier, reduce_max, th, hqk, hv, pk):
+    """Per-kernel live timing of a prefill step (the library's CUDA events on
+    its launch stream) and each kernel's roofline: the prologue streams the
+    step's inputs once (q, k per q/k head, v, g, beta) against HBM; the walk
+    carries the three 64 x 128 x 128 contractions (6 K V flop) against the
+    bf16 tensor peak."""
+    from linear_attention_serving_fwd_gb300 import _native
+    _native.trace_enable(True)
+    time_device(torch, step, steps, flush, barrier)
+    tr = _native.trace_read()
+    _native.trace_enable(False)
+    in_bytes = 2 * 256 / (hv // hqk) + 512 + 2
+    model = {
+        "kda_prologue": {"bound": "hbm", "unit": "GB/s", "peak": pk["hbm"], "work": th * in_bytes,
+                         "scale": 1e9, "peak_source": f"{pk['src']} HBM copy bandwidth",
+                         "per_unit": f"{in_bytes:.0f} B of q/k/v/g/beta per (token, v-head)"},
+        "kda_walk": {"bound": "tensor", "unit": "TFLOP/s", "peak": pk["bf16"], "work": th * 6 * D * D,
+                     "scale": 1e12, "peak_source": f"{pk['src']} bf16 dense (burst)",
+                     "per_unit": "6 K V flop per (token, v-head)"},
+    }
+    kernels = {}
+    for name, kd in model.items():
+        if name not in tr:
+            continue
+        ms = reduce_max(tr[name][0] / tr[name][1])
+        ach = kd["work"] / (ms / 1e3) / kd["scale"]
+        kernels[name] = {"bound": kd["bound"], "achieved": round(ach, 3), "peak": kd["peak"],
+                         "unit": kd["unit"], "frac": round(ach / kd["peak"], 4),
+                         "per_launch_ms": round(ms, 4), "per_unit": kd["per_unit"],
+                         "peak_source": kd["peak_source"]}
+    launches = sum(c for _, c in tr.values()) // max(1, steps)
+    ms_all = {k: round(v[0] / v[1], 4) for k, v in tr.items()}
+    return kernels, launches, ms_all
+
+
 def run_ours(args, rank, world, barrier, reduce_max):
     import torch
 
     import linear_attention_serving_fwd_gb300 as kda
-    from linear_attention_serving_fwd_gb300 import _native, workloads as W
+    from linear_attention_serving_fwd_gb300 import workloads as W
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     dev = torch.device("cuda")
     pk = peaks()
     w = WORKLOAD
-    x = W.dense_prefill(w["B"], w["T"], w["hqk"], w["hv"], seed=rank, device=dev)
-    n = w["B"]
-    T = x.t_total
+    x = W.workload(w["name"], seed=rank, device=dev)
+    n, T = w["B"], x.t_total
     out = torch.empty((T, w["hv"], D), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((n, w["hv"], D, D), dtype=torch.float32, device=dev)
     ws = torch.empty(kda.chunk_workspace_bytes(n, T, w["hv"], 0), dtype=torch.uint8, device=dev)
@@ -230,8 +278,10 @@ def run_ours(args, rank, world, barrier, reduce_max):
     def step():
         kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, A_log=x.A_log, dt_bias=x.dt_bias,
                           scale=x.scale, lower_bound=x.lower_bound, n_seqs=n,
-                          initial_state=x.initial_state, final_state=fin, out=out,
-                          workspace=ws)
+                          final_state=fin, out=out, workspace=ws)
+
+    def no_flush():  # the inputs (4.3 GB) are larger than L2
+        pass
 
     flush = make_flush(torch)
     bus = None
@@ -245,7 +295,7 @@ def run_ours(args, rank, world, barrier, reduce_max):
     torch.cuda.synchronize()
     clocks.start()
     preroll(torch, step, 1.0)
-    secs = time_device(torch, step, args.steps, flush, barrier)
+    secs = time_device(torch, step, args.steps, no_flush, barrier)
     clk = clocks.stop()
     secs = reduce_max(secs)
     ms_per_step = secs / args.steps * 1e3
@@ -254,57 +304,49 @@ def run_ours(args, rank, world, barrier, reduce_max):
     th = n * w["T"] * w["hv"]
     tflops = th * flop_per_token_head() * args.steps * world / secs / 1e12
 
-    # dominant kernel, timed live with the library's event tracing (CUDA
-    # events recorded by the library on its launch stream)
-    _native.trace_enable(True)
-    time_device(torch, step, args.steps, flush, barrier)
-    tr = _native.trace_read()
-    _native.trace_enable(False)
-    launches = sum(c for _, c in tr.values())
-    dom = max(tr, key=lambda k: tr[k][0])
-    dom_ms = tr[dom][0] / tr[dom][1]
-    # Algorithmic work per (token, v-head) by kernel.  The prologue streams the
-    # step's inputs once (q, k per q/k head, v, g, beta): an HBM roofline.  The
-    # walk carries the method's three 64 x 128 x 128 contractions (6 K V flop)
-    # and writes o: a tensor roofline over a serial chain.
-    r = w["hv"] // w["hqk"]
-    in_bytes = 2 * 256 / r + 512 + 2
-    kern = {
-        "kda_prologue": {"bound": "hbm", "unit": "GB/s", "peak": pk["hbm"],
-                         "work": th * in_bytes, "scale": 1e9,
-                         "peak_source": f"{pk['src']} HBM copy bandwidth",
-                         "per_unit": f"{in_bytes:.0f} B of q/k/v/g/beta per (token, v-head)"},
-        "kda_walk": {"bound": "tensor", "unit": "TFLOP/s", "peak": pk["bf16"],
-                     "work": th * 6 * D * D, "scale": 1e12,
-                     "peak_source": f"{pk['src']} bf16 dense (burst)",
-                     "per_unit": "6 K V flop per (token, v-head)"},
-    }
-    details = {}
-    for name, kd in kern.items():
-        if name not in tr:
-            continue
-        ms = tr[name][0] / tr[name][1]
-        ach = kd["work"] / (ms / 1e3) / kd["scale"]
-        details[name] = {"bound": kd["bound"], "achieved": round(ach, 3), "peak": kd["peak"],
-                         "unit": kd["unit"], "frac": round(ach / kd["peak"], 4),
-                         "per_launch_ms": round(ms, 4), "per_unit": kd["per_unit"]}
-    d = details.get(dom)
-    if d is None:  # a kernel without a model: report its time only
-        d = {"bound": "tensor", "achieved": None, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": None,
-             "per_launch_ms": round(dom_ms, 4)}
+    kernels, launches, ms_all = prefill_kernels(torch, step, args.steps, no_flush, barrier, reduce_max,
+                                                th, w["hqk"], w["hv"], pk)
+    dom = max(ms_all, key=lambda k: ms_all[k])
+    d = kernels.get(dom, {"bound": "tensor", "achieved": None, "peak": pk["bf16"], "unit": "TFLOP/s",
+                          "frac": None, "per_launch_ms": ms_all.get(dom), "per_unit": None,
+                          "peak_source": None})
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
                 "unit": d["unit"], "frac": d["frac"],
-                "traffic": profiled_traffic(dom) if dom in KERNEL_SOURCES else None,
-                "peak_source": kern.get(dom, {}).get("peak_source"),
-                "per_launch_ms": d["per_launch_ms"], "per_unit": d.get("per_unit"),
-                "kernels": details,
-                "kernels_ms_per_step": {k: round(v[0] / v[1], 4) for k, v in tr.items()}}
+                "traffic": profiled_traffic(dom, w["name"]) if dom in KERNEL_SOURCES else None,
+                "peak_source": d["peak_source"], "per_launch_ms": d["per_launch_ms"],
+                "per_unit": d["per_unit"], "kernels": kernels, "kernels_ms_per_step": ms_all}
 
-    # end to end through the public host-memory call: page-locked host
-    # inputs, outputs and states; the library copies segments in, runs them
-    # as chunked prefill and copies the outputs back, overlapped
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, random gate parameters, no weights)",
+        "config": config_dict(world),
+        "parallelism": f"replicas x{world}", "l2": "inputs (4.3 GB) larger than L2: no flush",
+        "groups": "auto (1 at this workload)",
+        "tflops": round(tflops, 3), "pct_bf16_peak": round(100 * tflops / pk["bf16"], 2),
+        "hbm_gbs_algorithmic": round(th * prefill_bytes_per_token_head(w["hqk"], w["hv"])
+                                     * args.steps * world / secs / 1e9, 1),
+        "roofline": roofline,
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        line["e2e"] = e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x)
+    if not args.no_extras:
+        line["extras"] = extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world, x)
+    return line
+
+
+def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
+    """End to end through the public host-memory call: page-locked host
+    inputs, output and final state; the library copies segments in, runs them
+    as chunked prefill and copies the outputs back, overlapped."""
+    dev = out.device
     host = {name: getattr(x, name).cpu().pin_memory()
-            for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")}
+            for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias")}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -316,44 +358,31 @@ def run_ours(args, rank, world, barrier, reduce_max):
     def e2e_step():
         kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"],
                                A_log=host["A_log"], dt_bias=host["dt_bias"], scale=x.scale,
-                               lower_bound=x.lower_bound, n_seqs=n,
-                               initial_state=host["initial_state"], final_state=fin_h, out=out_h,
+                               lower_bound=x.lower_bound, n_seqs=n, final_state=fin_h, out=out_h,
                                workspace=ws_host)
 
-    for _ in range(3):
+    for _ in range(2):
         e2e_step()
-    e2e_secs = reduce_max(time_device(torch, e2e_step, max(5, args.steps // 5), flush, barrier))
-    e2e_value = tokens * max(5, args.steps // 5) / e2e_secs
-
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) activations, random gate parameters, no weights)",
-        "config": {"workload": workload_desc(), "global_batch": n * world, "seq_len": w["T"],
-                   "parallelism": f"replicas x{world}", "l2": "flushed before each step (256 MB write)",
-                   "groups": "auto"},
-        "tflops": round(tflops, 3), "pct_bf16_peak": round(100 * tflops / pk["bf16"], 2),
-        "hbm_gbs_algorithmic": round(th * prefill_bytes_per_token_head(w["hqk"], w["hv"])
-                                     * args.steps * world / secs / 1e9, 1),
-        "roofline": roofline,
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches,
-        "clocks": clk,
-    }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(x)
-    if not args.no_extras:
-        line["extras"] = extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world)
-    return line
+    k = max(3, args.steps // 4)
+    secs = reduce_max(time_device(torch, e2e_step, k, lambda: None, barrier))
+    res = {"value": round(tokens * k / secs, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(secs / k * 1e3, 3),
+           "call": "kda_chunk_fwd_host on page-locked host buffers"}
+    del host, out_h, fin_h, ws_host
+    torch.cuda.empty_cache()
+    return res
 
 
-def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
-    from linear_attention_serving_fwd_gb300 import _native
+def _hbm(gbs, pk):
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(gbs / pk["hbm"], 4)}
+
+
+def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world, xl):
     res = {}
     steps = max(5, min(args.steps, 20))
     sb = 4 * D * D
+    want = set(args.extras.split(","))
 
     def restoring(pool):
         """Before each timed run of a call that updates ``pool`` in place: put
@@ -364,190 +393,20 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
             pool.copy_(start)
             flush()
         return fn
-    # decode / verify on the 256-request batch, H=32, 512-slot pool
-    want = set(args.extras.split(","))
-    for window in (1, 4):
-        if not ({"decode", "verify", "verify_conv", "commit"} & want):
-            break
-        y = W.workload("decode", window=window, seed=rank, device="cuda")
-        pool = y.state_pool
-        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
-        counter = torch.zeros(1, dtype=torch.int32, device="cuda")
-        corr = torch.empty((y.n_seqs, y.hv, window, D), dtype=torch.float32, device="cuda")
-        kg = torch.empty((y.n_seqs, y.hv, window, 2 * D), dtype=torch.bfloat16, device="cuda")
-        for verify in (False, True):
-            if verify and window == 1:
-                continue
-            if ("verify" if verify else "decode") not in want:
-                continue
 
-            def fn():
-                if verify:
-                    kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens,
-                                   y.state_indices, window, A_log=y.A_log, dt_bias=y.dt_bias,
-                                   out=out, corr=corr, kg=kg, work_counter=counter)
-                else:
-                    kda.kda_decode(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens,
-                                   y.state_indices, window, A_log=y.A_log, dt_bias=y.dt_bias,
-                                   out=out)
-            for _ in range(3):
-                fn()
-            secs = reduce_max(time_device(torch, fn, steps, flush if verify else restoring(pool), barrier))
-            items = y.n_seqs * y.hv
-            t = secs / steps
-            state_bytes = items * sb * (1 if verify else 2)
-            act_bytes = y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)  # q,k per v-head (GVA 1), v,g,o
-            rec_bytes = (y.t_total * y.hv * (4 * D + 4 * D)) if verify else 0
-            gbs = (state_bytes + act_bytes + rec_bytes) / t / 1e9
-            key = f"{'verify' if verify else 'decode'}_q{window}"
-            res[key] = {"tokens_per_s": round(y.t_total * world / t, 1),
-                        "ms_per_step": round(t * 1e3, 4),
-                        "state_gbs": round(state_bytes / t / 1e9, 1),
-                        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
-                                     "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                                     "traffic": profiled_traffic("kda_window") if window == 1 and not verify
-                                     else None,
-                                     "peak_source": f"{pk['src']} HBM copy bandwidth"},
-                        "workload": f"256 requests x window {window}, Hqk=Hv=32, 512-slot fp32 pool"}
-        if "verify_conv" in want and window == 4:
-            # verify on the raw projection bands: width-4 conv + SiLU after the
-            # history at the accepted column, conv state rolled (bf16 taps)
-            w, cst = W.conv_inputs(y.hqk, y.hv, pool.shape[0], window + 2, seed=rank, device="cuda")
-            acc = torch.randint(1, window + 1, (y.n_seqs,), dtype=torch.int32, device="cuda")
-
-            def fv():
-                kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, window,
-                               A_log=y.A_log, dt_bias=y.dt_bias, out=out, corr=corr, kg=kg,
-                               work_counter=counter, conv_weight=w, conv_state=cst,
-                               num_accepted_tokens=acc)
-            for _ in range(3):
-                fv()
-            secs = reduce_max(time_device(torch, fv, steps, flush, barrier))
-            t = secs / steps
-            items = y.n_seqs * y.hv
-            nbytes = (items * sb + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
-                      + y.t_total * y.hv * (4 * D + 4 * D))
-            gbs = nbytes / t / 1e9
-            res["verify_conv_q4"] = {"tokens_per_s": round(y.t_total * world / t, 1),
-                                     "ms_per_step": round(t * 1e3, 4),
-                                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
-                                                  "peak": pk["hbm"], "unit": "GB/s",
-                                                  "frac": round(gbs / pk["hbm"], 4), "traffic": None,
-                                                  "peak_source": f"{pk['src']} HBM copy bandwidth"},
-                                     "workload": "256 requests x window 4, Hqk=Hv=32, 512-slot fp32 pool, "
-                                                 "width-4 conv + SiLU on raw q/k/v (bf16 taps), "
-                                                 "6-position conv state, accepted U{1..4}"}
-            del w, cst, acc
-        if "commit" in want and window == 4:
-            # rebuild every request's state after all 4 verified tokens from
-            # verify's records, in place: 64 KB in + 64 KB out per item
-            kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, window,
-                           A_log=y.A_log, dt_bias=y.dt_bias, out=out, corr=corr, kg=kg,
-                           work_counter=counter)
-            acc = torch.full((y.n_seqs,), window, dtype=torch.int32, device="cuda")
-
-            def fc():
-                kda.kda_commit(pool, y.state_indices, acc, corr, kg, window, A_log=y.A_log,
-                               dt_bias=y.dt_bias, lower_bound=y.lower_bound)
-            for _ in range(3):
-                fc()
-            secs = reduce_max(time_device(torch, fc, steps, restoring(pool), barrier))
-            items = y.n_seqs * y.hv
-            t = secs / steps
-            nbytes = items * (2 * sb + window * (4 * D + 4 * D))
-            gbs = nbytes / t / 1e9
-            res["commit_q4"] = {"requests_per_s": round(y.n_seqs * world / t, 1),
-                                "ms_per_step": round(t * 1e3, 4),
-                                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
-                                             "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                                             "traffic": None,
-                                             "peak_source": f"{pk['src']} HBM copy bandwidth"},
-                                "workload": "256 requests x 4 accepted tokens, Hv=32, 512-slot fp32 pool"}
-        del y, pool
-    if "decode_steps" in want:
-        # speculative multi-token decode with a [request, step] slot table:
-        # start from the accepted column's row, store the state after every
-        # token into its own row (64 KB in + 4 x 64 KB out per item)
-        window = 4
-        y = W.decode_batch(256, window, 32, 32, slots=1280, seed=rank, device="cuda",
-                           name="decode_steps_q4")
-        table, acc = W.decode_slot_table(256, window, 1280, seed=rank, device="cuda")
-        pool = y.state_pool
-        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
-
-        def fs():
-            kda.kda_decode_steps(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, table, window,
-                                 num_accepted_tokens=acc, A_log=y.A_log, dt_bias=y.dt_bias, out=out)
-        for _ in range(3):
-            fs()
-        secs = reduce_max(time_device(torch, fs, steps, restoring(pool), barrier))
-        items = y.n_seqs * y.hv
-        t = secs / steps
-        nbytes = items * sb * (1 + window) + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
-        gbs = nbytes / t / 1e9
-        res["decode_steps_q4"] = {"tokens_per_s": round(y.t_total * world / t, 1),
-                                  "ms_per_step": round(t * 1e3, 4),
-                                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
-                                               "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                                               "traffic": None,
-                                               "peak_source": f"{pk['src']} HBM copy bandwidth"},
-                                  "workload": "256 requests x 4 tokens, Hqk=Hv=32, 1280-row fp32 pool, "
-                                              "slot table of 4 rows per request, accepted counts U{1..4}"}
-        del y, pool, table, acc
-        torch.cuda.empty_cache()
-    if "decode_bf16" in want:
-        # Q = 1 decode on a bf16 pool (rounded after the token): half the
-        # state bytes of the fp32 pool
-        y = W.decode_batch(256, 1, 32, 32, slots=512, seed=rank, device="cuda", state_dtype=torch.bfloat16,
-                           name="decode_q1_bf16")
-        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
-
-        def fb():
-            kda.kda_decode(y.q, y.k, y.v, y.g, y.beta, y.state_pool, y.cu_seqlens, y.state_indices, 1,
-                           A_log=y.A_log, dt_bias=y.dt_bias, out=out)
-        for _ in range(3):
-            fb()
-        secs = reduce_max(time_device(torch, fb, steps, restoring(y.state_pool), barrier))
-        t = secs / steps
-        items = y.n_seqs * y.hv
-        nbytes = items * (sb // 2) * 2 + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
-        gbs = nbytes / t / 1e9
-        res["decode_q1_bf16_state"] = {"tokens_per_s": round(y.t_total * world / t, 1),
-                                       "ms_per_step": round(t * 1e3, 4),
-                                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
-                                                    "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                                                    "traffic": None,
-                                                    "peak_source": f"{pk['src']} HBM copy bandwidth"},
-                                       "workload": "256 requests x window 1, Hqk=Hv=32, 512-slot bf16 pool"}
-        del y, out
-    if "prefill_fp16" in want:
-        # the headline prefill (B=2, T=4096, H=16) with fp16 activations and output
-        z = W.dense_prefill(2, 4096, 16, 16, seed=rank, device="cuda", act_dtype=torch.float16)
-        out = torch.empty((z.t_total, z.hv, D), dtype=torch.float16, device="cuda")
-        fin = torch.empty((2, z.hv, D, D), dtype=torch.float32, device="cuda")
-        ws = torch.empty(kda.chunk_workspace_bytes(2, z.t_total, z.hv, 0), dtype=torch.uint8, device="cuda")
-
-        def ff():
-            kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias, n_seqs=2,
-                              initial_state=z.initial_state, final_state=fin, out=out, workspace=ws)
-        for _ in range(3):
-            ff()
-        secs = reduce_max(time_device(torch, ff, steps, flush, barrier))
-        t = secs / steps
-        res["prefill_fp16"] = {"tokens_per_s": round(z.t_total * world / t, 1), "ms_per_step": round(t * 1e3, 4),
-                               "workload": "B=2 T=4096 Hqk=Hv=16, fp16 q/k/v/g/beta and output, fp32 states"}
-        del z, out, fin, ws
-    # varlen paged and long-context prefill
-    for name in ("varlen", "checkpoint", "prefill_conv", "long"):
+    # ---- the other prefill configurations, each with its kernels' rooflines
+    for name in ("dense", "varlen", "checkpoint", "prefill_conv", "prefill_fp16"):
         if name not in want:
             continue
-        z = W.workload("long" if name == "long" else "varlen", seed=rank, device="cuda")
+        wl = "dense" if name in ("dense", "prefill_fp16") else "varlen"
+        z = (W.dense_prefill(2, 4096, 16, 16, seed=rank, device="cuda", act_dtype=torch.float16)
+             if name == "prefill_fp16" else W.workload(wl, seed=rank, device="cuda"))
         ck = {}
         q_in, k_in, v_in = z.q, z.k, z.v
         if name == "prefill_conv":
             # raw projection bands as strided views of one fused [T, C]
             # projection; width-4 conv + SiLU (bf16 taps) before the prologue
-            T_, C_ = z.t_total, (2 * z.hqk + z.hv) * D
+            T_ = z.t_total
             qkv = torch.cat([z.q.reshape(T_, -1), z.k.reshape(T_, -1), z.v.reshape(T_, -1)], dim=1)
             a_, b_ = z.hqk * D, 2 * z.hqk * D
             q_in = qkv[:, :a_].view(T_, z.hqk, D)
@@ -565,9 +424,9 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
             ck = dict(checkpoint_state=z.state_pool,
                       checkpoint_offsets=((lens // 2) // 64 * 64).to(torch.int32),
                       checkpoint_state_indices=torch.tensor(spare, dtype=torch.int32, device="cuda"))
-        out = torch.empty((z.t_total, z.hv, D), dtype=torch.bfloat16, device="cuda")
-        ws = torch.empty(kda.chunk_workspace_bytes(z.n_seqs, z.t_total, z.hv, 0),
-                         dtype=torch.uint8, device="cuda")
+        out = torch.empty((z.t_total, z.hv, D), dtype=z.q.dtype, device="cuda")
+        ws = torch.empty(kda.chunk_workspace_bytes(z.n_seqs, z.t_total, z.hv, 0), dtype=torch.uint8,
+                         device="cuda")
         fin = None
         if z.state_pool is None:
             fin = torch.empty((z.n_seqs, z.hv, D, D), dtype=torch.float32, device="cuda")
@@ -580,56 +439,198 @@ def extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world):
                                   has_initial_state=z.has_initial_state, out=out, workspace=ws, **ck)
             else:
                 kda.kda_chunk_fwd(z.q, z.k, z.v, z.g, z.beta, A_log=z.A_log, dt_bias=z.dt_bias,
-                                  n_seqs=z.n_seqs, final_state=fin, out=out, workspace=ws)
-        fn()
+                                  n_seqs=z.n_seqs, initial_state=z.initial_state, final_state=fin,
+                                  out=out, workspace=ws)
+        for _ in range(3):
+            fn()
         torch.cuda.synchronize()
-        s2 = 3 if name == "long" else steps
-        secs = reduce_max(time_device(torch, fn, s2, flush, barrier))
-        t = secs / s2
+        secs = reduce_max(time_device(torch, fn, steps, flush, barrier))
+        t = secs / steps
         th = z.t_total * z.hv
         tfl = th * flop_per_token_head() / t / 1e12
-        res[name] = {"tokens_per_s": round(z.t_total * world / t, 1), "ms_per_step": round(t * 1e3, 3),
-                     "tflops": round(tfl, 3), "pct_bf16_peak": round(100 * tfl / pk["bf16"], 2),
-                     "workload": {"varlen": "8 seqs (U[64,8192] rescaled to 32768), Hqk=8 Hv=32, paged fp32 cache",
-                                  "checkpoint": "varlen workload plus one snapshot per sequence at its "
-                                                "64-aligned midpoint into a spare cache row",
-                                  "prefill_conv": "varlen workload on raw q/k/v bands of a fused "
-                                                  "projection: width-4 conv + SiLU (bf16 taps) in a "
-                                                  "pass of its own into a conv scratch, conv state updated",
-                                  "long": "B=1 T=131072 Hqk=Hv=32, zero initial state"}[name]}
-        if name == "prefill_conv" and "varlen" in res:
-            res[name]["overhead_vs_varlen"] = round(t * 1e3 / res["varlen"]["ms_per_step"] - 1, 4)
-        if name == "checkpoint":
-            res[name]["snapshot_bytes"] = int((ck["checkpoint_offsets"] > 0).sum().item()) * z.hv * 4 * D * D
-            if "varlen" in res:
-                res[name]["overhead_vs_varlen"] = round(t * 1e3 / res["varlen"]["ms_per_step"] - 1, 4)
-        del z, out, ws
+        r = {"ms": round(t * 1e3, 4), "tokens_per_s": round(z.t_total * world / t, 1),
+             "tflops": round(tfl, 3), "pct_bf16_peak": round(100 * tfl / pk["bf16"], 2),
+             "workload": {"dense": "B=2 T=4096 Hqk=Hv=16, h0 N(0,0.02), final state; L2 flushed",
+                          "varlen": "8 seqs U[64,8192] rescaled to 32768, Hqk=8 Hv=32, paged fp32 cache; "
+                                    "L2 flushed",
+                          "checkpoint": "varlen plus one snapshot per sequence at its 64-aligned midpoint",
+                          "prefill_conv": "varlen on raw q/k/v bands: width-4 conv + SiLU (bf16 taps) "
+                                          "in its own pass, conv state updated",
+                          "prefill_fp16": "dense with fp16 q/k/v/g/beta and output"}[name]}
+        if name in ("dense", "varlen"):
+            kern, _, _ = prefill_kernels(torch, fn, steps, flush, barrier, reduce_max, th, z.hqk, z.hv, pk)
+            r["roofline"] = {k: {"frac": v["frac"], "achieved": v["achieved"], "unit": v["unit"],
+                                 "ms": v["per_launch_ms"],
+                                 "traffic": profiled_traffic(k, name)} for k, v in kern.items()}
+        if name in ("checkpoint", "prefill_conv") and "varlen" in res:
+            r["overhead_vs_varlen"] = round(t * 1e3 / res["varlen"]["ms"] - 1, 4)
+        res[name] = r
+        del z, out, ws, fin, ck
+        torch.cuda.empty_cache()
+
+    # ---- chunk groups on the long workload: G = 1 (auto) against 4 and 8
+    if "groups" in want:
+        n, T, hv = 1, xl.t_total, xl.hv
+        g = {}
+        for G in (1, 4, 8):
+            ws = torch.empty(kda.chunk_workspace_bytes(n, T, hv, G), dtype=torch.uint8, device="cuda")
+            out = torch.empty((T, hv, D), dtype=torch.bfloat16, device="cuda")
+            fin = torch.empty((n, hv, D, D), dtype=torch.float32, device="cuda")
+
+            def fg():
+                kda.kda_chunk_fwd(xl.q, xl.k, xl.v, xl.g, xl.beta, A_log=xl.A_log, dt_bias=xl.dt_bias,
+                                  n_seqs=n, final_state=fin, out=out, workspace=ws, groups=G)
+            for _ in range(2):
+                fg()
+            s2 = 5
+            g[f"G{G}_ms"] = round(reduce_max(time_device(torch, fg, s2, lambda: None, barrier)) / s2 * 1e3, 3)
+            del ws, out, fin
+            torch.cuda.empty_cache()
+        res["groups_long"] = g
+
+    # ---- speculative decode: commit and the slot-table decode
+    if "commit" in want:
+        y = W.workload("decode", window=4, seed=rank, device="cuda")
+        pool = y.state_pool
+        counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, 4,
+                       A_log=y.A_log, dt_bias=y.dt_bias, work_counter=counter)
+        out, corr, kg = kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, 4,
+                                       A_log=y.A_log, dt_bias=y.dt_bias, work_counter=counter)
+        acc = torch.full((y.n_seqs,), 4, dtype=torch.int32, device="cuda")
+
+        def fc():
+            kda.kda_commit(pool, y.state_indices, acc, corr, kg, 4, A_log=y.A_log,
+                           dt_bias=y.dt_bias, lower_bound=y.lower_bound)
+        for _ in range(3):
+            fc()
+        secs = reduce_max(time_device(torch, fc, steps, restoring(pool), barrier))
+        t = secs / steps
+        nbytes = y.n_seqs * y.hv * (2 * sb + 4 * (4 * D + 4 * D))
+        res["commit_q4"] = {"ms": round(t * 1e3, 4), **_hbm(nbytes / t / 1e9, pk),
+                            "workload": "256 requests x 4 accepted tokens, Hv=32, fp32 pool"}
+        del y, pool, out, corr, kg
+    if "decode_steps" in want:
+        # a [request, step] slot table: start from the accepted column's row,
+        # store the state after every token (64 KB in + 4 x 64 KB out per item)
+        y = W.decode_batch(256, 4, 32, 32, slots=1280, seed=rank, device="cuda", name="decode_steps_q4")
+        table, acc = W.decode_slot_table(256, 4, 1280, seed=rank, device="cuda")
+        pool = y.state_pool
+        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
+
+        def fs():
+            kda.kda_decode_steps(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, table, 4,
+                                 num_accepted_tokens=acc, A_log=y.A_log, dt_bias=y.dt_bias, out=out)
+        for _ in range(3):
+            fs()
+        secs = reduce_max(time_device(torch, fs, steps, restoring(pool), barrier))
+        t = secs / steps
+        nbytes = y.n_seqs * y.hv * sb * 5 + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
+        res["decode_steps_q4"] = {"ms": round(t * 1e3, 4), "tokens_per_s": round(y.t_total * world / t, 1),
+                                  **_hbm(nbytes / t / 1e9, pk),
+                                  "workload": "256 requests x 4 tokens, H=32, slot table of 4 rows each"}
+        del y, pool, table, acc, out
+        torch.cuda.empty_cache()
+    if "decode_bf16" in want:
+        y = W.decode_batch(256, 1, 32, 32, slots=512, seed=rank, device="cuda", state_dtype=torch.bfloat16,
+                           name="decode_q1_bf16")
+        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
+
+        def fb():
+            kda.kda_decode(y.q, y.k, y.v, y.g, y.beta, y.state_pool, y.cu_seqlens, y.state_indices, 1,
+                           A_log=y.A_log, dt_bias=y.dt_bias, out=out)
+        for _ in range(3):
+            fb()
+        secs = reduce_max(time_device(torch, fb, steps, restoring(y.state_pool), barrier))
+        t = secs / steps
+        nbytes = y.n_seqs * y.hv * sb + y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)
+        res["decode_q1_bf16_state"] = {"ms": round(t * 1e3, 4), "tokens_per_s": round(y.t_total * world / t, 1),
+                                       **_hbm(nbytes / t / 1e9, pk),
+                                       "workload": "256 requests x 1 token, H=32, bf16 pool"}
+        del y, out
+
+    # ---- verify, then decode last (Q = 4, then Q = 1) on the serving batch:
+    # 256 requests, Hqk=Hv=32, 512-slot fp32 pool
+    for window in (4, 1):
+        if not ({"decode", "verify", "verify_conv"} & want):
+            break
+        y = W.workload("decode", window=window, seed=rank, device="cuda")
+        pool = y.state_pool
+        out = torch.empty((y.t_total, y.hv, D), dtype=torch.bfloat16, device="cuda")
+        counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+        corr = torch.empty((y.n_seqs, y.hv, window, D), dtype=torch.float32, device="cuda")
+        kg = torch.empty((y.n_seqs, y.hv, window, 2 * D), dtype=torch.bfloat16, device="cuda")
+        act = y.t_total * y.hv * (2 * 256 + 256 + 2 + 256)  # q, k per v-head (GVA 1), v, g, o
+        rec = y.t_total * y.hv * (4 * D + 4 * D)           # verify's corr and kg records
+        items = y.n_seqs * y.hv
+        if window == 4 and "verify_conv" in want:
+            wc, cst = W.conv_inputs(y.hqk, y.hv, pool.shape[0], window + 2, seed=rank, device="cuda")
+            acc = torch.randint(1, window + 1, (y.n_seqs,), dtype=torch.int32, device="cuda")
+
+            def fv():
+                kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens, y.state_indices, window,
+                               A_log=y.A_log, dt_bias=y.dt_bias, out=out, corr=corr, kg=kg,
+                               work_counter=counter, conv_weight=wc, conv_state=cst,
+                               num_accepted_tokens=acc)
+            for _ in range(3):
+                fv()
+            t = reduce_max(time_device(torch, fv, steps, flush, barrier)) / steps
+            res["verify_conv_q4"] = {"ms": round(t * 1e3, 4), **_hbm((items * sb + act + rec) / t / 1e9, pk),
+                                     "workload": "verify Q=4 on raw q/k/v: width-4 conv + SiLU, conv state"}
+            del wc, cst, acc
+        for verify in (True, False):
+            if verify and (window == 1 or "verify" not in want):
+                continue
+            if not verify and "decode" not in want:
+                continue
+
+            def fn():
+                if verify:
+                    kda.kda_verify(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens,
+                                   y.state_indices, window, A_log=y.A_log, dt_bias=y.dt_bias,
+                                   out=out, corr=corr, kg=kg, work_counter=counter)
+                else:
+                    kda.kda_decode(y.q, y.k, y.v, y.g, y.beta, pool, y.cu_seqlens,
+                                   y.state_indices, window, A_log=y.A_log, dt_bias=y.dt_bias,
+                                   out=out)
+            for _ in range(3):
+                fn()
+            t = reduce_max(time_device(torch, fn, steps, flush if verify else restoring(pool), barrier)) / steps
+            state_bytes = items * sb * (1 if verify else 2)
+            nbytes = state_bytes + act + (rec if verify else 0)
+            key = f"{'verify' if verify else 'decode'}_q{window}"
+            res[key] = {"ms": round(t * 1e3, 4), "tokens_per_s": round(y.t_total * world / t, 1),
+                        "state_gbs": round(state_bytes / t / 1e9, 1), **_hbm(nbytes / t / 1e9, pk),
+                        "traffic": profiled_traffic("kda_window", key) if not verify else None,
+                        "workload": f"256 requests x {window}, H=32, 512-slot fp32 pool"}
+        del y, pool
         torch.cuda.empty_cache()
     return res
 
 
-def cpu_baseline(x, min_seconds=10.0, max_reps=200):
-    """The fp64 oracle, as it stands, on the whole dense workload (every
-    sequence and head), repeated until ``min_seconds`` of wall time."""
+def cpu_baseline(x, min_seconds=10.0):
+    """The fp64 oracle, as it stands, on the whole long-context workload
+    (every head over the whole sequence, eight heads per call), repeated
+    until ``min_seconds`` of wall time have passed."""
     import oracle
-    q, k, v, g, b = (t.cpu() for t in (x.q, x.k, x.v, x.g, x.beta))
-    A_log, dt = x.A_log.cpu(), x.dt_bias.cpu()
-    h0 = x.initial_state.cpu() if x.initial_state is not None else None
-    cu = x.cu_seqlens.cpu()
     threads = os.cpu_count() or 1
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.recurrence(q, k, v, g, b, cu, A_log=A_log, dt_bias=dt, lower_bound=x.lower_bound,
-                          h0=h0, want_out=True, want_state=True, n_threads=threads)
+    hv, T = x.hv, x.t_total
+    slabs = [(h, min(hv, h + 8)) for h in range(0, hv, 8)]
+    cpu = {name: getattr(x, name).cpu() for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias")}
+    cu = x.cu_seqlens.cpu()
+    reps, elapsed = 0, 0.0
+    while elapsed < min_seconds:
+        for h0, h1 in slabs:
+            q, k, v, g, b = (cpu[nm][:, h0:h1] for nm in ("q", "k", "v", "g", "beta"))
+            t0 = time.perf_counter()
+            oracle.recurrence(q, k, v, g, b, cu, A_log=cpu["A_log"][h0:h1], dt_bias=cpu["dt_bias"][h0:h1],
+                              lower_bound=x.lower_bound, want_out=True, want_state=True, n_threads=threads)
+            elapsed += time.perf_counter() - t0
         reps += 1
-        dt_s = time.perf_counter() - t0
-        if dt_s >= min_seconds or reps >= max_reps:
-            break
-    return {"value": round(x.t_total * reps / dt_s, 2), "unit": "tokens/s", "cores": threads,
-            "kind": "oracle", "seconds": round(dt_s, 3),
-            "sample": f"the whole dense workload ({x.n_seqs} x {x.t_total // x.n_seqs} tokens, Hv={x.hv}) "
-                      f"{reps} times (fp64 token recurrence, OpenMP over sequence, head and value block)"}
+    return {"value": round(T * reps / elapsed, 2), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle", "seconds": round(elapsed, 3),
+            "sample": f"the whole long-context workload ({T} tokens, Hv={hv}), {reps} time(s), eight "
+                      f"heads per oracle call (fp64 token recurrence, OpenMP over head and value block)"}
 
 
 # ---------------------------------------------------------------------------
@@ -641,28 +642,32 @@ def run_reference(args):
     import oracle
     from linear_attention_serving_fwd_gb300 import workloads as W
     w = WORKLOAD
-    # one step = the whole dense workload (every sequence and head)
-    x = W.dense_prefill(w["B"], w["T"], w["hqk"], w["hv"], seed=0)
+    x = W.workload(w["name"], seed=0)
     threads = os.cpu_count() or 1
-    args_ = (x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens)
-    kw = dict(A_log=x.A_log, dt_bias=x.dt_bias, lower_bound=x.lower_bound,
-              h0=x.initial_state, n_threads=threads)
+    hs = REF_SAMPLE_HEADS
+    # one step = heads 0 .. hs-1 of the workload over the whole sequence;
+    # its tokens/s is scaled to the workload's (all Hv heads)
+    args_ = tuple(t[:, :hs].contiguous() for t in (x.q, x.k, x.v, x.g, x.beta)) + (x.cu_seqlens,)
+    kw = dict(A_log=x.A_log[:hs].contiguous(), dt_bias=x.dt_bias[:hs].contiguous(),
+              lower_bound=x.lower_bound, n_threads=threads)
+    del x
     for _ in range(max(1, args.warmup)):
         oracle.recurrence(*args_, **kw)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle.recurrence(*args_, **kw)
     secs = time.perf_counter() - t0
-    value = x.t_total * args.steps / secs
-    sample = (f"per step: the whole dense workload ({w['B']} x {w['T']} tokens, Hv={w['hv']}; fp64 token "
-              f"recurrence, OpenMP, {threads} threads)")
+    value = w["T"] * w["B"] * (hs / w["hv"]) * args.steps / secs
+    sample = (f"per step: heads 0..{hs - 1} of the {w['hv']} over the whole sequence ({w['T']} tokens), "
+              f"value scaled by {hs}/{w['hv']} to the workload's tokens/s; fp64 token recurrence, OpenMP, "
+              f"{threads} threads")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(), "global_batch": w["B"], "seq_len": w["T"],
-                   "parallelism": "cpu oracle, rank 0"},
+        "config": config_dict(args.gpus),
+        "parallelism": "cpu oracle, rank 0",
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

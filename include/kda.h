@@ -472,6 +472,19 @@ const char* kda_last_error(void);
 int kda_device_status(void* stream, int32_t clear);
 
 /*
+ * kda_selftest_wait_timeout - test aid for the bounded device waits; the
+ * pages have no counterpart.  Launches one CTA on ``stream`` that holds
+ * tensor memory as the chunk kernels do and waits, with their bounded
+ * mbarrier wait, on a barrier that nothing arrives at.  After ``limit_us``
+ * microseconds (1 .. 1,000,000) of wall time the wait gives up: the kernel
+ * sets the timeout bit of the device error word, frees its tensor memory
+ * and returns, so the context stays usable.  kda_device_status then returns
+ * KDA_ERR_DEVICE_TIMEOUT.  Nothing faults or traps.  Returns KDA_OK once
+ * launched, KDA_ERR_INVALID_ARGUMENT for a limit out of range.
+ */
+int kda_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
+/*
  * Kernel tracing (off by default).  kda_trace_enable(1) clears the totals and
  * starts recording a CUDA event pair around every kernel the library
  * launches, on the launching stream; kda_trace_enable(0) stops.

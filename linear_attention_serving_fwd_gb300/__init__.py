@@ -527,3 +527,10 @@ def kda_commit(state_pool, slots, num_accepted, corr, kg, window, *, A_log=None,
 def kda_device_status(stream=None, clear: bool = True) -> int:
     """Synchronise and read the device error word (0 = clean)."""
     return int(_native.lib().kda_device_status(_stream_handle(stream), int(clear)))
+
+
+def kda_selftest_wait_timeout(limit_us: int = 1000, stream=None) -> None:
+    """Launch the bounded-wait self-test: one CTA waits on a barrier nothing
+    arrives at and gives up after ``limit_us`` microseconds, setting the
+    timeout bit that ``kda_device_status`` then reports."""
+    _native.check(_native.lib().kda_selftest_wait_timeout(int(limit_us), _stream_handle(stream)))

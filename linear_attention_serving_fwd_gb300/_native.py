@@ -13,6 +13,7 @@ from . import build as _build
 
 _lock = threading.Lock()
 _lib = None
+_variant = None  # None: the regular library; "phase_timing": the measurement build
 
 KDA_OK = 0
 KDA_ERR_INVALID_ARGUMENT = 1
@@ -28,7 +29,7 @@ EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_veri
            "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
            "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
            "kda_decode_steps", "kda_verify_ex", "kda_commit_ex", "kda_chunk_fwd_host",
-           "kda_chunk_fwd_host_workspace_bytes", "kda_conv_scratch_bytes")
+           "kda_chunk_fwd_host_workspace_bytes", "kda_conv_scratch_bytes", "kda_selftest_wait_timeout")
 
 
 class KdaActivations(ctypes.Structure):
@@ -102,6 +103,8 @@ def _declare(lib):
     lib.kda_last_error.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [P, I32]
     lib.kda_device_status.restype = ctypes.c_int
+    lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_trace_enable.argtypes = [I32]
     lib.kda_trace_enable.restype = ctypes.c_int
     lib.kda_trace_read.argtypes = [I32, ctypes.c_char_p, I32, ctypes.POINTER(ctypes.c_double),
@@ -113,7 +116,17 @@ def _declare(lib):
 
 
 def lib_path() -> str:
-    return _build.LIB
+    return _build.lib_path(_variant)
+
+
+def select_variant(name) -> None:
+    """Load a measurement build (``"phase_timing"``) instead of the regular
+    library; only before the library is first used in this process."""
+    global _variant
+    with _lock:
+        if _lib is not None:
+            raise RuntimeError("select_variant must come before the library is loaded")
+        _variant = name
 
 
 def lib():
@@ -121,7 +134,7 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = _build.build(variant=_variant)
             if not os.path.exists(path):
                 raise ImportError(f"libkda.so missing at {path}")
             _lib = _declare(ctypes.CDLL(path))

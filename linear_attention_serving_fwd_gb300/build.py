@@ -3,6 +3,10 @@
 Each translation unit compiles in parallel to an object file, then nvcc
 links the shared library.  Output goes to ``linear_attention_serving_fwd_gb300/
 _build/`` (git-ignored); nothing is installed into site-packages.
+
+``variant="phase_timing"`` builds a measurement copy into ``_build/phase_timing/``
+with ``-DKDA_PHASE_TIMING``: the prologue adds up clock64 cycles per phase
+(see :mod:`.phase_timing`).  The regular library carries none of that code.
 """
 from __future__ import annotations
 
@@ -16,6 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
+VARIANTS = {None: [], "phase_timing": ["-DKDA_PHASE_TIMING"]}
 SOURCES = ["kda_api.cu", "kda_window.cu", "kda_chunk.cu", "kda_noalloc.cu", "kda_commit.cu", "kda_conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -38,23 +43,30 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def lib_path(variant=None) -> str:
+    return LIB if variant is None else os.path.join(BUILD, variant, "libkda.so")
+
+
+def up_to_date(variant=None) -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, variant=None) -> str:
+    lib = lib_path(variant)
+    if not force and up_to_date(variant):
+        return lib
+    out_dir = os.path.dirname(lib)
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *FLAGS, *VARIANTS[variant], "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -66,13 +78,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -40,15 +40,21 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// The error word's device address, resolved once per device (under the
+// library lock).  The address stays valid for the life of the device's
+// primary context: a cudaDeviceReset inside the process after the first
+// call is not supported.
 unsigned* error_word_ptr() {
   static unsigned* ptrs[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
+  static uint64_t done = 0;
+  int dev = -1;
+  const bool have = kda::once_per_device(done, [&](int d) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned*>(p);
-  }
+    if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) ptrs[d] = static_cast<unsigned*>(p);
+    else cudaGetLastError();
+  });
+  if (!have || cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lk(kda::host_mutex());
   return ptrs[dev];
 }
 
@@ -197,6 +203,11 @@ void trace_drain() {  // caller holds the lock
 }  // namespace
 
 namespace kda {
+std::mutex& host_mutex() {
+  static std::mutex m;
+  return m;
+}
+
 void set_last_error(int code, const char* msg) {
   (void)code;
   g_last_error = msg;
@@ -927,6 +938,16 @@ int kda_device_status(void* stream, int32_t clear) {
   if (word & kda::ERR_TIMEOUT) return fail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device wait expired.");
   if (word & kda::ERR_INDEX)
     return fail(KDA_ERR_DEVICE_INDEX, "a kernel met an out-of-range slot or sequence length.");
+  return ok();
+}
+
+int kda_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(KDA_ERR_INVALID_ARGUMENT, "limit_us must lie in [1, 1000000] (got %u).", limit_us);
+  unsigned* err = error_word_ptr();
+  if (!err) return fail(KDA_ERR_CUDA, "the device error word could not be resolved.");
+  if (kda::launch_wait_selftest(err, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream)) != 0)
+    return cuda_fail(cudaGetLastError(), "kda_selftest_wait_timeout launch");
   return ok();
 }
 

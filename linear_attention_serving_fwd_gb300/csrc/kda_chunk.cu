@@ -91,9 +91,10 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 }
 
 // Bounded mbarrier wait that also gives up once another thread of the CTA has
-// raised the abort flag.
+// raised the abort flag.  ``limit_ns`` of wall time (WAIT_NS in the kernels;
+// the self-test below passes a short one).
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t phase, volatile int* abort,
-                                              unsigned* err) {
+                                              unsigned* err, uint64_t limit_ns = WAIT_NS) {
   if (mbar_test_wait(bar, phase)) return true;  // already complete: no parking round trip
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < WAIT_CAP; ++i) {
@@ -101,11 +102,48 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t phase, vol
     if (*abort) return false;
     const uint64_t t = globaltimer_ns();
     if (t0 == 0) t0 = t;
-    else if (t - t0 > WAIT_NS) break;
+    else if (t - t0 > limit_ns) break;
   }
   set_error(err, ERR_TIMEOUT);
   *abort = 1;
   return false;
+}
+
+// --------------------------------------------------------------------------
+// Self-test of the bounded-wait abort path (no fault, no trap): one CTA of
+// four warps holds TMEM as the chunk kernels do and waits, with the chunk
+// kernels' wait_or_abort, on an mbarrier that nothing ever arrives at.  The
+// first thread whose wait passes ``limit_ns`` sets ERR_TIMEOUT and raises
+// the CTA's abort flag; the other threads see the flag and stop; warp 0
+// frees the TMEM and the CTA returns.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(128, 1) kda_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem;
+  __shared__ int abort;
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem, 32);
+    tc::tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    abort = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  wait_or_abort(&bar, 0, &abort, err, limit_ns);  // phase 0 never completes
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 32);
+}
+
+int launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream) {
+  kda_wait_selftest_kernel<<<1, 128, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 // --------------------------------------------------------------------------
@@ -177,8 +215,6 @@ constexpr uint32_t P_A3 = 17408;     // fp16 [128][128] = [[T, 0], [-A_qk T, I]]
 constexpr uint32_t P_A2 = 50176;     // fp16 [128][64]  = [A_qk ; 0]
 constexpr uint32_t P_B2 = 66560;     // fp16 [64][64]   = T^T
 constexpr uint32_t P_TILES = 75776;  // bf16 tiles of the next item (below)
-constexpr uint32_t P_WT = 0;         // fp16 w^T, MN-major [k'][r] (over L^{-1} once dead)
-constexpr uint32_t WT_LBO = 128, WT_SBO = 1024;  // its 8-row r groups / 8-column k' groups
 static_assert(P_LI + 64 * LDT * 4 <= P_A && P_A + 64 * LDT * 4 <= P_W, "prologue carve");
 static_assert(P_W + 32 * LDW * 4 <= P_A3 + 32768 && P_A3 + 32768 <= P_A2, "A3 covers A and W");
 static_assert(P_A2 + 16384 <= P_B2 && P_B2 + 8192 <= P_TILES, "prologue carve");
@@ -315,6 +351,51 @@ __device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m
   return r;
 }
 
+// Per-phase cycle accounting of the prologue, compiled in only with
+// -DKDA_PHASE_TIMING (the package's ``phase_timing`` module builds and runs
+// that copy): thread 0 of each CTA adds the clock64 cycles between the
+// barriers that close the phases of every item, and at exit adds its sums
+// and item count to g_phase_cycles / g_phase_items.  Every phase ends with a
+// barrier of all threads, so these are the phases' wall times on the SM.
+#ifdef KDA_PHASE_TIMING
+constexpr int N_PHASES = 12;
+__device__ unsigned long long g_phase_cycles[N_PHASES];
+__device__ unsigned long long g_phase_items;
+#define PH_BEGIN()                                       \
+  __shared__ unsigned long long ph_acc[N_PHASES];        \
+  long long ph_t = clock64();                            \
+  int ph_items = 0;                                      \
+  if (tid == 0)                                          \
+    for (int i_ = 0; i_ < N_PHASES; ++i_) ph_acc[i_] = 0
+#define PH(i)                                            \
+  do {                                                   \
+    if (tid == 0) {                                      \
+      const long long n_ = clock64();                    \
+      ph_acc[i] += (unsigned long long)(n_ - ph_t);      \
+      ph_t = n_;                                         \
+    }                                                    \
+  } while (0)
+#define PH_ITEM() (++ph_items)
+#define PH_END()                                                                  \
+  do {                                                                            \
+    if (tid == 0) {                                                               \
+      for (int i_ = 0; i_ < N_PHASES; ++i_) atomicAdd(&g_phase_cycles[i_], ph_acc[i_]); \
+      atomicAdd(&g_phase_items, (unsigned long long)ph_items);                    \
+    }                                                                             \
+  } while (0)
+#else
+#define PH_BEGIN() \
+  do {             \
+  } while (0)
+#define PH(i) \
+  do {        \
+  } while (0)
+#define PH_ITEM() ((void)0)
+#define PH_END() \
+  do {           \
+  } while (0)
+#endif
+
 template <bool CONV, bool FP16>
 __global__ void __launch_bounds__(PRO_THREADS, 1)
     kda_prologue_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
@@ -324,6 +405,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   const int n_items = num_chunks_of(p) * p.hv;
   if ((int)blockIdx.x >= n_items) return;
   __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.XY + P_TILES);
+  PH_BEGIN();
 
   if (warp == 0) {
     tc::tmem_alloc(&s.tmem, 512);
@@ -358,6 +440,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     tile_phase ^= 1u;
     __syncthreads();
     if constexpr (CONV) conv_tiles(p, tiles, c_glob, h, tid);
+    PH_ITEM();
+    PH(0);
 
     // ---- phase 1: thread = (channel pair: channels c, c + 1 with c = 2 cp;
     // rows 8 hs .. 8 hs + 7, half hh of sub-chunk Rq = hs / 2) ------------------
@@ -438,6 +522,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
     }
     __syncthreads();
+    PH(1);
     float2 mR;  // Lam at row 16 Rq + 7, the sub-chunk's reference
     {
       float2 off = make_float2(0.f, 0.f);
@@ -459,6 +544,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
     }
     __syncthreads();
+    PH(2);
     {
       const float2 lamC = *reinterpret_cast<const float2*>(&s.lamc[c]);
       float2 F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
@@ -503,6 +589,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       tc::fence_before_sync();
       __syncthreads();
       tc::fence_after_sync();
+      PH(3);
 
       // ---- phase 2: A_kk / A_qk, one kind::tf32 product (N = 160) ------------
       if (tid == 0) {
@@ -548,6 +635,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
     tc::fence_after_sync();
+    PH(4);
 
     float* Af = reinterpret_cast<float*>(s.XY + P_A);
     float* Li = reinterpret_cast<float*>(s.XY + P_LI);
@@ -602,6 +690,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
     }
     __syncthreads();
+    PH(5);
 
     // the next item's rows stream in behind the carve
     if (has_next) {
@@ -631,6 +720,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       for (int i = 0; i < 16; ++i) Li[(b0 + i) * LDT + b0 + jc] = x[i];
     }
     __syncthreads();
+    PH(6);
     // 16-row pairs (a, b) = (2P, 2P + 1): thread (P, row i, column pair jp)
     // of the first 256 threads computes two entries
     if (tid < 256) {
@@ -665,6 +755,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       *reinterpret_cast<float2*>(&Li[(b0 + i) * LDT + a0 + j0]) = make_float2(-r.x, -r.y);
     }
     __syncthreads();
+    PH(7);
     // 32-row halves: thread (row pair rp, column pair cp) of the first 256
     // threads computes a 2 x 2 tile; the left factor's rows are 16-byte
     // broadcasts, the right factor's column pairs 8-byte loads
@@ -708,26 +799,21 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       *reinterpret_cast<float2*>(&Li[(33 + i0) * LDT + j0]) = make_float2(-r1.x, -r1.y);
     }
     __syncthreads();
+    PH(8);
 
-    // ---- phase 4: T = L^{-1} diag(beta) into A3 and B2, A3's zero and
-    // identity blocks; thread = (row r, K group g of 8)
+    // ---- phase 4: T^T = (L^{-1} diag(beta))^T into B2 (the B operand of
+    // A_qk T and of R = kg^T T) and the identity block of A3's rows 64..;
+    // thread = (row r, K group g of 8)
     {
       const int r = tid & 63, g = tid >> 6;
       const float br = s.beta[r];
-      uint32_t tv[4], bv[4], iv[4];
-      const float4 l0 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g]);
-      const float4 l1 = *reinterpret_cast<const float4*>(&Li[r * LDT + 8 * g + 4]);
-      const float lr[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+      uint32_t bv[4], iv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i0 = 8 * g + 2 * u;
-        tv[u] = pack_half2(lr[2 * u] * s.beta[i0], lr[2 * u + 1] * s.beta[i0 + 1]);
         bv[u] = pack_half2(Li[i0 * LDT + r] * br, Li[(i0 + 1) * LDT + r] * br);
         iv[u] = pack_half2(i0 == r ? 1.f : 0.f, i0 + 1 == r ? 1.f : 0.f);
       }
-      const uint4 t4 = make_uint4(tv[0], tv[1], tv[2], tv[3]);
-      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 8 * g, 128)) = t4;
-      *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(r, 64 + 8 * g, 128)) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 64 + 8 * g, 128)) =
           make_uint4(iv[0], iv[1], iv[2], iv[3]);
       *reinterpret_cast<uint4*>(B2 + tc::kmajor_offset(r, 8 * g, 64)) =
@@ -736,9 +822,12 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
+    PH(9);
 
-    // ---- phase 5: A_qk T (fp16 MMA) -> A3 rows 64.. (negated); R = kg^T T
-    // (A = kg^T) into columns 128.., read while phase 6 runs
+    // ---- phase 5: A_qk T (fp16 MMA) into columns 0..63 and R = kg^T T
+    // (A = kg^T) into columns 128..191.  Then -A_qk T goes to A3's rows 64..
+    // (beside the identity block) and R to the record and, as the A operand
+    // of P = -R Kg, over kg^T (its last reader was this product).
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
@@ -748,86 +837,86 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
     tc::fence_after_sync();
-    if ((warp & 3) < 2) {
-      const int r = 32 * (warp & 3) + lane, cg = warp >> 2;
-      float a[16];
-      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 16 * cg), a);
-      uint32_t neg[8];
-#pragma unroll
-      for (int t = 0; t < 16; t += 2) neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
-#pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8)
-        *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 16 * cg + 8 * g8, 128)) =
-            make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    // ---- phase 6: [w ; qg'] = A3 [Kg ; qg] (fp16 MMA): w^T to shared memory
-    // (MN-major B operand of P), qg' to the record; -o_intra = (-A_qk T) v
-    // (A = A3's rows 64.., M = 64: row r at lane r % 16 + 32 (r / 16)) into
-    // columns 256.., read while phase 7 runs.  Meanwhile R goes to the record.
-    if (tid == 0) {
-      tc::fence_after_sync();
-      tc::mma_kloop(tmem, smem_u32(A3), smem_u32(s.B3), 128, 128, 128, 0, false);
-      tc::mma_run<4>(tmem + 256, tc::smem_desc(smem_u32(A3) + 1024, 2048, 128),
-                     tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096, tc::idesc_f16(64, 128, 0), false);
-      tc::mma_commit(&s.bar);
-    }
     {
-      tc::fence_after_sync();
-      const int k = 32 * (warp & 3) + lane, cq = warp >> 2;
+      const int sp = warp & 3, cq = warp >> 2;
       float b[16];
-      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * (warp & 3), 128 + 16 * cq), b);
+      tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, 128 + 16 * cq), b);
       uint32_t rv[8];
 #pragma unroll
       for (int t = 0; t < 16; t += 2) rv[t >> 1] = pack_half2(b[t], b[t + 1]);
+      const int k = 32 * sp + lane;
 #pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8)
-        *reinterpret_cast<uint4*>(wsb + CH_R + tc::kmajor_offset(k, 16 * cq + 8 * g8, 128)) =
-            make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
-    }
-    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-    bar_phase ^= 1u;
-    tc::fence_after_sync();
-    unsigned char* WT = s.XY + P_WT;
-    {
-      const int row = 32 * (warp & 3) + lane, cq = warp >> 2;
-      float a[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 32 * cq), a);
-      uint32_t hv[16];
+      for (int g8 = 0; g8 < 2; ++g8) {
+        const uint4 r4 = make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
+        const uint32_t off = tc::kmajor_offset(k, 16 * cq + 8 * g8, 128);
+        *reinterpret_cast<uint4*>(s.KG + off) = r4;
+        *reinterpret_cast<uint4*>(wsb + CH_R + off) = r4;
+      }
+      if (sp < 2) {
+        const int r = 32 * sp + lane;
+        float a[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, 32 * sp, 16 * cq), a);
+        uint32_t neg[8];
 #pragma unroll
-      for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
+        for (int t = 0; t < 16; t += 2) neg[t >> 1] = pack_half2(-a[t], -a[t + 1]);
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const uint4 h4 = make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
-        const int k0 = 32 * cq + 8 * g8;
-        if (row < 64)  // w^T [n = k'][K = r]: 8 consecutive k' of row r
-          *reinterpret_cast<uint4*>(WT + tc::mnmajor_offset(k0, row, WT_LBO, WT_SBO)) = h4;
-        else
-          *reinterpret_cast<uint4*>(wsb + CH_QG + tc::kmajor_offset(row - 64, k0, 64)) = h4;
+        for (int g8 = 0; g8 < 2; ++g8)
+          *reinterpret_cast<uint4*>(A3 + tc::kmajor_offset(64 + r, 16 * cq + 8 * g8, 128)) =
+              make_uint4(neg[4 * g8], neg[4 * g8 + 1], neg[4 * g8 + 2], neg[4 * g8 + 3]);
       }
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
+    PH(10);
 
-    // ---- phase 7: P = -kg^T w (A = kg^T, B = w^T MN-major); meanwhile
-    // -o_intra goes to the record
+    // ---- phase 6, one round of three products (A3r = A3's rows 64..,
+    // M = 64: row r at TMEM lane r % 16 + 32 (r / 16)):
+    //   qg'      = A3r [Kg ; qg] = qg - A_qk T Kg            -> columns 0..127
+    //   P'       = R Kg  (P = -P' = -kg^T T Kg = -kg^T w)      -> columns 128..255
+    //   -o_intra = A3r[:, 0..63] v = -A_qk T v                -> columns 256..383
     if (tid == 0) {
       tc::fence_after_sync();
-      tc::mma_kloop_bmn(tmem, smem_u32(s.KG), smem_u32(WT), 128, 128, 64, WT_LBO, WT_SBO, false);
+      const uint64_t a3r = tc::smem_desc(smem_u32(A3) + 1024, 2048, 128);
+      tc::mma_run<8>(tmem, a3r, tc::smem_desc(smem_u32(s.B3), 2048, 128), 4096, 4096,
+                     tc::idesc_f16(64, 128, 0), false);
+      tc::mma_kloop(tmem + 128, smem_u32(s.KG), smem_u32(s.B3), 128, 128, 64, 0, false);
+      tc::mma_run<4>(tmem + 256, a3r, tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096,
+                     tc::idesc_f16(64, 128, 0), false);
       tc::mma_commit(&s.bar);
     }
+    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+    bar_phase ^= 1u;
+    tc::fence_after_sync();
     {
-      tc::fence_after_sync();
-      // o_intra, value block cq: lanes 0..15 of the warp hold rows 16 (warp & 3) + lane
-      const int cq = warp >> 2;
+      // P (all 128 lanes), then qg' and o_intra (lanes 0..15 of each
+      // sub-partition hold rows 16 sp + lane); warp = (sp, 32-column block cq)
+      const int sp = warp & 3, cq = warp >> 2;
       float a[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 256 + 32 * cq), a);
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 128 + 32 * cq), a);
+      {
+        const int k = 32 * sp + lane;
+        uint32_t hv[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(-a[t], -a[t + 1]);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(wsb + CH_P + tc::kmajor_offset(k, 32 * cq + 8 * g8, 128)) =
+              make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+      }
+      const int r = 16 * sp + (lane & 15);
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 32 * cq), a);
       if (lane < 16) {
-        const int r = 16 * (warp & 3) + lane;
+        uint32_t hv[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8)
+          *reinterpret_cast<uint4*>(wsb + CH_QG + tc::kmajor_offset(r, 32 * cq + 8 * g8, 64)) =
+              make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
+      }
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 256 + 32 * cq), a);
+      if (lane < 16) {
         uint32_t ov[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
@@ -840,24 +929,11 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
               make_uint4(ov[4 * g8], ov[4 * g8 + 1], ov[4 * g8 + 2], ov[4 * g8 + 3]);
       }
     }
-    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-    bar_phase ^= 1u;
-    tc::fence_after_sync();
-    {
-      const int k = 32 * (warp & 3) + lane, cq = warp >> 2;
-      float a[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * (warp & 3), 32 * cq), a);
-      uint32_t hv[16];
-#pragma unroll
-      for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(-a[t], -a[t + 1]);
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(wsb + CH_P + tc::kmajor_offset(k, 32 * cq + 8 * g8, 128)) =
-            make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
-    }
     tc::fence_before_sync();
     __syncthreads();
+    PH(11);
   }  // items
+  PH_END();
   // after an abort, leave no tile load in flight: wait (bounded) for the last
   tc::fence_before_sync();
   __syncthreads();
@@ -1324,8 +1400,8 @@ static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, in
 }
 
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
-  static bool attrs = false;
-  if (!attrs) {
+  static uint64_t attrs_done = 0;
+  once_per_device(attrs_done, [](int) {
     cudaFuncSetAttribute(kda_prologue_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(ProSmem));
     cudaFuncSetAttribute(kda_prologue_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1336,8 +1412,7 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
                          (int)sizeof(WalkSmem));
     cudaFuncSetAttribute(kda_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)((NB * D + D * D) * sizeof(float)));
-    attrs = true;
-  }
+  });
   int max_chunks = 0;
   chunk_workspace_floats(p.n_seqs, p.t_total, p.hv, p.groups, &max_chunks);
   int32_t* iw = reinterpret_cast<int32_t*>(workspace);
@@ -1432,3 +1507,23 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
 }
 
 }  // namespace kda
+
+#ifdef KDA_PHASE_TIMING
+// Measurement build only: copy the prologue's per-phase cycle sums (n of
+// them, at most 12) and its item count to ``out[0..n]`` (out[n] = items),
+// optionally clearing them.  Not part of the regular library's ABI.
+extern "C" int kda_phase_cycles(unsigned long long* out, int32_t n, int32_t reset) {
+  if (!out || n < 1 || n > kda::N_PHASES) return KDA_ERR_INVALID_ARGUMENT;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(out, kda::g_phase_cycles, n * sizeof(unsigned long long)) != cudaSuccess ||
+      cudaMemcpyFromSymbol(out + n, kda::g_phase_items, sizeof(unsigned long long)) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (reset) {
+    const unsigned long long zero[kda::N_PHASES + 1] = {};
+    if (cudaMemcpyToSymbol(kda::g_phase_cycles, zero, kda::N_PHASES * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMemcpyToSymbol(kda::g_phase_items, zero, sizeof(unsigned long long)) != cudaSuccess)
+      return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+#endif

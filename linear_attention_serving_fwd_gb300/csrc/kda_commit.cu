@@ -269,16 +269,18 @@ __global__ void __launch_bounds__(CM_THREADS, 1) kda_commit_kernel(const CommitP
 }
 
 int launch_commit(const CommitParams& p, cudaStream_t stream) {
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  static int sms[64] = {0};
+  static uint64_t done = 0;
+  int dev = 0;
+  once_per_device(done, [&](int d) {
+    cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d);
     cudaFuncSetAttribute(kda_commit_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(CommitSmem));
     cudaFuncSetAttribute(kda_commit_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)sizeof(CommitSmem));
-  }
+  });
+  cudaGetDevice(&dev);
+  const int num_sms = sms[dev & 63] > 0 ? sms[dev & 63] : 152;
   const int items = p.n_req * p.hv;
   if (items == 0) return 0;
   const int grid = items < num_sms ? items : num_sms;

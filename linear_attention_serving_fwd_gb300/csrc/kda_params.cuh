@@ -1,6 +1,8 @@
 // Kernel parameter blocks shared by the API layer and the kernels.
 #pragma once
 
+#include <mutex>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -118,6 +120,24 @@ void trace_end(cudaStream_t stream);
 // Set the thread-local text that kda_last_error() returns.
 void set_last_error(int code, const char* msg);
 
+// Host: per-device set-up (kernel attributes, SM counts, symbol addresses)
+// runs once per device under one library-wide lock, so that threads making
+// their first calls at the same time do not race.  ``done`` has one bit per
+// device (devices 0..63).  Returns false without running ``fn`` when no
+// device is current.
+std::mutex& host_mutex();
+template <class F>
+inline bool once_per_device(uint64_t& done, F&& fn) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(host_mutex());
+  if (!(done & (1ull << dev))) {
+    fn(dev);
+    done |= 1ull << dev;
+  }
+  return true;
+}
+
 // Launchers (kernels' translation units); return 0 or -1 (see cudaGetLastError).
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream);
 int launch_commit(const CommitParams& p, cudaStream_t stream);
@@ -126,5 +146,6 @@ int launch_conv_prefill(const ChunkParams& p, cudaStream_t stream);
 int launch_conv_roll(const WindowParams& p, cudaStream_t stream);
 size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* max_chunks_out);
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream);
+int launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace kda

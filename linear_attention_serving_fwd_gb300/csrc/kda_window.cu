@@ -818,14 +818,13 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
 template <bool VERIFY, bool SBF16, bool FP16, int WR, int NBUF = (WR == 4 ? 2 : 1)>
 static void launch_window_t(const WindowParams& p, int num_sms, cudaStream_t stream) {
   constexpr int smem = (int)sizeof(WinSmem) + (WR == 8 ? EXTRA_WR8 : EXTRA_WR4);
-  static bool attr = false;
-  if (!attr) {
+  static uint64_t done = 0;
+  once_per_device(done, [](int) {
     cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR, NBUF>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaFuncSetAttribute(kda_window_kernel<VERIFY, SBF16, FP16, WR, NBUF>,
                          cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    attr = true;
-  }
+  });
   const int items = p.n_req * p.hv;
   const int slots = (WR == 8 ? 2 : 1) * num_sms;  // resident CTAs
   const int grid = items < slots ? items : slots;
@@ -833,12 +832,12 @@ static void launch_window_t(const WindowParams& p, int num_sms, cudaStream_t str
 }
 
 int launch_window(const WindowParams& p, bool verify, cudaStream_t stream) {
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-  }
+  static int sms[64] = {0};
+  static uint64_t done = 0;
+  once_per_device(done, [&](int d) { cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d); });
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int num_sms = sms[dev & 63] > 0 ? sms[dev & 63] : 152;
   const int items = p.n_req * p.hv;
   if (items == 0) return 0;
   // decode of one token per request moves the state with almost no

@@ -23,6 +23,10 @@ intended serving traffic):
 
 q, k, v, g and the beta logits are N(0, 1); A_log = log(U[1, 16]) per head,
 dt_bias ~ N(0, 0.1) per head and channel, lower_bound = -5, scale = 128^-0.5.
+
+Without gate parameters (``log_decay=(lo, hi)``) g is drawn U[lo, hi] in its
+place in the draw order and used as the per-channel log decay itself; A_log
+and dt_bias are still drawn (the order stays fixed) and then dropped.
 """
 from __future__ import annotations
 
@@ -110,15 +114,21 @@ def _uniform(gen, shape, lo, hi, device):
     return torch.rand(shape, generator=gen, device=device, dtype=torch.float32) * (hi - lo) + lo
 
 
-def _draw_activations(gen, t_total, hqk, hv, device, g_std=1.0, g_shift=0.0, dtype=torch.bfloat16):
+def _draw_activations(gen, t_total, hqk, hv, device, g_std=1.0, g_shift=0.0, dtype=torch.bfloat16,
+                      log_decay=None):
     bf = dtype  # activation storage: bf16 (default) or fp16, from the same fp32 draws
     q = _normal(gen, (t_total, hqk, D), 1.0, device).to(bf)
     k = _normal(gen, (t_total, hqk, D), 1.0, device).to(bf)
     v = _normal(gen, (t_total, hv, D), 1.0, device).to(bf)
-    g = (_normal(gen, (t_total, hv, D), g_std, device) + g_shift).to(bf)
+    if log_decay is None:
+        g = (_normal(gen, (t_total, hv, D), g_std, device) + g_shift).to(bf)
+    else:
+        g = _uniform(gen, (t_total, hv, D), log_decay[0], log_decay[1], device).to(bf)
     beta = _normal(gen, (t_total, hv), 1.0, device).to(bf)
     A_log = torch.log(_uniform(gen, (hv,), 1.0, 16.0, device))
     dt_bias = _normal(gen, (hv, D), 0.1, device)
+    if log_decay is not None:  # no gate parameters: g is the log decay
+        A_log = dt_bias = None
     return q, k, v, g, beta, A_log, dt_bias
 
 
@@ -126,11 +136,13 @@ def dense_prefill(B: int, T: int, hqk: int, hv: int, *, seed: int = 0, device="c
                   init_state: bool = True, state_std: float = 0.02,
                   lower_bound: float = -5.0, g_shift: float = 0.0,
                   scale: float = D ** -0.5, name: str = "dense",
-                  act_dtype=torch.bfloat16, state_dtype=torch.float32) -> KdaInputs:
+                  act_dtype=torch.bfloat16, state_dtype=torch.float32,
+                  log_decay=None) -> KdaInputs:
     """Dense [B, T] prefill flattened to T_tot = B*T tokens."""
     gen = _gen(seed, device)
     q, k, v, g, beta, A_log, dt_bias = _draw_activations(gen, B * T, hqk, hv, device,
-                                                         g_shift=g_shift, dtype=act_dtype)
+                                                         g_shift=g_shift, dtype=act_dtype,
+                                                         log_decay=log_decay)
     h0 = _normal(gen, (B, hv, D, D), state_std, device).to(state_dtype) if init_state else None
     cu = torch.arange(0, B + 1, dtype=torch.int32, device=device) * T
     return KdaInputs(name=name, q=q, k=k, v=v, g=g, beta=beta, A_log=A_log,
@@ -153,7 +165,7 @@ def varlen_paged(lens_or_n, hqk: int, hv: int, *, total: Optional[int] = None,
                  lower_bound: float = -5.0, g_shift: float = 0.0,
                  state_std: float = 0.02, has_initial=None,
                  name: str = "varlen", act_dtype=torch.bfloat16,
-                 state_dtype=torch.float32) -> KdaInputs:
+                 state_dtype=torch.float32, log_decay=None) -> KdaInputs:
     """Varlen prefill on a paged state cache (fp32 unless ``state_dtype``).
 
     ``lens_or_n`` is either an explicit list of lengths or a sequence count,
@@ -170,7 +182,8 @@ def varlen_paged(lens_or_n, hqk: int, hv: int, *, total: Optional[int] = None,
         n = len(lens_or_n)
         t_total = int(sum(lens_or_n))
     q, k, v, g, beta, A_log, dt_bias = _draw_activations(gen, t_total, hqk, hv, device,
-                                                         g_shift=g_shift, dtype=act_dtype)
+                                                         g_shift=g_shift, dtype=act_dtype,
+                                                         log_decay=log_decay)
     pool = _normal(gen, (slots, hv, D, D), state_std, device).to(state_dtype)
     if isinstance(lens_or_n, int):
         lens = rescaled_lengths(gen, n, total, 64.0, 8192.0, device)
@@ -192,7 +205,8 @@ def decode_batch(n_req: int, window: int, hqk: int, hv: int, *, slots: int = 512
                  seed: int = 0, device="cpu", qlens=None, null_requests=(),
                  lower_bound: float = -5.0, g_shift: float = 0.0,
                  state_std: float = 0.02, name: str = "decode",
-                 act_dtype=torch.bfloat16, state_dtype=torch.float32) -> KdaInputs:
+                 act_dtype=torch.bfloat16, state_dtype=torch.float32,
+                 log_decay=None) -> KdaInputs:
     """Batched decode / verify: each request has ``window`` new tokens (or
     ``qlens[b]`` <= window), one state slot each, drawn without replacement.
     Requests listed in ``null_requests`` get slot -1 (a padding entry)."""
@@ -202,7 +216,8 @@ def decode_batch(n_req: int, window: int, hqk: int, hv: int, *, slots: int = 512
     assert all(0 <= x <= window for x in qlens)
     t_total = int(sum(qlens))
     q, k, v, g, beta, A_log, dt_bias = _draw_activations(gen, t_total, hqk, hv, device,
-                                                         g_shift=g_shift, dtype=act_dtype)
+                                                         g_shift=g_shift, dtype=act_dtype,
+                                                         log_decay=log_decay)
     pool = _normal(gen, (slots, hv, D, D), state_std, device).to(state_dtype)
     idx = torch.randperm(slots, generator=gen, device=device)[:n_req].to(torch.int32)
     for b in null_requests:

@@ -310,3 +310,11 @@ def test_host_prefill_validation():
     assert need > mirrors + 2 * hv * 128 * 128 * 4
     assert lib.kda_chunk_fwd_host_workspace_bytes(ctypes.byref(a), cu, 2, 100, 0) == 0
     assert "segment_tokens" in _msg()
+
+
+def test_wait_selftest_rejects_out_of_range_limits():
+    """The bounded-wait self-test validates its limit before any launch."""
+    lib = _native.lib()
+    for bad in (0, 2_000_000):
+        assert lib.kda_selftest_wait_timeout(bad, None) == INVALID
+        assert "limit_us" in lib.kda_last_error().decode()
