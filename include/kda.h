@@ -57,7 +57,10 @@ typedef enum kda_status {
   KDA_ERR_UNSUPPORTED_DTYPE = 2, /* a dtype outside bf16/fp16 activations */
   KDA_ERR_CUDA = 3,              /* a CUDA runtime call or launch failed */
   KDA_ERR_DEVICE_TIMEOUT = 4,    /* a bounded device wait expired */
-  KDA_ERR_DEVICE_INDEX = 5       /* a kernel met a bad slot / length */
+  KDA_ERR_DEVICE_INDEX = 5,      /* a kernel met a bad slot / length */
+  KDA_ERR_DEVICE_RANGE = 6       /* a prefill without gate parameters met a raw
+                                    log decay outside [-10.5, 0]: its outputs
+                                    and states are not valid */
 } kda_status;
 
 enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_FP16 = 1 };
@@ -200,8 +203,10 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
  * cu_seqlens must start at 0, be non-decreasing and end at T; a violation
  * found on the device sets KDA_ERR_DEVICE_INDEX.  The gate's 16-token
  * sub-chunk factorisation needs any 8 consecutive per-token log decays to
- * sum above -87, inside fp32's exponent range (always true for
- * lower_bound >= -10.5, which is enforced).
+ * sum above -87, inside fp32's exponent range: always true for
+ * lower_bound >= -10.5, which is enforced.  Without A_log / dt_bias every raw
+ * g must lie in [-10.5, 0]; a value outside it (or NaN) sets
+ * KDA_ERR_DEVICE_RANGE, and that call's outputs and states are not valid.
  */
 int kda_chunk_fwd(const kda_activations* x, void* out, const int32_t* cu_seqlens,
                   int32_t n_seqs, const void* initial_state, void* final_state,
@@ -466,8 +471,9 @@ const char* kda_last_error(void);
 
 /*
  * kda_device_status - synchronise ``stream``, read this device's error word
- * and return KDA_OK, KDA_ERR_DEVICE_INDEX or KDA_ERR_DEVICE_TIMEOUT (the
- * most severe seen since the last clear).  clear != 0 resets the word.
+ * and return KDA_OK, KDA_ERR_DEVICE_INDEX, KDA_ERR_DEVICE_RANGE or
+ * KDA_ERR_DEVICE_TIMEOUT (the most severe seen since the last clear, in the
+ * order timeout, index, range).  clear != 0 resets the word.
  */
 int kda_device_status(void* stream, int32_t clear);
 

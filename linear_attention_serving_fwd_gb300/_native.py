@@ -21,6 +21,7 @@ KDA_ERR_UNSUPPORTED_DTYPE = 2
 KDA_ERR_CUDA = 3
 KDA_ERR_DEVICE_TIMEOUT = 4
 KDA_ERR_DEVICE_INDEX = 5
+KDA_ERR_DEVICE_RANGE = 6
 KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP16 = 1
 

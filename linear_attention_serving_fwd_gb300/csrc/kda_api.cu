@@ -938,6 +938,9 @@ int kda_device_status(void* stream, int32_t clear) {
   if (word & kda::ERR_TIMEOUT) return fail(KDA_ERR_DEVICE_TIMEOUT, "a bounded device wait expired.");
   if (word & kda::ERR_INDEX)
     return fail(KDA_ERR_DEVICE_INDEX, "a kernel met an out-of-range slot or sequence length.");
+  if (word & kda::ERR_RANGE)
+    return fail(KDA_ERR_DEVICE_RANGE,
+                "a prefill without gate parameters met a raw log decay outside [-10.5, 0].");
   return ok();
 }
 

@@ -215,9 +215,18 @@ constexpr uint32_t P_A3 = 17408;     // fp16 [128][128] = [[T, 0], [-A_qk T, I]]
 constexpr uint32_t P_A2 = 50176;     // fp16 [128][64]  = [A_qk ; 0]
 constexpr uint32_t P_B2 = 66560;     // fp16 [64][64]   = T^T
 constexpr uint32_t P_TILES = 75776;  // bf16 tiles of the next item (below)
+// Record staging in the last round.  P is written while qg' and o_intra
+// still read A3, so its two 16 KB halves go where L^{-1} and A2 were; qg' and
+// o_intra follow over A3 once every product is done.
+constexpr uint32_t ST_P0 = 0;        // P record bytes [0, 16384)
+constexpr uint32_t ST_P1 = 50176;    // P record bytes [16384, 32768)
+constexpr uint32_t ST_QG = 16384;    // qg' then o_intra (32 KB)
 static_assert(P_LI + 64 * LDT * 4 <= P_A && P_A + 64 * LDT * 4 <= P_W, "prologue carve");
 static_assert(P_W + 32 * LDW * 4 <= P_A3 + 32768 && P_A3 + 32768 <= P_A2, "A3 covers A and W");
 static_assert(P_A2 + 16384 <= P_B2 && P_B2 + 8192 <= P_TILES, "prologue carve");
+static_assert(ST_P0 + 16384 <= P_A3 && P_A3 + 32768 <= ST_P1 && ST_P1 + 16384 <= P_TILES,
+              "P staging stays clear of A3, which the last products read");
+static_assert(ST_P0 + 16384 <= ST_QG && ST_QG + 32768 <= ST_P1, "record staging");
 
 struct __align__(1024) ProSmem {
   // X (tf32, 128 x 128) at XY, Y_0 .. Y_3 stacked (tf32 [YROWS][128]) at
@@ -226,15 +235,13 @@ struct __align__(1024) ProSmem {
   unsigned char B3[32768];  // fp16 [c][K]: K 0..63 = Kg rows, 64..127 = qg rows
   unsigned char KG[16384];  // fp16 kg^T, K-major [k][r]
   unsigned char VT[16384];  // fp16 v^T, K-major [v][r] (K groups 2048 bytes apart)
-  float ref[4][128];        // m_R = Lam at row 16R + 7
   float qtot[8][128];       // gate sum of each 8-row half sub-chunk
   float ssk[2][64];         // |k_r|^2 partial per group of 64 channels
   float ssq[2][64];
-  float lamc[128];          // Lam at row 63
-  float rk[64], rq[64];     // 1/|k_r| and scale/|q_r|
   float beta[64];
   int4 meta[2];             // (chunk, head, first token, rows) of this and the next item
   uint64_t bar;
+  uint64_t bar2;            // the P product of the last round, ahead of the others
   uint64_t tbar;            // tile loads
   uint32_t tmem;
   int abort;
@@ -413,6 +420,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   }
   if (tid == 0) {
     mbar_init(&s.bar, 1);
+    mbar_init(&s.bar2, 1);
     mbar_init(&s.tbar, 1);
     fence_mbar_init();
     s.abort = 0;
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
   ItemScalars sc = load_scalars(p, s.meta[0], tid);
-  uint32_t bar_phase = 0, tile_phase = 0, tiles_issued = 1;
+  uint32_t bar_phase = 0, bar2_phase = 0, tile_phase = 0, tiles_issued = 1;
   int cur = 0;
   for (int t = blockIdx.x; t < n_items; t += gridDim.x, cur ^= 1) {
     // this CTA's last item: the walk may start its setup on the SMs that
@@ -450,6 +458,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     float2 lam[8], kv[8], qv[8];  // per row, the two channels
     {
       float2 acc = make_float2(0.f, 0.f);
+      bool gate_bad = false;
       uint32_t vw[2][4];  // v of channels c and c + 1 as fp16 pairs along rows
       const float2 ah2 = make_float2(a_h, a_h), adt2 = make_float2(a_h * sc.dt.x, a_h * sc.dt.y);
       const float2 zero2 = make_float2(0.f, 0.f);
@@ -468,6 +477,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
             const float2 t = ffma2(ah2, g, adt2);
             const float2 den = fadd2(make_float2(__expf(-t.x), __expf(-t.y)), make_float2(1.f, 1.f));
             g = in ? make_float2(__fdividef(p.lower_bound, den.x), __fdividef(p.lower_bound, den.y)) : zero2;
+          } else {  // g is the log decay itself: it must lie in [-10.5, 0]
+            gate_bad |= !(g.x >= -10.5f && g.x <= 0.f && g.y >= -10.5f && g.y <= 0.f);
           }
           acc = fadd2(acc, g);
           lam[i + e] = acc;
@@ -476,6 +487,9 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         vw[0][i >> 1] = pack_half2(vv[0].x, vv[1].x);
         vw[1][i >> 1] = pack_half2(vv[0].y, vv[1].y);
       }
+      // a raw log decay outside [-10.5, 0] (or NaN) leaves the exponent range
+      // the factored A_kk / A_qk operands are built for: report it
+      if (!p.has_gate && __any_sync(0xffffffffu, gate_bad) && lane == 0) set_error(p.err, ERR_RANGE);
       // v^T of the two channels: the record's block c / 32, and VT for o_intra
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -520,49 +534,49 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         s.ssk[cp >> 5][row] = pk[0];
         s.ssq[cp >> 5][row] = pq[0];
       }
+      // the last item's record stores have read the staging area, which the
+      // X / Y build below overwrites
+      if (tid == 0) bulk_wait_read<0>();
     }
     __syncthreads();
     PH(1);
     float2 mR;  // Lam at row 16 Rq + 7, the sub-chunk's reference
     {
-      float2 off = make_float2(0.f, 0.f);
-      for (int h2 = 0; h2 < hs; ++h2) off = fadd2(off, *reinterpret_cast<const float2*>(&s.qtot[h2][c]));
+      // Every thread reads what it needs straight from the half-sub-chunk
+      // gate totals and the norm partials: its rows' offset (the totals of
+      // the halves before), the references m_R = Lam at row 16 R + 7 (the
+      // totals of halves 0 .. 2R), Lam_C (all eight) and its rows' norms.
+      float2 run = make_float2(0.f, 0.f), off = run, mref[4];
+#pragma unroll
+      for (int h2 = 0; h2 < 8; ++h2) {
+        if (h2 == hs) off = run;
+        run = fadd2(run, *reinterpret_cast<const float2*>(&s.qtot[h2][c]));
+        if ((h2 & 1) == 0) mref[h2 >> 1] = run;
+      }
+      const float2 lamC = run;
 #pragma unroll
       for (int i = 0; i < 8; ++i) lam[i] = fadd2(lam[i], off);
-      // the first half holds row 16 Rq + 7 itself; the second half starts after it
-      mR = hh == 0 ? lam[7] : off;
-      if (hh == 0) *reinterpret_cast<float2*>(&s.ref[Rq][c]) = mR;
-      if (hs == 7) {
-        *reinterpret_cast<float2*>(&s.lamc[c]) = lam[7];
-        *reinterpret_cast<float2*>(wsb + CH_D + 4 * c) = make_float2(__expf(lam[7].x), __expf(lam[7].y));
-      }
-      if (tid < 64) {
-        const float sk = s.ssk[0][tid] + s.ssk[1][tid];
-        const float sq = s.ssq[0][tid] + s.ssq[1][tid];
-        s.rk[tid] = rsqrtf(sk + 1e-6f);
-        s.rq[tid] = rsqrtf(sq + 1e-6f) * p.scale;
-      }
-    }
-    __syncthreads();
-    PH(2);
-    {
-      const float2 lamC = *reinterpret_cast<const float2*>(&s.lamc[c]);
+      mR = Rq == 0 ? mref[0] : (Rq == 1 ? mref[1] : (Rq == 2 ? mref[2] : mref[3]));
+      if (hs == 7)
+        *reinterpret_cast<float2*>(wsb + CH_D + 4 * c) = make_float2(__expf(lamC.x), __expf(lamC.y));
       float2 F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
 #pragma unroll
-      for (int R2 = 0; R2 < 4; ++R2) {
-        const float2 m2 = *reinterpret_cast<const float2*>(&s.ref[R2][c]);
-        F[R2] = R2 > Rq ? make_float2(__expf(m2.x - mR.x), __expf(m2.y - mR.y)) : make_float2(1.f, 1.f);
-      }
-      // normalised keys and queries (the row norms: 16-byte broadcasts)
+      for (int R2 = 0; R2 < 4; ++R2)
+        F[R2] = R2 > Rq ? make_float2(__expf(mref[R2].x - mR.x), __expf(mref[R2].y - mR.y)) : make_float2(1.f, 1.f);
+      // normalised keys and queries: lane l of the warp forms 1/|k_r| (l & 8
+      // clear) or scale/|q_r| (l & 8 set) of row r = 8 hs + (l & 7) from the
+      // two channel halves' partial sums; shuffles hand the warp's 8 rows to
+      // every lane
+      {
+        const int rr = 8 * hs + (lane & 7);
+        const bool isq = (lane & 8) != 0;
+        const float sum = isq ? s.ssq[0][rr] + s.ssq[1][rr] : s.ssk[0][rr] + s.ssk[1][rr];
+        const float nrm = isq ? rsqrtf(sum + 1e-6f) * p.scale : rsqrtf(sum + 1e-6f);
 #pragma unroll
-      for (int i4 = 0; i4 < 8; i4 += 4) {
-        const float4 r4 = *reinterpret_cast<const float4*>(&s.rk[8 * hs + i4]);
-        const float4 q4 = *reinterpret_cast<const float4*>(&s.rq[8 * hs + i4]);
-        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          kv[i4 + u] = fmul2(kv[i4 + u], make_float2(rr[u], rr[u]));
-          qv[i4 + u] = fmul2(qv[i4 + u], make_float2(qq[u], qq[u]));
+        for (int i = 0; i < 8; ++i) {
+          const float rr_k = __shfl_sync(0xffffffffu, nrm, i), rr_q = __shfl_sync(0xffffffffu, nrm, 8 + i);
+          kv[i] = fmul2(kv[i], make_float2(rr_k, rr_k));
+          qv[i] = fmul2(qv[i], make_float2(rr_q, rr_q));
         }
       }
       // X and Y first (8-byte pairs of tf32 along the channels): the A_kk /
@@ -635,6 +649,9 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
     tc::fence_after_sync();
+    // the product has read Y: the next item's rows stream in over it (the
+    // carve below stays under P_TILES)
+    if (tid == 32 && has_next) load_tiles<CONV>(p, maps, s.meta[cur ^ 1], tiles, &s.tbar);
     PH(4);
 
     float* Af = reinterpret_cast<float*>(s.XY + P_A);
@@ -692,12 +709,10 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     __syncthreads();
     PH(5);
 
-    // the next item's rows stream in behind the carve
+    // the next item's scalars (its tiles are already on their way)
     if (has_next) {
-      const int4 mn = s.meta[cur ^ 1];
-      if (tid == 96) load_tiles<CONV>(p, maps, mn, tiles, &s.tbar);  // a warp idle in the diagonal solve
       tiles_issued += 1;
-      sc = load_scalars(p, mn, tid);
+      sc = load_scalars(p, s.meta[cur ^ 1], tid);
     }
 
     // ---- phase 3: L^{-1} by recursive doubling ---------------------------------
@@ -826,8 +841,9 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
 
     // ---- phase 5: A_qk T (fp16 MMA) into columns 0..63 and R = kg^T T
     // (A = kg^T) into columns 128..191.  Then -A_qk T goes to A3's rows 64..
-    // (beside the identity block) and R to the record and, as the A operand
-    // of P = -R Kg, over kg^T (its last reader was this product).
+    // (beside the identity block) and R, as the A operand of P = -R Kg, over
+    // kg^T (its last reader was this product); R leaves for the record from
+    // there with the item's other records.
     if (tid == 0) {
       tc::fence_after_sync();
       tc::mma_kloop(tmem, smem_u32(A2), smem_u32(B2), 128, 64, 64, 0, false);
@@ -846,12 +862,9 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       for (int t = 0; t < 16; t += 2) rv[t >> 1] = pack_half2(b[t], b[t + 1]);
       const int k = 32 * sp + lane;
 #pragma unroll
-      for (int g8 = 0; g8 < 2; ++g8) {
-        const uint4 r4 = make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
-        const uint32_t off = tc::kmajor_offset(k, 16 * cq + 8 * g8, 128);
-        *reinterpret_cast<uint4*>(s.KG + off) = r4;
-        *reinterpret_cast<uint4*>(wsb + CH_R + off) = r4;
-      }
+      for (int g8 = 0; g8 < 2; ++g8)
+        *reinterpret_cast<uint4*>(s.KG + tc::kmajor_offset(k, 16 * cq + 8 * g8, 128)) =
+            make_uint4(rv[4 * g8], rv[4 * g8 + 1], rv[4 * g8 + 2], rv[4 * g8 + 3]);
       if (sp < 2) {
         const int r = 32 * sp + lane;
         float a[16];
@@ -877,20 +890,24 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     //   -o_intra = A3r[:, 0..63] v = -A_qk T v                -> columns 256..383
     if (tid == 0) {
       tc::fence_after_sync();
+      // P' first, on a barrier of its own: its epilogue runs while the
+      // tensor core works on qg' and o_intra
+      tc::mma_kloop(tmem + 128, smem_u32(s.KG), smem_u32(s.B3), 128, 128, 64, 0, false);
+      tc::mma_commit(&s.bar2);
       const uint64_t a3r = tc::smem_desc(smem_u32(A3) + 1024, 2048, 128);
       tc::mma_run<8>(tmem, a3r, tc::smem_desc(smem_u32(s.B3), 2048, 128), 4096, 4096,
                      tc::idesc_f16(64, 128, 0), false);
-      tc::mma_kloop(tmem + 128, smem_u32(s.KG), smem_u32(s.B3), 128, 128, 64, 0, false);
       tc::mma_run<4>(tmem + 256, a3r, tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096,
                      tc::idesc_f16(64, 128, 0), false);
       tc::mma_commit(&s.bar);
     }
-    wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
-    bar_phase ^= 1u;
+    wait_or_abort(&s.bar2, bar2_phase, &s.abort, p.err);
+    bar2_phase ^= 1u;
     tc::fence_after_sync();
     {
       // P (all 128 lanes), then qg' and o_intra (lanes 0..15 of each
-      // sub-partition hold rows 16 sp + lane); warp = (sp, 32-column block cq)
+      // sub-partition hold rows 16 sp + lane) into the staging area in their
+      // record layouts; warp = (sp, 32-column block cq)
       const int sp = warp & 3, cq = warp >> 2;
       float a[32];
       tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 128 + 32 * cq), a);
@@ -899,11 +916,16 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         uint32_t hv[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(-a[t], -a[t + 1]);
+        // columns 32 cq .. are K groups 4 cq .., record bytes 8192 cq ..
+        unsigned char* pst = s.XY + (cq < 2 ? ST_P0 : ST_P1 - 16384u);
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(wsb + CH_P + tc::kmajor_offset(k, 32 * cq + 8 * g8, 128)) =
+          *reinterpret_cast<uint4*>(pst + tc::kmajor_offset(k, 32 * cq + 8 * g8, 128)) =
               make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
       }
+      wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
+      bar_phase ^= 1u;
+      tc::fence_after_sync();
       const int r = 16 * sp + (lane & 15);
       tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 32 * cq), a);
       if (lane < 16) {
@@ -912,7 +934,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(wsb + CH_QG + tc::kmajor_offset(r, 32 * cq + 8 * g8, 64)) =
+          *reinterpret_cast<uint4*>(s.XY + ST_QG + tc::kmajor_offset(r, 32 * cq + 8 * g8, 64)) =
               make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
       }
       tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 256 + 32 * cq), a);
@@ -925,12 +947,23 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         }
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(wsb + CH_OI + cq * OI_BLOCK + r * 64 + 16 * g8) =
+          *reinterpret_cast<uint4*>(s.XY + ST_QG + (CH_OI - CH_QG) + cq * OI_BLOCK + r * 64 + 16 * g8) =
               make_uint4(ov[4 * g8], ov[4 * g8 + 1], ov[4 * g8 + 2], ov[4 * g8 + 3]);
       }
     }
+    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
+    // the item's P, R, qg' and o_intra records leave by four bulk stores;
+    // their shared-memory reads finish before the next item's X / Y build
+    // writes over the staging area (and its Kg build over R)
+    if (tid == 0) {
+      bulk_s2g(wsb + CH_P, s.XY + ST_P0, 16384);
+      bulk_s2g(wsb + CH_P + 16384, s.XY + ST_P1, 16384);
+      bulk_s2g(wsb + CH_R, s.KG, 128 * 64 * 2);
+      bulk_s2g(wsb + CH_QG, s.XY + ST_QG, CH_V16 - CH_QG);
+      bulk_commit();
+    }
     PH(11);
   }  // items
   PH_END();
@@ -938,6 +971,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (tid == 0 && s.abort) mbar_wait_bounded(&s.tbar, (tiles_issued - 1) & 1, p.err);
+  if (tid == 0) bulk_wait<0>();  // every record store has landed
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 

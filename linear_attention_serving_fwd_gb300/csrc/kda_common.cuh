@@ -17,6 +17,7 @@ constexpr int MAX_WINDOW = 8;
 // Error bits of the per-device error word.
 constexpr unsigned ERR_INDEX = 1u;    // bad slot / length seen by a kernel
 constexpr unsigned ERR_TIMEOUT = 2u;  // a bounded wait expired
+constexpr unsigned ERR_RANGE = 4u;    // a prefill without gate parameters met a log decay outside [-10.5, 0]
 
 // Bounded waits: every mbarrier / flag spin gives up after WAIT_NS of wall
 // time (read from %globaltimer every 64 rounds) or WAIT_CAP rounds, far

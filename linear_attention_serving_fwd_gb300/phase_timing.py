@@ -19,16 +19,16 @@ import json
 PHASES = (
     "tile wait (next item's q/k/v/g tiles)",
     "gate, gate cumsum, v record, row norms",
-    "offsets, sub-chunk references, 1/|k|, scale/|q|",
-    "X / Y operands (tf32)",
-    "A_kk / A_qk product (N = 160) with the Kg / qg / kg build",
+    "(offsets, references and norms: now inside the next phase)",
+    "offsets, references, norms; X / Y operands (tf32)",
+    "A_kk / A_qk product (N = 160) with the Kg / qg / kg build; next tiles issued",
     "TMEM read, A carve",
-    "next tiles issue, diagonal 16 x 16 inverses",
-    "16-row pairs (two products)",
-    "32-row halves (two products)",
+    "inverse: diagonal 16 x 16 blocks (forward substitution)",
+    "inverse: 16-row pairs (two products)",
+    "inverse: 32-row halves (two products)",
     "T^T and the identity block",
-    "A_qk T + R products, -A_qk T and R stores",
-    "qg' + P + o_intra products, their records",
+    "A_qk T + R products, -A_qk T and R to shared memory",
+    "qg' + P + o_intra products, records staged and bulk-stored",
 )
 
 

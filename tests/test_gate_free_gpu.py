@@ -117,3 +117,18 @@ def test_commit_gate_free():
         S = oracle.recurrence(x.q[qs:qs + a], x.k[qs:qs + a], x.v[qs:qs + a], x.g[qs:qs + a],
                               x.beta[qs:qs + a], [0, a], h0=pool0[idx[b]][None])["state"]
         check_state(got[idx[b]:idx[b] + 1], S, f"request {b} accepted {a}")
+
+
+def test_log_decay_out_of_range_is_reported():
+    """A raw log decay below -10.5 leaves the exponent range the chunk
+    kernels factor: the prefill reports KDA_ERR_DEVICE_RANGE (and a clean
+    call afterwards reports nothing)."""
+    import linear_attention_serving_fwd_gb300 as kda
+    from linear_attention_serving_fwd_gb300 import _native
+    x = W.dense_prefill(1, 130, 1, 2, seed=59, log_decay=STRONG).to("cuda")
+    g = x.g.clone()
+    g[70, 1, 5] = -11.0
+    kda.kda_chunk_fwd(x.q, x.k, x.v, g, x.beta, n_seqs=1, output_final_state=True)
+    assert kda.kda_device_status(clear=True) == _native.KDA_ERR_DEVICE_RANGE
+    kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, n_seqs=1, output_final_state=True)
+    assert kda.kda_device_status(clear=True) == 0
