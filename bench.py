@@ -37,7 +37,11 @@ sys.path.insert(0, ROOT)
 
 D = 128
 CHUNK = 64
-WORKLOAD = dict(name="long", B=1, T=131072, hqk=32, hv=32)
+# --workload dense: the dense serving prefill as the headline (profiling aid;
+# its inputs are about L2-sized, so L2 is flushed before every step)
+WORKLOADS = {"long": dict(name="long", B=1, T=131072, hqk=32, hv=32),
+             "dense": dict(name="dense", B=2, T=4096, hqk=16, hv=16)}
+WORKLOAD = dict(WORKLOADS["long"])
 METRIC = "chunk_kda prefill tokens/s"
 REF_SAMPLE_HEADS = 2  # heads of the workload the reference arm's step runs
 
@@ -56,13 +60,21 @@ def parse():
                     help="comma list of extra workloads: dense, varlen, groups, checkpoint, prefill_conv, "
                          "prefill_fp16, commit, decode_steps, decode_bf16, verify_conv, verify, decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long",
+                    help="the headline workload: long (default, B=1 T=131072 H=32) or dense "
+                         "(B=2 T=4096 H=16, h0 given)")
+    args = ap.parse_args()
+    WORKLOAD.clear()
+    WORKLOAD.update(WORKLOADS[args.workload])
+    return args
 
 
 def workload_desc():
     w = WORKLOAD
-    return (f"long-context prefill B={w['B']} T={w['T']} Hqk={w['hqk']} Hv={w['hv']} D=128, bf16 "
-            f"q/k/v/g/beta N(0,1), zero initial state, final state returned, lower_bound=-5, "
+    h0 = "zero initial state" if w["name"] == "long" else "initial state N(0,0.02)"
+    kind = "long-context" if w["name"] == "long" else "dense"
+    return (f"{kind} prefill B={w['B']} T={w['T']} Hqk={w['hqk']} Hv={w['hv']} D=128, bf16 "
+            f"q/k/v/g/beta N(0,1), {h0}, final state returned, lower_bound=-5, "
             f"A_log=log U[1,16], dt_bias N(0,0.1)")
 
 
@@ -278,12 +290,13 @@ def run_ours(args, rank, world, barrier, reduce_max):
     def step():
         kda.kda_chunk_fwd(x.q, x.k, x.v, x.g, x.beta, A_log=x.A_log, dt_bias=x.dt_bias,
                           scale=x.scale, lower_bound=x.lower_bound, n_seqs=n,
-                          final_state=fin, out=out, workspace=ws)
+                          initial_state=x.initial_state, final_state=fin, out=out, workspace=ws)
 
-    def no_flush():  # the inputs (4.3 GB) are larger than L2
+    def no_flush():  # the long workload's inputs (4.3 GB) are larger than L2
         pass
 
     flush = make_flush(torch)
+    step_flush = no_flush if w["name"] == "long" else flush
     bus = None
     try:
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
@@ -295,7 +308,7 @@ def run_ours(args, rank, world, barrier, reduce_max):
     torch.cuda.synchronize()
     clocks.start()
     preroll(torch, step, 1.0)
-    secs = time_device(torch, step, args.steps, no_flush, barrier)
+    secs = time_device(torch, step, args.steps, step_flush, barrier)
     clk = clocks.stop()
     secs = reduce_max(secs)
     ms_per_step = secs / args.steps * 1e3
@@ -304,7 +317,7 @@ def run_ours(args, rank, world, barrier, reduce_max):
     th = n * w["T"] * w["hv"]
     tflops = th * flop_per_token_head() * args.steps * world / secs / 1e12
 
-    kernels, launches, ms_all = prefill_kernels(torch, step, args.steps, no_flush, barrier, reduce_max,
+    kernels, launches, ms_all = prefill_kernels(torch, step, args.steps, step_flush, barrier, reduce_max,
                                                 th, w["hqk"], w["hv"], pk)
     dom = max(ms_all, key=lambda k: ms_all[k])
     d = kernels.get(dom, {"bound": "tensor", "achieved": None, "peak": pk["bf16"], "unit": "TFLOP/s",
@@ -322,7 +335,9 @@ def run_ours(args, rank, world, barrier, reduce_max):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, random gate parameters, no weights)",
         "config": config_dict(world),
-        "parallelism": f"replicas x{world}", "l2": "inputs (4.3 GB) larger than L2: no flush",
+        "parallelism": f"replicas x{world}",
+        "l2": ("inputs (4.3 GB) larger than L2: no flush" if w["name"] == "long"
+               else "flushed before each step (256 MB write)"),
         "groups": "auto (1 at this workload)",
         "tflops": round(tflops, 3), "pct_bf16_peak": round(100 * tflops / pk["bf16"], 2),
         "hbm_gbs_algorithmic": round(th * prefill_bytes_per_token_head(w["hqk"], w["hv"])
@@ -346,7 +361,8 @@ def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
     as chunked prefill and copies the outputs back, overlapped."""
     dev = out.device
     host = {name: getattr(x, name).cpu().pin_memory()
-            for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias")}
+            for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")
+            if getattr(x, name) is not None}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -358,8 +374,8 @@ def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
     def e2e_step():
         kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"],
                                A_log=host["A_log"], dt_bias=host["dt_bias"], scale=x.scale,
-                               lower_bound=x.lower_bound, n_seqs=n, final_state=fin_h, out=out_h,
-                               workspace=ws_host)
+                               lower_bound=x.lower_bound, n_seqs=n, initial_state=host.get("initial_state"),
+                               final_state=fin_h, out=out_h, workspace=ws_host)
 
     for _ in range(2):
         e2e_step()
@@ -618,18 +634,20 @@ def cpu_baseline(x, min_seconds=10.0):
     slabs = [(h, min(hv, h + 8)) for h in range(0, hv, 8)]
     cpu = {name: getattr(x, name).cpu() for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias")}
     cu = x.cu_seqlens.cpu()
+    s0 = None if x.initial_state is None else x.initial_state.cpu()
     reps, elapsed = 0, 0.0
     while elapsed < min_seconds:
         for h0, h1 in slabs:
             q, k, v, g, b = (cpu[nm][:, h0:h1] for nm in ("q", "k", "v", "g", "beta"))
             t0 = time.perf_counter()
             oracle.recurrence(q, k, v, g, b, cu, A_log=cpu["A_log"][h0:h1], dt_bias=cpu["dt_bias"][h0:h1],
-                              lower_bound=x.lower_bound, want_out=True, want_state=True, n_threads=threads)
+                              lower_bound=x.lower_bound, h0=None if s0 is None else s0[:, h0:h1],
+                              want_out=True, want_state=True, n_threads=threads)
             elapsed += time.perf_counter() - t0
         reps += 1
     return {"value": round(T * reps / elapsed, 2), "unit": "tokens/s", "cores": threads,
             "kind": "oracle", "seconds": round(elapsed, 3),
-            "sample": f"the whole long-context workload ({T} tokens, Hv={hv}), {reps} time(s), eight "
+            "sample": f"the whole {x.name} workload ({T} tokens, Hv={hv}), {reps} time(s), eight "
                       f"heads per oracle call (fp64 token recurrence, OpenMP over head and value block)"}
 
 

@@ -20,8 +20,9 @@
 // The prologue emits, per (chunk, head), the walk's tensor-core operands in
 // their shared-memory layout (fp16, K-major, no swizzle):
 //   P (128 x 128), R (128 x 64), d (fp32, 128), qg' (64 x 128),
-//   o_intra (bf16, four blocks of [64 r][32 v]) and v^T in four blocks of
-//   32 value columns.
+//   o_intra (bf16, four blocks of [64 r][32 v], each row's four 16-byte
+//   chunks rotated by r / 2: oi_offset) and v^T in four blocks of 32 value
+//   columns.
 //
 // Precision: A_kk / A_qk use kind::tf32 (their operands carry exponent
 // factors up to e^{8 |gate|}, outside fp16 range); every other product uses
@@ -60,6 +61,14 @@ constexpr uint32_t CH_V16 = CH_OI + 4 * OI_BLOCK;   // 4 x fp16 v^T blocks, one 
 constexpr uint32_t CH_BYTES = CH_V16 + 4 * VB_BYTES;  // 99328
 constexpr uint32_t CH_A_BYTES = CH_QG - CH_P;       // P, R, d: the chain's part (49664)
 constexpr uint32_t QG_BYTES = CH_OI - CH_QG;        // qg' (16384)
+
+// Byte offset of the 16-byte chunk j (value columns 8 j .. 8 j + 7) of row r
+// in an o_intra block: rows are 64 bytes apart and row r's chunks are
+// rotated by r / 2, so that 16 rows stored or loaded at once spread over the
+// shared-memory banks (2-way instead of 8-way).
+__host__ __device__ constexpr uint32_t oi_offset(int r, int j) {
+  return (uint32_t)(r * 64 + 16 * ((j + (r >> 1)) & 3));
+}
 
 __device__ __forceinline__ int seq_bos(const ChunkParams& p, int n) {
   return p.cu_seqlens ? p.cu_seqlens[n] : n * p.dense_len;
@@ -947,7 +956,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
         }
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(s.XY + ST_QG + (CH_OI - CH_QG) + cq * OI_BLOCK + r * 64 + 16 * g8) =
+          *reinterpret_cast<uint4*>(s.XY + ST_QG + (CH_OI - CH_QG) + cq * OI_BLOCK + oi_offset(r, g8)) =
               make_uint4(ov[4 * g8], ov[4 * g8 + 1], ov[4 * g8 + 2], ov[4 * g8 + 3]);
       }
     }
@@ -1240,7 +1249,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
       tc::tmem_ld32(tc::tmem_addr(tmem, 32 * q, T_O + 32 * ob), o);
       uint4 oi[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) oi[j] = *reinterpret_cast<const uint4*>(s.b[ob] + QG_BYTES + r * 64 + 16 * j);
+      for (int j = 0; j < 4; ++j) oi[j] = *reinterpret_cast<const uint4*>(s.b[ob] + QG_BYTES + oi_offset(r, j));
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.o_done[ob]);  // O[ob] and b[ob] read

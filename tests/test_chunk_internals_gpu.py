@@ -3,9 +3,9 @@
 kda_chunk_fwd's prologue writes, for every (chunk, head), the walk's
 tensor-core operands into the caller's workspace (fp16, K-major core-matrix
 layout): P = -kg^T w (128 x 128), R = kg^T T (128 x 64), d (fp32 128),
-qg' = qg - A_qk w (64 x 128), o_intra = A_qk T v (bf16, four row-major
-blocks of [64 rows][32 value columns]) and v^T in four blocks of 32 value
-columns.  This test decodes them and compares each with the same
+qg' = qg - A_qk w (64 x 128), o_intra = A_qk T v (bf16, four blocks of
+[64 rows][32 value columns], row r's 16-byte chunks rotated by r // 2) and
+v^T in four blocks of 32 value columns.  This test decodes them and compares each with the same
 quantity built by oracle/chunked.py, which pins the prologue's
 intermediates, not only the end result.
 """
@@ -101,8 +101,11 @@ def test_prologue_records_match_chunk_form(T, lb):
             got_d = rec[OFF_D:OFF_QG].view(np.float32).astype(np.float64)
             got_qg = _kmajor_decode(rec[OFF_QG:OFF_OI], 64, 128)
             oi_raw = rec[OFF_OI:OFF_V].view(np.uint16).astype(np.uint32) << 16
-            got_oi = np.concatenate([oi_raw.view(np.float32).astype(np.float64)[j * 2048:(j + 1) * 2048]
-                                     .reshape(64, 32) for j in range(4)], axis=1)
+            oi_blocks = oi_raw.view(np.float32).astype(np.float64).reshape(4, 64, 4, 8)  # block, row, slot, 8 cols
+            # row r's 16-byte chunk j (value columns 8 j ..) sits at slot (j + r // 2) % 4
+            rows = np.arange(64)[:, None]
+            slots = (np.arange(4)[None, :] + rows // 2) % 4
+            got_oi = np.concatenate([oi_blocks[jb][rows, slots].reshape(64, 32) for jb in range(4)], axis=1)
             tag = f"T={T} head {h} chunk {c} (len {L})"
             assert _rel(got_d, ops["d"]) < 1e-4, f"d {tag}"
             assert _err(got_R, want_R) < 5e-3, f"R {tag}: {_err(got_R, want_R)}"
