@@ -194,9 +194,16 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
  *   state_indices  device int32 [n_seqs]
  *   has_initial_state device uint8 [n_seqs] or NULL (= all true)
  *   groups         chunk groups per sequence (vLLM _chunk_groups): 1 walks
- *                  each chain serially; G > 1 runs the exact group scan
- *                  (pass one per group, serial composition of the transfer
- *                  operators, pass two); <= 0 lets the library choose
+ *                  each chain serially, in a launch after the prologue's;
+ *                  G > 1 runs the exact group scan (pass one per group,
+ *                  serial composition of the transfer operators, pass two);
+ *                  -1 runs the pipelined launch: one cooperative kernel in
+ *                  which one CTA per (sequence, head) chain walks all 128
+ *                  value columns while the other SMs run the prologue, the
+ *                  walk taking each chunk as soon as its record is ready
+ *                  (dense sequences only, no checkpoints, at most 48
+ *                  chains; KDA_ERR_INVALID_ARGUMENT otherwise); 0 (or any
+ *                  other value <= 0) lets the library choose among the three
  *   workspace      device scratch of >= kda_chunk_workspace_bytes(.., groups)
  *                  bytes, 16-byte aligned; contents need not be initialised
  *   stream         cudaStream_t

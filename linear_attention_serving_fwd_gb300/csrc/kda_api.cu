@@ -149,6 +149,7 @@ int device_sm_count() {
 // split starts at G = 4.
 int choose_groups(int32_t n_seqs, int32_t t_total, int32_t hv, int32_t requested) {
   if (requested > 0) return requested < 64 ? requested : 64;
+  if (requested == -1) return 1;  // the pipelined launch walks each chain serially
   const int sms = device_sm_count();
   const long pass1 = 8L * n_seqs * hv;
   const long chunks = ((long)t_total + kda::CHUNK - 1) / kda::CHUNK;
@@ -389,6 +390,7 @@ static int chunk_common(const kda_activations* x, void* out, const int32_t* cu_s
   p.slot_stride = slot_stride; p.n_slots = n_slots;
   p.state_indices = state_indices; p.has_init = has_initial_state;
   p.groups = G;
+  p.pipeline = groups == -1 ? 2 : (groups <= 0 && G == 1 ? 1 : 0);
   p.sm_count = device_sm_count();
   p.ckpt = checkpoint_state; p.ckpt_stride = checkpoint_row_stride; p.ckpt_rows = checkpoint_rows;
   p.ckpt_off = checkpoint_offsets; p.ckpt_idx = checkpoint_state_indices;

@@ -46,19 +46,21 @@
 
 namespace kda {
 
-// Per-(chunk, head) workspace record, bytes.  The walk's B operands of
-// 32 rows (value columns) keep their K groups VB_LBO = 528 bytes apart (not
-// 512) so that column-wise shared-memory stores avoid bank conflicts.
-constexpr uint32_t VB_LBO = 32 * 16 + 16;
-constexpr uint32_t VB_BYTES = VB_LBO * 64 / 8;      // fp16 v^T block [32 v][64 r]: 4224
+// Per-(chunk, head) workspace record, bytes.  v^T is one K-major operand of
+// 128 rows (value columns) by K = 64 (tokens): K groups 2048 bytes apart, so
+// that a product over all 128 columns takes it whole and one over 32 columns
+// takes, from each K group, the 512 bytes of its rows.
+constexpr uint32_t VB_ROWS_BYTES = 32 * 16;         // 32 value rows of one K group
+constexpr uint32_t VB_BYTES = VB_ROWS_BYTES * 64 / 8;  // a 32-column block, packed: 4096
 constexpr uint32_t CH_P = 0;                        // fp16 128 x 128, rows k, K = k'
 constexpr uint32_t CH_R = CH_P + 128 * 128 * 2;     // fp16 128 x 64,  rows k, K = r
 constexpr uint32_t CH_D = CH_R + 128 * 64 * 2;      // fp32 128
 constexpr uint32_t CH_QG = CH_D + 128 * 4;          // fp16 64 x 128,  rows r, K = k'
 constexpr uint32_t OI_BLOCK = 64 * 32 * 2;          // bf16 o_intra block [64 r][32 v]
 constexpr uint32_t CH_OI = CH_QG + 64 * 128 * 2;    // 4 o_intra blocks, one per 32 columns
-constexpr uint32_t CH_V16 = CH_OI + 4 * OI_BLOCK;   // 4 x fp16 v^T blocks, one per 32 columns
-constexpr uint32_t CH_BYTES = CH_V16 + 4 * VB_BYTES;  // 99328
+constexpr uint32_t CH_V16 = CH_OI + 4 * OI_BLOCK;   // fp16 v^T, [128 v][64 r] K-major
+constexpr uint32_t V16_BYTES = 128 * 64 * 2;
+constexpr uint32_t CH_BYTES = CH_V16 + V16_BYTES;   // 98816
 constexpr uint32_t CH_A_BYTES = CH_QG - CH_P;       // P, R, d: the chain's part (49664)
 constexpr uint32_t QG_BYTES = CH_OI - CH_QG;        // qg' (16384)
 
@@ -209,6 +211,10 @@ __global__ void kda_chunk_index_kernel(ChunkParams p) {
 // for the two 16-row pairs and then for the two 32-row halves.
 // --------------------------------------------------------------------------
 constexpr int PRO_THREADS = 512;
+// The thread that issues an item's record stores (and owns their bulk group):
+// its warp has no work in the inverse's rounds, where the pipelined launch
+// waits for the stores to land.
+constexpr int REC_THREAD = 256;
 constexpr int LDT = 68;  // row stride (floats) of the 64 x 64 fp32 matrices (16-byte rows)
 constexpr int LDW = 34;  // row stride of the 32 x 32 fp32 temporary (8-byte column pairs)
 constexpr int YROWS = 160;  // rows of the stacked Y operand
@@ -253,6 +259,7 @@ struct __align__(1024) ProSmem {
   uint64_t bar2;            // the P product of the last round, ahead of the others
   uint64_t tbar;            // tile loads
   uint32_t tmem;
+  int next_t;               // the next item
   int abort;
 };
 // The tiles: q, k, v, each HALO rows (the three tokens before the chunk,
@@ -265,9 +272,20 @@ static_assert((P_TILES + HALO * D * 2) % 128 == 0 && (TILE_QKV * 2) % 128 == 0, 
 __device__ __forceinline__ int tile_row(int x, int r) { return x * TILE_QKV + (HALO + r) * D; }
 __device__ __forceinline__ int g_row(int r) { return 3 * TILE_QKV + r * D; }
 
-// item t = chunk * Hv + head
+// Item t of the prologue: t = chunk * Hv + head; in the pipelined launch
+// (walk_ctas > 0, dense sequences) level-major instead, t = (j * n_seqs + n)
+// * Hv + head for in-sequence chunk j, so that every chain's chunk j is
+// produced before any chain's chunk j + 1 is started.
 __device__ __forceinline__ int4 item_meta(const ChunkParams& p, int t) {
-  const int c = t / p.hv, h = t - c * p.hv;
+  int c, h;
+  if (p.walk_ctas > 0) {
+    const int chains = p.n_seqs * p.hv, j = t / chains, r = t - j * chains, n = r / p.hv;
+    h = r - n * p.hv;
+    c = chunk_off_of(p, n) + j;
+  } else {
+    c = t / p.hv;
+    h = t - c * p.hv;
+  }
   const int n = chunk_seq_of(p, c);
   const int bos = seq_bos(p, n) + chunk_j_of(p, c) * CHUNK;
   return make_int4(c, h, bos, min(CHUNK, seq_eos(p, n) - bos));
@@ -412,14 +430,24 @@ __device__ unsigned long long g_phase_items;
   } while (0)
 #endif
 
+// The ready flag of a record: set once the record's stores have completed,
+// with release semantics at GPU scope (the bulk stores are ordered before it
+// by the proxy fence).  The walk acquires it before loading the record.
+__device__ __forceinline__ void publish_ready(unsigned* flag) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+}
+
+// The prologue's items first, first + stride, ... on one CTA (smem_raw: a
+// ProSmem).  With p.ready set, each item's ready flag is raised once its
+// record has landed: at the next item's first barrier, or at the end.
 template <bool CONV, bool FP16>
-__global__ void __launch_bounds__(PRO_THREADS, 1)
-    kda_prologue_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
+__device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileMaps& maps, int first,
+                                               int stride, unsigned char* smem_raw) {
   ProSmem& s = *reinterpret_cast<ProSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = num_chunks_of(p) * p.hv;
-  if ((int)blockIdx.x >= n_items) return;
+  if (first >= n_items) return;
   __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(s.XY + P_TILES);
   PH_BEGIN();
 
@@ -433,20 +461,29 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     mbar_init(&s.tbar, 1);
     fence_mbar_init();
     s.abort = 0;
-    s.meta[0] = item_meta(p, blockIdx.x);
-    load_tiles<CONV>(p, maps, s.meta[0], tiles, &s.tbar);
+    // items first, first + stride, ...; or, with p.item_counter, whichever
+    // item is next when this CTA asks (an SM that runs slower takes fewer)
+    const int t0 = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : first;
+    s.next_t = t0;
+    if (t0 < n_items) {
+      s.meta[0] = item_meta(p, t0);
+      load_tiles<CONV>(p, maps, s.meta[0], tiles, &s.tbar);
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
-  ItemScalars sc = load_scalars(p, s.meta[0], tid);
-  uint32_t bar_phase = 0, bar2_phase = 0, tile_phase = 0, tiles_issued = 1;
+  int t = s.next_t;
+  ItemScalars sc = {};
+  if (t < n_items) sc = load_scalars(p, s.meta[0], tid);
+  uint32_t bar_phase = 0, bar2_phase = 0, tile_phase = 0, tiles_issued = t < n_items ? 1 : 0;
   int cur = 0;
-  for (int t = blockIdx.x; t < n_items; t += gridDim.x, cur ^= 1) {
+  int pending = -1;  // REC_THREAD: the record whose stores are in flight (pipelined launch)
+  for (; t < n_items; cur ^= 1) {
     // this CTA's last item: the walk may start its setup on the SMs that
     // finish first (it waits for this grid before reading any record)
-    if (t + (int)gridDim.x >= n_items) griddep_launch_dependents();
+    if (!p.item_counter && t + stride >= n_items) griddep_launch_dependents();
     const int4 meta = s.meta[cur];
     const int c_glob = meta.x, h = meta.y, len = meta.w;
     const float a_h = p.has_gate ? __expf(sc.alog) : 0.f;
@@ -461,8 +498,8 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     PH(0);
 
     // ---- phase 1: thread = (channel pair: channels c, c + 1 with c = 2 cp;
-    // rows 8 hs .. 8 hs + 7, half hh of sub-chunk Rq = hs / 2) ------------------
-    const int cp = tid & 63, hs = tid >> 6, Rq = hs >> 1, hh = hs & 1;
+    // rows 8 hs .. 8 hs + 7, half hs % 2 of sub-chunk Rq = hs / 2) ------------
+    const int cp = tid & 63, hs = tid >> 6, Rq = hs >> 1;
     const int c = 2 * cp;
     float2 lam[8], kv[8], qv[8];  // per row, the two channels
     {
@@ -499,14 +536,13 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       // a raw log decay outside [-10.5, 0] (or NaN) leaves the exponent range
       // the factored A_kk / A_qk operands are built for: report it
       if (!p.has_gate && __any_sync(0xffffffffu, gate_bad) && lane == 0) set_error(p.err, ERR_RANGE);
-      // v^T of the two channels: the record's block c / 32, and VT for o_intra
+      // v^T of the two channels: the record and VT (for o_intra) share a layout
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int ch = c + e;
+        const uint32_t o = tc::kmajor_offset(c + e, 8 * hs, 128);
         const uint4 v4 = make_uint4(vw[e][0], vw[e][1], vw[e][2], vw[e][3]);
-        *reinterpret_cast<uint4*>(wsb + CH_V16 + (ch >> 5) * VB_BYTES +
-                                  tc::kmajor_offset_lbo(ch & 31, 8 * hs, VB_LBO)) = v4;
-        *reinterpret_cast<uint4*>(s.VT + tc::kmajor_offset(ch, 8 * hs, 128)) = v4;
+        *reinterpret_cast<uint4*>(wsb + CH_V16 + o) = v4;
+        *reinterpret_cast<uint4*>(s.VT + o) = v4;
       }
       *reinterpret_cast<float2*>(&s.qtot[hs][c]) = acc;
       // row norms: the 8 per-row partials reduce-scatter over the warp's 64
@@ -545,7 +581,7 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
       // the last item's record stores have read the staging area, which the
       // X / Y build below overwrites
-      if (tid == 0) bulk_wait_read<0>();
+      if (tid == REC_THREAD) bulk_wait_read<0>();
     }
     __syncthreads();
     PH(1);
@@ -653,14 +689,19 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
       }
       fence_proxy_async_smem();
     }
-    const bool has_next = t + (int)gridDim.x < n_items;
-    if (tid == 32 && has_next) s.meta[cur ^ 1] = item_meta(p, t + gridDim.x);
+    // the next item (thread 32; every thread reads it after phase 5's barrier)
+    int t_next = 0;
+    if (tid == 32) {
+      t_next = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : t + stride;
+      s.next_t = t_next;
+      if (t_next < n_items) s.meta[cur ^ 1] = item_meta(p, t_next);
+    }
     wait_or_abort(&s.bar, bar_phase, &s.abort, p.err);
     bar_phase ^= 1u;
     tc::fence_after_sync();
     // the product has read Y: the next item's rows stream in over it (the
     // carve below stays under P_TILES)
-    if (tid == 32 && has_next) load_tiles<CONV>(p, maps, s.meta[cur ^ 1], tiles, &s.tbar);
+    if (tid == 32 && t_next < n_items) load_tiles<CONV>(p, maps, s.meta[cur ^ 1], tiles, &s.tbar);
     PH(4);
 
     float* Af = reinterpret_cast<float*>(s.XY + P_A);
@@ -719,9 +760,19 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     PH(5);
 
     // the next item's scalars (its tiles are already on their way)
+    t_next = s.next_t;
+    const bool has_next = t_next < n_items;
     if (has_next) {
       tiles_issued += 1;
       sc = load_scalars(p, s.meta[cur ^ 1], tid);
+    }
+    // pipelined launch: the record thread's warp idles through the inverse
+    // below (threads 64.. here, 256.. in the next two rounds), so it waits
+    // there for the last item's stores to land and then raises its flag
+    if (tid == REC_THREAD && pending >= 0) {
+      bulk_wait<0>();
+      publish_ready(p.ready + pending);
+      pending = -1;
     }
 
     // ---- phase 3: L^{-1} by recursive doubling ---------------------------------
@@ -966,22 +1017,34 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
     // the item's P, R, qg' and o_intra records leave by four bulk stores;
     // their shared-memory reads finish before the next item's X / Y build
     // writes over the staging area (and its Kg build over R)
-    if (tid == 0) {
+    if (tid == REC_THREAD) {
       bulk_s2g(wsb + CH_P, s.XY + ST_P0, 16384);
       bulk_s2g(wsb + CH_P + 16384, s.XY + ST_P1, 16384);
       bulk_s2g(wsb + CH_R, s.KG, 128 * 64 * 2);
       bulk_s2g(wsb + CH_QG, s.XY + ST_QG, CH_V16 - CH_QG);
       bulk_commit();
+      if (p.ready) pending = c_glob * p.hv + h;
     }
     PH(11);
+    t = t_next;
   }  // items
   PH_END();
   // after an abort, leave no tile load in flight: wait (bounded) for the last
   tc::fence_before_sync();
   __syncthreads();
   if (tid == 0 && s.abort) mbar_wait_bounded(&s.tbar, (tiles_issued - 1) & 1, p.err);
-  if (tid == 0) bulk_wait<0>();  // every record store has landed
+  if (tid == REC_THREAD) {
+    bulk_wait<0>();  // every record store has landed
+    if (pending >= 0 && !s.abort) publish_ready(p.ready + pending);
+  }
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+template <bool CONV, bool FP16>
+__global__ void __launch_bounds__(PRO_THREADS, 1)
+    kda_prologue_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  prologue_items<CONV, FP16>(p, maps, blockIdx.x, gridDim.x, smem_raw);
 }
 
 // --------------------------------------------------------------------------
@@ -1010,7 +1073,7 @@ constexpr uint32_t B_BYTES = QG_BYTES + OI_BLOCK;  // qg' and this block's o_int
 
 struct __align__(1024) WalkSmem {
   unsigned char a[3][CH_A_BYTES];   // P, R, d of a chunk
-  unsigned char va[3][VB_BYTES];    // this block's v^T, fp16 [v][r]
+  unsigned char va[3][VB_BYTES];    // this block's v^T, fp16 [v][r] (K groups packed)
   unsigned char b[2][B_BYTES];      // qg' and o_intra of a chunk
   unsigned char s16[3][S16_BYTES];  // fp16 S of the chunk being entered
   uint64_t fullA[3], emptyA[3], fullB[2];
@@ -1293,7 +1356,10 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         mbar_arrive_expect_tx(&s.fullA[ab], CH_A_BYTES + (ident ? 0u : VB_BYTES));
         bulk_g2s(s.a[ab], src + CH_P, 32768, &s.fullA[ab]);
         bulk_g2s(s.a[ab] + 32768, src + CH_P + 32768, CH_A_BYTES - 32768, &s.fullA[ab]);
-        if (!ident) bulk_g2s(s.va[ab], src + CH_V16 + vblk * VB_BYTES, VB_BYTES, &s.fullA[ab]);
+        if (!ident)  // the block's 32 rows of each of the 8 K groups
+          for (int kg = 0; kg < 8; ++kg)
+            bulk_g2s(s.va[ab] + kg * VB_ROWS_BYTES, src + CH_V16 + kg * 2048 + vblk * VB_ROWS_BYTES,
+                     VB_ROWS_BYTES, &s.fullA[ab]);
         s.issuedA[ab] += 1;
       }
     } else if (lane == 16 && outp) {
@@ -1301,7 +1367,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
         if (it + LOOKAHEAD < nch)
           bulk_prefetch_l2(wsb + ((size_t)(c0 + it + LOOKAHEAD) * p.hv + h) * CH_BYTES + CH_QG,
-                           QG_BYTES + 4 * OI_BLOCK + 4 * VB_BYTES);
+                           CH_BYTES - CH_QG);
         const int bb = it & 1;
         if (it >= 2 && !wait_or_abort(&s.o_done[bb], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
         mbar_arrive_expect_tx(&s.fullB[bb], B_BYTES);
@@ -1319,7 +1385,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
         if (!wait_or_abort(&s.fullA[ab], (it / 3) & 1, &s.abort, p.err)) return false;
         tc::fence_after_sync();
         tc::mma_kloop(tmem + T_RV + 32 * (it & 1), smem_u32(s.a[ab] + CH_R), smem_u32(s.va[ab]), 128, 32,
-                      64, 0, false, VB_LBO);
+                      64, 0, false);
         tc::mma_commit(&s.bar_y[it & 1]);
         return true;
       };
@@ -1354,6 +1420,367 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
   }
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
+
+// --------------------------------------------------------------------------
+// Pipelined launch: one cooperative kernel whose first walk_ctas CTAs each
+// walk one (sequence, head) chain over all 128 value columns, while the
+// other CTAs run the prologue in level-major item order (chunk j of every
+// chain before chunk j + 1 of any) and raise a ready flag per record.  A
+// walk CTA loads chunk c's record once its flag is up, so a chain's walk
+// runs behind the prologue instead of after it.  Prologue CTAs never wait
+// on a walk CTA, and a cooperative launch keeps every CTA resident, so each
+// flag a walk CTA waits for is eventually raised.
+//
+// Walk CTA (512 threads), per chunk c of the chain:
+//   Y = P_c S_c (two K halves, R_c v_c added to half 0),  S_{c+1} = d_c * S_c + Y
+//   o_c = qg'_c S_c + o_intra_c                            (M = 64)
+// warps 0-7    the chain: thread (k, ch) holds state row k, value columns
+//              64 ch .. 64 ch + 63 in fp32 (TMEM lane k); threads 0 and 32
+//              issue the two K halves of P S, thread 0 also R v.
+// warps 8-11   the output: rows 16 q .. 16 q + 15 (TMEM lanes 32 q ..), plus
+//              o_intra read from the record, to out.
+// warp 12      lane 0 waits for each record's flag, then loads P, R, d, v^T
+//              (A, double buffered) and qg' (B, double buffered).
+// warp 13      lane 0 issues qg' S_c once chunk c's P S has completed (its
+//              fp16 S is then written).
+// TMEM: Y half 0 at column 0, half 1 at 128, the output at 256 and 384.
+// --------------------------------------------------------------------------
+constexpr int PIPE_MAX_CHAINS = 48;      // walk CTAs at most
+constexpr int PIPE_MIN_PROLOGUE = 64;    // prologue CTAs at least
+constexpr uint32_t WA_BYTES = CH_A_BYTES + V16_BYTES;  // P, R, d, then v^T
+constexpr uint32_t S16F_BYTES = 128 * 128 * 2;         // fp16 S, MN-major [v][k]
+
+struct __align__(1024) Walk128Smem {
+  unsigned char a[2][WA_BYTES];
+  unsigned char b[2][QG_BYTES];
+  unsigned char s16[2][S16F_BYTES];
+  uint64_t fullA[2], emptyA[2], fullB[2], freeB[2], bar_y[2], bar_o[2], o_done[2], s_free[2];
+  int issuedA[2], issuedB[2];
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(Walk128Smem) <= 227 * 1024, "pipelined walk shared memory");
+static_assert(WA_BYTES % 16 == 0 && CH_A_BYTES % 16 == 0, "bulk copy alignment");
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait for a record's ready flag (bounded, like wait_or_abort): on expiry
+// sets ERR_TIMEOUT and raises the CTA's abort flag.
+__device__ __forceinline__ bool wait_ready_or_abort(const unsigned* flag, volatile int* abort, unsigned* err) {
+  if (ld_acquire_gpu(flag)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < WAIT_CAP; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > WAIT_NS) break;
+  }
+  set_error(err, ERR_TIMEOUT);
+  *abort = 1;
+  return false;
+}
+
+// Measurement build only: cycles of the pipelined walk's chain (thread 0)
+// per activity, summed over chunks and walk CTAs: [0] waiting for the next
+// record and S16 buffer, [1] waiting for P S, [2] the state update and S16
+// write, [3] barrier and issue; the loader's [4] ready-flag and [5] buffer
+// waits; [6] chunk steps.
+#ifdef KDA_PHASE_TIMING
+constexpr int N_WALK_CTR = 6;
+__device__ unsigned long long g_walk_cycles[N_WALK_CTR + 1];
+#define WK_MARK(t) const long long t = clock64()
+#define WK_ADD(acc, t)                                                  \
+  do {                                                                  \
+    const long long n_ = clock64();                                     \
+    acc += (unsigned long long)(n_ - t);                                \
+  } while (0)
+#else
+#define WK_MARK(t) \
+  do {             \
+  } while (0)
+#define WK_ADD(acc, t) \
+  do {                 \
+  } while (0)
+#endif
+
+__device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, unsigned char* smem_raw) {
+  Walk128Smem& s = *reinterpret_cast<Walk128Smem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = chain / p.hv, h = chain - n * p.hv;
+  const int c0 = chunk_off_of(p, n), nch = chunk_off_of(p, n + 1) - c0;
+  const unsigned char* wsb = reinterpret_cast<const unsigned char*>(p.ch);
+  const unsigned* ready = p.ready + (size_t)c0 * p.hv + h;  // chunk it's flag: ready[it * Hv]
+
+  if (warp == 0) {
+    tc::tmem_alloc(&s.tmem, 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.fullA[i], 1);
+      mbar_init(&s.emptyA[i], 2);  // threads 0 and 32, once their products have read A
+      mbar_init(&s.fullB[i], 1);
+      mbar_init(&s.freeB[i], 1);
+      mbar_init(&s.bar_y[i], 2);   // the two P S halves (R v with half 0)
+      mbar_init(&s.bar_o[i], 1);
+      mbar_init(&s.o_done[i], 4);  // the four output warps
+      mbar_init(&s.s_free[i], 1);
+      s.issuedA[i] = 0;
+      s.issuedB[i] = 0;
+    }
+    fence_mbar_init();
+    s.abort = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s.tmem;
+  constexpr uint32_t T_Y = 0, T_O = 256;
+
+  if (warp < 8) {
+    // ---------------- chain ----------------
+    const int k = tid & 127, ch = tid >> 7;
+    const int half = tid == 0 ? 0 : (tid == 32 ? 1 : -1);
+    float S[64];
+    {
+      const int64_t ioff = initial_state_off(p, n, h);
+#pragma unroll
+      for (int v = 0; v < 64; ++v)
+        S[v] = ioff >= 0 ? state_load(p, init_base(p), ioff + (int64_t)(64 * ch + v) * D + k) : 0.f;
+    }
+    auto write_s16 = [&](int sb) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(s.s16[sb] + tc::mnmajor_offset(64 * ch + 8 * j, k, S16_LBO, S16_SBO)) =
+            make_uint4(pack_half2(S[8 * j], S[8 * j + 1]), pack_half2(S[8 * j + 2], S[8 * j + 3]),
+                       pack_half2(S[8 * j + 4], S[8 * j + 5]), pack_half2(S[8 * j + 6], S[8 * j + 7]));
+    };
+    // chunk it's products from A[it & 1] and S16[it & 1]: Y half = P[:, half] S[half, :]
+    auto issue = [&](int it) {
+      const int b = it & 1;
+      tc::mma_kloop_bmn(tmem + T_Y + 128 * half, smem_u32(s.a[b] + CH_P) + half * 8 * 2048,
+                        smem_u32(s.s16[b]) + half * 8 * S16_LBO, 128, 128, 64, S16_LBO, S16_SBO, false);
+      if (half == 0)
+        tc::mma_kloop(tmem + T_Y, smem_u32(s.a[b] + CH_R), smem_u32(s.a[b] + CH_A_BYTES), 128, 128, 64, 0, true);
+      tc::mma_commit(&s.bar_y[b]);
+      tc::mma_commit(&s.emptyA[b]);
+    };
+    float dcur = 0.f;
+    bool fail = false;
+    if (nch > 0) {
+      fail = !wait_or_abort(&s.fullA[0], 0, &s.abort, p.err);
+      if (!fail) dcur = reinterpret_cast<const float*>(s.a[0] + CH_D)[k];
+      write_s16(0);
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      fail = named_bar_or(1, CHAIN_THREADS, fail);
+      if (half >= 0 && !fail) {
+        tc::fence_after_sync();
+        issue(0);
+      }
+    }
+#ifdef KDA_PHASE_TIMING
+    unsigned long long wk[4] = {0, 0, 0, 0};
+#endif
+    for (int it = 0; !fail && it < nch; ++it) {
+      const int b = it & 1, nb = b ^ 1;
+      const bool more = it + 1 < nch;
+      float dnext = 0.f;
+      WK_MARK(wk0);
+      // while P S runs: the next record (its d) and the S16 buffer the next
+      // state goes to, last read by the output product of chunk it - 1
+      if (more) {
+        fail = !wait_or_abort(&s.fullA[nb], ((it + 1) >> 1) & 1, &s.abort, p.err);
+        if (!fail) dnext = reinterpret_cast<const float*>(s.a[nb] + CH_D)[k];
+        if (!fail && it >= 1) fail = !wait_or_abort(&s.s_free[nb], ((it - 1) >> 1) & 1, &s.abort, p.err);
+      }
+      WK_ADD(wk[0], wk0);
+      WK_MARK(wk1);
+      if (!fail) fail = !wait_or_abort(&s.bar_y[b], (it >> 1) & 1, &s.abort, p.err);
+      WK_ADD(wk[1], wk1);
+      WK_MARK(wk2);
+      if (!fail) {
+        tc::fence_after_sync();
+        const uint32_t lanes = tc::tmem_addr(tmem, 32 * (warp & 3), 64 * ch);
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          uint32_t y0[16], y1[16];
+          tc::tmem_ld16_async(lanes + T_Y + 16 * pc, y0);
+          tc::tmem_ld16_async(lanes + T_Y + 128 + 16 * pc, y1);
+          tc::tmem_wait_ld();
+          tc::tmem_regs(y0);
+          tc::tmem_regs(y1);
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            S[16 * pc + v] = fmaf(dcur, S[16 * pc + v], __uint_as_float(y0[v]) + __uint_as_float(y1[v]));
+        }
+        if (more) {
+          write_s16(nb);
+          fence_proxy_async_smem();
+        }
+      }
+      WK_ADD(wk[2], wk2);
+      WK_MARK(wk3);
+      tc::fence_before_sync();
+      fail = named_bar_or(1, CHAIN_THREADS, fail);  // Y read; S16[nb] holds S_{it+1}
+      if (fail) break;
+      if (half >= 0 && more) {
+        tc::fence_after_sync();
+        issue(it + 1);
+      }
+      WK_ADD(wk[3], wk3);
+      dcur = dnext;
+    }
+#ifdef KDA_PHASE_TIMING
+    if (tid == 0) {
+      for (int i = 0; i < 4; ++i) atomicAdd(&g_walk_cycles[i], wk[i]);
+      atomicAdd(&g_walk_cycles[N_WALK_CTR], (unsigned long long)nch);
+    }
+#endif
+    if (!s.abort) {
+      const int64_t fo = final_state_off(p, n, h);
+      if (fo >= 0)
+#pragma unroll
+        for (int v = 0; v < 64; ++v) state_store(p, final_base(p), fo + (int64_t)(64 * ch + v) * D + k, S[v]);
+    }
+  } else if (warp < 12) {
+    // ---------------- output rows 16 q .. 16 q + 15 ----------------
+    const int q = warp - 8, r = 16 * q + (lane & 15);
+    for (int it = 0; it < nch; ++it) {
+      const int ob = it & 1;
+      if (!wait_or_abort(&s.bar_o[ob], (it >> 1) & 1, &s.abort, p.err)) break;
+      tc::fence_after_sync();
+      // the output product read this record, so its flag is up: acquire it
+      // for the o_intra reads
+      (void)ld_acquire_gpu(ready + (size_t)it * p.hv);
+      const unsigned char* oi_src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES + CH_OI;
+      uint4 oi[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        oi[j] = __ldcg(reinterpret_cast<const uint4*>(oi_src + (j >> 2) * OI_BLOCK + oi_offset(r, j & 3)));
+      const int bos = seq_bos(p, n) + it * CHUNK;
+      const int len = min(CHUNK, seq_eos(p, n) - bos);
+      __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D;
+#pragma unroll
+      for (int jb = 0; jb < 4; ++jb) {
+        float o[32];
+        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * q, T_O + 128 * ob + 32 * jb), o);
+        if (lane < 16 && r < len) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162* ib = reinterpret_cast<const __nv_bfloat162*>(&oi[4 * jb + j]);
+            uint4 w;
+            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 f = __bfloat1622float2(ib[u]);
+              const float a0 = o[8 * j + 2 * u] + f.x, a1 = o[8 * j + 2 * u + 1] + f.y;
+              wp[u] = p.in_fp16 ? act_pack2<true>(a0, a1) : act_pack2<false>(a0, a1);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * jb + 8 * j) = w;
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.o_done[ob]);  // O[ob] read
+    }
+  } else if (warp == 12) {
+    // ---------------- loader ----------------
+    if (lane == 0) {
+#ifdef KDA_PHASE_TIMING
+      unsigned long long wf = 0, wb = 0;
+#endif
+      for (int it = 0; it < nch; ++it) {
+        const int b = it & 1;
+        WK_MARK(wl0);
+        if (!wait_ready_or_abort(ready + (size_t)it * p.hv, &s.abort, p.err)) break;
+        WK_ADD(wf, wl0);
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // the bulk loads below read it
+        const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
+        WK_MARK(wl1);
+        if (it >= 2 && !wait_or_abort(&s.emptyA[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+        WK_ADD(wb, wl1);
+        mbar_arrive_expect_tx(&s.fullA[b], WA_BYTES);
+        bulk_g2s(s.a[b], src + CH_P, 32768, &s.fullA[b]);
+        bulk_g2s(s.a[b] + 32768, src + CH_P + 32768, CH_A_BYTES - 32768, &s.fullA[b]);
+        bulk_g2s(s.a[b] + CH_A_BYTES, src + CH_V16, V16_BYTES, &s.fullA[b]);
+        s.issuedA[b] += 1;
+        if (it >= 2 && !wait_or_abort(&s.freeB[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+        mbar_arrive_expect_tx(&s.fullB[b], QG_BYTES);
+        bulk_g2s(s.b[b], src + CH_QG, QG_BYTES, &s.fullB[b]);
+        s.issuedB[b] += 1;
+      }
+#ifdef KDA_PHASE_TIMING
+      atomicAdd(&g_walk_cycles[4], wf);
+      atomicAdd(&g_walk_cycles[5], wb);
+#endif
+    }
+  } else if (warp == 13) {
+    // ---------------- qg' S ----------------
+    if (lane == 0) {
+      for (int it = 0; it < nch; ++it) {
+        const int b = it & 1;
+        // chunk it's P S has completed, so S16[b] holds S_it
+        if (!wait_or_abort(&s.bar_y[b], (it >> 1) & 1, &s.abort, p.err)) break;
+        if (!wait_or_abort(&s.fullB[b], (it >> 1) & 1, &s.abort, p.err)) break;
+        if (it >= 2 && !wait_or_abort(&s.o_done[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+        tc::fence_after_sync();
+        tc::mma_kloop_bmn(tmem + T_O + 128 * b, smem_u32(s.b[b]), smem_u32(s.s16[b]), 64, 128, 128, S16_LBO,
+                          S16_SBO, false);
+        tc::mma_commit(&s.bar_o[b]);
+        tc::mma_commit(&s.s_free[b]);
+        tc::mma_commit(&s.freeB[b]);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0 && s.abort) {
+    // leave no bulk copy in flight: wait (bounded) for the last load of each buffer
+    for (int i = 0; i < 2; ++i) {
+      if (s.issuedA[i] > 0) mbar_wait_bounded(&s.fullA[i], (s.issuedA[i] - 1) & 1, p.err);
+      if (s.issuedB[i] > 0) mbar_wait_bounded(&s.fullB[i], (s.issuedB[i] - 1) & 1, p.err);
+    }
+  }
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// Measurement build only: each CTA's span in the pipelined kernel, as
+// %globaltimer ns at start and end and SM cycles in between (thread 0).
+#ifdef KDA_PHASE_TIMING
+constexpr int MAX_SPAN_CTAS = 256;
+__device__ unsigned long long g_cta_span[MAX_SPAN_CTAS][4];
+#endif
+
+template <bool CONV, bool FP16>
+__global__ void __launch_bounds__(PRO_THREADS, 1)
+    kda_pipelined_kernel(ChunkParams p, const __grid_constant__ TileMaps maps) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+#ifdef KDA_PHASE_TIMING
+  const unsigned long long g0 = globaltimer_ns();
+  const long long c0 = clock64();
+#endif
+  if ((int)blockIdx.x < p.walk_ctas)
+    walk_chain128(p, blockIdx.x, smem_raw);
+  else
+    prologue_items<CONV, FP16>(p, maps, blockIdx.x - p.walk_ctas, gridDim.x - p.walk_ctas, smem_raw);
+#ifdef KDA_PHASE_TIMING
+  if (threadIdx.x == 0 && blockIdx.x < MAX_SPAN_CTAS) {
+    g_cta_span[blockIdx.x][0] = g0;
+    g_cta_span[blockIdx.x][1] = globaltimer_ns();
+    g_cta_span[blockIdx.x][2] = (unsigned long long)(clock64() - c0);
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_cta_span[blockIdx.x][3] = smid;
+  }
+#endif
+}
+constexpr size_t PIPE_SMEM = sizeof(Walk128Smem) > sizeof(ProSmem) ? sizeof(Walk128Smem) : sizeof(ProSmem);
 
 // --------------------------------------------------------------------------
 // Group composition: S_{g+1}^T = S_g^T M_g^T + B_g^T serially over groups,
@@ -1411,6 +1838,7 @@ size_t chunk_workspace_floats(int n_seqs, int t_total, int hv, int groups, int* 
   size_t words = int_words(n_seqs, max_chunks);
   words += (size_t)max_chunks * hv * (CH_BYTES / 4);
   if (groups > 1) words += 3 * (size_t)n_seqs * hv * groups * D * D;
+  words += (size_t)max_chunks * hv + 1;  // the pipelined launch's ready flags and item counter
   return words;  // 4-byte words
 }
 
@@ -1442,6 +1870,20 @@ static bool encode_rows(CUtensorMap* map, const void* base, int heads, int T, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Does the pipelined launch beat the two launches?  Estimated step times (us)
+// from measured GB300 rates: a prologue item takes about T_ITEM on its SM, a
+// chunk step of the 32-column walk T_STEP32 and of the pipelined 128-column
+// walk T_STEP128.  Two launches: the prologue's waves, then the walk's
+// chains.  Pipelined: the prologue's waves on the SMs the chains leave, or
+// one item and a whole chain, whichever is longer.
+static bool pipeline_pays(int items, int chains, int chunks_per_chain, int sms) {
+  constexpr double T_ITEM = 10.0, T_STEP32 = 1.06, T_STEP128 = 1.3;
+  auto waves = [](long work, long width) { return (double)((work + width - 1) / width); };
+  const double two = waves(items, sms) * T_ITEM + waves(4L * chains, sms) * chunks_per_chain * T_STEP32;
+  const double pro = waves(items, sms - chains) * T_ITEM, walk = T_ITEM + chunks_per_chain * T_STEP128;
+  return (pro > walk ? pro : walk) < two;
+}
+
 int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   static uint64_t attrs_done = 0;
   once_per_device(attrs_done, [](int) {
@@ -1455,6 +1897,12 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
                          (int)sizeof(WalkSmem));
     cudaFuncSetAttribute(kda_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)((NB * D + D * D) * sizeof(float)));
+    cudaFuncSetAttribute(kda_pipelined_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)PIPE_SMEM);
+    cudaFuncSetAttribute(kda_pipelined_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)PIPE_SMEM);
+    cudaFuncSetAttribute(kda_pipelined_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)PIPE_SMEM);
   });
   int max_chunks = 0;
   chunk_workspace_floats(p.n_seqs, p.t_total, p.hv, p.groups, &max_chunks);
@@ -1472,6 +1920,19 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     p.gM = fw;
     p.gB = fw + plane;
     p.gS = fw + 2 * plane;
+    fw += 3 * plane;
+  }
+  unsigned* ready_flags = reinterpret_cast<unsigned*>(fw);
+  const int items = max_chunks * p.hv;
+  const int sms = p.sm_count > 0 ? p.sm_count : 152;
+  const int chains = p.n_seqs * p.hv;
+  const bool can_pipe = p.groups == 1 && !p.cu_seqlens && !p.ckpt && chains <= PIPE_MAX_CHAINS &&
+                        sms - chains >= PIPE_MIN_PROLOGUE;
+  if (p.pipeline == 2 && !can_pipe) {
+    set_last_error(KDA_ERR_INVALID_ARGUMENT,
+                   "kda_chunk_fwd: groups = -1 (pipelined launch) needs dense sequences (no cu_seqlens), no "
+                   "checkpoints and at most 48 (sequence, head) chains.");
+    return -2;
   }
   if (p.cu_seqlens) {  // dense sequences have closed-form chunk tables
     trace_begin("kda_chunk_index", stream);
@@ -1505,9 +1966,44 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
                    "(strides must be positive multiples of 8 elements below 2^39 bytes).");
     return -2;
   }
+  const int cps = p.dense_len > 0 ? (p.dense_len + CHUNK - 1) / CHUNK : 0;  // chunks per dense sequence
+  if (p.pipeline == 2 || (p.pipeline == 1 && can_pipe && pipeline_pays(chains * cps, chains, cps, sms))) {
+    const int grid = chains + (items < sms - chains ? items : sms - chains);
+    pp.walk_ctas = chains;
+    pp.ready = ready_flags;
+    pp.item_counter = ready_flags + items;
+    if (cudaMemsetAsync(ready_flags, 0, (size_t)(items + 1) * sizeof(unsigned), stream) != cudaSuccess) return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(PRO_THREADS);
+    cfg.dynamicSmemBytes = PIPE_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: each awaited flag gets raised
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    trace_begin("kda_pipelined", stream);
+    cudaError_t e;
+    if (pp.conv.state)
+      e = cudaLaunchKernelEx(&cfg, kda_pipelined_kernel<true, false>, pp, maps);
+    else if (pp.in_fp16)
+      e = cudaLaunchKernelEx(&cfg, kda_pipelined_kernel<false, true>, pp, maps);
+    else
+      e = cudaLaunchKernelEx(&cfg, kda_pipelined_kernel<false, false>, pp, maps);
+    trace_end(stream);
+    if (e == cudaSuccess) {
+      if (p.conv.state && launch_conv_prefill_state(p, stream) != 0) return -1;
+      return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    }
+    // not all CTAs could be resident at once (e.g. SMs held back): two launches
+    if (e != cudaErrorCooperativeLaunchTooLarge || p.pipeline == 2) return -1;
+    (void)cudaGetLastError();
+    pp.walk_ctas = 0;
+    pp.ready = nullptr;
+    pp.item_counter = nullptr;
+  }
   trace_begin("kda_prologue", stream);
-  const int items = max_chunks * p.hv;
-  const int sms = p.sm_count > 0 ? p.sm_count : 152;
   const int grid = items < sms ? items : sms;
   if (pp.conv.state)  // bf16 activations only (checked by the API layer)
     kda_prologue_kernel<true, false><<<grid, PRO_THREADS, sizeof(ProSmem), stream>>>(pp, maps);
@@ -1555,6 +2051,32 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
 // Measurement build only: copy the prologue's per-phase cycle sums (n of
 // them, at most 12) and its item count to ``out[0..n]`` (out[n] = items),
 // optionally clearing them.  Not part of the regular library's ABI.
+// The pipelined kernel's per-CTA spans of its last launch: for CTA i,
+// out[4 i .. 4 i + 3] = start ns, end ns, SM cycles, SM id (at most n CTAs).
+extern "C" int kda_cta_spans(unsigned long long* out, int32_t n) {
+  if (!out || n < 1 || n > kda::MAX_SPAN_CTAS) return KDA_ERR_INVALID_ARGUMENT;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(out, kda::g_cta_span, (size_t)n * 4 * sizeof(unsigned long long)) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
+// The pipelined walk's counters (n of them, at most 6, then the chunk steps
+// at out[n]), optionally clearing them.
+extern "C" int kda_walk_cycles(unsigned long long* out, int32_t n, int32_t reset) {
+  if (!out || n < 1 || n > kda::N_WALK_CTR) return KDA_ERR_INVALID_ARGUMENT;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KDA_ERR_CUDA;
+  unsigned long long all[kda::N_WALK_CTR + 1];
+  if (cudaMemcpyFromSymbol(all, kda::g_walk_cycles, sizeof(all)) != cudaSuccess) return KDA_ERR_CUDA;
+  for (int i = 0; i < n; ++i) out[i] = all[i];
+  out[n] = all[kda::N_WALK_CTR];
+  if (reset) {
+    const unsigned long long zero[kda::N_WALK_CTR + 1] = {};
+    if (cudaMemcpyToSymbol(kda::g_walk_cycles, zero, sizeof(zero)) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
 extern "C" int kda_phase_cycles(unsigned long long* out, int32_t n, int32_t reset) {
   if (!out || n < 1 || n > kda::N_PHASES) return KDA_ERR_INVALID_ARGUMENT;
   if (cudaDeviceSynchronize() != cudaSuccess) return KDA_ERR_CUDA;

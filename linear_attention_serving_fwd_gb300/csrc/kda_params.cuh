@@ -88,6 +88,14 @@ struct ChunkParams {
   int max_chunks;
   int groups;
   int sm_count;         // SMs of the device: the persistent prologue's grid
+  // pipelined launch: CTAs 0 .. walk_ctas - 1 walk one chain each (all 128
+  // value columns) while the others run the prologue in level-major order;
+  // ready[c * Hv + h] is raised once record (c, h) has landed.  0 / null in
+  // the two-launch path.
+  int walk_ctas;
+  unsigned* ready;
+  unsigned* item_counter;  // pipelined launch: prologue CTAs take their next item from it (zeroed)
+  int pipeline;         // host: 0 two launches, 1 the library chooses, 2 pipelined (groups = -1)
   // workspace carve
   int32_t* chunk_off;   // [N+1]
   int32_t* chunk_seq;   // [max_chunks]

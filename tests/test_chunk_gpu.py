@@ -103,12 +103,14 @@ def test_group_scan_paged_varlen():
     _check(x, out, fin, pool, ref, "G=4 varlen")
 
 
-def test_dense_prefill_full():
-    """B=2, T=4096, H=16, initial state N(0, 0.02), final state returned."""
+@pytest.mark.parametrize("groups", [1, -1])
+def test_dense_prefill_full(groups):
+    """B=2, T=4096, H=16, initial state N(0, 0.02), final state returned:
+    two launches with a serial walk (1) and the pipelined launch (-1)."""
     x = W.workload("dense")
     ref = oracle.prefill(x)
-    out, fin, pool = _run(x, dense=True)
-    _check(x, out, fin, pool, ref, "dense")
+    out, fin, pool = _run(x, groups=groups, dense=True)
+    _check(x, out, fin, pool, ref, f"dense G={groups}")
 
 
 def test_varlen_paged_full():
@@ -127,11 +129,11 @@ def _check_heads(out, fin, ref, tag, slab=8):
     check_state(fin, ref["state"], f"{tag} final state")
 
 
-@pytest.mark.parametrize("groups", [1, 8])
+@pytest.mark.parametrize("groups", [1, 8, -1])
 def test_long_prefill_all_heads(groups):
     """B=1, T=131072, H=32, zero initial state (2048 chunks of 64): every
-    head's output and final state against the oracle, serial walk and the
-    chunk-group scan with 8 groups."""
+    head's output and final state against the oracle: serial walk, the
+    chunk-group scan with 8 groups, and the pipelined launch."""
     import linear_attention_serving_fwd_gb300 as kda
     x = W.workload("long")
     ref = oracle.prefill(x)

@@ -5,7 +5,7 @@ tensor-core operands into the caller's workspace (fp16, K-major core-matrix
 layout): P = -kg^T w (128 x 128), R = kg^T T (128 x 64), d (fp32 128),
 qg' = qg - A_qk w (64 x 128), o_intra = A_qk T v (bf16, four blocks of
 [64 rows][32 value columns], row r's 16-byte chunks rotated by r // 2) and
-v^T in four blocks of 32 value columns.  This test decodes them and compares each with the same
+v^T (128 value columns x 64 rows).  This test decodes them and compares each with the same
 quantity built by oracle/chunked.py, which pins the prologue's
 intermediates, not only the end result.
 """
@@ -22,9 +22,7 @@ pytestmark = pytest.mark.gpu
 
 D, C = 128, 64
 OFF_P, OFF_R, OFF_D, OFF_QG, OFF_OI, OFF_V = 0, 32768, 49152, 49664, 66048, 82432
-VB_LBO = 528
-VB = VB_LBO * 8
-REC = OFF_V + 4 * VB
+REC = OFF_V + 128 * 64 * 2
 
 
 def _kmajor_decode(raw: np.ndarray, R: int, K: int) -> np.ndarray:
@@ -33,14 +31,6 @@ def _kmajor_decode(raw: np.ndarray, R: int, K: int) -> np.ndarray:
     rows = np.arange(R)[:, None]
     ks = np.arange(K)[None, :]
     idx = ((ks // 8) * (R * 16) + (rows // 8) * 128 + (rows % 8) * 16 + (ks % 8) * 2) // 2
-    return h[idx]
-
-
-def _kmajor_decode_lbo(raw: np.ndarray, R: int, K: int, lbo: int) -> np.ndarray:
-    h = raw.view(np.float16).astype(np.float64)
-    rows = np.arange(R)[:, None]
-    ks = np.arange(K)[None, :]
-    idx = ((ks // 8) * lbo + (rows // 8) * 128 + (rows % 8) * 16 + (ks % 8) * 2) // 2
     return h[idx]
 
 
@@ -112,9 +102,7 @@ def test_prologue_records_match_chunk_form(T, lb):
             assert _err(got_P, want_P) < 1e-2, f"P {tag}: {_err(got_P, want_P)}"
             assert _err(got_qg, want_qg) < 1e-2, f"qg' {tag}: {_err(got_qg, want_qg)}"
             assert _err(got_oi, want_oi) < 1e-2, f"o_intra {tag}: {_err(got_oi, want_oi)}"
-            # v^T blocks, fp16 [32 value columns][64 rows]: bf16 v converted to
-            # fp16, exact except below fp16's normal range (absolute 3e-8)
-            for jb in range(4):
-                got_v = _kmajor_decode_lbo(rec[OFF_V + jb * VB:OFF_V + (jb + 1) * VB], 32, 64, VB_LBO)
-                np.testing.assert_allclose(got_v, vv[:, 32 * jb:32 * (jb + 1)].T, rtol=0, atol=3e-8,
-                                           err_msg=f"v block {jb} {tag}")
+            # v^T, fp16 [128 value columns][64 rows]: bf16 v converted to fp16,
+            # exact except below fp16's normal range (absolute 3e-8)
+            got_v = _kmajor_decode(rec[OFF_V:REC], 128, 64)
+            np.testing.assert_allclose(got_v, vv.T, rtol=0, atol=3e-8, err_msg=f"v^T {tag}")
