@@ -473,7 +473,10 @@ int kda_commit_ex(void* state_pool, int64_t slot_stride, int64_t n_slots, const 
                   const float* corr, const void* kg, const float* A_log, const float* dt_bias,
                   float lower_bound, int32_t state_bf16, int32_t kg_fp16, void* stream);
 
-/* Thread-local text of the last error returned on this thread ("" if none). */
+/* Thread-local text of the last error returned on this thread ("" if none).
+ * kda_last_error_message is the same function under the name the serving
+ * contract uses; kda_last_error is kept for existing callers. */
+const char* kda_last_error_message(void);
 const char* kda_last_error(void);
 
 /*

@@ -27,7 +27,7 @@ KDA_DTYPE_FP16 = 1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_chunk_workspace_bytes", "kda_chunk_fwd", "kda_decode", "kda_verify",
-           "kda_last_error", "kda_device_status", "kda_trace_enable", "kda_trace_read",
+           "kda_last_error", "kda_last_error_message", "kda_device_status", "kda_trace_enable", "kda_trace_read",
            "kda_version", "kda_chunk_fwd_noalloc", "kda_commit", "kda_chunk_fwd_ex",
            "kda_decode_steps", "kda_verify_ex", "kda_commit_ex", "kda_chunk_fwd_host",
            "kda_chunk_fwd_host_workspace_bytes", "kda_conv_scratch_bytes", "kda_selftest_wait_timeout")
@@ -102,6 +102,8 @@ def _declare(lib):
     lib.kda_commit_ex.restype = ctypes.c_int
     lib.kda_last_error.argtypes = []
     lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_last_error_message.argtypes = []
+    lib.kda_last_error_message.restype = ctypes.c_char_p
     lib.kda_device_status.argtypes = [P, I32]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
@@ -145,7 +147,7 @@ def lib():
 def check(rc: int):
     if rc == KDA_OK:
         return
-    msg = lib().kda_last_error().decode()
+    msg = lib().kda_last_error_message().decode()
     if rc == KDA_ERR_INVALID_ARGUMENT:
         raise ValueError(msg)
     if rc == KDA_ERR_UNSUPPORTED_DTYPE:

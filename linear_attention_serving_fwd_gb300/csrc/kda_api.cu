@@ -258,6 +258,7 @@ int kda_trace_read(int32_t index, char* name, int32_t name_cap, double* total_ms
 const char* kda_version(void) { return "kda-gb300 0.1 sm_103a"; }
 
 const char* kda_last_error(void) { return g_last_error.c_str(); }
+const char* kda_last_error_message(void) { return g_last_error.c_str(); }
 
 size_t kda_conv_scratch_bytes(int32_t t_total, int32_t hqk, int32_t hv) {
   if (t_total < 0 || hqk <= 0 || hv <= 0) return 0;

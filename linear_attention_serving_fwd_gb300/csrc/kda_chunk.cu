@@ -462,7 +462,8 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     fence_mbar_init();
     s.abort = 0;
     // items first, first + stride, ...; or, with p.item_counter, whichever
-    // item is next when this CTA asks (an SM that runs slower takes fewer)
+    // item is next when this CTA asks (an SM that runs slower takes fewer;
+    // each CTA holds one drawn item beyond its next)
     const int t0 = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : first;
     s.next_t = t0;
     if (t0 < n_items) {
@@ -475,6 +476,10 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
   tc::fence_after_sync();
   const uint32_t tmem = s.tmem;
   int t = s.next_t;
+  // thread 32 draws the item after next one item ahead, so that the counter's
+  // round trip never delays the next item's tile loads
+  int t_ahead = 0;
+  if (tid == 32) t_ahead = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : t + stride;
   ItemScalars sc = {};
   if (t < n_items) sc = load_scalars(p, s.meta[0], tid);
   uint32_t bar_phase = 0, bar2_phase = 0, tile_phase = 0, tiles_issued = t < n_items ? 1 : 0;
@@ -692,7 +697,8 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     // the next item (thread 32; every thread reads it after phase 5's barrier)
     int t_next = 0;
     if (tid == 32) {
-      t_next = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : t + stride;
+      t_next = t_ahead;
+      t_ahead = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : t_next + stride;
       s.next_t = t_next;
       if (t_next < n_items) s.meta[cur ^ 1] = item_meta(p, t_next);
     }
