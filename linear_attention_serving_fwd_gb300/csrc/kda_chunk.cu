@@ -954,6 +954,10 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     //   qg'      = A3r [Kg ; qg] = qg - A_qk T Kg            -> columns 0..127
     //   P'       = R Kg  (P = -P' = -kg^T T Kg = -kg^T w)      -> columns 128..255
     //   -o_intra = A3r[:, 0..63] v = -A_qk T v                -> columns 256..383
+    // In the pipelined launch the walk forms o_intra itself: the record
+    // carries -qg' and -A_qk T (A3r's first 64 columns) instead of qg' and
+    // o_intra, and the third product is not made.
+    const bool piped = p.ready != nullptr;
     if (tid == 0) {
       tc::fence_after_sync();
       // P' first, on a barrier of its own: its epilogue runs while the
@@ -963,8 +967,9 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       const uint64_t a3r = tc::smem_desc(smem_u32(A3) + 1024, 2048, 128);
       tc::mma_run<8>(tmem, a3r, tc::smem_desc(smem_u32(s.B3), 2048, 128), 4096, 4096,
                      tc::idesc_f16(64, 128, 0), false);
-      tc::mma_run<4>(tmem + 256, a3r, tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096,
-                     tc::idesc_f16(64, 128, 0), false);
+      if (!piped)
+        tc::mma_run<4>(tmem + 256, a3r, tc::smem_desc(smem_u32(s.VT), 2048, 128), 4096, 4096,
+                       tc::idesc_f16(64, 128, 0), false);
       tc::mma_commit(&s.bar);
     }
     wait_or_abort(&s.bar2, bar2_phase, &s.abort, p.err);
@@ -993,18 +998,29 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       bar_phase ^= 1u;
       tc::fence_after_sync();
       const int r = 16 * sp + (lane & 15);
+      if (piped) {
+        // -A_qk T (A3's rows 64.., K groups 0..7) after -qg' in B3, packed to a
+        // 64-row K-major operand: thread = (K group tid / 64, row tid % 64)
+        const int kg = tid >> 6, rr = tid & 63;
+        *reinterpret_cast<uint4*>(s.B3 + QG_BYTES + kg * 1024 + rr * 16) =
+            *reinterpret_cast<const uint4*>(A3 + 1024 + kg * 2048 + rr * 16);
+      }
       tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 32 * cq), a);
       if (lane < 16) {
+        // qg' (pipelined: -qg', staged in B3, which the products have read,
+        // since ST_QG lies over A3)
+        const float sg = piped ? -1.f : 1.f;
+        unsigned char* qst = piped ? s.B3 : s.XY + ST_QG;
         uint32_t hv[16];
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(a[t], a[t + 1]);
+        for (int t = 0; t < 32; t += 2) hv[t >> 1] = pack_half2(sg * a[t], sg * a[t + 1]);
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
-          *reinterpret_cast<uint4*>(s.XY + ST_QG + tc::kmajor_offset(r, 32 * cq + 8 * g8, 64)) =
+          *reinterpret_cast<uint4*>(qst + tc::kmajor_offset(r, 32 * cq + 8 * g8, 64)) =
               make_uint4(hv[4 * g8], hv[4 * g8 + 1], hv[4 * g8 + 2], hv[4 * g8 + 3]);
       }
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 256 + 32 * cq), a);
-      if (lane < 16) {
+      if (!piped) tc::tmem_ld32(tc::tmem_addr(tmem, 32 * sp, 256 + 32 * cq), a);
+      if (!piped && lane < 16) {
         uint32_t ov[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
@@ -1027,7 +1043,11 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       bulk_s2g(wsb + CH_P, s.XY + ST_P0, 16384);
       bulk_s2g(wsb + CH_P + 16384, s.XY + ST_P1, 16384);
       bulk_s2g(wsb + CH_R, s.KG, 128 * 64 * 2);
-      bulk_s2g(wsb + CH_QG, s.XY + ST_QG, CH_V16 - CH_QG);
+      if (piped) {
+        bulk_s2g(wsb + CH_QG, s.B3, QG_BYTES + 64 * 64 * 2);  // -qg', -A_qk T
+      } else {
+        bulk_s2g(wsb + CH_QG, s.XY + ST_QG, CH_V16 - CH_QG);
+      }
       bulk_commit();
       if (p.ready) pending = c_glob * p.hv + h;
     }
@@ -1439,16 +1459,17 @@ __global__ void __launch_bounds__(WALK_THREADS, 1) kda_walk_kernel(ChunkParams p
 //
 // Walk CTA (512 threads), per chunk c of the chain:
 //   Y = P_c S_c (two K halves, R_c v_c added to half 0),  S_{c+1} = d_c * S_c + Y
-//   o_c = qg'_c S_c + o_intra_c                            (M = 64)
+//   o_c = -[(-qg'_c) S_c + (-A_qk T)_c v_c]               (M = 64)
+// (the record of this launch carries -qg' and -A_qk T; o_intra = A_qk T v
+// is formed here, off the chain)
 // warps 0-7    the chain: thread (k, ch) holds state row k, value columns
 //              64 ch .. 64 ch + 63 in fp32 (TMEM lane k); threads 0 and 32
 //              issue the two K halves of P S, thread 0 also R v.
-// warps 8-11   the output: rows 16 q .. 16 q + 15 (TMEM lanes 32 q ..), plus
-//              o_intra read from the record, to out.
+// warps 8-11   the output: rows 16 q .. 16 q + 15 (TMEM lanes 32 q ..) to out.
 // warp 12      lane 0 waits for each record's flag, then loads P, R, d, v^T
-//              (A, double buffered) and qg' (B, double buffered).
-// warp 13      lane 0 issues qg' S_c once chunk c's P S has completed (its
-//              fp16 S is then written).
+//              (A, double buffered) and -qg', -A_qk T (B).
+// warp 13      lane 0 issues chunk c's output products once its P S has
+//              completed (its fp16 S is then written).
 // TMEM: Y half 0 at column 0, half 1 at 128, the output at 256 and 384.
 // --------------------------------------------------------------------------
 constexpr int PIPE_MAX_CHAINS = 48;      // walk CTAs at most
@@ -1456,12 +1477,14 @@ constexpr int PIPE_MIN_PROLOGUE = 64;    // prologue CTAs at least
 constexpr uint32_t WA_BYTES = CH_A_BYTES + V16_BYTES;  // P, R, d, then v^T
 constexpr uint32_t S16F_BYTES = 128 * 128 * 2;         // fp16 S, MN-major [v][k]
 
+constexpr uint32_t WB_BYTES = QG_BYTES + 64 * 64 * 2;  // -qg', then -A_qk T (K-major, K groups 1024 B apart)
+
 struct __align__(1024) Walk128Smem {
   unsigned char a[2][WA_BYTES];
-  unsigned char b[2][QG_BYTES];
+  unsigned char b[WB_BYTES];
   unsigned char s16[2][S16F_BYTES];
-  uint64_t fullA[2], emptyA[2], fullB[2], freeB[2], bar_y[2], bar_o[2], o_done[2], s_free[2];
-  int issuedA[2], issuedB[2];
+  uint64_t fullA[2], emptyA[2], fullB, freeB, bar_y[2], bar_o[2], o_done[2], s_free[2];
+  int issuedA[2], issuedB;
   uint32_t tmem;
   int abort;
 };
@@ -1528,16 +1551,16 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.fullA[i], 1);
-      mbar_init(&s.emptyA[i], 2);  // threads 0 and 32, once their products have read A
-      mbar_init(&s.fullB[i], 1);
-      mbar_init(&s.freeB[i], 1);
+      mbar_init(&s.emptyA[i], 3);  // threads 0, 32 and warp 13's lane 0, once their products have read A
       mbar_init(&s.bar_y[i], 2);   // the two P S halves (R v with half 0)
       mbar_init(&s.bar_o[i], 1);
       mbar_init(&s.o_done[i], 4);  // the four output warps
       mbar_init(&s.s_free[i], 1);
       s.issuedA[i] = 0;
-      s.issuedB[i] = 0;
     }
+    mbar_init(&s.fullB, 1);
+    mbar_init(&s.freeB, 1);
+    s.issuedB = 0;
     fence_mbar_init();
     s.abort = 0;
   }
@@ -1660,14 +1683,6 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
       const int ob = it & 1;
       if (!wait_or_abort(&s.bar_o[ob], (it >> 1) & 1, &s.abort, p.err)) break;
       tc::fence_after_sync();
-      // the output product read this record, so its flag is up: acquire it
-      // for the o_intra reads
-      (void)ld_acquire_gpu(ready + (size_t)it * p.hv);
-      const unsigned char* oi_src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES + CH_OI;
-      uint4 oi[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        oi[j] = __ldcg(reinterpret_cast<const uint4*>(oi_src + (j >> 2) * OI_BLOCK + oi_offset(r, j & 3)));
       const int bos = seq_bos(p, n) + it * CHUNK;
       const int len = min(CHUNK, seq_eos(p, n) - bos);
       __nv_bfloat16* dst = p.out + ((int64_t)(bos + r) * p.hv + h) * D;
@@ -1678,13 +1693,11 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
         if (lane < 16 && r < len) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162* ib = reinterpret_cast<const __nv_bfloat162*>(&oi[4 * jb + j]);
             uint4 w;
             uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float2 f = __bfloat1622float2(ib[u]);
-              const float a0 = o[8 * j + 2 * u] + f.x, a1 = o[8 * j + 2 * u + 1] + f.y;
+            for (int u = 0; u < 4; ++u) {  // the accumulator holds -o
+              const float a0 = -o[8 * j + 2 * u], a1 = -o[8 * j + 2 * u + 1];
               wp[u] = p.in_fp16 ? act_pack2<true>(a0, a1) : act_pack2<false>(a0, a1);
             }
             *reinterpret_cast<uint4*>(dst + 32 * jb + 8 * j) = w;
@@ -1716,10 +1729,10 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
         bulk_g2s(s.a[b] + 32768, src + CH_P + 32768, CH_A_BYTES - 32768, &s.fullA[b]);
         bulk_g2s(s.a[b] + CH_A_BYTES, src + CH_V16, V16_BYTES, &s.fullA[b]);
         s.issuedA[b] += 1;
-        if (it >= 2 && !wait_or_abort(&s.freeB[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
-        mbar_arrive_expect_tx(&s.fullB[b], QG_BYTES);
-        bulk_g2s(s.b[b], src + CH_QG, QG_BYTES, &s.fullB[b]);
-        s.issuedB[b] += 1;
+        if (it >= 1 && !wait_or_abort(&s.freeB, (it - 1) & 1, &s.abort, p.err)) break;
+        mbar_arrive_expect_tx(&s.fullB, WB_BYTES);
+        bulk_g2s(s.b, src + CH_QG, WB_BYTES, &s.fullB);  // -qg' and -A_qk T are adjacent
+        s.issuedB += 1;
       }
 #ifdef KDA_PHASE_TIMING
       atomicAdd(&g_walk_cycles[4], wf);
@@ -1733,14 +1746,18 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
         const int b = it & 1;
         // chunk it's P S has completed, so S16[b] holds S_it
         if (!wait_or_abort(&s.bar_y[b], (it >> 1) & 1, &s.abort, p.err)) break;
-        if (!wait_or_abort(&s.fullB[b], (it >> 1) & 1, &s.abort, p.err)) break;
+        if (!wait_or_abort(&s.fullB, it & 1, &s.abort, p.err)) break;
         if (it >= 2 && !wait_or_abort(&s.o_done[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
         tc::fence_after_sync();
-        tc::mma_kloop_bmn(tmem + T_O + 128 * b, smem_u32(s.b[b]), smem_u32(s.s16[b]), 64, 128, 128, S16_LBO,
+        // -o = (-qg') S + (-A_qk T) v; v^T sits in chunk it's A buffer
+        tc::mma_kloop_bmn(tmem + T_O + 128 * b, smem_u32(s.b), smem_u32(s.s16[b]), 64, 128, 128, S16_LBO,
                           S16_SBO, false);
+        tc::mma_kloop(tmem + T_O + 128 * b, smem_u32(s.b + QG_BYTES), smem_u32(s.a[b] + CH_A_BYTES), 64, 128,
+                      64, 0, true);
         tc::mma_commit(&s.bar_o[b]);
         tc::mma_commit(&s.s_free[b]);
-        tc::mma_commit(&s.freeB[b]);
+        tc::mma_commit(&s.freeB);
+        tc::mma_commit(&s.emptyA[b]);
       }
     }
   }
@@ -1748,10 +1765,9 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
   __syncthreads();
   if (tid == 0 && s.abort) {
     // leave no bulk copy in flight: wait (bounded) for the last load of each buffer
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 2; ++i)
       if (s.issuedA[i] > 0) mbar_wait_bounded(&s.fullA[i], (s.issuedA[i] - 1) & 1, p.err);
-      if (s.issuedB[i] > 0) mbar_wait_bounded(&s.fullB[i], (s.issuedB[i] - 1) & 1, p.err);
-    }
+    if (s.issuedB > 0) mbar_wait_bounded(&s.fullB, (s.issuedB - 1) & 1, p.err);
   }
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
