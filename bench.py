@@ -99,6 +99,7 @@ KERNEL_SOURCES = {
     "kda_prologue": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh", "kda_conv.cuh"],
     "kda_walk": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh", "kda_conv.cuh"],
     "kda_pipelined": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh", "kda_conv.cuh"],
+    "kda_walk128": ["kda_chunk.cu", "kda_common.cuh", "kda_tc.cuh", "kda_params.cuh", "kda_conv.cuh"],
     "kda_window": ["kda_window.cu", "kda_common.cuh", "kda_params.cuh", "kda_conv.cuh"],
 }
 
@@ -258,6 +259,9 @@ def prefill_kernels(torch, step, steps, flush, barrier, reduce_max, th, hqk, hv,
         "kda_walk": {"bound": "tensor", "unit": "TFLOP/s", "peak": pk["bf16"], "work": th * 6 * D * D,
                      "scale": 1e12, "peak_source": f"{pk['src']} bf16 dense (burst)",
                      "per_unit": "6 K V flop per (token, v-head)"},
+        "kda_walk128": {"bound": "tensor", "unit": "TFLOP/s", "peak": pk["bf16"], "work": th * 6 * D * D,
+                        "scale": 1e12, "peak_source": f"{pk['src']} bf16 dense (burst)",
+                        "per_unit": "6 K V flop per (token, v-head)"},
         "kda_pipelined": {"bound": "hbm", "unit": "GB/s", "peak": pk["hbm"], "work": th * (in_bytes + 256) + state_io,
                           "scale": 1e9, "peak_source": f"{pk['src']} HBM copy bandwidth",
                           "per_unit": f"{in_bytes + 256:.0f} B of q/k/v/g/beta in and o out per (token, v-head), "
@@ -360,6 +364,17 @@ def run_ours(args, rank, world, barrier, reduce_max):
         line["cpu_baseline"] = cpu_baseline(x)
     if not args.no_extras:
         line["extras"] = extras(torch, kda, W, pk, args, flush, barrier, reduce_max, rank, world, x)
+        # the extras' headline figures once more, last on the line, where a
+        # reader of only its tail still finds them
+        summ = {}
+        for k, v in line["extras"].items():
+            if isinstance(v, dict) and "frac" in v:
+                summ[k] = {"ms": v.get("ms"), "hbm_frac": v["frac"]}
+            elif isinstance(v, dict) and "ms" in v:
+                summ[k] = {"ms": v["ms"]}
+            elif isinstance(v, dict):
+                summ[k] = v
+        line["extras_summary"] = summ
     return line
 
 

@@ -201,9 +201,9 @@ size_t kda_chunk_workspace_bytes(int32_t n_seqs, int32_t t_total, int32_t hv, in
  *                  which one CTA per (sequence, head) chain walks all 128
  *                  value columns while the other SMs run the prologue, the
  *                  walk taking each chunk as soon as its record is ready
- *                  (dense sequences only, no checkpoints, at most 48
- *                  chains; KDA_ERR_INVALID_ARGUMENT otherwise); 0 (or any
- *                  other value <= 0) lets the library choose among the three
+ *                  (dense sequences only, at most 48 chains;
+ *                  KDA_ERR_INVALID_ARGUMENT otherwise); 0 (or any other
+ *                  value <= 0) lets the library choose among the three
  *   workspace      device scratch of >= kda_chunk_workspace_bytes(.., groups)
  *                  bytes, 16-byte aligned; contents need not be initialised
  *   stream         cudaStream_t

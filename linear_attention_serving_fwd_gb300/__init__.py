@@ -200,9 +200,9 @@ def kda_chunk_fwd(q, k, v, g, beta, *, A_log=None, dt_bias=None, scale=None, low
     own rows.  Both give the same results.
     ``groups``: 0 lets the library choose; 1 walks each chain in a launch of
     its own after the prologue; G > 1 runs the chunk-group scan; -1 runs the
-    pipelined launch (dense sequences, at most 48 (sequence, head) chains, no
-    checkpoints), in which one CTA per chain walks while the prologue still
-    runs on the other SMs.
+    pipelined launch (dense sequences, at most 48 (sequence, head) chains), in
+    which one CTA per chain walks while the prologue still runs on the other
+    SMs.
     """
     dense_b = q.shape[0] if q.dim() == 4 else None
     q, k = _as_tokens(q, "q"), _as_tokens(k, "k")

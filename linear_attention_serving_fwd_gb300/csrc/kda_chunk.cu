@@ -954,10 +954,11 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     //   qg'      = A3r [Kg ; qg] = qg - A_qk T Kg            -> columns 0..127
     //   P'       = R Kg  (P = -P' = -kg^T T Kg = -kg^T w)      -> columns 128..255
     //   -o_intra = A3r[:, 0..63] v = -A_qk T v                -> columns 256..383
-    // In the pipelined launch the walk forms o_intra itself: the record
-    // carries -qg' and -A_qk T (A3r's first 64 columns) instead of qg' and
-    // o_intra, and the third product is not made.
-    const bool piped = p.ready != nullptr;
+    // For the 128-column walk (the pipelined launch, or its own launch) the
+    // walk forms o_intra itself: the record carries -qg' and -A_qk T (A3r's
+    // first 64 columns) instead of qg' and o_intra, and the third product is
+    // not made.
+    const bool piped = p.rec128 != 0;
     if (tid == 0) {
       tc::fence_after_sync();
       // P' first, on a barrier of its own: its epilogue runs while the
@@ -1542,7 +1543,7 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
   const int n = chain / p.hv, h = chain - n * p.hv;
   const int c0 = chunk_off_of(p, n), nch = chunk_off_of(p, n + 1) - c0;
   const unsigned char* wsb = reinterpret_cast<const unsigned char*>(p.ch);
-  const unsigned* ready = p.ready + (size_t)c0 * p.hv + h;  // chunk it's flag: ready[it * Hv]
+  const unsigned* ready = p.ready ? p.ready + (size_t)c0 * p.hv + h : nullptr;  // chunk it's flag: ready[it * Hv]
 
   if (warp == 0) {
     tc::tmem_alloc(&s.tmem, 512);
@@ -1598,6 +1599,22 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
       tc::mma_commit(&s.bar_y[b]);
       tc::mma_commit(&s.emptyA[b]);
     };
+    // mid-prefill snapshot of this sequence: the state after in-sequence chunk ck_j
+    int ck_j = -1;
+    int64_t ck_off = 0;
+    if (p.ckpt) {
+      const int o = p.ckpt_off[n];
+      const int len = seq_eos(p, n) - seq_bos(p, n);
+      const int64_t row = p.ckpt_idx ? (int64_t)p.ckpt_idx[n] : (int64_t)n;
+      if (o > 0 && o % CHUNK == 0 && o <= len && row >= 0) {
+        if (row < p.ckpt_rows) {
+          ck_j = o / CHUNK - 1;
+          ck_off = row * p.ckpt_stride + (int64_t)h * D * D;
+        } else if (tid == 0) {
+          set_error(p.err, ERR_INDEX);
+        }
+      }
+    }
     float dcur = 0.f;
     bool fail = false;
     if (nch > 0) {
@@ -1647,6 +1664,9 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
           for (int v = 0; v < 16; ++v)
             S[16 * pc + v] = fmaf(dcur, S[16 * pc + v], __uint_as_float(y0[v]) + __uint_as_float(y1[v]));
         }
+        if (it == ck_j)  // S now holds the state after the snapshot's chunk
+#pragma unroll
+          for (int v = 0; v < 64; ++v) state_store(p, p.ckpt, ck_off + (int64_t)(64 * ch + v) * D + k, S[v]);
         if (more) {
           write_s16(nb);
           fence_proxy_async_smem();
@@ -1717,9 +1737,13 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
       for (int it = 0; it < nch; ++it) {
         const int b = it & 1;
         WK_MARK(wl0);
-        if (!wait_ready_or_abort(ready + (size_t)it * p.hv, &s.abort, p.err)) break;
+        if (p.ready) {  // pipelined: this record's flag
+          if (!wait_ready_or_abort(ready + (size_t)it * p.hv, &s.abort, p.err)) break;
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // the bulk loads below read it
+        } else if (it == 0) {
+          griddep_wait();  // a launch of its own: the prologue before it has finished
+        }
         WK_ADD(wf, wl0);
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // the bulk loads below read it
         const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
         WK_MARK(wl1);
         if (it >= 2 && !wait_or_abort(&s.emptyA[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
@@ -1803,6 +1827,16 @@ __global__ void __launch_bounds__(PRO_THREADS, 1)
 #endif
 }
 constexpr size_t PIPE_SMEM = sizeof(Walk128Smem) > sizeof(ProSmem) ? sizeof(Walk128Smem) : sizeof(ProSmem);
+
+// The 128-column walk as a launch of its own after the prologue (one CTA per
+// (sequence, head) chain), for calls with more chains than the pipelined
+// launch takes: it needs a quarter of the 32-column walk's CTAs for about
+// the same time per chunk.  Launched programmatically; the loader waits for
+// the prologue before its first record load.
+__global__ void __launch_bounds__(PRO_THREADS, 1) kda_walk128_kernel(ChunkParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  walk_chain128(p, blockIdx.x, smem_raw);
+}
 
 // --------------------------------------------------------------------------
 // Group composition: S_{g+1}^T = S_g^T M_g^T + B_g^T serially over groups,
@@ -1925,6 +1959,8 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
                          (int)PIPE_SMEM);
     cudaFuncSetAttribute(kda_pipelined_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)PIPE_SMEM);
+    cudaFuncSetAttribute(kda_walk128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(Walk128Smem));
   });
   int max_chunks = 0;
   chunk_workspace_floats(p.n_seqs, p.t_total, p.hv, p.groups, &max_chunks);
@@ -1948,14 +1984,18 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
   const int items = max_chunks * p.hv;
   const int sms = p.sm_count > 0 ? p.sm_count : 152;
   const int chains = p.n_seqs * p.hv;
-  const bool can_pipe = p.groups == 1 && !p.cu_seqlens && !p.ckpt && chains <= PIPE_MAX_CHAINS &&
+  const bool can_pipe = p.groups == 1 && !p.cu_seqlens && chains <= PIPE_MAX_CHAINS &&
                         sms - chains >= PIPE_MIN_PROLOGUE;
   if (p.pipeline == 2 && !can_pipe) {
     set_last_error(KDA_ERR_INVALID_ARGUMENT,
-                   "kda_chunk_fwd: groups = -1 (pipelined launch) needs dense sequences (no cu_seqlens), no "
-                   "checkpoints and at most 48 (sequence, head) chains.");
+                   "kda_chunk_fwd: groups = -1 (pipelined launch) needs dense sequences (no cu_seqlens) and at "
+                   "most 48 (sequence, head) chains.");
     return -2;
   }
+  // a serial walk in a launch of its own: the 128-column walk (one CTA per
+  // chain) once the 32-column walk's four CTAs per chain would not fit on
+  // the SMs in one wave
+  const bool walk128 = p.groups == 1 && 4L * chains > sms;
   if (p.cu_seqlens) {  // dense sequences have closed-form chunk tables
     trace_begin("kda_chunk_index", stream);
     kda_chunk_index_kernel<<<1, 256, 0, stream>>>(p);
@@ -1989,7 +2029,9 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     return -2;
   }
   const int cps = p.dense_len > 0 ? (p.dense_len + CHUNK - 1) / CHUNK : 0;  // chunks per dense sequence
-  if (p.pipeline == 2 || (p.pipeline == 1 && can_pipe && pipeline_pays(chains * cps, chains, cps, sms))) {
+  const bool pipe = p.pipeline == 2 || (p.pipeline == 1 && can_pipe && pipeline_pays(chains * cps, chains, cps, sms));
+  pp.rec128 = (pipe || walk128) ? 1 : 0;
+  if (pipe) {
     const int grid = chains + (items < sms - chains ? items : sms - chains);
     pp.walk_ctas = chains;
     pp.ready = ready_flags;
@@ -2024,6 +2066,7 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     pp.walk_ctas = 0;
     pp.ready = nullptr;
     pp.item_counter = nullptr;
+    pp.rec128 = walk128 ? 1 : 0;
   }
   trace_begin("kda_prologue", stream);
   const int grid = items < sms ? items : sms;
@@ -2060,6 +2103,22 @@ int launch_chunk(ChunkParams p, void* workspace, cudaStream_t stream) {
     kda_compose_kernel<<<dim3(D / NB, p.hv, p.n_seqs), COMPOSE_THREADS,
                          (NB * D + D * D) * sizeof(float), stream>>>(p);
     trace_end(stream);
+  }
+  if (pp.rec128) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(chains);
+    cfg.blockDim = dim3(PRO_THREADS);
+    cfg.dynamicSmemBytes = sizeof(Walk128Smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    trace_begin("kda_walk128", stream);
+    if (cudaLaunchKernelEx(&cfg, kda_walk128_kernel, p) != cudaSuccess) return -1;
+    trace_end(stream);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
   }
   trace_begin("kda_walk", stream);
   if (launch_walk(dim3(D / NB, p.hv, p.n_seqs * p.groups), 0) != cudaSuccess) return -1;

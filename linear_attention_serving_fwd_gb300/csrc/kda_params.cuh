@@ -96,6 +96,7 @@ struct ChunkParams {
   unsigned* ready;
   unsigned* item_counter;  // pipelined launch: prologue CTAs take their next item from it (zeroed)
   int pipeline;         // host: 0 two launches, 1 the library chooses, 2 pipelined (groups = -1)
+  int rec128;           // records for the 128-column walk: -qg' and -A_qk T in place of qg' and o_intra
   // workspace carve
   int32_t* chunk_off;   // [N+1]
   int32_t* chunk_seq;   // [max_chunks]

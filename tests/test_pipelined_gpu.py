@@ -1,11 +1,14 @@
-"""GPU parity of the pipelined prefill launch (groups = -1), through the C ABI.
+"""GPU parity of the 128-column walk through the C ABI: the pipelined prefill
+launch (groups = -1) and the same walk as a launch of its own.
 
-One cooperative kernel: one CTA per (sequence, head) chain walks all 128 value
-columns while the other SMs run the prologue in level-major order, and a walk
-CTA takes each chunk's record once the prologue has flagged it ready.  Every
-case checks, through the library's kernel trace, that this kernel (and no
-separate prologue or walk) ran, and compares outputs and states with the fp64
-oracle at the spec's tolerances.
+The pipelined launch is one cooperative kernel: one CTA per (sequence, head)
+chain walks all 128 value columns while the other SMs run the prologue in
+level-major order, and a walk CTA takes each chunk's record once the prologue
+has flagged it ready.  With more chains than the 32-column walk fits on the
+SMs in one wave, the 128-column walk runs as a launch of its own after the
+prologue.  Every case checks, through the library's kernel trace, which
+kernels ran, and compares outputs and states with the fp64 oracle at the
+spec's tolerances.
 """
 from __future__ import annotations
 
@@ -226,3 +229,85 @@ def test_pipelined_repeats_bit_identical():
         assert torch.equal(out, ref_o), f"repeat {i}: outputs differ"
         assert torch.equal(fin, ref_f), f"repeat {i}: final states differ"
     assert kda.kda_device_status(clear=True) == 0
+
+
+# ---- the 128-column walk as a launch of its own (more chains than the
+# 32-column walk fits on the SMs in one wave: 4 x chains > SMs)
+
+def test_walk128_varlen_many_chains():
+    """8 ragged sequences x 8 heads = 64 chains on a paged cache: the
+    prologue and then the 128-column walk, against the oracle."""
+    import linear_attention_serving_fwd_gb300 as kda
+    x = W.varlen_paged([70, 1, 129, 64, 5, 300, 700, 33], 2, 8, slots=12, seed=87, lower_bound=-0.4,
+                       has_initial=[1, 1, 0, 1, 1, 1, 0, 1], state_std=0.3)
+    ref = oracle.prefill(x)
+    xd = x.to("cuda")
+    pool = xd.state_pool.clone()
+
+    def call():
+        return kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, A_log=xd.A_log, dt_bias=xd.dt_bias,
+                                 scale=x.scale, lower_bound=x.lower_bound, cu_seqlens=xd.cu_seqlens,
+                                 state_cache=pool, state_indices=xd.state_indices,
+                                 has_initial_state=xd.has_initial_state)
+    (out, _), names = _traced(call)
+    assert kda.kda_device_status(clear=True) == 0
+    assert "kda_walk128" in names and "kda_walk" not in names, sorted(names)
+    check_out(out, ref["out"], "walk128 out")
+    live = [s for s in x.state_indices.tolist() if s >= 0]
+    check_state(pool[live], ref["pool"][live], "walk128 cache rows")
+    untouched = [s for s in range(pool.shape[0]) if s not in live]
+    assert torch.equal(pool[untouched].cpu(), x.state_pool[untouched]), "untouched rows changed"
+
+
+def _prefix_state(x, n, o, h0):
+    bos = int(x.cu_seqlens[n])
+    return oracle.recurrence(x.q[bos:bos + o], x.k[bos:bos + o], x.v[bos:bos + o], x.g[bos:bos + o],
+                             x.beta[bos:bos + o], [0, o], A_log=x.A_log, dt_bias=x.dt_bias,
+                             lower_bound=x.lower_bound, h0=h0[None])["state"][0]
+
+
+@pytest.mark.parametrize("form", ["walk128", "pipelined"])
+def test_128_column_walk_checkpoints(form):
+    """Mid-prefill snapshots from the 128-column walk: on its own launch
+    (5 sequences x 8 heads = 40 chains) and in the pipelined launch (dense,
+    3 x 4 = 12 chains).  Valid offsets snapshot; 0, a misaligned offset and
+    one past the sequence's end leave their rows untouched."""
+    import linear_attention_serving_fwd_gb300 as kda
+    if form == "walk128":
+        lens = [200, 130, 517, 256, 640]
+        offs = [128, 0, 512, 100, 704]
+        x = W.varlen_paged(lens, 2, 8, slots=12, seed=89, lower_bound=-0.7, state_std=0.3)
+        h0 = [x.state_pool[int(x.state_indices[n])].double().numpy()
+              if int(x.state_indices[n]) >= 0 and bool(x.has_initial_state[n]) else np.zeros((x.hv, 128, 128))
+              for n in range(len(lens))]
+    else:
+        lens = [320, 320, 320]
+        offs = [64, 320, 100]
+        x = W.dense_prefill(3, 320, 2, 4, seed=91, lower_bound=-0.7, state_std=0.3)
+        h0 = [x.initial_state[n].double().numpy() for n in range(3)]
+    ref = oracle.prefill(x)
+    xd = x.to("cuda")
+    sentinel = torch.full((len(lens), x.hv, 128, 128), 7.0, dtype=torch.float32, device="cuda")
+    ck = sentinel.clone()
+    offs_d = torch.tensor(offs, dtype=torch.int32, device="cuda")
+
+    def call():
+        if form == "walk128":
+            pool = xd.state_pool.clone()
+            return kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, A_log=xd.A_log, dt_bias=xd.dt_bias,
+                                     lower_bound=x.lower_bound, cu_seqlens=xd.cu_seqlens, state_cache=pool,
+                                     state_indices=xd.state_indices, has_initial_state=xd.has_initial_state,
+                                     checkpoint_state=ck, checkpoint_offsets=offs_d)
+        return kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, A_log=xd.A_log, dt_bias=xd.dt_bias,
+                                 lower_bound=x.lower_bound, n_seqs=3, initial_state=xd.initial_state,
+                                 output_final_state=True, groups=-1, checkpoint_state=ck,
+                                 checkpoint_offsets=offs_d)
+    (out, _), names = _traced(call)
+    assert kda.kda_device_status(clear=True) == 0
+    assert ("kda_walk128" if form == "walk128" else "kda_pipelined") in names, sorted(names)
+    check_out(out, ref["out"], f"{form} out with checkpoints")
+    for n, o in enumerate(offs):
+        if o > 0 and o % 64 == 0 and o <= lens[n]:
+            check_state(ck[n:n + 1], _prefix_state(x, n, o, h0[n])[None], f"{form} snapshot {n} at {o}")
+        else:
+            assert torch.equal(ck[n], sentinel[n]), f"{form} sequence {n}: skipped snapshot wrote its row"
