@@ -61,6 +61,7 @@ constexpr uint32_t CH_OI = CH_QG + 64 * 128 * 2;    // 4 o_intra blocks, one per
 constexpr uint32_t CH_V16 = CH_OI + 4 * OI_BLOCK;   // fp16 v^T, [128 v][64 r] K-major
 constexpr uint32_t V16_BYTES = 128 * 64 * 2;
 constexpr uint32_t CH_BYTES = CH_V16 + V16_BYTES;   // 98816
+static_assert(CH_BYTES % 128 == 0, "records are whole 128-byte lines (the pipelined walk drops them from L2)");
 constexpr uint32_t CH_A_BYTES = CH_QG - CH_P;       // P, R, d: the chain's part (49664)
 constexpr uint32_t QG_BYTES = CH_OI - CH_QG;        // qg' (16384)
 
@@ -1492,6 +1493,12 @@ struct __align__(1024) Walk128Smem {
 static_assert(sizeof(Walk128Smem) <= 227 * 1024, "pipelined walk shared memory");
 static_assert(WA_BYTES % 16 == 0 && CH_A_BYTES % 16 == 0, "bulk copy alignment");
 
+// Drop one 128-byte line from L2 without writing it back (its contents
+// become undefined): for records that no one reads again.
+__device__ __forceinline__ void discard_l2(const void* line) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -1729,16 +1736,21 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
       if (lane == 0) mbar_arrive(&s.o_done[ob]);  // O[ob] read
     }
   } else if (warp == 12) {
-    // ---------------- loader ----------------
-    if (lane == 0) {
+    // ---------------- loader: lane 0 waits and loads; in the pipelined
+    // launch the whole warp then drops from L2 the record of two chunks
+    // back, which every reader has finished with (chunk it - 2's A buffer
+    // is empty and chunk it - 1's B load was allowed), so that a record that
+    // lives a few microseconds is never written back to HBM
 #ifdef KDA_PHASE_TIMING
-      unsigned long long wf = 0, wb = 0;
+    unsigned long long wf = 0, wb = 0;
 #endif
-      for (int it = 0; it < nch; ++it) {
-        const int b = it & 1;
+    for (int it = 0; it < nch; ++it) {
+      const int b = it & 1;
+      int go = 1;
+      if (lane == 0) {
         WK_MARK(wl0);
         if (p.ready) {  // pipelined: this record's flag
-          if (!wait_ready_or_abort(ready + (size_t)it * p.hv, &s.abort, p.err)) break;
+          if (!wait_ready_or_abort(ready + (size_t)it * p.hv, &s.abort, p.err)) go = 0;
           asm volatile("fence.proxy.async.global;" ::: "memory");  // the bulk loads below read it
         } else if (it == 0) {
           griddep_wait();  // a launch of its own: the prologue before it has finished
@@ -1746,23 +1758,37 @@ __device__ __forceinline__ void walk_chain128(const ChunkParams& p, int chain, u
         WK_ADD(wf, wl0);
         const unsigned char* src = wsb + ((size_t)(c0 + it) * p.hv + h) * CH_BYTES;
         WK_MARK(wl1);
-        if (it >= 2 && !wait_or_abort(&s.emptyA[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) break;
+        if (go && it >= 2 && !wait_or_abort(&s.emptyA[b], ((it >> 1) - 1) & 1, &s.abort, p.err)) go = 0;
         WK_ADD(wb, wl1);
-        mbar_arrive_expect_tx(&s.fullA[b], WA_BYTES);
-        bulk_g2s(s.a[b], src + CH_P, 32768, &s.fullA[b]);
-        bulk_g2s(s.a[b] + 32768, src + CH_P + 32768, CH_A_BYTES - 32768, &s.fullA[b]);
-        bulk_g2s(s.a[b] + CH_A_BYTES, src + CH_V16, V16_BYTES, &s.fullA[b]);
-        s.issuedA[b] += 1;
-        if (it >= 1 && !wait_or_abort(&s.freeB, (it - 1) & 1, &s.abort, p.err)) break;
-        mbar_arrive_expect_tx(&s.fullB, WB_BYTES);
-        bulk_g2s(s.b, src + CH_QG, WB_BYTES, &s.fullB);  // -qg' and -A_qk T are adjacent
-        s.issuedB += 1;
+        if (go) {
+          mbar_arrive_expect_tx(&s.fullA[b], WA_BYTES);
+          bulk_g2s(s.a[b], src + CH_P, 32768, &s.fullA[b]);
+          bulk_g2s(s.a[b] + 32768, src + CH_P + 32768, CH_A_BYTES - 32768, &s.fullA[b]);
+          bulk_g2s(s.a[b] + CH_A_BYTES, src + CH_V16, V16_BYTES, &s.fullA[b]);
+          s.issuedA[b] += 1;
+        }
+        if (go && it >= 1 && !wait_or_abort(&s.freeB, (it - 1) & 1, &s.abort, p.err)) go = 0;
+        if (go) {
+          mbar_arrive_expect_tx(&s.fullB, WB_BYTES);
+          bulk_g2s(s.b, src + CH_QG, WB_BYTES, &s.fullB);  // -qg' and -A_qk T are adjacent
+          s.issuedB += 1;
+        }
       }
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      // only whole lines of this record: the record area must be 128-byte
+      // aligned (the workspace need only be 16-byte aligned), or a line
+      // would reach into another chain's record
+      if (p.ready && it >= 2 && (reinterpret_cast<uintptr_t>(wsb) & 127u) == 0) {
+        const unsigned char* old = wsb + ((size_t)(c0 + it - 2) * p.hv + h) * CH_BYTES;
+        for (uint32_t off = 128u * lane; off < CH_BYTES; off += 32u * 128u) discard_l2(old + off);
+      }
+    }
 #ifdef KDA_PHASE_TIMING
+    if (lane == 0) {
       atomicAdd(&g_walk_cycles[4], wf);
       atomicAdd(&g_walk_cycles[5], wb);
-#endif
     }
+#endif
   } else if (warp == 13) {
     // ---------------- qg' S ----------------
     if (lane == 0) {

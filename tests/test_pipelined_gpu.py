@@ -311,3 +311,28 @@ def test_128_column_walk_checkpoints(form):
             check_state(ck[n:n + 1], _prefix_state(x, n, o, h0[n])[None], f"{form} snapshot {n} at {o}")
         else:
             assert torch.equal(ck[n], sentinel[n]), f"{form} sequence {n}: skipped snapshot wrote its row"
+
+
+def test_pipelined_workspace_offset_16_bytes():
+    """A workspace that is only 16-byte aligned (the API's requirement): the
+    records then straddle 128-byte lines, so the walk must not drop them
+    from L2; results as from an aligned workspace, against the oracle."""
+    import linear_attention_serving_fwd_gb300 as kda
+    x = W.dense_prefill(2, 64 * 12 + 7, 2, 4, seed=93, lower_bound=-0.3, state_std=0.3)
+    ref = oracle.prefill(x)
+    xd = x.to("cuda")
+    need = kda.chunk_workspace_bytes(2, x.t_total, x.hv, -1)
+    raw = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    ws = raw[16:16 + need]
+    assert ws.data_ptr() % 128 == 16
+
+    def call():
+        return kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, A_log=xd.A_log, dt_bias=xd.dt_bias,
+                                 scale=x.scale, lower_bound=x.lower_bound, n_seqs=2,
+                                 initial_state=xd.initial_state, output_final_state=True, groups=-1,
+                                 workspace=ws)
+    (out, fin), names = _traced(call)
+    assert kda.kda_device_status(clear=True) == 0
+    _assert_pipelined(names)
+    check_out(out, ref["out"], "offset workspace out")
+    check_state(fin, ref["state"], "offset workspace final state")
