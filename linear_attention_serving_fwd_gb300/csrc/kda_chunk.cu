@@ -773,9 +773,11 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       tiles_issued += 1;
       sc = load_scalars(p, s.meta[cur ^ 1], tid);
     }
-    // pipelined launch: the record thread's warp idles through the inverse
-    // below (threads 64.. here, 256.. in the next two rounds), so it waits
-    // there for the last item's stores to land and then raises its flag
+    // The inverse below runs on threads 0..255, which synchronise among
+    // themselves (barrier 1) until its last round; threads 256.. go straight
+    // to that round's barrier.  In the pipelined launch the record thread
+    // (256) meanwhile waits for the last item's stores to land and raises its
+    // flag, off the working threads' path.
     if (tid == REC_THREAD && pending >= 0) {
       bulk_wait<0>();
       publish_ready(p.ready + pending);
@@ -801,7 +803,7 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
 #pragma unroll
       for (int i = 0; i < 16; ++i) Li[(b0 + i) * LDT + b0 + jc] = x[i];
     }
-    __syncthreads();
+    if (tid < 256) named_bar_sync(1, 256);
     PH(6);
     // 16-row pairs (a, b) = (2P, 2P + 1): thread (P, row i, column pair jp)
     // of the first 256 threads computes two entries
@@ -820,7 +822,7 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       }
       *reinterpret_cast<float2*>(&Wt[(16 * P + i) * LDW + j0]) = r;
     }
-    __syncthreads();
+    if (tid < 256) named_bar_sync(1, 256);
     if (tid < 256) {
       // L^{-1}_ba = - L^{-1}_bb W
       const int P = tid >> 7, i = (tid >> 3) & 15, j0 = 2 * (tid & 7);
@@ -836,7 +838,7 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       }
       *reinterpret_cast<float2*>(&Li[(b0 + i) * LDT + a0 + j0]) = make_float2(-r.x, -r.y);
     }
-    __syncthreads();
+    if (tid < 256) named_bar_sync(1, 256);
     PH(7);
     // 32-row halves: thread (row pair rp, column pair cp) of the first 256
     // threads computes a 2 x 2 tile; the left factor's rows are 16-byte
@@ -860,7 +862,7 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       *reinterpret_cast<float2*>(&Wt[i0 * LDW + j0]) = r0;
       *reinterpret_cast<float2*>(&Wt[(i0 + 1) * LDW + j0]) = r1;
     }
-    __syncthreads();
+    if (tid < 256) named_bar_sync(1, 256);
     if (tid < 256) {
       // L^{-1}_{[32,64) [0,32)} = - L^{-1}_{[32,64) [32,64)} W
       const int i0 = 2 * (tid >> 4), j0 = 2 * (tid & 15);
