@@ -542,13 +542,14 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       // a raw log decay outside [-10.5, 0] (or NaN) leaves the exponent range
       // the factored A_kk / A_qk operands are built for: report it
       if (!p.has_gate && __any_sync(0xffffffffu, gate_bad) && lane == 0) set_error(p.err, ERR_RANGE);
-      // v^T of the two channels: the record and VT (for o_intra) share a layout
+      // v^T of the two channels: the record, and VT for the o_intra product
+      // (made here only for the 32-column walk); they share a layout
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const uint32_t o = tc::kmajor_offset(c + e, 8 * hs, 128);
         const uint4 v4 = make_uint4(vw[e][0], vw[e][1], vw[e][2], vw[e][3]);
         *reinterpret_cast<uint4*>(wsb + CH_V16 + o) = v4;
-        *reinterpret_cast<uint4*>(s.VT + o) = v4;
+        if (!p.rec128) *reinterpret_cast<uint4*>(s.VT + o) = v4;
       }
       *reinterpret_cast<float2*>(&s.qtot[hs][c]) = acc;
       // row norms: the 8 per-row partials reduce-scatter over the warp's 64

@@ -336,3 +336,34 @@ def test_pipelined_workspace_offset_16_bytes():
     _assert_pipelined(names)
     check_out(out, ref["out"], "offset workspace out")
     check_state(fin, ref["state"], "offset workspace final state")
+
+
+@pytest.mark.parametrize("act,state,decay", [(torch.float16, torch.float32, None),
+                                             (torch.bfloat16, torch.bfloat16, None),
+                                             (torch.bfloat16, torch.float32, (-0.1, 0.0))],
+                         ids=["fp16-act", "bf16-state", "gate-free"])
+def test_walk128_dtypes_and_gate_free(act, state, decay):
+    """The 128-column walk on its own launch (6 sequences x 8 heads = 48
+    chains) with fp16 activations, a bf16 cache, or raw log decays."""
+    import linear_attention_serving_fwd_gb300 as kda
+    x = W.varlen_paged([70, 129, 64, 5, 300, 33], 2, 8, slots=9, seed=95, lower_bound=-0.3, state_std=0.3,
+                       act_dtype=act, state_dtype=state, log_decay=decay)
+    ref = oracle.prefill(x)
+    xd = x.to("cuda")
+    pool = xd.state_pool.clone()
+
+    def call():
+        return kda.kda_chunk_fwd(xd.q, xd.k, xd.v, xd.g, xd.beta, A_log=xd.A_log, dt_bias=xd.dt_bias,
+                                 scale=x.scale, lower_bound=x.lower_bound, cu_seqlens=xd.cu_seqlens,
+                                 state_cache=pool, state_indices=xd.state_indices,
+                                 has_initial_state=xd.has_initial_state)
+    (out, _), names = _traced(call)
+    assert kda.kda_device_status(clear=True) == 0
+    assert "kda_walk128" in names, sorted(names)
+    assert out.dtype == act
+    check_out(out, ref["out"], "walk128 out")
+    live = [s for s in x.state_indices.tolist() if s >= 0]
+    if state == torch.bfloat16:
+        check_state_bf16(pool[live], ref["pool"][live], "walk128 bf16 cache rows")
+    else:
+        check_state(pool[live], ref["pool"][live], "walk128 cache rows")
