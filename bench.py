@@ -404,8 +404,17 @@ def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
         e2e_step()
     k = max(3, args.steps // 4)
     secs = reduce_max(time_device(torch, e2e_step, k, lambda: None, barrier))
+    # the host link itself, for reading the figure: one plain copy of the
+    # page-locked q buffer to the device, timed the same way
+    qd = torch.empty(host["q"].shape, dtype=host["q"].dtype, device=dev)
+    qd.copy_(host["q"], non_blocking=True)
+    link_s = reduce_max(time_device(torch, lambda: qd.copy_(host["q"], non_blocking=True), 2, lambda: None,
+                                    barrier)) / 2
+    link = host["q"].numel() * host["q"].element_size() / link_s / 1e9
+    del qd
     res = {"value": round(tokens * k / secs, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(secs / k * 1e3, 3),
+           "link_h2d_gbs": round(link, 1), "link_h2d_floor_ms": round(h2d / link / 1e6, 3),
            "call": "kda_chunk_fwd_host on page-locked host buffers"}
     del host, out_h, fin_h, ws_host
     torch.cuda.empty_cache()
