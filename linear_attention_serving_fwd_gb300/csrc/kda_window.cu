@@ -433,6 +433,46 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
   }
 }
 
+// Step (1) of the windowed solve, run by warp t < Q for token t: k^_t, q~_t,
+// e^{gate_t} and beta_t into shared memory, and verify's kg record.
+template <bool FP16>
+__device__ __forceinline__ void window_vectors(const WindowParams& p, WinSmem& s, const ItemInfo& it,
+                                               const __nv_bfloat16* ibuf, const TokenScalars& ts, int warp,
+                                               int lane) {
+  constexpr int QW = 4;
+  const int h = it.head;
+  float* z = &s.tp[0][0];
+  float* khat = z;
+  float* qtil = z + QW * D;
+  float* dec = z + 2 * QW * D;
+  const int c0 = 4 * lane;
+  const __nv_bfloat16* rowp = ibuf + warp * 4 * D;
+  float qv[4], kv[4], gv[4];
+  load_act4<FP16>(rowp + 0 * D + c0, qv);
+  load_act4<FP16>(rowp + 1 * D + c0, kv);
+  load_act4<FP16>(rowp + 3 * D + c0, gv);
+  const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
+  const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
+  const float rq = rsqrtf(sq + 1e-6f) * p.scale, rk = rsqrtf(sk + 1e-6f);
+  const float a = p.has_gate ? __expf(ts.alog) : 0.f;
+  const float dt[4] = {ts.dt.x, ts.dt.y, ts.dt.z, ts.dt.w};
+  float dv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float gate = p.has_gate ? p.lower_bound * sigmoidf_(a * (gv[j] + dt[j])) : gv[j];
+    dv[j] = __expf(gate);
+  }
+  *reinterpret_cast<float4*>(khat + warp * D + c0) = make_float4(kv[0] * rk, kv[1] * rk, kv[2] * rk, kv[3] * rk);
+  *reinterpret_cast<float4*>(qtil + warp * D + c0) = make_float4(qv[0] * rq, qv[1] * rq, qv[2] * rq, qv[3] * rq);
+  *reinterpret_cast<float4*>(dec + warp * D + c0) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+  if (lane == 0) s.tbeta[warp] = sigmoidf_(act_f<FP16>(ts.beta));
+  {  // verify's kg record
+    __nv_bfloat16* dst = p.kg + (((int64_t)it.request * p.hv + h) * p.window + warp) * 2 * D;
+    *reinterpret_cast<uint2*>(dst + c0) = *reinterpret_cast<const uint2*>(rowp + 1 * D + c0);
+    *reinterpret_cast<uint2*>(dst + D + c0) = *reinterpret_cast<const uint2*>(rowp + 3 * D + c0);
+  }
+}
+
 // Windowed solve of a 2..4-token window on an fp32 state (the verify page's
 // probes and coupling scalars, KdaTcVerify steps 2-4), replacing the token
 // loop: with P_t = prod_{i <= t} e^{gate_i} and r_{j,t} = k^_j prod_{i=j+1..t}
@@ -445,7 +485,8 @@ __device__ __forceinline__ void run_tokens(const WindowParams& p, WinSmem& s, co
 template <bool FP16, int WR>
 __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, const ItemInfo& it,
                                              const float2 (&S)[WR][4], const __nv_bfloat16* ibuf,
-                                             const TokenScalars& ts, int tid, int warp, int lane) {
+                                             const TokenScalars& ts, int tid, int warp, int lane,
+                                             bool vectors_done) {
   constexpr int QW = 4;
   const int Q = it.qlen, h = it.head;
   float* z = &s.tp[0][0];  // tp, tr, tdec, tkh: 16 KB of contiguous scratch
@@ -457,35 +498,12 @@ __device__ __forceinline__ void window_solve(const WindowParams& p, WinSmem& s, 
   float* pb = z;           // S0^T kG_t, over khat once the couplings are done
   float* pa = z + QW * D;  // S0^T qG_t, over qtil
   const int c0 = 4 * lane;
-  // (1) warp t < Q: k^_t, q~_t, e^{gate_t}, beta_t (and verify's kg record)
-  if (warp < Q) {
-    const __nv_bfloat16* rowp = ibuf + warp * 4 * D;
-    float qv[4], kv[4], gv[4];
-    load_act4<FP16>(rowp + 0 * D + c0, qv);
-    load_act4<FP16>(rowp + 1 * D + c0, kv);
-    load_act4<FP16>(rowp + 3 * D + c0, gv);
-    const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
-    const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
-    const float rq = rsqrtf(sq + 1e-6f) * p.scale, rk = rsqrtf(sk + 1e-6f);
-    const float a = p.has_gate ? __expf(ts.alog) : 0.f;
-    const float dt[4] = {ts.dt.x, ts.dt.y, ts.dt.z, ts.dt.w};
-    float dv[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float gate = p.has_gate ? p.lower_bound * sigmoidf_(a * (gv[j] + dt[j])) : gv[j];
-      dv[j] = __expf(gate);
-    }
-    *reinterpret_cast<float4*>(khat + warp * D + c0) = make_float4(kv[0] * rk, kv[1] * rk, kv[2] * rk, kv[3] * rk);
-    *reinterpret_cast<float4*>(qtil + warp * D + c0) = make_float4(qv[0] * rq, qv[1] * rq, qv[2] * rq, qv[3] * rq);
-    *reinterpret_cast<float4*>(dec + warp * D + c0) = make_float4(dv[0], dv[1], dv[2], dv[3]);
-    if (lane == 0) s.tbeta[warp] = sigmoidf_(act_f<FP16>(ts.beta));
-    {  // verify's kg record
-      __nv_bfloat16* dst = p.kg + (((int64_t)it.request * p.hv + h) * p.window + warp) * 2 * D;
-      *reinterpret_cast<uint2*>(dst + c0) = *reinterpret_cast<const uint2*>(rowp + 1 * D + c0);
-      *reinterpret_cast<uint2*>(dst + D + c0) = *reinterpret_cast<const uint2*>(rowp + 3 * D + c0);
-    }
+  // (1) vectors: done by the caller unless a conv rewrote the rows after
+  // the state was loaded
+  if (!vectors_done) {
+    if (warp < Q) window_vectors<FP16>(p, s, it, ibuf, ts, warp, lane);
+    __syncthreads();
   }
-  __syncthreads();
   // (2) warp j: P_j k^_j, P_j q~_j (zero for j >= Q), the chain r_{j,t}
   // and its couplings with tokens t >= j
   if (warp < QW) {
@@ -682,7 +700,14 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
   int b = 0, sb = 0;  // input buffer, state buffer
   bool stored = false;  // WR = 4: a bulk state store is in flight from sout
   while (cur < items) {
-    if (tid == 0) s.next = (nxt < items) ? (VERIFY ? take() : nxt + ctas) : items;
+    // verify's ticket is drawn here and resolved at the end of the item: a
+    // comparison on it here would hold warp 0, and the barrier below every
+    // warp, for the atomic's round trip
+    int ticket = 0;
+    if (tid == 0) {
+      if (!VERIFY) s.next = (nxt < items) ? nxt + ctas : items;
+      else if (nxt < items) ticket = atomicAdd(p.counter, 1);
+    }
     bool ok = true;
     const bool conv = VERIFY && !FP16 && p.conv.state != nullptr;  // conv: bf16 activations only
     // verify of 2..4 tokens on an fp32 state: the windowed solve (measured
@@ -704,8 +729,10 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
             if (u < 2 * it.qlen)
               conv_unit(p, it, s.in[b], extra + b * CONV_STAGE_BYTES, u >> 1, 64 * (u & 1) + 2 * lane, yc[k]);
           }
-        } else if (warp < it.qlen && !windowed) {
-          token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+        } else if (warp < it.qlen) {
+          // token t's vectors by warp t, beside the other warps' state loads
+          if (!windowed) token_vectors<FP16>(p, s, ts, s.in[b] + warp * 4 * D, warp, lane);
+          else if constexpr (VERIFY) window_vectors<FP16>(p, s, it, s.in[b], ts, warp, lane);
         }
         const float* sbuf = state_buf(sb);
 #pragma unroll
@@ -718,7 +745,7 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
           }
       }
     }
-    // the state buffer read, token vectors written, the next ticket published
+    // the state buffer read, token vectors written, decode's next item published
     if (__syncthreads_or(!ok)) {
       // a copy never landed (error word set): wait, bounded, for the copies
       // still in flight (the next item's inputs, and with two state buffers
@@ -730,8 +757,8 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
       if (WR == 4 && tid == 0) bulk_wait<0>();
       return;
     }
-    const int nn = s.next;
-    const ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
+    int nn = VERIFY ? items : s.next;
+    ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
     // the freed state buffer takes the state of the item after this one (one
     // buffer) or of the item after that (two buffers)
     if (tid == 0) {
@@ -761,7 +788,7 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
       bool solved = false;
       if constexpr (VERIFY) {
         if (windowed) {
-          window_solve<FP16, WR>(p, s, it, S, s.in[b], ts, tid, warp, lane);
+          window_solve<FP16, WR>(p, s, it, S, s.in[b], ts, tid, warp, lane, !conv);
           solved = true;
         }
       }
@@ -792,7 +819,19 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
       }
     }
     if (tid == 0 && it.bad) set_error(p.err, ERR_INDEX);
-    __syncthreads();  // input buffer b and the token vectors consumed, sout written
+    if (VERIFY && tid == 0) {
+      int v = items;
+      if (nxt < items) {
+        if (ticket == items - 1) atomicExch(p.counter, 0);
+        v = ticket + ctas;
+      }
+      s.next = v;
+    }
+    __syncthreads();  // input buffer b and the token vectors consumed, sout written, the ticket published
+    if (VERIFY) {
+      nn = s.next;
+      it2 = nn < items ? item_info(p, nn) : ItemInfo{};
+    }
     if (WR == 4 && !VERIFY && tid == 0 && it.work && it.wslot >= 0) {
       constexpr int bytes = SBF16 ? STATE_BYTES / 2 : STATE_BYTES;
       unsigned char* dst = state_row<SBF16>(p, it.wslot, it.head);
@@ -802,7 +841,9 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
       bulk_commit();
       stored = true;
     }
-    if (warp == 1 && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane, conv_stage(p, extra, b));
+    // verify: the last warp, which no window of up to four tokens gives a
+    // token, so that its wait on the item's metadata delays no token warp
+    if (warp == (VERIFY ? THREADS / 32 - 1 : 1) && nn < items && it2.work) issue_inputs(p, it2, s.in[b], &s.ibar[b], lane, conv_stage(p, extra, b));
     ts = ts_next;
     cur = nxt;
     nxt = nn;
