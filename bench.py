@@ -208,9 +208,10 @@ def make_flush(torch):
     return flush
 
 
-def time_device(torch, fn, steps, flush, barrier):
+def time_device(torch, fn, steps, flush, barrier, per_step=None):
     """Sum of per-step CUDA-event durations of ``fn`` on the current stream
-    (flush outside the events), bracketed by barrier + synchronize."""
+    (flush outside the events), bracketed by barrier + synchronize; each
+    step's milliseconds are appended to ``per_step`` when one is given."""
     stream = torch.cuda.current_stream()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -223,7 +224,10 @@ def time_device(torch, fn, steps, flush, barrier):
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier()
-    return sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3  # seconds
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if per_step is not None:
+        per_step.extend(ms)
+    return sum(ms) / 1e3  # seconds
 
 
 def preroll(torch, fn, seconds=1.0):
@@ -381,7 +385,11 @@ def run_ours(args, rank, world, barrier, reduce_max):
 def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
     """End to end through the public host-memory call: page-locked host
     inputs, output and final state; the library copies segments in, runs them
-    as chunked prefill and copies the outputs back, overlapped."""
+    as chunked prefill and copies the outputs back, overlapped.  The figure is
+    the mean over the timed steps; each step's milliseconds and their median
+    come with it, since a step whose copies meet other traffic on a shared
+    host link (one step of 110 ms among steps of 22 ms has been seen) moves
+    the mean but not the median."""
     dev = out.device
     host = {name: getattr(x, name).cpu().pin_memory()
             for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state")
@@ -402,8 +410,9 @@ def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
 
     for _ in range(2):
         e2e_step()
-    k = max(3, args.steps // 4)
-    secs = reduce_max(time_device(torch, e2e_step, k, lambda: None, barrier))
+    k = max(3, args.steps // 2)
+    per_step = []
+    secs = reduce_max(time_device(torch, e2e_step, k, lambda: None, barrier, per_step))
     # the host link itself, for reading the figure: one plain copy of the
     # page-locked q buffer to the device, timed the same way
     qd = torch.empty(host["q"].shape, dtype=host["q"].dtype, device=dev)
@@ -414,6 +423,8 @@ def e2e(torch, kda, x, n, out, fin, args, barrier, reduce_max, tokens):
     del qd
     res = {"value": round(tokens * k / secs, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(secs / k * 1e3, 3),
+           "step_ms": [round(t, 2) for t in per_step],
+           "median_ms": round(sorted(per_step)[len(per_step) // 2], 3),
            "link_h2d_gbs": round(link, 1), "link_h2d_floor_ms": round(h2d / link / 1e6, 3),
            "call": "kda_chunk_fwd_host on page-locked host buffers"}
     del host, out_h, fin_h, ws_host
