@@ -593,6 +593,7 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     __syncthreads();
     PH(1);
     float2 mR;  // Lam at row 16 Rq + 7, the sub-chunk's reference
+    float2 dr[8], eL0, eC7;  // the rows' decays e^{Lam_i - Lam_{i-1}}; e^{Lam_0}, e^{Lam_C - Lam_7}
     {
       // Every thread reads what it needs straight from the half-sub-chunk
       // gate totals and the norm partials: its rows' offset (the totals of
@@ -636,20 +637,40 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       auto tf32x2 = [](float2 v) {
         return make_uint2(__float_as_uint(tc::to_tf32_int(v.x)), __float_as_uint(tc::to_tf32_int(v.y)));
       };
+      // Every exponential below is e^{Lam_i - x} or e^{x - Lam_i} for this
+      // thread's 8 consecutive rows i, so each follows from one anchor by
+      // the rows' decays dr_i = e^{Lam_i - Lam_{i-1}}: 4 exponentials a
+      // channel per row become 1.  The products telescope exactly over the
+      // (rounded) Lam, so they differ from the direct exponentials only by
+      // a few roundings, far below the tf32 / fp16 operands they scale.
+      dr[0] = make_float2(1.f, 1.f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 8 * hs + i;
-        // e^{Lam - m} and e^{m - Lam}, both within e^{+-84}
-        const float2 E = make_float2(__expf(lam[i].x - mR.x), __expf(lam[i].y - mR.y));
-        const float2 iE = make_float2(__expf(mR.x - lam[i].x), __expf(mR.y - lam[i].y));
-        const float2 xk = fmul2(kv[i], E), xq = fmul2(qv[i], E), y = fmul2(kv[i], iE);
-        *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(r, c, 128)) = tf32x2(xk);
-        *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tf32x2(xq);
+      for (int i = 1; i < 8; ++i) dr[i] = make_float2(__expf(lam[i].x - lam[i - 1].x), __expf(lam[i].y - lam[i - 1].y));
+      eL0 = make_float2(__expf(lam[0].x), __expf(lam[0].y));                     // e^{Lam_0}
+      eC7 = make_float2(__expf(lamC.x - lam[7].x), __expf(lamC.y - lam[7].y));   // e^{Lam_C - Lam_7}
+      {  // X = [k^; q~] e^{Lam - m}, rows upward from e^{Lam_0 - m} (within e^{+-84})
+        float2 E = make_float2(__expf(lam[0].x - mR.x), __expf(lam[0].y - mR.y));
 #pragma unroll
-        for (int R2 = 0; R2 < 4; ++R2)
-          if (R2 >= Rq)
-            *reinterpret_cast<uint2*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
-                tf32x2(fmul2(y, F[R2]));
+        for (int i = 0; i < 8; ++i) {
+          const int r = 8 * hs + i;
+          if (i > 0) E = fmul2(E, dr[i]);
+          *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(r, c, 128)) = tf32x2(fmul2(kv[i], E));
+          *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tf32x2(fmul2(qv[i], E));
+        }
+      }
+      {  // Y = k^ e^{m - Lam} (times F for later sub-chunks), rows downward from e^{m - Lam_7}
+        float2 iE = make_float2(__expf(mR.x - lam[7].x), __expf(mR.y - lam[7].y));
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+          const int r = 8 * hs + i;
+          if (i < 7) iE = fmul2(iE, dr[i + 1]);
+          const float2 y = fmul2(kv[i], iE);
+#pragma unroll
+          for (int R2 = 0; R2 < 4; ++R2)
+            if (R2 >= Rq)
+              *reinterpret_cast<uint2*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
+                  tf32x2(fmul2(y, F[R2]));
+        }
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -665,23 +686,31 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       // meanwhile: Kg = k^ e^{Lam}, qg = q~ e^{Lam}, kg = k^ e^{Lam_C - Lam}
       // (each factor at most 1: an underflow only drops a term below e^{-87})
       uint32_t Kgx[2][4], qgx[2][4], kgw[2][4];  // per channel, fp16 pairs along rows
+      {  // e^{Lam}: rows upward from e^{Lam_0}
+        float2 eL = eL0;
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        float2 Kg2[2], qg2[2], kg2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float2 eL = make_float2(__expf(lam[i + e].x), __expf(lam[i + e].y));
-          const float2 eC = make_float2(__expf(lamC.x - lam[i + e].x), __expf(lamC.y - lam[i + e].y));
-          Kg2[e] = fmul2(kv[i + e], eL);
-          qg2[e] = fmul2(qv[i + e], eL);
-          kg2[e] = fmul2(kv[i + e], eC);
+        for (int i = 0; i < 8; i += 2) {
+          if (i > 0) eL = fmul2(eL, dr[i]);
+          const float2 Kg0 = fmul2(kv[i], eL), qg0 = fmul2(qv[i], eL);
+          eL = fmul2(eL, dr[i + 1]);
+          const float2 Kg1 = fmul2(kv[i + 1], eL), qg1 = fmul2(qv[i + 1], eL);
+          Kgx[0][i >> 1] = pack_half2(Kg0.x, Kg1.x);
+          Kgx[1][i >> 1] = pack_half2(Kg0.y, Kg1.y);
+          qgx[0][i >> 1] = pack_half2(qg0.x, qg1.x);
+          qgx[1][i >> 1] = pack_half2(qg0.y, qg1.y);
         }
-        Kgx[0][i >> 1] = pack_half2(Kg2[0].x, Kg2[1].x);
-        Kgx[1][i >> 1] = pack_half2(Kg2[0].y, Kg2[1].y);
-        qgx[0][i >> 1] = pack_half2(qg2[0].x, qg2[1].x);
-        qgx[1][i >> 1] = pack_half2(qg2[0].y, qg2[1].y);
-        kgw[0][i >> 1] = pack_half2(kg2[0].x, kg2[1].x);
-        kgw[1][i >> 1] = pack_half2(kg2[0].y, kg2[1].y);
+      }
+      {  // e^{Lam_C - Lam}: rows downward from e^{Lam_C - Lam_7}
+        float2 eC = eC7;
+#pragma unroll
+        for (int i = 6; i >= 0; i -= 2) {
+          if (i < 6) eC = fmul2(eC, dr[i + 2]);
+          const float2 kg1 = fmul2(kv[i + 1], eC);
+          eC = fmul2(eC, dr[i + 1]);
+          const float2 kg0 = fmul2(kv[i], eC);
+          kgw[0][i >> 1] = pack_half2(kg0.x, kg1.x);
+          kgw[1][i >> 1] = pack_half2(kg0.y, kg1.y);
+        }
       }
       // B3 [c][K]: Kg row i at K = i, qg row r at K = 64 + r; KG [k = c][K = r]
 #pragma unroll

@@ -704,9 +704,15 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
     // comparison on it here would hold warp 0, and the barrier below every
     // warp, for the atomic's round trip
     int ticket = 0;
-    if (tid == 0) {
-      if (!VERIFY) s.next = (nxt < items) ? nxt + ctas : items;
-      else if (nxt < items) ticket = atomicAdd(p.counter, 1);
+    if (VERIFY && tid == 0 && nxt < items) ticket = atomicAdd(p.counter, 1);
+    // decode's static stride names the item after next here, so its
+    // metadata loads run under the state wait (with two state buffers its
+    // state is issued right after the barrier below)
+    int nn = items;
+    ItemInfo it2 = ItemInfo{};
+    if (!VERIFY) {
+      nn = nxt < items ? nxt + ctas : items;
+      if (nn < items) it2 = item_info(p, nn);
     }
     bool ok = true;
     const bool conv = VERIFY && !FP16 && p.conv.state != nullptr;  // conv: bf16 activations only
@@ -745,7 +751,7 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
           }
       }
     }
-    // the state buffer read, token vectors written, decode's next item published
+    // the state buffer read, token vectors written
     if (__syncthreads_or(!ok)) {
       // a copy never landed (error word set): wait, bounded, for the copies
       // still in flight (the next item's inputs, and with two state buffers
@@ -757,8 +763,6 @@ __global__ void __launch_bounds__(win_threads<WR>(), WR == 8 ? 2 : 1) kda_window
       if (WR == 4 && tid == 0) bulk_wait<0>();
       return;
     }
-    int nn = VERIFY ? items : s.next;
-    ItemInfo it2 = nn < items ? item_info(p, nn) : ItemInfo{};
     // the freed state buffer takes the state of the item after this one (one
     // buffer) or of the item after that (two buffers)
     if (tid == 0) {
