@@ -255,6 +255,12 @@ struct __align__(1024) ProSmem {
   float ssk[2][64];         // |k_r|^2 partial per group of 64 channels
   float ssq[2][64];
   float beta[64];
+  // the next item's scalars, fetched during this item's inverse by threads
+  // that have no part in it: sigmoid(beta) per row (0 past its length),
+  // a_h dt_bias per channel pair and a_h = e^{A_log} of its head
+  float beta_n[64];
+  float2 adt_n[64];
+  float ah_n;
   int4 meta[2];             // (chunk, head, first token, rows) of this and the next item
   uint64_t bar;
   uint64_t bar2;            // the P product of the last round, ahead of the others
@@ -371,19 +377,28 @@ __device__ __forceinline__ void conv_tiles(const ChunkParams& p, __nv_bfloat16* 
 
 // The item's raw per-row beta (threads 0..63), dt_bias of channel tid % 128
 // and A_log: loaded early, consumed at the item's start.
-struct ItemScalars {
-  __nv_bfloat16 beta;
-  float2 dt;  // dt_bias of the thread's channel pair 2 (tid % 64), + 1
-  float alog;
-};
-__device__ __forceinline__ ItemScalars load_scalars(const ChunkParams& p, int4 m, int tid) {
-  ItemScalars r;
+// Threads 320..447 of the prologue: item m's per-item scalars into shared
+// memory (the ProSmem fields beta_n, adt_n, ah_n).  They run it while the
+// others invert, so its global loads' latency is on no one's path.
+template <bool FP16>
+__device__ __forceinline__ void fetch_scalars(const ChunkParams& p, float* beta_n, float2* adt_n, float* ah_n,
+                                              int4 m, int tid) {
   const int h = m.y, bos = m.z, len = m.w;
-  r.beta = (tid < 64 && tid < len) ? p.beta[(int64_t)(bos + tid) * p.b_st + h * p.b_sh]
-                                   : __float2bfloat16(0.f);
-  r.dt = p.has_gate ? *reinterpret_cast<const float2*>(p.dt_bias + h * D + 2 * (tid & 63)) : make_float2(0.f, 0.f);
-  r.alog = p.has_gate ? p.A_log[h] : 0.f;
-  return r;
+  const int u = tid - 320;
+  if (u >= 0 && u < 64) {
+    beta_n[u] = u < len ? sigmoidf_(act_f<FP16>(p.beta[(int64_t)(bos + u) * p.b_st + h * p.b_sh])) : 0.f;
+  } else if (u >= 64 && u < 128) {
+    const int cp = u - 64;
+    float ah = 0.f;
+    float2 adt = make_float2(0.f, 0.f);
+    if (p.has_gate) {
+      ah = __expf(p.A_log[h]);
+      const float2 dt = *reinterpret_cast<const float2*>(p.dt_bias + h * D + 2 * cp);
+      adt = make_float2(ah * dt.x, ah * dt.y);
+    }
+    adt_n[cp] = adt;
+    if (cp == 0) *ah_n = ah;
+  }
 }
 
 // Per-phase cycle accounting of the prologue, compiled in only with
@@ -481,8 +496,8 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
   // round trip never delays the next item's tile loads
   int t_ahead = 0;
   if (tid == 32) t_ahead = p.item_counter ? (int)atomicAdd(p.item_counter, 1u) : t + stride;
-  ItemScalars sc = {};
-  if (t < n_items) sc = load_scalars(p, s.meta[0], tid);
+  if (t < n_items) fetch_scalars<FP16>(p, s.beta_n, s.adt_n, &s.ah_n, s.meta[0], tid);
+  __syncthreads();
   uint32_t bar_phase = 0, bar2_phase = 0, tile_phase = 0, tiles_issued = t < n_items ? 1 : 0;
   int cur = 0;
   int pending = -1;  // REC_THREAD: the record whose stores are in flight (pipelined launch)
@@ -492,8 +507,8 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     if (!p.item_counter && t + stride >= n_items) griddep_launch_dependents();
     const int4 meta = s.meta[cur];
     const int c_glob = meta.x, h = meta.y, len = meta.w;
-    const float a_h = p.has_gate ? __expf(sc.alog) : 0.f;
-    if (tid < 64) s.beta[tid] = tid < len ? sigmoidf_(act_f<FP16>(sc.beta)) : 0.f;
+    const float a_h = s.ah_n;
+    if (tid < 64) s.beta[tid] = s.beta_n[tid];
     unsigned char* wsb = reinterpret_cast<unsigned char*>(p.ch) + ((size_t)c_glob * p.hv + h) * CH_BYTES;
     // ---- phase 0: this item's tiles (issued during the previous item) -------
     wait_or_abort(&s.tbar, tile_phase, &s.abort, p.err);
@@ -512,7 +527,7 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       float2 acc = make_float2(0.f, 0.f);
       bool gate_bad = false;
       uint32_t vw[2][4];  // v of channels c and c + 1 as fp16 pairs along rows
-      const float2 ah2 = make_float2(a_h, a_h), adt2 = make_float2(a_h * sc.dt.x, a_h * sc.dt.y);
+      const float2 ah2 = make_float2(a_h, a_h), adt2 = s.adt_n[cp];
       const float2 zero2 = make_float2(0.f, 0.f);
       // rows at or past ``len`` belong to the next sequence
 #pragma unroll
@@ -796,12 +811,13 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
     __syncthreads();
     PH(5);
 
-    // the next item's scalars (its tiles are already on their way)
     t_next = s.next_t;
     const bool has_next = t_next < n_items;
+    // the next item's scalars (its tiles are already on their way), by
+    // threads that skip the inverse
     if (has_next) {
       tiles_issued += 1;
-      sc = load_scalars(p, s.meta[cur ^ 1], tid);
+      fetch_scalars<FP16>(p, s.beta_n, s.adt_n, &s.ah_n, s.meta[cur ^ 1], tid);
     }
     // The inverse below runs on threads 0..255, which synchronise among
     // themselves (barrier 1) until its last round; threads 256.. go straight
