@@ -627,10 +627,6 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
       mR = Rq == 0 ? mref[0] : (Rq == 1 ? mref[1] : (Rq == 2 ? mref[2] : mref[3]));
       if (hs == 7)
         *reinterpret_cast<float2*>(wsb + CH_D + 4 * c) = make_float2(__expf(lamC.x), __expf(lamC.y));
-      float2 F[4];  // e^{m_R2 - m_Rq} <= 1 for later sub-chunks R2
-#pragma unroll
-      for (int R2 = 0; R2 < 4; ++R2)
-        F[R2] = R2 > Rq ? make_float2(__expf(mref[R2].x - mR.x), __expf(mref[R2].y - mR.y)) : make_float2(1.f, 1.f);
       // normalised keys and queries: lane l of the warp forms 1/|k_r| (l & 8
       // clear) or scale/|q_r| (l & 8 set) of row r = 8 hs + (l & 7) from the
       // two channel halves' partial sums; shuffles hand the warp's 8 rows to
@@ -673,18 +669,27 @@ __device__ __forceinline__ void prologue_items(const ChunkParams& p, const TileM
           *reinterpret_cast<uint2*>(s.XY + tc::sw128_offset32(64 + r, c, 128)) = tf32x2(fmul2(qv[i], E));
         }
       }
-      {  // Y = k^ e^{m - Lam} (times F for later sub-chunks), rows downward from e^{m - Lam_7}
-        float2 iE = make_float2(__expf(mR.x - lam[7].x), __expf(mR.y - lam[7].y));
+      {  // Y_R2 = k^ e^{m_R2 - Lam} for this sub-chunk and the later ones
+         // (R2 >= Rq), rows downward from e^{m_R2 - Lam_7}.  Each factor is
+         // one exponential's worth: at most e^{84}, and flushed to zero only
+         // where the term it scales is below e^{-87} (a product through
+         // e^{m_R2 - m_Rq}, which spans 16 rows, could underflow while the
+         // term itself does not)
+        float2 yf[4];
+#pragma unroll
+        for (int R2 = 0; R2 < 4; ++R2)
+          yf[R2] = R2 >= Rq ? make_float2(__expf(mref[R2].x - lam[7].x), __expf(mref[R2].y - lam[7].y))
+                            : make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 7; i >= 0; --i) {
           const int r = 8 * hs + i;
-          if (i < 7) iE = fmul2(iE, dr[i + 1]);
-          const float2 y = fmul2(kv[i], iE);
 #pragma unroll
           for (int R2 = 0; R2 < 4; ++R2)
-            if (R2 >= Rq)
+            if (R2 >= Rq) {
+              if (i < 7) yf[R2] = fmul2(yf[R2], dr[i + 1]);
               *reinterpret_cast<uint2*>(s.XY + 65536 + tc::sw128_offset32(d_col(R2) + r, c, YROWS)) =
-                  tf32x2(fmul2(y, F[R2]));
+                  tf32x2(fmul2(kv[i], yf[R2]));
+            }
         }
       }
       fence_proxy_async_smem();

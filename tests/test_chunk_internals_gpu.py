@@ -45,7 +45,7 @@ def _err(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-6 * np.sqrt(b.size)))
 
 
-@pytest.mark.parametrize("T,lb", [(130, -0.3), (64, -5.0)])
+@pytest.mark.parametrize("T,lb", [(130, -0.3), (64, -5.0), (130, -10.5)])
 def test_prologue_records_match_chunk_form(T, lb):
     import linear_attention_serving_fwd_gb300 as kda
     x = W.dense_prefill(1, T, 1, 2, seed=21, lower_bound=lb, init_state=False)

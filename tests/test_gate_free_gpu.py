@@ -54,6 +54,20 @@ def test_dense_prefill_gate_free(decay, groups):
     check_state(fin, ref["state"], f"dense G={groups} final state")
 
 
+@pytest.mark.parametrize("groups", [1, -1], ids=["two-launch", "pipelined"])
+def test_dense_prefill_at_the_log_decay_limit(groups):
+    """Log decays U[-10.5, -10], at the limit of the range the chunk kernels
+    factor: 8 consecutive rows span e^{+-84}, so the operands' scale factors
+    (running products of the rows' decays from one anchor each) reach their
+    largest anchors, and every decay product beyond a few rows underflows."""
+    x = W.dense_prefill(2, 64 * 9 + 5, 2, 4, seed=47 + groups, log_decay=(-10.5, -10.0), state_std=0.3)
+    assert float(x.g.min()) >= -10.5
+    ref = oracle.prefill(x)
+    out, fin, _ = _prefill(x, groups, dense=True)
+    check_out(out, ref["out"], f"dense G={groups} out at the log decay limit")
+    check_state(fin, ref["state"], f"dense G={groups} final state at the log decay limit")
+
+
 @pytest.mark.parametrize("decay", [STRONG, WEAK], ids=["strong", "weak"])
 @pytest.mark.parametrize("groups", [1, 4])
 def test_varlen_paged_prefill_gate_free(decay, groups):

@@ -82,6 +82,25 @@ def test_pipelined_weak_decay(lb, shift):
     check_state(fin, ref["state"], "pipelined weak final state")
 
 
+@pytest.mark.parametrize("g_shift", [4.0, 0.0], ids=["gates-near-limit", "gates-spread"])
+@pytest.mark.parametrize("groups", [-1, 1], ids=["pipelined", "two-launch"])
+def test_gated_prefill_at_the_lower_bound_limit(groups, g_shift):
+    """lower_bound = -10.5, the API's limit.  With g shifted up the sigmoid
+    sits near 1 and most gates near -10.5: the operands' scale factors reach
+    their largest anchors (e^{+-84} over 8 rows).  With g ~ N(0, 1) the
+    channels decay at very different rates, and 16 rows of gates often sum
+    below -87: a later sub-chunk's Y factor must not pass through
+    e^{m_R2 - m_Rq}, which would flush to zero there (o_intra was once 5 %
+    off at the sub-chunks' first rows)."""
+    x = W.dense_prefill(2, 64 * 9 + 5, 2, 4, seed=79, lower_bound=-10.5, g_shift=g_shift, state_std=0.3)
+    ref = oracle.prefill(x)
+    out, fin, names = _dense(x, groups=groups)
+    if groups == -1:
+        _assert_pipelined(names)
+    check_out(out, ref["out"], f"G={groups} out at lower_bound -10.5")
+    check_state(fin, ref["state"], f"G={groups} final state at lower_bound -10.5")
+
+
 def test_pipelined_gate_free():
     x = W.dense_prefill(2, 64 * 9 + 40, 2, 4, seed=75, log_decay=(-0.1, 0.0), state_std=0.3)
     ref = oracle.prefill(x)
